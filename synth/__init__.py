@@ -1,0 +1,207 @@
+"""Seeded synthetic inputs for the fused Conv1d(implicit GEMM) + normalization operator.
+
+This module is shared by the tests, the benchmark and the smoke check. It holds
+only input generation (random numbers, value distributions and the five
+workload shapes); none of the operator's arithmetic lives here.
+
+Random numbers come from a counter-based generator: the SplitMix64 output
+function (Steele, Lea and Flood, "Fast splittable pseudorandom number
+generators", OOPSLA 2014) applied to ``stream_key + (i + 1) * 0x9E3779B97F4A7C15``
+for element ``i``. Every tensor has its own stream key, derived from the seed and
+a fixed tensor id, so tensors are independent of one another and of their
+sizes, and the whole thing vectorises in numpy.
+
+* uniform u in [0, 1): the top 53 bits of the 64-bit output times 2**-53;
+* U(-a, a) = a * (2u - 1);
+* N(mu, sigma): Box-Muller on two independent uniforms (element i uses the
+  counter values 2i and 2i+1 of its stream), mu + sigma * sqrt(-2 ln(1-u1)) *
+  cos(2 pi u2), computed in float64 and rounded once to float32.
+
+bf16 inputs are float32 values rounded to the nearest bf16 (ties to even) by
+``round_bf16``; both the oracle and the CUDA path consume exactly those values.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, Optional
+
+import numpy as np
+
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+# Fixed stream ids, one per tensor role.
+STREAM_X, STREAM_W, STREAM_B, STREAM_GAMMA, STREAM_BETA, STREAM_BIAS2 = 1, 2, 3, 4, 5, 6
+
+
+def _mix64(z: np.ndarray) -> np.ndarray:
+    """SplitMix64 output function on a uint64 array (wrapping arithmetic)."""
+    with np.errstate(over="ignore"):
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+        return z ^ (z >> np.uint64(31))
+
+
+def _stream_key(seed: int, stream: int) -> np.uint64:
+    with np.errstate(over="ignore"):
+        k = np.uint64(seed & 0xFFFFFFFFFFFFFFFF) ^ (np.uint64(stream) * _GOLDEN)
+        return _mix64(np.array([k], dtype=np.uint64))[0]
+
+
+def raw_u64(seed: int, stream: int, start: int, count: int) -> np.ndarray:
+    """64-bit outputs for counters start .. start+count-1 of one stream."""
+    key = _stream_key(seed, stream)
+    idx = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        return _mix64(key + idx * _GOLDEN)
+
+
+def uniform01(seed: int, stream: int, count: int, start: int = 0) -> np.ndarray:
+    """float64 uniforms in [0, 1)."""
+    return (raw_u64(seed, stream, start, count) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+def uniform_pm(seed: int, stream: int, count: int, a: float) -> np.ndarray:
+    """float32 samples of U(-a, a)."""
+    return (a * (2.0 * uniform01(seed, stream, count) - 1.0)).astype(np.float32)
+
+
+def normal(seed: int, stream: int, count: int, mu: float = 0.0, sigma: float = 1.0) -> np.ndarray:
+    """float32 samples of N(mu, sigma) (sigma is the standard deviation)."""
+    out = np.empty(count, dtype=np.float32)
+    chunk = 1 << 22
+    for s in range(0, count, chunk):
+        n = min(chunk, count - s)
+        u = uniform01(seed, stream, 2 * n, start=2 * s)
+        r = np.sqrt(-2.0 * np.log1p(-u[0::2]))
+        out[s:s + n] = (mu + sigma * r * np.cos(2.0 * math.pi * u[1::2])).astype(np.float32)
+    return out
+
+
+def round_bf16(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even); returns float32."""
+    bits = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (bits >> np.uint64(16)) & np.uint64(1)
+    r = ((bits + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) << np.uint64(16)
+    return (r & np.uint64(0xFFFFFFFF)).astype(np.uint32).view(np.float32)
+
+
+def bf16_bits(a: np.ndarray) -> np.ndarray:
+    """The upper 16 bits of float32 values that are already bf16-representable."""
+    return (np.ascontiguousarray(a, dtype=np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+# ----------------------------------------------------------------------------------------------
+# Workload shapes
+
+
+NORM_NONE, NORM_GROUP, NORM_CHANNEL_LAYER = 0, 1, 2
+POST_NONE, POST_GELU_ERF, POST_ROWMIN_BIAS = 0, 1, 2
+DTYPE_F32, DTYPE_BF16 = 0, 1
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One operator configuration plus the distributions its inputs are drawn from."""
+
+    name: str
+    N: int
+    C_in: int
+    C_out: int
+    T: int
+    k: int
+    stride: int = 1
+    pad_left: int = 0
+    pad_right: int = 0
+    dilation: int = 1
+    norm: int = NORM_NONE
+    groups: int = 1
+    eps: float = 1e-5
+    post: int = POST_NONE
+    dtype: int = DTYPE_F32
+    has_bias: bool = True
+    has_affine: bool = True
+    w_bound: Optional[float] = None      # U(+-w_bound) for w and b; default 1/sqrt(C_in*k)
+    description: str = ""
+
+    @property
+    def T_out(self) -> int:
+        return (self.T + self.pad_left + self.pad_right - self.dilation * (self.k - 1) - 1) // self.stride + 1
+
+    @property
+    def gemm_mnk(self):
+        return self.N * self.T_out, self.C_out, self.C_in * self.k
+
+    @property
+    def flops(self) -> float:
+        m, n, k = self.gemm_mnk
+        return 2.0 * m * n * k
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2 if self.dtype == DTYPE_BF16 else 4
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """x + w read once, b/gamma/beta(/bias2) read once, y written once."""
+        eb = self.elem_bytes
+        b = self.N * self.C_in * self.T * eb + self.C_out * self.C_in * self.k * eb
+        b += 4 * self.C_out * (int(self.has_bias) + 2 * int(self.has_affine and self.norm != NORM_NONE))
+        if self.post == POST_ROWMIN_BIAS:
+            b += 4 * self.C_out
+        b += self.N * self.C_out * self.T_out * eb
+        return b
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+CONV_GN_TINY = Workload(
+    "conv1d_groupnorm_f32_n2_c16x32_t128", N=2, C_in=16, C_out=32, T=128, k=3, pad_left=1, pad_right=1,
+    norm=NORM_GROUP, groups=4, description="Conv1d+GroupNorm fp32, N=2, C 16->32, T=128, k=3, pad 1/1, G=4")
+CONV_GN = Workload(
+    "conv1d_groupnorm_f32_n16_c128x256_t1024", N=16, C_in=128, C_out=256, T=1024, k=3, pad_left=1, pad_right=1,
+    norm=NORM_GROUP, groups=32,
+    description="Conv1d+GroupNorm fp32, N=16, C 128->256, T=1024, k=3, pad 1/1, G=32 (8 ch/group)")
+CAUSAL_CONV = Workload(
+    "causal_conv1d_f32_n32_c256x256_t8192_k4", N=32, C_in=256, C_out=256, T=8192, k=4, pad_left=3, pad_right=0,
+    norm=NORM_NONE, w_bound=1.0 / 32.0,
+    description="causal Conv1d fp32, no norm, N=32, C 256->256, T=8192, k=4, left pad 3")
+LINEAR_GN_ROWMIN = Workload(
+    "linear_groupnorm_rowmin_bias_f32_1024x8192x8192", N=1024, C_in=8192, C_out=8192, T=1, k=1,
+    norm=NORM_GROUP, groups=512, post=POST_ROWMIN_BIAS,
+    description="Linear 8192->8192 on 1024 rows + GroupNorm(512) + row-min + broadcast bias, fp32")
+CONV_LN_GELU_BF16 = Workload(
+    "conv1d_layernorm_gelu_bf16_n64_c256x512_t4096_k5_d2", N=64, C_in=256, C_out=512, T=4096, k=5, pad_left=4,
+    pad_right=4, dilation=2, norm=NORM_CHANNEL_LAYER, post=POST_GELU_ERF, dtype=DTYPE_BF16,
+    description="Conv1d+channel-LayerNorm+exact GELU bf16 (fp32 accumulate), N=64, C 256->512, T=4096, k=5, dil 2, pad 4/4")
+
+WORKLOADS = [CONV_GN_TINY, CONV_GN, CAUSAL_CONV, LINEAR_GN_ROWMIN, CONV_LN_GELU_BF16]
+BY_NAME: Dict[str, Workload] = {w.name: w for w in WORKLOADS}
+
+
+def make_inputs(wl: Workload, seed: int = 0, n_rows: Optional[int] = None) -> Dict[str, np.ndarray]:
+    """Draw the inputs of ``wl`` (float32 arrays; bf16 workloads get bf16-rounded values).
+
+    ``n_rows`` draws only the first ``n_rows`` batch entries of x (the counter-based
+    generator makes that prefix identical to the full draw).
+    """
+    n = wl.N if n_rows is None else n_rows
+    a = wl.w_bound if wl.w_bound is not None else 1.0 / math.sqrt(wl.C_in * wl.k)
+    x = normal(seed, STREAM_X, n * wl.C_in * wl.T).reshape(n, wl.C_in, wl.T)
+    w = uniform_pm(seed, STREAM_W, wl.C_out * wl.C_in * wl.k, a).reshape(wl.C_out, wl.C_in, wl.k)
+    out = {"x": x, "w": w}
+    out["b"] = uniform_pm(seed, STREAM_B, wl.C_out, a) if wl.has_bias else None
+    if wl.norm != NORM_NONE and wl.has_affine:
+        out["gamma"] = normal(seed, STREAM_GAMMA, wl.C_out, 1.0, 0.1)
+        out["beta"] = normal(seed, STREAM_BETA, wl.C_out, 0.0, 0.1)
+    else:
+        out["gamma"] = None
+        out["beta"] = None
+    out["bias2"] = normal(seed, STREAM_BIAS2, wl.C_out, 0.0, 1.0) if wl.post == POST_ROWMIN_BIAS else None
+    if wl.dtype == DTYPE_BF16:
+        out["x"] = round_bf16(out["x"])
+        out["w"] = round_bf16(out["w"])
+    return out
