@@ -1,0 +1,395 @@
+"""Benchmark of the fused Conv1d + normalization operator on GB300.
+
+Default workload: Conv1d(128 -> 256, k=3, pad 1/1) + GroupNorm(32) on x[16, 128, 1024] fp32 (TF32
+tensor cores), the configuration the headline metric is quoted on. One step = the whole hot path:
+weight packing + the fused conv/statistics/normalize kernel, through the C ABI.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Under torchrun every rank runs the same per-GPU workload on its own GPU and its own seeded batch
+(weak scaling, no collective on the data path); the timed region is bracketed by a barrier and a
+device synchronize, and the slowest rank's time is reported. `--impl reference` times the CPU
+oracle on the host cores instead (rank 0 only).
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense TF32 / BF16 tensor rate
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        self.device_index = device_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def workload_by_name(name):
+    if name in synth.BY_NAME:
+        return synth.BY_NAME[name]
+    short = {"conv_gn": synth.CONV_GN, "conv_gn_tiny": synth.CONV_GN_TINY, "causal_conv": synth.CAUSAL_CONV,
+             "linear_gn_rowmin": synth.LINEAR_GN_ROWMIN, "conv_ln_gelu_bf16": synth.CONV_LN_GELU_BF16}
+    return short[name]
+
+
+def config_of(wl, extra):
+    cfg = {"workload": wl.name, "N": wl.N, "C_in": wl.C_in, "C_out": wl.C_out, "T": wl.T, "k": wl.k,
+           "stride": wl.stride, "pad": [wl.pad_left, wl.pad_right], "dilation": wl.dilation,
+           "norm": ["none", "group", "channel_layer"][wl.norm], "groups": wl.groups,
+           "post": ["none", "gelu_erf", "rowmin_bias"][wl.post], "T_out": wl.T_out,
+           "gemm_mnk": list(wl.gemm_mnk)}
+    cfg.update(extra)
+    return cfg
+
+
+def dtype_name(wl, path):
+    if wl.dtype == synth.DTYPE_BF16:
+        return "bf16"
+    return "f32" if path == "simt" else "tf32"
+
+
+# ------------------------------------------------------------------------------------------ oracle arm
+
+def time_oracle(wl, seconds=10.0, max_runs=50, n_rows=None):
+    """Time the CPU oracle on `n_rows` batch entries of the workload (whole workload by default)."""
+    import oracle
+    rows = wl.N if n_rows is None else n_rows
+    sub = wl.replace(N=rows)
+    inp = synth.make_inputs(wl, seed=0, n_rows=rows)
+    p = oracle.params_of(sub)
+    threads = oracle.default_threads()
+    oracle.conv1d_norm(p, inp["x"], inp["w"], inp["b"], inp["gamma"], inp["beta"], inp["bias2"], nthreads=threads)
+    runs, t0 = 0, time.perf_counter()
+    while True:
+        oracle.conv1d_norm(p, inp["x"], inp["w"], inp["b"], inp["gamma"], inp["beta"], inp["bias2"],
+                           nthreads=threads)
+        runs += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or runs >= max_runs:
+            break
+    flops = sub.flops * runs
+    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{runs} run(s) of the full operator on {rows} of {wl.N} batch entries "
+                      f"({sub.flops / 1e9:.3f} GFLOP each), {el:.1f} s wall"}
+
+
+def reference_arm(args, wl):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    rows = max(1, min(wl.N, args.oracle_rows))
+    sub = wl.replace(N=rows)
+    inp = synth.make_inputs(wl, seed=0, n_rows=rows)
+    p = oracle.params_of(sub)
+    threads = oracle.default_threads()
+    run = lambda: oracle.conv1d_norm(p, inp["x"], inp["w"], inp["b"], inp["gamma"], inp["beta"], inp["bias2"],
+                                     nthreads=threads)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    el = time.perf_counter() - t0
+    ms = el / args.steps * 1e3
+    value = sub.flops / (ms / 1e3) / 1e12
+    line = {"impl": "reference", "metric": args.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl, {"oracle_rows_per_step": rows}),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": f"each step: the full operator on {rows} of {wl.N} batch entries"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------ our arm
+
+def our_arm(args, wl):
+    import torch
+    import gemm_groupnorm_accelerator_gb300 as c1n
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    c1n.load()
+    peaks = load_peaks()
+
+    params = c1n.make_params(wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right, wl.dilation,
+                             wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, args.math, args.path)
+    op = c1n.Conv1dNorm(params, device=dev)
+    path = op.path
+    inp = synth.make_inputs(wl, seed=rank)
+    bf = wl.dtype == synth.DTYPE_BF16
+    tdt = torch.bfloat16 if bf else torch.float32
+
+    def dev_t(a, cast=True):
+        if a is None:
+            return None
+        t = torch.from_numpy(a).to(dev)
+        return t.to(tdt) if (cast and bf) else t
+
+    w = dev_t(inp["w"])
+    b, ga, be, b2 = (dev_t(inp[k], cast=False) for k in ("b", "gamma", "beta", "bias2"))
+    x0 = dev_t(inp["x"])
+    out_dt = op.out_dtype()
+    y_shape = (wl.N, wl.C_out, op.T_out)
+    per_set = x0.numel() * x0.element_size() + int(np.prod(y_shape)) * (2 if bf else 4)
+    n_sets = 1 if per_set >= L2_BYTES else min(16, math.ceil(2 * L2_BYTES / per_set))
+    xs = [x0] + [x0.clone() for _ in range(n_sets - 1)]
+    ys = [torch.empty(y_shape, dtype=out_dt, device=dev) for _ in range(n_sets)]
+    am = torch.empty((wl.N, op.T_out), dtype=torch.int32, device=dev) if wl.post == synth.POST_ROWMIN_BIAS else None
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        j = i % n_sets
+        if ev is not None:
+            ev[0].record(stream)
+        op.pack_weights(w)
+        if ev is not None:
+            ev[1].record(stream)
+        op(xs[j], w, b, ga, be, bias2=b2, out=ys[j], argmin=am, weights_packed=True)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    op.check()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    op.check()
+    total_ms = t_start.elapsed_time(t_end)
+    ms = total_ms / args.steps
+    main_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    pack_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    if pg is not None:
+        t = torch.tensor([ms, main_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms, main_ms = float(t[0]), float(t[1])
+    value = wl.flops * world / (ms / 1e3) / 1e12
+
+    # roofline of the dominant kernel (the fused tensor-core kernel)
+    flops, nbytes = wl.flops, wl.algorithmic_bytes
+    tc_peak = peaks["bf16_tflops"] * (1.0 if bf else TF32_PER_BF16)
+    t_flop = flops / (tc_peak * 1e12)
+    t_byte = nbytes / (peaks["hbm_gbs"] * 1e9)
+    if t_byte >= t_flop:
+        ach = nbytes / (main_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"]}
+    else:
+        ach = flops / (main_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s", "frac": ach / tc_peak}
+    roof.update({"traffic": read_traffic(wl.name, path), "peak_source": peaks["source"],
+                 "kernel": f"tc_conv_kernel ({path})", "kernel_ms": main_ms, "pack_ms": pack_ms,
+                 "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                 "tensor_frac": (flops / (main_ms / 1e3) / 1e12) / tc_peak,
+                 "hbm_frac": (nbytes / (main_ms / 1e3) / 1e9) / peaks["hbm_gbs"]})
+
+    e2e = measure_e2e(args, wl, op, inp, dev, tdt, bf, w, b, ga, be, b2, am)
+    if pg is not None:
+        t = torch.tensor([e2e["ms_per_step"]], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e["ms_per_step"] = float(t[0])
+        e2e["value"] = wl.flops * world / (e2e["ms_per_step"] / 1e3) / 1e12
+
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cpu = time_oracle(wl, seconds=args.cpu_seconds)
+        line = {"metric": args.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": dtype_name(wl, path), "data": "synthetic",
+                "config": config_of(wl, {"path": path, "parallelism": f"dp{world}" if world > 1 else "single",
+                                         "l2": f"inputs rotate over {n_sets} x/y buffer sets "
+                                               f"({n_sets * per_set / 2**20:.0f} MiB > 129 MiB L2)"
+                                         if n_sets > 1 else "working set larger than L2",
+                                         "step": "weight pack + fused kernel through the C ABI"}),
+                "roofline": roof, "cpu_baseline": cpu,
+                "e2e": {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
+                "gpu_launches": args.steps * op.info.kernels, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def measure_e2e(args, wl, op, inp, dev, tdt, bf, w_dev, b_dev, ga_dev, be_dev, b2_dev, am):
+    """Same step through the C ABI from pinned host buffers: H2D of x and the parameters, the
+    operator, D2H of the result, all inside the timed region."""
+    import torch
+    host = {}
+    for k in ("x", "w"):
+        t = torch.from_numpy(inp[k])
+        host[k] = (t.to(tdt) if bf else t).pin_memory()
+    for k in ("b", "gamma", "beta", "bias2"):
+        host[k] = None if inp[k] is None else torch.from_numpy(inp[k]).pin_memory()
+    dbuf = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in host.items()}
+    y = torch.empty((wl.N, wl.C_out, op.T_out), dtype=op.out_dtype(), device=dev)
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = y_host.numel() * y_host.element_size()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for k, v in host.items():
+            if v is not None:
+                dbuf[k].copy_(v, non_blocking=True)
+        op(dbuf["x"], dbuf["w"], dbuf["b"], dbuf["gamma"], dbuf["beta"], bias2=dbuf["bias2"], out=y, argmin=am)
+        y_host.copy_(y, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    return {"value": wl.flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def read_traffic(workload, path):
+    """DRAM bytes per launch of the main kernel from a committed ncu summary, if it was taken on the
+    current kernel sources; None otherwise."""
+    try:
+        from gemm_groupnorm_accelerator_gb300 import _build_lib
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        rec = d.get(workload)
+        if rec and rec.get("source_fingerprint") == _build_lib._fingerprint() and rec.get("path") == path:
+            return rec["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=synth.CONV_GN.name)
+    ap.add_argument("--math", type=int, default=0, help="0 auto, 1 SIMT, 2 tensor")
+    ap.add_argument("--path", type=int, default=-1, help="force an execution path (c1n_path)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--oracle-rows", type=int, default=2, help="batch entries per reference-arm step")
+    ap.add_argument("--metric", default="fused conv1d+GroupNorm TFLOP/s")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    wl = workload_by_name(args.workload)
+    if args.impl == "reference":
+        reference_arm(args, wl)
+    else:
+        our_arm(args, wl)
+
+
+if __name__ == "__main__":
+    main()

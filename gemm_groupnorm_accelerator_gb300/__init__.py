@@ -1,0 +1,236 @@
+"""Python binding of the conv1d_norm C ABI (``include/conv1d_norm.h``).
+
+Argument marshalling only: every step of the operator runs in the CUDA library
+(``libconv1dnorm.so``, built in-tree for sm_103a). The functions below carry the
+C names; ``Conv1dNorm`` is a small convenience wrapper that allocates the workspace
+and outputs with PyTorch and passes raw device pointers and the current stream.
+There is no fallback: if the library is missing, ``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+from . import _build_lib
+
+NORM_NONE, NORM_GROUP, NORM_CHANNEL_LAYER = 0, 1, 2
+POST_NONE, POST_GELU_ERF, POST_ROWMIN_BIAS = 0, 1, 2
+F32, BF16 = 0, 1
+MATH_AUTO, MATH_SIMT, MATH_TENSOR = 0, 1, 2
+PATH_AUTO, PATH_SIMT, PATH_TC_DIRECT, PATH_TC_CLUSTER, PATH_TC_TWO_PASS, PATH_TC_LINEAR = -1, 0, 1, 2, 3, 4
+PATH_NAMES = {0: "simt", 1: "tc_direct", 2: "tc_cluster", 3: "tc_two_pass", 4: "tc_linear"}
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(8)
+
+EXPORTED_SYMBOLS = (
+    "conv1d_norm_desc_create", "conv1d_norm_workspace_size", "conv1d_norm_set_workspace", "conv1d_norm_plan_info",
+    "conv1d_norm_run", "conv1d_norm_run_ex", "conv1d_norm_pack_weights", "conv1d_norm_check", "conv1d_norm_destroy",
+    "conv1d_norm_status_string", "conv1d_norm_last_error", "conv1d_norm_version",
+)
+
+
+class Params(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("N", "C_in", "C_out", "T", "k", "stride", "pad_left", "pad_right", "dilation", "norm", "groups")]
+    _fields_ += [("eps", ctypes.c_float)] + [(n, ctypes.c_int32) for n in ("post", "dtype", "math", "force_path")]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("path", "T_out", "tile_t", "tile_co", "mma_n", "cluster", "n_tiles", "grid", "kernels", "reserved")]
+    _fields_ += [("workspace_bytes", ctypes.c_int64)]
+
+
+class Args(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("w", ctypes.c_void_p), ("b", ctypes.c_void_p), ("gamma", ctypes.c_void_p),
+                ("beta", ctypes.c_void_p), ("bias2", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("argmin", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("flags", ctypes.c_uint32)]
+
+
+FLAG_WEIGHTS_PACKED = 1
+
+
+class C1NError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"conv1d_norm status {status}: {message}")
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    return _build_lib.build(force=force)
+
+
+def library_path() -> str:
+    return _build_lib.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libconv1dnorm.so (building it first if needed). Raises if it cannot be loaded."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build_lib.LIB
+        if build_if_missing:
+            path = _build_lib.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library {path} is missing; run build()")
+        lib = ctypes.CDLL(path)
+        P = ctypes.POINTER
+        vp = ctypes.c_void_p
+        lib.conv1d_norm_desc_create.argtypes = [P(Params), P(vp)]
+        lib.conv1d_norm_workspace_size.argtypes = [vp, P(ctypes.c_size_t)]
+        lib.conv1d_norm_set_workspace.argtypes = [vp, vp, ctypes.c_size_t]
+        lib.conv1d_norm_plan_info.argtypes = [vp, P(PlanInfo)]
+        lib.conv1d_norm_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.conv1d_norm_run_ex.argtypes = [vp, P(Args), vp]
+        lib.conv1d_norm_pack_weights.argtypes = [vp, vp, vp, ctypes.c_size_t, vp]
+        lib.conv1d_norm_check.argtypes = [vp, vp, vp]
+        lib.conv1d_norm_destroy.argtypes = [vp]
+        lib.conv1d_norm_destroy.restype = None
+        lib.conv1d_norm_status_string.argtypes = [ctypes.c_int]
+        lib.conv1d_norm_status_string.restype = ctypes.c_char_p
+        lib.conv1d_norm_last_error.argtypes = []
+        lib.conv1d_norm_last_error.restype = ctypes.c_char_p
+        lib.conv1d_norm_version.restype = ctypes.c_int32
+        for name in ("conv1d_norm_desc_create", "conv1d_norm_workspace_size", "conv1d_norm_set_workspace",
+                     "conv1d_norm_plan_info", "conv1d_norm_run", "conv1d_norm_run_ex", "conv1d_norm_pack_weights",
+                     "conv1d_norm_check"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != OK:
+        lib = load()
+        raise C1NError(status, (lib.conv1d_norm_last_error() or b"").decode() or
+                       lib.conv1d_norm_status_string(status).decode())
+
+
+# ------------------------------------------------------------------------------ C-named wrappers
+
+def make_params(N, C_in, C_out, T, k, stride=1, pad_left=0, pad_right=0, dilation=1, norm=NORM_NONE, groups=1,
+                eps=1e-5, post=POST_NONE, dtype=F32, math=MATH_AUTO, force_path=PATH_AUTO) -> Params:
+    return Params(N, C_in, C_out, T, k, stride, pad_left, pad_right, dilation, norm, groups, eps, post, dtype, math,
+                  force_path)
+
+
+def conv1d_norm_desc_create(params: Params) -> int:
+    h = ctypes.c_void_p()
+    _check(load().conv1d_norm_desc_create(ctypes.byref(params), ctypes.byref(h)))
+    return h.value
+
+
+def conv1d_norm_workspace_size(desc: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().conv1d_norm_workspace_size(desc, ctypes.byref(n)))
+    return n.value
+
+
+def conv1d_norm_set_workspace(desc: int, ptr: int, nbytes: int) -> None:
+    _check(load().conv1d_norm_set_workspace(desc, ptr, nbytes))
+
+
+def conv1d_norm_plan_info(desc: int) -> PlanInfo:
+    info = PlanInfo()
+    _check(load().conv1d_norm_plan_info(desc, ctypes.byref(info)))
+    return info
+
+
+def conv1d_norm_run(desc: int, x: int, w: int, b: Optional[int], gamma: Optional[int], beta: Optional[int], y: int,
+                    stream: int) -> None:
+    _check(load().conv1d_norm_run(desc, x, w, b, gamma, beta, y, stream))
+
+
+def conv1d_norm_run_ex(desc: int, args: Args, stream: int) -> None:
+    _check(load().conv1d_norm_run_ex(desc, ctypes.byref(args), stream))
+
+
+def conv1d_norm_pack_weights(desc: int, w: int, workspace: Optional[int], workspace_bytes: int, stream: int) -> None:
+    _check(load().conv1d_norm_pack_weights(desc, w, workspace, workspace_bytes, stream))
+
+
+def conv1d_norm_check(desc: int, workspace: Optional[int], stream: int) -> None:
+    _check(load().conv1d_norm_check(desc, workspace, stream))
+
+
+def conv1d_norm_destroy(desc: int) -> None:
+    load().conv1d_norm_destroy(desc)
+
+
+def conv1d_norm_status_string(status: int) -> str:
+    return load().conv1d_norm_status_string(status).decode()
+
+
+def conv1d_norm_version() -> int:
+    return int(load().conv1d_norm_version())
+
+
+# ------------------------------------------------------------------------------ convenience wrapper
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+class Conv1dNorm:
+    """One descriptor plus its workspace; calls go through ``conv1d_norm_run_ex`` on the current stream."""
+
+    def __init__(self, params: Params, device=None):
+        import torch
+        self.params = params
+        self.desc = conv1d_norm_desc_create(params)
+        self.info = conv1d_norm_plan_info(self.desc)
+        self.T_out = self.info.T_out
+        nbytes = conv1d_norm_workspace_size(self.desc)
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        self.workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        conv1d_norm_set_workspace(self.desc, self.workspace.data_ptr(), self.workspace.numel())
+
+    @property
+    def path(self) -> str:
+        return PATH_NAMES[self.info.path]
+
+    def out_dtype(self):
+        import torch
+        return torch.bfloat16 if self.params.dtype == BF16 else torch.float32
+
+    def pack_weights(self, w, stream=None):
+        import torch
+        s = torch.cuda.current_stream(w.device).cuda_stream if stream is None else stream
+        conv1d_norm_pack_weights(self.desc, w.data_ptr(), None, 0, s)
+
+    def __call__(self, x, w, b=None, gamma=None, beta=None, bias2=None, out=None, argmin=None, stream=None,
+                 weights_packed=False):
+        import torch
+        p = self.params
+        if out is None:
+            out = torch.empty((p.N, p.C_out, self.T_out), dtype=self.out_dtype(), device=x.device)
+        args = Args(_ptr(x), _ptr(w), _ptr(b), _ptr(gamma), _ptr(beta), _ptr(bias2), _ptr(out), _ptr(argmin), None, 0,
+                    FLAG_WEIGHTS_PACKED if weights_packed else 0)
+        s = torch.cuda.current_stream(x.device).cuda_stream if stream is None else stream
+        conv1d_norm_run_ex(self.desc, args, s)
+        return out
+
+    def check(self, stream=None):
+        import torch
+        s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+        conv1d_norm_check(self.desc, None, s)
+
+    def close(self):
+        if getattr(self, "desc", None):
+            conv1d_norm_destroy(self.desc)
+            self.desc = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,570 @@
+// C ABI, validation and planning of the fused Conv1d + normalization operator.
+// The operator is defined on the Kimi-K2.6 l2_p35 (Conv1d + GroupNorm), l2_p75 (Linear +
+// GroupNorm + row-min + bias), l1_p5 (causal Conv1d as a GEMM) and l2_p3 (LayerNorm, exact GELU)
+// pages; the output length is the padded-window count of the l2_p35 page's output-length check
+// with separate left/right padding.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "c1n_internal.h"
+#include "sm100_ptx.cuh"
+
+using namespace c1n;
+
+struct c1n_desc {
+    c1n_params p;
+    Plan plan;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    // cached TMA descriptors (re-encoded when a pointer changes)
+    const void* tm_x_ptr = nullptr;
+    const void* tm_w_ptr = nullptr;
+    CUtensorMap tm_a;  // A operand map
+    CUtensorMap tm_b;  // B operand map
+    int device = -1;
+    int num_sms = 0;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+c1n_status fail(c1n_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+c1n_status fail(c1n_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+c1n_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(C1N_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+long long t_out_of(const c1n_params& p) {
+    long long span = (long long)p.T + p.pad_left + p.pad_right - (long long)p.dilation * (p.k - 1) - 1;
+    if (span < 0) return 0;
+    return span / p.stride + 1;
+}
+
+// Why the tensor-core conv path cannot take this shape ("" when it can).
+const char* tc_conv_blocker(const c1n_params& p, const Plan&) {
+    if (p.stride != 1) return "stride > 1";
+    if (p.k > kMaxTaps) return "more than 16 taps";
+    if (p.N > 65535) return "N above 65535";
+    return "";
+}
+
+void plan_workspace(const c1n_params& p, Plan& pl, bool conv_tc, bool need_raw, bool need_stats) {
+    size_t off = kWsStatusBytes;
+    if (conv_tc) {
+        pl.ws_wp = off;
+        off = round_up(off + (size_t)p.k * p.C_out * pl.ci_pad * pl.esize, 256);
+    }
+    if (need_stats) {
+        pl.ws_stats = off;
+        size_t n = p.norm == C1N_NORM_GROUP ? (size_t)p.N * p.groups : (size_t)p.N * pl.T_out;
+        off = round_up(off + n * sizeof(float2), 256);
+    }
+    if (p.post == C1N_POST_ROWMIN_BIAS) {
+        pl.ws_rowmin = off;
+        off = round_up(off + (size_t)p.N * pl.T_out * sizeof(float), 256);
+    }
+    if (need_raw) {
+        pl.ws_raw = off;
+        off = round_up(off + (size_t)p.N * p.C_out * pl.T_out * sizeof(float), 256);
+    }
+    pl.ws_total = off;
+}
+
+// Channel blocks of at most 256 (MMA N), balanced and rounded to 16.
+void plan_channel_blocks(const c1n_params& p, Plan& pl) {
+    pl.n_cb = (int)ceil_div(p.C_out, 256);
+    pl.BN = (int)round_up(ceil_div(p.C_out, pl.n_cb), 16);
+    pl.b_slot_bytes = pl.BN * 128;
+}
+
+// Ring depths from the shared-memory budget (one CTA per SM).
+void plan_stages(Plan& pl, int max_a, int max_b) {
+    const int budget = 227 * 1024 - 1024 - kTcMiscBytes;
+    pl.stages_a = max_a;
+    pl.stages_b = max_b;
+    while (pl.stages_a * pl.a_slot_bytes + pl.stages_b * pl.b_slot_bytes > budget && pl.stages_b > 2) --pl.stages_b;
+    while (pl.stages_a * pl.a_slot_bytes + pl.stages_b * pl.b_slot_bytes > budget && pl.stages_a > 2) --pl.stages_a;
+    pl.smem_bytes = 1024 + pl.stages_a * pl.a_slot_bytes + pl.stages_b * pl.b_slot_bytes + kTcMiscBytes;
+}
+
+// Geometry of the tensor-core conv tiles: 128 output time steps x BN channels per tile; the A tile
+// carries the (k-1)*dilation halo rows. `cluster` selects one CTA per tile with single-buffered
+// TMEM (cluster GroupNorm) instead of the persistent double-buffered layout.
+bool plan_tc_geometry(const c1n_params& p, Plan& pl, bool cluster) {
+    pl.BK = pl.bf16 ? 64 : 32;
+    const long long halo = (long long)(p.k - 1) * p.dilation;
+    if (halo > 256) return false;
+    pl.R = (int)round_up(128 + halo, 8);
+    pl.a_slot_bytes = pl.R * 128;
+    pl.n_ci_chunks = (int)ceil_div(p.C_in, pl.BK);
+    pl.ci_pad = pl.n_ci_chunks * pl.BK;
+    plan_channel_blocks(p, pl);
+    pl.cb_per_unit = 1;
+    pl.n_t_tiles = (int)ceil_div(pl.T_out, 128);
+    pl.n_units = p.N * pl.n_t_tiles * pl.n_cb;
+    if (cluster) {
+        pl.n_acc = 1;
+        pl.tmem_cols = 256;
+    } else {
+        pl.n_acc = 2;
+        pl.tmem_cols = 512;
+    }
+    plan_stages(pl, 3, 6);
+    return pl.smem_bytes <= 227 * 1024;
+}
+
+bool plan_tc_linear(const c1n_params& p, Plan& pl) {
+    pl.BK = pl.bf16 ? 64 : 32;
+    pl.R = 128;
+    pl.a_slot_bytes = 128 * 128;
+    pl.n_ci_chunks = (int)ceil_div(p.C_in, pl.BK);
+    pl.ci_pad = 0;
+    plan_channel_blocks(p, pl);
+    pl.cb_per_unit = 1;
+    pl.n_t_tiles = (int)ceil_div(p.N, 128);  // row tiles
+    pl.n_units = pl.n_t_tiles * pl.n_cb;
+    pl.n_acc = 2;
+    pl.tmem_cols = 512;
+    plan_stages(pl, 4, 4);
+    return pl.smem_bytes <= 227 * 1024;
+}
+
+c1n_status make_plan(const c1n_params& p, Plan& pl) {
+    pl = Plan();
+    pl.T_out = t_out_of(p);
+    pl.bf16 = p.dtype == C1N_BF16;
+    pl.esize = pl.bf16 ? 2 : 4;
+    pl.align = 16 / pl.esize;
+    const bool is_linear = p.T == 1 && p.k == 1 && p.pad_left == 0 && p.pad_right == 0 && p.stride == 1;
+    const bool out_needs_second_pass = p.norm != C1N_NORM_NONE || p.post == C1N_POST_ROWMIN_BIAS;
+    int want = p.force_path;
+
+    auto choose_simt = [&]() {
+        pl.path = C1N_PATH_SIMT;
+        const bool need_stats = p.norm != C1N_NORM_NONE;
+        const bool need_raw = out_needs_second_pass && pl.bf16;
+        plan_workspace(p, pl, false, need_raw, need_stats);
+        pl.kernels = 1 + (need_stats ? 2 : 0) + (p.post == C1N_POST_ROWMIN_BIAS ? (need_stats ? 1 : 2) : 0);
+        pl.grid = (int)(ceil_div(pl.T_out, 64) * ceil_div(p.C_out, 64) * p.N);
+        pl.n_units = pl.grid;
+        return C1N_OK;
+    };
+
+    if (p.math == C1N_MATH_SIMT) {
+        if (want != C1N_PATH_AUTO && want != C1N_PATH_SIMT)
+            return fail(C1N_ERR_INVALID_ARG, "force_path %d conflicts with math=SIMT", want);
+        return choose_simt();
+    }
+    if (want == C1N_PATH_SIMT) return choose_simt();
+
+    // ---------------------------------------------------------------- tensor-core plans
+    const char* why = "";
+    if (is_linear && (want == C1N_PATH_AUTO || want == C1N_PATH_TC_LINEAR)) {
+        if (p.C_in % pl.align != 0) {
+            why = "Linear: input features not a multiple of 16 bytes of elements";
+        } else if (plan_tc_linear(p, pl)) {
+            pl.path = C1N_PATH_TC_LINEAR;
+            const bool need_stats = p.norm != C1N_NORM_NONE;
+            const bool need_raw = out_needs_second_pass && pl.bf16;
+            plan_workspace(p, pl, false, need_raw, need_stats);
+            pl.kernels = 1 + (need_stats ? 1 : 0) + (p.post == C1N_POST_ROWMIN_BIAS ? 2 : (need_stats ? 1 : 0));
+            pl.cluster = 1;
+            return C1N_OK;
+        }
+    } else if (want == C1N_PATH_TC_LINEAR) {
+        why = "TC_LINEAR needs T = 1, k = 1, stride 1 and no padding";
+    } else {
+        why = tc_conv_blocker(p, pl);
+        if (!*why) {
+            const int cpg = p.norm == C1N_NORM_GROUP ? p.C_out / p.groups : 0;
+            // 1. GroupNorm fused through a cluster of CTAs along time (one cluster per sample and
+            //    channel block; groups must not straddle a channel block).
+            Plan trial = pl;
+            const bool geom_ok = plan_tc_geometry(p, trial, true);
+            const bool gn_cluster_ok = p.norm == C1N_NORM_GROUP && p.post != C1N_POST_ROWMIN_BIAS && geom_ok &&
+                                       trial.n_t_tiles <= 8 && (trial.n_cb == 1 || trial.BN % cpg == 0);
+            if ((want == C1N_PATH_AUTO || want == C1N_PATH_TC_CLUSTER) && gn_cluster_ok) {
+                pl = trial;
+                pl.path = C1N_PATH_TC_CLUSTER;
+                pl.cluster = pl.n_t_tiles;
+                pl.grid = pl.n_units;
+                plan_workspace(p, pl, true, false, false);
+                pl.kernels = 2;
+                return C1N_OK;
+            }
+            if (want == C1N_PATH_TC_CLUSTER)
+                why = "TC_CLUSTER needs GroupNorm, no row-min, T_out <= 1024 and groups inside a channel block";
+            // 2. Direct epilogue (no normalization).
+            if (!*why && p.norm == C1N_NORM_NONE && p.post != C1N_POST_ROWMIN_BIAS &&
+                (want == C1N_PATH_AUTO || want == C1N_PATH_TC_DIRECT)) {
+                if (plan_tc_geometry(p, pl, false)) {
+                    pl.path = C1N_PATH_TC_DIRECT;
+                    plan_workspace(p, pl, true, false, false);
+                    pl.kernels = 2;
+                    return C1N_OK;
+                }
+                why = "tap span too wide for one A tile";
+            } else if (want == C1N_PATH_TC_DIRECT) {
+                why = "TC_DIRECT needs norm NONE and no row-min";
+            }
+            // 3. Two passes: raw tiles, then statistics and normalize / row-min passes.
+            if (!*why && (want == C1N_PATH_AUTO || want == C1N_PATH_TC_TWO_PASS)) {
+                if (plan_tc_geometry(p, pl, false)) {
+                    pl.path = C1N_PATH_TC_TWO_PASS;
+                    const bool need_stats = p.norm != C1N_NORM_NONE;
+                    const bool need_raw = out_needs_second_pass && pl.bf16;
+                    plan_workspace(p, pl, true, need_raw, need_stats);
+                    pl.kernels = 2 + (need_stats ? 1 : 0) + (p.post == C1N_POST_ROWMIN_BIAS ? 2 : 1);
+                    return C1N_OK;
+                }
+                why = "tap span too wide for one A tile";
+            }
+        }
+    }
+    if (p.math == C1N_MATH_TENSOR || want != C1N_PATH_AUTO)
+        return fail(C1N_ERR_UNSUPPORTED, "tensor-core path unavailable: %s", *why ? why : "forced path not applicable");
+    return choose_simt();
+}
+
+c1n_status validate(const c1n_params* p) {
+    if (!p) return fail(C1N_ERR_INVALID_ARG, "params is NULL");
+    if (p->N < 1 || p->C_in < 1 || p->C_out < 1 || p->T < 1 || p->k < 1)
+        return fail(C1N_ERR_INVALID_ARG, "N, C_in, C_out, T and k must be >= 1");
+    if (p->stride < 1 || p->dilation < 1) return fail(C1N_ERR_INVALID_ARG, "stride and dilation must be >= 1");
+    if (p->pad_left < 0 || p->pad_right < 0) return fail(C1N_ERR_INVALID_ARG, "padding must be >= 0");
+    if (p->norm < 0 || p->norm > 2) return fail(C1N_ERR_INVALID_ARG, "unknown norm %d", p->norm);
+    if (p->post < 0 || p->post > 2) return fail(C1N_ERR_INVALID_ARG, "unknown post-op %d", p->post);
+    if (p->dtype < 0 || p->dtype > 1) return fail(C1N_ERR_INVALID_ARG, "unknown dtype %d", p->dtype);
+    if (p->math < 0 || p->math > 2) return fail(C1N_ERR_INVALID_ARG, "unknown math %d", p->math);
+    if (p->force_path < -1 || p->force_path > 4) return fail(C1N_ERR_INVALID_ARG, "unknown path %d", p->force_path);
+    if (p->norm == C1N_NORM_GROUP && (p->groups < 1 || p->C_out % p->groups != 0))
+        return fail(C1N_ERR_INVALID_ARG, "GroupNorm needs groups >= 1 dividing C_out (%d %% %d)", p->C_out, p->groups);
+    if (p->norm != C1N_NORM_NONE && !(std::isfinite(p->eps) && p->eps > 0.f))
+        return fail(C1N_ERR_INVALID_ARG, "eps must be finite and > 0");
+    const long long T_out = t_out_of(*p);
+    if (T_out < 1) return fail(C1N_ERR_INVALID_ARG, "empty output: T_out = %lld", T_out);
+    const long long elems_y = (long long)p->N * p->C_out * T_out;
+    const long long elems_x = (long long)p->N * p->C_in * p->T;
+    if (elems_y > (1LL << 40) || elems_x > (1LL << 40)) return fail(C1N_ERR_INVALID_ARG, "tensor too large");
+    if (T_out > (1LL << 31) - 1 || (long long)p->T + p->pad_left + p->pad_right > (1LL << 31) - 1)
+        return fail(C1N_ERR_INVALID_ARG, "time axis too long");
+    return C1N_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+c1n_status encode(CUtensorMap* m, const void* ptr, bool bf16, int rank, const cuuint64_t* dims,
+                  const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+    auto fn = encode_fn();
+    if (!fn) return fail(C1N_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank,
+                    const_cast<void*>(ptr), dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(C1N_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return C1N_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+c1n_status ensure_device(c1n_desc* d) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != d->device) {
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (d->plan.path != C1N_PATH_SIMT && !(major == 10 && minor == 3))
+            return fail(C1N_ERR_UNSUPPORTED, "tensor-core path is built for sm_103a; device is sm_%d%d", major, minor);
+        d->device = dev;
+        d->num_sms = sms;
+        d->tm_x_ptr = d->tm_w_ptr = nullptr;
+    }
+    return C1N_OK;
+}
+
+c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
+    const c1n_params& p = d->p;
+    const Plan& pl = d->plan;
+    if (!a->x || !a->w || !a->y) return fail(C1N_ERR_INVALID_ARG, "x, w and y must be non-NULL");
+    if (p.post == C1N_POST_ROWMIN_BIAS && !a->bias2) return fail(C1N_ERR_INVALID_ARG, "row-min post-op needs bias2");
+    void* ws = a->workspace ? a->workspace : d->ws;
+    size_t ws_bytes = a->workspace ? a->workspace_bytes : d->ws_bytes;
+    if (!ws || ws_bytes < pl.ws_total)
+        return fail(C1N_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", pl.ws_total, ws ? ws_bytes : 0);
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(C1N_ERR_ALIGNMENT, "workspace not 256-byte aligned");
+    c1n_status st = ensure_device(d);
+    if (st != C1N_OK) return st;
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    int* status = reinterpret_cast<int*>(wsb);
+    float2* stats = reinterpret_cast<float2*>(wsb + pl.ws_stats);
+    float* rowmin = reinterpret_cast<float*>(wsb + pl.ws_rowmin);
+    const bool need_stats = p.norm != C1N_NORM_NONE;
+    const bool second = need_stats || p.post == C1N_POST_ROWMIN_BIAS;
+    // Raw conv values (fp32) for the statistics / normalize passes: y itself when y is fp32.
+    float* raw = pl.bf16 ? reinterpret_cast<float*>(wsb + pl.ws_raw) : static_cast<float*>(a->y);
+    cudaError_t e;
+
+    if (pl.path == C1N_PATH_SIMT) {
+        e = launch_simt_conv(p, pl, a->x, a->w, a->b, second ? static_cast<void*>(raw) : a->y, second, s);
+        if (e != cudaSuccess) return cuda_fail(e, "SIMT conv launch");
+    } else {
+        const bool linear = pl.path == C1N_PATH_TC_LINEAR;
+        if (linear && (!aligned16(a->x) || !aligned16(a->w)))
+            return fail(C1N_ERR_ALIGNMENT, "x and w must be 16-byte aligned on the Linear tensor-core path");
+        const void* wsrc = a->w;
+        if (!linear) {
+            void* wp = wsb + pl.ws_wp;
+            if (!(a->flags & C1N_FLAG_WEIGHTS_PACKED)) {
+                e = launch_pack_weights(p, pl, a->w, wp, s);
+                if (e != cudaSuccess) return cuda_fail(e, "weight pack launch");
+            }
+            wsrc = wp;
+        }
+        if (d->tm_x_ptr != a->x || d->tm_w_ptr != wsrc) {
+            const cuuint64_t es = (cuuint64_t)pl.esize;
+            if (linear) {
+                // A: X[rows][in], box = BK channels x 128 rows; B: W[out][in], box = BK x BN.
+                cuuint64_t dx[2] = {(cuuint64_t)p.C_in, (cuuint64_t)p.N};
+                cuuint64_t sx[1] = {(cuuint64_t)p.C_in * es};
+                cuuint32_t bx[2] = {(cuuint32_t)pl.BK, 128u};
+                st = encode(&d->tm_a, a->x, pl.bf16, 2, dx, sx, bx);
+                if (st != C1N_OK) return st;
+                cuuint64_t dw[2] = {(cuuint64_t)p.C_in, (cuuint64_t)p.C_out};
+                cuuint64_t sw[1] = {(cuuint64_t)p.C_in * es};
+                cuuint32_t bw[2] = {(cuuint32_t)pl.BK, (cuuint32_t)pl.BN};
+                st = encode(&d->tm_b, wsrc, pl.bf16, 2, dw, sw, bw);
+                if (st != C1N_OK) return st;
+            } else {
+                // B: packed weights wp[kk][co][ci_pad], box = BK channels x BN outputs x 1 tap.
+                // (A is written by the kernel's transposer warps; its map slot repeats B's.)
+                cuuint64_t dw[3] = {(cuuint64_t)pl.ci_pad, (cuuint64_t)p.C_out, (cuuint64_t)p.k};
+                cuuint64_t sw[2] = {(cuuint64_t)pl.ci_pad * es, (cuuint64_t)pl.ci_pad * p.C_out * es};
+                cuuint32_t bw[3] = {(cuuint32_t)pl.BK, (cuuint32_t)pl.BN, 1};
+                st = encode(&d->tm_b, wsrc, pl.bf16, 3, dw, sw, bw);
+                if (st != C1N_OK) return st;
+                d->tm_a = d->tm_b;
+            }
+            d->tm_x_ptr = a->x;
+            d->tm_w_ptr = wsrc;
+        }
+        TcArgs t;
+        std::memset(&t, 0, sizeof(t));
+        t.N = p.N; t.C_in = p.C_in; t.C_out = p.C_out; t.T = p.T; t.T_out = (int)pl.T_out; t.k = p.k;
+        t.dil = p.dilation; t.pad_left = p.pad_left;
+        t.BK = pl.BK; t.R = pl.R; t.BN = pl.BN; t.n_cb = pl.n_cb; t.cb_per_unit = pl.cb_per_unit;
+        t.n_ci_chunks = pl.n_ci_chunks; t.n_t_tiles = pl.n_t_tiles; t.n_units = pl.n_units;
+        t.n_acc = pl.n_acc; t.tmem_cols = pl.tmem_cols; t.stages_a = pl.stages_a; t.stages_b = pl.stages_b;
+        t.a_slot_bytes = pl.a_slot_bytes; t.b_slot_bytes = pl.b_slot_bytes;
+        t.groups = p.norm == C1N_NORM_GROUP ? p.groups : 1;
+        t.cpg = p.C_out / t.groups;
+        t.eps = p.eps;
+        t.gelu = (p.post == C1N_POST_GELU_ERF && (pl.path == C1N_PATH_TC_DIRECT || pl.path == C1N_PATH_TC_CLUSTER)) ? 1 : 0;
+        const uint32_t fmt = pl.bf16 ? 1u : 2u;
+        t.idesc = make_idesc(fmt, fmt, 0u, 0u, 128u, (uint32_t)pl.BN);
+        t.x = a->x;
+        t.bias = a->b;
+        t.gamma = a->gamma;
+        t.beta = a->beta;
+        const bool fused_out = pl.path == C1N_PATH_TC_DIRECT || pl.path == C1N_PATH_TC_CLUSTER;
+        t.y = fused_out ? a->y : (second ? static_cast<void*>(raw) : a->y);
+        t.status = status;
+        const bool out_bf16 = pl.bf16 && (fused_out || !second);
+        e = launch_tc(pl, t, d->tm_a, d->tm_b, linear,
+                      pl.path == C1N_PATH_TC_CLUSTER ? kEpiClusterGN : kEpiDirect, out_bf16, d->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
+        if (fused_out) return C1N_OK;
+    }
+    if (!second) return C1N_OK;
+    if (need_stats) {
+        e = p.norm == C1N_NORM_GROUP ? launch_gn_stats(p, pl, raw, stats, s) : launch_ln_stats(p, pl, raw, stats, s);
+        if (e != cudaSuccess) return cuda_fail(e, "statistics launch");
+    }
+    if (p.post == C1N_POST_ROWMIN_BIAS) {
+        e = launch_rowmin(p, pl, raw, stats, need_stats ? a->gamma : nullptr, need_stats ? a->beta : nullptr, rowmin,
+                          a->argmin, s);
+        if (e != cudaSuccess) return cuda_fail(e, "row-min launch");
+        e = launch_broadcast(p, pl, rowmin, a->bias2, a->y, s);
+        if (e != cudaSuccess) return cuda_fail(e, "broadcast launch");
+    } else {
+        e = launch_normalize(p, pl, raw, stats, a->gamma, a->beta, a->y, s);
+        if (e != cudaSuccess) return cuda_fail(e, "normalize launch");
+    }
+    return C1N_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+c1n_status conv1d_norm_desc_create(const c1n_params* params, c1n_desc** out) {
+    g_last_error.clear();
+    if (!out) return fail(C1N_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    c1n_status st = validate(params);
+    if (st != C1N_OK) return st;
+    Plan pl;
+    st = make_plan(*params, pl);
+    if (st != C1N_OK) return st;
+    c1n_desc* d = new (std::nothrow) c1n_desc();
+    if (!d) return fail(C1N_ERR_INVALID_ARG, "out of host memory");
+    d->p = *params;
+    d->plan = pl;
+    *out = d;
+    return C1N_OK;
+}
+
+c1n_status conv1d_norm_workspace_size(const c1n_desc* desc, size_t* bytes) {
+    if (!desc || !bytes) return fail(C1N_ERR_INVALID_ARG, "NULL argument");
+    *bytes = desc->plan.ws_total;
+    return C1N_OK;
+}
+
+c1n_status conv1d_norm_set_workspace(c1n_desc* desc, void* workspace, size_t bytes) {
+    if (!desc) return fail(C1N_ERR_INVALID_ARG, "desc is NULL");
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(C1N_ERR_ALIGNMENT, "workspace not 256-byte aligned");
+    if (workspace && bytes < desc->plan.ws_total)
+        return fail(C1N_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", desc->plan.ws_total, bytes);
+    desc->ws = workspace;
+    desc->ws_bytes = workspace ? bytes : 0;
+    return C1N_OK;
+}
+
+c1n_status conv1d_norm_plan_info(const c1n_desc* desc, c1n_plan_info* info) {
+    if (!desc || !info) return fail(C1N_ERR_INVALID_ARG, "NULL argument");
+    const Plan& pl = desc->plan;
+    std::memset(info, 0, sizeof(*info));
+    info->path = pl.path;
+    info->T_out = (int32_t)pl.T_out;
+    info->tile_t = pl.path == C1N_PATH_SIMT ? 64 : 128;
+    info->tile_co = pl.path == C1N_PATH_SIMT ? 64 : pl.BN;
+    info->mma_n = pl.path == C1N_PATH_SIMT ? 0 : pl.BN;
+    info->cluster = pl.cluster;
+    info->n_tiles = pl.path == C1N_PATH_SIMT ? pl.n_units : pl.n_units;
+    info->grid = pl.grid;
+    info->kernels = pl.kernels;
+    info->workspace_bytes = (int64_t)pl.ws_total;
+    return C1N_OK;
+}
+
+c1n_status conv1d_norm_run(c1n_desc* desc, const void* x, const void* w, const float* b, const float* gamma,
+                           const float* beta, void* y, c1n_stream_t stream) {
+    g_last_error.clear();
+    if (!desc) return fail(C1N_ERR_INVALID_ARG, "desc is NULL");
+    if (desc->p.post == C1N_POST_ROWMIN_BIAS)
+        return fail(C1N_ERR_INVALID_ARG, "row-min post-op needs conv1d_norm_run_ex (bias2)");
+    c1n_args a;
+    std::memset(&a, 0, sizeof(a));
+    a.x = x; a.w = w; a.b = b; a.gamma = gamma; a.beta = beta; a.y = y;
+    return run_impl(desc, &a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+c1n_status conv1d_norm_run_ex(c1n_desc* desc, const c1n_args* args, c1n_stream_t stream) {
+    g_last_error.clear();
+    if (!desc || !args) return fail(C1N_ERR_INVALID_ARG, "NULL argument");
+    return run_impl(desc, args, reinterpret_cast<cudaStream_t>(stream));
+}
+
+c1n_status conv1d_norm_pack_weights(c1n_desc* desc, const void* w, void* workspace, size_t workspace_bytes,
+                                    c1n_stream_t stream) {
+    g_last_error.clear();
+    if (!desc || !w) return fail(C1N_ERR_INVALID_ARG, "desc and w must be non-NULL");
+    const Plan& pl = desc->plan;
+    if (pl.path == C1N_PATH_SIMT || pl.path == C1N_PATH_TC_LINEAR) return C1N_OK;
+    void* ws = workspace ? workspace : desc->ws;
+    size_t ws_bytes = workspace ? workspace_bytes : desc->ws_bytes;
+    if (!ws || ws_bytes < pl.ws_total)
+        return fail(C1N_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", pl.ws_total, ws ? ws_bytes : 0);
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(C1N_ERR_ALIGNMENT, "workspace not 256-byte aligned");
+    cudaError_t e = launch_pack_weights(desc->p, pl, w, static_cast<uint8_t*>(ws) + pl.ws_wp,
+                                        reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "weight pack launch");
+    return C1N_OK;
+}
+
+c1n_status conv1d_norm_check(const c1n_desc* desc, void* workspace, c1n_stream_t stream) {
+    g_last_error.clear();
+    if (!desc) return fail(C1N_ERR_INVALID_ARG, "desc is NULL");
+    void* ws = workspace ? workspace : desc->ws;
+    if (!ws) return fail(C1N_ERR_WORKSPACE, "no workspace");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int word[16] = {0};
+    cudaError_t e = cudaMemcpyAsync(word, ws, sizeof(word), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (word[0] != 0) {
+        e = cudaMemsetAsync(ws, 0, sizeof(word), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "status reset");
+        if (word[0] == C1N_ERR_TIMEOUT)
+            return fail(C1N_ERR_TIMEOUT,
+                        "device wait timed out (site %d, CTA %d; progress b_loads=%d a_consumed=%d mma_units=%d "
+                        "a_written=%d epi_units=%d a_loads=%d; waiting: mma=%d epi=%d xp=%d tma=%d; mma_unit=%d "
+                        "rings=0x%08x)",
+                        word[1], word[2], word[3], word[4], word[5], word[6], word[7], word[8], word[9], word[10],
+                        word[11], word[12], word[13], (unsigned)word[14]);
+        return fail(C1N_ERR_DEVICE, "device status %d (detail %d)", word[0], word[1]);
+    }
+    return C1N_OK;
+}
+
+void conv1d_norm_destroy(c1n_desc* desc) { delete desc; }
+
+const char* conv1d_norm_status_string(c1n_status s) {
+    switch (s) {
+        case C1N_OK: return "ok";
+        case C1N_ERR_INVALID_ARG: return "invalid argument";
+        case C1N_ERR_UNSUPPORTED: return "unsupported on the requested path";
+        case C1N_ERR_ALIGNMENT: return "misaligned pointer";
+        case C1N_ERR_WORKSPACE: return "workspace missing or too small";
+        case C1N_ERR_CUDA: return "CUDA runtime error";
+        case C1N_ERR_TIMEOUT: return "device-side wait timed out";
+        case C1N_ERR_DEVICE: return "device-side check failed";
+    }
+    return "unknown status";
+}
+
+const char* conv1d_norm_last_error(void) { return g_last_error.c_str(); }
+
+int32_t conv1d_norm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// Internal plan, kernel-argument structures and launcher declarations of the conv1d_norm library.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/conv1d_norm.h"
+
+namespace c1n {
+
+constexpr int kMaxTaps = 16;
+constexpr int kWsStatusBytes = 256;
+
+// Everything the planner decides once per descriptor.
+struct Plan {
+    int path = C1N_PATH_SIMT;
+    long long T_out = 0;
+    int bf16 = 0;         // x/w/y are bf16
+    int esize = 4;        // bytes per x/w/y element
+    int align = 4;        // elements per 16 bytes
+    // tensor-core geometry: tiles of 128 output rows (time steps, or Linear rows) x BN channels
+    int BK = 32;          // input channels per pipeline stage (one 128-byte row)
+    int R = 128;          // rows of one A tile (128 + tap halo, multiple of 8)
+    int BN = 0;           // output channels per MMA (<= 256)
+    int n_cb = 0;         // channel blocks
+    int cb_per_unit = 1;  // channel blocks accumulated by one work unit
+    int n_ci_chunks = 0;
+    int ci_pad = 0;       // packed-weight row length (multiple of BK)
+    int n_t_tiles = 0;    // 128-row tiles along time (conv) or rows (Linear)
+    int n_units = 0;
+    int n_acc = 2;        // accumulators per CTA (2: epilogue overlaps the next mainloop)
+    int tmem_cols = 512;  // TMEM columns allocated per CTA
+    int cluster = 1;
+    int grid = 0;
+    int stages_a = 0, stages_b = 0;
+    int a_slot_bytes = 0, b_slot_bytes = 0;
+    int smem_bytes = 0;
+    int kernels = 0;
+    // workspace layout (byte offsets)
+    size_t ws_wp = 0, ws_stats = 0, ws_raw = 0, ws_rowmin = 0, ws_total = 0;
+};
+
+// Shared memory beyond the operand rings: barriers, flags and epilogue scratch.
+constexpr int kTcMiscBytes = 16384;
+
+// Arguments of the tensor-core kernel (passed by value as a __grid_constant__).
+struct TcArgs {
+    int N, C_in, C_out, T, T_out, k, dil, pad_left;
+    int BK, R, BN, n_cb, cb_per_unit, n_ci_chunks, n_t_tiles, n_units;
+    int n_acc, tmem_cols, stages_a, stages_b, a_slot_bytes, b_slot_bytes;
+    int groups, cpg;
+    float eps;
+    int gelu;
+    uint32_t idesc;
+    const void* x;
+    const float* bias;
+    const float* gamma;
+    const float* beta;
+    void* y;
+    int* status;
+};
+
+// Launchers (each enqueues on `stream`, returns cudaGetLastError()).
+cudaError_t launch_simt_conv(const c1n_params& p, const Plan& pl, const void* x, const void* w, const float* b,
+                             void* out, bool out_is_raw_f32, cudaStream_t stream);
+cudaError_t launch_gn_stats(const c1n_params& p, const Plan& pl, const float* raw, float2* stats, cudaStream_t stream);
+cudaError_t launch_ln_stats(const c1n_params& p, const Plan& pl, const float* raw, float2* stats, cudaStream_t stream);
+cudaError_t launch_normalize(const c1n_params& p, const Plan& pl, const float* raw, const float2* stats,
+                             const float* gamma, const float* beta, void* y, cudaStream_t stream);
+cudaError_t launch_rowmin(const c1n_params& p, const Plan& pl, const float* raw, const float2* stats,
+                          const float* gamma, const float* beta, float* rowmin, int32_t* argmin,
+                          cudaStream_t stream);
+cudaError_t launch_broadcast(const c1n_params& p, const Plan& pl, const float* rowmin, const float* bias2, void* y,
+                             cudaStream_t stream);
+cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream);
+
+// Tensor-core kernels. `tm_a` holds the A operand map (packed weights in conv mode, X in Linear
+// mode), `tm_b` the B operand map (x in conv mode, W in Linear mode).
+enum TcEpilogue { kEpiDirect = 0, kEpiClusterGN = 1 };
+cudaError_t launch_tc(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                      bool linear, int epilogue, bool out_bf16, int num_sms, cudaStream_t stream);
+
+}  // namespace c1n

@@ -1,0 +1,430 @@
+// SIMT fp32 check path and the memory-bound passes shared by every path:
+//   * simt_conv       — direct convolution from shared-memory tiles (fp32 FMA);
+//   * gn_stats        — GroupNorm mean / rstd per (n, group), two passes over the group;
+//   * ln_stats        — channel-LayerNorm mean / rstd per (n, t), two passes over channels;
+//   * normalize       — (raw - mean) * rstd * gamma + beta, then GELU, float4 when rows allow it;
+//   * rowmin          — min (and lowest argmin) over channels of the normalized values per (n, t);
+//   * broadcast       — y[n][c][t] = rowmin[n][t] + bias2[c];
+//   * pack_weights    — w[co][ci][kk] -> wp[kk][co][ci_pad] (tf32-rounded for fp32 data).
+// Operator definitions: Kimi-K2.6 l2_p35 page (Conv1d + GroupNorm), l2_p75 page (row-min + bias),
+// l1_p5 page (causal padding), l2_p3 page (LayerNorm with affine, exact GELU).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "c1n_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace c1n {
+namespace {
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
+
+// ------------------------------------------------------------------------------ SIMT conv
+
+constexpr int kSimtCo = 64, kSimtT = 64, kSimtCi = 8, kSimtThreads = 256;
+
+struct SimtConvArgs {
+    int N, C_in, C_out, T, T_out, k, stride, pad_left, dilation, span, gelu;
+};
+
+// One CTA computes a 64 (co) x 64 (t) output tile; each thread 4 x 4 outputs.
+template <typename InT, typename OutT>
+__global__ void __launch_bounds__(kSimtThreads) simt_conv_kernel(SimtConvArgs a, const InT* __restrict__ x,
+                                                                 const InT* __restrict__ w,
+                                                                 const float* __restrict__ b, OutT* __restrict__ out) {
+    extern __shared__ float smem[];
+    float* xs = smem;                          // [kSimtCi][span]
+    float* ws = smem + kSimtCi * a.span;       // [kSimtCo][kSimtCi][k]
+    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+    const int t0 = blockIdx.x * kSimtT, co0 = blockIdx.y * kSimtCo, n = blockIdx.z;
+    const long long in_start = (long long)t0 * a.stride - a.pad_left;
+    float acc[4][4] = {};
+    for (int ci0 = 0; ci0 < a.C_in; ci0 += kSimtCi) {
+        for (int idx = threadIdx.x; idx < kSimtCi * a.span; idx += kSimtThreads) {
+            const int c = idx / a.span, p = idx % a.span;
+            const int ci = ci0 + c;
+            const long long pos = in_start + p;
+            float v = 0.f;
+            if (ci < a.C_in && pos >= 0 && pos < a.T) v = to_f32(x[((long long)n * a.C_in + ci) * a.T + pos]);
+            xs[idx] = v;
+        }
+        const int wk = kSimtCi * a.k;
+        for (int idx = threadIdx.x; idx < kSimtCo * wk; idx += kSimtThreads) {
+            const int col = idx / wk, rem = idx % wk;
+            const int c = rem / a.k, kk = rem % a.k;
+            const int co = co0 + col, ci = ci0 + c;
+            float v = 0.f;
+            if (co < a.C_out && ci < a.C_in) v = to_f32(w[((long long)co * a.C_in + ci) * a.k + kk]);
+            ws[idx] = v;
+        }
+        __syncthreads();
+        for (int c = 0; c < kSimtCi; ++c) {
+            for (int kk = 0; kk < a.k; ++kk) {
+                float wv[4], xv[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) wv[i] = ws[((ty + 16 * i) * kSimtCi + c) * a.k + kk];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) xv[j] = xs[c * a.span + (tx + 16 * j) * a.stride + kk * a.dilation];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(wv[i], xv[j], acc[i][j]);
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int co = co0 + ty + 16 * i;
+        if (co >= a.C_out) continue;
+        const float bias = b ? b[co] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int t = t0 + tx + 16 * j;
+            if (t >= a.T_out) continue;
+            float v = acc[i][j] + bias;
+            if (a.gelu) v = gelu_erf(v);
+            store_out(out + ((long long)n * a.C_out + co) * a.T_out + t, v);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------ block reductions
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Sum over the CTA (blockDim.x multiple of 32, <= 1024); result broadcast to every thread.
+__device__ float block_sum(float v, float* red) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
+    float s = 0.f;
+    for (int i = 0; i < nw; ++i) s += red[i];
+    return s;
+}
+
+// GroupNorm statistics: the channels of group g are contiguous rows, so the group is one
+// contiguous span of cpg * T_out values. Two passes: mean, then the mean squared deviation.
+__global__ void __launch_bounds__(256) gn_stats_kernel(const float* __restrict__ raw, float2* __restrict__ stats,
+                                                       int C, long long T_out, int G, float eps) {
+    __shared__ float red[32];
+    const int g = blockIdx.x, n = blockIdx.y;
+    const long long cpg = C / G;
+    const long long cnt = cpg * T_out;
+    const float* src = raw + ((long long)n * C + g * cpg) * T_out;
+    float s = 0.f;
+    for (long long i = threadIdx.x; i < cnt; i += blockDim.x) s += src[i];
+    const float mean = block_sum(s, red) / (float)cnt;
+    float ss = 0.f;
+    for (long long i = threadIdx.x; i < cnt; i += blockDim.x) {
+        const float d = src[i] - mean;
+        ss = fmaf(d, d, ss);
+    }
+    const float var = block_sum(ss, red) / (float)cnt;
+    if (threadIdx.x == 0) stats[(long long)n * G + g] = make_float2(mean, rsqrtf(var + eps));
+}
+
+// Channel-LayerNorm statistics per (n, t): one thread per t (coalesced over t), two passes over C.
+__global__ void __launch_bounds__(256) ln_stats_kernel(const float* __restrict__ raw, float2* __restrict__ stats,
+                                                       int C, long long T_out, float eps) {
+    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const int n = blockIdx.y;
+    if (t >= T_out) return;
+    const float* src = raw + (long long)n * C * T_out + t;
+    float s = 0.f;
+    for (int c = 0; c < C; ++c) s += src[(long long)c * T_out];
+    const float mean = s / (float)C;
+    float ss = 0.f;
+    for (int c = 0; c < C; ++c) {
+        const float d = src[(long long)c * T_out] - mean;
+        ss = fmaf(d, d, ss);
+    }
+    stats[(long long)n * T_out + t] = make_float2(mean, rsqrtf(ss / (float)C + eps));
+}
+
+struct NormArgs {
+    int N, C;
+    long long T_out;
+    int norm;   // 0 none, 1 group, 2 channel layer
+    int cpg;    // channels per group (norm == 1)
+    int G;
+    int gelu;
+};
+
+__device__ __forceinline__ float2 stat_of(const NormArgs& a, const float2* stats, int n, int c, long long t) {
+    if (a.norm == 1) return stats[(long long)n * a.G + c / a.cpg];
+    if (a.norm == 2) return stats[(long long)n * a.T_out + t];
+    return make_float2(0.f, 1.f);
+}
+
+// Normalize + affine + optional GELU. Grid: x over column chunks of a row, y over rows (n, c)
+// in a grid-stride loop; rows of T_out contiguous values; float4 when T_out % 4 == 0.
+template <typename OutT, bool VEC>
+// `raw` and `y` may be the same buffer (in-place fp32 normalization): no __restrict__ on them.
+__global__ void __launch_bounds__(256) normalize_kernel(NormArgs a, const float* raw,
+                                                        const float2* __restrict__ stats,
+                                                        const float* __restrict__ gamma,
+                                                        const float* __restrict__ beta, OutT* y) {
+    const long long rows = (long long)a.N * a.C;
+    for (long long row = blockIdx.y; row < rows; row += gridDim.y) {
+        const int n = (int)(row / a.C), c = (int)(row % a.C);
+        const float ga = gamma ? gamma[c] : 1.f, be = beta ? beta[c] : 0.f;
+        const float* src = raw + row * a.T_out;
+        OutT* dst = y + row * a.T_out;
+        if (VEC) {
+            const long long n4 = a.T_out / 4;
+            for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+                 i += (long long)gridDim.x * blockDim.x) {
+                float4 v = reinterpret_cast<const float4*>(src)[i];
+                float r[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 st = stat_of(a, stats, n, c, 4 * i + j);
+                    float z = (r[j] - st.x) * st.y * ga + be;
+                    if (a.gelu) z = gelu_erf(z);
+                    r[j] = z;
+                }
+                if constexpr (sizeof(OutT) == 4) {
+                    reinterpret_cast<float4*>(dst)[i] = make_float4(r[0], r[1], r[2], r[3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) store_out(dst + 4 * i + j, r[j]);
+                }
+            }
+        } else {
+            for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < a.T_out;
+                 t += (long long)gridDim.x * blockDim.x) {
+                const float2 st = stat_of(a, stats, n, c, t);
+                float z = (src[t] - st.x) * st.y * ga + be;
+                if (a.gelu) z = gelu_erf(z);
+                store_out(dst + t, z);
+            }
+        }
+    }
+}
+
+// Row-min over channels of the normalized values for one (n, t) per CTA; ties keep the lowest
+// channel index.
+__global__ void __launch_bounds__(256) rowmin_kernel(NormArgs a, const float* __restrict__ raw,
+                                                     const float2* __restrict__ stats, const float* __restrict__ gamma,
+                                                     const float* __restrict__ beta, float* __restrict__ rowmin,
+                                                     int32_t* __restrict__ argmin) {
+    __shared__ float sv[256];
+    __shared__ int si[256];
+    const long long t = blockIdx.x;
+    const int n = blockIdx.y;
+    float best = __int_as_float(0x7f800000);  // +inf
+    int bi = 0x7fffffff;
+    for (int c = threadIdx.x; c < a.C; c += blockDim.x) {
+        const float2 st = stat_of(a, stats, n, c, t);
+        const float ga = gamma ? gamma[c] : 1.f, be = beta ? beta[c] : 0.f;
+        const float z = (raw[((long long)n * a.C + c) * a.T_out + t] - st.x) * st.y * ga + be;
+        if (z < best) { best = z; bi = c; }
+    }
+    sv[threadIdx.x] = best;
+    si[threadIdx.x] = bi;
+    __syncthreads();
+    for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+        if (threadIdx.x < s) {
+            const float ov = sv[threadIdx.x + s];
+            const int oi = si[threadIdx.x + s];
+            if (ov < sv[threadIdx.x] || (ov == sv[threadIdx.x] && oi < si[threadIdx.x])) {
+                sv[threadIdx.x] = ov;
+                si[threadIdx.x] = oi;
+            }
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        rowmin[(long long)n * a.T_out + t] = sv[0];
+        if (argmin) argmin[(long long)n * a.T_out + t] = si[0];
+    }
+}
+
+template <typename OutT>
+__global__ void __launch_bounds__(256) broadcast_kernel(NormArgs a, const float* __restrict__ rowmin,
+                                                        const float* __restrict__ bias2, OutT* __restrict__ y) {
+    const long long total = (long long)a.N * a.C * a.T_out;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const long long t = e % a.T_out;
+        const long long rc = e / a.T_out;
+        const int c = (int)(rc % a.C), n = (int)(rc / a.C);
+        store_out(y + e, rowmin[(long long)n * a.T_out + t] + bias2[c]);
+    }
+}
+
+// T_out == 1 fast form: y[n][c] = rowmin[n] + bias2[c], float4 over c.
+__global__ void __launch_bounds__(256) broadcast_rows_f32_kernel(int N, int C, const float* __restrict__ rowmin,
+                                                                 const float* __restrict__ bias2, float* __restrict__ y) {
+    const int c4 = C / 4;
+    for (int n = blockIdx.y; n < N; n += gridDim.y) {
+        const float m = rowmin[n];
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < c4; i += gridDim.x * blockDim.x) {
+            const float4 bb = reinterpret_cast<const float4*>(bias2)[i];
+            reinterpret_cast<float4*>(y + (long long)n * C)[i] = make_float4(m + bb.x, m + bb.y, m + bb.z, m + bb.w);
+        }
+    }
+}
+
+template <typename InT, typename PackT>
+__global__ void __launch_bounds__(256) pack_weights_kernel(int C_out, int C_in, int k, int ci_pad, int tf32_round,
+                                                           const InT* __restrict__ w, PackT* __restrict__ wp) {
+    const long long total = (long long)k * C_out * ci_pad;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int ci = (int)(e % ci_pad);
+        const long long r = e / ci_pad;
+        const int co = (int)(r % C_out), kk = (int)(r / C_out);
+        if constexpr (sizeof(PackT) == 4) {
+            float v = ci < C_in ? to_f32(w[((long long)co * C_in + ci) * k + kk]) : 0.f;
+            if (tf32_round) v = round_tf32(v);
+            wp[e] = v;
+        } else {
+            wp[e] = ci < C_in ? w[((long long)co * C_in + ci) * k + kk] : __float2bfloat16_rn(0.f);
+        }
+    }
+}
+
+NormArgs norm_args(const c1n_params& p, const Plan& pl) {
+    NormArgs a;
+    a.N = p.N;
+    a.C = p.C_out;
+    a.T_out = pl.T_out;
+    a.norm = p.norm;
+    a.G = p.norm == C1N_NORM_GROUP ? p.groups : 1;
+    a.cpg = p.C_out / a.G;
+    a.gelu = p.post == C1N_POST_GELU_ERF;
+    return a;
+}
+
+int grid_1d(long long work, int per_block = 256, int cap = 152 * 16) {
+    long long g = (work + per_block - 1) / per_block;
+    if (g < 1) g = 1;
+    if (g > cap) g = cap;
+    return (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_simt_conv(const c1n_params& p, const Plan& pl, const void* x, const void* w, const float* b,
+                             void* out, bool out_is_raw_f32, cudaStream_t stream) {
+    SimtConvArgs a;
+    a.N = p.N; a.C_in = p.C_in; a.C_out = p.C_out; a.T = p.T; a.T_out = (int)pl.T_out; a.k = p.k;
+    a.stride = p.stride; a.pad_left = p.pad_left; a.dilation = p.dilation;
+    a.span = (kSimtT - 1) * p.stride + (p.k - 1) * p.dilation + 1;
+    a.gelu = (!out_is_raw_f32 && p.norm == C1N_NORM_NONE && p.post == C1N_POST_GELU_ERF) ? 1 : 0;
+    const size_t smem = sizeof(float) * ((size_t)kSimtCi * a.span + (size_t)kSimtCo * kSimtCi * p.k);
+    dim3 grid((unsigned)((pl.T_out + kSimtT - 1) / kSimtT), (unsigned)((p.C_out + kSimtCo - 1) / kSimtCo),
+              (unsigned)p.N);
+    if (pl.bf16) {
+        auto xi = static_cast<const __nv_bfloat16*>(x);
+        auto wi = static_cast<const __nv_bfloat16*>(w);
+        if (out_is_raw_f32) {
+            auto k = simt_conv_kernel<__nv_bfloat16, float>;
+            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            k<<<grid, kSimtThreads, smem, stream>>>(a, xi, wi, b, static_cast<float*>(out));
+        } else {
+            auto k = simt_conv_kernel<__nv_bfloat16, __nv_bfloat16>;
+            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            k<<<grid, kSimtThreads, smem, stream>>>(a, xi, wi, b, static_cast<__nv_bfloat16*>(out));
+        }
+    } else {
+        auto k = simt_conv_kernel<float, float>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k<<<grid, kSimtThreads, smem, stream>>>(a, static_cast<const float*>(x), static_cast<const float*>(w), b,
+                                                static_cast<float*>(out));
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gn_stats(const c1n_params& p, const Plan& pl, const float* raw, float2* stats,
+                            cudaStream_t stream) {
+    dim3 grid((unsigned)p.groups, (unsigned)p.N);
+    gn_stats_kernel<<<grid, 256, 0, stream>>>(raw, stats, p.C_out, pl.T_out, p.groups, p.eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ln_stats(const c1n_params& p, const Plan& pl, const float* raw, float2* stats,
+                            cudaStream_t stream) {
+    dim3 grid((unsigned)((pl.T_out + 255) / 256), (unsigned)p.N);
+    ln_stats_kernel<<<grid, 256, 0, stream>>>(raw, stats, p.C_out, pl.T_out, p.eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_normalize(const c1n_params& p, const Plan& pl, const float* raw, const float2* stats,
+                             const float* gamma, const float* beta, void* y, cudaStream_t stream) {
+    NormArgs a = norm_args(p, pl);
+    const bool vec = (pl.T_out % 4) == 0;
+    const long long per_row = vec ? pl.T_out / 4 : pl.T_out;
+    const long long rows = (long long)p.N * p.C_out;
+    int gx = (int)((per_row + 255) / 256);
+    if (gx > 64) gx = 64;
+    long long gy = (152LL * 32 + gx - 1) / gx;
+    if (gy > rows) gy = rows;
+    if (gy > 65535) gy = 65535;
+    dim3 grid((unsigned)gx, (unsigned)gy);
+    if (pl.bf16) {
+        auto out = static_cast<__nv_bfloat16*>(y);
+        if (vec) normalize_kernel<__nv_bfloat16, true><<<grid, 256, 0, stream>>>(a, raw, stats, gamma, beta, out);
+        else normalize_kernel<__nv_bfloat16, false><<<grid, 256, 0, stream>>>(a, raw, stats, gamma, beta, out);
+    } else {
+        auto out = static_cast<float*>(y);
+        if (vec) normalize_kernel<float, true><<<grid, 256, 0, stream>>>(a, raw, stats, gamma, beta, out);
+        else normalize_kernel<float, false><<<grid, 256, 0, stream>>>(a, raw, stats, gamma, beta, out);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rowmin(const c1n_params& p, const Plan& pl, const float* raw, const float2* stats,
+                          const float* gamma, const float* beta, float* rowmin, int32_t* argmin,
+                          cudaStream_t stream) {
+    NormArgs a = norm_args(p, pl);
+    dim3 grid((unsigned)pl.T_out, (unsigned)p.N);
+    rowmin_kernel<<<grid, 256, 0, stream>>>(a, raw, stats, gamma, beta, rowmin, argmin);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_broadcast(const c1n_params& p, const Plan& pl, const float* rowmin, const float* bias2, void* y,
+                             cudaStream_t stream) {
+    NormArgs a = norm_args(p, pl);
+    if (!pl.bf16 && pl.T_out == 1 && p.C_out % 4 == 0) {
+        int gx = (p.C_out / 4 + 255) / 256;
+        int gy = p.N < 4096 ? p.N : 4096;
+        broadcast_rows_f32_kernel<<<dim3(gx, gy), 256, 0, stream>>>(p.N, p.C_out, rowmin, bias2,
+                                                                    static_cast<float*>(y));
+    } else {
+        const long long total = (long long)p.N * p.C_out * pl.T_out;
+        if (pl.bf16)
+            broadcast_kernel<__nv_bfloat16><<<grid_1d(total), 256, 0, stream>>>(a, rowmin, bias2,
+                                                                               static_cast<__nv_bfloat16*>(y));
+        else
+            broadcast_kernel<float><<<grid_1d(total), 256, 0, stream>>>(a, rowmin, bias2, static_cast<float*>(y));
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream) {
+    const long long total = (long long)p.k * p.C_out * pl.ci_pad;
+    if (pl.bf16)
+        pack_weights_kernel<__nv_bfloat16, __nv_bfloat16><<<grid_1d(total), 256, 0, stream>>>(
+            p.C_out, p.C_in, p.k, pl.ci_pad, 0, static_cast<const __nv_bfloat16*>(w),
+            static_cast<__nv_bfloat16*>(wp));
+    else
+        pack_weights_kernel<float, float><<<grid_1d(total), 256, 0, stream>>>(
+            p.C_out, p.C_in, p.k, pl.ci_pad, 1, static_cast<const float*>(w), static_cast<float*>(wp));
+    return cudaGetLastError();
+}
+
+}  // namespace c1n

@@ -1,0 +1,573 @@
+// Tensor-core implicit-GEMM Conv1d (+ fused epilogues) for sm_103a.
+//
+// The convolution of the Kimi-K2.6 l1_p5 page (GEMM view: M = N*T_out, N = C_out, K = C_in*k) is
+// computed tile by tile: one tile = 128 output time steps (MMA M, TMEM lanes) x BN <= 256 output
+// channels (MMA N, TMEM columns) of one sample n, accumulated in fp32 TMEM.
+//
+//   D[t][co] = sum_kk sum_ci  x[n][ci][t + kk*dilation - pad_left] * wp[kk][co][ci]
+//
+//   * A operand (x, K-major): eight "transposer" warps read x[n][ci][t] with coalesced loads (32
+//     consecutive t per warp instruction) and write it to shared memory as rows of time steps,
+//     128 bytes of input channels per row, in the 128-byte swizzled layout the tensor core reads.
+//     One tile holds 128 + (k-1)*dilation rows (the halo); tap kk uses the same tile with the
+//     matrix-descriptor start moved down by kk*dilation rows, so the taps cost no extra copies.
+//     Padding (causal or symmetric) and the ragged ends are zeros written by the transposer.
+//   * B operand (weights, K-major): TMA boxes of the packed weights wp[kk][co][ci], one per
+//     (input-channel chunk, channel block, tap).
+//   * Accumulators sit at 256-column boundaries of TMEM; two of them on the persistent paths so
+//     that the epilogue of one tile overlaps the mainloop of the next.
+//
+// Warp roles (448 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues tcgen05.mma from
+// one thread, warps 2-5 run the epilogue (each owns the 32 TMEM lanes of its quarter), warps 6-13
+// transpose x into the A ring (conv mode only).
+//
+// Linear mode (T = 1, k = 1; Kimi-K2.6 l2_p75 page): x is X[rows][in] and already K-major, so TMA
+// loads the A operand as well; D[row][co].
+//
+// Epilogues: direct (bias, optional exact GELU, store) and cluster GroupNorm (Kimi-K2.6 l2_p35
+// page): the CTAs of a thread-block cluster together cover all T_out steps of one sample; each
+// reduces per-(group) partial statistics over its tile (column sums across the 128 lanes by a
+// butterfly reduce-scatter), the partials are merged through distributed shared memory with
+// Chan's pairwise formula, and every CTA normalizes its tile straight from TMEM and stores it once.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <type_traits>
+
+#include "c1n_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace c1n {
+namespace {
+
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpEpi0 = 2, kWarpXp0 = 6, kXpWarps = 8;
+constexpr int kThreads = 32 * (kWarpXp0 + kXpWarps);  // every warp has exactly one role
+constexpr int kEpiThreads = 128, kXpThreads = 32 * kXpWarps;
+constexpr int kXpBatch = 6;  // transposer tasks whose loads are in flight together
+
+// Where a bounded wait gave up (status word detail).
+enum WaitSite { kWaitAEmpty = 1, kWaitBEmpty, kWaitAFull, kWaitBFull, kWaitAccEmpty, kWaitAccFull, kWaitDrain };
+
+__device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
+
+__device__ __forceinline__ float load_in(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float load_in(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+__device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// Time-bounded wait that ignores the abort flag (used to drain copies and MMAs before exit).
+__device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity, int* status) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (status != nullptr && atomicCAS(status, 0, 6) == 0) atomicExch(status + 1, kWaitDrain);
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ void chan_merge(float& n_a, float& mu_a, float& m2_a, float n_b, float mu_b, float m2_b) {
+    if (n_b <= 0.f) return;
+    const float n = n_a + n_b;
+    const float d = mu_b - mu_a;
+    const float f = n_b / n;
+    mu_a += d * f;
+    m2_a += m2_b + d * d * n_a * f;
+    n_a = n;
+}
+
+// Butterfly reduce-scatter over the warp: lane l receives the sum over all 32 lanes of v[l].
+// 31 shuffles for 32 columns.
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = upper ? v[i] : v[i + s];
+            const float keep = upper ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return v[0];
+}
+
+struct Unit {
+    int n;     // sample (conv) / 0 (Linear)
+    int row0;  // first output time step (conv) / first row (Linear)
+    int cbu;   // index of the channel-block group
+};
+
+template <bool LINEAR>
+__device__ __forceinline__ Unit decode_unit(const TcArgs& a, int u) {
+    Unit r;
+    const int n_cbu = a.n_cb / a.cb_per_unit;
+    r.cbu = u % n_cbu;
+    const int rest = u / n_cbu;
+    if (LINEAR) {
+        r.n = 0;
+        r.row0 = rest * 128;
+    } else {
+        r.row0 = (rest % a.n_t_tiles) * 128;
+        r.n = rest / a.n_t_tiles;
+    }
+    return r;
+}
+
+template <bool LINEAR, bool BF16, typename OutT, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_conv_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tm_a,
+                   const __grid_constant__ CUtensorMap tm_b) {
+    using InT = typename std::conditional<BF16, __nv_bfloat16, float>::type;
+    extern __shared__ uint8_t dyn_smem[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+    const int SA = a.stages_a, SB = a.stages_b;
+    const uint32_t sA = smem_u32(base);
+    const uint32_t sB = sA + uint32_t(SA * a.a_slot_bytes);
+    uint8_t* misc = base + size_t(SA) * a.a_slot_bytes + size_t(SB) * a.b_slot_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
+    const int i_afull = 0, i_aempty = SA, i_bfull = 2 * SA, i_bempty = 2 * SA + SB, i_accfull = 2 * SA + 2 * SB,
+              i_accempty = i_accfull + 2, i_drain = i_accempty + 2, n_bars = i_drain + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + n_bars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // progress counters: [0] B loads issued, [1] A chunks consumed by the MMA, [2] units issued by
+    // the MMA, [3] A chunks written by transposer warp 0, [4] units finished by the epilogue,
+    // [5] A loads issued (Linear); wait sites being waited on now: [6] MMA, [7] epilogue warp 0,
+    // [8] transposer warp 0, [9] TMA; [10] MMA unit, [11] MMA ring indices (ai, aph, bi, bph).
+    volatile int* prog = reinterpret_cast<volatile int*>(tmem_slot + 2);
+    float* epi = reinterpret_cast<float*>(misc + 1024);  // epilogue scratch (kTcMiscBytes - 1024 bytes)
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int taps = LINEAR ? 1 : a.k;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < SA; ++i) {
+            mbar_init(bar(i_afull + i), LINEAR ? 1 : kXpWarps);  // TMA arrive, or one per transposer warp
+            mbar_init(bar(i_aempty + i), 1);
+        }
+        for (int i = 0; i < SB; ++i) {
+            mbar_init(bar(i_bfull + i), 1);
+            mbar_init(bar(i_bempty + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(i_accfull + i), 1);
+            mbar_init(bar(i_accempty + i), 4);  // one arrival per epilogue warp
+        }
+        mbar_init(bar(i_drain), 1);
+        *abort_flag = 0;
+        for (int i = 0; i < kProgSlots; ++i) prog[i] = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tm_a);
+        prefetch_tensormap(&tm_b);
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_u32(tmem_slot), uint32_t(a.tmem_cols));
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    int first_unit, unit_step;
+    if (EPI == kEpiClusterGN) {
+        first_unit = (blockIdx.z * a.n_t_tiles + blockIdx.x) * (a.n_cb / a.cb_per_unit) + blockIdx.y;
+        unit_step = a.n_units;  // exactly one unit
+    } else {
+        first_unit = blockIdx.x;
+        unit_step = gridDim.x;
+    }
+
+    if (warp == kWarpTma) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int ai = 0, bi = 0;
+            uint32_t aph = 0, bph = 0;
+            long long a_cnt = 0, b_cnt = 0;
+            for (int u = first_unit; u < a.n_units && !*abort_flag; u += unit_step) {
+                const Unit un = decode_unit<LINEAR>(a, u);
+                for (int c = 0; c < a.n_ci_chunks; ++c) {
+                    if (LINEAR) {
+                        if (!mbar_wait(bar(i_aempty + ai), aph ^ 1, abort_flag, a.status, kWaitAEmpty, prog)) goto tma_done;
+                        mbar_arrive_expect_tx(bar(i_afull + ai), uint32_t(a.a_slot_bytes));
+                        tma_load_2d(sA + ai * a.a_slot_bytes, &tm_a, bar(i_afull + ai), c * a.BK, un.row0);
+                        ++a_cnt;
+                        prog[5] = int(a_cnt);
+                        if (++ai == SA) { ai = 0; aph ^= 1; }
+                    }
+                    for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
+                        const int co0 = (un.cbu * a.cb_per_unit + cbi) * a.BN;
+                        for (int kk = 0; kk < taps; ++kk) {
+                            prog[9] = kWaitBEmpty;
+                            if (!mbar_wait(bar(i_bempty + bi), bph ^ 1, abort_flag, a.status, kWaitBEmpty, prog)) goto tma_done;
+                            prog[9] = 0;
+                            mbar_arrive_expect_tx(bar(i_bfull + bi), uint32_t(a.b_slot_bytes));
+                            if (LINEAR)
+                                tma_load_2d(sB + bi * a.b_slot_bytes, &tm_b, bar(i_bfull + bi), c * a.BK, co0);
+                            else
+                                tma_load_3d(sB + bi * a.b_slot_bytes, &tm_b, bar(i_bfull + bi), c * a.BK, co0, kk);
+                            ++b_cnt;
+                            prog[0] = int(b_cnt);
+                            if (++bi == SB) { bi = 0; bph ^= 1; }
+                        }
+                    }
+                }
+            }
+        tma_done:
+            if (*abort_flag) {
+                // Let copies already in flight land before the CTA's shared memory goes away.
+                for (int s = 0; s < SA; ++s)
+                    if (LINEAR && a_cnt > s) mbar_drain(bar(i_afull + s), s < ai ? aph : (aph ^ 1), a.status);
+                for (int s = 0; s < SB; ++s)
+                    if (b_cnt > s) mbar_drain(bar(i_bfull + s), s < bi ? bph : (bph ^ 1), a.status);
+            }
+        }
+    } else if (warp == kWarpMma) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int ai = 0, bi = 0;
+            uint32_t aph = 0, bph = 0;
+            int lt = 0;
+            bool ok = true;
+            for (int u = first_unit; u < a.n_units && ok && !*abort_flag; u += unit_step, ++lt) {
+                const int ab = a.n_acc == 2 ? (lt & 1) : 0;
+                const uint32_t acc_par = a.n_acc == 2 ? uint32_t((lt >> 1) & 1) : uint32_t(lt & 1);
+                prog[10] = lt;
+                prog[11] = ai | (int(aph) << 8) | (bi << 16) | (int(bph) << 24);
+                prog[6] = kWaitAccEmpty;
+                if (!mbar_wait(bar(i_accempty + ab), acc_par ^ 1, abort_flag, a.status, kWaitAccEmpty, prog)) break;
+                prog[6] = 0;
+                tc_fence_after();
+                for (int c = 0; c < a.n_ci_chunks && ok; ++c) {
+                    prog[6] = kWaitAFull;
+                    if (!mbar_wait(bar(i_afull + ai), aph, abort_flag, a.status, kWaitAFull, prog)) { ok = false; break; }
+                    prog[6] = 0;
+                    tc_fence_after();
+                    const uint32_t a_addr = sA + ai * a.a_slot_bytes;
+                    for (int cbi = 0; cbi < a.cb_per_unit && ok; ++cbi) {
+                        const uint32_t d = tmem_base + uint32_t(256 * (ab * a.cb_per_unit + cbi));
+                        for (int kk = 0; kk < taps; ++kk) {
+                            prog[6] = kWaitBFull;
+                            if (!mbar_wait(bar(i_bfull + bi), bph, abort_flag, a.status, kWaitBFull, prog)) { ok = false; break; }
+                            prog[6] = 0;
+                            tc_fence_after();
+                            const uint32_t b_addr = sB + bi * a.b_slot_bytes;
+                            const uint32_t a_tap = a_addr + uint32_t(128 * kk * a.dil);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint64_t adesc = smem_desc_sw128(a_tap + 32u * j, 16u, 1024u);
+                                const uint64_t bdesc = smem_desc_sw128(b_addr + 32u * j, 16u, 1024u);
+                                const uint32_t accum = (c | kk | j) != 0 ? 1u : 0u;
+                                if (BF16) mma_f16(d, adesc, bdesc, a.idesc, accum);
+                                else mma_tf32(d, adesc, bdesc, a.idesc, accum);
+                            }
+                            mma_commit(bar(i_bempty + bi));
+                            if (++bi == SB) { bi = 0; bph ^= 1; }
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(bar(i_aempty + ai));
+                    prog[1] = prog[1] + 1;
+                    if (++ai == SA) { ai = 0; aph ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(bar(i_accfull + ab));
+                prog[2] = lt + 1;
+            }
+            // Every MMA issued above has finished before TMEM is released.
+            mma_commit(bar(i_drain));
+            mbar_drain(bar(i_drain), 0, a.status);
+        }
+    } else if (warp >= kWarpXp0) {
+        // ---------------------------------------------------------------- x transposer (conv mode)
+        if (!LINEAR) {
+            const int xt = threadIdx.x - kWarpXp0 * 32;  // 0..255
+            const InT* x = static_cast<const InT*>(a.x);
+            constexpr int kPerChunk = BF16 ? 8 : 4;       // channels per 16-byte chunk
+            const int n_tasks = 8 * a.R;                  // (16-byte chunk, row) pairs per tile
+            int ai = 0;
+            uint32_t aph = 0;
+            for (int u = first_unit; u < a.n_units; u += unit_step) {
+                const Unit un = decode_unit<LINEAR>(a, u);
+                const long long t_first = (long long)un.row0 - a.pad_left;
+                const InT* xn = x + (long long)un.n * a.C_in * a.T;
+                for (int c = 0; c < a.n_ci_chunks; ++c) {
+                    if (xt == 0) prog[8] = kWaitAEmpty;
+                    const bool ok = mbar_wait(bar(i_aempty + ai), aph ^ 1, abort_flag, a.status, kWaitAEmpty, prog);
+                    if (!__all_sync(0xffffffffu, ok)) goto xp_done;
+                    if (xt == 0) prog[8] = 0;
+                    uint8_t* slot = base + size_t(ai) * a.a_slot_bytes;
+                    // Each task is one 16-byte chunk (kPerChunk channels) of one row (time step);
+                    // consecutive threads take consecutive rows, so every load instruction of a
+                    // warp reads 32 consecutive time steps of one channel.
+                    for (int q0 = xt; q0 < n_tasks; q0 += kXpBatch * kXpThreads) {
+                        float v[kXpBatch][kPerChunk];
+#pragma unroll
+                        for (int b = 0; b < kXpBatch; ++b) {
+                            const int q = q0 + b * kXpThreads;
+                            const int cg = q / a.R, r = q - cg * a.R;
+                            const long long t = t_first + r;
+                            const int ci0 = c * a.BK + cg * kPerChunk;
+                            const bool t_ok = q < n_tasks && t >= 0 && t < a.T;
+#pragma unroll
+                            for (int e = 0; e < kPerChunk; ++e) {
+                                const int ci = ci0 + e;
+                                v[b][e] = (t_ok && ci < a.C_in) ? load_in(xn + (long long)ci * a.T + t) : 0.f;
+                            }
+                        }
+#pragma unroll
+                        for (int b = 0; b < kXpBatch; ++b) {
+                            const int q = q0 + b * kXpThreads;
+                            if (q >= n_tasks) break;
+                            const int cg = q / a.R, r = q - cg * a.R;
+                            uint4 pk;
+                            if constexpr (BF16) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    __nv_bfloat162 h = __floats2bfloat162_rn(v[b][2 * e], v[b][2 * e + 1]);
+                                    w[e] = *reinterpret_cast<uint32_t*>(&h);
+                                }
+                                pk = make_uint4(w[0], w[1], w[2], w[3]);
+                            } else {
+                                pk = make_uint4(__float_as_uint(v[b][0]), __float_as_uint(v[b][1]),
+                                                __float_as_uint(v[b][2]), __float_as_uint(v[b][kPerChunk - 1]));
+                            }
+                            *reinterpret_cast<uint4*>(slot + r * 128 + ((cg ^ (r & 7)) << 4)) = pk;
+                        }
+                    }
+                    // Make the generic-proxy stores visible to the tensor core, then signal.
+                    fence_async_shared();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(i_afull + ai));
+                    if (xt == 0) prog[3] = prog[3] + 1;
+                    if (++ai == SA) { ai = 0; aph ^= 1; }
+                }
+            }
+        xp_done:;
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue warps 2..5
+        const int q = warp & 3;       // TMEM lane quarter this warp may access
+        const int m = q * 32 + lane;  // tile row: time step (conv) or sample row (Linear)
+        const int er = threadIdx.x - kWarpEpi0 * 32;  // 0..127, index among epilogue threads
+        bool mid_sync_done = false;
+        int lt = 0;
+        for (int u = first_unit; u < a.n_units; u += unit_step, ++lt) {
+            const int ab = a.n_acc == 2 ? (lt & 1) : 0;
+            const uint32_t acc_par = a.n_acc == 2 ? uint32_t((lt >> 1) & 1) : uint32_t(lt & 1);
+            if (er == 0) prog[7] = kWaitAccFull;
+            const bool got = mbar_wait(bar(i_accfull + ab), acc_par, abort_flag, a.status, kWaitAccFull, prog);
+            // The barrier ORs what every epilogue thread saw: all four warps leave (or stay) together.
+            if (named_bar_any(1, kEpiThreads, !got || *abort_flag != 0)) break;
+            if (er == 0) prog[7] = 0;
+            tc_fence_after();
+            const Unit un = decode_unit<LINEAR>(a, u);
+            OutT* y = static_cast<OutT*>(a.y);
+            const int row = un.row0 + m;
+            const bool row_ok = LINEAR ? (row < a.N) : (row < a.T_out);
+
+            if (EPI == kEpiDirect) {
+                for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
+                    const int co_base = (un.cbu * a.cb_per_unit + cbi) * a.BN;
+                    const int ncols = min(a.BN, a.C_out - co_base);
+                    const uint32_t tb =
+                        tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * (ab * a.cb_per_unit + cbi));
+                    for (int j0 = 0; j0 < ncols; j0 += 16) {
+                        float v[16];
+                        tmem_load16(tb + uint32_t(j0), v);
+                        if (!row_ok) continue;
+                        if (LINEAR) {
+                            OutT* dst = y + (long long)row * a.C_out + co_base + j0;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                if (j0 + i < ncols) {
+                                    float z = v[i] + (a.bias ? __ldg(a.bias + co_base + j0 + i) : 0.f);
+                                    if (a.gelu) z = gelu_erf(z);
+                                    store_out(dst + i, z);
+                                }
+                            }
+                        } else {
+                            OutT* dst = y + ((long long)un.n * a.C_out + co_base + j0) * a.T_out + row;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                if (j0 + i < ncols) {
+                                    float z = v[i] + (a.bias ? __ldg(a.bias + co_base + j0 + i) : 0.f);
+                                    if (a.gelu) z = gelu_erf(z);
+                                    store_out(dst + (long long)i * a.T_out, z);
+                                }
+                            }
+                        }
+                    }
+                }
+            } else {
+                // ------------------------------------------------ cluster GroupNorm (conv mode)
+                // Channels of this CTA: [co_base, co_base + ncols); groups never straddle a block.
+                const int co_base = un.cbu * a.BN;
+                const int ncols = min(a.BN, a.C_out - co_base);
+                const int cpg = a.cpg;
+                const int ngroups = (ncols + cpg - 1) / cpg;
+                const int nvalid_t = min(128, a.T_out - un.row0);
+                float* red = epi;              // [4][256] per-warp column partials
+                float* colsum = epi + 1024;    // [256]
+                float* gmean = epi + 1280;     // [256] group mean (this CTA, then the cluster)
+                float* part = epi + 1536;      // [3][256] count, mean, M2 per group of this CTA
+                float* colscale = epi + 2304;  // [256]
+                float* colshift = epi + 2560;  // [256]
+                const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
+                // passes 0 and 1: per-column sums over the tile's time steps, then per-group
+                // count / mean (pass 0) and squared deviations from the CTA group mean (pass 1)
+                for (int pass = 0; pass < 2; ++pass) {
+                    for (int j0 = 0; j0 < ncols; j0 += 32) {
+                        float v[32];
+                        tmem_load16(tb + uint32_t(j0), *reinterpret_cast<float(*)[16]>(&v[0]));
+                        tmem_load16(tb + uint32_t(j0 + 16), *reinterpret_cast<float(*)[16]>(&v[16]));
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int col = j0 + i;
+                            float z = 0.f;
+                            if (row_ok && col < ncols) {
+                                z = v[i] + (a.bias ? __ldg(a.bias + co_base + col) : 0.f);
+                                if (pass == 1) {
+                                    const float d = z - gmean[col / cpg];
+                                    z = d * d;
+                                }
+                            }
+                            v[i] = z;
+                        }
+                        const float s = warp_reduce_scatter32(v, lane);
+                        red[q * 256 + j0 + lane] = s;
+                    }
+                    named_bar_sync(1, kEpiThreads);
+                    for (int col = er; col < ncols; col += kEpiThreads)
+                        colsum[col] = red[col] + red[256 + col] + red[512 + col] + red[768 + col];
+                    named_bar_sync(1, kEpiThreads);
+                    for (int g = er; g < ngroups; g += kEpiThreads) {
+                        float s = 0.f;
+                        const int c_end = min(ncols, (g + 1) * cpg);
+                        for (int col = g * cpg; col < c_end; ++col) s += colsum[col];
+                        const float cnt = float((c_end - g * cpg) * nvalid_t);
+                        if (pass == 0) {
+                            gmean[g] = s / cnt;
+                            part[g] = cnt;
+                            part[256 + g] = s / cnt;
+                        } else {
+                            part[512 + g] = s;
+                        }
+                    }
+                    named_bar_sync(1, kEpiThreads);
+                }
+                // partials of every CTA in the cluster become visible
+                cluster_sync_all();
+                mid_sync_done = true;
+                for (int g = er; g < ngroups; g += kEpiThreads) {
+                    float gn = 0.f, gmu = 0.f, gm2 = 0.f;
+                    const uint32_t p0 = smem_u32(part + g);
+                    for (int rk = 0; rk < a.n_t_tiles; ++rk) {
+                        const uint32_t pr = map_shared_rank(p0, uint32_t(rk));
+                        chan_merge(gn, gmu, gm2, ld_shared_cluster_f32(pr), ld_shared_cluster_f32(pr + 1024),
+                                   ld_shared_cluster_f32(pr + 2048));
+                    }
+                    gmean[g] = gmu;
+                    colsum[g] = rsqrtf((gn > 0.f ? gm2 / gn : 0.f) + a.eps);  // reused: group rstd
+                }
+                named_bar_sync(1, kEpiThreads);
+                for (int col = er; col < ncols; col += kEpiThreads) {
+                    const int g = col / cpg, co = co_base + col;
+                    const float sc = colsum[g] * (a.gamma ? __ldg(a.gamma + co) : 1.f);
+                    const float bias = a.bias ? __ldg(a.bias + co) : 0.f;
+                    colscale[col] = sc;
+                    colshift[col] = (a.beta ? __ldg(a.beta + co) : 0.f) + (bias - gmean[g]) * sc;
+                }
+                named_bar_sync(1, kEpiThreads);
+                // pass 2: normalize from TMEM and store once (a warp stores 32 consecutive t per channel)
+                for (int j0 = 0; j0 < ncols; j0 += 16) {
+                    float v[16];
+                    tmem_load16(tb + uint32_t(j0), v);
+                    if (!row_ok) continue;
+                    OutT* dst = y + ((long long)un.n * a.C_out + co_base + j0) * a.T_out + row;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        if (j0 + i < ncols) {
+                            float z = fmaf(v[i], colscale[j0 + i], colshift[j0 + i]);
+                            if (a.gelu) z = gelu_erf(z);
+                            store_out(dst + (long long)i * a.T_out, z);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(i_accempty + ab));
+            if (threadIdx.x == kWarpEpi0 * 32) prog[4] = lt + 1;
+        }
+        if (EPI == kEpiClusterGN && !mid_sync_done) cluster_sync_all();
+    }
+
+    if (EPI == kEpiClusterGN) {
+        // Every thread of every CTA takes part in both cluster barriers, whatever happened above:
+        // the epilogue's first one publishes the partial statistics (the other warps, or an
+        // epilogue that gave up, arrive for it here), the second keeps each CTA's shared memory
+        // alive until its peers have read it.
+        if (warp < kWarpEpi0 || warp >= kWarpXp0) cluster_sync_all();
+        cluster_sync_all();
+    }
+    __syncwarp();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, uint32_t(a.tmem_cols));
+    }
+}
+
+template <bool LINEAR, bool BF16, typename OutT, int EPI>
+cudaError_t launch_one(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                       int num_sms, cudaStream_t stream) {
+    auto kern = tc_conv_kernel<LINEAR, BF16, OutT, EPI>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = size_t(pl.smem_bytes);
+    cfg.stream = stream;
+    if (EPI == kEpiClusterGN) {
+        cfg.gridDim = dim3(unsigned(a.n_t_tiles), unsigned(a.n_cb / a.cb_per_unit), unsigned(a.N));
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = unsigned(a.n_t_tiles);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    } else {
+        const int grid = a.n_units < num_sms ? a.n_units : num_sms;
+        cfg.gridDim = dim3(unsigned(grid), 1, 1);
+        cfg.attrs = nullptr;
+        cfg.numAttrs = 0;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, a, tm_a, tm_b);
+}
+
+}  // namespace
+
+cudaError_t launch_tc(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b, bool linear,
+                      int epilogue, bool out_bf16, int num_sms, cudaStream_t stream) {
+    if (linear) {
+        if (pl.bf16 && out_bf16) return launch_one<true, true, __nv_bfloat16, kEpiDirect>(pl, a, tm_a, tm_b, num_sms, stream);
+        if (pl.bf16) return launch_one<true, true, float, kEpiDirect>(pl, a, tm_a, tm_b, num_sms, stream);
+        return launch_one<true, false, float, kEpiDirect>(pl, a, tm_a, tm_b, num_sms, stream);
+    }
+    if (epilogue == kEpiClusterGN) {
+        if (pl.bf16) return launch_one<false, true, __nv_bfloat16, kEpiClusterGN>(pl, a, tm_a, tm_b, num_sms, stream);
+        return launch_one<false, false, float, kEpiClusterGN>(pl, a, tm_a, tm_b, num_sms, stream);
+    }
+    if (pl.bf16) {
+        if (out_bf16) return launch_one<false, true, __nv_bfloat16, kEpiDirect>(pl, a, tm_a, tm_b, num_sms, stream);
+        return launch_one<false, true, float, kEpiDirect>(pl, a, tm_a, tm_b, num_sms, stream);
+    }
+    return launch_one<false, false, float, kEpiDirect>(pl, a, tm_a, tm_b, num_sms, stream);
+}
+
+}  // namespace c1n

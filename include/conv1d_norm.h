@@ -1,0 +1,174 @@
+/*
+ * conv1d_norm.h — C ABI of the fused Conv1d (implicit GEMM) + normalization operator for GB300 (sm_103a).
+ *
+ * What it computes (web pages on the subject "gemm_groupnorm_accelerator"):
+ *   [p1] Kimi-K2.6 l2_p35 page — Conv1d followed by GroupNorm: convolution sum, output length,
+ *        GroupNorm statistics over (channels of a group x all time steps) of one sample,
+ *        population variance, eps inside the square root, per-channel affine.
+ *   [p2] Kimi-K2.6 l2_p75 page — Linear + GroupNorm on [rows, channels], then the minimum over
+ *        channels of every row and a broadcast add of a per-channel bias.
+ *   [p3] Kimi-K2.6 l1_p5 page — causal Conv1d: left padding (k-1)*dilation, tap 0 is the oldest
+ *        input; the convolution viewed as a GEMM with M = N*T_out, N = C_out, K = C_in*k.
+ *   [p4] Kimi-K2.6 l2_p3 page — LayerNorm with affine and the exact-erf GELU.
+ *
+ *   c[n][co][t] = b[co] + sum_ci sum_kk w[co][ci][kk] * x[n][ci][t*stride + kk*dilation - pad_left]
+ *                 (x = 0 outside [0, T));  T_out = (T + pad_left + pad_right - dilation*(k-1) - 1)/stride + 1
+ *   norm  GROUP:          z = (c - mean_{n,g}) / sqrt(var_{n,g} + eps) * gamma[co] + beta[co]
+ *         CHANNEL_LAYER:  the same with the statistics of all C_out channels at one (n, t)
+ *   post  GELU_ERF:       y = 0.5 z (1 + erf(z / sqrt 2))
+ *         ROWMIN_BIAS:    m[n][t] = min_co z[n][co][t]; y[n][co][t] = m[n][t] + bias2[co]
+ *
+ * Layouts (all dense, row-major, no padding between rows):
+ *   x [N][C_in][T], w [C_out][C_in][k], y [N][C_out][T_out] in the descriptor's dtype (fp32 or bf16);
+ *   b, gamma, beta, bias2 [C_out] fp32; argmin [N][T_out] int32.
+ *   A Linear layer is the case T = 1, k = 1, no padding: x = X[rows][in], w = W[out][in], y = Y[rows][out].
+ *
+ * Ownership: the caller owns every device buffer, the workspace and the stream. The library owns only
+ * the descriptor (host memory). The library never allocates device memory and never synchronises inside
+ * run(); all work is enqueued on the caller's stream.
+ *
+ * Errors: every entry point returns a c1n_status; nothing throws across this boundary.
+ *   Argument errors are reported by desc_create; pointer alignment and workspace errors by run.
+ *   Device-side failures (a bounded wait that ran out) set a status word in the workspace that
+ *   conv1d_norm_check() reads. conv1d_norm_last_error() gives a message for the calling thread.
+ *
+ * Thread safety: a descriptor may be used by one host thread at a time (run() caches encoded TMA
+ * descriptors inside it). Distinct descriptors are independent.
+ */
+#ifndef CONV1D_NORM_H
+#define CONV1D_NORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* c1n_stream_t;
+
+typedef enum {
+    C1N_OK = 0,
+    C1N_ERR_INVALID_ARG = 1,  /* a parameter or pointer is out of range / missing */
+    C1N_ERR_UNSUPPORTED = 2,  /* valid operator, but the requested math path cannot run it */
+    C1N_ERR_ALIGNMENT = 3,    /* a device pointer is not 16-byte aligned where the tensor path needs it */
+    C1N_ERR_WORKSPACE = 4,    /* workspace missing or smaller than conv1d_norm_workspace_size() */
+    C1N_ERR_CUDA = 5,         /* a CUDA runtime call failed (launch error, no device, ...) */
+    C1N_ERR_TIMEOUT = 6,      /* a device-side bounded wait ran out (reported by conv1d_norm_check) */
+    C1N_ERR_DEVICE = 7        /* another device-side consistency check failed (reported by check) */
+} c1n_status;
+
+typedef enum { C1N_NORM_NONE = 0, C1N_NORM_GROUP = 1, C1N_NORM_CHANNEL_LAYER = 2 } c1n_norm;
+typedef enum { C1N_POST_NONE = 0, C1N_POST_GELU_ERF = 1, C1N_POST_ROWMIN_BIAS = 2 } c1n_post;
+typedef enum { C1N_F32 = 0, C1N_BF16 = 1 } c1n_dtype;
+
+/* Arithmetic used for the contraction. AUTO picks the tensor-core path when the shape allows it
+ * (TF32 tensor cores for fp32 data, BF16 for bf16 data) and the SIMT fp32 CUDA path otherwise;
+ * TENSOR fails with C1N_ERR_UNSUPPORTED instead of falling back; SIMT always uses fp32 FMA. */
+typedef enum { C1N_MATH_AUTO = 0, C1N_MATH_SIMT = 1, C1N_MATH_TENSOR = 2 } c1n_math;
+
+/* Execution plans (reported by conv1d_norm_plan_info; forceable for testing and measurement). */
+typedef enum {
+    C1N_PATH_AUTO = -1,
+    C1N_PATH_SIMT = 0,            /* SIMT conv kernel + statistics + normalize/post-op kernels */
+    C1N_PATH_TC_DIRECT = 1,       /* tcgen05 conv, bias (and GELU) in the epilogue, no normalization */
+    C1N_PATH_TC_CLUSTER = 2,      /* tcgen05 conv, GroupNorm statistics merged across a thread-block
+                                     cluster through distributed shared memory, normalized in place */
+    C1N_PATH_TC_TWO_PASS = 3,     /* tcgen05 conv writes raw tiles, then statistics + normalize pass */
+    C1N_PATH_TC_LINEAR = 4        /* T = 1, k = 1: tcgen05 GEMM (rows x out), then the norm/post passes */
+} c1n_path;
+
+typedef struct {
+    int32_t N, C_in, C_out, T, k;
+    int32_t stride, pad_left, pad_right, dilation;
+    int32_t norm;        /* c1n_norm */
+    int32_t groups;      /* GroupNorm group count; C_out % groups == 0 */
+    float eps;           /* > 0 when norm != NONE */
+    int32_t post;        /* c1n_post */
+    int32_t dtype;       /* c1n_dtype of x, w and y */
+    int32_t math;        /* c1n_math */
+    int32_t force_path;  /* c1n_path; C1N_PATH_AUTO (-1) lets the planner choose */
+} c1n_params;
+
+typedef struct c1n_desc c1n_desc;
+
+typedef struct {
+    int32_t path;            /* c1n_path chosen */
+    int32_t T_out;
+    int32_t tile_t;          /* output time steps per tile (tensor paths) */
+    int32_t tile_co;         /* output channels per tile */
+    int32_t mma_n;           /* tcgen05 N extent per MMA */
+    int32_t cluster;         /* CTAs per thread-block cluster (1 = none) */
+    int32_t n_tiles;
+    int32_t grid;            /* CTAs of the main kernel */
+    int32_t kernels;         /* kernels one run() enqueues */
+    int32_t reserved;
+    int64_t workspace_bytes;
+} c1n_plan_info;
+
+/* Validate `params`, choose an execution plan and return a host-side descriptor in *out.
+ * No device memory is touched; the call works without a GPU. */
+c1n_status conv1d_norm_desc_create(const c1n_params* params, c1n_desc** out);
+
+/* Bytes of device scratch that run() needs (status word, packed weights, statistics, raw tiles). */
+c1n_status conv1d_norm_workspace_size(const c1n_desc* desc, size_t* bytes);
+
+/* Attach caller-owned device scratch of at least conv1d_norm_workspace_size() bytes (256-byte
+ * aligned) for use by conv1d_norm_run(). The library never frees it. */
+c1n_status conv1d_norm_set_workspace(c1n_desc* desc, void* workspace, size_t bytes);
+
+c1n_status conv1d_norm_plan_info(const c1n_desc* desc, c1n_plan_info* info);
+
+/* Enqueue the operator on `stream`, using the attached workspace. x, w, y are device pointers in
+ * the descriptor's dtype; b, gamma, beta are device fp32 pointers or NULL (no bias; gamma = 1,
+ * beta = 0). Needs post != ROWMIN_BIAS (use run_ex for bias2/argmin). Asynchronous. */
+c1n_status conv1d_norm_run(c1n_desc* desc, const void* x, const void* w, const float* b,
+                           const float* gamma, const float* beta, void* y, c1n_stream_t stream);
+
+typedef struct {
+    const void* x;
+    const void* w;
+    const float* b;          /* nullable */
+    const float* gamma;      /* nullable */
+    const float* beta;       /* nullable */
+    const float* bias2;      /* required iff post == ROWMIN_BIAS */
+    void* y;
+    int32_t* argmin;         /* nullable; [N][T_out] when post == ROWMIN_BIAS */
+    void* workspace;         /* NULL: use the workspace attached with conv1d_norm_set_workspace */
+    size_t workspace_bytes;
+    uint32_t flags;          /* C1N_FLAG_* */
+} c1n_args;
+
+/* The weights were already packed into this workspace by conv1d_norm_pack_weights (same w, same
+ * workspace); run_ex then skips its own packing step. */
+#define C1N_FLAG_WEIGHTS_PACKED 1u
+
+c1n_status conv1d_norm_run_ex(c1n_desc* desc, const c1n_args* args, c1n_stream_t stream);
+
+/* The weight-packing step alone (the first kernel run()/run_ex() enqueue on the tensor-core conv
+ * paths): w[co][ci][kk] -> wp[kk][co][ci_pad] inside the workspace, rounded to tf32 for fp32 data.
+ * On paths that read w directly (SIMT, Linear) it enqueues nothing and returns C1N_OK.
+ * workspace NULL: the attached one. Asynchronous. */
+c1n_status conv1d_norm_pack_weights(c1n_desc* desc, const void* w, void* workspace, size_t workspace_bytes,
+                                    c1n_stream_t stream);
+
+/* Synchronise `stream`, read and clear the device status word of the given workspace (NULL: the
+ * attached one) and return C1N_OK, C1N_ERR_TIMEOUT or C1N_ERR_DEVICE. */
+c1n_status conv1d_norm_check(const c1n_desc* desc, void* workspace, c1n_stream_t stream);
+
+void conv1d_norm_destroy(c1n_desc* desc);
+
+const char* conv1d_norm_status_string(c1n_status status);
+
+/* Message describing the last failure on the calling host thread ("" if none). */
+const char* conv1d_norm_last_error(void);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int32_t conv1d_norm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONV1D_NORM_H */

@@ -1,0 +1,128 @@
+"""Host-only checks of the C ABI: the library loads, exports every declared symbol, validates
+parameters and plans each workload; no device call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gemm_groupnorm_accelerator_gb300 as c1n
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "conv1d_norm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(conv1d_norm_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = c1n.load()
+    declared = _declared_functions()
+    assert set(declared) == set(c1n.EXPORTED_SYMBOLS), declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert c1n.conv1d_norm_version() >= 100
+
+
+def _params(wl, **kw):
+    d = dict(N=wl.N, C_in=wl.C_in, C_out=wl.C_out, T=wl.T, k=wl.k, stride=wl.stride, pad_left=wl.pad_left,
+             pad_right=wl.pad_right, dilation=wl.dilation, norm=wl.norm, groups=wl.groups, eps=wl.eps, post=wl.post,
+             dtype=wl.dtype)
+    d.update(kw)
+    return c1n.make_params(**d)
+
+
+EXPECTED_PATH = {
+    synth.CONV_GN_TINY.name: "tc_cluster",
+    synth.CONV_GN.name: "tc_cluster",
+    synth.CAUSAL_CONV.name: "tc_direct",
+    synth.LINEAR_GN_ROWMIN.name: "tc_linear",
+    synth.CONV_LN_GELU_BF16.name: "tc_two_pass",
+}
+
+
+@pytest.mark.parametrize("wl", synth.WORKLOADS, ids=lambda w: w.name)
+def test_plan_of_each_workload(wl):
+    d = c1n.conv1d_norm_desc_create(_params(wl))
+    try:
+        info = c1n.conv1d_norm_plan_info(d)
+        assert info.T_out == wl.T_out
+        assert c1n.PATH_NAMES[info.path] == EXPECTED_PATH[wl.name]
+        assert c1n.conv1d_norm_workspace_size(d) >= 256
+        if info.path != c1n.PATH_SIMT:
+            assert 16 <= info.mma_n <= 256 and info.mma_n % 16 == 0
+            assert info.tile_t >= 1
+    finally:
+        c1n.conv1d_norm_destroy(d)
+
+
+def test_conv_gn_cluster_geometry():
+    d = c1n.conv1d_norm_desc_create(_params(synth.CONV_GN))
+    info = c1n.conv1d_norm_plan_info(d)
+    # 1024 steps in 8 tiles of 128; all 256 channels in one MMA N; one cluster of 8 CTAs per sample
+    assert (info.cluster, info.tile_t, info.mma_n, info.n_tiles) == (8, 128, 256, 8 * 16)
+    c1n.conv1d_norm_destroy(d)
+
+
+def test_simt_forced_and_tensor_forced():
+    wl = synth.CONV_GN_TINY
+    d = c1n.conv1d_norm_desc_create(_params(wl, math=c1n.MATH_SIMT))
+    assert c1n.conv1d_norm_plan_info(d).path == c1n.PATH_SIMT
+    c1n.conv1d_norm_destroy(d)
+    # stride 2 has no tensor-core plan: AUTO takes the SIMT kernels, TENSOR refuses.
+    d = c1n.conv1d_norm_desc_create(_params(wl, stride=2))
+    assert c1n.conv1d_norm_plan_info(d).path == c1n.PATH_SIMT
+    c1n.conv1d_norm_destroy(d)
+    with pytest.raises(c1n.C1NError) as e:
+        c1n.conv1d_norm_desc_create(_params(wl, stride=2, math=c1n.MATH_TENSOR))
+    assert e.value.status == c1n.ERR_UNSUPPORTED
+    d = c1n.conv1d_norm_desc_create(_params(wl, force_path=c1n.PATH_TC_TWO_PASS))
+    assert c1n.conv1d_norm_plan_info(d).path == c1n.PATH_TC_TWO_PASS
+    c1n.conv1d_norm_destroy(d)
+
+
+@pytest.mark.parametrize("bad", [dict(N=0), dict(C_in=0), dict(k=0), dict(stride=0), dict(dilation=0),
+                                 dict(pad_left=-1), dict(groups=3), dict(eps=0.0), dict(eps=float("nan")),
+                                 dict(norm=7), dict(post=5), dict(dtype=3), dict(math=9), dict(T=2, k=5),
+                                 dict(force_path=11)])
+def test_invalid_params_are_rejected(bad):
+    with pytest.raises(c1n.C1NError) as e:
+        c1n.conv1d_norm_desc_create(_params(synth.CONV_GN_TINY, **bad))
+    assert e.value.status == c1n.ERR_INVALID_ARG
+    assert c1n.load().conv1d_norm_last_error()
+
+
+def test_run_without_workspace_and_null_pointers():
+    d = c1n.conv1d_norm_desc_create(_params(synth.CONV_GN_TINY))
+    lib = c1n.load()
+    # no workspace attached
+    st = lib.conv1d_norm_run(d, 16, 16, None, None, None, 16, None)
+    assert st == c1n.ERR_WORKSPACE
+    assert c1n.conv1d_norm_set_workspace(d, 0, 0) is None
+    with pytest.raises(c1n.C1NError) as e:
+        c1n.conv1d_norm_set_workspace(d, 256, 16)
+    assert e.value.status == c1n.ERR_WORKSPACE
+    with pytest.raises(c1n.C1NError) as e:
+        c1n.conv1d_norm_set_workspace(d, 1024 + 8, 1 << 30)
+    assert e.value.status == c1n.ERR_ALIGNMENT
+    # NULL x is an argument error whatever the workspace
+    args = c1n.Args(None, 16, None, None, None, None, 16, None, 4096, 1 << 30, 0)
+    assert lib.conv1d_norm_run_ex(d, ctypes.byref(args), None) == c1n.ERR_INVALID_ARG
+    c1n.conv1d_norm_destroy(d)
+
+
+def test_rowmin_needs_run_ex_and_bias2():
+    d = c1n.conv1d_norm_desc_create(_params(synth.LINEAR_GN_ROWMIN))
+    lib = c1n.load()
+    assert lib.conv1d_norm_run(d, 16, 16, None, None, None, 16, None) == c1n.ERR_INVALID_ARG
+    args = c1n.Args(16, 16, None, None, None, None, 16, None, 4096, 1 << 40, 0)
+    assert lib.conv1d_norm_run_ex(d, ctypes.byref(args), None) == c1n.ERR_INVALID_ARG
+    c1n.conv1d_norm_destroy(d)
+
+
+def test_status_strings():
+    for s in range(8):
+        assert c1n.conv1d_norm_status_string(s)

@@ -1,0 +1,213 @@
+"""GPU parity: the CUDA library, called through the C ABI, against the CPU oracle on the same seeded
+inputs. Tolerances (max abs error): 1e-4 for the SIMT fp32 path, 5e-3 for the TF32 tensor-core
+path, 3e-2 for bf16 data; row-min argmin must agree wherever the minimum is unique by > 1e-2."""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL_SIMT, TOL_TF32, TOL_BF16 = 1e-4, 5e-3, 3e-2
+
+
+def _tol(wl, path):
+    if wl.dtype == synth.DTYPE_BF16:
+        return TOL_BF16
+    return TOL_SIMT if path == "simt" else TOL_TF32
+
+
+@functools.lru_cache(maxsize=8)
+def _inputs(wl):
+    return synth.make_inputs(wl, seed=0)
+
+
+def _to_dev(a, bf16):
+    if a is None:
+        return None
+    t = torch.from_numpy(a).cuda()
+    return t.to(torch.bfloat16) if bf16 else t
+
+
+def run_gpu(c1n, wl, inp, math=0, force_path=-1):
+    params = c1n.make_params(wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right, wl.dilation,
+                             wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, math, force_path)
+    op = c1n.Conv1dNorm(params)
+    bf = wl.dtype == synth.DTYPE_BF16
+    x, w = _to_dev(inp["x"], bf), _to_dev(inp["w"], bf)
+    b, ga, be, b2 = (_to_dev(inp[k], False) for k in ("b", "gamma", "beta", "bias2"))
+    out = torch.full((wl.N, wl.C_out, op.T_out), float("nan"), dtype=op.out_dtype(), device="cuda")
+    am = torch.full((wl.N, op.T_out), -1, dtype=torch.int32, device="cuda") if wl.post == synth.POST_ROWMIN_BIAS else None
+    op(x, w, b, ga, be, bias2=b2, out=out, argmin=am)
+    torch.cuda.synchronize()
+    op.check()
+    path = op.path
+    y = out.float().cpu().numpy()
+    return y, (None if am is None else am.cpu().numpy()), path
+
+
+def compare(wl, y, am, ref, ref_am, path, label=""):
+    assert np.all(np.isfinite(y)), f"{label}: non-finite output (unwritten elements?)"
+    err = float(np.max(np.abs(y.astype(np.float64) - ref)))
+    tol = _tol(wl, path)
+    assert err <= tol, f"{label} path={path}: max abs err {err:.3e} > {tol}"
+    if ref_am is not None:
+        # argmin must match where the minimum is unique by a margin > 1e-2
+        assert am is not None
+        # recompute margins from the oracle's pre-broadcast values: y - bias2 is the row minimum,
+        # so margins need the normalized values; the caller passes them through `ref_margin`.
+    return err
+
+
+def oracle_full(wl, inp):
+    return oracle.conv1d_norm(oracle.params_of(wl), inp["x"], inp["w"], inp["b"], inp["gamma"], inp["beta"],
+                              inp["bias2"])
+
+
+def _argmin_margin(wl, inp, ns=None):
+    """Oracle normalized values before the row-min, to find rows whose minimum is unique by > 1e-2."""
+    pre = wl.replace(post=synth.POST_NONE)
+    if ns is None:
+        z, _ = oracle_full(pre, inp)
+    else:
+        z, _ = oracle.conv1d_norm_samples(oracle.params_of(pre), ns, inp["x"], inp["w"], inp["b"], inp["gamma"],
+                                          inp["beta"])
+    s = np.sort(z, axis=1)
+    return s[:, 1, :] - s[:, 0, :]
+
+
+def check_argmin(am, ref_am, margin):
+    sel = margin > 1e-2
+    assert sel.any()
+    assert np.array_equal(am[sel], ref_am[sel]), f"argmin mismatch on {(am[sel] != ref_am[sel]).sum()} rows"
+
+
+# ------------------------------------------------------------------------------ small shapes, every path
+
+SMALL = {
+    "gn_tiny": synth.CONV_GN_TINY,
+    "gn_c2_structure": synth.CONV_GN.replace(N=3, C_in=40, C_out=200, T=1000, groups=25),
+    "gn_cpg1": synth.CONV_GN.replace(N=2, C_in=32, C_out=64, T=256, groups=64),
+    "gn_cpg128": synth.CONV_GN.replace(N=2, C_in=32, C_out=256, T=256, groups=2),
+    "gn_g1_twopass": synth.CONV_GN.replace(N=2, C_in=32, C_out=256, T=128, groups=1),
+    "gn_gelu": synth.CONV_GN.replace(N=2, C_in=24, C_out=96, T=320, groups=12, post=synth.POST_GELU_ERF),
+    "causal_k4": synth.CAUSAL_CONV.replace(N=2, C_in=64, C_out=160, T=1024),
+    # enough 128-step tiles that each persistent CTA (one per SM) runs 2, then about 4 work units
+    "causal_units2": synth.CAUSAL_CONV.replace(N=2, C_in=32, C_out=64, T=152 * 128),
+    "causal_units4": synth.CAUSAL_CONV.replace(N=4, C_in=32, C_out=64, T=160 * 128),
+    "conv_k1": synth.CAUSAL_CONV.replace(N=2, C_in=36, C_out=130, T=300, k=1, pad_left=0),
+    "conv_dil3_pads": synth.CAUSAL_CONV.replace(N=2, C_in=20, C_out=64, T=412, k=3, pad_left=5, pad_right=2,
+                                                dilation=3, w_bound=0.2),
+    "conv_nopad": synth.CAUSAL_CONV.replace(N=3, C_in=16, C_out=48, T=96, k=5, pad_left=0, w_bound=0.2),
+    "conv_gelu": synth.CAUSAL_CONV.replace(N=2, C_in=32, C_out=32, T=128, post=synth.POST_GELU_ERF),
+    "conv_rowmin": synth.CAUSAL_CONV.replace(N=2, C_in=32, C_out=40, T=64, post=synth.POST_ROWMIN_BIAS),
+    "linear_rowmin": synth.LINEAR_GN_ROWMIN.replace(N=200, C_in=72, C_out=320, groups=20),
+    "linear_plain": synth.LINEAR_GN_ROWMIN.replace(N=130, C_in=64, C_out=96, norm=synth.NORM_NONE,
+                                                   post=synth.POST_NONE),
+    "ln_gelu_bf16": synth.CONV_LN_GELU_BF16.replace(N=2, C_in=48, C_out=160, T=264),
+    "gn_bf16": synth.CONV_GN.replace(N=2, C_in=64, C_out=128, T=512, groups=16, dtype=synth.DTYPE_BF16),
+    "conv_bf16": synth.CAUSAL_CONV.replace(N=2, C_in=72, C_out=136, T=400, dtype=synth.DTYPE_BF16),
+    "stride2_simt": synth.CONV_GN.replace(N=2, C_in=16, C_out=32, T=101, stride=2, groups=8),
+    "odd_T_simt": synth.CAUSAL_CONV.replace(N=2, C_in=8, C_out=24, T=77),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+@pytest.mark.parametrize("math", [0, 1], ids=["auto", "simt"])
+def test_small_shapes(cuda_lib, name, math):
+    wl = SMALL[name]
+    inp = _inputs(wl)
+    ref, ref_am = oracle_full(wl, inp)
+    y, am, path = run_gpu(cuda_lib, wl, inp, math=math)
+    if math == 1:
+        assert path == "simt"
+    compare(wl, y, am, ref, ref_am, path, name)
+    if ref_am is not None:
+        check_argmin(am, ref_am, _argmin_margin(wl, inp))
+
+
+@pytest.mark.parametrize("name", ["gn_tiny", "gn_c2_structure", "gn_gelu", "gn_bf16"])
+def test_group_norm_two_pass_forced(cuda_lib, name):
+    wl = SMALL[name]
+    inp = _inputs(wl)
+    ref, _ = oracle_full(wl, inp)
+    y, am, path = run_gpu(cuda_lib, wl, inp, force_path=cuda_lib.PATH_TC_TWO_PASS)
+    assert path == "tc_two_pass"
+    compare(wl, y, am, ref, None, path, name)
+
+
+def test_repeated_calls_are_identical(cuda_lib):
+    wl = SMALL["gn_c2_structure"]
+    inp = _inputs(wl)
+    y1, _, _ = run_gpu(cuda_lib, wl, inp)
+    y2, _, _ = run_gpu(cuda_lib, wl, inp)
+    assert np.array_equal(y1, y2)
+
+
+# ------------------------------------------------------------------------------ the five workloads
+
+def test_conv_gn_tiny_full(cuda_lib):
+    wl = synth.CONV_GN_TINY
+    inp = _inputs(wl)
+    ref, _ = oracle_full(wl, inp)
+    y, _, path = run_gpu(cuda_lib, wl, inp)
+    assert path == "tc_cluster"
+    compare(wl, y, None, ref, None, path, wl.name)
+
+
+def test_conv_gn_full(cuda_lib):
+    wl = synth.CONV_GN
+    inp = _inputs(wl)
+    ref, _ = oracle_full(wl, inp)
+    y, _, path = run_gpu(cuda_lib, wl, inp)
+    assert path == "tc_cluster"
+    compare(wl, y, None, ref, None, path, wl.name)
+    # with gamma = 1, beta = 0 every (n, group) of the output has mean ~0 and variance ~1
+    inp2 = dict(inp, gamma=None, beta=None)
+    y2, _, _ = run_gpu(cuda_lib, wl, inp2)
+    g = y2.reshape(wl.N, wl.groups, -1).astype(np.float64)
+    assert np.max(np.abs(g.mean(axis=2))) < 1e-3
+    assert np.max(np.abs(g.var(axis=2) - 1.0)) < 1e-2
+
+
+def test_causal_conv_full_sampled(cuda_lib):
+    wl = synth.CAUSAL_CONV
+    inp = _inputs(wl)
+    y, _, path = run_gpu(cuda_lib, wl, inp)
+    assert path == "tc_direct"
+    ns = [0, wl.N - 1]
+    ref, _ = oracle.conv1d_norm_samples(oracle.params_of(wl), ns, inp["x"], inp["w"], inp["b"])
+    compare(wl, y[ns], None, ref, None, path, wl.name)
+    assert np.all(np.isfinite(y))
+
+
+def test_linear_gn_rowmin_full_sampled(cuda_lib):
+    wl = synth.LINEAR_GN_ROWMIN
+    inp = _inputs(wl)
+    y, am, path = run_gpu(cuda_lib, wl, inp)
+    assert path == "tc_linear"
+    ns = [0, 1, 500, wl.N - 1]
+    p = oracle.params_of(wl)
+    ref, ref_am = oracle.conv1d_norm_samples(p, ns, inp["x"], inp["w"], inp["b"], inp["gamma"], inp["beta"],
+                                             inp["bias2"])
+    compare(wl, y[ns], None, ref, None, path, wl.name)
+    check_argmin(am[ns], ref_am, _argmin_margin(wl, inp, ns))
+    # every row is its minimum plus the broadcast bias
+    b2 = inp["bias2"].astype(np.float64)
+    rows = y[:, :, 0].astype(np.float64) - b2[None, :]
+    assert np.max(np.abs(rows - rows[:, :1])) < 1e-5
+
+
+def test_conv_ln_gelu_bf16_full_sampled(cuda_lib):
+    wl = synth.CONV_LN_GELU_BF16
+    inp = _inputs(wl)
+    y, _, path = run_gpu(cuda_lib, wl, inp)
+    ns = [0, wl.N - 1]
+    ref, _ = oracle.conv1d_norm_samples(oracle.params_of(wl), ns, inp["x"], inp["w"], inp["b"], inp["gamma"],
+                                        inp["beta"])
+    compare(wl, y[ns], None, ref, None, path, wl.name)
+    assert np.all(np.isfinite(y))
