@@ -62,8 +62,9 @@ long long t_out_of(const c1n_params& p) {
 }
 
 // Why the tensor-core conv path cannot take this shape ("" when it can).
-const char* tc_conv_blocker(const c1n_params& p, const Plan&) {
+const char* tc_conv_blocker(const c1n_params& p, const Plan& pl) {
     if (p.stride != 1) return "stride > 1";
+    if (p.T % pl.align != 0) return "T is not a multiple of 16 bytes of elements (TMA row stride of x)";
     if (p.k > kMaxTaps) return "more than 16 taps";
     if (p.N > 65535) return "N above 65535";
     return "";
@@ -99,13 +100,18 @@ void plan_channel_blocks(const c1n_params& p, Plan& pl) {
 }
 
 // Ring depths from the shared-memory budget (one CTA per SM).
-void plan_stages(Plan& pl, int max_a, int max_b) {
+void plan_stages(Plan& pl, int max_a, int max_b, int max_s) {
     const int budget = 227 * 1024 - 1024 - kTcMiscBytes;
     pl.stages_a = max_a;
     pl.stages_b = max_b;
-    while (pl.stages_a * pl.a_slot_bytes + pl.stages_b * pl.b_slot_bytes > budget && pl.stages_b > 2) --pl.stages_b;
-    while (pl.stages_a * pl.a_slot_bytes + pl.stages_b * pl.b_slot_bytes > budget && pl.stages_a > 2) --pl.stages_a;
-    pl.smem_bytes = 1024 + pl.stages_a * pl.a_slot_bytes + pl.stages_b * pl.b_slot_bytes + kTcMiscBytes;
+    pl.stages_s = pl.s_slot_bytes > 0 ? max_s : 0;
+    auto total = [&]() {
+        return pl.stages_a * pl.a_slot_bytes + pl.stages_b * pl.b_slot_bytes + pl.stages_s * pl.s_slot_bytes;
+    };
+    while (total() > budget && pl.stages_b > 2) --pl.stages_b;
+    while (total() > budget && pl.stages_s > 2) --pl.stages_s;
+    while (total() > budget && pl.stages_a > 2) --pl.stages_a;
+    pl.smem_bytes = 1024 + total() + kTcMiscBytes;
 }
 
 // Geometry of the tensor-core conv tiles: 128 output time steps x BN channels per tile; the A tile
@@ -114,9 +120,15 @@ void plan_stages(Plan& pl, int max_a, int max_b) {
 bool plan_tc_geometry(const c1n_params& p, Plan& pl, bool cluster) {
     pl.BK = pl.bf16 ? 64 : 32;
     const long long halo = (long long)(p.k - 1) * p.dilation;
-    if (halo > 256) return false;
     pl.R = (int)round_up(128 + halo, 8);
+    // x is staged by TMA from a 16-byte aligned time coordinate: pad_left rounded up to the
+    // alignment, so A row r is staged index r + t_shift.
+    const long long pl_al = (long long)round_up(p.pad_left, pl.align);
+    pl.t_shift = (int)(pl_al - p.pad_left);
+    pl.RS = (int)round_up(pl.R + pl.t_shift, pl.align);
+    if (pl.RS > 256) return false;  // one TMA box per (chunk, tile)
     pl.a_slot_bytes = pl.R * 128;
+    pl.s_slot_bytes = (int)round_up((size_t)pl.BK * pl.RS * pl.esize, 1024);
     pl.n_ci_chunks = (int)ceil_div(p.C_in, pl.BK);
     pl.ci_pad = pl.n_ci_chunks * pl.BK;
     plan_channel_blocks(p, pl);
@@ -130,7 +142,7 @@ bool plan_tc_geometry(const c1n_params& p, Plan& pl, bool cluster) {
         pl.n_acc = 2;
         pl.tmem_cols = 512;
     }
-    plan_stages(pl, 3, 6);
+    plan_stages(pl, 2, 4, 4);
     return pl.smem_bytes <= 227 * 1024;
 }
 
@@ -146,7 +158,8 @@ bool plan_tc_linear(const c1n_params& p, Plan& pl) {
     pl.n_units = pl.n_t_tiles * pl.n_cb;
     pl.n_acc = 2;
     pl.tmem_cols = 512;
-    plan_stages(pl, 4, 4);
+    pl.s_slot_bytes = 0;
+    plan_stages(pl, 4, 4, 0);
     return pl.smem_bytes <= 227 * 1024;
 }
 
@@ -287,13 +300,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 c1n_status encode(CUtensorMap* m, const void* ptr, bool bf16, int rank, const cuuint64_t* dims,
-                  const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+                  const cuuint64_t* strides_bytes, const cuuint32_t* box,
+                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = encode_fn();
     if (!fn) return fail(C1N_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank,
                     const_cast<void*>(ptr), dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(C1N_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return C1N_OK;
@@ -348,8 +362,8 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         if (e != cudaSuccess) return cuda_fail(e, "SIMT conv launch");
     } else {
         const bool linear = pl.path == C1N_PATH_TC_LINEAR;
-        if (linear && (!aligned16(a->x) || !aligned16(a->w)))
-            return fail(C1N_ERR_ALIGNMENT, "x and w must be 16-byte aligned on the Linear tensor-core path");
+        if (!aligned16(a->x) || (linear && !aligned16(a->w)))
+            return fail(C1N_ERR_ALIGNMENT, "x (and w on the Linear path) must be 16-byte aligned for TMA");
         const void* wsrc = a->w;
         if (!linear) {
             void* wp = wsb + pl.ws_wp;
@@ -381,7 +395,13 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
                 cuuint32_t bw[3] = {(cuuint32_t)pl.BK, (cuuint32_t)pl.BN, 1};
                 st = encode(&d->tm_b, wsrc, pl.bf16, 3, dw, sw, bw);
                 if (st != C1N_OK) return st;
-                d->tm_a = d->tm_b;
+                // A source: x[n][ci][t], box = RS time steps x BK channels x 1 sample, unswizzled
+                // (the kernel transposes it in shared memory).
+                cuuint64_t dx[3] = {(cuuint64_t)p.T, (cuuint64_t)p.C_in, (cuuint64_t)p.N};
+                cuuint64_t sx[2] = {(cuuint64_t)p.T * es, (cuuint64_t)p.T * p.C_in * es};
+                cuuint32_t bx[3] = {(cuuint32_t)pl.RS, (cuuint32_t)pl.BK, 1};
+                st = encode(&d->tm_a, a->x, pl.bf16, 3, dx, sx, bx, CU_TENSOR_MAP_SWIZZLE_NONE);
+                if (st != C1N_OK) return st;
             }
             d->tm_x_ptr = a->x;
             d->tm_w_ptr = wsrc;
@@ -394,6 +414,7 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         t.n_ci_chunks = pl.n_ci_chunks; t.n_t_tiles = pl.n_t_tiles; t.n_units = pl.n_units;
         t.n_acc = pl.n_acc; t.tmem_cols = pl.tmem_cols; t.stages_a = pl.stages_a; t.stages_b = pl.stages_b;
         t.a_slot_bytes = pl.a_slot_bytes; t.b_slot_bytes = pl.b_slot_bytes;
+        t.RS = pl.RS; t.t_shift = pl.t_shift; t.stages_s = pl.stages_s; t.s_slot_bytes = pl.s_slot_bytes;
         t.groups = p.norm == C1N_NORM_GROUP ? p.groups : 1;
         t.cpg = p.C_out / t.groups;
         t.eps = p.eps;

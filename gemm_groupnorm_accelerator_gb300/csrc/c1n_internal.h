@@ -6,7 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/conv1d_norm.h"
+#include "conv1d_norm.h"
 
 namespace c1n {
 
@@ -23,6 +23,8 @@ struct Plan {
     // tensor-core geometry: tiles of 128 output rows (time steps, or Linear rows) x BN channels
     int BK = 32;          // input channels per pipeline stage (one 128-byte row)
     int R = 128;          // rows of one A tile (128 + tap halo, multiple of 8)
+    int RS = 0;           // time steps of one staged x box (R + alignment shift, multiple of 16 bytes)
+    int t_shift = 0;      // staged index of A row 0 (pad_left rounded up to 16 bytes, minus pad_left)
     int BN = 0;           // output channels per MMA (<= 256)
     int n_cb = 0;         // channel blocks
     int cb_per_unit = 1;  // channel blocks accumulated by one work unit
@@ -34,8 +36,8 @@ struct Plan {
     int tmem_cols = 512;  // TMEM columns allocated per CTA
     int cluster = 1;
     int grid = 0;
-    int stages_a = 0, stages_b = 0;
-    int a_slot_bytes = 0, b_slot_bytes = 0;
+    int stages_a = 0, stages_b = 0, stages_s = 0;
+    int a_slot_bytes = 0, b_slot_bytes = 0, s_slot_bytes = 0;
     int smem_bytes = 0;
     int kernels = 0;
     // workspace layout (byte offsets)
@@ -50,6 +52,7 @@ struct TcArgs {
     int N, C_in, C_out, T, T_out, k, dil, pad_left;
     int BK, R, BN, n_cb, cb_per_unit, n_ci_chunks, n_t_tiles, n_units;
     int n_acc, tmem_cols, stages_a, stages_b, a_slot_bytes, b_slot_bytes;
+    int RS, t_shift, stages_s, s_slot_bytes;  // x staging ring (conv mode)
     int groups, cpg;
     float eps;
     int gelu;
@@ -76,8 +79,8 @@ cudaError_t launch_broadcast(const c1n_params& p, const Plan& pl, const float* r
                              cudaStream_t stream);
 cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream);
 
-// Tensor-core kernels. `tm_a` holds the A operand map (packed weights in conv mode, X in Linear
-// mode), `tm_b` the B operand map (x in conv mode, W in Linear mode).
+// Tensor-core kernels. `tm_a`: x (conv mode, staged time-contiguous boxes) or X (Linear mode);
+// `tm_b`: packed weights (conv mode) or W (Linear mode).
 enum TcEpilogue { kEpiDirect = 0, kEpiClusterGN = 1 };
 cudaError_t launch_tc(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                       bool linear, int epilogue, bool out_bf16, int num_sms, cudaStream_t stream);

@@ -6,9 +6,10 @@
 //
 //   D[t][co] = sum_kk sum_ci  x[n][ci][t + kk*dilation - pad_left] * wp[kk][co][ci]
 //
-//   * A operand (x, K-major): eight "transposer" warps read x[n][ci][t] with coalesced loads (32
-//     consecutive t per warp instruction) and write it to shared memory as rows of time steps,
-//     128 bytes of input channels per row, in the 128-byte swizzled layout the tensor core reads.
+//   * A operand (x, K-major): x[n][ci][t] arrives by TMA in time-contiguous boxes (a staging ring
+//     several chunks deep), and eight "transposer" warps rewrite each box in shared memory as rows
+//     of time steps, 128 bytes of input channels per row, in the 128-byte swizzled layout the
+//     tensor core reads.
 //     One tile holds 128 + (k-1)*dilation rows (the halo); tap kk uses the same tile with the
 //     matrix-descriptor start moved down by kk*dilation rows, so the taps cost no extra copies.
 //     Padding (causal or symmetric) and the ragged ends are zeros written by the transposer.
@@ -17,9 +18,10 @@
 //   * Accumulators sit at 256-column boundaries of TMEM; two of them on the persistent paths so
 //     that the epilogue of one tile overlaps the mainloop of the next.
 //
-// Warp roles (448 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues tcgen05.mma from
-// one thread, warps 2-5 run the epilogue (each owns the 32 TMEM lanes of its quarter), warps 6-13
-// transpose x into the A ring (conv mode only).
+// Warp roles (480 threads): warp 0 issues the weight TMA loads, warp 1 owns TMEM and issues
+// tcgen05.mma from one thread, warps 2-5 run the epilogue (each owns the 32 TMEM lanes of its
+// quarter), warp 14 TMA-loads x boxes into a staging ring and warps 6-13 transpose them into the A
+// ring (conv mode only).
 //
 // Linear mode (T = 1, k = 1; Kimi-K2.6 l2_p75 page): x is X[rows][in] and already K-major, so TMA
 // loads the A operand as well; D[row][co].
@@ -41,12 +43,15 @@ namespace c1n {
 namespace {
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpEpi0 = 2, kWarpXp0 = 6, kXpWarps = 8;
-constexpr int kThreads = 32 * (kWarpXp0 + kXpWarps);  // every warp has exactly one role
+constexpr int kWarpXld = kWarpXp0 + kXpWarps;  // x staging loader (conv mode)
+constexpr int kThreads = 32 * (kWarpXld + 1);  // every warp has exactly one role
 constexpr int kEpiThreads = 128, kXpThreads = 32 * kXpWarps;
-constexpr int kXpBatch = 6;  // transposer tasks whose loads are in flight together
 
 // Where a bounded wait gave up (status word detail).
-enum WaitSite { kWaitAEmpty = 1, kWaitBEmpty, kWaitAFull, kWaitBFull, kWaitAccEmpty, kWaitAccFull, kWaitDrain };
+enum WaitSite {
+    kWaitAEmpty = 1, kWaitBEmpty, kWaitAFull, kWaitBFull, kWaitAccEmpty, kWaitAccFull, kWaitDrain, kWaitSEmpty,
+    kWaitSFull
+};
 
 __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
 
@@ -122,13 +127,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     using InT = typename std::conditional<BF16, __nv_bfloat16, float>::type;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-    const int SA = a.stages_a, SB = a.stages_b;
+    const int SA = a.stages_a, SB = a.stages_b, SS = LINEAR ? 0 : a.stages_s;
     const uint32_t sA = smem_u32(base);
     const uint32_t sB = sA + uint32_t(SA * a.a_slot_bytes);
-    uint8_t* misc = base + size_t(SA) * a.a_slot_bytes + size_t(SB) * a.b_slot_bytes;
+    const size_t s_off = size_t(SA) * a.a_slot_bytes + size_t(SB) * a.b_slot_bytes;  // x staging ring
+    const uint32_t sS = sA + uint32_t(s_off);
+    uint8_t* misc = base + s_off + size_t(SS) * a.s_slot_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
     const int i_afull = 0, i_aempty = SA, i_bfull = 2 * SA, i_bempty = 2 * SA + SB, i_accfull = 2 * SA + 2 * SB,
-              i_accempty = i_accfull + 2, i_drain = i_accempty + 2, n_bars = i_drain + 1;
+              i_accempty = i_accfull + 2, i_drain = i_accempty + 2, i_sfull = i_drain + 1, i_sempty = i_sfull + SS,
+              n_bars = i_sempty + SS;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + n_bars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // progress counters: [0] B loads issued, [1] A chunks consumed by the MMA, [2] units issued by
@@ -156,6 +164,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(i_accempty + i), 4);  // one arrival per epilogue warp
         }
         mbar_init(bar(i_drain), 1);
+        for (int i = 0; i < SS; ++i) {
+            mbar_init(bar(i_sfull + i), 1);
+            mbar_init(bar(i_sempty + i), kXpWarps);  // one arrival per transposer warp
+        }
         *abort_flag = 0;
         for (int i = 0; i < kProgSlots; ++i) prog[i] = 0;
         fence_mbar_init();
@@ -280,70 +292,86 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar(i_drain));
             mbar_drain(bar(i_drain), 0, a.status);
         }
+    } else if (warp == kWarpXld) {
+        // ---------------------------------------------------------------- x staging loader (conv mode)
+        // One TMA box per (tile, input-channel chunk): RS time steps (from a 16-byte aligned time
+        // coordinate) x BK channels of one sample, time-contiguous. Boxes that reach past either
+        // end of the sequence or past C_in are zero-filled by the TMA unit, which is exactly the
+        // convolution's zero padding.
+        if (!LINEAR && lane == 0) {
+            const uint32_t box_bytes = uint32_t(a.RS * a.BK * (BF16 ? 2 : 4));
+            int si = 0;
+            uint32_t sph = 0;
+            long long s_cnt = 0;
+            for (int u = first_unit; u < a.n_units && !*abort_flag; u += unit_step) {
+                const Unit un = decode_unit<LINEAR>(a, u);
+                const int t0 = un.row0 - a.pad_left - a.t_shift;  // multiple of 16 bytes of elements
+                for (int c = 0; c < a.n_ci_chunks; ++c) {
+                    if (!mbar_wait(bar(i_sempty + si), sph ^ 1, abort_flag, a.status, kWaitSEmpty, prog)) goto xld_done;
+                    mbar_arrive_expect_tx(bar(i_sfull + si), box_bytes);
+                    tma_load_3d(sS + si * a.s_slot_bytes, &tm_a, bar(i_sfull + si), t0, c * a.BK, un.n);
+                    ++s_cnt;
+                    if (++si == SS) { si = 0; sph ^= 1; }
+                }
+            }
+        xld_done:
+            if (*abort_flag)
+                for (int s2 = 0; s2 < SS; ++s2)
+                    if (s_cnt > s2) mbar_drain(bar(i_sfull + s2), s2 < si ? sph : (sph ^ 1), a.status);
+        }
     } else if (warp >= kWarpXp0) {
         // ---------------------------------------------------------------- x transposer (conv mode)
+        // Staged x (rows = channels, time-contiguous) -> A tile (rows = time steps, 128 bytes of
+        // channels per row, 128-byte swizzle). A task is one 16-byte chunk of one A row; lanes take
+        // consecutive rows, so the staged reads are consecutive words (conflict-free) and the
+        // swizzled 16-byte writes of 8 consecutive lanes cover all 32 banks.
         if (!LINEAR) {
             const int xt = threadIdx.x - kWarpXp0 * 32;  // 0..255
-            const InT* x = static_cast<const InT*>(a.x);
             constexpr int kPerChunk = BF16 ? 8 : 4;       // channels per 16-byte chunk
             const int n_tasks = 8 * a.R;                  // (16-byte chunk, row) pairs per tile
-            int ai = 0;
-            uint32_t aph = 0;
+            int ai = 0, si = 0;
+            uint32_t aph = 0, sph = 0;
             for (int u = first_unit; u < a.n_units; u += unit_step) {
-                const Unit un = decode_unit<LINEAR>(a, u);
-                const long long t_first = (long long)un.row0 - a.pad_left;
-                const InT* xn = x + (long long)un.n * a.C_in * a.T;
                 for (int c = 0; c < a.n_ci_chunks; ++c) {
-                    if (xt == 0) prog[8] = kWaitAEmpty;
-                    const bool ok = mbar_wait(bar(i_aempty + ai), aph ^ 1, abort_flag, a.status, kWaitAEmpty, prog);
-                    if (!__all_sync(0xffffffffu, ok)) goto xp_done;
+                    if (xt == 0) prog[8] = kWaitSFull;
+                    // One lane waits; the shuffle hands its answer to the warp and reconverges it.
+                    int ok = 0;
+                    if (lane == 0)
+                        ok = mbar_wait(bar(i_sfull + si), sph, abort_flag, a.status, kWaitSFull, prog) &&
+                             mbar_wait(bar(i_aempty + ai), aph ^ 1, abort_flag, a.status, kWaitAEmpty, prog);
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) goto xp_done;
                     if (xt == 0) prog[8] = 0;
+                    const InT* stg = reinterpret_cast<const InT*>(base + s_off + size_t(si) * a.s_slot_bytes);
                     uint8_t* slot = base + size_t(ai) * a.a_slot_bytes;
-                    // Each task is one 16-byte chunk (kPerChunk channels) of one row (time step);
-                    // consecutive threads take consecutive rows, so every load instruction of a
-                    // warp reads 32 consecutive time steps of one channel.
-                    for (int q0 = xt; q0 < n_tasks; q0 += kXpBatch * kXpThreads) {
-                        float v[kXpBatch][kPerChunk];
+                    for (int q = xt; q < n_tasks; q += kXpThreads) {
+                        const int cg = q / a.R, r = q - cg * a.R;
+                        const InT* src = stg + (cg * kPerChunk) * a.RS + r + a.t_shift;
+                        uint4 pk;
+                        if constexpr (BF16) {
+                            uint32_t w[4];
 #pragma unroll
-                        for (int b = 0; b < kXpBatch; ++b) {
-                            const int q = q0 + b * kXpThreads;
-                            const int cg = q / a.R, r = q - cg * a.R;
-                            const long long t = t_first + r;
-                            const int ci0 = c * a.BK + cg * kPerChunk;
-                            const bool t_ok = q < n_tasks && t >= 0 && t < a.T;
-#pragma unroll
-                            for (int e = 0; e < kPerChunk; ++e) {
-                                const int ci = ci0 + e;
-                                v[b][e] = (t_ok && ci < a.C_in) ? load_in(xn + (long long)ci * a.T + t) : 0.f;
+                            for (int e = 0; e < 4; ++e) {
+                                const uint32_t lo = *reinterpret_cast<const uint16_t*>(src + (2 * e) * a.RS);
+                                const uint32_t hi = *reinterpret_cast<const uint16_t*>(src + (2 * e + 1) * a.RS);
+                                w[e] = lo | (hi << 16);
                             }
+                            pk = make_uint4(w[0], w[1], w[2], w[3]);
+                        } else {
+                            pk = make_uint4(__float_as_uint(src[0]), __float_as_uint(src[a.RS]),
+                                            __float_as_uint(src[2 * a.RS]), __float_as_uint(src[3 * a.RS]));
                         }
-#pragma unroll
-                        for (int b = 0; b < kXpBatch; ++b) {
-                            const int q = q0 + b * kXpThreads;
-                            if (q >= n_tasks) break;
-                            const int cg = q / a.R, r = q - cg * a.R;
-                            uint4 pk;
-                            if constexpr (BF16) {
-                                uint32_t w[4];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    __nv_bfloat162 h = __floats2bfloat162_rn(v[b][2 * e], v[b][2 * e + 1]);
-                                    w[e] = *reinterpret_cast<uint32_t*>(&h);
-                                }
-                                pk = make_uint4(w[0], w[1], w[2], w[3]);
-                            } else {
-                                pk = make_uint4(__float_as_uint(v[b][0]), __float_as_uint(v[b][1]),
-                                                __float_as_uint(v[b][2]), __float_as_uint(v[b][kPerChunk - 1]));
-                            }
-                            *reinterpret_cast<uint4*>(slot + r * 128 + ((cg ^ (r & 7)) << 4)) = pk;
-                        }
+                        *reinterpret_cast<uint4*>(slot + r * 128 + ((cg ^ (r & 7)) << 4)) = pk;
                     }
                     // Make the generic-proxy stores visible to the tensor core, then signal.
                     fence_async_shared();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(i_afull + ai));
+                    if (lane == 0) {
+                        mbar_arrive(bar(i_afull + ai));
+                        mbar_arrive(bar(i_sempty + si));
+                    }
                     if (xt == 0) prog[3] = prog[3] + 1;
                     if (++ai == SA) { ai = 0; aph ^= 1; }
+                    if (++si == SS) { si = 0; sph ^= 1; }
                 }
             }
         xp_done:;
@@ -354,14 +382,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m = q * 32 + lane;  // tile row: time step (conv) or sample row (Linear)
         const int er = threadIdx.x - kWarpEpi0 * 32;  // 0..127, index among epilogue threads
         bool mid_sync_done = false;
+        // Per-channel parameters of the current channel block, staged once in shared memory so the
+        // element loops below read them with conflict-free broadcast loads instead of global loads.
+        float* s_bias = epi + 3072;  // [256]
+        int staged_co = -1;
         int lt = 0;
         for (int u = first_unit; u < a.n_units; u += unit_step, ++lt) {
             const int ab = a.n_acc == 2 ? (lt & 1) : 0;
             const uint32_t acc_par = a.n_acc == 2 ? uint32_t((lt >> 1) & 1) : uint32_t(lt & 1);
             if (er == 0) prog[7] = kWaitAccFull;
-            const bool got = mbar_wait(bar(i_accfull + ab), acc_par, abort_flag, a.status, kWaitAccFull, prog);
-            // The barrier ORs what every epilogue thread saw: all four warps leave (or stay) together.
+            // One lane per warp waits; the shuffle reconverges the warp (the TMEM loads below are
+            // warp-collective), and the barrier ORs what every epilogue thread saw, so all four
+            // warps leave (or stay) together.
+            int got = 0;
+            if (lane == 0) got = mbar_wait(bar(i_accfull + ab), acc_par, abort_flag, a.status, kWaitAccFull, prog);
+            got = __shfl_sync(0xffffffffu, got, 0);
             if (named_bar_any(1, kEpiThreads, !got || *abort_flag != 0)) break;
+            __syncwarp();
             if (er == 0) prog[7] = 0;
             tc_fence_after();
             const Unit un = decode_unit<LINEAR>(a, u);
@@ -373,32 +410,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
                     const int co_base = (un.cbu * a.cb_per_unit + cbi) * a.BN;
                     const int ncols = min(a.BN, a.C_out - co_base);
+                    if (co_base != staged_co) {  // uniform over the epilogue threads
+                        named_bar_sync(1, kEpiThreads);
+                        for (int col = er; col < a.BN; col += kEpiThreads)
+                            s_bias[col] = (a.bias && col < ncols) ? __ldg(a.bias + co_base + col) : 0.f;
+                        named_bar_sync(1, kEpiThreads);
+                        staged_co = co_base;
+                    }
                     const uint32_t tb =
                         tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * (ab * a.cb_per_unit + cbi));
                     for (int j0 = 0; j0 < ncols; j0 += 16) {
                         float v[16];
                         tmem_load16(tb + uint32_t(j0), v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] += s_bias[j0 + i];
+                        if (a.gelu) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
+                        }
                         if (!row_ok) continue;
                         if (LINEAR) {
                             OutT* dst = y + (long long)row * a.C_out + co_base + j0;
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                if (j0 + i < ncols) {
-                                    float z = v[i] + (a.bias ? __ldg(a.bias + co_base + j0 + i) : 0.f);
-                                    if (a.gelu) z = gelu_erf(z);
-                                    store_out(dst + i, z);
-                                }
-                            }
+                            for (int i = 0; i < 16; ++i)
+                                if (j0 + i < ncols) store_out(dst + i, v[i]);
                         } else {
                             OutT* dst = y + ((long long)un.n * a.C_out + co_base + j0) * a.T_out + row;
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                if (j0 + i < ncols) {
-                                    float z = v[i] + (a.bias ? __ldg(a.bias + co_base + j0 + i) : 0.f);
-                                    if (a.gelu) z = gelu_erf(z);
-                                    store_out(dst + (long long)i * a.T_out, z);
-                                }
-                            }
+                            for (int i = 0; i < 16; ++i)
+                                if (j0 + i < ncols) store_out(dst + (long long)i * a.T_out, v[i]);
                         }
                     }
                 }
@@ -416,7 +456,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* part = epi + 1536;      // [3][256] count, mean, M2 per group of this CTA
                 float* colscale = epi + 2304;  // [256]
                 float* colshift = epi + 2560;  // [256]
+                // epi + 3072: s_bias [256], epi + 3328: s_colmean [256]
+                float* s_colmean = epi + 3328;  // [256] mean of each column's group
                 const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
+                for (int col = er; col < 256; col += kEpiThreads) {
+                    s_bias[col] = (a.bias && col < ncols) ? __ldg(a.bias + co_base + col) : 0.f;
+                    s_colmean[col] = 0.f;
+                }
+                named_bar_sync(1, kEpiThreads);
+                const float row_mask = row_ok ? 1.f : 0.f;
                 // passes 0 and 1: per-column sums over the tile's time steps, then per-group
                 // count / mean (pass 0) and squared deviations from the CTA group mean (pass 1)
                 for (int pass = 0; pass < 2; ++pass) {
@@ -426,16 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_load16(tb + uint32_t(j0 + 16), *reinterpret_cast<float(*)[16]>(&v[16]));
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
-                            const int col = j0 + i;
-                            float z = 0.f;
-                            if (row_ok && col < ncols) {
-                                z = v[i] + (a.bias ? __ldg(a.bias + co_base + col) : 0.f);
-                                if (pass == 1) {
-                                    const float d = z - gmean[col / cpg];
-                                    z = d * d;
-                                }
-                            }
-                            v[i] = z;
+                            // columns past ncols have zero bias and zero mean; their sums are unused
+                            const float z = v[i] + s_bias[j0 + i] - s_colmean[j0 + i];
+                            v[i] = (pass == 0 ? z : z * z) * row_mask;
                         }
                         const float s = warp_reduce_scatter32(v, lane);
                         red[q * 256 + j0 + lane] = s;
@@ -458,6 +499,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     named_bar_sync(1, kEpiThreads);
+                    if (pass == 0) {
+                        for (int col = er; col < ncols; col += kEpiThreads) s_colmean[col] = gmean[col / cpg];
+                        named_bar_sync(1, kEpiThreads);
+                    }
                 }
                 // partials of every CTA in the cluster become visible
                 cluster_sync_all();
@@ -474,28 +519,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     colsum[g] = rsqrtf((gn > 0.f ? gm2 / gn : 0.f) + a.eps);  // reused: group rstd
                 }
                 named_bar_sync(1, kEpiThreads);
-                for (int col = er; col < ncols; col += kEpiThreads) {
-                    const int g = col / cpg, co = co_base + col;
-                    const float sc = colsum[g] * (a.gamma ? __ldg(a.gamma + co) : 1.f);
-                    const float bias = a.bias ? __ldg(a.bias + co) : 0.f;
+                for (int col = er; col < 256; col += kEpiThreads) {
+                    float sc = 0.f, sh = 0.f;
+                    if (col < ncols) {
+                        const int g = col / cpg, co = co_base + col;
+                        sc = colsum[g] * (a.gamma ? __ldg(a.gamma + co) : 1.f);
+                        sh = (a.beta ? __ldg(a.beta + co) : 0.f) + (s_bias[col] - gmean[g]) * sc;
+                    }
                     colscale[col] = sc;
-                    colshift[col] = (a.beta ? __ldg(a.beta + co) : 0.f) + (bias - gmean[g]) * sc;
+                    colshift[col] = sh;
                 }
                 named_bar_sync(1, kEpiThreads);
                 // pass 2: normalize from TMEM and store once (a warp stores 32 consecutive t per channel)
                 for (int j0 = 0; j0 < ncols; j0 += 16) {
                     float v[16];
                     tmem_load16(tb + uint32_t(j0), v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = fmaf(v[i], colscale[j0 + i], colshift[j0 + i]);
+                    if (a.gelu) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
+                    }
                     if (!row_ok) continue;
                     OutT* dst = y + ((long long)un.n * a.C_out + co_base + j0) * a.T_out + row;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        if (j0 + i < ncols) {
-                            float z = fmaf(v[i], colscale[j0 + i], colshift[j0 + i]);
-                            if (a.gelu) z = gelu_erf(z);
-                            store_out(dst + (long long)i * a.T_out, z);
-                        }
-                    }
+                    for (int i = 0; i < 16; ++i)
+                        if (j0 + i < ncols) store_out(dst + (long long)i * a.T_out, v[i]);
                 }
             }
             tc_fence_before();
