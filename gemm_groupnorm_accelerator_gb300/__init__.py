@@ -27,8 +27,10 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA, ER
 EXPORTED_SYMBOLS = (
     "conv1d_norm_desc_create", "conv1d_norm_workspace_size", "conv1d_norm_set_workspace", "conv1d_norm_plan_info",
     "conv1d_norm_run", "conv1d_norm_run_ex", "conv1d_norm_pack_weights", "conv1d_norm_check", "conv1d_norm_destroy",
-    "conv1d_norm_status_string", "conv1d_norm_last_error", "conv1d_norm_version",
+    "conv1d_norm_status_string", "conv1d_norm_last_error", "conv1d_norm_version", "conv1d_norm_run_static_scratch",
 )
+
+STATIC_SCRATCH_BYTES = 4 << 20  # C1N_STATIC_SCRATCH_BYTES
 
 
 class Params(ctypes.Structure):
@@ -93,6 +95,7 @@ def load(build_if_missing: bool = True):
         lib.conv1d_norm_run_ex.argtypes = [vp, P(Args), vp]
         lib.conv1d_norm_pack_weights.argtypes = [vp, vp, vp, ctypes.c_size_t, vp]
         lib.conv1d_norm_check.argtypes = [vp, vp, vp]
+        lib.conv1d_norm_run_static_scratch.argtypes = [vp, P(Args), vp]
         lib.conv1d_norm_destroy.argtypes = [vp]
         lib.conv1d_norm_destroy.restype = None
         lib.conv1d_norm_status_string.argtypes = [ctypes.c_int]
@@ -102,7 +105,7 @@ def load(build_if_missing: bool = True):
         lib.conv1d_norm_version.restype = ctypes.c_int32
         for name in ("conv1d_norm_desc_create", "conv1d_norm_workspace_size", "conv1d_norm_set_workspace",
                      "conv1d_norm_plan_info", "conv1d_norm_run", "conv1d_norm_run_ex", "conv1d_norm_pack_weights",
-                     "conv1d_norm_check"):
+                     "conv1d_norm_check", "conv1d_norm_run_static_scratch"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -156,6 +159,11 @@ def conv1d_norm_run_ex(desc: int, args: Args, stream: int) -> None:
 
 def conv1d_norm_pack_weights(desc: int, w: int, workspace: Optional[int], workspace_bytes: int, stream: int) -> None:
     _check(load().conv1d_norm_pack_weights(desc, w, workspace, workspace_bytes, stream))
+
+
+def conv1d_norm_run_static_scratch(desc: int, args: Args, stream: int) -> None:
+    """Run without any allocation, using the library's fixed device scratch (see the C header)."""
+    _check(load().conv1d_norm_run_static_scratch(desc, ctypes.byref(args), stream))
 
 
 def conv1d_norm_check(desc: int, workspace: Optional[int], stream: int) -> None:

@@ -454,6 +454,10 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
 
 }  // namespace
 
+namespace c1n {
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+}  // namespace c1n
+
 extern "C" {
 
 c1n_status conv1d_norm_desc_create(const c1n_params* params, c1n_desc** out) {

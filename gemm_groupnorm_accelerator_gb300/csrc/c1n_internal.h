@@ -65,6 +65,9 @@ struct TcArgs {
     int* status;
 };
 
+// Sets the calling thread's message returned by conv1d_norm_last_error().
+void set_last_error(const char* msg);
+
 // Launchers (each enqueues on `stream`, returns cudaGetLastError()).
 cudaError_t launch_simt_conv(const c1n_params& p, const Plan& pl, const void* x, const void* w, const float* b,
                              void* out, bool out_is_raw_f32, cudaStream_t stream);

@@ -157,6 +157,28 @@ c1n_status conv1d_norm_pack_weights(c1n_desc* desc, const void* w, void* workspa
  * attached one) and return C1N_OK, C1N_ERR_TIMEOUT or C1N_ERR_DEVICE. */
 c1n_status conv1d_norm_check(const c1n_desc* desc, void* workspace, c1n_stream_t stream);
 
+/* Operator run for callers that cannot allocate device memory (no counterpart on the pages; this is
+ * an interface of this library only). Some callers may not call cudaMalloc or any other allocator
+ * where they run the operator: code inside a host framework that owns all device allocations, a
+ * plugin whose host forbids allocating after start-up, a real-time loop that must not block on an
+ * allocator. This entry point allocates nothing. Its scratch is one array of
+ * C1N_STATIC_SCRATCH_BYTES bytes in device global memory, part of the library's device image: every
+ * GPU that loads the library holds it until the process exits.
+ *
+ *   - args->x, w, b, gamma, beta, bias2, y, argmin as for conv1d_norm_run_ex; args->workspace must
+ *     be NULL (the array is the workspace).
+ *   - Returns C1N_ERR_WORKSPACE if conv1d_norm_workspace_size(desc) exceeds C1N_STATIC_SCRATCH_BYTES.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call clears the status word at the start of the array (stream-ordered) and attaches the
+ *     array to `desc` as its workspace, replacing any workspace attached before, so that
+ *     conv1d_norm_check(desc, NULL, stream) reads this call's device status.
+ *   - All calls, from every descriptor and stream, share the one array and it keeps the last call's
+ *     contents: calls that overlap on the GPU (different streams, no ordering between them) race.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine. Asynchronous like run_ex. */
+#define C1N_STATIC_SCRATCH_BYTES (4u << 20)
+c1n_status conv1d_norm_run_static_scratch(c1n_desc* desc, const c1n_args* args, c1n_stream_t stream);
+
 void conv1d_norm_destroy(c1n_desc* desc);
 
 const char* conv1d_norm_status_string(c1n_status status);
