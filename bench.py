@@ -204,7 +204,10 @@ def our_arm(args, wl):
                              wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, args.math, args.path)
     op = c1n.Conv1dNorm(params, device=dev)
     path = op.path
-    inp = synth.make_inputs(wl, seed=rank)
+    # Weak scaling: rank r runs the per-GPU workload on batch rows [r*N, (r+1)*N) of one global
+    # batch of world*N entries (GroupNorm / LayerNorm / row-min statistics are per sample or per
+    # row, so no data crosses ranks).
+    inp = shard_inputs(wl, rank)
     bf = wl.dtype == synth.DTYPE_BF16
     tdt = torch.bfloat16 if bf else torch.float32
 
@@ -269,7 +272,7 @@ def our_arm(args, wl):
         t = torch.tensor([ms, main_ms], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms, main_ms = float(t[0]), float(t[1])
-    value = wl.flops * world / (ms / 1e3) / 1e12
+    value, ms = aggregate([ms], wl.flops, world)
 
     # roofline of the dominant kernel (the fused tensor-core kernel)
     flops, nbytes = wl.flops, wl.algorithmic_bytes
@@ -352,6 +355,17 @@ def measure_e2e(args, wl, op, inp, dev, tdt, bf, w_dev, b_dev, ga_dev, be_dev, b
     ms = e0.elapsed_time(e1) / args.steps
     return {"value": wl.flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def shard_inputs(wl, rank, seed=0):
+    """Inputs of rank `rank`: batch rows [rank*N, (rank+1)*N) of the global batch."""
+    return synth.make_inputs(wl, seed=seed, n_rows=wl.N, row_offset=rank * wl.N)
+
+
+def aggregate(ms_per_rank, flops_per_rank, world):
+    """Whole-job throughput: all ranks' work divided by the slowest rank's time (TFLOP/s)."""
+    slowest = max(ms_per_rank)
+    return flops_per_rank * world / (slowest / 1e3) / 1e12, slowest
 
 
 def read_traffic(workload, path):

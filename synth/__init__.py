@@ -68,16 +68,21 @@ def uniform_pm(seed: int, stream: int, count: int, a: float) -> np.ndarray:
     return (a * (2.0 * uniform01(seed, stream, count) - 1.0)).astype(np.float32)
 
 
-def normal(seed: int, stream: int, count: int, mu: float = 0.0, sigma: float = 1.0) -> np.ndarray:
-    """float32 samples of N(mu, sigma) (sigma is the standard deviation)."""
+def normal_slice(seed: int, stream: int, start: int, count: int, mu: float = 0.0, sigma: float = 1.0) -> np.ndarray:
+    """Elements start .. start+count-1 of the stream's N(mu, sigma) sequence (float32)."""
     out = np.empty(count, dtype=np.float32)
     chunk = 1 << 22
     for s in range(0, count, chunk):
         n = min(chunk, count - s)
-        u = uniform01(seed, stream, 2 * n, start=2 * s)
+        u = uniform01(seed, stream, 2 * n, start=2 * (start + s))
         r = np.sqrt(-2.0 * np.log1p(-u[0::2]))
         out[s:s + n] = (mu + sigma * r * np.cos(2.0 * math.pi * u[1::2])).astype(np.float32)
     return out
+
+
+def normal(seed: int, stream: int, count: int, mu: float = 0.0, sigma: float = 1.0) -> np.ndarray:
+    """float32 samples of N(mu, sigma) (sigma is the standard deviation)."""
+    return normal_slice(seed, stream, 0, count, mu, sigma)
 
 
 def round_bf16(a: np.ndarray) -> np.ndarray:
@@ -182,15 +187,17 @@ WORKLOADS = [CONV_GN_TINY, CONV_GN, CAUSAL_CONV, LINEAR_GN_ROWMIN, CONV_LN_GELU_
 BY_NAME: Dict[str, Workload] = {w.name: w for w in WORKLOADS}
 
 
-def make_inputs(wl: Workload, seed: int = 0, n_rows: Optional[int] = None) -> Dict[str, np.ndarray]:
+def make_inputs(wl: Workload, seed: int = 0, n_rows: Optional[int] = None, row_offset: int = 0) -> Dict[str, np.ndarray]:
     """Draw the inputs of ``wl`` (float32 arrays; bf16 workloads get bf16-rounded values).
 
-    ``n_rows`` draws only the first ``n_rows`` batch entries of x (the counter-based
-    generator makes that prefix identical to the full draw).
+    ``n_rows`` / ``row_offset`` draw only batch entries [row_offset, row_offset + n_rows) of x
+    (the counter-based generator makes any such slice identical to the same rows of a larger
+    draw); parameters are the same for every slice.
     """
     n = wl.N if n_rows is None else n_rows
     a = wl.w_bound if wl.w_bound is not None else 1.0 / math.sqrt(wl.C_in * wl.k)
-    x = normal(seed, STREAM_X, n * wl.C_in * wl.T).reshape(n, wl.C_in, wl.T)
+    per_row = wl.C_in * wl.T
+    x = normal_slice(seed, STREAM_X, row_offset * per_row, n * per_row).reshape(n, wl.C_in, wl.T)
     w = uniform_pm(seed, STREAM_W, wl.C_out * wl.C_in * wl.k, a).reshape(wl.C_out, wl.C_in, wl.k)
     out = {"x": x, "w": w}
     out["b"] = uniform_pm(seed, STREAM_B, wl.C_out, a) if wl.has_bias else None
