@@ -27,8 +27,10 @@ struct c1n_desc {
     // cached TMA descriptors (re-encoded when a pointer changes)
     const void* tm_x_ptr = nullptr;
     const void* tm_w_ptr = nullptr;
+    const void* tm_y_ptr = nullptr;
     CUtensorMap tm_a;  // A operand map
     CUtensorMap tm_b;  // B operand map
+    CUtensorMap tm_y;  // output map (TMA store of the fused GroupNorm tile)
     int device = -1;
     int num_sms = 0;
 };
@@ -53,6 +55,10 @@ c1n_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// SM count assumed when planning without a device (the smallest Blackwell part); the cooperative
+// exchange is re-checked against the real device at run time.
+constexpr int kMinSmCount = 148;
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 long long t_out_of(const c1n_params& p) {
@@ -211,23 +217,35 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
         why = tc_conv_blocker(p, pl);
         if (!*why) {
             const int cpg = p.norm == C1N_NORM_GROUP ? p.C_out / p.groups : 0;
-            // 1. GroupNorm fused through a cluster of CTAs along time (one cluster per sample and
-            //    channel block; groups must not straddle a channel block).
+            // 1. GroupNorm fused into the conv kernel: one CTA per (sample, time tile, channel
+            //    block); groups must not straddle a channel block. The CTAs of a sample exchange
+            //    partial statistics across a cooperative grid (whole grid resident at once) or a
+            //    thread-block cluster of at most 8 CTAs.
             Plan trial = pl;
             const bool geom_ok = plan_tc_geometry(p, trial, true);
-            const bool gn_cluster_ok = p.norm == C1N_NORM_GROUP && p.post != C1N_POST_ROWMIN_BIAS && geom_ok &&
-                                       trial.n_t_tiles <= 8 && (trial.n_cb == 1 || trial.BN % cpg == 0);
-            if ((want == C1N_PATH_AUTO || want == C1N_PATH_TC_CLUSTER) && gn_cluster_ok) {
+            const bool groups_ok = p.norm == C1N_NORM_GROUP && p.post != C1N_POST_ROWMIN_BIAS && geom_ok &&
+                                   (trial.n_cb == 1 || trial.BN % cpg == 0);
+            const bool cluster_ok = groups_ok && trial.n_t_tiles <= 8;
+            const bool grid_ok = groups_ok && trial.n_units <= kMinSmCount;
+            const bool fused_ok = want == C1N_PATH_TC_FUSED_GN_DSMEM ? cluster_ok : (cluster_ok || grid_ok);
+            if ((want == C1N_PATH_AUTO || want == C1N_PATH_TC_FUSED_GN || want == C1N_PATH_TC_FUSED_GN_DSMEM) &&
+                fused_ok) {
                 pl = trial;
-                pl.path = C1N_PATH_TC_CLUSTER;
+                pl.path = want == C1N_PATH_TC_FUSED_GN_DSMEM ? C1N_PATH_TC_FUSED_GN_DSMEM : C1N_PATH_TC_FUSED_GN;
                 pl.cluster = pl.n_t_tiles;
                 pl.grid = pl.n_units;
                 plan_workspace(p, pl, true, false, false);
+                // grid exchange: arrival counters and per-(sample, block, tile, group) partials
+                pl.gsync_count = p.N * pl.n_cb;
+                pl.ws_gsync = pl.ws_total;
+                pl.ws_gpart = round_up(pl.ws_gsync + (size_t)pl.gsync_count * 4, 256);
+                pl.ws_total = round_up(pl.ws_gpart + (size_t)pl.n_units * 256 * sizeof(float4), 256);
                 pl.kernels = 2;
                 return C1N_OK;
             }
-            if (want == C1N_PATH_TC_CLUSTER)
-                why = "TC_CLUSTER needs GroupNorm, no row-min, T_out <= 1024 and groups inside a channel block";
+            if (want == C1N_PATH_TC_FUSED_GN || want == C1N_PATH_TC_FUSED_GN_DSMEM)
+                why = "fused GroupNorm needs groups inside a channel block, no row-min, and the CTAs of a sample "
+                      "in one cluster (<= 8) or the whole grid resident at once";
             // 2. Direct epilogue (no normalization).
             if (!*why && p.norm == C1N_NORM_NONE && p.post != C1N_POST_ROWMIN_BIAS &&
                 (want == C1N_PATH_AUTO || want == C1N_PATH_TC_DIRECT)) {
@@ -270,7 +288,7 @@ c1n_status validate(const c1n_params* p) {
     if (p->post < 0 || p->post > 2) return fail(C1N_ERR_INVALID_ARG, "unknown post-op %d", p->post);
     if (p->dtype < 0 || p->dtype > 1) return fail(C1N_ERR_INVALID_ARG, "unknown dtype %d", p->dtype);
     if (p->math < 0 || p->math > 2) return fail(C1N_ERR_INVALID_ARG, "unknown math %d", p->math);
-    if (p->force_path < -1 || p->force_path > 4) return fail(C1N_ERR_INVALID_ARG, "unknown path %d", p->force_path);
+    if (p->force_path < -1 || p->force_path > 5) return fail(C1N_ERR_INVALID_ARG, "unknown path %d", p->force_path);
     if (p->norm == C1N_NORM_GROUP && (p->groups < 1 || p->C_out % p->groups != 0))
         return fail(C1N_ERR_INVALID_ARG, "GroupNorm needs groups >= 1 dividing C_out (%d %% %d)", p->C_out, p->groups);
     if (p->norm != C1N_NORM_NONE && !(std::isfinite(p->eps) && p->eps > 0.f))
@@ -368,7 +386,8 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         if (!linear) {
             void* wp = wsb + pl.ws_wp;
             if (!(a->flags & C1N_FLAG_WEIGHTS_PACKED)) {
-                e = launch_pack_weights(p, pl, a->w, wp, s);
+                unsigned* zero = pl.gsync_count ? reinterpret_cast<unsigned*>(wsb + pl.ws_gsync) : nullptr;
+                e = launch_pack_weights(p, pl, a->w, wp, s, zero, pl.gsync_count);
                 if (e != cudaSuccess) return cuda_fail(e, "weight pack launch");
             }
             wsrc = wp;
@@ -406,6 +425,21 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
             d->tm_x_ptr = a->x;
             d->tm_w_ptr = wsrc;
         }
+        const bool fused_gn = pl.path == C1N_PATH_TC_FUSED_GN || pl.path == C1N_PATH_TC_FUSED_GN_DSMEM;
+        // The fused GroupNorm tile is stored by one TMA bulk store when y's rows are 16-byte
+        // multiples and the staging tile fits in the operand rings.
+        const bool tma_store = fused_gn && aligned16(a->y) && (pl.T_out * pl.esize) % 16 == 0 &&
+                               (size_t)pl.BN * 128 * pl.esize <=
+                                   (size_t)pl.stages_b * pl.b_slot_bytes + (size_t)pl.stages_s * pl.s_slot_bytes;
+        if (tma_store && d->tm_y_ptr != a->y) {
+            const cuuint64_t es = (cuuint64_t)pl.esize;
+            cuuint64_t dy[3] = {(cuuint64_t)pl.T_out, (cuuint64_t)p.C_out, (cuuint64_t)p.N};
+            cuuint64_t sy[2] = {(cuuint64_t)pl.T_out * es, (cuuint64_t)pl.T_out * p.C_out * es};
+            cuuint32_t by[3] = {128u, (cuuint32_t)pl.BN, 1};
+            st = encode(&d->tm_y, a->y, pl.bf16, 3, dy, sy, by, CU_TENSOR_MAP_SWIZZLE_NONE);
+            if (st != C1N_OK) return st;
+            d->tm_y_ptr = a->y;
+        }
         TcArgs t;
         std::memset(&t, 0, sizeof(t));
         t.N = p.N; t.C_in = p.C_in; t.C_out = p.C_out; t.T = p.T; t.T_out = (int)pl.T_out; t.k = p.k;
@@ -417,20 +451,32 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         t.RS = pl.RS; t.t_shift = pl.t_shift; t.stages_s = pl.stages_s; t.s_slot_bytes = pl.s_slot_bytes;
         t.groups = p.norm == C1N_NORM_GROUP ? p.groups : 1;
         t.cpg = p.C_out / t.groups;
+        t.sub = (t.cpg == 4 || t.cpg == 8) ? t.cpg : (t.cpg % 16 == 0 ? 16 : 0);
+        t.tma_store = tma_store ? 1 : 0;
+        t.gpart = reinterpret_cast<float4*>(wsb + pl.ws_gpart);
+        t.gsync = reinterpret_cast<unsigned*>(wsb + pl.ws_gsync);
         t.eps = p.eps;
-        t.gelu = (p.post == C1N_POST_GELU_ERF && (pl.path == C1N_PATH_TC_DIRECT || pl.path == C1N_PATH_TC_CLUSTER)) ? 1 : 0;
+        t.gelu = (p.post == C1N_POST_GELU_ERF && (pl.path == C1N_PATH_TC_DIRECT || fused_gn)) ? 1 : 0;
         const uint32_t fmt = pl.bf16 ? 1u : 2u;
         t.idesc = make_idesc(fmt, fmt, 0u, 0u, 128u, (uint32_t)pl.BN);
         t.x = a->x;
         t.bias = a->b;
         t.gamma = a->gamma;
         t.beta = a->beta;
-        const bool fused_out = pl.path == C1N_PATH_TC_DIRECT || pl.path == C1N_PATH_TC_CLUSTER;
+        const bool fused_out = pl.path == C1N_PATH_TC_DIRECT || fused_gn;
         t.y = fused_out ? a->y : (second ? static_cast<void*>(raw) : a->y);
         t.status = status;
         const bool out_bf16 = pl.bf16 && (fused_out || !second);
-        e = launch_tc(pl, t, d->tm_a, d->tm_b, linear,
-                      pl.path == C1N_PATH_TC_CLUSTER ? kEpiClusterGN : kEpiDirect, out_bf16, d->num_sms, s);
+        int epi = kEpiDirect;
+        if (fused_gn) {
+            // Cooperative grid when every CTA fits on the device at once (one per SM), else a cluster.
+            const bool grid_fits = pl.path == C1N_PATH_TC_FUSED_GN && pl.n_units <= d->num_sms;
+            if (grid_fits) epi = kEpiGridGN;
+            else if (pl.n_t_tiles <= 8) epi = kEpiClusterGN;
+            else return fail(C1N_ERR_UNSUPPORTED, "fused GroupNorm grid of %d CTAs exceeds the %d SMs of this device",
+                             pl.n_units, d->num_sms);
+        }
+        e = launch_tc(pl, t, d->tm_a, d->tm_b, tma_store ? d->tm_y : d->tm_b, linear, epi, out_bf16, d->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
         if (fused_out) return C1N_OK;
     }
@@ -540,8 +586,9 @@ c1n_status conv1d_norm_pack_weights(c1n_desc* desc, const void* w, void* workspa
     if (!ws || ws_bytes < pl.ws_total)
         return fail(C1N_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", pl.ws_total, ws ? ws_bytes : 0);
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(C1N_ERR_ALIGNMENT, "workspace not 256-byte aligned");
+    unsigned* zero = pl.gsync_count ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + pl.ws_gsync) : nullptr;
     cudaError_t e = launch_pack_weights(desc->p, pl, w, static_cast<uint8_t*>(ws) + pl.ws_wp,
-                                        reinterpret_cast<cudaStream_t>(stream));
+                                        reinterpret_cast<cudaStream_t>(stream), zero, pl.gsync_count);
     if (e != cudaSuccess) return cuda_fail(e, "weight pack launch");
     return C1N_OK;
 }

@@ -42,6 +42,8 @@ struct Plan {
     int kernels = 0;
     // workspace layout (byte offsets)
     size_t ws_wp = 0, ws_stats = 0, ws_raw = 0, ws_rowmin = 0, ws_total = 0;
+    size_t ws_gsync = 0, ws_gpart = 0;  // fused GroupNorm across a cooperative grid
+    int gsync_count = 0;
 };
 
 // Shared memory beyond the operand rings: barriers, flags and epilogue scratch.
@@ -54,6 +56,8 @@ struct TcArgs {
     int n_acc, tmem_cols, stages_a, stages_b, a_slot_bytes, b_slot_bytes;
     int RS, t_shift, stages_s, s_slot_bytes;  // x staging ring (conv mode)
     int groups, cpg;
+    int sub;        // channels per partial-sum run in the GroupNorm statistics (4, 8, 16; 0 = per column)
+    int tma_store;  // fused GroupNorm: store the tile with one TMA bulk store
     float eps;
     int gelu;
     uint32_t idesc;
@@ -63,6 +67,8 @@ struct TcArgs {
     const float* beta;
     void* y;
     int* status;
+    float4* gpart;     // per (sample, channel block, time tile, group): count, mean, M2
+    unsigned* gsync;   // per (sample, channel block): arrival counter
 };
 
 // Sets the calling thread's message returned by conv1d_norm_last_error().
@@ -80,12 +86,15 @@ cudaError_t launch_rowmin(const c1n_params& p, const Plan& pl, const float* raw,
                           cudaStream_t stream);
 cudaError_t launch_broadcast(const c1n_params& p, const Plan& pl, const float* rowmin, const float* bias2, void* y,
                              cudaStream_t stream);
-cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream);
+// Also zeroes `nzero` words at `zero` (the fused-GroupNorm arrival counters) when given.
+cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream,
+                                unsigned* zero = nullptr, int nzero = 0);
 
 // Tensor-core kernels. `tm_a`: x (conv mode, staged time-contiguous boxes) or X (Linear mode);
 // `tm_b`: packed weights (conv mode) or W (Linear mode).
-enum TcEpilogue { kEpiDirect = 0, kEpiClusterGN = 1 };
+enum TcEpilogue { kEpiDirect = 0, kEpiClusterGN = 1, kEpiGridGN = 2 };
 cudaError_t launch_tc(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                      bool linear, int epilogue, bool out_bf16, int num_sms, cudaStream_t stream);
+                      const CUtensorMap& tm_y, bool linear, int epilogue, bool out_bf16, int num_sms,
+                      cudaStream_t stream);
 
 }  // namespace c1n

@@ -280,7 +280,10 @@ __global__ void __launch_bounds__(256) broadcast_rows_f32_kernel(int N, int C, c
 
 template <typename InT, typename PackT>
 __global__ void __launch_bounds__(256) pack_weights_kernel(int C_out, int C_in, int k, int ci_pad, int tf32_round,
-                                                           const InT* __restrict__ w, PackT* __restrict__ wp) {
+                                                           const InT* __restrict__ w, PackT* __restrict__ wp,
+                                                           unsigned* __restrict__ zero, int nzero) {
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0u;
     const long long total = (long long)k * C_out * ci_pad;
     for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
          e += (long long)gridDim.x * blockDim.x) {
@@ -415,15 +418,16 @@ cudaError_t launch_broadcast(const c1n_params& p, const Plan& pl, const float* r
     return cudaGetLastError();
 }
 
-cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream) {
+cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream,
+                                unsigned* zero, int nzero) {
     const long long total = (long long)p.k * p.C_out * pl.ci_pad;
     if (pl.bf16)
         pack_weights_kernel<__nv_bfloat16, __nv_bfloat16><<<grid_1d(total), 256, 0, stream>>>(
             p.C_out, p.C_in, p.k, pl.ci_pad, 0, static_cast<const __nv_bfloat16*>(w),
-            static_cast<__nv_bfloat16*>(wp));
+            static_cast<__nv_bfloat16*>(wp), zero, nzero);
     else
         pack_weights_kernel<float, float><<<grid_1d(total), 256, 0, stream>>>(
-            p.C_out, p.C_in, p.k, pl.ci_pad, 1, static_cast<const float*>(w), static_cast<float*>(wp));
+            p.C_out, p.C_in, p.k, pl.ci_pad, 1, static_cast<const float*>(w), static_cast<float*>(wp), zero, nzero);
     return cudaGetLastError();
 }
 

@@ -50,7 +50,7 @@ constexpr int kEpiThreads = 128, kXpThreads = 32 * kXpWarps;
 // Where a bounded wait gave up (status word detail).
 enum WaitSite {
     kWaitAEmpty = 1, kWaitBEmpty, kWaitAFull, kWaitBFull, kWaitAccEmpty, kWaitAccFull, kWaitDrain, kWaitSEmpty,
-    kWaitSFull
+    kWaitSFull, kWaitGridPeers
 };
 
 __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
@@ -98,6 +98,60 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
     return v[0];
 }
 
+// Per-thread sums of each run of SUB consecutive channels of this thread's row (SUB = 4, 8, 16;
+// SUB divides the group size), then one butterfly reduce-scatter per 32 sums: afterwards
+// red[q*256 + j] holds the warp's total of run j. Values are (x + bias - colmean) in pass 0 and
+// its square in pass 1, masked by row validity.
+template <int SUB>
+__device__ __forceinline__ void gn_run_sums(uint32_t tb, int ncols, int pass, float row_mask, const float* s_bias,
+                                            const float* s_colmean, float* red, int q, int lane) {
+    constexpr int kRuns = 256 / SUB;
+    constexpr int kBlocks = (kRuns + 31) / 32;
+    float acc[kBlocks * 32];
+#pragma unroll
+    for (int i = 0; i < kBlocks * 32; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int c16 = 0; c16 < 16; ++c16) {
+        const int j0 = c16 * 16;
+        if (j0 < ncols) {  // uniform over the CTA
+            float v[16];
+            tmem_load16(tb + uint32_t(j0), v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float z = v[i] + s_bias[j0 + i] - s_colmean[j0 + i];
+                v[i] = (pass ? z * z : z) * row_mask;
+            }
+#pragma unroll
+            for (int r = 0; r < 16 / SUB; ++r) {
+                float sum = 0.f;
+#pragma unroll
+                for (int i = 0; i < SUB; ++i) sum += v[r * SUB + i];
+                acc[c16 * (16 / SUB) + r] = sum;
+            }
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < kBlocks; ++b)
+        red[q * 256 + b * 32 + lane] = warp_reduce_scatter32(*reinterpret_cast<float(*)[32]>(&acc[b * 32]), lane);
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(m)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_store_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 struct Unit {
     int n;     // sample (conv) / 0 (Linear)
     int row0;  // first output time step (conv) / first row (Linear)
@@ -123,7 +177,8 @@ __device__ __forceinline__ Unit decode_unit(const TcArgs& a, int u) {
 template <bool LINEAR, bool BF16, typename OutT, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_conv_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tm_a,
-                   const __grid_constant__ CUtensorMap tm_b) {
+                   const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_y) {
+    constexpr bool kFusedGN = EPI == kEpiClusterGN || EPI == kEpiGridGN;
     using InT = typename std::conditional<BF16, __nv_bfloat16, float>::type;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -184,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     int first_unit, unit_step;
-    if (EPI == kEpiClusterGN) {
+    if (kFusedGN) {
         first_unit = (blockIdx.z * a.n_t_tiles + blockIdx.x) * (a.n_cb / a.cb_per_unit) + blockIdx.y;
         unit_step = a.n_units;  // exactly one unit
     } else {
@@ -443,21 +498,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else {
-                // ------------------------------------------------ cluster GroupNorm (conv mode)
-                // Channels of this CTA: [co_base, co_base + ncols); groups never straddle a block.
+                // ------------------------------------------------ fused GroupNorm (conv mode)
+                // The CTAs of one (sample, channel block) together cover all T_out steps. Each
+                // reduces per-group partial statistics over its tile, the partials are exchanged
+                // (distributed shared memory inside a cluster, or global memory across a
+                // cooperative grid) and merged with Chan's formula, and each CTA normalizes its
+                // tile from TMEM and stores it once.
                 const int co_base = un.cbu * a.BN;
                 const int ncols = min(a.BN, a.C_out - co_base);
                 const int cpg = a.cpg;
                 const int ngroups = (ncols + cpg - 1) / cpg;
                 const int nvalid_t = min(128, a.T_out - un.row0);
-                float* red = epi;              // [4][256] per-warp column partials
+                const int tt = un.row0 / 128;
+                float* red = epi;              // [4][256] per-warp partial sums
                 float* colsum = epi + 1024;    // [256]
-                float* gmean = epi + 1280;     // [256] group mean (this CTA, then the cluster)
+                float* gmean = epi + 1280;     // [256] group mean (this CTA, then all CTAs)
                 float* part = epi + 1536;      // [3][256] count, mean, M2 per group of this CTA
                 float* colscale = epi + 2304;  // [256]
                 float* colshift = epi + 2560;  // [256]
-                // epi + 3072: s_bias [256], epi + 3328: s_colmean [256]
-                float* s_colmean = epi + 3328;  // [256] mean of each column's group
+                float* s_colmean = epi + 3328; // [256] mean of each column's group
                 const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
                 for (int col = er; col < 256; col += kEpiThreads) {
                     s_bias[col] = (a.bias && col < ncols) ? __ldg(a.bias + co_base + col) : 0.f;
@@ -465,37 +524,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 named_bar_sync(1, kEpiThreads);
                 const float row_mask = row_ok ? 1.f : 0.f;
-                // passes 0 and 1: per-column sums over the tile's time steps, then per-group
-                // count / mean (pass 0) and squared deviations from the CTA group mean (pass 1)
+                // pass 0: group sums -> count and mean of this CTA; pass 1: squared deviations
+                // from that mean -> M2 of this CTA
                 for (int pass = 0; pass < 2; ++pass) {
-                    for (int j0 = 0; j0 < ncols; j0 += 32) {
-                        float v[32];
-                        tmem_load16(tb + uint32_t(j0), *reinterpret_cast<float(*)[16]>(&v[0]));
-                        tmem_load16(tb + uint32_t(j0 + 16), *reinterpret_cast<float(*)[16]>(&v[16]));
+                    if (a.sub == 4) {
+                        gn_run_sums<4>(tb, ncols, pass, row_mask, s_bias, s_colmean, red, q, lane);
+                    } else if (a.sub == 8) {
+                        gn_run_sums<8>(tb, ncols, pass, row_mask, s_bias, s_colmean, red, q, lane);
+                    } else if (a.sub == 16) {
+                        gn_run_sums<16>(tb, ncols, pass, row_mask, s_bias, s_colmean, red, q, lane);
+                    } else {
+                        // any group size: per-column sums over the tile's time steps
+                        for (int j0 = 0; j0 < ncols; j0 += 32) {
+                            float v[32];
+                            tmem_load16(tb + uint32_t(j0), *reinterpret_cast<float(*)[16]>(&v[0]));
+                            tmem_load16(tb + uint32_t(j0 + 16), *reinterpret_cast<float(*)[16]>(&v[16]));
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            // columns past ncols have zero bias and zero mean; their sums are unused
-                            const float z = v[i] + s_bias[j0 + i] - s_colmean[j0 + i];
-                            v[i] = (pass == 0 ? z : z * z) * row_mask;
+                            for (int i = 0; i < 32; ++i) {
+                                // columns past ncols have zero bias and mean; their sums are unused
+                                const float z = v[i] + s_bias[j0 + i] - s_colmean[j0 + i];
+                                v[i] = (pass == 0 ? z : z * z) * row_mask;
+                            }
+                            red[q * 256 + j0 + lane] = warp_reduce_scatter32(v, lane);
                         }
-                        const float s = warp_reduce_scatter32(v, lane);
-                        red[q * 256 + j0 + lane] = s;
                     }
                     named_bar_sync(1, kEpiThreads);
-                    for (int col = er; col < ncols; col += kEpiThreads)
-                        colsum[col] = red[col] + red[256 + col] + red[512 + col] + red[768 + col];
-                    named_bar_sync(1, kEpiThreads);
+                    const int runs_per_group = a.sub > 0 ? cpg / a.sub : 0;
                     for (int g = er; g < ngroups; g += kEpiThreads) {
-                        float s = 0.f;
+                        float sum = 0.f;
                         const int c_end = min(ncols, (g + 1) * cpg);
-                        for (int col = g * cpg; col < c_end; ++col) s += colsum[col];
+                        if (a.sub > 0) {
+                            for (int j = g * runs_per_group; j < (g + 1) * runs_per_group; ++j)
+                                sum += red[j] + red[256 + j] + red[512 + j] + red[768 + j];
+                        } else {
+                            for (int col = g * cpg; col < c_end; ++col)
+                                sum += red[col] + red[256 + col] + red[512 + col] + red[768 + col];
+                        }
                         const float cnt = float((c_end - g * cpg) * nvalid_t);
                         if (pass == 0) {
-                            gmean[g] = s / cnt;
+                            gmean[g] = sum / cnt;
                             part[g] = cnt;
-                            part[256 + g] = s / cnt;
+                            part[256 + g] = sum / cnt;
                         } else {
-                            part[512 + g] = s;
+                            part[512 + g] = sum;
                         }
                     }
                     named_bar_sync(1, kEpiThreads);
@@ -504,19 +575,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                         named_bar_sync(1, kEpiThreads);
                     }
                 }
-                // partials of every CTA in the cluster become visible
-                cluster_sync_all();
-                mid_sync_done = true;
-                for (int g = er; g < ngroups; g += kEpiThreads) {
-                    float gn = 0.f, gmu = 0.f, gm2 = 0.f;
-                    const uint32_t p0 = smem_u32(part + g);
-                    for (int rk = 0; rk < a.n_t_tiles; ++rk) {
-                        const uint32_t pr = map_shared_rank(p0, uint32_t(rk));
-                        chan_merge(gn, gmu, gm2, ld_shared_cluster_f32(pr), ld_shared_cluster_f32(pr + 1024),
-                                   ld_shared_cluster_f32(pr + 2048));
+                if (EPI == kEpiClusterGN) {
+                    // partials of every CTA in the cluster become visible
+                    cluster_sync_all();
+                    mid_sync_done = true;
+                    for (int g = er; g < ngroups; g += kEpiThreads) {
+                        float gn = 0.f, gmu = 0.f, gm2 = 0.f;
+                        const uint32_t p0 = smem_u32(part + g);
+                        for (int rk = 0; rk < a.n_t_tiles; ++rk) {
+                            const uint32_t pr = map_shared_rank(p0, uint32_t(rk));
+                            chan_merge(gn, gmu, gm2, ld_shared_cluster_f32(pr), ld_shared_cluster_f32(pr + 1024),
+                                       ld_shared_cluster_f32(pr + 2048));
+                        }
+                        gmean[g] = gmu;
+                        colsum[g] = rsqrtf((gn > 0.f ? gm2 / gn : 0.f) + a.eps);  // group rstd
                     }
-                    gmean[g] = gmu;
-                    colsum[g] = rsqrtf((gn > 0.f ? gm2 / gn : 0.f) + a.eps);  // reused: group rstd
+                } else {
+                    // publish this CTA's partials, count arrivals, wait (bounded) for the peers
+                    const size_t slot0 = size_t(un.n * a.n_cb + un.cbu) * a.n_t_tiles;
+                    float4* gp = a.gpart + (slot0 + tt) * 256;
+                    for (int g = er; g < ngroups; g += kEpiThreads)
+                        gp[g] = make_float4(part[g], part[256 + g], part[512 + g], 0.f);
+                    __threadfence();
+                    named_bar_sync(1, kEpiThreads);
+                    if (er == 0) {
+                        unsigned* cnt = a.gsync + (un.n * a.n_cb + un.cbu);
+                        const unsigned n_peers = unsigned(a.n_t_tiles);
+                        const unsigned old = atomicAdd(cnt, 1u);
+                        const unsigned target = (old / n_peers + 1u) * n_peers;
+                        const uint64_t t0 = global_timer_ns();
+                        while (int(ld_acquire_gpu(cnt) - target) < 0) {
+                            if (*abort_flag) break;
+                            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                                if (atomicCAS(a.status, 0, 6) == 0) {
+                                    atomicExch(a.status + 1, kWaitGridPeers);
+                                    atomicExch(a.status + 2, int(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)));
+                                }
+                                *abort_flag = 1;
+                                break;
+                            }
+                            __nanosleep(64);
+                        }
+                    }
+                    named_bar_sync(1, kEpiThreads);
+                    const float4* gq = a.gpart + slot0 * 256;
+                    for (int g = er; g < ngroups; g += kEpiThreads) {
+                        float gn = 0.f, gmu = 0.f, gm2 = 0.f;
+                        for (int rk = 0; rk < a.n_t_tiles; ++rk) {
+                            const float4 pv = __ldcg(gq + size_t(rk) * 256 + g);
+                            chan_merge(gn, gmu, gm2, pv.x, pv.y, pv.z);
+                        }
+                        gmean[g] = gmu;
+                        colsum[g] = rsqrtf((gn > 0.f ? gm2 / gn : 0.f) + a.eps);  // group rstd
+                    }
                 }
                 named_bar_sync(1, kEpiThreads);
                 for (int col = er; col < 256; col += kEpiThreads) {
@@ -530,21 +641,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                     colshift[col] = sh;
                 }
                 named_bar_sync(1, kEpiThreads);
-                // pass 2: normalize from TMEM and store once (a warp stores 32 consecutive t per channel)
-                for (int j0 = 0; j0 < ncols; j0 += 16) {
-                    float v[16];
-                    tmem_load16(tb + uint32_t(j0), v);
+                // normalize from TMEM; store once
+                if (a.tma_store) {
+                    // Stage the tile as [channel][time] (a warp writes 32 consecutive words per
+                    // channel) in the operand rings, idle now that the tile's MMAs are done, then
+                    // one TMA bulk store; rows past T_out and channels past C_out are clipped.
+                    OutT* so = reinterpret_cast<OutT*>(base + size_t(SA) * a.a_slot_bytes);
+                    for (int j0 = 0; j0 < ncols; j0 += 16) {
+                        float v[16];
+                        tmem_load16(tb + uint32_t(j0), v);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = fmaf(v[i], colscale[j0 + i], colshift[j0 + i]);
-                    if (a.gelu) {
+                        for (int i = 0; i < 16; ++i) v[i] = fmaf(v[i], colscale[j0 + i], colshift[j0 + i]);
+                        if (a.gelu) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
+                            for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) store_out(so + (j0 + i) * 128 + m, v[i]);
                     }
-                    if (!row_ok) continue;
-                    OutT* dst = y + ((long long)un.n * a.C_out + co_base + j0) * a.T_out + row;
+                    fence_async_shared();
+                    named_bar_sync(1, kEpiThreads);
+                    if (er == 0) {
+                        tma_store_3d(&tm_y, smem_u32(so), un.row0, co_base, un.n);
+                        tma_store_wait_read();
+                    }
+                } else {
+                    for (int j0 = 0; j0 < ncols; j0 += 16) {
+                        float v[16];
+                        tmem_load16(tb + uint32_t(j0), v);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (j0 + i < ncols) store_out(dst + (long long)i * a.T_out, v[i]);
+                        for (int i = 0; i < 16; ++i) v[i] = fmaf(v[i], colscale[j0 + i], colshift[j0 + i]);
+                        if (a.gelu) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
+                        }
+                        if (!row_ok) continue;
+                        OutT* dst = y + ((long long)un.n * a.C_out + co_base + j0) * a.T_out + row;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (j0 + i < ncols) store_out(dst + (long long)i * a.T_out, v[i]);
+                    }
                 }
             }
             tc_fence_before();
@@ -573,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <bool LINEAR, bool BF16, typename OutT, int EPI>
 cudaError_t launch_one(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                       int num_sms, cudaStream_t stream) {
+                       const CUtensorMap& tm_y, int num_sms, cudaStream_t stream) {
     auto kern = tc_conv_kernel<LINEAR, BF16, OutT, EPI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
     if (e != cudaSuccess) return e;
@@ -590,33 +726,47 @@ cudaError_t launch_one(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a,
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
+    } else if (EPI == kEpiGridGN) {
+        // every CTA of a sample waits for its peers: all CTAs must be resident at once
+        cfg.gridDim = dim3(unsigned(a.n_t_tiles), unsigned(a.n_cb / a.cb_per_unit), unsigned(a.N));
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
     } else {
         const int grid = a.n_units < num_sms ? a.n_units : num_sms;
         cfg.gridDim = dim3(unsigned(grid), 1, 1);
         cfg.attrs = nullptr;
         cfg.numAttrs = 0;
     }
-    return cudaLaunchKernelEx(&cfg, kern, a, tm_a, tm_b);
+    return cudaLaunchKernelEx(&cfg, kern, a, tm_a, tm_b, tm_y);
 }
 
 }  // namespace
 
-cudaError_t launch_tc(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b, bool linear,
-                      int epilogue, bool out_bf16, int num_sms, cudaStream_t stream) {
+cudaError_t launch_tc(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                      const CUtensorMap& tm_y, bool linear, int epilogue, bool out_bf16, int num_sms,
+                      cudaStream_t stream) {
+#define C1N_LAUNCH(L, B, O, E) launch_one<L, B, O, E>(pl, a, tm_a, tm_b, tm_y, num_sms, stream)
     if (linear) {
-        if (pl.bf16 && out_bf16) return launch_one<true, true, __nv_bfloat16, kEpiDirect>(pl, a, tm_a, tm_b, num_sms, stream);
-        if (pl.bf16) return launch_one<true, true, float, kEpiDirect>(pl, a, tm_a, tm_b, num_sms, stream);
-        return launch_one<true, false, float, kEpiDirect>(pl, a, tm_a, tm_b, num_sms, stream);
+        if (pl.bf16 && out_bf16) return C1N_LAUNCH(true, true, __nv_bfloat16, kEpiDirect);
+        if (pl.bf16) return C1N_LAUNCH(true, true, float, kEpiDirect);
+        return C1N_LAUNCH(true, false, float, kEpiDirect);
     }
     if (epilogue == kEpiClusterGN) {
-        if (pl.bf16) return launch_one<false, true, __nv_bfloat16, kEpiClusterGN>(pl, a, tm_a, tm_b, num_sms, stream);
-        return launch_one<false, false, float, kEpiClusterGN>(pl, a, tm_a, tm_b, num_sms, stream);
+        if (pl.bf16) return C1N_LAUNCH(false, true, __nv_bfloat16, kEpiClusterGN);
+        return C1N_LAUNCH(false, false, float, kEpiClusterGN);
+    }
+    if (epilogue == kEpiGridGN) {
+        if (pl.bf16) return C1N_LAUNCH(false, true, __nv_bfloat16, kEpiGridGN);
+        return C1N_LAUNCH(false, false, float, kEpiGridGN);
     }
     if (pl.bf16) {
-        if (out_bf16) return launch_one<false, true, __nv_bfloat16, kEpiDirect>(pl, a, tm_a, tm_b, num_sms, stream);
-        return launch_one<false, true, float, kEpiDirect>(pl, a, tm_a, tm_b, num_sms, stream);
+        if (out_bf16) return C1N_LAUNCH(false, true, __nv_bfloat16, kEpiDirect);
+        return C1N_LAUNCH(false, true, float, kEpiDirect);
     }
-    return launch_one<false, false, float, kEpiDirect>(pl, a, tm_a, tm_b, num_sms, stream);
+    return C1N_LAUNCH(false, false, float, kEpiDirect);
+#undef C1N_LAUNCH
 }
 
 }  // namespace c1n

@@ -73,10 +73,14 @@ typedef enum {
     C1N_PATH_AUTO = -1,
     C1N_PATH_SIMT = 0,            /* SIMT conv kernel + statistics + normalize/post-op kernels */
     C1N_PATH_TC_DIRECT = 1,       /* tcgen05 conv, bias (and GELU) in the epilogue, no normalization */
-    C1N_PATH_TC_CLUSTER = 2,      /* tcgen05 conv, GroupNorm statistics merged across a thread-block
-                                     cluster through distributed shared memory, normalized in place */
+    C1N_PATH_TC_FUSED_GN = 2,     /* tcgen05 conv with GroupNorm fused: the CTAs covering one sample
+                                     exchange partial statistics (through global memory across a
+                                     cooperative grid when the whole grid fits on the GPU at once,
+                                     else through distributed shared memory inside a thread-block
+                                     cluster), then normalize their tiles in place and store once */
     C1N_PATH_TC_TWO_PASS = 3,     /* tcgen05 conv writes raw tiles, then statistics + normalize pass */
-    C1N_PATH_TC_LINEAR = 4        /* T = 1, k = 1: tcgen05 GEMM (rows x out), then the norm/post passes */
+    C1N_PATH_TC_LINEAR = 4,       /* T = 1, k = 1: tcgen05 GEMM (rows x out), then the norm/post passes */
+    C1N_PATH_TC_FUSED_GN_DSMEM = 5 /* as TC_FUSED_GN, always through a thread-block cluster (DSMEM) */
 } c1n_path;
 
 typedef struct {

@@ -36,8 +36,8 @@ def _params(wl, **kw):
 
 
 EXPECTED_PATH = {
-    synth.CONV_GN_TINY.name: "tc_cluster",
-    synth.CONV_GN.name: "tc_cluster",
+    synth.CONV_GN_TINY.name: "tc_fused_gn",
+    synth.CONV_GN.name: "tc_fused_gn",
     synth.CAUSAL_CONV.name: "tc_direct",
     synth.LINEAR_GN_ROWMIN.name: "tc_linear",
     synth.CONV_LN_GELU_BF16.name: "tc_two_pass",

@@ -93,6 +93,11 @@ SMALL = {
     "gn_c2_structure": synth.CONV_GN.replace(N=3, C_in=40, C_out=200, T=1000, groups=25),
     "gn_cpg1": synth.CONV_GN.replace(N=2, C_in=32, C_out=64, T=256, groups=64),
     "gn_cpg128": synth.CONV_GN.replace(N=2, C_in=32, C_out=256, T=256, groups=2),
+    "gn_cpg4": synth.CONV_GN.replace(N=2, C_in=32, C_out=64, T=384, groups=16),
+    "gn_cpg16": synth.CONV_GN.replace(N=3, C_in=40, C_out=128, T=512, groups=8),
+    "gn_cpg25": synth.CONV_GN.replace(N=2, C_in=16, C_out=200, T=256, groups=8),
+    # T_out = 251: rows are not 16-byte multiples, so the fused tile is stored without TMA
+    "gn_ragged_out": synth.CONV_GN.replace(N=2, C_in=24, C_out=48, T=252, k=4, groups=6),
     "gn_g1_twopass": synth.CONV_GN.replace(N=2, C_in=32, C_out=256, T=128, groups=1),
     "gn_gelu": synth.CONV_GN.replace(N=2, C_in=24, C_out=96, T=320, groups=12, post=synth.POST_GELU_ERF),
     "causal_k4": synth.CAUSAL_CONV.replace(N=2, C_in=64, C_out=160, T=1024),
@@ -140,6 +145,21 @@ def test_group_norm_two_pass_forced(cuda_lib, name):
     compare(wl, y, am, ref, None, path, name)
 
 
+GN_NAMES = ["gn_tiny", "gn_c2_structure", "gn_cpg1", "gn_cpg4", "gn_cpg16", "gn_cpg25", "gn_cpg128", "gn_gelu",
+            "gn_bf16", "gn_ragged_out"]
+
+
+@pytest.mark.parametrize("name", GN_NAMES)
+def test_group_norm_cluster_exchange_forced(cuda_lib, name):
+    # the same fused kernel with the partial statistics exchanged through a cluster's DSMEM
+    wl = SMALL[name]
+    inp = _inputs(wl)
+    ref, _ = oracle_full(wl, inp)
+    y, am, path = run_gpu(cuda_lib, wl, inp, force_path=cuda_lib.PATH_TC_FUSED_GN_DSMEM)
+    assert path == "tc_fused_gn_dsmem"
+    compare(wl, y, am, ref, None, path, name)
+
+
 def test_repeated_calls_are_identical(cuda_lib):
     wl = SMALL["gn_c2_structure"]
     inp = _inputs(wl)
@@ -155,7 +175,7 @@ def test_conv_gn_tiny_full(cuda_lib):
     inp = _inputs(wl)
     ref, _ = oracle_full(wl, inp)
     y, _, path = run_gpu(cuda_lib, wl, inp)
-    assert path == "tc_cluster"
+    assert path == "tc_fused_gn"
     compare(wl, y, None, ref, None, path, wl.name)
 
 
@@ -164,8 +184,10 @@ def test_conv_gn_full(cuda_lib):
     inp = _inputs(wl)
     ref, _ = oracle_full(wl, inp)
     y, _, path = run_gpu(cuda_lib, wl, inp)
-    assert path == "tc_cluster"
+    assert path == "tc_fused_gn"
     compare(wl, y, None, ref, None, path, wl.name)
+    y_dsmem, _, path = run_gpu(cuda_lib, wl, inp, force_path=cuda_lib.PATH_TC_FUSED_GN_DSMEM)
+    compare(wl, y_dsmem, None, ref, None, path, wl.name + " (cluster exchange)")
     # with gamma = 1, beta = 0 every (n, group) of the output has mean ~0 and variance ~1
     inp2 = dict(inp, gamma=None, beta=None)
     y2, _, _ = run_gpu(cuda_lib, wl, inp2)
