@@ -71,6 +71,7 @@ long long t_out_of(const c1n_params& p) {
 const char* tc_conv_blocker(const c1n_params& p, const Plan& pl) {
     if (p.stride != 1) return "stride > 1";
     if (p.T % pl.align != 0) return "T is not a multiple of 16 bytes of elements (TMA row stride of x)";
+    if ((long long)p.C_in * p.k > 32768) return "C_in * k above 32768 (one weight row per packing CTA)";
     if (p.k > kMaxTaps) return "more than 16 taps";
     if (p.N > 65535) return "N above 65535";
     return "";

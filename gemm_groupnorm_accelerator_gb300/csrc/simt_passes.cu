@@ -278,25 +278,33 @@ __global__ void __launch_bounds__(256) broadcast_rows_f32_kernel(int N, int C, c
     }
 }
 
+// One CTA per output channel co: read the row w[co][*][*] (C_in*k contiguous values) with
+// coalesced loads into shared memory, then write each tap's row wp[kk][co][0..ci_pad) contiguously.
 template <typename InT, typename PackT>
 __global__ void __launch_bounds__(256) pack_weights_kernel(int C_out, int C_in, int k, int ci_pad, int tf32_round,
                                                            const InT* __restrict__ w, PackT* __restrict__ wp,
                                                            unsigned* __restrict__ zero, int nzero) {
+    extern __shared__ float row[];  // [C_in * k]
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0u;
-    const long long total = (long long)k * C_out * ci_pad;
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-         e += (long long)gridDim.x * blockDim.x) {
-        const int ci = (int)(e % ci_pad);
-        const long long r = e / ci_pad;
-        const int co = (int)(r % C_out), kk = (int)(r / C_out);
-        if constexpr (sizeof(PackT) == 4) {
-            float v = ci < C_in ? to_f32(w[((long long)co * C_in + ci) * k + kk]) : 0.f;
-            if (tf32_round) v = round_tf32(v);
-            wp[e] = v;
-        } else {
-            wp[e] = ci < C_in ? w[((long long)co * C_in + ci) * k + kk] : __float2bfloat16_rn(0.f);
+    const long long rk = (long long)C_in * k;
+    for (int co = blockIdx.x; co < C_out; co += gridDim.x) {
+        const InT* src = w + co * rk;
+        for (long long i = threadIdx.x; i < rk; i += blockDim.x) row[i] = to_f32(src[i]);
+        __syncthreads();
+        for (int kk = 0; kk < k; ++kk) {
+            PackT* dst = wp + ((long long)kk * C_out + co) * ci_pad;
+            for (int ci = threadIdx.x; ci < ci_pad; ci += blockDim.x) {
+                float v = ci < C_in ? row[(long long)ci * k + kk] : 0.f;
+                if constexpr (sizeof(PackT) == 4) {
+                    if (tf32_round) v = round_tf32(v);
+                    dst[ci] = v;
+                } else {
+                    dst[ci] = __float2bfloat16_rn(v);  // exact: v came from a bf16
+                }
+            }
         }
+        __syncthreads();
     }
 }
 
@@ -420,14 +428,19 @@ cudaError_t launch_broadcast(const c1n_params& p, const Plan& pl, const float* r
 
 cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream,
                                 unsigned* zero, int nzero) {
-    const long long total = (long long)p.k * p.C_out * pl.ci_pad;
-    if (pl.bf16)
-        pack_weights_kernel<__nv_bfloat16, __nv_bfloat16><<<grid_1d(total), 256, 0, stream>>>(
-            p.C_out, p.C_in, p.k, pl.ci_pad, 0, static_cast<const __nv_bfloat16*>(w),
-            static_cast<__nv_bfloat16*>(wp), zero, nzero);
-    else
-        pack_weights_kernel<float, float><<<grid_1d(total), 256, 0, stream>>>(
-            p.C_out, p.C_in, p.k, pl.ci_pad, 1, static_cast<const float*>(w), static_cast<float*>(wp), zero, nzero);
+    const size_t smem = sizeof(float) * (size_t)p.C_in * p.k;
+    const int grid = p.C_out < 4096 ? p.C_out : 4096;
+    if (pl.bf16) {
+        auto k = pack_weights_kernel<__nv_bfloat16, __nv_bfloat16>;
+        if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k<<<grid, 256, smem, stream>>>(p.C_out, p.C_in, p.k, pl.ci_pad, 0, static_cast<const __nv_bfloat16*>(w),
+                                       static_cast<__nv_bfloat16*>(wp), zero, nzero);
+    } else {
+        auto k = pack_weights_kernel<float, float>;
+        if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k<<<grid, 256, smem, stream>>>(p.C_out, p.C_in, p.k, pl.ci_pad, 1, static_cast<const float*>(w),
+                                       static_cast<float*>(wp), zero, nzero);
+    }
     return cudaGetLastError();
 }
 

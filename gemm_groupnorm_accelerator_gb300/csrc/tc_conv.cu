@@ -98,41 +98,66 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
     return v[0];
 }
 
-// Per-thread sums of each run of SUB consecutive channels of this thread's row (SUB = 4, 8, 16;
-// SUB divides the group size), then one butterfly reduce-scatter per 32 sums: afterwards
-// red[q*256 + j] holds the warp's total of run j. Values are (x + bias - colmean) in pass 0 and
-// its square in pass 1, masked by row validity.
-template <int SUB>
-__device__ __forceinline__ void gn_run_sums(uint32_t tb, int ncols, int pass, float row_mask, const float* s_bias,
-                                            const float* s_colmean, float* red, int q, int lane) {
+// Per-thread sums over runs of SUB consecutive channels of this thread's row (SUB = 4, 8, 16
+// divides the group size; SUB = 1 is one run per channel), then one butterfly reduce-scatter per
+// 32 runs: afterwards red[q*256 + j] holds the warp's total of run j. SQUARED = false sums the raw
+// accumulator; SQUARED = true sums (acc - shift[col])^2. Rows past T_out contribute zero.
+template <int SUB, bool SQUARED>
+__device__ __forceinline__ void gn_run_sums(uint32_t tb, int ncols, bool row_ok, const float* shift, float* red,
+                                            int q, int lane) {
+    if (SUB == 1) {
+        // one run per channel: reduce each 32-column chunk as soon as it is loaded
+        for (int j0 = 0; j0 < ncols; j0 += 32) {
+            float v[32];
+            tmem_load32(tb + uint32_t(j0), v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float d = SQUARED ? v[i] - shift[j0 + i] : v[i];
+                v[i] = row_ok ? (SQUARED ? d * d : d) : 0.f;
+            }
+            red[q * 256 + j0 + lane] = warp_reduce_scatter32(v, lane);
+        }
+        return;
+    }
     constexpr int kRuns = 256 / SUB;
     constexpr int kBlocks = (kRuns + 31) / 32;
     float acc[kBlocks * 32];
 #pragma unroll
     for (int i = 0; i < kBlocks * 32; ++i) acc[i] = 0.f;
 #pragma unroll
-    for (int c16 = 0; c16 < 16; ++c16) {
-        const int j0 = c16 * 16;
+    for (int c32 = 0; c32 < 8; ++c32) {
+        const int j0 = c32 * 32;
         if (j0 < ncols) {  // uniform over the CTA
-            float v[16];
-            tmem_load16(tb + uint32_t(j0), v);
+            float v[32];
+            tmem_load32(tb + uint32_t(j0), v);
+            if (SQUARED) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float z = v[i] + s_bias[j0 + i] - s_colmean[j0 + i];
-                v[i] = (pass ? z * z : z) * row_mask;
+                for (int i = 0; i < 32; ++i) {
+                    const float d = v[i] - shift[j0 + i];
+                    v[i] = d * d;
+                }
             }
 #pragma unroll
-            for (int r = 0; r < 16 / SUB; ++r) {
+            for (int r = 0; r < 32 / SUB; ++r) {
                 float sum = 0.f;
 #pragma unroll
                 for (int i = 0; i < SUB; ++i) sum += v[r * SUB + i];
-                acc[c16 * (16 / SUB) + r] = sum;
+                acc[c32 * (32 / SUB) + r] = row_ok ? sum : 0.f;
             }
         }
     }
 #pragma unroll
     for (int b = 0; b < kBlocks; ++b)
         red[q * 256 + b * 32 + lane] = warp_reduce_scatter32(*reinterpret_cast<float(*)[32]>(&acc[b * 32]), lane);
+}
+
+template <bool SQUARED>
+__device__ __forceinline__ void gn_run_sums_any(int sub, uint32_t tb, int ncols, bool row_ok, const float* shift,
+                                                float* red, int q, int lane) {
+    if (sub == 4) gn_run_sums<4, SQUARED>(tb, ncols, row_ok, shift, red, q, lane);
+    else if (sub == 8) gn_run_sums<8, SQUARED>(tb, ncols, row_ok, shift, red, q, lane);
+    else if (sub == 16) gn_run_sums<16, SQUARED>(tb, ncols, row_ok, shift, red, q, lane);
+    else gn_run_sums<1, SQUARED>(tb, ncols, row_ok, shift, red, q, lane);
 }
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
@@ -441,6 +466,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // element loops below read them with conflict-free broadcast loads instead of global loads.
         float* s_bias = epi + 3072;  // [256]
         int staged_co = -1;
+        if (kFusedGN && first_unit < a.n_units) {
+            // One unit per CTA: stage bias, gamma and beta of its channel block while the
+            // mainloop runs (gamma and beta go where the column scale / shift end up).
+            const int co_base = decode_unit<LINEAR>(a, first_unit).cbu * a.BN;
+            const int ncols = min(a.BN, a.C_out - co_base);
+            for (int col = er; col < 256; col += kEpiThreads) {
+                const bool ok = col < ncols;
+                s_bias[col] = (ok && a.bias) ? __ldg(a.bias + co_base + col) : 0.f;
+                epi[2304 + col] = ok ? (a.gamma ? __ldg(a.gamma + co_base + col) : 1.f) : 0.f;
+                epi[2560 + col] = (ok && a.beta) ? __ldg(a.beta + co_base + col) : 0.f;
+            }
+            named_bar_sync(1, kEpiThreads);
+        }
         int lt = 0;
         for (int u = first_unit; u < a.n_units; u += unit_step, ++lt) {
             const int ab = a.n_acc == 2 ? (lt & 1) : 0;
@@ -516,65 +554,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* part = epi + 1536;      // [3][256] count, mean, M2 per group of this CTA
                 float* colscale = epi + 2304;  // [256]
                 float* colshift = epi + 2560;  // [256]
-                float* s_colmean = epi + 3328; // [256] mean of each column's group
+                float* s_shift = epi + 3328;   // [256] group mean - bias, per column
                 const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
-                for (int col = er; col < 256; col += kEpiThreads) {
-                    s_bias[col] = (a.bias && col < ncols) ? __ldg(a.bias + co_base + col) : 0.f;
-                    s_colmean[col] = 0.f;
+                // pass 0: sums of the raw accumulator; the bias enters at group level as
+                // nvalid_t * sum(bias) -> count and mean of this CTA's part of each group
+                gn_run_sums_any<false>(a.sub, tb, ncols, row_ok, s_shift, red, q, lane);
+                named_bar_sync(1, kEpiThreads);
+                const int run = a.sub > 0 ? a.sub : 1;
+                for (int g = er; g < ngroups; g += kEpiThreads) {
+                    const int c0 = g * cpg, c_end = min(ncols, c0 + cpg);
+                    float sum = 0.f, bsum = 0.f;
+                    for (int j = c0 / run; j < (c_end + run - 1) / run; ++j)
+                        sum += red[j] + red[256 + j] + red[512 + j] + red[768 + j];
+                    for (int col = c0; col < c_end; ++col) bsum += s_bias[col];
+                    const float cnt = float((c_end - c0) * nvalid_t);
+                    const float mean = (sum + float(nvalid_t) * bsum) / cnt;
+                    gmean[g] = mean;
+                    part[g] = cnt;
+                    part[256 + g] = mean;
                 }
                 named_bar_sync(1, kEpiThreads);
-                const float row_mask = row_ok ? 1.f : 0.f;
-                // pass 0: group sums -> count and mean of this CTA; pass 1: squared deviations
-                // from that mean -> M2 of this CTA
-                for (int pass = 0; pass < 2; ++pass) {
-                    if (a.sub == 4) {
-                        gn_run_sums<4>(tb, ncols, pass, row_mask, s_bias, s_colmean, red, q, lane);
-                    } else if (a.sub == 8) {
-                        gn_run_sums<8>(tb, ncols, pass, row_mask, s_bias, s_colmean, red, q, lane);
-                    } else if (a.sub == 16) {
-                        gn_run_sums<16>(tb, ncols, pass, row_mask, s_bias, s_colmean, red, q, lane);
-                    } else {
-                        // any group size: per-column sums over the tile's time steps
-                        for (int j0 = 0; j0 < ncols; j0 += 32) {
-                            float v[32];
-                            tmem_load16(tb + uint32_t(j0), *reinterpret_cast<float(*)[16]>(&v[0]));
-                            tmem_load16(tb + uint32_t(j0 + 16), *reinterpret_cast<float(*)[16]>(&v[16]));
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                // columns past ncols have zero bias and mean; their sums are unused
-                                const float z = v[i] + s_bias[j0 + i] - s_colmean[j0 + i];
-                                v[i] = (pass == 0 ? z : z * z) * row_mask;
-                            }
-                            red[q * 256 + j0 + lane] = warp_reduce_scatter32(v, lane);
-                        }
-                    }
-                    named_bar_sync(1, kEpiThreads);
-                    const int runs_per_group = a.sub > 0 ? cpg / a.sub : 0;
-                    for (int g = er; g < ngroups; g += kEpiThreads) {
-                        float sum = 0.f;
-                        const int c_end = min(ncols, (g + 1) * cpg);
-                        if (a.sub > 0) {
-                            for (int j = g * runs_per_group; j < (g + 1) * runs_per_group; ++j)
-                                sum += red[j] + red[256 + j] + red[512 + j] + red[768 + j];
-                        } else {
-                            for (int col = g * cpg; col < c_end; ++col)
-                                sum += red[col] + red[256 + col] + red[512 + col] + red[768 + col];
-                        }
-                        const float cnt = float((c_end - g * cpg) * nvalid_t);
-                        if (pass == 0) {
-                            gmean[g] = sum / cnt;
-                            part[g] = cnt;
-                            part[256 + g] = sum / cnt;
-                        } else {
-                            part[512 + g] = sum;
-                        }
-                    }
-                    named_bar_sync(1, kEpiThreads);
-                    if (pass == 0) {
-                        for (int col = er; col < ncols; col += kEpiThreads) s_colmean[col] = gmean[col / cpg];
-                        named_bar_sync(1, kEpiThreads);
-                    }
+                for (int col = er; col < 256; col += kEpiThreads)
+                    s_shift[col] = col < ncols ? gmean[col / cpg] - s_bias[col] : 0.f;
+                named_bar_sync(1, kEpiThreads);
+                // pass 1: squared deviations from this CTA's group mean -> M2
+                gn_run_sums_any<true>(a.sub, tb, ncols, row_ok, s_shift, red, q, lane);
+                named_bar_sync(1, kEpiThreads);
+                for (int g = er; g < ngroups; g += kEpiThreads) {
+                    const int c0 = g * cpg, c_end = min(ncols, c0 + cpg);
+                    float sum = 0.f;
+                    for (int j = c0 / run; j < (c_end + run - 1) / run; ++j)
+                        sum += red[j] + red[256 + j] + red[512 + j] + red[768 + j];
+                    part[512 + g] = sum;
                 }
+                named_bar_sync(1, kEpiThreads);
                 if (EPI == kEpiClusterGN) {
                     // partials of every CTA in the cluster become visible
                     cluster_sync_all();
@@ -631,11 +644,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 named_bar_sync(1, kEpiThreads);
                 for (int col = er; col < 256; col += kEpiThreads) {
+                    // colscale / colshift hold gamma / beta (staged before the mainloop)
                     float sc = 0.f, sh = 0.f;
                     if (col < ncols) {
-                        const int g = col / cpg, co = co_base + col;
-                        sc = colsum[g] * (a.gamma ? __ldg(a.gamma + co) : 1.f);
-                        sh = (a.beta ? __ldg(a.beta + co) : 0.f) + (s_bias[col] - gmean[g]) * sc;
+                        const int g = col / cpg;
+                        sc = colsum[g] * colscale[col];
+                        sh = colshift[col] + (s_bias[col] - gmean[g]) * sc;
                     }
                     colscale[col] = sc;
                     colshift[col] = sh;
@@ -647,17 +661,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // channel) in the operand rings, idle now that the tile's MMAs are done, then
                     // one TMA bulk store; rows past T_out and channels past C_out are clipped.
                     OutT* so = reinterpret_cast<OutT*>(base + size_t(SA) * a.a_slot_bytes);
-                    for (int j0 = 0; j0 < ncols; j0 += 16) {
-                        float v[16];
-                        tmem_load16(tb + uint32_t(j0), v);
+                    for (int j0 = 0; j0 < ncols; j0 += 32) {
+                        float v[32];
+                        tmem_load32(tb + uint32_t(j0), v);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = fmaf(v[i], colscale[j0 + i], colshift[j0 + i]);
+                        for (int i = 0; i < 32; ++i) v[i] = fmaf(v[i], colscale[j0 + i], colshift[j0 + i]);
                         if (a.gelu) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
+                            for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
                         }
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) store_out(so + (j0 + i) * 128 + m, v[i]);
+                        for (int i = 0; i < 32; ++i)
+                            if (j0 + i < a.BN) store_out(so + (j0 + i) * 128 + m, v[i]);
                     }
                     fence_async_shared();
                     named_bar_sync(1, kEpiThreads);
