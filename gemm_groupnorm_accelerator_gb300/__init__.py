@@ -20,8 +20,9 @@ POST_NONE, POST_GELU_ERF, POST_ROWMIN_BIAS = 0, 1, 2
 F32, BF16 = 0, 1
 MATH_AUTO, MATH_SIMT, MATH_TENSOR = 0, 1, 2
 PATH_AUTO, PATH_SIMT, PATH_TC_DIRECT, PATH_TC_FUSED_GN, PATH_TC_TWO_PASS, PATH_TC_LINEAR = -1, 0, 1, 2, 3, 4
-PATH_TC_FUSED_GN_DSMEM = 5
-PATH_NAMES = {0: "simt", 1: "tc_direct", 2: "tc_fused_gn", 3: "tc_two_pass", 4: "tc_linear", 5: "tc_fused_gn_dsmem"}
+PATH_TC_FUSED_GN_DSMEM, PATH_TC_FUSED_LN = 5, 6
+PATH_NAMES = {0: "simt", 1: "tc_direct", 2: "tc_fused_gn", 3: "tc_two_pass", 4: "tc_linear", 5: "tc_fused_gn_dsmem",
+              6: "tc_fused_ln"}
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(8)
 

@@ -205,11 +205,26 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
             why = "Linear: input features not a multiple of 16 bytes of elements";
         } else if (plan_tc_linear(p, pl)) {
             pl.path = C1N_PATH_TC_LINEAR;
+            pl.cluster = 1;
+            // Fused row epilogue: GroupNorm groups of 8/16/32 channels inside one channel block
+            // (or no normalization), any post-op.
+            const int cpg = p.norm == C1N_NORM_GROUP ? p.C_out / p.groups : 0;
+            const bool row_ok = p.norm == C1N_NORM_NONE ||
+                                (p.norm == C1N_NORM_GROUP && (cpg == 8 || cpg == 16 || cpg == 32) && pl.BN % cpg == 0);
+            if (row_ok && (p.norm != C1N_NORM_NONE || p.post == C1N_POST_ROWMIN_BIAS)) {
+                pl.row_epilogue = 1;
+                plan_workspace(p, pl, false, false, false);
+                if (p.post == C1N_POST_ROWMIN_BIAS) {
+                    pl.ws_rowpart = pl.ws_total;
+                    pl.ws_total = round_up(pl.ws_total + (size_t)p.N * pl.n_cb * sizeof(float2), 256);
+                }
+                pl.kernels = p.post == C1N_POST_ROWMIN_BIAS ? 2 : 1;
+                return C1N_OK;
+            }
             const bool need_stats = p.norm != C1N_NORM_NONE;
             const bool need_raw = out_needs_second_pass && pl.bf16;
             plan_workspace(p, pl, false, need_raw, need_stats);
             pl.kernels = 1 + (need_stats ? 1 : 0) + (p.post == C1N_POST_ROWMIN_BIAS ? 2 : (need_stats ? 1 : 0));
-            pl.cluster = 1;
             return C1N_OK;
         }
     } else if (want == C1N_PATH_TC_LINEAR) {
@@ -247,6 +262,26 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
             if (want == C1N_PATH_TC_FUSED_GN || want == C1N_PATH_TC_FUSED_GN_DSMEM)
                 why = "fused GroupNorm needs groups inside a channel block, no row-min, and the CTAs of a sample "
                       "in one cluster (<= 8) or the whole grid resident at once";
+            // 1b. Channel LayerNorm fused: one CTA holds every channel (C_out <= 512) of its tile.
+            // AUTO takes it only when two accumulators fit (C_out <= 256) so the epilogue overlaps
+            // the next tile's mainloop; with 512 channels the two-pass plan is faster today.
+            if (!*why && p.norm == C1N_NORM_CHANNEL_LAYER && p.post != C1N_POST_ROWMIN_BIAS && p.C_out <= 512 &&
+                (want == C1N_PATH_TC_FUSED_LN || (want == C1N_PATH_AUTO && p.C_out <= 256))) {
+                Plan ln = pl;
+                if (plan_tc_geometry(p, ln, false)) {
+                    ln.cb_per_unit = ln.n_cb;
+                    ln.n_units = p.N * ln.n_t_tiles;
+                    ln.n_acc = ln.n_cb == 1 ? 2 : 1;  // two accumulators only when they fit in TMEM
+                    ln.tmem_cols = 512;
+                    pl = ln;
+                    pl.path = C1N_PATH_TC_FUSED_LN;
+                    plan_workspace(p, pl, true, false, false);
+                    pl.kernels = 2;
+                    return C1N_OK;
+                }
+            }
+            if (want == C1N_PATH_TC_FUSED_LN && !*why)
+                why = "TC_FUSED_LN needs channel LayerNorm, no row-min and C_out <= 512";
             // 2. Direct epilogue (no normalization).
             if (!*why && p.norm == C1N_NORM_NONE && p.post != C1N_POST_ROWMIN_BIAS &&
                 (want == C1N_PATH_AUTO || want == C1N_PATH_TC_DIRECT)) {
@@ -289,7 +324,7 @@ c1n_status validate(const c1n_params* p) {
     if (p->post < 0 || p->post > 2) return fail(C1N_ERR_INVALID_ARG, "unknown post-op %d", p->post);
     if (p->dtype < 0 || p->dtype > 1) return fail(C1N_ERR_INVALID_ARG, "unknown dtype %d", p->dtype);
     if (p->math < 0 || p->math > 2) return fail(C1N_ERR_INVALID_ARG, "unknown math %d", p->math);
-    if (p->force_path < -1 || p->force_path > 5) return fail(C1N_ERR_INVALID_ARG, "unknown path %d", p->force_path);
+    if (p->force_path < -1 || p->force_path > 6) return fail(C1N_ERR_INVALID_ARG, "unknown path %d", p->force_path);
     if (p->norm == C1N_NORM_GROUP && (p->groups < 1 || p->C_out % p->groups != 0))
         return fail(C1N_ERR_INVALID_ARG, "GroupNorm needs groups >= 1 dividing C_out (%d %% %d)", p->C_out, p->groups);
     if (p->norm != C1N_NORM_NONE && !(std::isfinite(p->eps) && p->eps > 0.f))
@@ -456,19 +491,26 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         t.tma_store = tma_store ? 1 : 0;
         t.gpart = reinterpret_cast<float4*>(wsb + pl.ws_gpart);
         t.gsync = reinterpret_cast<unsigned*>(wsb + pl.ws_gsync);
+        t.row_cpg = (pl.row_epilogue && p.norm == C1N_NORM_GROUP) ? p.C_out / p.groups : 0;
+        t.rowmin = (pl.row_epilogue && p.post == C1N_POST_ROWMIN_BIAS) ? 1 : 0;
+        t.rowpart = reinterpret_cast<float2*>(wsb + pl.ws_rowpart);
         t.eps = p.eps;
-        t.gelu = (p.post == C1N_POST_GELU_ERF && (pl.path == C1N_PATH_TC_DIRECT || fused_gn)) ? 1 : 0;
+        const bool fused_ln = pl.path == C1N_PATH_TC_FUSED_LN;
+        t.gelu = (p.post == C1N_POST_GELU_ERF && (pl.path == C1N_PATH_TC_DIRECT || fused_gn || fused_ln ||
+                                                  pl.row_epilogue)) ? 1 : 0;
         const uint32_t fmt = pl.bf16 ? 1u : 2u;
         t.idesc = make_idesc(fmt, fmt, 0u, 0u, 128u, (uint32_t)pl.BN);
         t.x = a->x;
         t.bias = a->b;
         t.gamma = a->gamma;
         t.beta = a->beta;
-        const bool fused_out = pl.path == C1N_PATH_TC_DIRECT || fused_gn;
+        const bool fused_out = pl.path == C1N_PATH_TC_DIRECT || fused_gn || fused_ln || pl.row_epilogue;
         t.y = fused_out ? a->y : (second ? static_cast<void*>(raw) : a->y);
         t.status = status;
         const bool out_bf16 = pl.bf16 && (fused_out || !second);
         int epi = kEpiDirect;
+        if (fused_ln) epi = kEpiLN;
+        if (pl.row_epilogue) epi = kEpiRowGN;
         if (fused_gn) {
             // Cooperative grid when every CTA fits on the device at once (one per SM), else a cluster.
             const bool grid_fits = pl.path == C1N_PATH_TC_FUSED_GN && pl.n_units <= d->num_sms;
@@ -479,6 +521,10 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         }
         e = launch_tc(pl, t, d->tm_a, d->tm_b, tma_store ? d->tm_y : d->tm_b, linear, epi, out_bf16, d->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
+        if (pl.row_epilogue && p.post == C1N_POST_ROWMIN_BIAS) {
+            e = launch_rowmin_finish(p, pl, t.rowpart, a->bias2, a->y, a->argmin, s);
+            if (e != cudaSuccess) return cuda_fail(e, "row-min finisher launch");
+        }
         if (fused_out) return C1N_OK;
     }
     if (!second) return C1N_OK;

@@ -43,6 +43,8 @@ struct Plan {
     // workspace layout (byte offsets)
     size_t ws_wp = 0, ws_stats = 0, ws_raw = 0, ws_rowmin = 0, ws_total = 0;
     size_t ws_gsync = 0, ws_gpart = 0;  // fused GroupNorm across a cooperative grid
+    size_t ws_rowpart = 0;              // fused row-min partials
+    int row_epilogue = 0;               // Linear plan with the fused row epilogue
     int gsync_count = 0;
 };
 
@@ -69,6 +71,9 @@ struct TcArgs {
     int* status;
     float4* gpart;     // per (sample, channel block, time tile, group): count, mean, M2
     unsigned* gsync;   // per (sample, channel block): arrival counter
+    int row_cpg;       // row epilogue: GroupNorm over runs of row_cpg channels (8, 16, 32; 0 = none)
+    int rowmin;        // row epilogue: keep (min, argmin) per row instead of storing y
+    float2* rowpart;   // row epilogue: per (row, channel block) minimum and its channel (int bits)
 };
 
 // Sets the calling thread's message returned by conv1d_norm_last_error().
@@ -87,12 +92,16 @@ cudaError_t launch_rowmin(const c1n_params& p, const Plan& pl, const float* raw,
 cudaError_t launch_broadcast(const c1n_params& p, const Plan& pl, const float* rowmin, const float* bias2, void* y,
                              cudaStream_t stream);
 // Also zeroes `nzero` words at `zero` (the fused-GroupNorm arrival counters) when given.
+// Row-min finisher: per row, the minimum (lowest channel on ties) over the per-block partials,
+// then y[row][c] = min + bias2[c]; argmin optional.
+cudaError_t launch_rowmin_finish(const c1n_params& p, const Plan& pl, const float2* part, const float* bias2, void* y,
+                                 int32_t* argmin, cudaStream_t stream);
 cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream,
                                 unsigned* zero = nullptr, int nzero = 0);
 
 // Tensor-core kernels. `tm_a`: x (conv mode, staged time-contiguous boxes) or X (Linear mode);
 // `tm_b`: packed weights (conv mode) or W (Linear mode).
-enum TcEpilogue { kEpiDirect = 0, kEpiClusterGN = 1, kEpiGridGN = 2 };
+enum TcEpilogue { kEpiDirect = 0, kEpiClusterGN = 1, kEpiGridGN = 2, kEpiRowGN = 3, kEpiLN = 4 };
 cudaError_t launch_tc(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                       const CUtensorMap& tm_y, bool linear, int epilogue, bool out_bf16, int num_sms,
                       cudaStream_t stream);

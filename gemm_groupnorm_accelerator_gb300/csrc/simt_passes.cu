@@ -278,6 +278,51 @@ __global__ void __launch_bounds__(256) broadcast_rows_f32_kernel(int N, int C, c
     }
 }
 
+// Row-min finisher for the fused Linear epilogue: one CTA per row; the row's minimum (lowest channel
+// on ties) over its per-block partials, then y[row][c] = min + bias2[c] (16-byte stores when the
+// row length allows).
+template <typename OutT>
+__global__ void __launch_bounds__(256) rowmin_finish_kernel(int C, int n_cb, const float2* __restrict__ part,
+                                                            const float* __restrict__ bias2, OutT* __restrict__ y,
+                                                            int32_t* __restrict__ argmin) {
+    __shared__ float sv[256];
+    __shared__ int si[256];
+    const int row = blockIdx.x;
+    float best = __int_as_float(0x7f800000);
+    int bi = 0x7fffffff;
+    for (int j = threadIdx.x; j < n_cb; j += blockDim.x) {
+        const float2 pv = part[(size_t)row * n_cb + j];
+        const int idx = __float_as_int(pv.y);
+        if (pv.x < best || (pv.x == best && idx < bi)) { best = pv.x; bi = idx; }
+    }
+    sv[threadIdx.x] = best;
+    si[threadIdx.x] = bi;
+    __syncthreads();
+    for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+        if (threadIdx.x < s) {
+            const float ov = sv[threadIdx.x + s];
+            const int oi = si[threadIdx.x + s];
+            if (ov < sv[threadIdx.x] || (ov == sv[threadIdx.x] && oi < si[threadIdx.x])) {
+                sv[threadIdx.x] = ov;
+                si[threadIdx.x] = oi;
+            }
+        }
+        __syncthreads();
+    }
+    const float m = sv[0];
+    if (threadIdx.x == 0 && argmin) argmin[row] = si[0];
+    OutT* dst = y + (size_t)row * C;
+    if (sizeof(OutT) == 4 && (C % 4) == 0 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0 &&
+        (reinterpret_cast<uintptr_t>(bias2) & 15) == 0) {
+        for (int i = threadIdx.x; i < C / 4; i += blockDim.x) {
+            const float4 b = reinterpret_cast<const float4*>(bias2)[i];
+            reinterpret_cast<float4*>(dst)[i] = make_float4(m + b.x, m + b.y, m + b.z, m + b.w);
+        }
+    } else {
+        for (int i = threadIdx.x; i < C; i += blockDim.x) store_out(dst + i, m + bias2[i]);
+    }
+}
+
 // One CTA per output channel co: read the row w[co][*][*] (C_in*k contiguous values) with
 // coalesced loads into shared memory, then write each tap's row wp[kk][co][0..ci_pad) contiguously.
 template <typename InT, typename PackT>
@@ -423,6 +468,17 @@ cudaError_t launch_broadcast(const c1n_params& p, const Plan& pl, const float* r
         else
             broadcast_kernel<float><<<grid_1d(total), 256, 0, stream>>>(a, rowmin, bias2, static_cast<float*>(y));
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rowmin_finish(const c1n_params& p, const Plan& pl, const float2* part, const float* bias2, void* y,
+                                 int32_t* argmin, cudaStream_t stream) {
+    if (pl.bf16)
+        rowmin_finish_kernel<__nv_bfloat16><<<p.N, 256, 0, stream>>>(p.C_out, pl.n_cb, part, bias2,
+                                                                      static_cast<__nv_bfloat16*>(y), argmin);
+    else
+        rowmin_finish_kernel<float><<<p.N, 256, 0, stream>>>(p.C_out, pl.n_cb, part, bias2, static_cast<float*>(y),
+                                                             argmin);
     return cudaGetLastError();
 }
 

@@ -160,6 +160,31 @@ __device__ __forceinline__ void gn_run_sums_any(int sub, uint32_t tb, int ncols,
     else gn_run_sums<1, SQUARED>(tb, ncols, row_ok, shift, red, q, lane);
 }
 
+// GroupNorm of the runs of CPG consecutive channels held by one thread (CPG divides 32): two passes
+// over the registers, population variance, then affine with the per-channel gamma / beta.
+template <int CPG>
+__device__ __forceinline__ void row_group_norm(float (&v)[32], const float* gamma, const float* beta, float eps) {
+#pragma unroll
+    for (int g = 0; g < 32 / CPG; ++g) {
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < CPG; ++i) s += v[g * CPG + i];
+        const float mean = s * (1.f / CPG);
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < CPG; ++i) {
+            const float d = v[g * CPG + i] - mean;
+            ss = fmaf(d, d, ss);
+        }
+        const float rstd = rsqrtf(ss * (1.f / CPG) + eps);
+#pragma unroll
+        for (int i = 0; i < CPG; ++i) {
+            const int c = g * CPG + i;
+            v[c] = fmaf((v[c] - mean) * rstd, gamma[c], beta[c]);
+        }
+    }
+}
+
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -535,6 +560,124 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
+            } else if (EPI == kEpiRowGN) {
+                // ------------------------------------------------ row epilogue (Linear mode)
+                // One thread owns one row (sample) and the channel block's columns: bias, optional
+                // GroupNorm over runs of row_cpg channels, affine, then either GELU + store or a
+                // running minimum (lowest channel on ties) for the row-min post-op.
+                const int co_base = un.cbu * a.BN;
+                const int ncols = min(a.BN, a.C_out - co_base);
+                float* s_gamma = epi + 2304;
+                float* s_beta = epi + 2560;
+                if (co_base != staged_co) {  // uniform over the epilogue threads
+                    named_bar_sync(1, kEpiThreads);
+                    for (int col = er; col < 256; col += kEpiThreads) {
+                        const bool ok = col < ncols;
+                        s_bias[col] = (ok && a.bias) ? __ldg(a.bias + co_base + col) : 0.f;
+                        s_gamma[col] = ok ? (a.gamma ? __ldg(a.gamma + co_base + col) : 1.f) : 0.f;
+                        s_beta[col] = (ok && a.beta) ? __ldg(a.beta + co_base + col) : 0.f;
+                    }
+                    named_bar_sync(1, kEpiThreads);
+                    staged_co = co_base;
+                }
+                const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
+                float best = __int_as_float(0x7f800000);
+                int best_i = 0x7fffffff;
+                OutT* dst = y + (long long)(row_ok ? row : 0) * a.C_out + co_base;
+                for (int j0 = 0; j0 < ncols; j0 += 32) {
+                    float v[32];
+                    tmem_load32(tb + uint32_t(j0), v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] += s_bias[j0 + i];
+                    if (a.row_cpg == 8) row_group_norm<8>(v, s_gamma + j0, s_beta + j0, a.eps);
+                    else if (a.row_cpg == 16) row_group_norm<16>(v, s_gamma + j0, s_beta + j0, a.eps);
+                    else if (a.row_cpg == 32) row_group_norm<32>(v, s_gamma + j0, s_beta + j0, a.eps);
+                    if (a.rowmin) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (j0 + i < ncols && v[i] < best) { best = v[i]; best_i = co_base + j0 + i; }
+                    } else {
+                        if (a.gelu) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+                        }
+                        if (row_ok) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (j0 + i < ncols) store_out(dst + j0 + i, v[i]);
+                        }
+                    }
+                }
+                if (a.rowmin && row_ok)
+                    a.rowpart[(size_t)row * a.n_cb + un.cbu] = make_float2(best, __int_as_float(best_i));
+            } else if (EPI == kEpiLN) {
+                // ------------------------------------------------ channel LayerNorm (conv mode)
+                // All C_out channels of the tile sit in TMEM (cb_per_unit blocks at 256-column
+                // steps); one thread owns one time step: mean, then squared deviations, then
+                // normalize + affine (+ GELU) and store (a warp stores 32 consecutive steps).
+                float* s_gamma = epi + 512;
+                float* s_beta = epi + 1024;
+                if (staged_co < 0) {
+                    for (int c = er; c < 512; c += kEpiThreads) {
+                        const bool ok = c < a.C_out;
+                        epi[c] = (ok && a.bias) ? __ldg(a.bias + c) : 0.f;
+                        s_gamma[c] = ok ? (a.gamma ? __ldg(a.gamma + c) : 1.f) : 0.f;
+                        s_beta[c] = (ok && a.beta) ? __ldg(a.beta + c) : 0.f;
+                    }
+                    named_bar_sync(1, kEpiThreads);
+                    staged_co = 0;
+                }
+                const float* ln_bias = epi;
+                const uint32_t tb0 = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab * a.cb_per_unit);
+                float sum = 0.f;
+                for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
+                    const int cb0 = cbi * a.BN, ncols = min(a.BN, a.C_out - cb0);
+                    for (int j0 = 0; j0 < ncols; j0 += 32) {
+                        float v[32];
+                        tmem_load32(tb0 + uint32_t(256 * cbi + j0), v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (j0 + i < ncols) sum += v[i] + ln_bias[cb0 + j0 + i];
+                    }
+                }
+                const float mean = sum / float(a.C_out);
+                float ss = 0.f;
+                for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
+                    const int cb0 = cbi * a.BN, ncols = min(a.BN, a.C_out - cb0);
+                    for (int j0 = 0; j0 < ncols; j0 += 32) {
+                        float v[32];
+                        tmem_load32(tb0 + uint32_t(256 * cbi + j0), v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (j0 + i < ncols) {
+                                const float d = v[i] + ln_bias[cb0 + j0 + i] - mean;
+                                ss = fmaf(d, d, ss);
+                            }
+                    }
+                }
+                const float rstd = rsqrtf(ss / float(a.C_out) + a.eps);
+                for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
+                    const int cb0 = cbi * a.BN, ncols = min(a.BN, a.C_out - cb0);
+                    OutT* dst = y + ((long long)un.n * a.C_out + cb0) * a.T_out + row;
+                    for (int j0 = 0; j0 < ncols; j0 += 32) {
+                        float v[32];
+                        tmem_load32(tb0 + uint32_t(256 * cbi + j0), v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int c = cb0 + j0 + i;
+                            v[i] = fmaf((v[i] + ln_bias[c] - mean) * rstd, s_gamma[c], s_beta[c]);
+                        }
+                        if (a.gelu) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+                        }
+                        if (row_ok) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (j0 + i < ncols) store_out(dst + (long long)(j0 + i) * a.T_out, v[i]);
+                        }
+                    }
+                }
             } else {
                 // ------------------------------------------------ fused GroupNorm (conv mode)
                 // The CTAs of one (sample, channel block) together cover all T_out steps. Each
@@ -764,9 +907,17 @@ cudaError_t launch_tc(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, 
                       cudaStream_t stream) {
 #define C1N_LAUNCH(L, B, O, E) launch_one<L, B, O, E>(pl, a, tm_a, tm_b, tm_y, num_sms, stream)
     if (linear) {
+        if (epilogue == kEpiRowGN) {
+            if (pl.bf16) return C1N_LAUNCH(true, true, __nv_bfloat16, kEpiRowGN);
+            return C1N_LAUNCH(true, false, float, kEpiRowGN);
+        }
         if (pl.bf16 && out_bf16) return C1N_LAUNCH(true, true, __nv_bfloat16, kEpiDirect);
         if (pl.bf16) return C1N_LAUNCH(true, true, float, kEpiDirect);
         return C1N_LAUNCH(true, false, float, kEpiDirect);
+    }
+    if (epilogue == kEpiLN) {
+        if (pl.bf16) return C1N_LAUNCH(false, true, __nv_bfloat16, kEpiLN);
+        return C1N_LAUNCH(false, false, float, kEpiLN);
     }
     if (epilogue == kEpiClusterGN) {
         if (pl.bf16) return C1N_LAUNCH(false, true, __nv_bfloat16, kEpiClusterGN);

@@ -79,8 +79,13 @@ typedef enum {
                                      else through distributed shared memory inside a thread-block
                                      cluster), then normalize their tiles in place and store once */
     C1N_PATH_TC_TWO_PASS = 3,     /* tcgen05 conv writes raw tiles, then statistics + normalize pass */
-    C1N_PATH_TC_LINEAR = 4,       /* T = 1, k = 1: tcgen05 GEMM (rows x out), then the norm/post passes */
-    C1N_PATH_TC_FUSED_GN_DSMEM = 5 /* as TC_FUSED_GN, always through a thread-block cluster (DSMEM) */
+    C1N_PATH_TC_LINEAR = 4,       /* T = 1, k = 1: tcgen05 GEMM (rows x out); GroupNorm over groups of
+                                     8/16/32 channels, affine, GELU or row-min fused in the epilogue
+                                     (row-min then needs one finisher kernel); other shapes use the
+                                     statistics / normalize / row-min passes */
+    C1N_PATH_TC_FUSED_GN_DSMEM = 5, /* as TC_FUSED_GN, always through a thread-block cluster (DSMEM) */
+    C1N_PATH_TC_FUSED_LN = 6      /* tcgen05 conv with channel LayerNorm (+ GELU) fused: one CTA holds
+                                     all C_out <= 512 channels of a 128-step tile in TMEM */
 } c1n_path;
 
 typedef struct {

@@ -113,7 +113,15 @@ SMALL = {
     "linear_rowmin": synth.LINEAR_GN_ROWMIN.replace(N=200, C_in=72, C_out=320, groups=20),
     "linear_plain": synth.LINEAR_GN_ROWMIN.replace(N=130, C_in=64, C_out=96, norm=synth.NORM_NONE,
                                                    post=synth.POST_NONE),
+    "linear_gn_gelu": synth.LINEAR_GN_ROWMIN.replace(N=150, C_in=96, C_out=512, groups=64, post=synth.POST_GELU_ERF),
+    "linear_gn_cpg32_bf16": synth.LINEAR_GN_ROWMIN.replace(N=140, C_in=128, C_out=256, groups=8,
+                                                           post=synth.POST_NONE, dtype=synth.DTYPE_BF16),
+    "linear_rowmin_nonorm": synth.LINEAR_GN_ROWMIN.replace(N=70, C_in=64, C_out=288, norm=synth.NORM_NONE),
+    "linear_gn_cpg4_twopass": synth.LINEAR_GN_ROWMIN.replace(N=66, C_in=32, C_out=96, groups=24),
     "ln_gelu_bf16": synth.CONV_LN_GELU_BF16.replace(N=2, C_in=48, C_out=160, T=264),
+    "ln_c384_f32": synth.CONV_LN_GELU_BF16.replace(N=2, C_in=40, C_out=384, T=200, dtype=synth.DTYPE_F32,
+                                                   post=synth.POST_NONE),
+    "ln_c512_bf16": synth.CONV_LN_GELU_BF16.replace(N=2, C_in=64, C_out=512, T=320),
     "gn_bf16": synth.CONV_GN.replace(N=2, C_in=64, C_out=128, T=512, groups=16, dtype=synth.DTYPE_BF16),
     "conv_bf16": synth.CAUSAL_CONV.replace(N=2, C_in=72, C_out=136, T=400, dtype=synth.DTYPE_BF16),
     "stride2_simt": synth.CONV_GN.replace(N=2, C_in=16, C_out=32, T=101, stride=2, groups=8),
@@ -157,6 +165,27 @@ def test_group_norm_cluster_exchange_forced(cuda_lib, name):
     ref, _ = oracle_full(wl, inp)
     y, am, path = run_gpu(cuda_lib, wl, inp, force_path=cuda_lib.PATH_TC_FUSED_GN_DSMEM)
     assert path == "tc_fused_gn_dsmem"
+    compare(wl, y, am, ref, None, path, name)
+
+
+@pytest.mark.parametrize("name", ["ln_gelu_bf16", "ln_c384_f32"])
+def test_layer_norm_two_pass_forced(cuda_lib, name):
+    wl = SMALL[name]
+    inp = _inputs(wl)
+    ref, _ = oracle_full(wl, inp)
+    y, am, path = run_gpu(cuda_lib, wl, inp, force_path=cuda_lib.PATH_TC_TWO_PASS)
+    assert path == "tc_two_pass"
+    compare(wl, y, am, ref, None, path, name)
+
+
+@pytest.mark.parametrize("name", ["ln_gelu_bf16", "ln_c384_f32", "ln_c512_bf16"])
+def test_layer_norm_fused_forced(cuda_lib, name):
+    # the whole channel row of a tile (up to 512 channels) normalized in the tensor-core epilogue
+    wl = SMALL[name]
+    inp = _inputs(wl)
+    ref, _ = oracle_full(wl, inp)
+    y, am, path = run_gpu(cuda_lib, wl, inp, force_path=cuda_lib.PATH_TC_FUSED_LN)
+    assert path == "tc_fused_ln"
     compare(wl, y, am, ref, None, path, name)
 
 
@@ -228,8 +257,11 @@ def test_conv_ln_gelu_bf16_full_sampled(cuda_lib):
     wl = synth.CONV_LN_GELU_BF16
     inp = _inputs(wl)
     y, _, path = run_gpu(cuda_lib, wl, inp)
+    y2, _, path2 = run_gpu(cuda_lib, wl, inp, force_path=cuda_lib.PATH_TC_FUSED_LN)
+    assert path2 == "tc_fused_ln"
     ns = [0, wl.N - 1]
     ref, _ = oracle.conv1d_norm_samples(oracle.params_of(wl), ns, inp["x"], inp["w"], inp["b"], inp["gamma"],
                                         inp["beta"])
     compare(wl, y[ns], None, ref, None, path, wl.name)
-    assert np.all(np.isfinite(y))
+    compare(wl, y2[ns], None, ref, None, path2, wl.name + " (fused LayerNorm)")
+    assert np.all(np.isfinite(y)) and np.all(np.isfinite(y2))

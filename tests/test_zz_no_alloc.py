@@ -17,9 +17,9 @@ pytestmark = pytest.mark.gpu
 TOL_TF32 = 5e-3  # the tensor-core fp32 tolerance the parity tests use
 
 
-def _params(c1n, wl):
+def _params(c1n, wl, force_path=-1):
     return c1n.make_params(wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right, wl.dilation,
-                           wl.norm, wl.groups, wl.eps, wl.post, wl.dtype)
+                           wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, force_path=force_path)
 
 
 def test_static_scratch_matches_regular_entry_point_twice(cuda_lib):
@@ -54,7 +54,7 @@ def test_static_scratch_matches_regular_entry_point_twice(cuda_lib):
 def test_static_scratch_rejects_operators_that_need_more(cuda_lib):
     c1n = cuda_lib
     wl = synth.CONV_LN_GELU_BF16  # its two-pass plan keeps a raw fp32 copy of y in the workspace
-    desc = c1n.conv1d_norm_desc_create(_params(c1n, wl))
+    desc = c1n.conv1d_norm_desc_create(_params(c1n, wl, force_path=c1n.PATH_TC_TWO_PASS))
     try:
         assert c1n.conv1d_norm_workspace_size(desc) > c1n.STATIC_SCRATCH_BYTES
         buf = torch.zeros(16, dtype=torch.float32, device="cuda")
