@@ -19,6 +19,7 @@ NORM_NONE, NORM_GROUP, NORM_CHANNEL_LAYER = 0, 1, 2
 POST_NONE, POST_GELU_ERF, POST_ROWMIN_BIAS = 0, 1, 2
 F32, BF16 = 0, 1
 MATH_AUTO, MATH_SIMT, MATH_TENSOR = 0, 1, 2
+MAINLOOP_AUTO, MAINLOOP_SINGLE, MAINLOOP_PAIR = 0, 1, 2
 PATH_AUTO, PATH_SIMT, PATH_TC_DIRECT, PATH_TC_FUSED_GN, PATH_TC_TWO_PASS, PATH_TC_LINEAR = -1, 0, 1, 2, 3, 4
 PATH_TC_FUSED_GN_DSMEM, PATH_TC_FUSED_LN = 5, 6
 PATH_NAMES = {0: "simt", 1: "tc_direct", 2: "tc_fused_gn", 3: "tc_two_pass", 4: "tc_linear", 5: "tc_fused_gn_dsmem",
@@ -38,12 +39,13 @@ STATIC_SCRATCH_BYTES = 4 << 20  # C1N_STATIC_SCRATCH_BYTES
 class Params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("N", "C_in", "C_out", "T", "k", "stride", "pad_left", "pad_right", "dilation", "norm", "groups")]
-    _fields_ += [("eps", ctypes.c_float)] + [(n, ctypes.c_int32) for n in ("post", "dtype", "math", "force_path")]
+    _fields_ += [("eps", ctypes.c_float)] + [(n, ctypes.c_int32) for n in ("post", "dtype", "math", "force_path",
+                                                                          "mainloop")]
 
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("path", "T_out", "tile_t", "tile_co", "mma_n", "cluster", "n_tiles", "grid", "kernels", "reserved")]
+                ("path", "T_out", "tile_t", "tile_co", "mma_n", "cluster", "n_tiles", "grid", "kernels", "cta_pair")]
     _fields_ += [("workspace_bytes", ctypes.c_int64)]
 
 
@@ -123,9 +125,10 @@ def _check(status: int):
 # ------------------------------------------------------------------------------ C-named wrappers
 
 def make_params(N, C_in, C_out, T, k, stride=1, pad_left=0, pad_right=0, dilation=1, norm=NORM_NONE, groups=1,
-                eps=1e-5, post=POST_NONE, dtype=F32, math=MATH_AUTO, force_path=PATH_AUTO) -> Params:
+                eps=1e-5, post=POST_NONE, dtype=F32, math=MATH_AUTO, force_path=PATH_AUTO,
+                mainloop=MAINLOOP_AUTO) -> Params:
     return Params(N, C_in, C_out, T, k, stride, pad_left, pad_right, dilation, norm, groups, eps, post, dtype, math,
-                  force_path)
+                  force_path, mainloop)
 
 
 def conv1d_norm_desc_create(params: Params) -> int:

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -121,10 +122,15 @@ void plan_stages(Plan& pl, int max_a, int max_b, int max_s) {
     pl.smem_bytes = 1024 + total() + kTcMiscBytes;
 }
 
-// Geometry of the tensor-core conv tiles: 128 output time steps x BN channels per tile; the A tile
-// carries the (k-1)*dilation halo rows. `cluster` selects one CTA per tile with single-buffered
-// TMEM (cluster GroupNorm) instead of the persistent double-buffered layout.
-bool plan_tc_geometry(const c1n_params& p, Plan& pl, bool cluster) {
+// CTA pairs (cta_group::2) need an MMA N that splits into two halves of whole 16-row groups, and
+// are used unless the caller asked for single CTAs.
+bool pair_ok(const c1n_params& p, const Plan& pl) { return p.mainloop != C1N_MAINLOOP_SINGLE && pl.BN % 32 == 0; }
+
+// Geometry of the tensor-core conv tiles: 128 output time steps x BN channels per tile (256 steps
+// for a CTA pair, 128 per CTA); the A tile carries the (k-1)*dilation halo rows. `cluster` selects
+// one CTA per tile with single-buffered TMEM (cluster GroupNorm) instead of the persistent
+// double-buffered layout.
+bool plan_tc_geometry(const c1n_params& p, Plan& pl, bool cluster, bool pair = false) {
     pl.BK = pl.bf16 ? 64 : 32;
     const long long halo = (long long)(p.k - 1) * p.dilation;
     pl.R = (int)round_up(128 + halo, 8);
@@ -139,8 +145,10 @@ bool plan_tc_geometry(const c1n_params& p, Plan& pl, bool cluster) {
     pl.n_ci_chunks = (int)ceil_div(p.C_in, pl.BK);
     pl.ci_pad = pl.n_ci_chunks * pl.BK;
     plan_channel_blocks(p, pl);
+    pl.pair = (pair && !cluster && pair_ok(p, pl)) ? 1 : 0;
+    if (pl.pair) pl.b_slot_bytes = pl.BN / 2 * 128;
     pl.cb_per_unit = 1;
-    pl.n_t_tiles = (int)ceil_div(pl.T_out, 128);
+    pl.n_t_tiles = (int)ceil_div(pl.T_out, pl.pair ? 256 : 128);
     pl.n_units = p.N * pl.n_t_tiles * pl.n_cb;
     if (cluster) {
         pl.n_acc = 1;
@@ -149,7 +157,8 @@ bool plan_tc_geometry(const c1n_params& p, Plan& pl, bool cluster) {
         pl.n_acc = 2;
         pl.tmem_cols = 512;
     }
-    plan_stages(pl, 2, 4, 4);
+    if (pl.pair) plan_stages(pl, 2, 8, 3);  // half-size B slots: a deeper weight ring
+    else plan_stages(pl, 2, 4, 4);
     return pl.smem_bytes <= 227 * 1024;
 }
 
@@ -160,14 +169,21 @@ bool plan_tc_linear(const c1n_params& p, Plan& pl) {
     pl.n_ci_chunks = (int)ceil_div(p.C_in, pl.BK);
     pl.ci_pad = 0;
     plan_channel_blocks(p, pl);
+    pl.pair = pair_ok(p, pl) ? 1 : 0;
+    if (pl.pair) pl.b_slot_bytes = pl.BN / 2 * 128;
     pl.cb_per_unit = 1;
-    pl.n_t_tiles = (int)ceil_div(p.N, 128);  // row tiles
+    pl.n_t_tiles = (int)ceil_div(p.N, pl.pair ? 256 : 128);  // row tiles
     pl.n_units = pl.n_t_tiles * pl.n_cb;
     pl.n_acc = 2;
     pl.tmem_cols = 512;
     pl.s_slot_bytes = 0;
-    plan_stages(pl, 4, 4, 0);
-    return pl.smem_bytes <= 227 * 1024;
+    // one ring: stage i holds A chunk i and B chunk i (one full / empty barrier pair)
+    const int budget = 227 * 1024 - 1024 - kTcMiscBytes;
+    const int stages = std::min(8, budget / (pl.a_slot_bytes + pl.b_slot_bytes));
+    pl.stages_a = pl.stages_b = stages;
+    pl.stages_s = 0;
+    pl.smem_bytes = 1024 + stages * (pl.a_slot_bytes + pl.b_slot_bytes) + kTcMiscBytes;
+    return stages >= 2 && pl.smem_bytes <= 227 * 1024;
 }
 
 c1n_status make_plan(const c1n_params& p, Plan& pl) {
@@ -268,7 +284,7 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
             if (!*why && p.norm == C1N_NORM_CHANNEL_LAYER && p.post != C1N_POST_ROWMIN_BIAS && p.C_out <= 512 &&
                 (want == C1N_PATH_TC_FUSED_LN || (want == C1N_PATH_AUTO && p.C_out <= 256))) {
                 Plan ln = pl;
-                if (plan_tc_geometry(p, ln, false)) {
+                if (plan_tc_geometry(p, ln, false, true)) {
                     ln.cb_per_unit = ln.n_cb;
                     ln.n_units = p.N * ln.n_t_tiles;
                     ln.n_acc = ln.n_cb == 1 ? 2 : 1;  // two accumulators only when they fit in TMEM
@@ -285,7 +301,7 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
             // 2. Direct epilogue (no normalization).
             if (!*why && p.norm == C1N_NORM_NONE && p.post != C1N_POST_ROWMIN_BIAS &&
                 (want == C1N_PATH_AUTO || want == C1N_PATH_TC_DIRECT)) {
-                if (plan_tc_geometry(p, pl, false)) {
+                if (plan_tc_geometry(p, pl, false, true)) {
                     pl.path = C1N_PATH_TC_DIRECT;
                     plan_workspace(p, pl, true, false, false);
                     pl.kernels = 2;
@@ -297,7 +313,7 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
             }
             // 3. Two passes: raw tiles, then statistics and normalize / row-min passes.
             if (!*why && (want == C1N_PATH_AUTO || want == C1N_PATH_TC_TWO_PASS)) {
-                if (plan_tc_geometry(p, pl, false)) {
+                if (plan_tc_geometry(p, pl, false, true)) {
                     pl.path = C1N_PATH_TC_TWO_PASS;
                     const bool need_stats = p.norm != C1N_NORM_NONE;
                     const bool need_raw = out_needs_second_pass && pl.bf16;
@@ -325,6 +341,7 @@ c1n_status validate(const c1n_params* p) {
     if (p->dtype < 0 || p->dtype > 1) return fail(C1N_ERR_INVALID_ARG, "unknown dtype %d", p->dtype);
     if (p->math < 0 || p->math > 2) return fail(C1N_ERR_INVALID_ARG, "unknown math %d", p->math);
     if (p->force_path < -1 || p->force_path > 6) return fail(C1N_ERR_INVALID_ARG, "unknown path %d", p->force_path);
+    if (p->mainloop < 0 || p->mainloop > 2) return fail(C1N_ERR_INVALID_ARG, "unknown mainloop %d", p->mainloop);
     if (p->norm == C1N_NORM_GROUP && (p->groups < 1 || p->C_out % p->groups != 0))
         return fail(C1N_ERR_INVALID_ARG, "GroupNorm needs groups >= 1 dividing C_out (%d %% %d)", p->C_out, p->groups);
     if (p->norm != C1N_NORM_NONE && !(std::isfinite(p->eps) && p->eps > 0.f))
@@ -439,7 +456,8 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
                 if (st != C1N_OK) return st;
                 cuuint64_t dw[2] = {(cuuint64_t)p.C_in, (cuuint64_t)p.C_out};
                 cuuint64_t sw[1] = {(cuuint64_t)p.C_in * es};
-                cuuint32_t bw[2] = {(cuuint32_t)pl.BK, (cuuint32_t)pl.BN};
+                // (a CTA pair: each CTA loads BN/2 of the BN rows)
+                cuuint32_t bw[2] = {(cuuint32_t)pl.BK, (cuuint32_t)(pl.pair ? pl.BN / 2 : pl.BN)};
                 st = encode(&d->tm_b, wsrc, pl.bf16, 2, dw, sw, bw);
                 if (st != C1N_OK) return st;
             } else {
@@ -447,7 +465,7 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
                 // (A is written by the kernel's transposer warps; its map slot repeats B's.)
                 cuuint64_t dw[3] = {(cuuint64_t)pl.ci_pad, (cuuint64_t)p.C_out, (cuuint64_t)p.k};
                 cuuint64_t sw[2] = {(cuuint64_t)pl.ci_pad * es, (cuuint64_t)pl.ci_pad * p.C_out * es};
-                cuuint32_t bw[3] = {(cuuint32_t)pl.BK, (cuuint32_t)pl.BN, 1};
+                cuuint32_t bw[3] = {(cuuint32_t)pl.BK, (cuuint32_t)(pl.pair ? pl.BN / 2 : pl.BN), 1};
                 st = encode(&d->tm_b, wsrc, pl.bf16, 3, dw, sw, bw);
                 if (st != C1N_OK) return st;
                 // A source: x[n][ci][t], box = RS time steps x BK channels x 1 sample, unswizzled
@@ -499,7 +517,7 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         t.gelu = (p.post == C1N_POST_GELU_ERF && (pl.path == C1N_PATH_TC_DIRECT || fused_gn || fused_ln ||
                                                   pl.row_epilogue)) ? 1 : 0;
         const uint32_t fmt = pl.bf16 ? 1u : 2u;
-        t.idesc = make_idesc(fmt, fmt, 0u, 0u, 128u, (uint32_t)pl.BN);
+        t.idesc = make_idesc(fmt, fmt, 0u, 0u, pl.pair ? 256u : 128u, (uint32_t)pl.BN);
         t.x = a->x;
         t.bias = a->b;
         t.gamma = a->gamma;
@@ -562,6 +580,8 @@ c1n_status conv1d_norm_desc_create(const c1n_params* params, c1n_desc** out) {
     Plan pl;
     st = make_plan(*params, pl);
     if (st != C1N_OK) return st;
+    if (params->mainloop == C1N_MAINLOOP_PAIR && !pl.pair)
+        return fail(C1N_ERR_UNSUPPORTED, "the chosen plan (path %d, MMA N %d) cannot run on CTA pairs", pl.path, pl.BN);
     c1n_desc* d = new (std::nothrow) c1n_desc();
     if (!d) return fail(C1N_ERR_INVALID_ARG, "out of host memory");
     d->p = *params;
@@ -593,13 +613,14 @@ c1n_status conv1d_norm_plan_info(const c1n_desc* desc, c1n_plan_info* info) {
     std::memset(info, 0, sizeof(*info));
     info->path = pl.path;
     info->T_out = (int32_t)pl.T_out;
-    info->tile_t = pl.path == C1N_PATH_SIMT ? 64 : 128;
+    info->tile_t = pl.path == C1N_PATH_SIMT ? 64 : (pl.pair ? 256 : 128);
     info->tile_co = pl.path == C1N_PATH_SIMT ? 64 : pl.BN;
     info->mma_n = pl.path == C1N_PATH_SIMT ? 0 : pl.BN;
     info->cluster = pl.cluster;
     info->n_tiles = pl.path == C1N_PATH_SIMT ? pl.n_units : pl.n_units;
     info->grid = pl.grid;
     info->kernels = pl.kernels;
+    info->cta_pair = pl.pair;
     info->workspace_bytes = (int64_t)pl.ws_total;
     return C1N_OK;
 }
@@ -684,6 +705,6 @@ const char* conv1d_norm_status_string(c1n_status s) {
 
 const char* conv1d_norm_last_error(void) { return g_last_error.c_str(); }
 
-int32_t conv1d_norm_version(void) { return 100; }
+int32_t conv1d_norm_version(void) { return 110; }
 
 }  // extern "C"

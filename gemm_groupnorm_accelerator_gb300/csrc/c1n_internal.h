@@ -30,11 +30,12 @@ struct Plan {
     int cb_per_unit = 1;  // channel blocks accumulated by one work unit
     int n_ci_chunks = 0;
     int ci_pad = 0;       // packed-weight row length (multiple of BK)
-    int n_t_tiles = 0;    // 128-row tiles along time (conv) or rows (Linear)
+    int n_t_tiles = 0;    // row tiles along time (conv) or rows (Linear): 128 rows, 256 with a CTA pair
     int n_units = 0;
     int n_acc = 2;        // accumulators per CTA (2: epilogue overlaps the next mainloop)
     int tmem_cols = 512;  // TMEM columns allocated per CTA
     int cluster = 1;
+    int pair = 0;         // CTA-pair mainloop (cta_group::2): units of 256 rows, each CTA loads half of B
     int grid = 0;
     int stages_a = 0, stages_b = 0, stages_s = 0;
     int a_slot_bytes = 0, b_slot_bytes = 0, s_slot_bytes = 0;
@@ -91,11 +92,11 @@ cudaError_t launch_rowmin(const c1n_params& p, const Plan& pl, const float* raw,
                           cudaStream_t stream);
 cudaError_t launch_broadcast(const c1n_params& p, const Plan& pl, const float* rowmin, const float* bias2, void* y,
                              cudaStream_t stream);
-// Also zeroes `nzero` words at `zero` (the fused-GroupNorm arrival counters) when given.
 // Row-min finisher: per row, the minimum (lowest channel on ties) over the per-block partials,
 // then y[row][c] = min + bias2[c]; argmin optional.
 cudaError_t launch_rowmin_finish(const c1n_params& p, const Plan& pl, const float2* part, const float* bias2, void* y,
                                  int32_t* argmin, cudaStream_t stream);
+// Also zeroes `nzero` words at `zero` (the fused-GroupNorm arrival counters) when given.
 cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream,
                                 unsigned* zero = nullptr, int nzero = 0);
 

@@ -36,6 +36,11 @@ __device__ __forceinline__ void fence_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Same ordering for every state space (shared memory that another CTA's tensor core will read).
+__device__ __forceinline__ void fence_async_all() {
+    asm volatile("fence.proxy.async;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
@@ -86,6 +91,49 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
     }
 }
 
+// Arrive on an mbarrier in another CTA of the cluster (`bar` is a shared::cluster address from
+// mapa); release at cluster scope, so the arriving thread's earlier writes are visible to a thread
+// of the peer that observes the phase.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait for barriers that also collect arrivals from the peer CTA of a pair (acquire at
+// cluster scope); same limit and error reporting.
+static __device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                      int* status, int where, const volatile int* prog = nullptr) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                if (status != nullptr && atomicCAS(status, 0, 6 /* C1N_ERR_TIMEOUT */) == 0) {
+                    atomicExch(status + 1, where);
+                    atomicExch(status + 2, int(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)));
+                    if (prog != nullptr)
+                        for (int i = 0; i < kProgSlots; ++i) atomicExch(status + 3 + i, prog[i]);
+                }
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
@@ -103,6 +151,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
                                             int c2) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// Pair forms: the copy lands in this CTA's shared memory and its byte count is signalled on `bar`,
+// which may sit in the peer CTA of the pair (a shared::cluster address from mapa).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1,
+                                                 int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
@@ -158,6 +223,55 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
+// ---- CTA-pair forms (cta_group::2). A kernel uses either these or the single-CTA forms above for
+// every tcgen05 instruction, never both. The pair is CTA ranks {2p, 2p+1} of the cluster: the
+// even CTA issues the MMAs; A rows 0-127 and accumulator lanes come from / go to the even CTA, rows
+// 128-255 from / to the odd one; B columns [0, N/2) are read from the even CTA's shared memory and
+// [N/2, N) from the odd CTA's, both at the same shared-memory offsets.
+
+// Both CTAs of the pair issue this from the same warp; the columns are allocated in both TMEMs.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the barrier at offset `bar` in every CTA of `cta_mask` when the pair MMAs issued
+// so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(bar), "h"(cta_mask)
+        : "memory");
+}
+
 // Load 16 consecutive 32-bit columns of this warp's 32 TMEM lanes (one lane per thread) and wait
 // for the load in the same statement, so no use of the registers can be scheduled before the wait.
 __device__ __forceinline__ void tmem_load16(uint32_t taddr, float (&v)[16]) {
@@ -205,6 +319,32 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05
     d |= static_cast<uint64_t>(2) << 61;  // SWIZZLE_128B
     return d;
+}
+
+// The two words of smem_desc_sw128(addr, 16, 1024): the low word carries the start address
+// (bits 0-13, 16-byte units) and the leading byte offset; the high word is the same for every
+// operand slot of the kernel (stride byte offset 1024, version 1, 128-byte swizzle).
+constexpr uint32_t kDescHiSw128 = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t desc_lo_sw128(uint32_t saddr) { return ((saddr >> 4) & 0x3FFFu) | (1u << 16); }
+
+// One MMA from descriptor low words (high word kDescHiSw128): tf32 or bf16 operands, one CTA or
+// a CTA pair.
+template <bool BF16, bool PAIR>
+__device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                          uint32_t accumulate) {
+#define C1N_MMA_ASM(KIND, GROUP)                                                                   \
+    asm volatile("{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"                                   \
+                 "setp.ne.b32 p, %4, 0;\n\t"                                                        \
+                 "mov.b64 ad, {%1, %5};\n\t"                                                        \
+                 "mov.b64 bd, {%2, %5};\n\t"                                                        \
+                 "tcgen05.mma." GROUP ".kind::" KIND " [%0], ad, bd, %3, p;\n\t}"                   \
+                 ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kDescHiSw128) \
+                 : "memory")
+    if constexpr (BF16 && PAIR) C1N_MMA_ASM("f16", "cta_group::2");
+    else if constexpr (BF16) C1N_MMA_ASM("f16", "cta_group::1");
+    else if constexpr (PAIR) C1N_MMA_ASM("tf32", "cta_group::2");
+    else C1N_MMA_ASM("tf32", "cta_group::1");
+#undef C1N_MMA_ASM
 }
 
 // Instruction descriptor for kind::tf32 / kind::f16 with fp32 accumulation.

@@ -208,27 +208,33 @@ struct Unit {
     int cbu;   // index of the channel-block group
 };
 
-template <bool LINEAR>
-__device__ __forceinline__ Unit decode_unit(const TcArgs& a, int u) {
+// A unit covers 128 rows (one CTA) or 256 rows (a CTA pair; `rank` selects the CTA's half).
+// Linear mode walks the row tiles fastest, so the CTAs running at the same time share weight
+// blocks in L2; conv mode walks the channel blocks fastest, so they share the x tile.
+template <bool LINEAR, bool PAIR>
+__device__ __forceinline__ Unit decode_unit(const TcArgs& a, int u, uint32_t rank) {
     Unit r;
-    const int n_cbu = a.n_cb / a.cb_per_unit;
-    r.cbu = u % n_cbu;
-    const int rest = u / n_cbu;
+    constexpr int kRows = PAIR ? 256 : 128;
     if (LINEAR) {
         r.n = 0;
-        r.row0 = rest * 128;
+        r.row0 = (u % a.n_t_tiles) * kRows + 128 * int(rank);
+        r.cbu = u / a.n_t_tiles;
     } else {
-        r.row0 = (rest % a.n_t_tiles) * 128;
+        const int n_cbu = a.n_cb / a.cb_per_unit;
+        r.cbu = u % n_cbu;
+        const int rest = u / n_cbu;
+        r.row0 = (rest % a.n_t_tiles) * kRows + 128 * int(rank);
         r.n = rest / a.n_t_tiles;
     }
     return r;
 }
 
-template <bool LINEAR, bool BF16, typename OutT, int EPI>
+template <bool LINEAR, bool BF16, typename OutT, int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_conv_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tm_a,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_y) {
     constexpr bool kFusedGN = EPI == kEpiClusterGN || EPI == kEpiGridGN;
+    static_assert(!(PAIR && kFusedGN), "the fused GroupNorm grid / cluster exchange runs one CTA per tile");
     using InT = typename std::conditional<BF16, __nv_bfloat16, float>::type;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -250,14 +256,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     // [8] transposer warp 0, [9] TMA; [10] MMA unit, [11] MMA ring indices (ai, aph, bi, bph).
     volatile int* prog = reinterpret_cast<volatile int*>(tmem_slot + 2);
     float* epi = reinterpret_cast<float*>(misc + 1024);  // epilogue scratch (kTcMiscBytes - 1024 bytes)
-    auto bar = [&](int i) { return smem_u32(bars + i); };
+    const uint32_t bars_u32 = smem_u32(bars);
+    auto bar = [&](int i) { return bars_u32 + 8u * uint32_t(i); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int taps = LINEAR ? 1 : a.k;
+    // CTA pair (cta_group::2): rank 0 issues the MMAs over both CTAs' operands and owns the
+    // full / accumulator-empty barriers; rank 1 signals those through the cluster.
+    const uint32_t rank = PAIR ? (cluster_ctarank() & 1u) : 0u;
+    const bool leader = rank == 0;
+    // Bounded wait with an inline first test (the common case in a full pipeline costs no call).
+    auto wait_bar = [&](int i, uint32_t parity, int site) -> bool {
+        if constexpr (PAIR) {
+            if (mbar_try_wait_cluster(bar(i), parity)) return true;
+            return mbar_wait_cluster(bar(i), parity, abort_flag, a.status, site, prog);
+        } else {
+            if (mbar_try_wait(bar(i), parity)) return true;
+            return mbar_wait(bar(i), parity, abort_flag, a.status, site, prog);
+        }
+    };
+    auto leader_bar = [&](int i) -> uint32_t {
+        if constexpr (PAIR) return map_shared_rank(bar(i), 0);
+        else return bar(i);
+    };
+    auto arrive_leader = [&](int i) {
+        if (PAIR && !leader) mbar_arrive_cluster(leader_bar(i));
+        else mbar_arrive(bar(i));
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < SA; ++i) {
-            mbar_init(bar(i_afull + i), LINEAR ? 1 : kXpWarps);  // TMA arrive, or one per transposer warp
+            // TMA arrive, or one per transposer warp (of both CTAs of a pair)
+            mbar_init(bar(i_afull + i), LINEAR ? 1 : (PAIR ? 2 : 1) * kXpWarps);
             mbar_init(bar(i_aempty + i), 1);
         }
         for (int i = 0; i < SB; ++i) {
@@ -266,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(i_accfull + i), 1);
-            mbar_init(bar(i_accempty + i), 4);  // one arrival per epilogue warp
+            mbar_init(bar(i_accempty + i), PAIR ? 8 : 4);  // one arrival per epilogue warp (of the pair)
         }
         mbar_init(bar(i_drain), 1);
         for (int i = 0; i < SS; ++i) {
@@ -280,11 +310,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tm_b);
     }
     if (warp == kWarpMma) {
-        tmem_alloc(smem_u32(tmem_slot), uint32_t(a.tmem_cols));
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), uint32_t(a.tmem_cols));
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), uint32_t(a.tmem_cols));
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if (PAIR) cluster_sync_all();  // the peer's barriers are initialized before any remote arrival
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -292,6 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kFusedGN) {
         first_unit = (blockIdx.z * a.n_t_tiles + blockIdx.x) * (a.n_cb / a.cb_per_unit) + blockIdx.y;
         unit_step = a.n_units;  // exactly one unit
+    } else if (PAIR) {
+        first_unit = blockIdx.x >> 1;  // one unit per CTA pair (cluster of two)
+        unit_step = gridDim.x >> 1;
     } else {
         first_unit = blockIdx.x;
         unit_step = gridDim.x;
@@ -299,102 +338,123 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kWarpTma) {
         // ---------------------------------------------------------------- TMA producer
+        // Linear mode: one ring of stages, each holding the A and the B chunk of one K step under
+        // one full / empty barrier pair. Conv mode: the B (weight) ring only; A comes from the
+        // transposer warps. A pair's full barriers (in the leader) expect both CTAs' bytes; each
+        // CTA loads its own 128 rows of A and its half (BN/2 channels) of the B tile.
         if (lane == 0) {
-            int ai = 0, bi = 0;
-            uint32_t aph = 0, bph = 0;
-            long long a_cnt = 0, b_cnt = 0;
+            int bi = 0;
+            uint32_t bph = 0;
+            long long b_cnt = 0;
+            const uint32_t tx_mult = PAIR ? 2u : 1u;
+            const uint32_t tx_stage = tx_mult * uint32_t(a.b_slot_bytes + (LINEAR ? a.a_slot_bytes : 0));
+            const int co_half = PAIR ? int(rank) * (a.BN / 2) : 0;
             for (int u = first_unit; u < a.n_units && !*abort_flag; u += unit_step) {
-                const Unit un = decode_unit<LINEAR>(a, u);
+                const Unit un = decode_unit<LINEAR, PAIR>(a, u, rank);
                 for (int c = 0; c < a.n_ci_chunks; ++c) {
-                    if (LINEAR) {
-                        if (!mbar_wait(bar(i_aempty + ai), aph ^ 1, abort_flag, a.status, kWaitAEmpty, prog)) goto tma_done;
-                        mbar_arrive_expect_tx(bar(i_afull + ai), uint32_t(a.a_slot_bytes));
-                        tma_load_2d(sA + ai * a.a_slot_bytes, &tm_a, bar(i_afull + ai), c * a.BK, un.row0);
-                        ++a_cnt;
-                        prog[5] = int(a_cnt);
-                        if (++ai == SA) { ai = 0; aph ^= 1; }
-                    }
                     for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
-                        const int co0 = (un.cbu * a.cb_per_unit + cbi) * a.BN;
+                        const int co0 = (un.cbu * a.cb_per_unit + cbi) * a.BN + co_half;
                         for (int kk = 0; kk < taps; ++kk) {
-                            prog[9] = kWaitBEmpty;
-                            if (!mbar_wait(bar(i_bempty + bi), bph ^ 1, abort_flag, a.status, kWaitBEmpty, prog)) goto tma_done;
-                            prog[9] = 0;
-                            mbar_arrive_expect_tx(bar(i_bfull + bi), uint32_t(a.b_slot_bytes));
-                            if (LINEAR)
-                                tma_load_2d(sB + bi * a.b_slot_bytes, &tm_b, bar(i_bfull + bi), c * a.BK, co0);
-                            else
-                                tma_load_3d(sB + bi * a.b_slot_bytes, &tm_b, bar(i_bfull + bi), c * a.BK, co0, kk);
+                            if (!wait_bar(i_bempty + bi, bph ^ 1, kWaitBEmpty)) goto tma_done;
+                            if (leader) mbar_arrive_expect_tx(bar(i_bfull + bi), tx_stage);
+                            const uint32_t full = leader_bar(i_bfull + bi);
+                            const uint32_t dst_b = sB + uint32_t(bi * a.b_slot_bytes);
+                            if (LINEAR) {
+                                const uint32_t dst_a = sA + uint32_t(bi * a.a_slot_bytes);
+                                if constexpr (PAIR) {
+                                    tma_load_2d_pair(dst_a, &tm_a, full, c * a.BK, un.row0);
+                                    tma_load_2d_pair(dst_b, &tm_b, full, c * a.BK, co0);
+                                } else {
+                                    tma_load_2d(dst_a, &tm_a, full, c * a.BK, un.row0);
+                                    tma_load_2d(dst_b, &tm_b, full, c * a.BK, co0);
+                                }
+                            } else {
+                                if constexpr (PAIR) tma_load_3d_pair(dst_b, &tm_b, full, c * a.BK, co0, kk);
+                                else tma_load_3d(dst_b, &tm_b, full, c * a.BK, co0, kk);
+                            }
                             ++b_cnt;
-                            prog[0] = int(b_cnt);
                             if (++bi == SB) { bi = 0; bph ^= 1; }
                         }
                     }
                 }
+                prog[0] = int(b_cnt);
             }
         tma_done:
             if (*abort_flag) {
                 // Let copies already in flight land before the CTA's shared memory goes away.
-                for (int s = 0; s < SA; ++s)
-                    if (LINEAR && a_cnt > s) mbar_drain(bar(i_afull + s), s < ai ? aph : (aph ^ 1), a.status);
-                for (int s = 0; s < SB; ++s)
-                    if (b_cnt > s) mbar_drain(bar(i_bfull + s), s < bi ? bph : (bph ^ 1), a.status);
+                if (leader) {
+                    for (int s = 0; s < SB; ++s)
+                        if (b_cnt > s) mbar_drain(bar(i_bfull + s), s < bi ? bph : (bph ^ 1), a.status);
+                } else {
+                    // the second CTA of a pair signals the leader's barriers and cannot watch its
+                    // own copies: give them a fixed 200 us to land
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 200000ull) __nanosleep(1000);
+                }
             }
         }
     } else if (warp == kWarpMma) {
         // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // Descriptors are built once: every operand slot is 128-byte swizzled, K-major, with
+        // 8-row groups 1024 bytes apart, so only the start-address field (low word, in 16-byte
+        // units) changes between MMAs: +2 per 32-byte K step, +8*dilation per tap (A tile
+        // shifted down by dilation rows), + slot size per ring slot.
+        if (lane == 0 && leader) {
             int ai = 0, bi = 0;
             uint32_t aph = 0, bph = 0;
             int lt = 0;
             bool ok = true;
+            const uint32_t a_lo0 = desc_lo_sw128(sA), b_lo0 = desc_lo_sw128(sB);
+            const uint32_t a_step = uint32_t(a.a_slot_bytes) >> 4, b_step = uint32_t(a.b_slot_bytes) >> 4;
+            const uint32_t tap_step = uint32_t(8 * a.dil);
+            const uint32_t idesc = a.idesc;
+            // Completion of the MMAs so far arrives on barrier i (in both CTAs of a pair).
+            auto commit = [&](int i) {
+                if constexpr (PAIR) mma_commit_pair(bar(i), 3);
+                else mma_commit(bar(i));
+            };
             for (int u = first_unit; u < a.n_units && ok && !*abort_flag; u += unit_step, ++lt) {
                 const int ab = a.n_acc == 2 ? (lt & 1) : 0;
                 const uint32_t acc_par = a.n_acc == 2 ? uint32_t((lt >> 1) & 1) : uint32_t(lt & 1);
                 prog[10] = lt;
                 prog[11] = ai | (int(aph) << 8) | (bi << 16) | (int(bph) << 24);
-                prog[6] = kWaitAccEmpty;
-                if (!mbar_wait(bar(i_accempty + ab), acc_par ^ 1, abort_flag, a.status, kWaitAccEmpty, prog)) break;
-                prog[6] = 0;
+                if (!wait_bar(i_accempty + ab, acc_par ^ 1, kWaitAccEmpty)) break;
                 tc_fence_after();
+                const uint32_t d0 = tmem_base + uint32_t(256 * ab * a.cb_per_unit);
                 for (int c = 0; c < a.n_ci_chunks && ok; ++c) {
-                    prog[6] = kWaitAFull;
-                    if (!mbar_wait(bar(i_afull + ai), aph, abort_flag, a.status, kWaitAFull, prog)) { ok = false; break; }
-                    prog[6] = 0;
-                    tc_fence_after();
-                    const uint32_t a_addr = sA + ai * a.a_slot_bytes;
+                    uint32_t a_lo = a_lo0 + uint32_t(ai) * a_step;
+                    if (!LINEAR) {
+                        if (!wait_bar(i_afull + ai, aph, kWaitAFull)) { ok = false; break; }
+                    }
                     for (int cbi = 0; cbi < a.cb_per_unit && ok; ++cbi) {
-                        const uint32_t d = tmem_base + uint32_t(256 * (ab * a.cb_per_unit + cbi));
+                        const uint32_t d = d0 + uint32_t(256 * cbi);
                         for (int kk = 0; kk < taps; ++kk) {
-                            prog[6] = kWaitBFull;
-                            if (!mbar_wait(bar(i_bfull + bi), bph, abort_flag, a.status, kWaitBFull, prog)) { ok = false; break; }
-                            prog[6] = 0;
+                            if (!wait_bar(i_bfull + bi, bph, kWaitBFull)) { ok = false; break; }
                             tc_fence_after();
-                            const uint32_t b_addr = sB + bi * a.b_slot_bytes;
-                            const uint32_t a_tap = a_addr + uint32_t(128 * kk * a.dil);
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const uint64_t adesc = smem_desc_sw128(a_tap + 32u * j, 16u, 1024u);
-                                const uint64_t bdesc = smem_desc_sw128(b_addr + 32u * j, 16u, 1024u);
-                                const uint32_t accum = (c | kk | j) != 0 ? 1u : 0u;
-                                if (BF16) mma_f16(d, adesc, bdesc, a.idesc, accum);
-                                else mma_tf32(d, adesc, bdesc, a.idesc, accum);
-                            }
-                            mma_commit(bar(i_bempty + bi));
+                            const uint32_t al = LINEAR ? a_lo0 + uint32_t(bi) * a_step : a_lo + uint32_t(kk) * tap_step;
+                            const uint32_t bl = b_lo0 + uint32_t(bi) * b_step;
+                            const uint32_t acc0 = (c | kk) != 0 ? 1u : 0u;
+                            mma_issue<BF16, PAIR>(d, al, bl, idesc, acc0);
+                            mma_issue<BF16, PAIR>(d, al + 2u, bl + 2u, idesc, 1u);
+                            mma_issue<BF16, PAIR>(d, al + 4u, bl + 4u, idesc, 1u);
+                            mma_issue<BF16, PAIR>(d, al + 6u, bl + 6u, idesc, 1u);
+                            commit(i_bempty + bi);
                             if (++bi == SB) { bi = 0; bph ^= 1; }
                         }
                     }
                     if (!ok) break;
-                    mma_commit(bar(i_aempty + ai));
-                    prog[1] = prog[1] + 1;
-                    if (++ai == SA) { ai = 0; aph ^= 1; }
+                    if (!LINEAR) {
+                        commit(i_aempty + ai);
+                        if (++ai == SA) { ai = 0; aph ^= 1; }
+                    }
                 }
                 if (!ok) break;
-                mma_commit(bar(i_accfull + ab));
+                commit(i_accfull + ab);
                 prog[2] = lt + 1;
             }
             // Every MMA issued above has finished before TMEM is released.
-            mma_commit(bar(i_drain));
+            if constexpr (PAIR) mma_commit_pair(bar(i_drain), 1);
+            else mma_commit(bar(i_drain));
             mbar_drain(bar(i_drain), 0, a.status);
         }
     } else if (warp == kWarpXld) {
@@ -409,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t sph = 0;
             long long s_cnt = 0;
             for (int u = first_unit; u < a.n_units && !*abort_flag; u += unit_step) {
-                const Unit un = decode_unit<LINEAR>(a, u);
+                const Unit un = decode_unit<LINEAR, PAIR>(a, u, rank);
                 const int t0 = un.row0 - a.pad_left - a.t_shift;  // multiple of 16 bytes of elements
                 for (int c = 0; c < a.n_ci_chunks; ++c) {
                     if (!mbar_wait(bar(i_sempty + si), sph ^ 1, abort_flag, a.status, kWaitSEmpty, prog)) goto xld_done;
@@ -443,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int ok = 0;
                     if (lane == 0)
                         ok = mbar_wait(bar(i_sfull + si), sph, abort_flag, a.status, kWaitSFull, prog) &&
-                             mbar_wait(bar(i_aempty + ai), aph ^ 1, abort_flag, a.status, kWaitAEmpty, prog);
+                             wait_bar(i_aempty + ai, aph ^ 1, kWaitAEmpty);
                     if (!__shfl_sync(0xffffffffu, ok, 0)) goto xp_done;
                     if (xt == 0) prog[8] = 0;
                     const InT* stg = reinterpret_cast<const InT*>(base + s_off + size_t(si) * a.s_slot_bytes);
@@ -468,10 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<uint4*>(slot + r * 128 + ((cg ^ (r & 7)) << 4)) = pk;
                     }
                     // Make the generic-proxy stores visible to the tensor core, then signal.
-                    fence_async_shared();
+                    if (PAIR) fence_async_all();
+                    else fence_async_shared();
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(bar(i_afull + ai));
+                        arrive_leader(i_afull + ai);
                         mbar_arrive(bar(i_sempty + si));
                     }
                     if (xt == 0) prog[3] = prog[3] + 1;
@@ -494,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kFusedGN && first_unit < a.n_units) {
             // One unit per CTA: stage bias, gamma and beta of its channel block while the
             // mainloop runs (gamma and beta go where the column scale / shift end up).
-            const int co_base = decode_unit<LINEAR>(a, first_unit).cbu * a.BN;
+            const int co_base = decode_unit<LINEAR, PAIR>(a, first_unit, rank).cbu * a.BN;
             const int ncols = min(a.BN, a.C_out - co_base);
             for (int col = er; col < 256; col += kEpiThreads) {
                 const bool ok = col < ncols;
@@ -513,13 +574,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // warp-collective), and the barrier ORs what every epilogue thread saw, so all four
             // warps leave (or stay) together.
             int got = 0;
-            if (lane == 0) got = mbar_wait(bar(i_accfull + ab), acc_par, abort_flag, a.status, kWaitAccFull, prog);
+            if (lane == 0) got = wait_bar(i_accfull + ab, acc_par, kWaitAccFull);
             got = __shfl_sync(0xffffffffu, got, 0);
             if (named_bar_any(1, kEpiThreads, !got || *abort_flag != 0)) break;
             __syncwarp();
             if (er == 0) prog[7] = 0;
             tc_fence_after();
-            const Unit un = decode_unit<LINEAR>(a, u);
+            const Unit un = decode_unit<LINEAR, PAIR>(a, u, rank);
             OutT* y = static_cast<OutT*>(a.y);
             const int row = un.row0 + m;
             const bool row_ok = LINEAR ? (row < a.N) : (row < a.T_out);
@@ -843,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(i_accempty + ab));
+            if (lane == 0) arrive_leader(i_accempty + ab);
             if (threadIdx.x == kWarpEpi0 * 32) prog[4] = lt + 1;
         }
         if (EPI == kEpiClusterGN && !mid_sync_done) cluster_sync_all();
@@ -858,17 +919,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync_all();
     }
     __syncwarp();
-    __syncthreads();
+    // A pair leaves together: the leader's MMAs read the peer's shared memory and write its TMEM,
+    // and the peer's copies and arrivals target the leader's barriers.
+    if (PAIR) cluster_sync_all();
+    else __syncthreads();
     if (warp == kWarpMma) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, uint32_t(a.tmem_cols));
+        if constexpr (PAIR) tmem_dealloc_pair(tmem_base, uint32_t(a.tmem_cols));
+        else tmem_dealloc(tmem_base, uint32_t(a.tmem_cols));
     }
 }
 
-template <bool LINEAR, bool BF16, typename OutT, int EPI>
+template <bool LINEAR, bool BF16, typename OutT, int EPI, bool PAIR>
 cudaError_t launch_one(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                        const CUtensorMap& tm_y, int num_sms, cudaStream_t stream) {
-    auto kern = tc_conv_kernel<LINEAR, BF16, OutT, EPI>;
+    auto kern = tc_conv_kernel<LINEAR, BF16, OutT, EPI, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -876,21 +941,32 @@ cudaError_t launch_one(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a,
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = size_t(pl.smem_bytes);
     cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (EPI == kEpiClusterGN) {
         cfg.gridDim = dim3(unsigned(a.n_t_tiles), unsigned(a.n_cb / a.cb_per_unit), unsigned(a.N));
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = unsigned(a.n_t_tiles);
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
     } else if (EPI == kEpiGridGN) {
         // every CTA of a sample waits for its peers: all CTAs must be resident at once
         cfg.gridDim = dim3(unsigned(a.n_t_tiles), unsigned(a.n_cb / a.cb_per_unit), unsigned(a.N));
         attr[0].id = cudaLaunchAttributeCooperative;
         attr[0].val.cooperative = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+    } else if (PAIR) {
+        // persistent CTA pairs: as many clusters of two as can be resident at once
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(unsigned(num_sms & ~1), 1, 1);
+        int max_clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+        const int pairs = a.n_units < max_clusters ? a.n_units : max_clusters;
+        cfg.gridDim = dim3(unsigned(2 * pairs), 1, 1);
     } else {
         const int grid = a.n_units < num_sms ? a.n_units : num_sms;
         cfg.gridDim = dim3(unsigned(grid), 1, 1);
@@ -905,33 +981,35 @@ cudaError_t launch_one(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a,
 cudaError_t launch_tc(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                       const CUtensorMap& tm_y, bool linear, int epilogue, bool out_bf16, int num_sms,
                       cudaStream_t stream) {
-#define C1N_LAUNCH(L, B, O, E) launch_one<L, B, O, E>(pl, a, tm_a, tm_b, tm_y, num_sms, stream)
+#define C1N_LAUNCH(L, B, O, E, P) launch_one<L, B, O, E, P>(pl, a, tm_a, tm_b, tm_y, num_sms, stream)
+#define C1N_LAUNCH2(L, B, O, E) (pl.pair ? C1N_LAUNCH(L, B, O, E, true) : C1N_LAUNCH(L, B, O, E, false))
     if (linear) {
         if (epilogue == kEpiRowGN) {
-            if (pl.bf16) return C1N_LAUNCH(true, true, __nv_bfloat16, kEpiRowGN);
-            return C1N_LAUNCH(true, false, float, kEpiRowGN);
+            if (pl.bf16) return C1N_LAUNCH2(true, true, __nv_bfloat16, kEpiRowGN);
+            return C1N_LAUNCH2(true, false, float, kEpiRowGN);
         }
-        if (pl.bf16 && out_bf16) return C1N_LAUNCH(true, true, __nv_bfloat16, kEpiDirect);
-        if (pl.bf16) return C1N_LAUNCH(true, true, float, kEpiDirect);
-        return C1N_LAUNCH(true, false, float, kEpiDirect);
+        if (pl.bf16 && out_bf16) return C1N_LAUNCH2(true, true, __nv_bfloat16, kEpiDirect);
+        if (pl.bf16) return C1N_LAUNCH2(true, true, float, kEpiDirect);
+        return C1N_LAUNCH2(true, false, float, kEpiDirect);
     }
     if (epilogue == kEpiLN) {
-        if (pl.bf16) return C1N_LAUNCH(false, true, __nv_bfloat16, kEpiLN);
-        return C1N_LAUNCH(false, false, float, kEpiLN);
+        if (pl.bf16) return C1N_LAUNCH2(false, true, __nv_bfloat16, kEpiLN);
+        return C1N_LAUNCH2(false, false, float, kEpiLN);
     }
     if (epilogue == kEpiClusterGN) {
-        if (pl.bf16) return C1N_LAUNCH(false, true, __nv_bfloat16, kEpiClusterGN);
-        return C1N_LAUNCH(false, false, float, kEpiClusterGN);
+        if (pl.bf16) return C1N_LAUNCH(false, true, __nv_bfloat16, kEpiClusterGN, false);
+        return C1N_LAUNCH(false, false, float, kEpiClusterGN, false);
     }
     if (epilogue == kEpiGridGN) {
-        if (pl.bf16) return C1N_LAUNCH(false, true, __nv_bfloat16, kEpiGridGN);
-        return C1N_LAUNCH(false, false, float, kEpiGridGN);
+        if (pl.bf16) return C1N_LAUNCH(false, true, __nv_bfloat16, kEpiGridGN, false);
+        return C1N_LAUNCH(false, false, float, kEpiGridGN, false);
     }
     if (pl.bf16) {
-        if (out_bf16) return C1N_LAUNCH(false, true, __nv_bfloat16, kEpiDirect);
-        return C1N_LAUNCH(false, true, float, kEpiDirect);
+        if (out_bf16) return C1N_LAUNCH2(false, true, __nv_bfloat16, kEpiDirect);
+        return C1N_LAUNCH2(false, true, float, kEpiDirect);
     }
-    return C1N_LAUNCH(false, false, float, kEpiDirect);
+    return C1N_LAUNCH2(false, false, float, kEpiDirect);
+#undef C1N_LAUNCH2
 #undef C1N_LAUNCH
 }
 

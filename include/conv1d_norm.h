@@ -88,6 +88,14 @@ typedef enum {
                                      all C_out <= 512 channels of a 128-step tile in TMEM */
 } c1n_path;
 
+/* Tensor-core mainloop. AUTO uses CTA pairs where the plan allows: two CTAs on neighbouring SMs
+ * (a thread-block cluster of two) compute one 256-row x BN tile with tcgen05.mma.cta_group::2;
+ * each CTA stages its own 128 rows of A and half of the BN columns of B, so every SM streams a
+ * third less operand data per MMA. SINGLE keeps one CTA per 128-row tile; PAIR fails with
+ * C1N_ERR_UNSUPPORTED where the plan cannot use pairs (fused GroupNorm, SIMT, BN not a multiple
+ * of 32). */
+typedef enum { C1N_MAINLOOP_AUTO = 0, C1N_MAINLOOP_SINGLE = 1, C1N_MAINLOOP_PAIR = 2 } c1n_mainloop;
+
 typedef struct {
     int32_t N, C_in, C_out, T, k;
     int32_t stride, pad_left, pad_right, dilation;
@@ -98,6 +106,7 @@ typedef struct {
     int32_t dtype;       /* c1n_dtype of x, w and y */
     int32_t math;        /* c1n_math */
     int32_t force_path;  /* c1n_path; C1N_PATH_AUTO (-1) lets the planner choose */
+    int32_t mainloop;    /* c1n_mainloop; 0 = AUTO */
 } c1n_params;
 
 typedef struct c1n_desc c1n_desc;
@@ -112,7 +121,7 @@ typedef struct {
     int32_t n_tiles;
     int32_t grid;            /* CTAs of the main kernel */
     int32_t kernels;         /* kernels one run() enqueues */
-    int32_t reserved;
+    int32_t cta_pair;        /* 1 when the tensor-core mainloop runs on CTA pairs (tile_t = 256) */
     int64_t workspace_bytes;
 } c1n_plan_info;
 

@@ -67,6 +67,31 @@ def test_conv_gn_cluster_geometry():
     c1n.conv1d_norm_destroy(d)
 
 
+@pytest.mark.parametrize("wl", [synth.CAUSAL_CONV, synth.LINEAR_GN_ROWMIN, synth.CONV_LN_GELU_BF16],
+                         ids=lambda w: w.name)
+def test_cta_pair_mainloop(wl):
+    # the large contractions run on CTA pairs: 256-row tiles, each CTA stages half of the B tile
+    d = c1n.conv1d_norm_desc_create(_params(wl))
+    info = c1n.conv1d_norm_plan_info(d)
+    assert (info.cta_pair, info.tile_t, info.mma_n) == (1, 256, 256)
+    c1n.conv1d_norm_destroy(d)
+    d = c1n.conv1d_norm_desc_create(_params(wl, mainloop=c1n.MAINLOOP_SINGLE))
+    info = c1n.conv1d_norm_plan_info(d)
+    assert (info.cta_pair, info.tile_t) == (0, 128)
+    c1n.conv1d_norm_destroy(d)
+
+
+def test_cta_pair_refused_where_the_plan_cannot_pair():
+    # fused GroupNorm exchanges statistics between single CTAs; MMA N = 48 does not split in two 16-row halves
+    for wl in (synth.CONV_GN, synth.CAUSAL_CONV.replace(C_out=48)):
+        with pytest.raises(c1n.C1NError) as e:
+            c1n.conv1d_norm_desc_create(_params(wl, mainloop=c1n.MAINLOOP_PAIR))
+        assert e.value.status == c1n.ERR_UNSUPPORTED
+    d = c1n.conv1d_norm_desc_create(_params(synth.CONV_GN))
+    assert c1n.conv1d_norm_plan_info(d).cta_pair == 0
+    c1n.conv1d_norm_destroy(d)
+
+
 def test_simt_forced_and_tensor_forced():
     wl = synth.CONV_GN_TINY
     d = c1n.conv1d_norm_desc_create(_params(wl, math=c1n.MATH_SIMT))
@@ -87,7 +112,7 @@ def test_simt_forced_and_tensor_forced():
 @pytest.mark.parametrize("bad", [dict(N=0), dict(C_in=0), dict(k=0), dict(stride=0), dict(dilation=0),
                                  dict(pad_left=-1), dict(groups=3), dict(eps=0.0), dict(eps=float("nan")),
                                  dict(norm=7), dict(post=5), dict(dtype=3), dict(math=9), dict(T=2, k=5),
-                                 dict(force_path=11)])
+                                 dict(force_path=11), dict(mainloop=3), dict(mainloop=-1)])
 def test_invalid_params_are_rejected(bad):
     with pytest.raises(c1n.C1NError) as e:
         c1n.conv1d_norm_desc_create(_params(synth.CONV_GN_TINY, **bad))

@@ -33,9 +33,9 @@ def _to_dev(a, bf16):
     return t.to(torch.bfloat16) if bf16 else t
 
 
-def run_gpu(c1n, wl, inp, math=0, force_path=-1):
+def run_gpu(c1n, wl, inp, math=0, force_path=-1, mainloop=0):
     params = c1n.make_params(wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right, wl.dilation,
-                             wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, math, force_path)
+                             wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, math, force_path, mainloop)
     op = c1n.Conv1dNorm(params)
     bf = wl.dtype == synth.DTYPE_BF16
     x, w = _to_dev(inp["x"], bf), _to_dev(inp["w"], bf)
@@ -130,12 +130,16 @@ SMALL = {
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
-@pytest.mark.parametrize("math", [0, 1], ids=["auto", "simt"])
-def test_small_shapes(cuda_lib, name, math):
+@pytest.mark.parametrize("mode", ["auto", "simt", "single"])
+def test_small_shapes(cuda_lib, name, mode):
+    # auto: the planner's choice (CTA-pair mainloop where the plan allows it); single: one CTA per
+    # 128-row tile; simt: the fp32 CUDA-core check path
     wl = SMALL[name]
     inp = _inputs(wl)
     ref, ref_am = oracle_full(wl, inp)
-    y, am, path = run_gpu(cuda_lib, wl, inp, math=math)
+    math = 1 if mode == "simt" else 0
+    mainloop = cuda_lib.MAINLOOP_SINGLE if mode == "single" else cuda_lib.MAINLOOP_AUTO
+    y, am, path = run_gpu(cuda_lib, wl, inp, math=math, mainloop=mainloop)
     if math == 1:
         assert path == "simt"
     compare(wl, y, am, ref, ref_am, path, name)
@@ -230,10 +234,12 @@ def test_causal_conv_full_sampled(cuda_lib):
     inp = _inputs(wl)
     y, _, path = run_gpu(cuda_lib, wl, inp)
     assert path == "tc_direct"
+    y1, _, _ = run_gpu(cuda_lib, wl, inp, mainloop=cuda_lib.MAINLOOP_SINGLE)
     ns = [0, wl.N - 1]
     ref, _ = oracle.conv1d_norm_samples(oracle.params_of(wl), ns, inp["x"], inp["w"], inp["b"])
     compare(wl, y[ns], None, ref, None, path, wl.name)
-    assert np.all(np.isfinite(y))
+    compare(wl, y1[ns], None, ref, None, path, wl.name + " (single-CTA mainloop)")
+    assert np.all(np.isfinite(y)) and np.all(np.isfinite(y1))
 
 
 def test_linear_gn_rowmin_full_sampled(cuda_lib):
