@@ -382,6 +382,19 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
     return v;
 }
 
+// One lane of the (fully active) warp returns true: the lowest active lane.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(r)
+        :
+        : "memory");
+    return r != 0;
+}
+
 // Named barrier over `nthreads` threads (id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -336,31 +336,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         unit_step = gridDim.x;
     }
 
+    // The producer and MMA warps run their loops with all 32 lanes (so loop state, addresses and
+    // descriptors stay warp-uniform) and issue each copy / MMA / commit from one elected lane.
+    // Every wait is taken by all lanes and agreed on with a vote.
+    auto wait_warp = [&](int i, uint32_t parity, int site) -> bool {
+        return __all_sync(0xffffffffu, wait_bar(i, parity, site));
+    };
+    auto aborting = [&]() -> bool { return __any_sync(0xffffffffu, *abort_flag != 0); };
     if (warp == kWarpTma) {
         // ---------------------------------------------------------------- TMA producer
         // Linear mode: one ring of stages, each holding the A and the B chunk of one K step under
         // one full / empty barrier pair. Conv mode: the B (weight) ring only; A comes from the
         // transposer warps. A pair's full barriers (in the leader) expect both CTAs' bytes; each
         // CTA loads its own 128 rows of A and its half (BN/2 channels) of the B tile.
-        if (lane == 0) {
-            int bi = 0;
-            uint32_t bph = 0;
-            long long b_cnt = 0;
-            const uint32_t tx_mult = PAIR ? 2u : 1u;
-            const uint32_t tx_stage = tx_mult * uint32_t(a.b_slot_bytes + (LINEAR ? a.a_slot_bytes : 0));
-            const int co_half = PAIR ? int(rank) * (a.BN / 2) : 0;
-            for (int u = first_unit; u < a.n_units && !*abort_flag; u += unit_step) {
-                const Unit un = decode_unit<LINEAR, PAIR>(a, u, rank);
-                for (int c = 0; c < a.n_ci_chunks; ++c) {
-                    for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
-                        const int co0 = (un.cbu * a.cb_per_unit + cbi) * a.BN + co_half;
-                        for (int kk = 0; kk < taps; ++kk) {
-                            if (!wait_bar(i_bempty + bi, bph ^ 1, kWaitBEmpty)) goto tma_done;
+        int bi = 0;
+        uint32_t bph = 0;
+        long long b_cnt = 0;
+        const uint32_t tx_mult = PAIR ? 2u : 1u;
+        const uint32_t tx_stage = tx_mult * uint32_t(a.b_slot_bytes + (LINEAR ? a.a_slot_bytes : 0));
+        const int co_half = PAIR ? int(rank) * (a.BN / 2) : 0;
+        for (int u = first_unit; u < a.n_units && !aborting(); u += unit_step) {
+            const Unit un = decode_unit<LINEAR, PAIR>(a, u, rank);
+            for (int c = 0; c < a.n_ci_chunks; ++c) {
+                for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
+                    const int co0 = (un.cbu * a.cb_per_unit + cbi) * a.BN + co_half;
+                    for (int kk = 0; kk < taps; ++kk) {
+                        if (!wait_warp(i_bempty + bi, bph ^ 1, kWaitBEmpty)) goto tma_done;
+                        const uint32_t full = leader_bar(i_bfull + bi);
+                        const uint32_t dst_b = sB + uint32_t(bi * a.b_slot_bytes);
+                        const uint32_t dst_a = sA + uint32_t(bi * a.a_slot_bytes);
+                        if (elect_one()) {
                             if (leader) mbar_arrive_expect_tx(bar(i_bfull + bi), tx_stage);
-                            const uint32_t full = leader_bar(i_bfull + bi);
-                            const uint32_t dst_b = sB + uint32_t(bi * a.b_slot_bytes);
                             if (LINEAR) {
-                                const uint32_t dst_a = sA + uint32_t(bi * a.a_slot_bytes);
                                 if constexpr (PAIR) {
                                     tma_load_2d_pair(dst_a, &tm_a, full, c * a.BK, un.row0);
                                     tma_load_2d_pair(dst_b, &tm_b, full, c * a.BK, co0);
@@ -372,25 +379,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if constexpr (PAIR) tma_load_3d_pair(dst_b, &tm_b, full, c * a.BK, co0, kk);
                                 else tma_load_3d(dst_b, &tm_b, full, c * a.BK, co0, kk);
                             }
-                            ++b_cnt;
-                            if (++bi == SB) { bi = 0; bph ^= 1; }
                         }
+                        __syncwarp();
+                        ++b_cnt;
+                        if (++bi == SB) { bi = 0; bph ^= 1; }
                     }
                 }
-                prog[0] = int(b_cnt);
             }
-        tma_done:
-            if (*abort_flag) {
-                // Let copies already in flight land before the CTA's shared memory goes away.
-                if (leader) {
-                    for (int s = 0; s < SB; ++s)
-                        if (b_cnt > s) mbar_drain(bar(i_bfull + s), s < bi ? bph : (bph ^ 1), a.status);
-                } else {
-                    // the second CTA of a pair signals the leader's barriers and cannot watch its
-                    // own copies: give them a fixed 200 us to land
-                    const uint64_t t0 = global_timer_ns();
-                    while (global_timer_ns() - t0 < 200000ull) __nanosleep(1000);
-                }
+            if (lane == 0) prog[0] = int(b_cnt);
+        }
+    tma_done:
+        if (aborting() && lane == 0) {
+            // Let copies already in flight land before the CTA's shared memory goes away.
+            if (leader) {
+                for (int s = 0; s < SB; ++s)
+                    if (b_cnt > s) mbar_drain(bar(i_bfull + s), s < bi ? bph : (bph ^ 1), a.status);
+            } else {
+                // the second CTA of a pair signals the leader's barriers and cannot watch its
+                // own copies: give them a fixed 200 us to land
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 200000ull) __nanosleep(1000);
             }
         }
     } else if (warp == kWarpMma) {
@@ -399,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 8-row groups 1024 bytes apart, so only the start-address field (low word, in 16-byte
         // units) changes between MMAs: +2 per 32-byte K step, +8*dilation per tap (A tile
         // shifted down by dilation rows), + slot size per ring slot.
-        if (lane == 0 && leader) {
+        if (leader) {
             int ai = 0, bi = 0;
             uint32_t aph = 0, bph = 0;
             int lt = 0;
@@ -413,49 +421,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (PAIR) mma_commit_pair(bar(i), 3);
                 else mma_commit(bar(i));
             };
-            for (int u = first_unit; u < a.n_units && ok && !*abort_flag; u += unit_step, ++lt) {
+            for (int u = first_unit; u < a.n_units && ok && !aborting(); u += unit_step, ++lt) {
                 const int ab = a.n_acc == 2 ? (lt & 1) : 0;
                 const uint32_t acc_par = a.n_acc == 2 ? uint32_t((lt >> 1) & 1) : uint32_t(lt & 1);
-                prog[10] = lt;
-                prog[11] = ai | (int(aph) << 8) | (bi << 16) | (int(bph) << 24);
-                if (!wait_bar(i_accempty + ab, acc_par ^ 1, kWaitAccEmpty)) break;
+                if (lane == 0) {
+                    prog[10] = lt;
+                    prog[11] = ai | (int(aph) << 8) | (bi << 16) | (int(bph) << 24);
+                }
+                if (!wait_warp(i_accempty + ab, acc_par ^ 1, kWaitAccEmpty)) break;
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + uint32_t(256 * ab * a.cb_per_unit);
                 for (int c = 0; c < a.n_ci_chunks && ok; ++c) {
-                    uint32_t a_lo = a_lo0 + uint32_t(ai) * a_step;
+                    const uint32_t a_lo = a_lo0 + uint32_t(ai) * a_step;
                     if (!LINEAR) {
-                        if (!wait_bar(i_afull + ai, aph, kWaitAFull)) { ok = false; break; }
+                        if (!wait_warp(i_afull + ai, aph, kWaitAFull)) { ok = false; break; }
                     }
                     for (int cbi = 0; cbi < a.cb_per_unit && ok; ++cbi) {
                         const uint32_t d = d0 + uint32_t(256 * cbi);
                         for (int kk = 0; kk < taps; ++kk) {
-                            if (!wait_bar(i_bfull + bi, bph, kWaitBFull)) { ok = false; break; }
+                            if (!wait_warp(i_bfull + bi, bph, kWaitBFull)) { ok = false; break; }
                             tc_fence_after();
                             const uint32_t al = LINEAR ? a_lo0 + uint32_t(bi) * a_step : a_lo + uint32_t(kk) * tap_step;
                             const uint32_t bl = b_lo0 + uint32_t(bi) * b_step;
                             const uint32_t acc0 = (c | kk) != 0 ? 1u : 0u;
-                            mma_issue<BF16, PAIR>(d, al, bl, idesc, acc0);
-                            mma_issue<BF16, PAIR>(d, al + 2u, bl + 2u, idesc, 1u);
-                            mma_issue<BF16, PAIR>(d, al + 4u, bl + 4u, idesc, 1u);
-                            mma_issue<BF16, PAIR>(d, al + 6u, bl + 6u, idesc, 1u);
-                            commit(i_bempty + bi);
+                            if (elect_one()) {
+                                mma_issue<BF16, PAIR>(d, al, bl, idesc, acc0);
+                                mma_issue<BF16, PAIR>(d, al + 2u, bl + 2u, idesc, 1u);
+                                mma_issue<BF16, PAIR>(d, al + 4u, bl + 4u, idesc, 1u);
+                                mma_issue<BF16, PAIR>(d, al + 6u, bl + 6u, idesc, 1u);
+                                commit(i_bempty + bi);
+                            }
+                            __syncwarp();
                             if (++bi == SB) { bi = 0; bph ^= 1; }
                         }
                     }
                     if (!ok) break;
                     if (!LINEAR) {
-                        commit(i_aempty + ai);
+                        if (elect_one()) commit(i_aempty + ai);
+                        __syncwarp();
                         if (++ai == SA) { ai = 0; aph ^= 1; }
                     }
                 }
                 if (!ok) break;
-                commit(i_accfull + ab);
-                prog[2] = lt + 1;
+                if (elect_one()) commit(i_accfull + ab);
+                __syncwarp();
+                if (lane == 0) prog[2] = lt + 1;
             }
-            // Every MMA issued above has finished before TMEM is released.
-            if constexpr (PAIR) mma_commit_pair(bar(i_drain), 1);
-            else mma_commit(bar(i_drain));
-            mbar_drain(bar(i_drain), 0, a.status);
+            // Every MMA issued above has finished before TMEM is released (the commit comes from
+            // the lane that issued them: elect.sync picks the lowest active lane each time).
+            if (elect_one()) {
+                if constexpr (PAIR) mma_commit_pair(bar(i_drain), 1);
+                else mma_commit(bar(i_drain));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_drain(bar(i_drain), 0, a.status);
         }
     } else if (warp == kWarpXld) {
         // ---------------------------------------------------------------- x staging loader (conv mode)
@@ -487,49 +506,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= kWarpXp0) {
         // ---------------------------------------------------------------- x transposer (conv mode)
         // Staged x (rows = channels, time-contiguous) -> A tile (rows = time steps, 128 bytes of
-        // channels per row, 128-byte swizzle). A task is one 16-byte chunk of one A row; lanes take
-        // consecutive rows, so the staged reads are consecutive words (conflict-free) and the
-        // swizzled 16-byte writes of 8 consecutive lanes cover all 32 banks.
+        // channels per row, 128-byte swizzle). Transposer warp w owns the 16-byte column chunk w of
+        // every A row; its lanes take consecutive rows, so the staged reads are consecutive
+        // elements (one wavefront) and each group of 8 lanes writes 8 distinct swizzled chunks
+        // (all 32 banks).
         if (!LINEAR) {
             const int xt = threadIdx.x - kWarpXp0 * 32;  // 0..255
+            const int cg = warp - kWarpXp0;               // 0..7
             constexpr int kPerChunk = BF16 ? 8 : 4;       // channels per 16-byte chunk
-            const int n_tasks = 8 * a.R;                  // (16-byte chunk, row) pairs per tile
+            const int R = a.R, RS = a.RS;
             int ai = 0, si = 0;
             uint32_t aph = 0, sph = 0;
             for (int u = first_unit; u < a.n_units; u += unit_step) {
                 for (int c = 0; c < a.n_ci_chunks; ++c) {
-                    if (xt == 0) prog[8] = kWaitSFull;
                     // One lane waits; the shuffle hands its answer to the warp and reconverges it.
                     int ok = 0;
                     if (lane == 0)
                         ok = mbar_wait(bar(i_sfull + si), sph, abort_flag, a.status, kWaitSFull, prog) &&
                              wait_bar(i_aempty + ai, aph ^ 1, kWaitAEmpty);
                     if (!__shfl_sync(0xffffffffu, ok, 0)) goto xp_done;
-                    if (xt == 0) prog[8] = 0;
-                    const InT* stg = reinterpret_cast<const InT*>(base + s_off + size_t(si) * a.s_slot_bytes);
+                    const InT* col = reinterpret_cast<const InT*>(base + s_off + size_t(si) * a.s_slot_bytes) +
+                                     (cg * kPerChunk) * RS + a.t_shift;
                     uint8_t* slot = base + size_t(ai) * a.a_slot_bytes;
-                    for (int q = xt; q < n_tasks; q += kXpThreads) {
-                        const int cg = q / a.R, r = q - cg * a.R;
-                        const InT* src = stg + (cg * kPerChunk) * a.RS + r + a.t_shift;
+#pragma unroll 2
+                    for (int r = lane; r < R; r += 32) {
+                        const InT* src = col + r;
                         uint4 pk;
                         if constexpr (BF16) {
                             uint32_t w[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const uint32_t lo = *reinterpret_cast<const uint16_t*>(src + (2 * e) * a.RS);
-                                const uint32_t hi = *reinterpret_cast<const uint16_t*>(src + (2 * e + 1) * a.RS);
+                                const uint32_t lo = *reinterpret_cast<const uint16_t*>(src + (2 * e) * RS);
+                                const uint32_t hi = *reinterpret_cast<const uint16_t*>(src + (2 * e + 1) * RS);
                                 w[e] = lo | (hi << 16);
                             }
                             pk = make_uint4(w[0], w[1], w[2], w[3]);
                         } else {
-                            pk = make_uint4(__float_as_uint(src[0]), __float_as_uint(src[a.RS]),
-                                            __float_as_uint(src[2 * a.RS]), __float_as_uint(src[3 * a.RS]));
+                            pk = make_uint4(__float_as_uint(src[0]), __float_as_uint(src[RS]),
+                                            __float_as_uint(src[2 * RS]), __float_as_uint(src[3 * RS]));
                         }
+                        // 16-byte chunk cg of row r sits at chunk position cg ^ (r & 7)
                         *reinterpret_cast<uint4*>(slot + r * 128 + ((cg ^ (r & 7)) << 4)) = pk;
                     }
                     // Make the generic-proxy stores visible to the tensor core, then signal.
-                    if (PAIR) fence_async_all();
-                    else fence_async_shared();
+                    fence_async_shared();
                     __syncwarp();
                     if (lane == 0) {
                         arrive_leader(i_afull + ai);
