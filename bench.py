@@ -201,7 +201,7 @@ def our_arm(args, wl):
     peaks = load_peaks()
 
     params = c1n.make_params(wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right, wl.dilation,
-                             wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, args.math, args.path)
+                             wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, args.math, args.path, args.mainloop)
     op = c1n.Conv1dNorm(params, device=dev)
     path = op.path
     # Weak scaling: rank r runs the per-GPU workload on batch rows [r*N, (r+1)*N) of one global
@@ -274,23 +274,36 @@ def our_arm(args, wl):
         ms, main_ms = float(t[0]), float(t[1])
     value, ms = aggregate([ms], wl.flops, world)
 
-    # roofline of the dominant kernel (the fused tensor-core kernel)
-    flops, nbytes = wl.flops, wl.algorithmic_bytes
+    # per-kernel device times from the library's event marks (a few extra steps after the timed
+    # region, same inputs and launch configuration)
+    kern = kernel_times(op, step, args.warmup + args.steps, n=5)
+    conv_name = "simt_conv" if path == "simt" else "tc_conv"
+    conv_ms = kern.get(conv_name, main_ms)
+
+    # roofline of the dominant kernel (the conv kernel with its fused epilogue). Its algorithmic
+    # bytes: x and w read once, the per-channel parameters, and its output written once (y, or
+    # the fp32 raw tile on the two-pass plans).
+    flops = wl.flops
+    nbytes = wl.algorithmic_bytes
+    y_elems = wl.N * wl.C_out * wl.T_out
+    if kern.get("normalize") is not None or kern.get("rowmin") is not None:
+        nbytes += y_elems * (4 - wl.elem_bytes)  # raw fp32 tile instead of y
     tc_peak = peaks["bf16_tflops"] * (1.0 if bf else TF32_PER_BF16)
     t_flop = flops / (tc_peak * 1e12)
     t_byte = nbytes / (peaks["hbm_gbs"] * 1e9)
     if t_byte >= t_flop:
-        ach = nbytes / (main_ms / 1e3) / 1e9
+        ach = nbytes / (conv_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"]}
     else:
-        ach = flops / (main_ms / 1e3) / 1e12
+        ach = flops / (conv_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s", "frac": ach / tc_peak}
     roof.update({"traffic": read_traffic(wl.name, path), "peak_source": peaks["source"],
-                 "kernel": f"tc_conv_kernel ({path})", "kernel_ms": main_ms, "pack_ms": pack_ms,
-                 "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
-                 "tensor_frac": (flops / (main_ms / 1e3) / 1e12) / tc_peak,
-                 "hbm_frac": (nbytes / (main_ms / 1e3) / 1e9) / peaks["hbm_gbs"]})
+                 "kernel": f"tc_conv_kernel ({path})", "kernel_ms": conv_ms, "op_ms": main_ms, "pack_ms": pack_ms,
+                 "kernels_ms": kern, "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                 "tensor_frac": (flops / (conv_ms / 1e3) / 1e12) / tc_peak,
+                 "hbm_frac": (nbytes / (conv_ms / 1e3) / 1e9) / peaks["hbm_gbs"]})
+    norm_pass = normalize_pass_roofline(wl, kern, peaks)
 
     e2e = measure_e2e(args, wl, op, inp, dev, tdt, bf, w, b, ga, be, b2, am)
     if pg is not None:
@@ -306,17 +319,47 @@ def our_arm(args, wl):
         line = {"metric": args.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": dtype_name(wl, path), "data": "synthetic",
-                "config": config_of(wl, {"path": path, "parallelism": f"dp{world}" if world > 1 else "single",
+                "config": config_of(wl, {"path": path, "cta_pair": int(op.info.cta_pair), "parallelism": f"dp{world}" if world > 1 else "single",
                                          "l2": f"inputs rotate over {n_sets} x/y buffer sets "
                                                f"({n_sets * per_set / 2**20:.0f} MiB > 129 MiB L2)"
                                          if n_sets > 1 else "working set larger than L2",
                                          "step": "weight pack + fused kernel through the C ABI"}),
-                "roofline": roof, "cpu_baseline": cpu,
+                "roofline": roof, "normalize_pass": norm_pass, "cpu_baseline": cpu,
                 "e2e": {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
                 "gpu_launches": args.steps * op.info.kernels, "clocks": clocks}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+def kernel_times(op, step, i0, n=5):
+    """Mean device time per kernel name over n profiled steps (the library's event marks)."""
+    import torch
+    acc = {}
+    op.set_profiling(True)
+    try:
+        for i in range(n):
+            step(i0 + i)
+            for name, ms in op.kernel_times():
+                acc.setdefault(name, []).append(ms)
+    finally:
+        op.set_profiling(False)
+    torch.cuda.synchronize()
+    return {k: statistics.mean(v) for k, v in acc.items()}
+
+
+def normalize_pass_roofline(wl, kern, peaks):
+    """GB/s of the memory-bound passes of a two-pass plan: statistics (read the fp32 raw tile) and
+    normalize (read raw + write y), against the measured HBM copy bandwidth; None when the plan
+    fuses normalization into the conv kernel."""
+    y_elems = wl.N * wl.C_out * wl.T_out
+    out = {}
+    for name, nbytes in (("gn_stats", 4 * y_elems), ("ln_stats", 4 * y_elems),
+                         ("normalize", (4 + wl.elem_bytes) * y_elems)):
+        if name in kern and kern[name] > 0:
+            gbs = nbytes / (kern[name] / 1e3) / 1e9
+            out[name] = {"ms": kern[name], "bytes": nbytes, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"]}
+    return out or None
 
 
 def measure_e2e(args, wl, op, inp, dev, tdt, bf, w_dev, b_dev, ga_dev, be_dev, b2_dev, am):
@@ -392,6 +435,7 @@ def main():
     ap.add_argument("--workload", default=synth.CONV_GN.name)
     ap.add_argument("--math", type=int, default=0, help="0 auto, 1 SIMT, 2 tensor")
     ap.add_argument("--path", type=int, default=-1, help="force an execution path (c1n_path)")
+    ap.add_argument("--mainloop", type=int, default=0, help="0 auto, 1 one CTA per tile, 2 CTA pairs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--oracle-rows", type=int, default=2, help="batch entries per reference-arm step")

@@ -31,6 +31,7 @@ EXPORTED_SYMBOLS = (
     "conv1d_norm_desc_create", "conv1d_norm_workspace_size", "conv1d_norm_set_workspace", "conv1d_norm_plan_info",
     "conv1d_norm_run", "conv1d_norm_run_ex", "conv1d_norm_pack_weights", "conv1d_norm_check", "conv1d_norm_destroy",
     "conv1d_norm_status_string", "conv1d_norm_last_error", "conv1d_norm_version", "conv1d_norm_run_static_scratch",
+    "conv1d_norm_set_profiling", "conv1d_norm_kernel_times",
 )
 
 STATIC_SCRATCH_BYTES = 4 << 20  # C1N_STATIC_SCRATCH_BYTES
@@ -47,6 +48,10 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("path", "T_out", "tile_t", "tile_co", "mma_n", "cluster", "n_tiles", "grid", "kernels", "cta_pair")]
     _fields_ += [("workspace_bytes", ctypes.c_int64)]
+
+
+class KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("ms", ctypes.c_float)]
 
 
 class Args(ctypes.Structure):
@@ -100,6 +105,8 @@ def load(build_if_missing: bool = True):
         lib.conv1d_norm_pack_weights.argtypes = [vp, vp, vp, ctypes.c_size_t, vp]
         lib.conv1d_norm_check.argtypes = [vp, vp, vp]
         lib.conv1d_norm_run_static_scratch.argtypes = [vp, P(Args), vp]
+        lib.conv1d_norm_set_profiling.argtypes = [vp, ctypes.c_int32]
+        lib.conv1d_norm_kernel_times.argtypes = [vp, P(KernelTime), ctypes.c_int32, P(ctypes.c_int32)]
         lib.conv1d_norm_destroy.argtypes = [vp]
         lib.conv1d_norm_destroy.restype = None
         lib.conv1d_norm_status_string.argtypes = [ctypes.c_int]
@@ -109,7 +116,8 @@ def load(build_if_missing: bool = True):
         lib.conv1d_norm_version.restype = ctypes.c_int32
         for name in ("conv1d_norm_desc_create", "conv1d_norm_workspace_size", "conv1d_norm_set_workspace",
                      "conv1d_norm_plan_info", "conv1d_norm_run", "conv1d_norm_run_ex", "conv1d_norm_pack_weights",
-                     "conv1d_norm_check", "conv1d_norm_run_static_scratch"):
+                     "conv1d_norm_check", "conv1d_norm_run_static_scratch", "conv1d_norm_set_profiling",
+                     "conv1d_norm_kernel_times"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -175,6 +183,18 @@ def conv1d_norm_check(desc: int, workspace: Optional[int], stream: int) -> None:
     _check(load().conv1d_norm_check(desc, workspace, stream))
 
 
+def conv1d_norm_set_profiling(desc: int, enable: bool) -> None:
+    _check(load().conv1d_norm_set_profiling(desc, 1 if enable else 0))
+
+
+def conv1d_norm_kernel_times(desc: int):
+    """[(kernel name, ms)] of the last profiled run, in launch order (waits for it to finish)."""
+    buf = (KernelTime * 8)()
+    n = ctypes.c_int32()
+    _check(load().conv1d_norm_kernel_times(desc, buf, 8, ctypes.byref(n)))
+    return [(buf[i].name.decode(), float(buf[i].ms)) for i in range(min(n.value, 8))]
+
+
 def conv1d_norm_destroy(desc: int) -> None:
     load().conv1d_norm_destroy(desc)
 
@@ -236,6 +256,12 @@ class Conv1dNorm:
         import torch
         s = torch.cuda.current_stream().cuda_stream if stream is None else stream
         conv1d_norm_check(self.desc, None, s)
+
+    def set_profiling(self, enable: bool = True) -> None:
+        conv1d_norm_set_profiling(self.desc, enable)
+
+    def kernel_times(self):
+        return conv1d_norm_kernel_times(self.desc)
 
     def close(self):
         if getattr(self, "desc", None):

@@ -34,6 +34,13 @@ struct c1n_desc {
     CUtensorMap tm_y;  // output map (TMA store of the fused GroupNorm tile)
     int device = -1;
     int num_sms = 0;
+    // kernel timing (conv1d_norm_set_profiling): one event before each launch of a run, one after
+    static constexpr int kMaxMarks = 8;
+    int profiling = 0;
+    int events_ready = 0;
+    int n_marks = 0;
+    cudaEvent_t ev[kMaxMarks] = {};
+    const char* ev_name[kMaxMarks] = {};
 };
 
 namespace {
@@ -107,30 +114,40 @@ void plan_channel_blocks(const c1n_params& p, Plan& pl) {
     pl.b_slot_bytes = pl.BN * 128;
 }
 
-// Ring depths from the shared-memory budget (one CTA per SM).
+// Ring depths from the shared-memory budget (one CTA per SM), after the output staging area.
+// The weight and x-staging rings give way first, down to three slots, then to two.
 void plan_stages(Plan& pl, int max_a, int max_b, int max_s) {
     const int budget = 227 * 1024 - 1024 - kTcMiscBytes;
     pl.stages_a = max_a;
     pl.stages_b = max_b;
     pl.stages_s = pl.s_slot_bytes > 0 ? max_s : 0;
     auto total = [&]() {
-        return pl.stages_a * pl.a_slot_bytes + pl.stages_b * pl.b_slot_bytes + pl.stages_s * pl.s_slot_bytes;
+        return pl.stages_a * pl.a_slot_bytes + pl.stages_b * pl.b_slot_bytes + pl.stages_s * pl.s_slot_bytes +
+               pl.o_bytes;
     };
+    while (total() > budget && pl.stages_b > 3) --pl.stages_b;
+    while (total() > budget && pl.stages_s > 3) --pl.stages_s;
     while (total() > budget && pl.stages_b > 2) --pl.stages_b;
     while (total() > budget && pl.stages_s > 2) --pl.stages_s;
     while (total() > budget && pl.stages_a > 2) --pl.stages_a;
     pl.smem_bytes = 1024 + total() + kTcMiscBytes;
 }
 
-// CTA pairs (cta_group::2) need an MMA N that splits into two halves of whole 16-row groups, and
-// are used unless the caller asked for single CTAs.
-bool pair_ok(const c1n_params& p, const Plan& pl) { return p.mainloop != C1N_MAINLOOP_SINGLE && pl.BN % 32 == 0; }
+// CTA pairs (cta_group::2) need an MMA N that splits into two halves of whole 16-row groups. AUTO
+// uses them for the Linear GEMM (measured 0.88 vs 0.70 of tensor peak on 1024x8192x8192) but not
+// for the convolution, whose A tiles are rebuilt by each CTA's transposer warps and where one CTA
+// per tile measured faster (causal 32x256x8192 k4: 0.185 vs 0.204 ms).
+bool pair_ok(const c1n_params& p, const Plan& pl, bool linear) {
+    if (pl.BN % 32 != 0 || p.mainloop == C1N_MAINLOOP_SINGLE) return false;
+    return linear || p.mainloop == C1N_MAINLOOP_PAIR;
+}
 
 // Geometry of the tensor-core conv tiles: 128 output time steps x BN channels per tile (256 steps
 // for a CTA pair, 128 per CTA); the A tile carries the (k-1)*dilation halo rows. `cluster` selects
 // one CTA per tile with single-buffered TMEM (cluster GroupNorm) instead of the persistent
-// double-buffered layout.
-bool plan_tc_geometry(const c1n_params& p, Plan& pl, bool cluster, bool pair = false) {
+// double-buffered layout; `o_bytes` reserves output staging.
+bool plan_tc_geometry(const c1n_params& p, Plan& pl, bool cluster, bool pair = false, int o_bytes = 0) {
+    pl.o_bytes = o_bytes;
     pl.BK = pl.bf16 ? 64 : 32;
     const long long halo = (long long)(p.k - 1) * p.dilation;
     pl.R = (int)round_up(128 + halo, 8);
@@ -145,7 +162,7 @@ bool plan_tc_geometry(const c1n_params& p, Plan& pl, bool cluster, bool pair = f
     pl.n_ci_chunks = (int)ceil_div(p.C_in, pl.BK);
     pl.ci_pad = pl.n_ci_chunks * pl.BK;
     plan_channel_blocks(p, pl);
-    pl.pair = (pair && !cluster && pair_ok(p, pl)) ? 1 : 0;
+    pl.pair = (pair && !cluster && pair_ok(p, pl, false)) ? 1 : 0;
     if (pl.pair) pl.b_slot_bytes = pl.BN / 2 * 128;
     pl.cb_per_unit = 1;
     pl.n_t_tiles = (int)ceil_div(pl.T_out, pl.pair ? 256 : 128);
@@ -169,7 +186,7 @@ bool plan_tc_linear(const c1n_params& p, Plan& pl) {
     pl.n_ci_chunks = (int)ceil_div(p.C_in, pl.BK);
     pl.ci_pad = 0;
     plan_channel_blocks(p, pl);
-    pl.pair = pair_ok(p, pl) ? 1 : 0;
+    pl.pair = pair_ok(p, pl, true) ? 1 : 0;
     if (pl.pair) pl.b_slot_bytes = pl.BN / 2 * 128;
     pl.cb_per_unit = 1;
     pl.n_t_tiles = (int)ceil_div(p.N, pl.pair ? 256 : 128);  // row tiles
@@ -278,17 +295,21 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
             if (want == C1N_PATH_TC_FUSED_GN || want == C1N_PATH_TC_FUSED_GN_DSMEM)
                 why = "fused GroupNorm needs groups inside a channel block, no row-min, and the CTAs of a sample "
                       "in one cluster (<= 8) or the whole grid resident at once";
-            // 1b. Channel LayerNorm fused: one CTA holds every channel (C_out <= 512) of its tile.
-            // AUTO takes it only when two accumulators fit (C_out <= 256) so the epilogue overlaps
-            // the next tile's mainloop; with 512 channels the two-pass plan is faster today.
+            // 1b. Channel LayerNorm fused. C_out <= 256: one CTA holds every channel of its tile.
+            //     256 < C_out <= 512: the two CTAs of a cluster hold one channel half each of the
+            //     same 128 time steps and exchange per-step partial sums through distributed shared
+            //     memory. Either way each CTA keeps two accumulators, so the epilogue of one tile
+            //     overlaps the mainloop of the next.
             if (!*why && p.norm == C1N_NORM_CHANNEL_LAYER && p.post != C1N_POST_ROWMIN_BIAS && p.C_out <= 512 &&
-                (want == C1N_PATH_TC_FUSED_LN || (want == C1N_PATH_AUTO && p.C_out <= 256))) {
+                (want == C1N_PATH_AUTO || want == C1N_PATH_TC_FUSED_LN)) {
                 Plan ln = pl;
-                if (plan_tc_geometry(p, ln, false, true)) {
-                    ln.cb_per_unit = ln.n_cb;
+                const bool two = p.C_out > 256;
+                if (plan_tc_geometry(p, ln, false, !two, 4 * 2 * 32 * 32 * ln.esize)) {
+                    ln.cb_per_unit = two ? 1 : ln.n_cb;
                     ln.n_units = p.N * ln.n_t_tiles;
-                    ln.n_acc = ln.n_cb == 1 ? 2 : 1;  // two accumulators only when they fit in TMEM
+                    ln.n_acc = 2;
                     ln.tmem_cols = 512;
+                    ln.cluster = two ? 2 : 1;
                     pl = ln;
                     pl.path = C1N_PATH_TC_FUSED_LN;
                     plan_workspace(p, pl, true, false, false);
@@ -406,7 +427,33 @@ c1n_status ensure_device(c1n_desc* d) {
     return C1N_OK;
 }
 
+// Records a timing event before the launch of kernel `name` (nullptr: after the last one).
+void mark(c1n_desc* d, cudaStream_t s, const char* name) {
+    if (!d->profiling || !d->events_ready || d->n_marks >= c1n_desc::kMaxMarks) return;
+    if (cudaEventRecord(d->ev[d->n_marks], s) == cudaSuccess) d->ev_name[d->n_marks++] = name;
+}
+
+c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s);
+
 c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
+    d->n_marks = 0;
+    if (d->profiling && !d->events_ready) {
+        for (int i = 0; i < c1n_desc::kMaxMarks; ++i) {
+            cudaError_t e = cudaEventCreate(&d->ev[i]);
+            if (e != cudaSuccess) {
+                for (int j = 0; j < i; ++j) cudaEventDestroy(d->ev[j]);
+                return cuda_fail(e, "cudaEventCreate (profiling)");
+            }
+        }
+        d->events_ready = 1;
+    }
+    c1n_status st = run_body(d, a, s);
+    if (st == C1N_OK) mark(d, s, nullptr);
+    else d->n_marks = 0;
+    return st;
+}
+
+c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
     const c1n_params& p = d->p;
     const Plan& pl = d->plan;
     if (!a->x || !a->w || !a->y) return fail(C1N_ERR_INVALID_ARG, "x, w and y must be non-NULL");
@@ -429,6 +476,7 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
     cudaError_t e;
 
     if (pl.path == C1N_PATH_SIMT) {
+        mark(d, s, "simt_conv");
         e = launch_simt_conv(p, pl, a->x, a->w, a->b, second ? static_cast<void*>(raw) : a->y, second, s);
         if (e != cudaSuccess) return cuda_fail(e, "SIMT conv launch");
     } else {
@@ -440,6 +488,7 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
             void* wp = wsb + pl.ws_wp;
             if (!(a->flags & C1N_FLAG_WEIGHTS_PACKED)) {
                 unsigned* zero = pl.gsync_count ? reinterpret_cast<unsigned*>(wsb + pl.ws_gsync) : nullptr;
+                mark(d, s, "pack_weights");
                 e = launch_pack_weights(p, pl, a->w, wp, s, zero, pl.gsync_count);
                 if (e != cudaSuccess) return cuda_fail(e, "weight pack launch");
             }
@@ -480,16 +529,21 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
             d->tm_w_ptr = wsrc;
         }
         const bool fused_gn = pl.path == C1N_PATH_TC_FUSED_GN || pl.path == C1N_PATH_TC_FUSED_GN_DSMEM;
+        const bool fused_ln_path = pl.path == C1N_PATH_TC_FUSED_LN;
         // The fused GroupNorm tile is stored by one TMA bulk store when y's rows are 16-byte
-        // multiples and the staging tile fits in the operand rings.
-        const bool tma_store = fused_gn && aligned16(a->y) && (pl.T_out * pl.esize) % 16 == 0 &&
-                               (size_t)pl.BN * 128 * pl.esize <=
-                                   (size_t)pl.stages_b * pl.b_slot_bytes + (size_t)pl.stages_s * pl.s_slot_bytes;
+        // multiples and the staging tile fits in the operand rings. The fused LayerNorm stores
+        // 32 x 32 tiles staged per warp; their 32-channel boxes must not reach into the other
+        // CTA's channel half (BN a multiple of 32 when the channels are split).
+        const bool y_tma_ok = aligned16(a->y) && (pl.T_out * pl.esize) % 16 == 0;
+        const bool tma_store =
+            y_tma_ok && ((fused_gn && (size_t)pl.BN * 128 * pl.esize <=
+                                          (size_t)pl.stages_b * pl.b_slot_bytes + (size_t)pl.stages_s * pl.s_slot_bytes) ||
+                         (fused_ln_path && pl.o_bytes > 0 && (pl.n_cb == 1 || pl.BN % 32 == 0)));
         if (tma_store && d->tm_y_ptr != a->y) {
             const cuuint64_t es = (cuuint64_t)pl.esize;
             cuuint64_t dy[3] = {(cuuint64_t)pl.T_out, (cuuint64_t)p.C_out, (cuuint64_t)p.N};
             cuuint64_t sy[2] = {(cuuint64_t)pl.T_out * es, (cuuint64_t)pl.T_out * p.C_out * es};
-            cuuint32_t by[3] = {128u, (cuuint32_t)pl.BN, 1};
+            cuuint32_t by[3] = {fused_ln_path ? 32u : 128u, fused_ln_path ? 32u : (cuuint32_t)pl.BN, 1};
             st = encode(&d->tm_y, a->y, pl.bf16, 3, dy, sy, by, CU_TENSOR_MAP_SWIZZLE_NONE);
             if (st != C1N_OK) return st;
             d->tm_y_ptr = a->y;
@@ -507,6 +561,8 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         t.cpg = p.C_out / t.groups;
         t.sub = (t.cpg == 4 || t.cpg == 8) ? t.cpg : (t.cpg % 16 == 0 ? 16 : 0);
         t.tma_store = tma_store ? 1 : 0;
+        t.o_bytes = pl.o_bytes;
+        t.o_off = pl.stages_a * pl.a_slot_bytes + pl.stages_b * pl.b_slot_bytes + pl.stages_s * pl.s_slot_bytes;
         t.gpart = reinterpret_cast<float4*>(wsb + pl.ws_gpart);
         t.gsync = reinterpret_cast<unsigned*>(wsb + pl.ws_gsync);
         t.row_cpg = (pl.row_epilogue && p.norm == C1N_NORM_GROUP) ? p.C_out / p.groups : 0;
@@ -514,8 +570,10 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         t.rowpart = reinterpret_cast<float2*>(wsb + pl.ws_rowpart);
         t.eps = p.eps;
         const bool fused_ln = pl.path == C1N_PATH_TC_FUSED_LN;
-        t.gelu = (p.post == C1N_POST_GELU_ERF && (pl.path == C1N_PATH_TC_DIRECT || fused_gn || fused_ln ||
-                                                  pl.row_epilogue)) ? 1 : 0;
+        // GELU in the kernel whenever no later pass sees the values (the normalize pass applies it
+        // otherwise).
+        const bool last_pass = pl.path == C1N_PATH_TC_DIRECT || fused_gn || fused_ln || pl.row_epilogue || !second;
+        t.gelu = (p.post == C1N_POST_GELU_ERF && last_pass) ? 1 : 0;
         const uint32_t fmt = pl.bf16 ? 1u : 2u;
         t.idesc = make_idesc(fmt, fmt, 0u, 0u, pl.pair ? 256u : 128u, (uint32_t)pl.BN);
         t.x = a->x;
@@ -527,7 +585,7 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         t.status = status;
         const bool out_bf16 = pl.bf16 && (fused_out || !second);
         int epi = kEpiDirect;
-        if (fused_ln) epi = kEpiLN;
+        if (fused_ln) epi = pl.cluster == 2 ? kEpiLNX : kEpiLN;
         if (pl.row_epilogue) epi = kEpiRowGN;
         if (fused_gn) {
             // Cooperative grid when every CTA fits on the device at once (one per SM), else a cluster.
@@ -537,9 +595,11 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
             else return fail(C1N_ERR_UNSUPPORTED, "fused GroupNorm grid of %d CTAs exceeds the %d SMs of this device",
                              pl.n_units, d->num_sms);
         }
+        mark(d, s, "tc_conv");
         e = launch_tc(pl, t, d->tm_a, d->tm_b, tma_store ? d->tm_y : d->tm_b, linear, epi, out_bf16, d->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
         if (pl.row_epilogue && p.post == C1N_POST_ROWMIN_BIAS) {
+            mark(d, s, "rowmin_finish");
             e = launch_rowmin_finish(p, pl, t.rowpart, a->bias2, a->y, a->argmin, s);
             if (e != cudaSuccess) return cuda_fail(e, "row-min finisher launch");
         }
@@ -547,16 +607,20 @@ c1n_status run_impl(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
     }
     if (!second) return C1N_OK;
     if (need_stats) {
+        mark(d, s, p.norm == C1N_NORM_GROUP ? "gn_stats" : "ln_stats");
         e = p.norm == C1N_NORM_GROUP ? launch_gn_stats(p, pl, raw, stats, s) : launch_ln_stats(p, pl, raw, stats, s);
         if (e != cudaSuccess) return cuda_fail(e, "statistics launch");
     }
     if (p.post == C1N_POST_ROWMIN_BIAS) {
+        mark(d, s, "rowmin");
         e = launch_rowmin(p, pl, raw, stats, need_stats ? a->gamma : nullptr, need_stats ? a->beta : nullptr, rowmin,
                           a->argmin, s);
         if (e != cudaSuccess) return cuda_fail(e, "row-min launch");
+        mark(d, s, "broadcast");
         e = launch_broadcast(p, pl, rowmin, a->bias2, a->y, s);
         if (e != cudaSuccess) return cuda_fail(e, "broadcast launch");
     } else {
+        mark(d, s, "normalize");
         e = launch_normalize(p, pl, raw, stats, a->gamma, a->beta, a->y, s);
         if (e != cudaSuccess) return cuda_fail(e, "normalize launch");
     }
@@ -687,7 +751,38 @@ c1n_status conv1d_norm_check(const c1n_desc* desc, void* workspace, c1n_stream_t
     return C1N_OK;
 }
 
-void conv1d_norm_destroy(c1n_desc* desc) { delete desc; }
+c1n_status conv1d_norm_set_profiling(c1n_desc* desc, int32_t enable) {
+    if (!desc) return fail(C1N_ERR_INVALID_ARG, "desc is NULL");
+    desc->profiling = enable ? 1 : 0;
+    desc->n_marks = 0;
+    return C1N_OK;
+}
+
+c1n_status conv1d_norm_kernel_times(c1n_desc* desc, c1n_kernel_time* out, int32_t capacity, int32_t* count) {
+    if (!desc || !count || (capacity > 0 && !out)) return fail(C1N_ERR_INVALID_ARG, "NULL argument");
+    *count = 0;
+    const int n = desc->n_marks;
+    if (n < 2) return C1N_OK;
+    cudaError_t e = cudaEventSynchronize(desc->ev[n - 1]);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize (profiling)");
+    int k = 0;
+    for (int i = 0; i + 1 < n && k < capacity; ++i, ++k) {
+        float ms = 0.f;
+        e = cudaEventElapsedTime(&ms, desc->ev[i], desc->ev[i + 1]);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime (profiling)");
+        std::memset(out[k].name, 0, sizeof(out[k].name));
+        std::snprintf(out[k].name, sizeof(out[k].name), "%s", desc->ev_name[i]);
+        out[k].ms = ms;
+    }
+    *count = n - 1;
+    return C1N_OK;
+}
+
+void conv1d_norm_destroy(c1n_desc* desc) {
+    if (desc && desc->events_ready)
+        for (int i = 0; i < c1n_desc::kMaxMarks; ++i) cudaEventDestroy(desc->ev[i]);
+    delete desc;
+}
 
 const char* conv1d_norm_status_string(c1n_status s) {
     switch (s) {

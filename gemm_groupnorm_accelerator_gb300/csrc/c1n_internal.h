@@ -39,6 +39,7 @@ struct Plan {
     int grid = 0;
     int stages_a = 0, stages_b = 0, stages_s = 0;
     int a_slot_bytes = 0, b_slot_bytes = 0, s_slot_bytes = 0;
+    int o_bytes = 0;      // output staging (fused LayerNorm: 4 warps x 2 tiles of 32 x 32 elements)
     int smem_bytes = 0;
     int kernels = 0;
     // workspace layout (byte offsets)
@@ -60,7 +61,9 @@ struct TcArgs {
     int RS, t_shift, stages_s, s_slot_bytes;  // x staging ring (conv mode)
     int groups, cpg;
     int sub;        // channels per partial-sum run in the GroupNorm statistics (4, 8, 16; 0 = per column)
-    int tma_store;  // fused GroupNorm: store the tile with one TMA bulk store
+    int tma_store;  // fused GroupNorm / LayerNorm: store the output through TMA bulk stores
+    int o_off;      // LayerNorm: byte offset of the per-warp output staging tiles in shared memory
+    int o_bytes;    // ... and their size (shared memory between the operand rings and the barriers)
     float eps;
     int gelu;
     uint32_t idesc;
@@ -102,7 +105,8 @@ cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void*
 
 // Tensor-core kernels. `tm_a`: x (conv mode, staged time-contiguous boxes) or X (Linear mode);
 // `tm_b`: packed weights (conv mode) or W (Linear mode).
-enum TcEpilogue { kEpiDirect = 0, kEpiClusterGN = 1, kEpiGridGN = 2, kEpiRowGN = 3, kEpiLN = 4 };
+// kEpiLNX: channel LayerNorm over the two channel halves held by the two CTAs of a cluster.
+enum TcEpilogue { kEpiDirect = 0, kEpiClusterGN = 1, kEpiGridGN = 2, kEpiRowGN = 3, kEpiLN = 4, kEpiLNX = 5 };
 cudaError_t launch_tc(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                       const CUtensorMap& tm_y, bool linear, int epilogue, bool out_bf16, int num_sms,
                       cudaStream_t stream);

@@ -50,10 +50,35 @@ constexpr int kEpiThreads = 128, kXpThreads = 32 * kXpWarps;
 // Where a bounded wait gave up (status word detail).
 enum WaitSite {
     kWaitAEmpty = 1, kWaitBEmpty, kWaitAFull, kWaitBFull, kWaitAccEmpty, kWaitAccFull, kWaitDrain, kWaitSEmpty,
-    kWaitSFull, kWaitGridPeers
+    kWaitSFull, kWaitGridPeers, kWaitExchange
 };
 
-__device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
+// Exact (erf) GELU, 0.5 z (1 + erf(z / sqrt 2)), with erf from the rational-exponential
+// approximation 7.1.26 of Abramowitz & Stegun's Handbook of Mathematical Functions (Hastings):
+// erf(x) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-x^2), t = 1 / (1 + p x), x >= 0, with
+// |error| <= 1.5e-7; odd symmetry for x < 0. The reciprocal and exp2 use the hardware
+// approximations (a few ulp), which keeps the GELU error below 1e-6 * |z| -- far inside the fp32
+// and bf16 output tolerances -- at about a dozen instructions.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float exp2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float gelu_erf(float z) {
+    const float x = fabsf(z) * 0.70710678118654752f;
+    const float t = rcp_approx(fmaf(0.3275911f, x, 1.0f));
+    const float poly =
+        t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
+    const float e = exp2_approx(-x * x * 1.4426950408889634f);
+    const float erf_abs = fmaf(-poly, e, 1.0f);
+    const float erf_v = copysignf(erf_abs, z);
+    return 0.5f * z * (1.0f + erf_v);
+}
 
 __device__ __forceinline__ float load_in(const float* p) { return __ldg(p); }
 __device__ __forceinline__ float load_in(const __nv_bfloat16* p) { return __bfloat162float(*p); }
@@ -202,6 +227,16 @@ __device__ __forceinline__ void tma_store_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// At most one of this thread's bulk stores may still be reading its shared-memory source.
+__device__ __forceinline__ void tma_store_wait_read_le1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// Every bulk store issued by this thread has completed (its writes are done).
+__device__ __forceinline__ void tma_store_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 struct Unit {
     int n;     // sample (conv) / 0 (Linear)
     int row0;  // first output time step (conv) / first row (Linear)
@@ -234,7 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_conv_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tm_a,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_y) {
     constexpr bool kFusedGN = EPI == kEpiClusterGN || EPI == kEpiGridGN;
-    static_assert(!(PAIR && kFusedGN), "the fused GroupNorm grid / cluster exchange runs one CTA per tile");
+    // kEpiLNX: the two CTAs of a cluster hold the two channel halves of the same 128 rows and
+    // exchange per-row LayerNorm partial sums through distributed shared memory.
+    constexpr bool kClusterX = EPI == kEpiLNX;
+    static_assert(!(PAIR && (kFusedGN || kClusterX)), "the exchanging epilogues run one CTA per tile");
     using InT = typename std::conditional<BF16, __nv_bfloat16, float>::type;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -243,11 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sB = sA + uint32_t(SA * a.a_slot_bytes);
     const size_t s_off = size_t(SA) * a.a_slot_bytes + size_t(SB) * a.b_slot_bytes;  // x staging ring
     const uint32_t sS = sA + uint32_t(s_off);
-    uint8_t* misc = base + s_off + size_t(SS) * a.s_slot_bytes;
+    uint8_t* misc = base + s_off + size_t(SS) * a.s_slot_bytes + size_t(a.o_bytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
     const int i_afull = 0, i_aempty = SA, i_bfull = 2 * SA, i_bempty = 2 * SA + SB, i_accfull = 2 * SA + 2 * SB,
               i_accempty = i_accfull + 2, i_drain = i_accempty + 2, i_sfull = i_drain + 1, i_sempty = i_sfull + SS,
-              n_bars = i_sempty + SS;
+              i_ex = i_sempty + SS, n_bars = i_ex + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + n_bars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // progress counters: [0] B loads issued, [1] A chunks consumed by the MMA, [2] units issued by
@@ -263,7 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int taps = LINEAR ? 1 : a.k;
     // CTA pair (cta_group::2): rank 0 issues the MMAs over both CTAs' operands and owns the
     // full / accumulator-empty barriers; rank 1 signals those through the cluster.
-    const uint32_t rank = PAIR ? (cluster_ctarank() & 1u) : 0u;
+    const uint32_t crank = (PAIR || kClusterX) ? (cluster_ctarank() & 1u) : 0u;
+    const uint32_t rank = PAIR ? crank : 0u;
     const bool leader = rank == 0;
     // Bounded wait with an inline first test (the common case in a full pipeline costs no call).
     auto wait_bar = [&](int i, uint32_t parity, int site) -> bool {
@@ -278,6 +317,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto leader_bar = [&](int i) -> uint32_t {
         if constexpr (PAIR) return map_shared_rank(bar(i), 0);
         else return bar(i);
+    };
+    // Unit u of this CTA; with kEpiLNX a unit is one (sample, 128-row tile) and the cluster rank
+    // picks the channel half.
+    auto decode = [&](int u) -> Unit {
+        if constexpr (kClusterX) {
+            Unit r;
+            r.n = u / a.n_t_tiles;
+            r.row0 = (u - r.n * a.n_t_tiles) * 128;
+            r.cbu = int(crank);
+            return r;
+        } else {
+            return decode_unit<LINEAR, PAIR>(a, u, rank);
+        }
     };
     auto arrive_leader = [&](int i) {
         if (PAIR && !leader) mbar_arrive_cluster(leader_bar(i));
@@ -299,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(i_accempty + i), PAIR ? 8 : 4);  // one arrival per epilogue warp (of the pair)
         }
         mbar_init(bar(i_drain), 1);
+        for (int i = 0; i < 2; ++i) mbar_init(bar(i_ex + i), kEpiThreads);  // the peer's epilogue threads
         for (int i = 0; i < SS; ++i) {
             mbar_init(bar(i_sfull + i), 1);
             mbar_init(bar(i_sempty + i), kXpWarps);  // one arrival per transposer warp
@@ -319,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     tc_fence_before();
-    if (PAIR) cluster_sync_all();  // the peer's barriers are initialized before any remote arrival
+    if (PAIR || kClusterX) cluster_sync_all();  // the peer's barriers exist before any remote arrival
     else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
@@ -328,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kFusedGN) {
         first_unit = (blockIdx.z * a.n_t_tiles + blockIdx.x) * (a.n_cb / a.cb_per_unit) + blockIdx.y;
         unit_step = a.n_units;  // exactly one unit
-    } else if (PAIR) {
-        first_unit = blockIdx.x >> 1;  // one unit per CTA pair (cluster of two)
+    } else if (PAIR || kClusterX) {
+        first_unit = blockIdx.x >> 1;  // one unit per cluster of two
         unit_step = gridDim.x >> 1;
     } else {
         first_unit = blockIdx.x;
@@ -356,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tx_stage = tx_mult * uint32_t(a.b_slot_bytes + (LINEAR ? a.a_slot_bytes : 0));
         const int co_half = PAIR ? int(rank) * (a.BN / 2) : 0;
         for (int u = first_unit; u < a.n_units && !aborting(); u += unit_step) {
-            const Unit un = decode_unit<LINEAR, PAIR>(a, u, rank);
+            const Unit un = decode(u);
             for (int c = 0; c < a.n_ci_chunks; ++c) {
                 for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
                     const int co0 = (un.cbu * a.cb_per_unit + cbi) * a.BN + co_half;
@@ -488,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t sph = 0;
             long long s_cnt = 0;
             for (int u = first_unit; u < a.n_units && !*abort_flag; u += unit_step) {
-                const Unit un = decode_unit<LINEAR, PAIR>(a, u, rank);
+                const Unit un = decode(u);
                 const int t0 = un.row0 - a.pad_left - a.t_shift;  // multiple of 16 bytes of elements
                 for (int c = 0; c < a.n_ci_chunks; ++c) {
                     if (!mbar_wait(bar(i_sempty + si), sph ^ 1, abort_flag, a.status, kWaitSEmpty, prog)) goto xld_done;
@@ -572,10 +625,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // element loops below read them with conflict-free broadcast loads instead of global loads.
         float* s_bias = epi + 3072;  // [256]
         int staged_co = -1;
+        int obuf = 0;  // LayerNorm output staging: which of this warp's two tiles is next
         if (kFusedGN && first_unit < a.n_units) {
             // One unit per CTA: stage bias, gamma and beta of its channel block while the
             // mainloop runs (gamma and beta go where the column scale / shift end up).
-            const int co_base = decode_unit<LINEAR, PAIR>(a, first_unit, rank).cbu * a.BN;
+            const int co_base = decode(first_unit).cbu * a.BN;
             const int ncols = min(a.BN, a.C_out - co_base);
             for (int col = er; col < 256; col += kEpiThreads) {
                 const bool ok = col < ncols;
@@ -600,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (er == 0) prog[7] = 0;
             tc_fence_after();
-            const Unit un = decode_unit<LINEAR, PAIR>(a, u, rank);
+            const Unit un = decode(u);
             OutT* y = static_cast<OutT*>(a.y);
             const int row = un.row0 + m;
             const bool row_ok = LINEAR ? (row < a.N) : (row < a.T_out);
@@ -691,63 +745,99 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (a.rowmin && row_ok)
                     a.rowpart[(size_t)row * a.n_cb + un.cbu] = make_float2(best, __int_as_float(best_i));
-            } else if (EPI == kEpiLN) {
+            } else if (EPI == kEpiLN || EPI == kEpiLNX) {
                 // ------------------------------------------------ channel LayerNorm (conv mode)
-                // All C_out channels of the tile sit in TMEM (cb_per_unit blocks at 256-column
-                // steps); one thread owns one time step: mean, then squared deviations, then
-                // normalize + affine (+ GELU) and store (a warp stores 32 consecutive steps).
-                float* s_gamma = epi + 512;
-                float* s_beta = epi + 1024;
+                // One thread owns one time step. kEpiLN: this CTA holds every channel of the tile.
+                // kEpiLNX: it holds channels [crank*BN, crank*BN + BN) and its cluster peer the rest
+                // of the same 128 steps. Statistics: one pass of sums shifted by the step's first
+                // value gives this half's mean and M2; kEpiLNX exchanges them with the peer
+                // (distributed shared memory + a remote arrival) and both merge the halves with
+                // Chan's formula in rank order, so both compute the same mean and variance. Then
+                // normalize + affine (+ GELU), staged per warp as [32 channels][32 steps] tiles in
+                // shared memory and written by TMA bulk stores (or direct stores when y's layout
+                // does not allow TMA).
+                float* s_bias = epi;
+                float* s_gamma = epi + 256;
+                float* s_beta = epi + 512;
+                float* xbuf = epi + 768;  // [2][128]: the peer's mean and M2 per step
+                const int co_base = un.cbu * a.BN;
+                const int ncols = min(a.BN, a.C_out - co_base);
                 if (staged_co < 0) {
-                    for (int c = er; c < 512; c += kEpiThreads) {
-                        const bool ok = c < a.C_out;
-                        epi[c] = (ok && a.bias) ? __ldg(a.bias + c) : 0.f;
-                        s_gamma[c] = ok ? (a.gamma ? __ldg(a.gamma + c) : 1.f) : 0.f;
-                        s_beta[c] = (ok && a.beta) ? __ldg(a.beta + c) : 0.f;
+                    for (int c = er; c < 256; c += kEpiThreads) {
+                        const bool ok = c < ncols;
+                        s_bias[c] = (ok && a.bias) ? __ldg(a.bias + co_base + c) : 0.f;
+                        s_gamma[c] = ok ? (a.gamma ? __ldg(a.gamma + co_base + c) : 1.f) : 0.f;
+                        s_beta[c] = (ok && a.beta) ? __ldg(a.beta + co_base + c) : 0.f;
                     }
                     named_bar_sync(1, kEpiThreads);
-                    staged_co = 0;
+                    staged_co = co_base;
                 }
-                const float* ln_bias = epi;
-                const uint32_t tb0 = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab * a.cb_per_unit);
-                float sum = 0.f;
-                for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
-                    const int cb0 = cbi * a.BN, ncols = min(a.BN, a.C_out - cb0);
-                    for (int j0 = 0; j0 < ncols; j0 += 32) {
-                        float v[32];
-                        tmem_load32(tb0 + uint32_t(256 * cbi + j0), v);
+                const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
+                float shift = 0.f, s1 = 0.f, s2 = 0.f;
+                for (int j0 = 0; j0 < ncols; j0 += 32) {
+                    float v[32];
+                    tmem_load32(tb + uint32_t(j0), v);
+                    if (j0 == 0) shift = v[0] + s_bias[0];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (j0 + i < ncols) sum += v[i] + ln_bias[cb0 + j0 + i];
-                    }
-                }
-                const float mean = sum / float(a.C_out);
-                float ss = 0.f;
-                for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
-                    const int cb0 = cbi * a.BN, ncols = min(a.BN, a.C_out - cb0);
-                    for (int j0 = 0; j0 < ncols; j0 += 32) {
-                        float v[32];
-                        tmem_load32(tb0 + uint32_t(256 * cbi + j0), v);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (j0 + i < ncols) {
-                                const float d = v[i] + ln_bias[cb0 + j0 + i] - mean;
-                                ss = fmaf(d, d, ss);
-                            }
-                    }
-                }
-                const float rstd = rsqrtf(ss / float(a.C_out) + a.eps);
-                for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
-                    const int cb0 = cbi * a.BN, ncols = min(a.BN, a.C_out - cb0);
-                    OutT* dst = y + ((long long)un.n * a.C_out + cb0) * a.T_out + row;
-                    for (int j0 = 0; j0 < ncols; j0 += 32) {
-                        float v[32];
-                        tmem_load32(tb0 + uint32_t(256 * cbi + j0), v);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int c = cb0 + j0 + i;
-                            v[i] = fmaf((v[i] + ln_bias[c] - mean) * rstd, s_gamma[c], s_beta[c]);
+                    for (int i = 0; i < 32; ++i)
+                        if (j0 + i < ncols) {
+                            const float d = v[i] + s_bias[j0 + i] - shift;
+                            s1 += d;
+                            s2 = fmaf(d, d, s2);
                         }
+                }
+                const float n_own = float(ncols);
+                float mean = shift + s1 / n_own;
+                float m2 = fmaxf(s2 - s1 * (s1 / n_own), 0.f);
+                if constexpr (kClusterX) {
+                    const uint32_t peer = crank ^ 1u;
+                    st_shared_cluster_f32(map_shared_rank(smem_u32(xbuf + m), peer), mean);
+                    st_shared_cluster_f32(map_shared_rank(smem_u32(xbuf + 128 + m), peer), m2);
+                    mbar_arrive_cluster(map_shared_rank(bar(i_ex), peer));
+                    mbar_wait_cluster(bar(i_ex), uint32_t(lt & 1), abort_flag, a.status, kWaitExchange, prog);
+                    const float n_peer = float(a.C_out - ncols);
+                    const float p_mean = xbuf[m], p_m2 = xbuf[128 + m];
+                    // Chan's merge of (rank 0 half, rank 1 half)
+                    const float na = crank == 0 ? n_own : n_peer, nb = crank == 0 ? n_peer : n_own;
+                    const float ma = crank == 0 ? mean : p_mean, mb = crank == 0 ? p_mean : mean;
+                    const float Ma = crank == 0 ? m2 : p_m2, Mb = crank == 0 ? p_m2 : m2;
+                    const float nt = na + nb, dlt = mb - ma;
+                    mean = ma + dlt * (nb / nt);
+                    m2 = Ma + Mb + dlt * dlt * (na * (nb / nt));
+                }
+                const float rstd = rsqrtf(m2 / float(a.C_out) + a.eps);
+                if (a.tma_store) {
+                    OutT* ostage = reinterpret_cast<OutT*>(base + a.o_off) + q * (2 * 32 * 32);
+                    for (int j0 = 0; j0 < ncols; j0 += 32) {
+                        float v[32];
+                        tmem_load32(tb + uint32_t(j0), v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = fmaf((v[i] + (s_bias[j0 + i] - mean)) * rstd, s_gamma[j0 + i], s_beta[j0 + i]);
+                        if (a.gelu) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+                        }
+                        // the store issued from this buffer two chunks ago has read it
+                        if (lane == 0) tma_store_wait_read_le1();
+                        __syncwarp();
+                        OutT* ob = ostage + obuf * (32 * 32);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) store_out(ob + i * 32 + lane, v[i]);
+                        fence_async_shared();
+                        __syncwarp();
+                        if (lane == 0)
+                            tma_store_3d(&tm_y, smem_u32(ob), un.row0 + q * 32, co_base + j0, un.n);
+                        obuf ^= 1;
+                    }
+                } else {
+                    OutT* dst = y + ((long long)un.n * a.C_out + co_base) * a.T_out + row;
+                    for (int j0 = 0; j0 < ncols; j0 += 32) {
+                        float v[32];
+                        tmem_load32(tb + uint32_t(j0), v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = fmaf((v[i] + (s_bias[j0 + i] - mean)) * rstd, s_gamma[j0 + i], s_beta[j0 + i]);
                         if (a.gelu) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
@@ -928,6 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (threadIdx.x == kWarpEpi0 * 32) prog[4] = lt + 1;
         }
         if (EPI == kEpiClusterGN && !mid_sync_done) cluster_sync_all();
+        if ((EPI == kEpiLN || EPI == kEpiLNX) && a.tma_store && lane == 0) tma_store_wait_all();
     }
 
     if (EPI == kEpiClusterGN) {
@@ -939,9 +1030,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync_all();
     }
     __syncwarp();
-    // A pair leaves together: the leader's MMAs read the peer's shared memory and write its TMEM,
-    // and the peer's copies and arrivals target the leader's barriers.
-    if (PAIR) cluster_sync_all();
+    // A cluster leaves together: a pair leader's MMAs read the peer's shared memory and write its
+    // TMEM, the peer's copies and arrivals target the leader's barriers, and exchanging epilogues
+    // write into each other's shared memory.
+    if (PAIR || kClusterX) cluster_sync_all();
     else __syncthreads();
     if (warp == kWarpMma) {
         tc_fence_after();
@@ -974,8 +1066,8 @@ cudaError_t launch_one(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a,
         cfg.gridDim = dim3(unsigned(a.n_t_tiles), unsigned(a.n_cb / a.cb_per_unit), unsigned(a.N));
         attr[0].id = cudaLaunchAttributeCooperative;
         attr[0].val.cooperative = 1;
-    } else if (PAIR) {
-        // persistent CTA pairs: as many clusters of two as can be resident at once
+    } else if (PAIR || EPI == kEpiLNX) {
+        // persistent clusters of two: as many as can be resident at once
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
@@ -1015,6 +1107,10 @@ cudaError_t launch_tc(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, 
     if (epilogue == kEpiLN) {
         if (pl.bf16) return C1N_LAUNCH2(false, true, __nv_bfloat16, kEpiLN);
         return C1N_LAUNCH2(false, false, float, kEpiLN);
+    }
+    if (epilogue == kEpiLNX) {
+        if (pl.bf16) return C1N_LAUNCH(false, true, __nv_bfloat16, kEpiLNX, false);
+        return C1N_LAUNCH(false, false, float, kEpiLNX, false);
     }
     if (epilogue == kEpiClusterGN) {
         if (pl.bf16) return C1N_LAUNCH(false, true, __nv_bfloat16, kEpiClusterGN, false);

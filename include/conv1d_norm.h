@@ -88,12 +88,12 @@ typedef enum {
                                      all C_out <= 512 channels of a 128-step tile in TMEM */
 } c1n_path;
 
-/* Tensor-core mainloop. AUTO uses CTA pairs where the plan allows: two CTAs on neighbouring SMs
- * (a thread-block cluster of two) compute one 256-row x BN tile with tcgen05.mma.cta_group::2;
- * each CTA stages its own 128 rows of A and half of the BN columns of B, so every SM streams a
- * third less operand data per MMA. SINGLE keeps one CTA per 128-row tile; PAIR fails with
- * C1N_ERR_UNSUPPORTED where the plan cannot use pairs (fused GroupNorm, SIMT, BN not a multiple
- * of 32). */
+/* Tensor-core mainloop. PAIR: two CTAs on neighbouring SMs (a thread-block cluster of two)
+ * compute one 256-row x BN tile with tcgen05.mma.cta_group::2; each CTA stages its own 128 rows of
+ * A and half of the BN columns of B, so every SM streams a third less operand data per MMA.
+ * SINGLE: one CTA per 128-row tile. AUTO takes PAIR for the Linear plan and SINGLE for the
+ * convolution plans (the faster of the two on each). PAIR fails with C1N_ERR_UNSUPPORTED where the
+ * plan cannot use pairs (fused GroupNorm, SIMT, MMA N not a multiple of 32). */
 typedef enum { C1N_MAINLOOP_AUTO = 0, C1N_MAINLOOP_SINGLE = 1, C1N_MAINLOOP_PAIR = 2 } c1n_mainloop;
 
 typedef struct {
@@ -203,6 +203,20 @@ const char* conv1d_norm_status_string(c1n_status status);
 
 /* Message describing the last failure on the calling host thread ("" if none). */
 const char* conv1d_norm_last_error(void);
+
+/* Kernel timing. With profiling enabled, every run records a CUDA event on its stream before each
+ * kernel it launches and one after the last (event creation happens on the first such run).
+ * conv1d_norm_kernel_times() waits for the last run's final event and reports, in launch order,
+ * each kernel's name and the time between its event and the next (milliseconds, that kernel's
+ * device time when the stream runs nothing else). *count = number of kernels of the last run (0
+ * before any profiled run); at most `capacity` entries are written. Not thread-safe against a
+ * concurrent run() on the same descriptor. No counterpart on the pages: a measurement aid. */
+typedef struct {
+    char name[32];
+    float ms;
+} c1n_kernel_time;
+c1n_status conv1d_norm_set_profiling(c1n_desc* desc, int32_t enable);
+c1n_status conv1d_norm_kernel_times(c1n_desc* desc, c1n_kernel_time* out, int32_t capacity, int32_t* count);
 
 /* Library version: major*10000 + minor*100 + patch. */
 int32_t conv1d_norm_version(void);

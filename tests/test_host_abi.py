@@ -40,7 +40,7 @@ EXPECTED_PATH = {
     synth.CONV_GN.name: "tc_fused_gn",
     synth.CAUSAL_CONV.name: "tc_direct",
     synth.LINEAR_GN_ROWMIN.name: "tc_linear",
-    synth.CONV_LN_GELU_BF16.name: "tc_two_pass",
+    synth.CONV_LN_GELU_BF16.name: "tc_fused_ln",
 }
 
 
@@ -70,14 +70,38 @@ def test_conv_gn_cluster_geometry():
 @pytest.mark.parametrize("wl", [synth.CAUSAL_CONV, synth.LINEAR_GN_ROWMIN, synth.CONV_LN_GELU_BF16],
                          ids=lambda w: w.name)
 def test_cta_pair_mainloop(wl):
-    # the large contractions run on CTA pairs: 256-row tiles, each CTA stages half of the B tile
+    # CTA pairs: 256-row tiles, each CTA stages half of the B tile; AUTO pairs the Linear GEMM only
+    linear = wl is synth.LINEAR_GN_ROWMIN
     d = c1n.conv1d_norm_desc_create(_params(wl))
+    info = c1n.conv1d_norm_plan_info(d)
+    assert (info.cta_pair, info.tile_t) == ((1, 256) if linear else (0, 128))
+    c1n.conv1d_norm_destroy(d)
+    # (the 512-channel LayerNorm cluster plan exchanges statistics between single CTAs: pairs need
+    # the two-pass plan there)
+    forced = c1n.PATH_TC_TWO_PASS if wl is synth.CONV_LN_GELU_BF16 else -1
+    d = c1n.conv1d_norm_desc_create(_params(wl, mainloop=c1n.MAINLOOP_PAIR, force_path=forced))
     info = c1n.conv1d_norm_plan_info(d)
     assert (info.cta_pair, info.tile_t, info.mma_n) == (1, 256, 256)
     c1n.conv1d_norm_destroy(d)
+    if wl is synth.CONV_LN_GELU_BF16:
+        with pytest.raises(c1n.C1NError) as e:
+            c1n.conv1d_norm_desc_create(_params(wl, mainloop=c1n.MAINLOOP_PAIR))
+        assert e.value.status == c1n.ERR_UNSUPPORTED
     d = c1n.conv1d_norm_desc_create(_params(wl, mainloop=c1n.MAINLOOP_SINGLE))
     info = c1n.conv1d_norm_plan_info(d)
     assert (info.cta_pair, info.tile_t) == (0, 128)
+    c1n.conv1d_norm_destroy(d)
+
+
+def test_layer_norm_cluster_plan():
+    # 512 channels: two CTAs per 128-step tile (a cluster of two), 256 channels and two accumulators each
+    d = c1n.conv1d_norm_desc_create(_params(synth.CONV_LN_GELU_BF16))
+    info = c1n.conv1d_norm_plan_info(d)
+    assert (c1n.PATH_NAMES[info.path], info.cluster, info.mma_n, info.tile_t) == ("tc_fused_ln", 2, 256, 128)
+    assert info.n_tiles == synth.CONV_LN_GELU_BF16.N * synth.CONV_LN_GELU_BF16.T_out // 128
+    c1n.conv1d_norm_destroy(d)
+    d = c1n.conv1d_norm_desc_create(_params(synth.CONV_LN_GELU_BF16, C_out=256))
+    assert c1n.conv1d_norm_plan_info(d).cluster == 1
     c1n.conv1d_norm_destroy(d)
 
 
@@ -145,6 +169,14 @@ def test_rowmin_needs_run_ex_and_bias2():
     assert lib.conv1d_norm_run(d, 16, 16, None, None, None, 16, None) == c1n.ERR_INVALID_ARG
     args = c1n.Args(16, 16, None, None, None, None, 16, None, 4096, 1 << 40, 0)
     assert lib.conv1d_norm_run_ex(d, ctypes.byref(args), None) == c1n.ERR_INVALID_ARG
+    c1n.conv1d_norm_destroy(d)
+
+
+def test_profiling_toggle_without_a_run():
+    d = c1n.conv1d_norm_desc_create(_params(synth.CONV_GN_TINY))
+    c1n.conv1d_norm_set_profiling(d, True)
+    assert c1n.conv1d_norm_kernel_times(d) == []  # no profiled run yet
+    c1n.conv1d_norm_set_profiling(d, False)
     c1n.conv1d_norm_destroy(d)
 
 

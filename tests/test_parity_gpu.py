@@ -118,6 +118,8 @@ SMALL = {
                                                            post=synth.POST_NONE, dtype=synth.DTYPE_BF16),
     "linear_rowmin_nonorm": synth.LINEAR_GN_ROWMIN.replace(N=70, C_in=64, C_out=288, norm=synth.NORM_NONE),
     "linear_gn_cpg4_twopass": synth.LINEAR_GN_ROWMIN.replace(N=66, C_in=32, C_out=96, groups=24),
+    "linear_gelu_nonorm": synth.LINEAR_GN_ROWMIN.replace(N=140, C_in=48, C_out=96, norm=synth.NORM_NONE,
+                                                         post=synth.POST_GELU_ERF),
     "ln_gelu_bf16": synth.CONV_LN_GELU_BF16.replace(N=2, C_in=48, C_out=160, T=264),
     "ln_c384_f32": synth.CONV_LN_GELU_BF16.replace(N=2, C_in=40, C_out=384, T=200, dtype=synth.DTYPE_F32,
                                                    post=synth.POST_NONE),
@@ -130,15 +132,22 @@ SMALL = {
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
-@pytest.mark.parametrize("mode", ["auto", "simt", "single"])
+@pytest.mark.parametrize("mode", ["auto", "simt", "single", "pair"])
 def test_small_shapes(cuda_lib, name, mode):
-    # auto: the planner's choice (CTA-pair mainloop where the plan allows it); single: one CTA per
-    # 128-row tile; simt: the fp32 CUDA-core check path
+    # auto: the planner's choice; single: one CTA per 128-row tile; pair: CTA-pair (cta_group::2)
+    # mainloop where the plan allows it; simt: the fp32 CUDA-core check path
     wl = SMALL[name]
     inp = _inputs(wl)
     ref, ref_am = oracle_full(wl, inp)
     math = 1 if mode == "simt" else 0
-    mainloop = cuda_lib.MAINLOOP_SINGLE if mode == "single" else cuda_lib.MAINLOOP_AUTO
+    mainloop = {"single": cuda_lib.MAINLOOP_SINGLE, "pair": cuda_lib.MAINLOOP_PAIR}.get(mode, cuda_lib.MAINLOOP_AUTO)
+    if mode == "pair":
+        try:
+            cuda_lib.conv1d_norm_destroy(cuda_lib.conv1d_norm_desc_create(cuda_lib.make_params(
+                wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right, wl.dilation, wl.norm,
+                wl.groups, wl.eps, wl.post, wl.dtype, 0, -1, mainloop)))
+        except cuda_lib.C1NError:
+            pytest.skip("plan cannot run on CTA pairs")
     y, am, path = run_gpu(cuda_lib, wl, inp, math=math, mainloop=mainloop)
     if math == 1:
         assert path == "simt"
@@ -193,6 +202,46 @@ def test_layer_norm_fused_forced(cuda_lib, name):
     compare(wl, y, am, ref, None, path, name)
 
 
+@pytest.mark.parametrize("name,kernels", [("gn_tiny", ["pack_weights", "tc_conv"]),
+                                          ("ln_c384_f32", ["pack_weights", "tc_conv", "ln_stats", "normalize"]),
+                                          ("linear_rowmin", ["tc_conv", "rowmin_finish"]),
+                                          ("stride2_simt", ["simt_conv", "gn_stats", "normalize"])])
+def test_kernel_times_list_every_launch(cuda_lib, name, kernels):
+    # the profiling hook reports each kernel one run launches, in order, with its device time
+    wl = SMALL[name]
+    inp = _inputs(wl)
+    params = cuda_lib.make_params(wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right,
+                                  wl.dilation, wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, 0,
+                                  cuda_lib.PATH_TC_TWO_PASS if name == "ln_c384_f32" else -1)
+    op = cuda_lib.Conv1dNorm(params)
+    op.set_profiling(True)
+    x, w = _to_dev(inp["x"], False), _to_dev(inp["w"], False)
+    b, ga, be, b2 = (_to_dev(inp[k], False) for k in ("b", "gamma", "beta", "bias2"))
+    out = torch.empty((wl.N, wl.C_out, op.T_out), dtype=op.out_dtype(), device="cuda")
+    am = torch.empty((wl.N, op.T_out), dtype=torch.int32, device="cuda") if wl.post == synth.POST_ROWMIN_BIAS else None
+    op(x, w, b, ga, be, bias2=b2, out=out, argmin=am)
+    times = op.kernel_times()
+    assert [n for n, _ in times] == kernels
+    assert len(times) == op.info.kernels
+    assert all(ms > 0 for _, ms in times)
+    op.check()
+
+
+def test_gelu_accuracy_on_exact_inputs(cuda_lib):
+    # Linear with identity weights and no bias: the GEMM reproduces x exactly (x on a grid of 1/64
+    # steps is exact in tf32), so the output differs from the oracle's float64 exact-erf GELU by the
+    # kernel's GELU alone.
+    wl = synth.LINEAR_GN_ROWMIN.replace(N=384, C_in=64, C_out=64, norm=synth.NORM_NONE, post=synth.POST_GELU_ERF)
+    grid = (np.arange(wl.N * wl.C_in, dtype=np.float64) % 769 - 384) / 64.0  # -6 .. 6
+    inp = {"x": grid.astype(np.float32).reshape(wl.N, wl.C_in, 1), "w": np.eye(64, dtype=np.float32)[:, :, None],
+           "b": np.zeros(64, np.float32), "gamma": None, "beta": None, "bias2": None}
+    ref, _ = oracle_full(wl, inp)
+    y, _, path = run_gpu(cuda_lib, wl, inp)
+    assert path == "tc_linear"
+    err = np.abs(y.astype(np.float64) - ref)
+    assert err.max() < 3e-6, err.max()
+
+
 def test_repeated_calls_are_identical(cuda_lib):
     wl = SMALL["gn_c2_structure"]
     inp = _inputs(wl)
@@ -234,11 +283,11 @@ def test_causal_conv_full_sampled(cuda_lib):
     inp = _inputs(wl)
     y, _, path = run_gpu(cuda_lib, wl, inp)
     assert path == "tc_direct"
-    y1, _, _ = run_gpu(cuda_lib, wl, inp, mainloop=cuda_lib.MAINLOOP_SINGLE)
+    y1, _, _ = run_gpu(cuda_lib, wl, inp, mainloop=cuda_lib.MAINLOOP_PAIR)
     ns = [0, wl.N - 1]
     ref, _ = oracle.conv1d_norm_samples(oracle.params_of(wl), ns, inp["x"], inp["w"], inp["b"])
     compare(wl, y[ns], None, ref, None, path, wl.name)
-    compare(wl, y1[ns], None, ref, None, path, wl.name + " (single-CTA mainloop)")
+    compare(wl, y1[ns], None, ref, None, path, wl.name + " (CTA-pair mainloop)")
     assert np.all(np.isfinite(y)) and np.all(np.isfinite(y1))
 
 
@@ -263,11 +312,12 @@ def test_conv_ln_gelu_bf16_full_sampled(cuda_lib):
     wl = synth.CONV_LN_GELU_BF16
     inp = _inputs(wl)
     y, _, path = run_gpu(cuda_lib, wl, inp)
-    y2, _, path2 = run_gpu(cuda_lib, wl, inp, force_path=cuda_lib.PATH_TC_FUSED_LN)
-    assert path2 == "tc_fused_ln"
+    assert path == "tc_fused_ln"
+    y2, _, path2 = run_gpu(cuda_lib, wl, inp, force_path=cuda_lib.PATH_TC_TWO_PASS)
+    assert path2 == "tc_two_pass"
     ns = [0, wl.N - 1]
     ref, _ = oracle.conv1d_norm_samples(oracle.params_of(wl), ns, inp["x"], inp["w"], inp["b"], inp["gamma"],
                                         inp["beta"])
     compare(wl, y[ns], None, ref, None, path, wl.name)
-    compare(wl, y2[ns], None, ref, None, path2, wl.name + " (fused LayerNorm)")
+    compare(wl, y2[ns], None, ref, None, path2, wl.name + " (two-pass)")
     assert np.all(np.isfinite(y)) and np.all(np.isfinite(y2))
