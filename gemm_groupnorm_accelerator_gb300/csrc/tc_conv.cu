@@ -97,6 +97,21 @@ __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity, int* stat
     }
 }
 
+// N consecutive floats from 16-byte aligned shared memory as N/4 vector loads (the epilogues read
+// per-channel parameters for a whole chunk of columns at once, not one broadcast load per element).
+template <int N>
+__device__ __forceinline__ void lds_vec(const float* p, float (&out)[N]) {
+    static_assert(N % 4 == 0, "whole float4s");
+#pragma unroll
+    for (int k = 0; k < N / 4; ++k) {
+        const float4 t = reinterpret_cast<const float4*>(p)[k];
+        out[4 * k] = t.x;
+        out[4 * k + 1] = t.y;
+        out[4 * k + 2] = t.z;
+        out[4 * k + 3] = t.w;
+    }
+}
+
 __device__ __forceinline__ void chan_merge(float& n_a, float& mu_a, float& m2_a, float n_b, float mu_b, float m2_b) {
     if (n_b <= 0.f) return;
     const float n = n_a + n_b;
@@ -188,7 +203,10 @@ __device__ __forceinline__ void gn_run_sums_any(int sub, uint32_t tb, int ncols,
 // GroupNorm of the runs of CPG consecutive channels held by one thread (CPG divides 32): two passes
 // over the registers, population variance, then affine with the per-channel gamma / beta.
 template <int CPG>
-__device__ __forceinline__ void row_group_norm(float (&v)[32], const float* gamma, const float* beta, float eps) {
+__device__ __forceinline__ void row_group_norm(float (&v)[32], const float* gamma_s, const float* beta_s, float eps) {
+    float gamma[32], beta[32];
+    lds_vec(gamma_s, gamma);
+    lds_vec(beta_s, beta);
 #pragma unroll
     for (int g = 0; g < 32 / CPG; ++g) {
         float s = 0.f;
@@ -675,8 +693,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j0 = 0; j0 < ncols; j0 += 16) {
                         float v[16];
                         tmem_load16(tb + uint32_t(j0), v);
+                        {
+                            float bb[16];
+                            lds_vec(s_bias + j0, bb);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] += s_bias[j0 + i];
+                            for (int i = 0; i < 16; ++i) v[i] += bb[i];
+                        }
                         if (a.gelu) {
 #pragma unroll
                             for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
@@ -722,8 +744,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j0 = 0; j0 < ncols; j0 += 32) {
                     float v[32];
                     tmem_load32(tb + uint32_t(j0), v);
+                    {
+                        float bb[32];
+                        lds_vec(s_bias + j0, bb);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] += s_bias[j0 + i];
+                        for (int i = 0; i < 32; ++i) v[i] += bb[i];
+                    }
                     if (a.row_cpg == 8) row_group_norm<8>(v, s_gamma + j0, s_beta + j0, a.eps);
                     else if (a.row_cpg == 16) row_group_norm<16>(v, s_gamma + j0, s_beta + j0, a.eps);
                     else if (a.row_cpg == 32) row_group_norm<32>(v, s_gamma + j0, s_beta + j0, a.eps);
@@ -777,11 +803,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j0 = 0; j0 < ncols; j0 += 32) {
                     float v[32];
                     tmem_load32(tb + uint32_t(j0), v);
-                    if (j0 == 0) shift = v[0] + s_bias[0];
+                    float bb[32];
+                    lds_vec(s_bias + j0, bb);
+                    if (j0 == 0) shift = v[0] + bb[0];
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         if (j0 + i < ncols) {
-                            const float d = v[i] + s_bias[j0 + i] - shift;
+                            const float d = v[i] + bb[i] - shift;
                             s1 += d;
                             s2 = fmaf(d, d, s2);
                         }
@@ -812,8 +840,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float v[32];
                         tmem_load32(tb + uint32_t(j0), v);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = fmaf((v[i] + (s_bias[j0 + i] - mean)) * rstd, s_gamma[j0 + i], s_beta[j0 + i]);
+                        for (int h = 0; h < 32; h += 16) {
+                            float bb[16], gg[16], be[16];
+                            lds_vec(s_bias + j0 + h, bb);
+                            lds_vec(s_gamma + j0 + h, gg);
+                            lds_vec(s_beta + j0 + h, be);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                v[h + i] = fmaf((v[h + i] + (bb[i] - mean)) * rstd, gg[i], be[i]);
+                        }
                         if (a.gelu) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
@@ -836,8 +871,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float v[32];
                         tmem_load32(tb + uint32_t(j0), v);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = fmaf((v[i] + (s_bias[j0 + i] - mean)) * rstd, s_gamma[j0 + i], s_beta[j0 + i]);
+                        for (int h = 0; h < 32; h += 16) {
+                            float bb[16], gg[16], be[16];
+                            lds_vec(s_bias + j0 + h, bb);
+                            lds_vec(s_gamma + j0 + h, gg);
+                            lds_vec(s_beta + j0 + h, be);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                v[h + i] = fmaf((v[h + i] + (bb[i] - mean)) * rstd, gg[i], be[i]);
+                        }
                         if (a.gelu) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
@@ -979,7 +1021,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float v[32];
                         tmem_load32(tb + uint32_t(j0), v);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = fmaf(v[i], colscale[j0 + i], colshift[j0 + i]);
+                        for (int h = 0; h < 32; h += 16) {
+                            float sc[16], sh[16];
+                            lds_vec(colscale + j0 + h, sc);
+                            lds_vec(colshift + j0 + h, sh);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[h + i] = fmaf(v[h + i], sc[i], sh[i]);
+                        }
                         if (a.gelu) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
@@ -998,8 +1046,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j0 = 0; j0 < ncols; j0 += 16) {
                         float v[16];
                         tmem_load16(tb + uint32_t(j0), v);
+                        {
+                            float sc[16], sh[16];
+                            lds_vec(colscale + j0, sc);
+                            lds_vec(colshift + j0, sh);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = fmaf(v[i], colscale[j0 + i], colshift[j0 + i]);
+                            for (int i = 0; i < 16; ++i) v[i] = fmaf(v[i], sc[i], sh[i]);
+                        }
                         if (a.gelu) {
 #pragma unroll
                             for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
