@@ -106,7 +106,8 @@ def workload_by_name(name):
     if name in synth.BY_NAME:
         return synth.BY_NAME[name]
     short = {"conv_gn": synth.CONV_GN, "conv_gn_tiny": synth.CONV_GN_TINY, "causal_conv": synth.CAUSAL_CONV,
-             "linear_gn_rowmin": synth.LINEAR_GN_ROWMIN, "conv_ln_gelu_bf16": synth.CONV_LN_GELU_BF16}
+             "linear_gn_rowmin": synth.LINEAR_GN_ROWMIN, "conv_ln_gelu_bf16": synth.CONV_LN_GELU_BF16,
+             "causal_conv_gn32": synth.CAUSAL_CONV_GN32}
     return short[name]
 
 

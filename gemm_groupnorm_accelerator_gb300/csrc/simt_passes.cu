@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "c1n_internal.h"
+#include "c1n_math.cuh"
 #include "sm100_ptx.cuh"
 
 namespace c1n {
@@ -22,7 +23,7 @@ __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162flo
 __device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
-__device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
+
 
 // ------------------------------------------------------------------------------ SIMT conv
 
@@ -115,42 +116,101 @@ __device__ float block_sum(float v, float* red) {
 }
 
 // GroupNorm statistics: the channels of group g are contiguous rows, so the group is one
-// contiguous span of cpg * T_out values. Two passes: mean, then the mean squared deviation.
-__global__ void __launch_bounds__(256) gn_stats_kernel(const float* __restrict__ raw, float2* __restrict__ stats,
+// contiguous span of cpg * T_out values, read once: sums of (v - shift) and of its square with the
+// group's first value as the shift, then mean = shift + S1/n and variance = (S2 - S1^2/n) / n.
+__global__ void __launch_bounds__(512) gn_stats_kernel(const float* __restrict__ raw, float2* __restrict__ stats,
                                                        int C, long long T_out, int G, float eps) {
     __shared__ float red[32];
     const int g = blockIdx.x, n = blockIdx.y;
     const long long cpg = C / G;
     const long long cnt = cpg * T_out;
     const float* src = raw + ((long long)n * C + g * cpg) * T_out;
-    float s = 0.f;
-    for (long long i = threadIdx.x; i < cnt; i += blockDim.x) s += src[i];
-    const float mean = block_sum(s, red) / (float)cnt;
-    float ss = 0.f;
-    for (long long i = threadIdx.x; i < cnt; i += blockDim.x) {
-        const float d = src[i] - mean;
-        ss = fmaf(d, d, ss);
+    const float shift = __ldg(src);
+    float s1 = 0.f, s2 = 0.f;
+    if ((cnt & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        const float4* s4 = reinterpret_cast<const float4*>(src);
+        const long long n4 = cnt / 4;
+#pragma unroll 4
+        for (long long i = threadIdx.x; i < n4; i += blockDim.x) {
+            const float4 v = __ldg(s4 + i);
+            const float d0 = v.x - shift, d1 = v.y - shift, d2 = v.z - shift, d3 = v.w - shift;
+            s1 += (d0 + d1) + (d2 + d3);
+            s2 = fmaf(d0, d0, fmaf(d1, d1, fmaf(d2, d2, fmaf(d3, d3, s2))));
+        }
+    } else {
+        for (long long i = threadIdx.x; i < cnt; i += blockDim.x) {
+            const float d = src[i] - shift;
+            s1 += d;
+            s2 = fmaf(d, d, s2);
+        }
     }
-    const float var = block_sum(ss, red) / (float)cnt;
-    if (threadIdx.x == 0) stats[(long long)n * G + g] = make_float2(mean, rsqrtf(var + eps));
+    s1 = block_sum(s1, red);
+    s2 = block_sum(s2, red);
+    const float inv = 1.f / (float)cnt;
+    const float m1 = s1 * inv;
+    const float var = fmaxf(s2 * inv - m1 * m1, 0.f);
+    if (threadIdx.x == 0) stats[(long long)n * G + g] = make_float2(shift + m1, rsqrtf(var + eps));
 }
 
-// Channel-LayerNorm statistics per (n, t): one thread per t (coalesced over t), two passes over C.
+// Channel-LayerNorm statistics per (n, t), read once. A CTA covers 32 * VEC consecutive t of one
+// sample; lane l of every warp owns t0 + VEC*l .. + VEC-1 (coalesced over t) and warp w the
+// channels c = w, w + 8, ...; sums of (v - shift) and of its square with the channel-0 value as the
+// shift, combined over the 8 warps in shared memory.
+template <int VEC>
 __global__ void __launch_bounds__(256) ln_stats_kernel(const float* __restrict__ raw, float2* __restrict__ stats,
                                                        int C, long long T_out, float eps) {
-    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    __shared__ float part[2][8][32 * VEC];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int n = blockIdx.y;
-    if (t >= T_out) return;
-    const float* src = raw + (long long)n * C * T_out + t;
-    float s = 0.f;
-    for (int c = 0; c < C; ++c) s += src[(long long)c * T_out];
-    const float mean = s / (float)C;
-    float ss = 0.f;
-    for (int c = 0; c < C; ++c) {
-        const float d = src[(long long)c * T_out] - mean;
-        ss = fmaf(d, d, ss);
+    const long long t0 = (long long)blockIdx.x * (32 * VEC) + (long long)lane * VEC;
+    const bool ok = t0 < T_out;  // with VEC = 4, T_out is a multiple of 4
+    const float* src = raw + (long long)n * C * T_out + (ok ? t0 : 0);
+    float sh[VEC], s1[VEC], s2[VEC];
+    if (VEC == 4) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(src));
+        sh[0] = v.x; sh[1] = v.y; sh[2] = v.z; sh[3] = v.w;
+    } else {
+        sh[0] = __ldg(src);
     }
-    stats[(long long)n * T_out + t] = make_float2(mean, rsqrtf(ss / (float)C + eps));
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) s1[j] = s2[j] = 0.f;
+#pragma unroll 8
+    for (int c = w; c < C; c += 8) {
+        float v[VEC];
+        if (VEC == 4) {
+            const float4 q = __ldg(reinterpret_cast<const float4*>(src + (long long)c * T_out));
+            v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+        } else {
+            v[0] = __ldg(src + (long long)c * T_out);
+        }
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+            const float d = v[j] - sh[j];
+            s1[j] += d;
+            s2[j] = fmaf(d, d, s2[j]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+        part[0][w][lane * VEC + j] = s1[j];
+        part[1][w][lane * VEC + j] = s2[j];
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < 32 * VEC; k += blockDim.x) {
+        const long long t = (long long)blockIdx.x * (32 * VEC) + k;
+        if (t >= T_out) continue;
+        float a1 = 0.f, a2 = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < 8; ++ww) {
+            a1 += part[0][ww][k];
+            a2 += part[1][ww][k];
+        }
+        const float inv = 1.f / (float)C;
+        const float m1 = a1 * inv;
+        const float var = fmaxf(a2 * inv - m1 * m1, 0.f);
+        const float shift = raw[(long long)n * C * T_out + t];
+        stats[(long long)n * T_out + t] = make_float2(shift + m1, rsqrtf(var + eps));
+    }
 }
 
 struct NormArgs {
@@ -210,6 +270,109 @@ __global__ void __launch_bounds__(256) normalize_kernel(NormArgs a, const float*
                 if (a.gelu) z = gelu_erf(z);
                 store_out(dst + t, z);
             }
+        }
+    }
+}
+
+// Normalize + affine + optional GELU, eight consecutive elements of a row per thread (two 16-byte
+// loads; one 16- or two 16-byte stores), for rows whose length is a multiple of 8 and 16-byte
+// aligned buffers. Grid: x over 2048-element segments of a row, y over rows (grid-stride).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+    const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    return a | (b << 16);
+}
+
+template <typename OutT, int NORM, bool GELU>
+__global__ void __launch_bounds__(256) normalize8_kernel(NormArgs a, const float* raw,
+                                                         const float2* __restrict__ stats,
+                                                         const float* __restrict__ gamma,
+                                                         const float* __restrict__ beta, OutT* y) {
+    const long long rows = (long long)a.N * a.C;
+    const long long per_row = a.T_out / 8;
+    for (long long row = blockIdx.y; row < rows; row += gridDim.y) {
+        const int n = (int)(row / a.C), c = (int)(row % a.C);
+        const float ga = gamma ? __ldg(gamma + c) : 1.f, be = beta ? __ldg(beta + c) : 0.f;
+        float2 gs = make_float2(0.f, 1.f);
+        if (NORM == 1) gs = __ldg(stats + (long long)n * a.G + c / a.cpg);
+        const float4* src = reinterpret_cast<const float4*>(raw + row * a.T_out);
+        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < per_row;
+             i += (long long)gridDim.x * blockDim.x) {
+            const float4 v0 = src[2 * i], v1 = src[2 * i + 1];
+            float r[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            if (NORM == 2) {
+                const float4* st4 = reinterpret_cast<const float4*>(stats + (long long)n * a.T_out + 8 * i);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float4 q = __ldg(st4 + k);  // (mean, rstd) of two consecutive t
+                    r[2 * k] = fmaf((r[2 * k] - q.x) * q.y, ga, be);
+                    r[2 * k + 1] = fmaf((r[2 * k + 1] - q.z) * q.w, ga, be);
+                }
+            } else {
+                const float sc = gs.y * ga, of = be - gs.x * gs.y * ga;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) r[j] = fmaf(r[j], sc, of);
+            }
+            if (GELU) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) r[j] = gelu_erf(r[j]);
+            }
+            if constexpr (sizeof(OutT) == 4) {
+                float4* dst = reinterpret_cast<float4*>(y + row * a.T_out);
+                dst[2 * i] = make_float4(r[0], r[1], r[2], r[3]);
+                dst[2 * i + 1] = make_float4(r[4], r[5], r[6], r[7]);
+            } else {
+                uint4* dst = reinterpret_cast<uint4*>(y + row * a.T_out);
+                dst[i] = make_uint4(pack_bf16x2(r[0], r[1]), pack_bf16x2(r[2], r[3]), pack_bf16x2(r[4], r[5]),
+                                    pack_bf16x2(r[6], r[7]));
+            }
+        }
+    }
+}
+
+// Channel-LayerNorm form of the above: statistics are per (n, t), so a thread keeps the (mean,
+// rstd) of its eight consecutive t in registers and walks a block of 64 channels (rows) of one
+// sample. Grid: x over 2048-step segments, y over 64-channel blocks, z over samples.
+template <typename OutT, bool GELU>
+__global__ void __launch_bounds__(256) normalize8_ln_kernel(NormArgs a, const float* raw,
+                                                            const float2* __restrict__ stats,
+                                                            const float* __restrict__ gamma,
+                                                            const float* __restrict__ beta, OutT* y) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // 8-step chunk index
+    if (i >= a.T_out / 8) return;
+    const int n = blockIdx.z;
+    float mu[8], rs[8];
+    const float4* st4 = reinterpret_cast<const float4*>(stats + (long long)n * a.T_out + 8 * i);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float4 q = __ldg(st4 + k);
+        mu[2 * k] = q.x;
+        rs[2 * k] = q.y;
+        mu[2 * k + 1] = q.z;
+        rs[2 * k + 1] = q.w;
+    }
+    const int c_end = min(a.C, (int)(blockIdx.y + 1) * 64);
+#pragma unroll 2
+    for (int c = blockIdx.y * 64; c < c_end; ++c) {
+        const long long row = (long long)n * a.C + c;
+        const float ga = gamma ? __ldg(gamma + c) : 1.f, be = beta ? __ldg(beta + c) : 0.f;
+        const float4* src = reinterpret_cast<const float4*>(raw + row * a.T_out);
+        const float4 v0 = src[2 * i], v1 = src[2 * i + 1];
+        float r[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) r[j] = fmaf((r[j] - mu[j]) * rs[j], ga, be);
+        if (GELU) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) r[j] = gelu_erf(r[j]);
+        }
+        if constexpr (sizeof(OutT) == 4) {
+            float4* dst = reinterpret_cast<float4*>(y + row * a.T_out);
+            dst[2 * i] = make_float4(r[0], r[1], r[2], r[3]);
+            dst[2 * i + 1] = make_float4(r[4], r[5], r[6], r[7]);
+        } else {
+            uint4* dst = reinterpret_cast<uint4*>(y + row * a.T_out);
+            dst[i] = make_uint4(pack_bf16x2(r[0], r[1]), pack_bf16x2(r[2], r[3]), pack_bf16x2(r[4], r[5]),
+                                pack_bf16x2(r[6], r[7]));
         }
     }
 }
@@ -408,20 +571,65 @@ cudaError_t launch_simt_conv(const c1n_params& p, const Plan& pl, const void* x,
 cudaError_t launch_gn_stats(const c1n_params& p, const Plan& pl, const float* raw, float2* stats,
                             cudaStream_t stream) {
     dim3 grid((unsigned)p.groups, (unsigned)p.N);
-    gn_stats_kernel<<<grid, 256, 0, stream>>>(raw, stats, p.C_out, pl.T_out, p.groups, p.eps);
+    gn_stats_kernel<<<grid, 512, 0, stream>>>(raw, stats, p.C_out, pl.T_out, p.groups, p.eps);
     return cudaGetLastError();
 }
 
 cudaError_t launch_ln_stats(const c1n_params& p, const Plan& pl, const float* raw, float2* stats,
                             cudaStream_t stream) {
-    dim3 grid((unsigned)((pl.T_out + 255) / 256), (unsigned)p.N);
-    ln_stats_kernel<<<grid, 256, 0, stream>>>(raw, stats, p.C_out, pl.T_out, p.eps);
+    if (pl.T_out % 4 == 0) {
+        dim3 grid((unsigned)((pl.T_out + 127) / 128), (unsigned)p.N);
+        ln_stats_kernel<4><<<grid, 256, 0, stream>>>(raw, stats, p.C_out, pl.T_out, p.eps);
+    } else {
+        dim3 grid((unsigned)((pl.T_out + 31) / 32), (unsigned)p.N);
+        ln_stats_kernel<1><<<grid, 256, 0, stream>>>(raw, stats, p.C_out, pl.T_out, p.eps);
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_normalize(const c1n_params& p, const Plan& pl, const float* raw, const float2* stats,
                              const float* gamma, const float* beta, void* y, cudaStream_t stream) {
     NormArgs a = norm_args(p, pl);
+    const long long rows8 = (long long)p.N * p.C_out;
+    if (pl.T_out % 8 == 0 && (reinterpret_cast<uintptr_t>(raw) & 15) == 0 &&
+        (reinterpret_cast<uintptr_t>(y) & 15) == 0) {
+        const long long per_row = pl.T_out / 8;
+        int gx = (int)((per_row + 255) / 256);
+        if (gx > 64) gx = 64;
+        long long gy = (152LL * 16 + gx - 1) / gx;
+        if (gy > rows8) gy = rows8;
+        if (gy > 65535) gy = 65535;
+        dim3 grid((unsigned)gx, (unsigned)gy);
+#define C1N_NORM8(T, NORM)                                                                                  \
+    (a.gelu ? (normalize8_kernel<T, NORM, true><<<grid, 256, 0, stream>>>(a, raw, stats, gamma, beta, out), 0) \
+            : (normalize8_kernel<T, NORM, false><<<grid, 256, 0, stream>>>(a, raw, stats, gamma, beta, out), 0))
+        if (a.norm == 2 && p.N <= 65535) {
+            dim3 g3((unsigned)((per_row + 255) / 256), (unsigned)((p.C_out + 63) / 64), (unsigned)p.N);
+            if (pl.bf16) {
+                auto out = static_cast<__nv_bfloat16*>(y);
+                if (a.gelu) normalize8_ln_kernel<__nv_bfloat16, true><<<g3, 256, 0, stream>>>(a, raw, stats, gamma, beta, out);
+                else normalize8_ln_kernel<__nv_bfloat16, false><<<g3, 256, 0, stream>>>(a, raw, stats, gamma, beta, out);
+            } else {
+                auto out = static_cast<float*>(y);
+                if (a.gelu) normalize8_ln_kernel<float, true><<<g3, 256, 0, stream>>>(a, raw, stats, gamma, beta, out);
+                else normalize8_ln_kernel<float, false><<<g3, 256, 0, stream>>>(a, raw, stats, gamma, beta, out);
+            }
+            return cudaGetLastError();
+        }
+        if (pl.bf16) {
+            auto out = static_cast<__nv_bfloat16*>(y);
+            if (a.norm == 2) C1N_NORM8(__nv_bfloat16, 2);
+            else if (a.norm == 1) C1N_NORM8(__nv_bfloat16, 1);
+            else C1N_NORM8(__nv_bfloat16, 0);
+        } else {
+            auto out = static_cast<float*>(y);
+            if (a.norm == 2) C1N_NORM8(float, 2);
+            else if (a.norm == 1) C1N_NORM8(float, 1);
+            else C1N_NORM8(float, 0);
+        }
+#undef C1N_NORM8
+        return cudaGetLastError();
+    }
     const bool vec = (pl.T_out % 4) == 0;
     const long long per_row = vec ? pl.T_out / 4 : pl.T_out;
     const long long rows = (long long)p.N * p.C_out;

@@ -37,6 +37,7 @@
 #include <type_traits>
 
 #include "c1n_internal.h"
+#include "c1n_math.cuh"
 #include "sm100_ptx.cuh"
 
 namespace c1n {
@@ -53,32 +54,6 @@ enum WaitSite {
     kWaitSFull, kWaitGridPeers, kWaitExchange
 };
 
-// Exact (erf) GELU, 0.5 z (1 + erf(z / sqrt 2)), with erf from the rational-exponential
-// approximation 7.1.26 of Abramowitz & Stegun's Handbook of Mathematical Functions (Hastings):
-// erf(x) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-x^2), t = 1 / (1 + p x), x >= 0, with
-// |error| <= 1.5e-7; odd symmetry for x < 0. The reciprocal and exp2 use the hardware
-// approximations (a few ulp), which keeps the GELU error below 1e-6 * |z| -- far inside the fp32
-// and bf16 output tolerances -- at about a dozen instructions.
-__device__ __forceinline__ float rcp_approx(float x) {
-    float r;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-    return r;
-}
-__device__ __forceinline__ float exp2_approx(float x) {
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-    return r;
-}
-__device__ __forceinline__ float gelu_erf(float z) {
-    const float x = fabsf(z) * 0.70710678118654752f;
-    const float t = rcp_approx(fmaf(0.3275911f, x, 1.0f));
-    const float poly =
-        t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
-    const float e = exp2_approx(-x * x * 1.4426950408889634f);
-    const float erf_abs = fmaf(-poly, e, 1.0f);
-    const float erf_v = copysignf(erf_abs, z);
-    return 0.5f * z * (1.0f + erf_v);
-}
 
 __device__ __forceinline__ float load_in(const float* p) { return __ldg(p); }
 __device__ __forceinline__ float load_in(const __nv_bfloat16* p) { return __bfloat162float(*p); }
@@ -806,13 +781,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float bb[32];
                     lds_vec(s_bias + j0, bb);
                     if (j0 == 0) shift = v[0] + bb[0];
+                    if (j0 + 32 <= ncols) {  // whole chunk (uniform): no per-column test
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (j0 + i < ncols) {
+                        for (int i = 0; i < 32; ++i) {
                             const float d = v[i] + bb[i] - shift;
                             s1 += d;
                             s2 = fmaf(d, d, s2);
                         }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (j0 + i < ncols) {
+                                const float d = v[i] + bb[i] - shift;
+                                s1 += d;
+                                s2 = fmaf(d, d, s2);
+                            }
+                    }
                 }
                 const float n_own = float(ncols);
                 float mean = shift + s1 / n_own;

@@ -184,7 +184,15 @@ CONV_LN_GELU_BF16 = Workload(
     description="Conv1d+channel-LayerNorm+exact GELU bf16 (fp32 accumulate), N=64, C 256->512, T=4096, k=5, dil 2, pad 4/4")
 
 WORKLOADS = [CONV_GN_TINY, CONV_GN, CAUSAL_CONV, LINEAR_GN_ROWMIN, CONV_LN_GELU_BF16]
-BY_NAME: Dict[str, Workload] = {w.name: w for w in WORKLOADS}
+
+# The largest fp32 output of the five with GroupNorm switched on (G = 32, 8 channels per group):
+# the shape on which the memory-bound statistics / normalize passes of the two-pass plan are
+# measured (268 MB of raw fp32 output read back and rewritten).
+CAUSAL_CONV_GN32 = CAUSAL_CONV.replace(
+    name="causal_conv1d_groupnorm32_f32_n32_c256x256_t8192_k4", norm=NORM_GROUP, groups=32,
+    description="causal Conv1d fp32 + GroupNorm(32), N=32, C 256->256, T=8192, k=4, left pad 3")
+
+BY_NAME: Dict[str, Workload] = {w.name: w for w in WORKLOADS + [CAUSAL_CONV_GN32]}
 
 
 def make_inputs(wl: Workload, seed: int = 0, n_rows: Optional[int] = None, row_offset: int = 0) -> Dict[str, np.ndarray]:
