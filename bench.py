@@ -230,16 +230,10 @@ def our_arm(args, wl):
     am = torch.empty((wl.N, op.T_out), dtype=torch.int32, device=dev) if wl.post == synth.POST_ROWMIN_BIAS else None
     stream = torch.cuda.current_stream(dev)
 
-    def step(i, ev=None):
+    def step(i):
         j = i % n_sets
-        if ev is not None:
-            ev[0].record(stream)
         op.pack_weights(w)
-        if ev is not None:
-            ev[1].record(stream)
         op(xs[j], w, b, ga, be, bias2=b2, out=ys[j], argmin=am, weights_packed=True)
-        if ev is not None:
-            ev[2].record(stream)
 
     def barrier():
         if pg is not None:
@@ -250,7 +244,21 @@ def our_arm(args, wl):
     torch.cuda.synchronize()
     op.check()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # One CUDA graph per input buffer set holds one step (pack + operator) as the device runs it, so
+    # the timed region measures the GPU rather than the host's per-launch overhead (at ~20 us per
+    # step on the small workloads the eager Python loop cannot keep the GPU busy).
+    graphs = capture_graphs(step, n_sets, dev) if not args.eager else None
+    launch_mode = "cuda graph replay, one graph per step" if graphs else "eager"
+
+    def run_step(i):
+        if graphs:
+            graphs[i % n_sets].replay()
+        else:
+            step(i)
+
+    for i in range(max(3, args.warmup)):
+        run_step(i)
+    torch.cuda.synchronize()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
@@ -259,7 +267,7 @@ def our_arm(args, wl):
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
-        step(args.warmup + i, evs[i])
+        run_step(args.warmup + i)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -267,8 +275,10 @@ def our_arm(args, wl):
     op.check()
     total_ms = t_start.elapsed_time(t_end)
     ms = total_ms / args.steps
-    main_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    pack_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    # device time of the weight pack alone and of the operator alone, the same way
+    pack_ms = time_replays(lambda i: op.pack_weights(w), n_sets, dev, args.steps, eager=not graphs)
+    main_ms = time_replays(lambda i: op(xs[i % n_sets], w, b, ga, be, bias2=b2, out=ys[i % n_sets], argmin=am,
+                                        weights_packed=True), n_sets, dev, args.steps, eager=not graphs)
     if pg is not None:
         t = torch.tensor([ms, main_ms], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -276,8 +286,8 @@ def our_arm(args, wl):
     value, ms = aggregate([ms], wl.flops, world)
 
     # per-kernel device times from the library's event marks (a few extra steps after the timed
-    # region, same inputs and launch configuration)
-    kern = kernel_times(op, step, args.warmup + args.steps, n=5)
+    # region, same inputs and launch configuration, replayed from a graph when the step is)
+    kern = kernel_times(op, step, args.warmup + args.steps, dev, n=5, graphs=bool(graphs))
     conv_name = "simt_conv" if path == "simt" else "tc_conv"
     conv_ms = kern.get(conv_name, main_ms)
 
@@ -324,7 +334,8 @@ def our_arm(args, wl):
                                          "l2": f"inputs rotate over {n_sets} x/y buffer sets "
                                                f"({n_sets * per_set / 2**20:.0f} MiB > 129 MiB L2)"
                                          if n_sets > 1 else "working set larger than L2",
-                                         "step": "weight pack + fused kernel through the C ABI"}),
+                                         "step": "weight pack + fused kernel through the C ABI",
+                                         "launch": launch_mode}),
                 "roofline": roof, "normalize_pass": norm_pass, "cpu_baseline": cpu,
                 "e2e": {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
                 "gpu_launches": args.steps * op.info.kernels, "clocks": clocks}
@@ -333,15 +344,72 @@ def our_arm(args, wl):
         pg.destroy_process_group()
 
 
-def kernel_times(op, step, i0, n=5):
-    """Mean device time per kernel name over n profiled steps (the library's event marks)."""
+def capture_graphs(fn, n, dev):
+    """One CUDA graph per call fn(j), j < n, captured on a side stream; None if capture fails (the
+    bench then times the eager loop and says so)."""
+    import torch
+    try:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for j in range(n):
+                fn(j)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize()
+        graphs = []
+        for j in range(n):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn(j)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        return graphs
+    except Exception as e:  # pragma: no cover - depends on the driver
+        print(f"bench: CUDA graph capture failed ({e}); timing the eager loop", file=sys.stderr)
+        torch.cuda.synchronize()
+        return None
+
+
+def time_replays(fn, n_sets, dev, steps, eager=False):
+    """Mean device ms of fn(i) over `steps` calls, replayed from per-set graphs unless eager."""
+    import torch
+    graphs = None if eager else capture_graphs(fn, n_sets, dev)
+    run = (lambda i: graphs[i % n_sets].replay()) if graphs else fn
+    for i in range(3):
+        run(i)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(steps):
+        run(i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def kernel_times(op, step, i0, dev, n=5, graphs=True):
+    """Mean device time per kernel name over n profiled steps (the library's event marks, recorded
+    inside a replayed graph when graphs=True, so host launch gaps do not count)."""
     import torch
     acc = {}
     op.set_profiling(True)
     try:
+        step(i0)  # an eager profiled run creates the library's events before any capture
+        torch.cuda.synchronize()
+        g = capture_graphs(lambda j: step(i0), 1, dev) if graphs else None
         for i in range(n):
-            step(i0 + i)
-            for name, ms in op.kernel_times():
+            if g:
+                g[0].replay()
+            else:
+                step(i0 + i)
+            try:
+                times = op.kernel_times()
+            except Exception as e:  # pragma: no cover - event timing inside graphs unsupported
+                print(f"bench: kernel times from the graph failed ({e}); using eager steps", file=sys.stderr)
+                g = None
+                step(i0 + i)
+                times = op.kernel_times()
+            for name, ms in times:
                 acc.setdefault(name, []).append(ms)
     finally:
         op.set_profiling(False)
@@ -441,6 +509,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--oracle-rows", type=int, default=2, help="batch entries per reference-arm step")
     ap.add_argument("--metric", default="fused conv1d+GroupNorm TFLOP/s")
+    ap.add_argument("--eager", action="store_true", help="time the eager launch loop instead of CUDA graph replays")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     wl = workload_by_name(args.workload)

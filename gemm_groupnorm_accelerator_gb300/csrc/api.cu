@@ -428,9 +428,18 @@ c1n_status ensure_device(c1n_desc* d) {
 }
 
 // Records a timing event before the launch of kernel `name` (nullptr: after the last one).
+// Under stream capture the record becomes an event-record node of the graph (external), so a
+// replay of the graph times its kernels too.
 void mark(c1n_desc* d, cudaStream_t s, const char* name) {
     if (!d->profiling || !d->events_ready || d->n_marks >= c1n_desc::kMaxMarks) return;
-    if (cudaEventRecord(d->ev[d->n_marks], s) == cudaSuccess) d->ev_name[d->n_marks++] = name;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        e = cudaEventRecordWithFlags(d->ev[d->n_marks], s, cudaEventRecordExternal);
+    else if (e == cudaSuccess)
+        e = cudaEventRecord(d->ev[d->n_marks], s);
+    if (e == cudaSuccess) d->ev_name[d->n_marks++] = name;
+    else cudaGetLastError();  // timing is best effort: leave no error behind for the launches
 }
 
 c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s);
@@ -535,15 +544,17 @@ c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         // 32 x 32 tiles staged per warp; their 32-channel boxes must not reach into the other
         // CTA's channel half (BN a multiple of 32 when the channels are split).
         const bool y_tma_ok = aligned16(a->y) && (pl.T_out * pl.esize) % 16 == 0;
+        const bool box_ok = pl.n_cb == 1 || pl.BN % 32 == 0;  // 32-channel boxes stay in this CTA's block
         const bool tma_store =
-            y_tma_ok && ((fused_gn && (size_t)pl.BN * 128 * pl.esize <=
-                                          (size_t)pl.stages_b * pl.b_slot_bytes + (size_t)pl.stages_s * pl.s_slot_bytes) ||
-                         (fused_ln_path && pl.o_bytes > 0 && (pl.n_cb == 1 || pl.BN % 32 == 0)));
+            y_tma_ok && box_ok &&
+            ((fused_gn && (size_t)round_up(pl.BN, 32) * 128 * pl.esize <=
+                              (size_t)pl.stages_b * pl.b_slot_bytes + (size_t)pl.stages_s * pl.s_slot_bytes) ||
+             (fused_ln_path && pl.o_bytes > 0));
         if (tma_store && d->tm_y_ptr != a->y) {
             const cuuint64_t es = (cuuint64_t)pl.esize;
             cuuint64_t dy[3] = {(cuuint64_t)pl.T_out, (cuuint64_t)p.C_out, (cuuint64_t)p.N};
             cuuint64_t sy[2] = {(cuuint64_t)pl.T_out * es, (cuuint64_t)pl.T_out * p.C_out * es};
-            cuuint32_t by[3] = {fused_ln_path ? 32u : 128u, fused_ln_path ? 32u : (cuuint32_t)pl.BN, 1};
+            cuuint32_t by[3] = {32u, 32u, 1};  // one warp's 32 steps x 32 channels
             st = encode(&d->tm_y, a->y, pl.bf16, 3, dy, sy, by, CU_TENSOR_MAP_SWIZZLE_NONE);
             if (st != C1N_OK) return st;
             d->tm_y_ptr = a->y;
@@ -764,12 +775,18 @@ c1n_status conv1d_norm_kernel_times(c1n_desc* desc, c1n_kernel_time* out, int32_
     const int n = desc->n_marks;
     if (n < 2) return C1N_OK;
     cudaError_t e = cudaEventSynchronize(desc->ev[n - 1]);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize (profiling)");
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // not sticky: keep it from surfacing at the next launch
+        return cuda_fail(e, "cudaEventSynchronize (profiling)");
+    }
     int k = 0;
     for (int i = 0; i + 1 < n && k < capacity; ++i, ++k) {
         float ms = 0.f;
         e = cudaEventElapsedTime(&ms, desc->ev[i], desc->ev[i + 1]);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime (profiling)");
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return cuda_fail(e, "cudaEventElapsedTime (profiling)");
+        }
         std::memset(out[k].name, 0, sizeof(out[k].name));
         std::snprintf(out[k].name, sizeof(out[k].name), "%s", desc->ev_name[i]);
         out[k].ms = ms;

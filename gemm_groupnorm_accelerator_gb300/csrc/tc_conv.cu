@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "c1n_internal.h"
@@ -949,9 +950,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float4* gp = a.gpart + (slot0 + tt) * 256;
                     for (int g = er; g < ngroups; g += kEpiThreads)
                         gp[g] = make_float4(part[g], part[256 + g], part[512 + g], 0.f);
-                    __threadfence();
                     named_bar_sync(1, kEpiThreads);
                     if (er == 0) {
+                        // the CTA's partials (ordered before this thread by the barrier) become
+                        // visible device-wide before the arrival is counted
+                        __threadfence();
                         unsigned* cnt = a.gsync + (un.n * a.n_cb + un.cbu);
                         const unsigned n_peers = unsigned(a.n_t_tiles);
                         const unsigned old = atomicAdd(cnt, 1u);
@@ -967,7 +970,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 *abort_flag = 1;
                                 break;
                             }
-                            __nanosleep(64);
+                            __nanosleep(32);
                         }
                     }
                     named_bar_sync(1, kEpiThreads);
@@ -997,10 +1000,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar_sync(1, kEpiThreads);
                 // normalize from TMEM; store once
                 if (a.tma_store) {
-                    // Stage the tile as [channel][time] (a warp writes 32 consecutive words per
-                    // channel) in the operand rings, idle now that the tile's MMAs are done, then
-                    // one TMA bulk store; rows past T_out and channels past C_out are clipped.
-                    OutT* so = reinterpret_cast<OutT*>(base + size_t(SA) * a.a_slot_bytes);
+                    // Each warp stages its 32 time steps of every 32-channel chunk as a [32 ch][32 t]
+                    // tile in the operand rings (idle now that the tile's MMAs are done) and sends
+                    // it with a TMA bulk store at once, so the stores overlap the staging of the
+                    // next chunks; rows past T_out and channels past C_out are clipped.
+                    const int nch = (a.BN + 31) / 32;
+                    OutT* so = reinterpret_cast<OutT*>(base + size_t(SA) * a.a_slot_bytes) + q * (nch * 32 * 32);
                     for (int j0 = 0; j0 < ncols; j0 += 32) {
                         float v[32];
                         tmem_load32(tb + uint32_t(j0), v);
@@ -1016,16 +1021,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
                         }
+                        OutT* ob = so + (j0 / 32) * (32 * 32);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (j0 + i < a.BN) store_out(so + (j0 + i) * 128 + m, v[i]);
+                        for (int i = 0; i < 32; ++i) store_out(ob + i * 32 + lane, v[i]);
+                        fence_async_shared();
+                        __syncwarp();
+                        if (lane == 0) tma_store_3d(&tm_y, smem_u32(ob), un.row0 + q * 32, co_base + j0, un.n);
                     }
-                    fence_async_shared();
-                    named_bar_sync(1, kEpiThreads);
-                    if (er == 0) {
-                        tma_store_3d(&tm_y, smem_u32(so), un.row0, co_base, un.n);
-                        tma_store_wait_read();
-                    }
+                    if (lane == 0) tma_store_wait_all();  // the staging must outlive the copies
+                    __syncwarp();
                 } else {
                     for (int j0 = 0; j0 < ncols; j0 += 16) {
                         float v[16];
@@ -1083,8 +1087,23 @@ template <bool LINEAR, bool BF16, typename OutT, int EPI, bool PAIR>
 cudaError_t launch_one(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                        const CUtensorMap& tm_y, int num_sms, cudaStream_t stream) {
     auto kern = tc_conv_kernel<LINEAR, BF16, OutT, EPI, PAIR>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
+    // Host work per launch stays small: the shared-memory attribute and the resident-cluster count
+    // are set / queried once per device and shared-memory size (per kernel instantiation).
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> smem_set[kMaxDev];
+    static std::atomic<long long> clusters_cached[kMaxDev];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const bool cacheable = dev >= 0 && dev < kMaxDev;
+    if (!cacheable || smem_set[dev].load(std::memory_order_acquire) < pl.smem_bytes) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
+        if (e != cudaSuccess) return e;
+        if (cacheable) {
+            int cur = smem_set[dev].load();
+            while (cur < pl.smem_bytes && !smem_set[dev].compare_exchange_weak(cur, pl.smem_bytes)) {}
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1111,8 +1130,14 @@ cudaError_t launch_one(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a,
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3(unsigned(num_sms & ~1), 1, 1);
         int max_clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
-        if (e != cudaSuccess) return e;
+        const long long cached = cacheable ? clusters_cached[dev].load(std::memory_order_acquire) : 0;
+        if (cached != 0 && int(cached >> 32) == pl.smem_bytes) {
+            max_clusters = int(cached & 0xffffffff);
+        } else {
+            e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+            if (e != cudaSuccess) return e;
+            if (cacheable) clusters_cached[dev].store((static_cast<long long>(pl.smem_bytes) << 32) | max_clusters);
+        }
         if (max_clusters < 1) return cudaErrorInvalidConfiguration;
         const int pairs = a.n_units < max_clusters ? a.n_units : max_clusters;
         cfg.gridDim = dim3(unsigned(2 * pairs), 1, 1);
