@@ -284,8 +284,8 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
                 pl.cluster = pl.n_t_tiles;
                 pl.grid = pl.n_units;
                 plan_workspace(p, pl, true, false, false);
-                // grid exchange: arrival counters and per-(sample, block, tile, group) partials
-                pl.gsync_count = p.N * pl.n_cb;
+                // grid exchange: per-(sample, block, tile, group) partials and release flags
+                pl.gsync_count = pl.n_units * 256;
                 pl.ws_gsync = pl.ws_total;
                 pl.ws_gpart = round_up(pl.ws_gsync + (size_t)pl.gsync_count * 4, 256);
                 pl.ws_total = round_up(pl.ws_gpart + (size_t)pl.n_units * 256 * sizeof(float4), 256);

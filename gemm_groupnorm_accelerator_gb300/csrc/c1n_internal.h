@@ -74,7 +74,7 @@ struct TcArgs {
     void* y;
     int* status;
     float4* gpart;     // per (sample, channel block, time tile, group): count, mean, M2
-    unsigned* gsync;   // per (sample, channel block): arrival counter
+    unsigned* gsync;   // per (sample, channel block, time tile, group): release flag of the partial
     int row_cpg;       // row epilogue: GroupNorm over runs of row_cpg channels (8, 16, 32; 0 = none)
     int rowmin;        // row epilogue: keep (min, argmin) per row instead of storing y
     float2* rowpart;   // row epilogue: per (row, channel block) minimum and its channel (int bits)

@@ -493,8 +493,10 @@ __global__ void __launch_bounds__(256) pack_weights_kernel(int C_out, int C_in, 
                                                            const InT* __restrict__ w, PackT* __restrict__ wp,
                                                            unsigned* __restrict__ zero, int nzero) {
     extern __shared__ float row[];  // [C_in * k]
-    if (blockIdx.x == 0)
-        for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0u;
+    // the conv kernel that follows may start its setup now (it waits for this kernel before it
+    // reads the packed weights)
+    griddep_launch_dependents();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nzero; i += gridDim.x * blockDim.x) zero[i] = 0u;
     const long long rk = (long long)C_in * k;
     for (int co = blockIdx.x; co < C_out; co += gridDim.x) {
         const InT* src = w + co * rk;

@@ -382,6 +382,15 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
     return v;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may start
+// while the previous kernel of its stream still runs; griddep_wait() returns once that kernel has
+// completed and its memory operations are visible. griddep_launch_dependents() lets the next kernel
+// of the stream start early (it still waits for this one at its own griddep_wait()).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // One lane of the (fully active) warp returns true: the lowest active lane.
 __device__ __forceinline__ bool elect_one() {
     uint32_t r;

@@ -204,6 +204,19 @@ __device__ __forceinline__ void row_group_norm(float (&v)[32], const float* gamm
     }
 }
 
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Orders this thread's later loads after the relaxed loads that observed the peers' release stores.
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -370,6 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above (barriers, TMEM, tensor-map prefetch) may overlap the previous kernel of the
+    // stream; no global memory it may write (x, weights, parameters, workspace) is touched before
+    // this point.
+    griddep_wait();
 
     int first_unit, unit_step;
     if (kFusedGN) {
@@ -886,6 +903,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int co_base = un.cbu * a.BN;
                 const int ncols = min(a.BN, a.C_out - co_base);
                 const int cpg = a.cpg;
+                // the exchange epoch: this CTA's own flag, read now so the load overlaps the passes
+                unsigned gn_epoch = 0;
+                if (EPI == kEpiGridGN)
+                    gn_epoch = *reinterpret_cast<volatile unsigned*>(
+                        a.gsync + (size_t(un.n * a.n_cb + un.cbu) * a.n_t_tiles + un.row0 / 128) * 256);
                 const int ngroups = (ncols + cpg - 1) / cpg;
                 const int nvalid_t = min(128, a.T_out - un.row0);
                 const int tt = un.row0 / 128;
@@ -945,38 +967,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                         colsum[g] = rsqrtf((gn > 0.f ? gm2 / gn : 0.f) + a.eps);  // group rstd
                     }
                 } else {
-                    // publish this CTA's partials, count arrivals, wait (bounded) for the peers
+                    // Publish this CTA's partials, each with a release flag per group; then every
+                    // thread waits (bounded) for its groups' flags from all peers and merges. All
+                    // flags of a (sample, channel block) advance together, one step per launch, so
+                    // this launch's value is one past the CTA's own flag as read before the
+                    // statistics passes (the workspace starts at zero and the weight pack re-zeroes it).
                     const size_t slot0 = size_t(un.n * a.n_cb + un.cbu) * a.n_t_tiles;
                     float4* gp = a.gpart + (slot0 + tt) * 256;
-                    for (int g = er; g < ngroups; g += kEpiThreads)
+                    const unsigned target = gn_epoch + 1u;
+                    for (int g = er; g < ngroups; g += kEpiThreads) {
                         gp[g] = make_float4(part[g], part[256 + g], part[512 + g], 0.f);
-                    named_bar_sync(1, kEpiThreads);
-                    if (er == 0) {
-                        // the CTA's partials (ordered before this thread by the barrier) become
-                        // visible device-wide before the arrival is counted
-                        __threadfence();
-                        unsigned* cnt = a.gsync + (un.n * a.n_cb + un.cbu);
-                        const unsigned n_peers = unsigned(a.n_t_tiles);
-                        const unsigned old = atomicAdd(cnt, 1u);
-                        const unsigned target = (old / n_peers + 1u) * n_peers;
-                        const uint64_t t0 = global_timer_ns();
-                        while (int(ld_acquire_gpu(cnt) - target) < 0) {
-                            if (*abort_flag) break;
-                            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                                if (atomicCAS(a.status, 0, 6) == 0) {
-                                    atomicExch(a.status + 1, kWaitGridPeers);
-                                    atomicExch(a.status + 2, int(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)));
-                                }
-                                *abort_flag = 1;
-                                break;
-                            }
-                            __nanosleep(32);
-                        }
+                        st_release_gpu(a.gsync + (slot0 + tt) * 256 + g, target);
                     }
-                    named_bar_sync(1, kEpiThreads);
                     const float4* gq = a.gpart + slot0 * 256;
                     for (int g = er; g < ngroups; g += kEpiThreads) {
                         float gn = 0.f, gmu = 0.f, gm2 = 0.f;
+                        // all peers' flags of group g, polled together with relaxed loads (up to 16
+                        // tiles per load round), then one acquire fence before their partials are read
+                        const uint64_t t0 = global_timer_ns();
+                        for (int base_rk = 0; base_rk < a.n_t_tiles; base_rk += 16) {
+                            const int nrk = min(16, a.n_t_tiles - base_rk);
+                            for (;;) {
+                                bool all = true;
+#pragma unroll
+                                for (int r = 0; r < 16; ++r)
+                                    if (r < nrk)
+                                        all &= int(ld_relaxed_gpu(a.gsync + (slot0 + base_rk + r) * 256 + g) - target) >= 0;
+                                if (all || *abort_flag) break;
+                                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                                    if (atomicCAS(a.status, 0, 6) == 0) {
+                                        atomicExch(a.status + 1, kWaitGridPeers);
+                                        atomicExch(a.status + 2, int(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)));
+                                    }
+                                    *abort_flag = 1;
+                                    break;
+                                }
+                            }
+                        }
+                        fence_acquire_gpu();
                         for (int rk = 0; rk < a.n_t_tiles; ++rk) {
                             const float4 pv = __ldcg(gq + size_t(rk) * 256 + g);
                             chan_merge(gn, gmu, gm2, pv.x, pv.y, pv.z);
@@ -1105,7 +1133,7 @@ cudaError_t launch_one(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a,
         }
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = size_t(pl.smem_bytes);
     cfg.stream = stream;
@@ -1144,8 +1172,20 @@ cudaError_t launch_one(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a,
     } else {
         const int grid = a.n_units < num_sms ? a.n_units : num_sms;
         cfg.gridDim = dim3(unsigned(grid), 1, 1);
-        cfg.attrs = nullptr;
         cfg.numAttrs = 0;
+    }
+    // Programmatic dependent launch: the CTAs set up while the previous kernel (usually the weight
+    // pack) finishes. If the driver refuses the combination, launch without it from then on.
+    static std::atomic<int> pdl_refused{0};
+    if (!pdl_refused.load(std::memory_order_relaxed)) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs += 1;
+        e = cudaLaunchKernelEx(&cfg, kern, a, tm_a, tm_b, tm_y);
+        if (e == cudaSuccess) return e;
+        cudaGetLastError();
+        pdl_refused.store(1);
+        cfg.numAttrs -= 1;
     }
     return cudaLaunchKernelEx(&cfg, kern, a, tm_a, tm_b, tm_y);
 }
