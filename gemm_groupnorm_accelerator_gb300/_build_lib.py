@@ -43,7 +43,9 @@ def _fingerprint() -> str:
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode())
             h.update(fh.read())
-    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    # flags without the (machine-dependent) include paths: the same sources and flags give the same
+    # fingerprint on every machine, so a profile taken on one box matches a build on another
+    h.update(" ".join(ARCH + [f for f in NVCC_FLAGS if f not in (INCLUDE, CSRC)]).encode())
     return h.hexdigest()
 
 
