@@ -21,14 +21,14 @@ __device__ __forceinline__ float exp2_approx(float x) {
 }
 // Written as GELU(z) = z * Phi(z) with the normal CDF Phi(z) = 1 - Q (z >= 0) or Q (z < 0), where
 // Q = erfc(|z| / sqrt 2) / 2 is the approximation's tail term (its coefficients halved and
-// 1/sqrt(2) folded into p; exp(-z^2/2) as exp2).
+// 1/sqrt(2) folded into p; exp(-z^2/2) as exp2). Both cases are max(z, 0) - |z| * Q.
 __device__ __forceinline__ float gelu_erf(float z) {
-    const float t = rcp_approx(fmaf(0.3275911f * 0.70710678118654752f, fabsf(z), 1.0f));
+    const float az = fabsf(z);
+    const float t = rcp_approx(fmaf(0.3275911f * 0.70710678118654752f, az, 1.0f));
     const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 0.5f * 1.061405429f, 0.5f * -1.453152027f),
                                                 0.5f * 1.421413741f), 0.5f * -0.284496736f), 0.5f * 0.254829592f);
     const float q = poly * exp2_approx(z * z * (-0.5f * 1.4426950408889634f));
-    const float zq = z * q;
-    return z >= 0.f ? z - zq : zq;
+    return fmaf(-az, q, fmaxf(z, 0.f));
 }
 
 }  // namespace c1n

@@ -61,6 +61,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Suspend time hint of the waits' slow path: a waiting thread sleeps in hardware until the phase
+// completes or this many nanoseconds pass, instead of spinning on issue slots the other warps of
+// its SM sub-partition need.
+constexpr uint32_t kSuspendHintNs = 20000;
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
+
 // Per-CTA progress counters kept in shared memory by the pipeline roles; copied into the status
 // word area when a wait gives up, so the host can see where the pipeline stood.
 constexpr int kProgSlots = 12;
@@ -74,8 +91,8 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15u) == 0) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        {
             if (*abort_flag) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
                 if (status != nullptr && atomicCAS(status, 0, 6 /* C1N_ERR_TIMEOUT */) == 0) {
@@ -110,6 +127,18 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_try_wait_cluster_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
+
 // mbar_wait for barriers that also collect arrivals from the peer CTA of a pair (acquire at
 // cluster scope); same limit and error reporting.
 static __device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -117,8 +146,8 @@ static __device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t par
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((it & 15u) == 0) {
+        if (mbar_try_wait_cluster_sleep(bar, parity)) return true;
+        {
             if (*abort_flag) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
                 if (status != nullptr && atomicCAS(status, 0, 6 /* C1N_ERR_TIMEOUT */) == 0) {
@@ -304,6 +333,59 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Two 32-column loads in flight, one wait: the first wait touches both destination arrays (the
+// second through an empty statement), so no use of either is scheduled before it.
+__device__ __forceinline__ void tmem_load32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void reg_touch32(uint32_t (&r)[32], bool wait) {
+    if (wait) {
+        asm volatile("tcgen05.wait::ld.sync.aligned;"
+                     : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                       "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                       "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                       "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                       "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                     :
+                     : "memory");
+    } else {
+        asm volatile(""
+                     : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                       "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                       "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                       "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                       "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                     :
+                     : "memory");
+    }
+}
+
+// Load TMEM columns [j0, j0 + 64) of this warp's lanes (the second half only when it is below
+// ncols) with one wait; ncols is uniform over the warp.
+__device__ __forceinline__ void tmem_load64(uint32_t tb, int j0, int ncols, float (&v)[64]) {
+    uint32_t ra[32], rb[32];
+    const bool two = j0 + 32 < ncols;
+    tmem_load32_issue(tb + uint32_t(j0), ra);
+    if (two) tmem_load32_issue(tb + uint32_t(j0 + 32), rb);
+    reg_touch32(ra, true);
+    if (two) reg_touch32(rb, false);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        v[i] = __uint_as_float(ra[i]);
+        v[32 + i] = two ? __uint_as_float(rb[i]) : 0.f;
+    }
 }
 
 // ------------------------------------------------------------------------------ descriptors
