@@ -337,7 +337,7 @@ def our_arm(args, wl):
                                          "step": "weight pack + fused kernel through the C ABI",
                                          "launch": launch_mode}),
                 "roofline": roof, "normalize_pass": norm_pass, "cpu_baseline": cpu,
-                "e2e": {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
+                "e2e": {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step", "pipeline")},
                 "gpu_launches": args.steps * op.info.kernels, "clocks": clocks}
         print(json.dumps(line), flush=True)
     if pg is not None:
@@ -432,8 +432,11 @@ def normalize_pass_roofline(wl, kern, peaks):
 
 
 def measure_e2e(args, wl, op, inp, dev, tdt, bf, w_dev, b_dev, ga_dev, be_dev, b2_dev, am):
-    """Same step through the C ABI from pinned host buffers: H2D of x and the parameters, the
-    operator, D2H of the result, all inside the timed region."""
+    """The operator end to end through the C ABI, fed from and read back to pinned host memory: every
+    step copies its inputs (x and the parameters) host -> device, runs the operator (weight pack
+    included) and copies y device -> host, all inside the timed region. Steps are pipelined over
+    three streams and two buffer sets, as a serving loop would run them: while step i computes,
+    step i+1's inputs upload and step i-1's output downloads."""
     import torch
     host = {}
     for k in ("x", "w"):
@@ -441,32 +444,54 @@ def measure_e2e(args, wl, op, inp, dev, tdt, bf, w_dev, b_dev, ga_dev, be_dev, b
         host[k] = (t.to(tdt) if bf else t).pin_memory()
     for k in ("b", "gamma", "beta", "bias2"):
         host[k] = None if inp[k] is None else torch.from_numpy(inp[k]).pin_memory()
-    dbuf = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in host.items()}
-    y = torch.empty((wl.N, wl.C_out, op.T_out), dtype=op.out_dtype(), device=dev)
-    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    nbuf = 2
+    dsets = [{k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in host.items()}
+             for _ in range(nbuf)]
+    ys = [torch.empty((wl.N, wl.C_out, op.T_out), dtype=op.out_dtype(), device=dev) for _ in range(nbuf)]
+    y_hosts = [torch.empty(ys[0].shape, dtype=ys[0].dtype).pin_memory() for _ in range(nbuf)]
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
-    d2h = y_host.numel() * y_host.element_size()
-    stream = torch.cuda.current_stream(dev)
+    d2h = y_hosts[0].numel() * y_hosts[0].element_size()
+    s_in, s_op, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_op = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]
+    used = [False] * nbuf
 
-    def step():
-        for k, v in host.items():
-            if v is not None:
-                dbuf[k].copy_(v, non_blocking=True)
-        op(dbuf["x"], dbuf["w"], dbuf["b"], dbuf["gamma"], dbuf["beta"], bias2=dbuf["bias2"], out=y, argmin=am)
-        y_host.copy_(y, non_blocking=True)
+    def step(i):
+        j = i % nbuf
+        d = dsets[j]
+        if used[j]:
+            s_in.wait_event(ev_op[j])    # the operator of step i - nbuf has read set j
+            s_op.wait_event(ev_out[j])   # ... and step i - nbuf's y has been read back
+        with torch.cuda.stream(s_in):
+            for k, v in host.items():
+                if v is not None:
+                    d[k].copy_(v, non_blocking=True)
+            ev_in[j].record(s_in)
+        s_op.wait_event(ev_in[j])
+        with torch.cuda.stream(s_op):
+            op(d["x"], d["w"], d["b"], d["gamma"], d["beta"], bias2=d["bias2"], out=ys[j], argmin=am)
+            ev_op[j].record(s_op)
+        s_out.wait_event(ev_op[j])
+        with torch.cuda.stream(s_out):
+            y_hosts[j].copy_(ys[j], non_blocking=True)
+            ev_out[j].record(s_out)
+        used[j] = True
 
-    for _ in range(max(1, args.warmup)):
-        step()
+    for i in range(max(2, args.warmup)):
+        step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(args.steps):
+        step(i)
+    s_out.wait_event(ev_out[(args.steps - 1) % nbuf])
+    e1.record(s_out)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     return {"value": wl.flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "pipeline": "3 streams (H2D / operator / D2H), 2 buffer sets"}
 
 
 def shard_inputs(wl, rank, seed=0):
