@@ -156,6 +156,12 @@ bool plan_tc_geometry(const c1n_params& p, Plan& pl, bool cluster, bool pair = f
     const long long pl_al = (long long)round_up(p.pad_left, pl.align);
     pl.t_shift = (int)(pl_al - p.pad_left);
     pl.RS = (int)round_up(pl.R + pl.t_shift, pl.align);
+    // bf16: the transposer's ldmatrix reads 8 channel rows of 16 bytes at the row pitch RS; an odd
+    // multiple of 16 bytes puts them in 8 different bank groups
+    if (pl.bf16) {
+        pl.RS = (int)round_up(pl.R + pl.t_shift, 8);
+        if (pl.RS % 16 != 8) pl.RS += 8;
+    }
     if (pl.RS > 256) return false;  // one TMA box per (chunk, tile)
     pl.a_slot_bytes = pl.R * 128;
     pl.s_slot_bytes = (int)round_up((size_t)pl.BK * pl.RS * pl.esize, 1024);

@@ -44,10 +44,13 @@
 namespace c1n {
 namespace {
 
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpEpi0 = 2, kWarpXp0 = 6, kXpWarps = 8;
-constexpr int kWarpXld = kWarpXp0 + kXpWarps;  // x staging loader (conv mode)
-constexpr int kThreads = 32 * (kWarpXld + 1);  // every warp has exactly one role
-constexpr int kEpiThreads = 128, kXpThreads = 32 * kXpWarps;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpEpi0 = 2, kWarpXld = 14;
+constexpr int kThreads = 32 * (kWarpXld + 1);  // 15 warps
+constexpr int kEpiThreads = 128;
+// x transposer warps: fp32 data, warps 6-13 (16-byte column chunk per warp); bf16 data, warps 10-13
+// (8x8 block transposes with ldmatrix / stmatrix); warps 6-9 then have no role.
+template <bool BF16> __host__ __device__ constexpr int xp_first() { return BF16 ? 10 : 6; }
+template <bool BF16> __host__ __device__ constexpr int xp_warps() { return BF16 ? 4 : 8; }
 
 // Where a bounded wait gave up (status word detail).
 enum WaitSite {
@@ -346,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < SA; ++i) {
             // TMA arrive, or one per transposer warp (of both CTAs of a pair)
-            mbar_init(bar(i_afull + i), LINEAR ? 1 : (PAIR ? 2 : 1) * kXpWarps);
+            mbar_init(bar(i_afull + i), LINEAR ? 1 : (PAIR ? 2 : 1) * xp_warps<BF16>());
             mbar_init(bar(i_aempty + i), 1);
         }
         for (int i = 0; i < SB; ++i) {
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) mbar_init(bar(i_ex + i), kEpiThreads);  // the peer's epilogue threads
         for (int i = 0; i < SS; ++i) {
             mbar_init(bar(i_sfull + i), 1);
-            mbar_init(bar(i_sempty + i), kXpWarps);  // one arrival per transposer warp
+            mbar_init(bar(i_sempty + i), xp_warps<BF16>());  // one arrival per transposer warp
         }
         *abort_flag = 0;
         for (int i = 0; i < kProgSlots; ++i) prog[i] = 0;
@@ -567,17 +570,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int s2 = 0; s2 < SS; ++s2)
                     if (s_cnt > s2) mbar_drain(bar(i_sfull + s2), s2 < si ? sph : (sph ^ 1), a.status);
         }
-    } else if (warp >= kWarpXp0) {
+    } else if (warp >= xp_first<BF16>() && warp < xp_first<BF16>() + xp_warps<BF16>()) {
         // ---------------------------------------------------------------- x transposer (conv mode)
         // Staged x (rows = channels, time-contiguous) -> A tile (rows = time steps, 128 bytes of
-        // channels per row, 128-byte swizzle). Transposer warp w owns the 16-byte column chunk w of
-        // every A row; its lanes take consecutive rows, so the staged reads are consecutive
-        // elements (one wavefront) and each group of 8 lanes writes 8 distinct swizzled chunks
-        // (all 32 banks).
+        // channels per row, 128-byte swizzle).
         if (!LINEAR) {
-            const int xt = threadIdx.x - kWarpXp0 * 32;  // 0..255
-            const int cg = warp - kWarpXp0;               // 0..7
-            constexpr int kPerChunk = BF16 ? 8 : 4;       // channels per 16-byte chunk
+            constexpr int kXp0 = xp_first<BF16>(), kXpW = xp_warps<BF16>();
+            const int xw = warp - kXp0;
             const int R = a.R, RS = a.RS;
             int ai = 0, si = 0;
             uint32_t aph = 0, sph = 0;
@@ -589,28 +588,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = mbar_wait(bar(i_sfull + si), sph, abort_flag, a.status, kWaitSFull, prog) &&
                              wait_bar(i_aempty + ai, aph ^ 1, kWaitAEmpty);
                     if (!__shfl_sync(0xffffffffu, ok, 0)) goto xp_done;
-                    const InT* col = reinterpret_cast<const InT*>(base + s_off + size_t(si) * a.s_slot_bytes) +
-                                     (cg * kPerChunk) * RS + a.t_shift;
                     uint8_t* slot = base + size_t(ai) * a.a_slot_bytes;
-#pragma unroll 2
-                    for (int r = lane; r < R; r += 32) {
-                        const InT* src = col + r;
-                        uint4 pk;
-                        if constexpr (BF16) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const uint32_t lo = *reinterpret_cast<const uint16_t*>(src + (2 * e) * RS);
-                                const uint32_t hi = *reinterpret_cast<const uint16_t*>(src + (2 * e + 1) * RS);
-                                w[e] = lo | (hi << 16);
-                            }
-                            pk = make_uint4(w[0], w[1], w[2], w[3]);
-                        } else {
-                            pk = make_uint4(__float_as_uint(src[0]), __float_as_uint(src[RS]),
-                                            __float_as_uint(src[2 * RS]), __float_as_uint(src[3 * RS]));
+                    if constexpr (BF16) {
+                        // 8x8 blocks (8 channels x 8 staged steps) through ldmatrix.trans + stmatrix,
+                        // four blocks (channel groups 4*quad .. 4*quad+3) per instruction pair. Lane l
+                        // gives row l%8 of block l/8: the source row is channel 8*cg + l%8 at staged
+                        // steps 8*tg.., the destination row is A row 8*tg + l%8 - t_shift (rows
+                        // outside the tile go to a scratch row). The staging row pitch RS is an odd
+                        // multiple of 16 bytes, so the 8 rows of a block hit 8 different bank groups.
+                        const uint32_t stg = sS + uint32_t(si * a.s_slot_bytes);
+                        const uint32_t dslot = smem_u32(slot);
+                        const uint32_t dummy = smem_u32(misc + 512) + uint32_t(lane * 16);
+                        const int n_tg = (a.t_shift + R + 7) / 8;
+                        const int mi = lane >> 3, ii = lane & 7;
+                        for (int opi = xw; opi < 2 * n_tg; opi += kXpW) {
+                            const int tg = opi >> 1, cg = (opi & 1) * 4 + mi;
+                            uint32_t r[4];
+                            ldmatrix_x4_trans(stg + uint32_t(((8 * cg + ii) * RS + 8 * tg) * 2), r);
+                            const int rr = 8 * tg + ii - a.t_shift;
+                            const uint32_t dst = (rr >= 0 && rr < R)
+                                                     ? dslot + uint32_t(rr * 128 + ((cg ^ (rr & 7)) << 4))
+                                                     : dummy;
+                            stmatrix_x4(dst, r);
                         }
-                        // 16-byte chunk cg of row r sits at chunk position cg ^ (r & 7)
-                        *reinterpret_cast<uint4*>(slot + r * 128 + ((cg ^ (r & 7)) << 4)) = pk;
+                    } else {
+                        // Warp w owns the 16-byte column chunk w of every A row; its lanes take
+                        // consecutive rows, so the staged reads are consecutive elements (one
+                        // wavefront) and each group of 8 lanes writes 8 distinct swizzled chunks.
+                        const int cg = xw;
+                        const InT* col = reinterpret_cast<const InT*>(base + s_off + size_t(si) * a.s_slot_bytes) +
+                                         (cg * 4) * RS + a.t_shift;
+#pragma unroll 2
+                        for (int r = lane; r < R; r += 32) {
+                            const InT* src = col + r;
+                            const uint4 pk = make_uint4(__float_as_uint(src[0]), __float_as_uint(src[RS]),
+                                                        __float_as_uint(src[2 * RS]), __float_as_uint(src[3 * RS]));
+                            // 16-byte chunk cg of row r sits at chunk position cg ^ (r & 7)
+                            *reinterpret_cast<uint4*>(slot + r * 128 + ((cg ^ (r & 7)) << 4)) = pk;
+                        }
                     }
                     // Make the generic-proxy stores visible to the tensor core, then signal.
                     fence_async_shared();
@@ -619,14 +634,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         arrive_leader(i_afull + ai);
                         mbar_arrive(bar(i_sempty + si));
                     }
-                    if (xt == 0) prog[3] = prog[3] + 1;
+                    if (threadIdx.x == kXp0 * 32) prog[3] = prog[3] + 1;
                     if (++ai == SA) { ai = 0; aph ^= 1; }
                     if (++si == SS) { si = 0; sph ^= 1; }
                 }
             }
         xp_done:;
         }
-    } else {
+    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
         // ---------------------------------------------------------------- epilogue warps 2..5
         const int q = warp & 3;       // TMEM lane quarter this warp may access
         const int m = q * 32 + lane;  // tile row: time step (conv) or sample row (Linear)
@@ -1095,7 +1110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the epilogue's first one publishes the partial statistics (the other warps, or an
         // epilogue that gave up, arrive for it here), the second keeps each CTA's shared memory
         // alive until its peers have read it.
-        if (warp < kWarpEpi0 || warp >= kWarpXp0) cluster_sync_all();
+        if (warp < kWarpEpi0 || warp >= kWarpEpi0 + 4) cluster_sync_all();
         cluster_sync_all();
     }
     __syncwarp();
