@@ -310,7 +310,8 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
                 (want == C1N_PATH_AUTO || want == C1N_PATH_TC_FUSED_LN)) {
                 Plan ln = pl;
                 const bool two = p.C_out > 256;
-                if (plan_tc_geometry(p, ln, false, !two, 4 * 2 * 32 * 32 * ln.esize)) {
+                // output staging: 2 tiles of 32 x 32 per epilogue warp (8 warps for bf16, else 4)
+                if (plan_tc_geometry(p, ln, false, !two, (ln.bf16 ? 8 : 4) * 2 * 32 * 32 * ln.esize)) {
                     ln.cb_per_unit = two ? 1 : ln.n_cb;
                     ln.n_units = p.N * ln.n_t_tiles;
                     ln.n_acc = 2;

@@ -283,6 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // exchange per-row LayerNorm partial sums through distributed shared memory.
     constexpr bool kClusterX = EPI == kEpiLNX;
     static_assert(!(PAIR && (kFusedGN || kClusterX)), "the exchanging epilogues run one CTA per tile");
+    // Epilogue warps: 4 (one per TMEM lane quarter), or 8 for the bf16 LayerNorm epilogues (two per
+    // quarter, each taking a column range); the bf16 transposer leaves warps 6-9 free for them.
+    constexpr int kEpiW = (BF16 && (EPI == kEpiLN || EPI == kEpiLNX)) ? 8 : 4;
+    constexpr int kEpiT = 32 * kEpiW;
+    static_assert(kWarpEpi0 + kEpiW <= xp_first<BF16>(), "epilogue and transposer warps overlap");
     using InT = typename std::conditional<BF16, __nv_bfloat16, float>::type;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -358,10 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(i_accfull + i), 1);
-            mbar_init(bar(i_accempty + i), PAIR ? 8 : 4);  // one arrival per epilogue warp (of the pair)
+            mbar_init(bar(i_accempty + i), (PAIR ? 2 : 1) * kEpiW);  // one arrival per epilogue warp (of the pair)
         }
         mbar_init(bar(i_drain), 1);
-        for (int i = 0; i < 2; ++i) mbar_init(bar(i_ex + i), kEpiThreads);  // the peer's epilogue threads
+        for (int i = 0; i < 2; ++i) mbar_init(bar(i_ex + i), 128);  // one per step, from the peer's first 4 epilogue warps
         for (int i = 0; i < SS; ++i) {
             mbar_init(bar(i_sfull + i), 1);
             mbar_init(bar(i_sempty + i), xp_warps<BF16>());  // one arrival per transposer warp
@@ -641,11 +646,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         xp_done:;
         }
-    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
-        // ---------------------------------------------------------------- epilogue warps 2..5
+    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiW) {
+        // ---------------------------------------------------------------- epilogue warps 2..(2+kEpiW-1)
         const int q = warp & 3;       // TMEM lane quarter this warp may access
         const int m = q * 32 + lane;  // tile row: time step (conv) or sample row (Linear)
-        const int er = threadIdx.x - kWarpEpi0 * 32;  // 0..127, index among epilogue threads
+        const int er = threadIdx.x - kWarpEpi0 * 32;  // index among the epilogue threads
+        const int eg = (warp - kWarpEpi0) >> 2;       // column range (two warps per quarter)
         bool mid_sync_done = false;
         // Per-channel parameters of the current channel block, staged once in shared memory so the
         // element loops below read them with conflict-free broadcast loads instead of global loads.
@@ -657,13 +663,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // mainloop runs (gamma and beta go where the column scale / shift end up).
             const int co_base = decode(first_unit).cbu * a.BN;
             const int ncols = min(a.BN, a.C_out - co_base);
-            for (int col = er; col < 256; col += kEpiThreads) {
+            for (int col = er; col < 256; col += kEpiT) {
                 const bool ok = col < ncols;
                 s_bias[col] = (ok && a.bias) ? __ldg(a.bias + co_base + col) : 0.f;
                 epi[2304 + col] = ok ? (a.gamma ? __ldg(a.gamma + co_base + col) : 1.f) : 0.f;
                 epi[2560 + col] = (ok && a.beta) ? __ldg(a.beta + co_base + col) : 0.f;
             }
-            named_bar_sync(1, kEpiThreads);
+            named_bar_sync(1, kEpiT);
         }
         int lt = 0;
         for (int u = first_unit; u < a.n_units; u += unit_step, ++lt) {
@@ -676,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int got = 0;
             if (lane == 0) got = wait_bar(i_accfull + ab, acc_par, kWaitAccFull);
             got = __shfl_sync(0xffffffffu, got, 0);
-            if (named_bar_any(1, kEpiThreads, !got || *abort_flag != 0)) break;
+            if (named_bar_any(1, kEpiT, !got || *abort_flag != 0)) break;
             __syncwarp();
             if (er == 0) prog[7] = 0;
             tc_fence_after();
@@ -690,10 +696,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int co_base = (un.cbu * a.cb_per_unit + cbi) * a.BN;
                     const int ncols = min(a.BN, a.C_out - co_base);
                     if (co_base != staged_co) {  // uniform over the epilogue threads
-                        named_bar_sync(1, kEpiThreads);
-                        for (int col = er; col < a.BN; col += kEpiThreads)
+                        named_bar_sync(1, kEpiT);
+                        for (int col = er; col < a.BN; col += kEpiT)
                             s_bias[col] = (a.bias && col < ncols) ? __ldg(a.bias + co_base + col) : 0.f;
-                        named_bar_sync(1, kEpiThreads);
+                        named_bar_sync(1, kEpiT);
                         staged_co = co_base;
                     }
                     const uint32_t tb =
@@ -735,14 +741,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* s_gamma = epi + 2304;
                 float* s_beta = epi + 2560;
                 if (co_base != staged_co) {  // uniform over the epilogue threads
-                    named_bar_sync(1, kEpiThreads);
-                    for (int col = er; col < 256; col += kEpiThreads) {
+                    named_bar_sync(1, kEpiT);
+                    for (int col = er; col < 256; col += kEpiT) {
                         const bool ok = col < ncols;
                         s_bias[col] = (ok && a.bias) ? __ldg(a.bias + co_base + col) : 0.f;
                         s_gamma[col] = ok ? (a.gamma ? __ldg(a.gamma + co_base + col) : 1.f) : 0.f;
                         s_beta[col] = (ok && a.beta) ? __ldg(a.beta + co_base + col) : 0.f;
                     }
-                    named_bar_sync(1, kEpiThreads);
+                    named_bar_sync(1, kEpiT);
                     staged_co = co_base;
                 }
                 const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
@@ -783,38 +789,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ------------------------------------------------ channel LayerNorm (conv mode)
                 // One thread owns one time step. kEpiLN: this CTA holds every channel of the tile.
                 // kEpiLNX: it holds channels [crank*BN, crank*BN + BN) and its cluster peer the rest
-                // of the same 128 steps. Statistics: one pass of sums shifted by the step's first
-                // value gives this half's mean and M2; kEpiLNX exchanges them with the peer
-                // (distributed shared memory + a remote arrival) and both merge the halves with
-                // Chan's formula in rank order, so both compute the same mean and variance. Then
-                // normalize + affine (+ GELU), staged per warp as [32 channels][32 steps] tiles in
-                // shared memory and written by TMA bulk stores (or direct stores when y's layout
-                // does not allow TMA).
+                // of the same 128 steps. With bf16 data two epilogue warps share each TMEM lane
+                // quarter and split the channels in two column ranges. Statistics: one pass of sums
+                // shifted by the range's first value gives each range's mean and M2; the ranges of
+                // a CTA are merged through shared memory, the CTA halves of kEpiLNX through
+                // distributed shared memory (remote stores + a remote arrival), all with Chan's
+                // formula in a fixed order, so every thread of both CTAs computes the same mean and
+                // variance. Then normalize + affine (+ GELU), staged per warp as [32 channels][32
+                // steps] tiles in shared memory and written by TMA bulk stores (or direct stores
+                // when y's layout does not allow TMA).
                 float* s_bias = epi;
                 float* s_gamma = epi + 256;
                 float* s_beta = epi + 512;
-                float* xbuf = epi + 768;  // [2][128]: the peer's mean and M2 per step
+                float* xbuf = epi + 768 + 256 * (lt & 1);  // [2 tiles][2][128]: the peer's mean and M2
+                float* hst = epi + 1280 + 512 * (lt & 1);  // [2 tiles][2 ranges][128][2]: range statistics
                 const int co_base = un.cbu * a.BN;
                 const int ncols = min(a.BN, a.C_out - co_base);
                 if (staged_co < 0) {
-                    for (int c = er; c < 256; c += kEpiThreads) {
+                    for (int c = er; c < 256; c += kEpiT) {
                         const bool ok = c < ncols;
                         s_bias[c] = (ok && a.bias) ? __ldg(a.bias + co_base + c) : 0.f;
                         s_gamma[c] = ok ? (a.gamma ? __ldg(a.gamma + co_base + c) : 1.f) : 0.f;
                         s_beta[c] = (ok && a.beta) ? __ldg(a.beta + co_base + c) : 0.f;
                     }
-                    named_bar_sync(1, kEpiThreads);
+                    named_bar_sync(1, kEpiT);
                     staged_co = co_base;
                 }
+                // this warp's column range [c_lo, c_hi) (whole 32-column chunks but the last)
+                const int half = kEpiW == 8 ? ((ncols + 63) / 64) * 32 : ncols;
+                const int c_lo = eg == 0 ? 0 : min(half, ncols);
+                const int c_hi = eg == 0 ? min(half, ncols) : ncols;
                 const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
                 float shift = 0.f, s1 = 0.f, s2 = 0.f;
-                for (int j0 = 0; j0 < ncols; j0 += 32) {
+                for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
                     float v[32];
                     tmem_load32(tb + uint32_t(j0), v);
                     float bb[32];
                     lds_vec(s_bias + j0, bb);
-                    if (j0 == 0) shift = v[0] + bb[0];
-                    if (j0 + 32 <= ncols) {  // whole chunk (uniform): no per-column test
+                    if (j0 == c_lo) shift = v[0] + bb[0];
+                    if (j0 + 32 <= c_hi) {  // whole chunk (uniform): no per-column test
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const float d = v[i] + bb[i] - shift;
@@ -824,26 +837,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            if (j0 + i < ncols) {
+                            if (j0 + i < c_hi) {
                                 const float d = v[i] + bb[i] - shift;
                                 s1 += d;
                                 s2 = fmaf(d, d, s2);
                             }
                     }
                 }
-                const float n_own = float(ncols);
-                float mean = shift + s1 / n_own;
-                float m2 = fmaxf(s2 - s1 * (s1 / n_own), 0.f);
+                const float n_own = float(c_hi - c_lo);
+                float mean = n_own > 0.f ? shift + s1 / n_own : 0.f;
+                float m2 = n_own > 0.f ? fmaxf(s2 - s1 * (s1 / n_own), 0.f) : 0.f;
+                float n_cta = n_own;
+                if constexpr (kEpiW == 8) {
+                    // the two column ranges of this CTA, merged in range order
+                    hst[(eg * 128 + m) * 2] = mean;
+                    hst[(eg * 128 + m) * 2 + 1] = m2;
+                    named_bar_sync(1, kEpiT);
+                    float n0 = float(min(half, ncols)), mu0 = hst[m * 2], m20 = hst[m * 2 + 1];
+                    chan_merge(n0, mu0, m20, float(ncols) - float(min(half, ncols)), hst[(128 + m) * 2],
+                               hst[(128 + m) * 2 + 1]);
+                    mean = mu0;
+                    m2 = m20;
+                    n_cta = n0;
+                }
                 if constexpr (kClusterX) {
                     const uint32_t peer = crank ^ 1u;
-                    st_shared_cluster_f32(map_shared_rank(smem_u32(xbuf + m), peer), mean);
-                    st_shared_cluster_f32(map_shared_rank(smem_u32(xbuf + 128 + m), peer), m2);
-                    mbar_arrive_cluster(map_shared_rank(bar(i_ex), peer));
+                    if (eg == 0) {
+                        st_shared_cluster_f32(map_shared_rank(smem_u32(xbuf + m), peer), mean);
+                        st_shared_cluster_f32(map_shared_rank(smem_u32(xbuf + 128 + m), peer), m2);
+                        mbar_arrive_cluster(map_shared_rank(bar(i_ex), peer));
+                    }
                     mbar_wait_cluster(bar(i_ex), uint32_t(lt & 1), abort_flag, a.status, kWaitExchange, prog);
                     const float n_peer = float(a.C_out - ncols);
                     const float p_mean = xbuf[m], p_m2 = xbuf[128 + m];
                     // Chan's merge of (rank 0 half, rank 1 half)
-                    const float na = crank == 0 ? n_own : n_peer, nb = crank == 0 ? n_peer : n_own;
+                    const float na = crank == 0 ? n_cta : n_peer, nb = crank == 0 ? n_peer : n_cta;
                     const float ma = crank == 0 ? mean : p_mean, mb = crank == 0 ? p_mean : mean;
                     const float Ma = crank == 0 ? m2 : p_m2, Mb = crank == 0 ? p_m2 : m2;
                     const float nt = na + nb, dlt = mb - ma;
@@ -852,8 +880,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float rstd = rsqrtf(m2 / float(a.C_out) + a.eps);
                 if (a.tma_store) {
-                    OutT* ostage = reinterpret_cast<OutT*>(base + a.o_off) + q * (2 * 32 * 32);
-                    for (int j0 = 0; j0 < ncols; j0 += 32) {
+                    OutT* ostage = reinterpret_cast<OutT*>(base + a.o_off) + (warp - kWarpEpi0) * (2 * 32 * 32);
+                    for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
                         float v[32];
                         tmem_load32(tb + uint32_t(j0), v);
 #pragma unroll
@@ -884,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
                     OutT* dst = y + ((long long)un.n * a.C_out + co_base) * a.T_out + row;
-                    for (int j0 = 0; j0 < ncols; j0 += 32) {
+                    for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
                         float v[32];
                         tmem_load32(tb + uint32_t(j0), v);
 #pragma unroll
@@ -904,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (row_ok) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i)
-                                if (j0 + i < ncols) store_out(dst + (long long)(j0 + i) * a.T_out, v[i]);
+                                if (j0 + i < c_hi) store_out(dst + (long long)(j0 + i) * a.T_out, v[i]);
                         }
                     }
                 }
@@ -937,9 +965,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // pass 0: sums of the raw accumulator; the bias enters at group level as
                 // nvalid_t * sum(bias) -> count and mean of this CTA's part of each group
                 gn_run_sums_any<false>(a.sub, tb, ncols, row_ok, s_shift, red, q, lane);
-                named_bar_sync(1, kEpiThreads);
+                named_bar_sync(1, kEpiT);
                 const int run = a.sub > 0 ? a.sub : 1;
-                for (int g = er; g < ngroups; g += kEpiThreads) {
+                for (int g = er; g < ngroups; g += kEpiT) {
                     const int c0 = g * cpg, c_end = min(ncols, c0 + cpg);
                     float sum = 0.f, bsum = 0.f;
                     for (int j = c0 / run; j < (c_end + run - 1) / run; ++j)
@@ -951,26 +979,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     part[g] = cnt;
                     part[256 + g] = mean;
                 }
-                named_bar_sync(1, kEpiThreads);
-                for (int col = er; col < 256; col += kEpiThreads)
+                named_bar_sync(1, kEpiT);
+                for (int col = er; col < 256; col += kEpiT)
                     s_shift[col] = col < ncols ? gmean[col / cpg] - s_bias[col] : 0.f;
-                named_bar_sync(1, kEpiThreads);
+                named_bar_sync(1, kEpiT);
                 // pass 1: squared deviations from this CTA's group mean -> M2
                 gn_run_sums_any<true>(a.sub, tb, ncols, row_ok, s_shift, red, q, lane);
-                named_bar_sync(1, kEpiThreads);
-                for (int g = er; g < ngroups; g += kEpiThreads) {
+                named_bar_sync(1, kEpiT);
+                for (int g = er; g < ngroups; g += kEpiT) {
                     const int c0 = g * cpg, c_end = min(ncols, c0 + cpg);
                     float sum = 0.f;
                     for (int j = c0 / run; j < (c_end + run - 1) / run; ++j)
                         sum += red[j] + red[256 + j] + red[512 + j] + red[768 + j];
                     part[512 + g] = sum;
                 }
-                named_bar_sync(1, kEpiThreads);
+                named_bar_sync(1, kEpiT);
                 if (EPI == kEpiClusterGN) {
                     // partials of every CTA in the cluster become visible
                     cluster_sync_all();
                     mid_sync_done = true;
-                    for (int g = er; g < ngroups; g += kEpiThreads) {
+                    for (int g = er; g < ngroups; g += kEpiT) {
                         float gn = 0.f, gmu = 0.f, gm2 = 0.f;
                         const uint32_t p0 = smem_u32(part + g);
                         for (int rk = 0; rk < a.n_t_tiles; ++rk) {
@@ -990,12 +1018,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const size_t slot0 = size_t(un.n * a.n_cb + un.cbu) * a.n_t_tiles;
                     float4* gp = a.gpart + (slot0 + tt) * 256;
                     const unsigned target = gn_epoch + 1u;
-                    for (int g = er; g < ngroups; g += kEpiThreads) {
+                    for (int g = er; g < ngroups; g += kEpiT) {
                         gp[g] = make_float4(part[g], part[256 + g], part[512 + g], 0.f);
                         st_release_gpu(a.gsync + (slot0 + tt) * 256 + g, target);
                     }
                     const float4* gq = a.gpart + slot0 * 256;
-                    for (int g = er; g < ngroups; g += kEpiThreads) {
+                    for (int g = er; g < ngroups; g += kEpiT) {
                         float gn = 0.f, gmu = 0.f, gm2 = 0.f;
                         // all peers' flags of group g, polled together with relaxed loads (up to 16
                         // tiles per load round), then one acquire fence before their partials are read
@@ -1028,8 +1056,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         colsum[g] = rsqrtf((gn > 0.f ? gm2 / gn : 0.f) + a.eps);  // group rstd
                     }
                 }
-                named_bar_sync(1, kEpiThreads);
-                for (int col = er; col < 256; col += kEpiThreads) {
+                named_bar_sync(1, kEpiT);
+                for (int col = er; col < 256; col += kEpiT) {
                     // colscale / colshift hold gamma / beta (staged before the mainloop)
                     float sc = 0.f, sh = 0.f;
                     if (col < ncols) {
@@ -1040,7 +1068,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     colscale[col] = sc;
                     colshift[col] = sh;
                 }
-                named_bar_sync(1, kEpiThreads);
+                named_bar_sync(1, kEpiT);
                 // normalize from TMEM; store once
                 if (a.tma_store) {
                     // Each warp stages its 32 time steps of every 32-channel chunk as a [32 ch][32 t]
@@ -1110,7 +1138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the epilogue's first one publishes the partial statistics (the other warps, or an
         // epilogue that gave up, arrive for it here), the second keeps each CTA's shared memory
         // alive until its peers have read it.
-        if (warp < kWarpEpi0 || warp >= kWarpEpi0 + 4) cluster_sync_all();
+        if (warp < kWarpEpi0 || warp >= kWarpEpi0 + kEpiW) cluster_sync_all();
         cluster_sync_all();
     }
     __syncwarp();
