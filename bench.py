@@ -121,10 +121,12 @@ def config_of(wl, extra):
     return cfg
 
 
-def dtype_name(wl, path):
+def dtype_name(wl, path, math=0):
     if wl.dtype == synth.DTYPE_BF16:
         return "bf16"
-    return "f32" if path == "simt" else "tf32"
+    if path == "simt":
+        return "f32"
+    return "tf32x3" if math == 3 else "tf32"
 
 
 # ------------------------------------------------------------------------------------------ oracle arm
@@ -329,7 +331,7 @@ def our_arm(args, wl):
             cpu = time_oracle(wl, seconds=args.cpu_seconds)
         line = {"metric": args.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": dtype_name(wl, path), "data": "synthetic",
+                "vs_baseline": None, "dtype": dtype_name(wl, path, args.math), "data": "synthetic",
                 "config": config_of(wl, {"path": path, "cta_pair": int(op.info.cta_pair), "parallelism": f"dp{world}" if world > 1 else "single",
                                          "l2": f"inputs rotate over {n_sets} x/y buffer sets "
                                                f"({n_sets * per_set / 2**20:.0f} MiB > 129 MiB L2)"
@@ -527,7 +529,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=synth.CONV_GN.name)
-    ap.add_argument("--math", type=int, default=0, help="0 auto, 1 SIMT, 2 tensor")
+    ap.add_argument("--math", type=int, default=0, help="0 auto, 1 SIMT, 2 tensor, 3 tensor 3xTF32 (fp32-accurate)")
     ap.add_argument("--path", type=int, default=-1, help="force an execution path (c1n_path)")
     ap.add_argument("--mainloop", type=int, default=0, help="0 auto, 1 one CTA per tile, 2 CTA pairs")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -18,7 +18,7 @@ from . import _build_lib
 NORM_NONE, NORM_GROUP, NORM_CHANNEL_LAYER = 0, 1, 2
 POST_NONE, POST_GELU_ERF, POST_ROWMIN_BIAS = 0, 1, 2
 F32, BF16 = 0, 1
-MATH_AUTO, MATH_SIMT, MATH_TENSOR = 0, 1, 2
+MATH_AUTO, MATH_SIMT, MATH_TENSOR, MATH_TENSOR_X3 = 0, 1, 2, 3
 MAINLOOP_AUTO, MAINLOOP_SINGLE, MAINLOOP_PAIR = 0, 1, 2
 PATH_AUTO, PATH_SIMT, PATH_TC_DIRECT, PATH_TC_FUSED_GN, PATH_TC_TWO_PASS, PATH_TC_LINEAR = -1, 0, 1, 2, 3, 4
 PATH_TC_FUSED_GN_DSMEM, PATH_TC_FUSED_LN = 5, 6

@@ -89,7 +89,7 @@ void plan_workspace(const c1n_params& p, Plan& pl, bool conv_tc, bool need_raw, 
     size_t off = kWsStatusBytes;
     if (conv_tc) {
         pl.ws_wp = off;
-        off = round_up(off + (size_t)p.k * p.C_out * pl.ci_pad * pl.esize, 256);
+        off = round_up(off + (size_t)(pl.x3 ? 2 : 1) * p.k * p.C_out * pl.ci_pad * pl.esize, 256);
     }
     if (need_stats) {
         pl.ws_stats = off;
@@ -138,7 +138,7 @@ void plan_stages(Plan& pl, int max_a, int max_b, int max_s) {
 // for the convolution, whose A tiles are rebuilt by each CTA's transposer warps and where one CTA
 // per tile measured faster (causal 32x256x8192 k4: 0.185 vs 0.204 ms).
 bool pair_ok(const c1n_params& p, const Plan& pl, bool linear) {
-    if (pl.BN % 32 != 0 || p.mainloop == C1N_MAINLOOP_SINGLE) return false;
+    if (pl.BN % 32 != 0 || p.mainloop == C1N_MAINLOOP_SINGLE || pl.x3) return false;
     return linear || p.mainloop == C1N_MAINLOOP_PAIR;
 }
 
@@ -163,7 +163,7 @@ bool plan_tc_geometry(const c1n_params& p, Plan& pl, bool cluster, bool pair = f
         if (pl.RS % 16 != 8) pl.RS += 8;
     }
     if (pl.RS > 256) return false;  // one TMA box per (chunk, tile)
-    pl.a_slot_bytes = pl.R * 128;
+    pl.a_slot_bytes = pl.R * 128 * (pl.x3 ? 2 : 1);  // 3xTF32: head tile then tail tile
     pl.s_slot_bytes = (int)round_up((size_t)pl.BK * pl.RS * pl.esize, 1024);
     pl.n_ci_chunks = (int)ceil_div(p.C_in, pl.BK);
     pl.ci_pad = pl.n_ci_chunks * pl.BK;
@@ -214,6 +214,8 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
     pl.T_out = t_out_of(p);
     pl.bf16 = p.dtype == C1N_BF16;
     pl.esize = pl.bf16 ? 2 : 4;
+    pl.x3 = p.math == C1N_MATH_TENSOR_X3 ? 1 : 0;
+    if (pl.x3 && pl.bf16) return fail(C1N_ERR_UNSUPPORTED, "3xTF32 math needs fp32 data");
     pl.align = 16 / pl.esize;
     const bool is_linear = p.T == 1 && p.k == 1 && p.pad_left == 0 && p.pad_right == 0 && p.stride == 1;
     const bool out_needs_second_pass = p.norm != C1N_NORM_NONE || p.post == C1N_POST_ROWMIN_BIAS;
@@ -239,7 +241,9 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
 
     // ---------------------------------------------------------------- tensor-core plans
     const char* why = "";
-    if (is_linear && (want == C1N_PATH_AUTO || want == C1N_PATH_TC_LINEAR)) {
+    if (is_linear && pl.x3) {
+        why = "3xTF32 math is built for the convolution plans, not the Linear GEMM";
+    } else if (is_linear && (want == C1N_PATH_AUTO || want == C1N_PATH_TC_LINEAR)) {
         if (p.C_in % pl.align != 0) {
             why = "Linear: input features not a multiple of 16 bytes of elements";
         } else if (plan_tc_linear(p, pl)) {
@@ -353,7 +357,7 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
             }
         }
     }
-    if (p.math == C1N_MATH_TENSOR || want != C1N_PATH_AUTO)
+    if (p.math == C1N_MATH_TENSOR || p.math == C1N_MATH_TENSOR_X3 || want != C1N_PATH_AUTO)
         return fail(C1N_ERR_UNSUPPORTED, "tensor-core path unavailable: %s", *why ? why : "forced path not applicable");
     return choose_simt();
 }
@@ -367,7 +371,7 @@ c1n_status validate(const c1n_params* p) {
     if (p->norm < 0 || p->norm > 2) return fail(C1N_ERR_INVALID_ARG, "unknown norm %d", p->norm);
     if (p->post < 0 || p->post > 2) return fail(C1N_ERR_INVALID_ARG, "unknown post-op %d", p->post);
     if (p->dtype < 0 || p->dtype > 1) return fail(C1N_ERR_INVALID_ARG, "unknown dtype %d", p->dtype);
-    if (p->math < 0 || p->math > 2) return fail(C1N_ERR_INVALID_ARG, "unknown math %d", p->math);
+    if (p->math < 0 || p->math > 3) return fail(C1N_ERR_INVALID_ARG, "unknown math %d", p->math);
     if (p->force_path < -1 || p->force_path > 6) return fail(C1N_ERR_INVALID_ARG, "unknown path %d", p->force_path);
     if (p->mainloop < 0 || p->mainloop > 2) return fail(C1N_ERR_INVALID_ARG, "unknown mainloop %d", p->mainloop);
     if (p->norm == C1N_NORM_GROUP && (p->groups < 1 || p->C_out % p->groups != 0))
@@ -528,7 +532,8 @@ c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
             } else {
                 // B: packed weights wp[kk][co][ci_pad], box = BK channels x BN outputs x 1 tap.
                 // (A is written by the kernel's transposer warps; its map slot repeats B's.)
-                cuuint64_t dw[3] = {(cuuint64_t)pl.ci_pad, (cuuint64_t)p.C_out, (cuuint64_t)p.k};
+                // (3xTF32: the TF32 tails follow as taps k..2k-1)
+                cuuint64_t dw[3] = {(cuuint64_t)pl.ci_pad, (cuuint64_t)p.C_out, (cuuint64_t)p.k * (pl.x3 ? 2 : 1)};
                 cuuint64_t sw[2] = {(cuuint64_t)pl.ci_pad * es, (cuuint64_t)pl.ci_pad * p.C_out * es};
                 cuuint32_t bw[3] = {(cuuint32_t)pl.BK, (cuuint32_t)(pl.pair ? pl.BN / 2 : pl.BN), 1};
                 st = encode(&d->tm_b, wsrc, pl.bf16, 3, dw, sw, bw);
@@ -579,6 +584,7 @@ c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         t.cpg = p.C_out / t.groups;
         t.sub = (t.cpg == 4 || t.cpg == 8) ? t.cpg : (t.cpg % 16 == 0 ? 16 : 0);
         t.tma_store = tma_store ? 1 : 0;
+        t.x3 = pl.x3;
         t.o_bytes = pl.o_bytes;
         t.o_off = pl.stages_a * pl.a_slot_bytes + pl.stages_b * pl.b_slot_bytes + pl.stages_s * pl.s_slot_bytes;
         t.gpart = reinterpret_cast<float4*>(wsb + pl.ws_gpart);

@@ -36,6 +36,7 @@ struct Plan {
     int tmem_cols = 512;  // TMEM columns allocated per CTA
     int cluster = 1;
     int pair = 0;         // CTA-pair mainloop (cta_group::2): units of 256 rows, each CTA loads half of B
+    int x3 = 0;           // 3xTF32: A and B split into TF32 head + tail, three MMAs per step
     int grid = 0;
     int stages_a = 0, stages_b = 0, stages_s = 0;
     int a_slot_bytes = 0, b_slot_bytes = 0, s_slot_bytes = 0;
@@ -62,6 +63,7 @@ struct TcArgs {
     int groups, cpg;
     int sub;        // channels per partial-sum run in the GroupNorm statistics (4, 8, 16; 0 = per column)
     int tma_store;  // fused GroupNorm / LayerNorm: store the output through TMA bulk stores
+    int x3;         // 3xTF32 mainloop (A slots hold the head tile then the tail tile; B stages alternate)
     int o_off;      // LayerNorm: byte offset of the per-warp output staging tiles in shared memory
     int o_bytes;    // ... and their size (shared memory between the operand rings and the barriers)
     float eps;
@@ -100,6 +102,7 @@ cudaError_t launch_broadcast(const c1n_params& p, const Plan& pl, const float* r
 cudaError_t launch_rowmin_finish(const c1n_params& p, const Plan& pl, const float2* part, const float* bias2, void* y,
                                  int32_t* argmin, cudaStream_t stream);
 // Also zeroes `nzero` words at `zero` (the fused-GroupNorm arrival counters) when given.
+// fp32 weights are rounded to TF32; with pl.x3 the TF32 tail w - tf32(w) follows as taps k..2k-1.
 cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream,
                                 unsigned* zero = nullptr, int nzero = 0);
 

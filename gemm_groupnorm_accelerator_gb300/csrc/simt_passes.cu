@@ -488,8 +488,9 @@ __global__ void __launch_bounds__(256) rowmin_finish_kernel(int C, int n_cb, con
 
 // One CTA per output channel co: read the row w[co][*][*] (C_in*k contiguous values) with
 // coalesced loads into shared memory, then write each tap's row wp[kk][co][0..ci_pad) contiguously.
+// tf32_mode: 0 none (bf16), 1 round to TF32, 2 TF32 head at taps 0..k-1 and TF32 tail at taps k..2k-1.
 template <typename InT, typename PackT>
-__global__ void __launch_bounds__(256) pack_weights_kernel(int C_out, int C_in, int k, int ci_pad, int tf32_round,
+__global__ void __launch_bounds__(256) pack_weights_kernel(int C_out, int C_in, int k, int ci_pad, int tf32_mode,
                                                            const InT* __restrict__ w, PackT* __restrict__ wp,
                                                            unsigned* __restrict__ zero, int nzero) {
     extern __shared__ float row[];  // [C_in * k]
@@ -507,8 +508,9 @@ __global__ void __launch_bounds__(256) pack_weights_kernel(int C_out, int C_in, 
             for (int ci = threadIdx.x; ci < ci_pad; ci += blockDim.x) {
                 float v = ci < C_in ? row[(long long)ci * k + kk] : 0.f;
                 if constexpr (sizeof(PackT) == 4) {
-                    if (tf32_round) v = round_tf32(v);
-                    dst[ci] = v;
+                    const float hi = tf32_mode ? round_tf32(v) : v;
+                    dst[ci] = hi;
+                    if (tf32_mode == 2) dst[(long long)k * C_out * ci_pad + ci] = round_tf32(v - hi);
                 } else {
                     dst[ci] = __float2bfloat16_rn(v);  // exact: v came from a bf16
                 }
@@ -704,7 +706,7 @@ cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void*
     } else {
         auto k = pack_weights_kernel<float, float>;
         if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k<<<grid, 256, smem, stream>>>(p.C_out, p.C_in, p.k, pl.ci_pad, 1, static_cast<const float*>(w),
+        k<<<grid, 256, smem, stream>>>(p.C_out, p.C_in, p.k, pl.ci_pad, pl.x3 ? 2 : 1, static_cast<const float*>(w),
                                        static_cast<float*>(wp), zero, nzero);
     }
     return cudaGetLastError();

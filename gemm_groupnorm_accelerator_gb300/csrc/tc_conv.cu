@@ -427,12 +427,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tx_mult = PAIR ? 2u : 1u;
         const uint32_t tx_stage = tx_mult * uint32_t(a.b_slot_bytes + (LINEAR ? a.a_slot_bytes : 0));
         const int co_half = PAIR ? int(rank) * (a.BN / 2) : 0;
+        const int nparts = (!LINEAR && !BF16 && a.x3) ? 2 : 1;
         for (int u = first_unit; u < a.n_units && !aborting(); u += unit_step) {
             const Unit un = decode(u);
             for (int c = 0; c < a.n_ci_chunks; ++c) {
                 for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
                     const int co0 = (un.cbu * a.cb_per_unit + cbi) * a.BN + co_half;
-                    for (int kk = 0; kk < taps; ++kk) {
+                    for (int kkp = 0; kkp < taps * nparts; ++kkp) {
+                        // 3xTF32: the head tile (part 0) then the tail tile (part 1) of each tap
+                        const int kk = kkp / nparts, part = kkp - kk * nparts;
                         if (!wait_warp(i_bempty + bi, bph ^ 1, kWaitBEmpty)) goto tma_done;
                         const uint32_t full = leader_bar(i_bfull + bi);
                         const uint32_t dst_b = sB + uint32_t(bi * a.b_slot_bytes);
@@ -448,8 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     tma_load_2d(dst_b, &tm_b, full, c * a.BK, co0);
                                 }
                             } else {
-                                if constexpr (PAIR) tma_load_3d_pair(dst_b, &tm_b, full, c * a.BK, co0, kk);
-                                else tma_load_3d(dst_b, &tm_b, full, c * a.BK, co0, kk);
+                                if constexpr (PAIR) tma_load_3d_pair(dst_b, &tm_b, full, c * a.BK, co0, kk + part * a.k);
+                                else tma_load_3d(dst_b, &tm_b, full, c * a.BK, co0, kk + part * a.k);
                             }
                         }
                         __syncwarp();
@@ -488,6 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t a_step = uint32_t(a.a_slot_bytes) >> 4, b_step = uint32_t(a.b_slot_bytes) >> 4;
             const uint32_t tap_step = uint32_t(8 * a.dil);
             const uint32_t idesc = a.idesc;
+            const bool x3 = !LINEAR && !BF16 && a.x3;  // 3xTF32: hi*hi + hi*lo + lo*hi per step
+            const uint32_t a_tail = uint32_t(a.R * 8);  // the A tail tile follows the head tile (16-byte units)
             // Completion of the MMAs so far arrives on barrier i (in both CTAs of a pair).
             auto commit = [&](int i) {
                 if constexpr (PAIR) mma_commit_pair(bar(i), 3);
@@ -512,19 +517,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t d = d0 + uint32_t(256 * cbi);
                         for (int kk = 0; kk < taps; ++kk) {
                             if (!wait_warp(i_bfull + bi, bph, kWaitBFull)) { ok = false; break; }
+                            // 3xTF32: the tail tile of B is the next stage of the ring
+                            const int bi2 = bi + 1 == SB ? 0 : bi + 1;
+                            const uint32_t bph2 = bi + 1 == SB ? (bph ^ 1u) : bph;
+                            if (x3 && !wait_warp(i_bfull + bi2, bph2, kWaitBFull)) { ok = false; break; }
                             tc_fence_after();
                             const uint32_t al = LINEAR ? a_lo0 + uint32_t(bi) * a_step : a_lo + uint32_t(kk) * tap_step;
                             const uint32_t bl = b_lo0 + uint32_t(bi) * b_step;
+                            const uint32_t bl2 = b_lo0 + uint32_t(bi2) * b_step;
                             const uint32_t acc0 = (c | kk) != 0 ? 1u : 0u;
                             if (elect_one()) {
                                 mma_issue<BF16, PAIR>(d, al, bl, idesc, acc0);
                                 mma_issue<BF16, PAIR>(d, al + 2u, bl + 2u, idesc, 1u);
                                 mma_issue<BF16, PAIR>(d, al + 4u, bl + 4u, idesc, 1u);
                                 mma_issue<BF16, PAIR>(d, al + 6u, bl + 6u, idesc, 1u);
+                                if (x3) {
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) {
+                                        mma_issue<BF16, PAIR>(d, al + 2u * j, bl2 + 2u * j, idesc, 1u);           // A head x B tail
+                                        mma_issue<BF16, PAIR>(d, al + a_tail + 2u * j, bl + 2u * j, idesc, 1u);   // A tail x B head
+                                    }
+                                }
                                 commit(i_bempty + bi);
+                                if (x3) commit(i_bempty + bi2);
                             }
                             __syncwarp();
                             if (++bi == SB) { bi = 0; bph ^= 1; }
+                            if (x3 && ++bi == SB) { bi = 0; bph ^= 1; }
                         }
                     }
                     if (!ok) break;
@@ -623,13 +642,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int cg = xw;
                         const InT* col = reinterpret_cast<const InT*>(base + s_off + size_t(si) * a.s_slot_bytes) +
                                          (cg * 4) * RS + a.t_shift;
+                        if (a.x3) {
+                            // 3xTF32: the TF32 head (rounded) in the first tile, the tail x - head in
+                            // the second (R rows further)
 #pragma unroll 2
-                        for (int r = lane; r < R; r += 32) {
-                            const InT* src = col + r;
-                            const uint4 pk = make_uint4(__float_as_uint(src[0]), __float_as_uint(src[RS]),
-                                                        __float_as_uint(src[2 * RS]), __float_as_uint(src[3 * RS]));
-                            // 16-byte chunk cg of row r sits at chunk position cg ^ (r & 7)
-                            *reinterpret_cast<uint4*>(slot + r * 128 + ((cg ^ (r & 7)) << 4)) = pk;
+                            for (int r = lane; r < R; r += 32) {
+                                const InT* src = col + r;
+                                float v[4] = {float(src[0]), float(src[RS]), float(src[2 * RS]), float(src[3 * RS])};
+                                float h[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) h[e] = round_tf32(v[e]);
+                                const int off = r * 128 + ((cg ^ (r & 7)) << 4);
+                                *reinterpret_cast<uint4*>(slot + off) = make_uint4(
+                                    __float_as_uint(h[0]), __float_as_uint(h[1]), __float_as_uint(h[2]), __float_as_uint(h[3]));
+                                *reinterpret_cast<uint4*>(slot + R * 128 + off) =
+                                    make_uint4(__float_as_uint(v[0] - h[0]), __float_as_uint(v[1] - h[1]),
+                                               __float_as_uint(v[2] - h[2]), __float_as_uint(v[3] - h[3]));
+                            }
+                        } else {
+#pragma unroll 2
+                            for (int r = lane; r < R; r += 32) {
+                                const InT* src = col + r;
+                                const uint4 pk = make_uint4(__float_as_uint(src[0]), __float_as_uint(src[RS]),
+                                                            __float_as_uint(src[2 * RS]), __float_as_uint(src[3 * RS]));
+                                // 16-byte chunk cg of row r sits at chunk position cg ^ (r & 7)
+                                *reinterpret_cast<uint4*>(slot + r * 128 + ((cg ^ (r & 7)) << 4)) = pk;
+                            }
                         }
                     }
                     // Make the generic-proxy stores visible to the tensor core, then signal.

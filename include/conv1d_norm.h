@@ -65,8 +65,13 @@ typedef enum { C1N_F32 = 0, C1N_BF16 = 1 } c1n_dtype;
 
 /* Arithmetic used for the contraction. AUTO picks the tensor-core path when the shape allows it
  * (TF32 tensor cores for fp32 data, BF16 for bf16 data) and the SIMT fp32 CUDA path otherwise;
- * TENSOR fails with C1N_ERR_UNSUPPORTED instead of falling back; SIMT always uses fp32 FMA. */
-typedef enum { C1N_MATH_AUTO = 0, C1N_MATH_SIMT = 1, C1N_MATH_TENSOR = 2 } c1n_math;
+ * TENSOR fails with C1N_ERR_UNSUPPORTED instead of falling back; SIMT always uses fp32 FMA.
+ * TENSOR_X3 (fp32 data, convolution plans): fp32-accurate tensor cores. Each operand is split into
+ * a TF32 head and a TF32 tail (x = hi + lo, hi = x rounded to TF32, lo = x - hi) and the products
+ * are accumulated in fp32 as hi*hi + hi*lo + lo*hi (three MMAs per step; lo*lo, ~2^-22 of the
+ * product, is dropped), which meets fp32-level tolerances at about a third of the TF32 rate.
+ * Unsupported (C1N_ERR_UNSUPPORTED) for bf16 data and for the Linear plan. */
+typedef enum { C1N_MATH_AUTO = 0, C1N_MATH_SIMT = 1, C1N_MATH_TENSOR = 2, C1N_MATH_TENSOR_X3 = 3 } c1n_math;
 
 /* Execution plans (reported by conv1d_norm_plan_info; forceable for testing and measurement). */
 typedef enum {

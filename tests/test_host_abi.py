@@ -116,6 +116,20 @@ def test_cta_pair_refused_where_the_plan_cannot_pair():
     c1n.conv1d_norm_destroy(d)
 
 
+def test_tensor_x3_plans():
+    # 3xTF32: fp32 convolution plans only; the packed weights hold the TF32 head and tail
+    base = c1n.conv1d_norm_desc_create(_params(synth.CONV_GN))
+    d = c1n.conv1d_norm_desc_create(_params(synth.CONV_GN, math=c1n.MATH_TENSOR_X3))
+    assert c1n.PATH_NAMES[c1n.conv1d_norm_plan_info(d).path] == "tc_fused_gn"
+    assert c1n.conv1d_norm_workspace_size(d) > c1n.conv1d_norm_workspace_size(base)
+    c1n.conv1d_norm_destroy(d)
+    c1n.conv1d_norm_destroy(base)
+    for wl in (synth.CONV_LN_GELU_BF16, synth.LINEAR_GN_ROWMIN):
+        with pytest.raises(c1n.C1NError) as e:
+            c1n.conv1d_norm_desc_create(_params(wl, math=c1n.MATH_TENSOR_X3))
+        assert e.value.status == c1n.ERR_UNSUPPORTED
+
+
 def test_simt_forced_and_tensor_forced():
     wl = synth.CONV_GN_TINY
     d = c1n.conv1d_norm_desc_create(_params(wl, math=c1n.MATH_SIMT))
@@ -135,7 +149,7 @@ def test_simt_forced_and_tensor_forced():
 
 @pytest.mark.parametrize("bad", [dict(N=0), dict(C_in=0), dict(k=0), dict(stride=0), dict(dilation=0),
                                  dict(pad_left=-1), dict(groups=3), dict(eps=0.0), dict(eps=float("nan")),
-                                 dict(norm=7), dict(post=5), dict(dtype=3), dict(math=9), dict(T=2, k=5),
+                                 dict(norm=7), dict(post=5), dict(dtype=3), dict(math=9), dict(math=4), dict(T=2, k=5),
                                  dict(force_path=11), dict(mainloop=3), dict(mainloop=-1)])
 def test_invalid_params_are_rejected(bad):
     with pytest.raises(c1n.C1NError) as e:

@@ -50,10 +50,10 @@ def run_gpu(c1n, wl, inp, math=0, force_path=-1, mainloop=0):
     return y, (None if am is None else am.cpu().numpy()), path
 
 
-def compare(wl, y, am, ref, ref_am, path, label=""):
+def compare(wl, y, am, ref, ref_am, path, label="", tol=None):
     assert np.all(np.isfinite(y)), f"{label}: non-finite output (unwritten elements?)"
     err = float(np.max(np.abs(y.astype(np.float64) - ref)))
-    tol = _tol(wl, path)
+    tol = _tol(wl, path) if tol is None else tol
     assert err <= tol, f"{label} path={path}: max abs err {err:.3e} > {tol}"
     if ref_am is not None:
         # argmin must match where the minimum is unique by a margin > 1e-2
@@ -240,6 +240,31 @@ def test_gelu_accuracy_on_exact_inputs(cuda_lib):
     assert path == "tc_linear"
     err = np.abs(y.astype(np.float64) - ref)
     assert err.max() < 3e-6, err.max()
+
+
+X3_NAMES = ["gn_tiny", "gn_c2_structure", "gn_cpg4", "gn_gelu", "gn_ragged_out", "causal_k4", "conv_dil3_pads",
+            "conv_k1", "conv_gelu", "ln_c384_f32"]
+
+
+@pytest.mark.parametrize("name", X3_NAMES)
+def test_tensor_x3_meets_fp32_tolerance(cuda_lib, name):
+    # 3xTF32 (head + tail split of both operands, three MMAs per step): the tensor-core path held to
+    # the fp32 tolerance of the SIMT check path
+    wl = SMALL[name]
+    inp = _inputs(wl)
+    ref, _ = oracle_full(wl, inp)
+    y, am, path = run_gpu(cuda_lib, wl, inp, math=cuda_lib.MATH_TENSOR_X3)
+    assert path != "simt"
+    compare(wl, y, am, ref, None, path, name + " (3xTF32)", tol=TOL_SIMT)
+
+
+def test_tensor_x3_full_conv_gn(cuda_lib):
+    wl = synth.CONV_GN
+    inp = _inputs(wl)
+    ref, _ = oracle_full(wl, inp)
+    y, _, path = run_gpu(cuda_lib, wl, inp, math=cuda_lib.MATH_TENSOR_X3)
+    assert path == "tc_fused_gn"
+    compare(wl, y, None, ref, None, path, wl.name + " (3xTF32)", tol=TOL_SIMT)
 
 
 def test_repeated_calls_are_identical(cuda_lib):
