@@ -294,11 +294,11 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
                 pl.cluster = pl.n_t_tiles;
                 pl.grid = pl.n_units;
                 plan_workspace(p, pl, true, false, false);
-                // grid exchange: per-(sample, block, tile, group) partials and release flags
-                pl.gsync_count = pl.n_units * 256;
-                pl.ws_gsync = pl.ws_total;
-                pl.ws_gpart = round_up(pl.ws_gsync + (size_t)pl.gsync_count * 4, 256);
-                pl.ws_total = round_up(pl.ws_gpart + (size_t)pl.n_units * 256 * sizeof(float4), 256);
+                // grid exchange: per (sample, channel block, time tile, group) two 64-bit words
+                pl.gstride = (std::min(pl.BN, p.C_out) + cpg - 1) / cpg;
+                pl.gx_words = pl.n_units * pl.gstride * 4;
+                pl.ws_gx = pl.ws_total;
+                pl.ws_total = round_up(pl.ws_gx + (size_t)pl.gx_words * 4, 256);
                 pl.kernels = 2;
                 return C1N_OK;
             }
@@ -507,9 +507,9 @@ c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         if (!linear) {
             void* wp = wsb + pl.ws_wp;
             if (!(a->flags & C1N_FLAG_WEIGHTS_PACKED)) {
-                unsigned* zero = pl.gsync_count ? reinterpret_cast<unsigned*>(wsb + pl.ws_gsync) : nullptr;
+                unsigned* zero = pl.gx_words ? reinterpret_cast<unsigned*>(wsb + pl.ws_gx) : nullptr;
                 mark(d, s, "pack_weights");
-                e = launch_pack_weights(p, pl, a->w, wp, s, zero, pl.gsync_count);
+                e = launch_pack_weights(p, pl, a->w, wp, s, zero, pl.gx_words);
                 if (e != cudaSuccess) return cuda_fail(e, "weight pack launch");
             }
             wsrc = wp;
@@ -587,8 +587,11 @@ c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         t.x3 = pl.x3;
         t.o_bytes = pl.o_bytes;
         t.o_off = pl.stages_a * pl.a_slot_bytes + pl.stages_b * pl.b_slot_bytes + pl.stages_s * pl.s_slot_bytes;
-        t.gpart = reinterpret_cast<float4*>(wsb + pl.ws_gpart);
-        t.gsync = reinterpret_cast<unsigned*>(wsb + pl.ws_gsync);
+        t.gx = reinterpret_cast<unsigned long long*>(wsb + pl.ws_gx);
+        t.gstride = pl.gstride;
+        // x may be read before the kernel waits on its predecessor only when that predecessor is
+        // the weight pack launched just above (which itself starts after all earlier work)
+        t.early_inputs = (!linear && !(a->flags & C1N_FLAG_WEIGHTS_PACKED)) ? 1 : 0;
         t.row_cpg = (pl.row_epilogue && p.norm == C1N_NORM_GROUP) ? p.C_out / p.groups : 0;
         t.rowmin = (pl.row_epilogue && p.post == C1N_POST_ROWMIN_BIAS) ? 1 : 0;
         t.rowpart = reinterpret_cast<float2*>(wsb + pl.ws_rowpart);
@@ -742,9 +745,9 @@ c1n_status conv1d_norm_pack_weights(c1n_desc* desc, const void* w, void* workspa
     if (!ws || ws_bytes < pl.ws_total)
         return fail(C1N_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", pl.ws_total, ws ? ws_bytes : 0);
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(C1N_ERR_ALIGNMENT, "workspace not 256-byte aligned");
-    unsigned* zero = pl.gsync_count ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + pl.ws_gsync) : nullptr;
+    unsigned* zero = pl.gx_words ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + pl.ws_gx) : nullptr;
     cudaError_t e = launch_pack_weights(desc->p, pl, w, static_cast<uint8_t*>(ws) + pl.ws_wp,
-                                        reinterpret_cast<cudaStream_t>(stream), zero, pl.gsync_count);
+                                        reinterpret_cast<cudaStream_t>(stream), zero, pl.gx_words);
     if (e != cudaSuccess) return cuda_fail(e, "weight pack launch");
     return C1N_OK;
 }

@@ -45,10 +45,11 @@ struct Plan {
     int kernels = 0;
     // workspace layout (byte offsets)
     size_t ws_wp = 0, ws_stats = 0, ws_raw = 0, ws_rowmin = 0, ws_total = 0;
-    size_t ws_gsync = 0, ws_gpart = 0;  // fused GroupNorm across a cooperative grid
+    size_t ws_gx = 0;                   // fused GroupNorm across a cooperative grid: exchange words
     size_t ws_rowpart = 0;              // fused row-min partials
     int row_epilogue = 0;               // Linear plan with the fused row epilogue
-    int gsync_count = 0;
+    int gx_words = 0;   // 32-bit words of the exchange area (zeroed by the weight pack)
+    int gstride = 0;    // groups per channel block (exchange words per tile / 2)
 };
 
 // Shared memory beyond the operand rings: barriers, flags and epilogue scratch.
@@ -75,8 +76,11 @@ struct TcArgs {
     const float* beta;
     void* y;
     int* status;
-    float4* gpart;     // per (sample, channel block, time tile, group): count, mean, M2
-    unsigned* gsync;   // per (sample, channel block, time tile, group): release flag of the partial
+    // per (sample, channel block, time tile, group) two 64-bit words: (mean | epoch), (M2 | epoch)
+    unsigned long long* gx;
+    int gstride;       // groups per (sample, channel block, time tile) in gx
+    int early_inputs;  // the preceding launch is this library's weight pack (launched without
+                       // programmatic dependence): x may be read before griddepcontrol.wait
     int row_cpg;       // row epilogue: GroupNorm over runs of row_cpg channels (8, 16, 32; 0 = none)
     int rowmin;        // row epilogue: keep (min, argmin) per row instead of storing y
     float2* rowpart;   // row epilogue: per (row, channel block) minimum and its channel (int bits)

@@ -46,7 +46,6 @@ namespace {
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpEpi0 = 2, kWarpXld = 14;
 constexpr int kThreads = 32 * (kWarpXld + 1);  // 15 warps
-constexpr int kEpiThreads = 128;
 // x transposer warps: fp32 data, warps 6-13 (16-byte column chunk per warp); bf16 data, warps 10-13
 // (8x8 block transposes with ldmatrix / stmatrix); warps 6-9 then have no role.
 template <bool BF16> __host__ __device__ constexpr int xp_first() { return BF16 ? 10 : 6; }
@@ -101,82 +100,159 @@ __device__ __forceinline__ void chan_merge(float& n_a, float& mu_a, float& m2_a,
     n_a = n;
 }
 
-// Butterfly reduce-scatter over the warp: lane l receives the sum over all 32 lanes of v[l].
-// 31 shuffles for 32 columns.
-__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-        const bool upper = (lane & s) != 0;
-#pragma unroll
-        for (int i = 0; i < s; ++i) {
-            const float send = upper ? v[i] : v[i + s];
-            const float keep = upper ? v[i + s] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-        }
-    }
-    return v[0];
+// Chan's merge in (count, sum, M2) form: (n_a, s_a, m2_a) absorbs (n_b, s_b, m2_b).
+__device__ __forceinline__ void chan_merge_sum(float& n_a, float& s_a, float& m2_a, float n_b, float s_b, float m2_b) {
+    const float n = n_a + n_b;
+    const float den = n_a * n_b * n;
+    const float t = n_b * s_a - n_a * s_b;  // n_a * n_b * (mean_a - mean_b)
+    m2_a += m2_b + (den > 0.f ? t * t / den : 0.f);
+    s_a += s_b;
+    n_a = n;
 }
 
-// Per-thread sums over runs of SUB consecutive channels of this thread's row (SUB = 4, 8, 16
-// divides the group size; SUB = 1 is one run per channel), then one butterfly reduce-scatter per
-// 32 runs: afterwards red[q*256 + j] holds the warp's total of run j. SQUARED = false sums the raw
-// accumulator; SQUARED = true sums (acc - shift[col])^2. Rows past T_out contribute zero.
-template <int SUB, bool SQUARED>
-__device__ __forceinline__ void gn_run_sums(uint32_t tb, int ncols, bool row_ok, const float* shift, float* red,
-                                            int q, int lane) {
-    if (SUB == 1) {
-        // one run per channel: reduce each 32-column chunk as soon as it is loaded
-        for (int j0 = 0; j0 < ncols; j0 += 32) {
-            float v[32];
-            tmem_load32(tb + uint32_t(j0), v);
+// One level (lane distance d) of a butterfly reduce-scatter of (sum, M2) partials merged with
+// Chan's formula, for the slot pair (lo, lo + d): the lower lane of each lane pair keeps slot lo,
+// the upper one slot lo + d, each merged with its partner's copy. n / np: values behind this lane's
+// / the partner's partials; r = 1 / (n * np * (n + np)) (0 when either count is 0).
+__device__ __forceinline__ void chan_level(float& s_lo, float& m_lo, float s_hi, float m_hi, float n, float np,
+                                           float r, bool upper, int d) {
+    const float s_keep = upper ? s_hi : s_lo, s_send = upper ? s_lo : s_hi;
+    const float m_keep = upper ? m_hi : m_lo, m_send = upper ? m_lo : m_hi;
+    const float s_recv = __shfl_xor_sync(0xffffffffu, s_send, d);
+    const float m_recv = __shfl_xor_sync(0xffffffffu, m_send, d);
+    const float t = np * s_keep - n * s_recv;  // n * np * (mean_keep - mean_recv)
+    s_lo = s_keep + s_recv;
+    m_lo = fmaf(t * t, r, m_keep + m_recv);
+}
+
+__device__ __forceinline__ float chan_level_r(float n, float np) {
+    const float den = n * np * (n + np);
+    return den > 0.f ? 1.f / den : 0.f;
+}
+
+// Levels D, D/2, ..., 1 of the reduce-scatter over slots [0, 2D): every slot of a lane describes
+// `n` values on entry (one count for all its slots); on exit lane l holds, in slot 0, slot
+// (l mod 2D) merged over the 2D lanes that agree with l above bit log2(D).
+template <int D>
+__device__ __forceinline__ void warp_chan_scatter(float* s, float* m, float n, int lane) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float d = SQUARED ? v[i] - shift[j0 + i] : v[i];
-                v[i] = row_ok ? (SQUARED ? d * d : d) : 0.f;
-            }
-            red[q * 256 + j0 + lane] = warp_reduce_scatter32(v, lane);
-        }
-        return;
+    for (int d = D; d >= 1; d >>= 1) {
+        const float np = __shfl_xor_sync(0xffffffffu, n, d);
+        const float r = chan_level_r(n, np);
+        const bool upper = (lane & d) != 0;
+#pragma unroll
+        for (int i = 0; i < d; ++i) chan_level(s[i], m[i], s[i + d], m[i + d], n, np, r, upper, d);
+        n += np;
     }
-    constexpr int kRuns = 256 / SUB;
-    constexpr int kBlocks = (kRuns + 31) / 32;
-    float acc[kBlocks * 32];
-#pragma unroll
-    for (int i = 0; i < kBlocks * 32; ++i) acc[i] = 0.f;
-#pragma unroll
-    for (int c32 = 0; c32 < 8; ++c32) {
-        const int j0 = c32 * 32;
-        if (j0 < ncols) {  // uniform over the CTA
-            float v[32];
+}
+
+// One pass over columns [c_lo, c_hi) of this warp's TMEM lane quarter (c_lo a multiple of 32):
+// for every run of SUB consecutive channels of the thread's row (SUB = 4, 8, 16 divides the group
+// size; SUB = 1 is one run per channel), the sum and the sum of squared deviations from the run
+// mean of y = acc + bias (two passes over registers), then a Chan reduce-scatter over the warp's
+// rows. Afterwards red_s[q*256 + j] / red_m[q*256 + j] hold run j over the warp's valid rows
+// (rows past T_out count zero).
+template <int SUB>
+__device__ __forceinline__ void gn_run_stats(uint32_t tb, int c_lo, int c_hi, bool row_ok, const float* bias,
+                                             float* red_s, float* red_m, int q, int lane) {
+    const float n0 = row_ok ? float(SUB) : 0.f;
+    if constexpr (SUB == 1) {
+        for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
+            float v[32], m[32];
             tmem_load32(tb + uint32_t(j0), v);
-            if (SQUARED) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float d = v[i] - shift[j0 + i];
-                    v[i] = d * d;
+            for (int h = 0; h < 32; h += 16) {
+                float bb[16];
+                lds_vec(bias + j0 + h, bb);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[h + i] = row_ok ? v[h + i] + bb[i] : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) m[i] = 0.f;
+            warp_chan_scatter<16>(v, m, n0, lane);
+            if (j0 + lane < c_hi) {
+                red_s[q * 256 + j0 + lane] = v[0];
+                red_m[q * 256 + j0 + lane] = m[0];
+            }
+        }
+    } else {
+        // A window of up to 128 columns holds up to 32 runs (slot = run within the window). The
+        // scatter's first level (lanes 16 apart, slots 16 apart) is taken as soon as a slot >= 16
+        // is made, so only 16 (sum, M2) pairs stay live.
+        constexpr int kRunsPerChunk = 32 / SUB;           // runs per 32-column TMEM load
+        constexpr int kWin = 32 * SUB < 128 ? 32 * SUB : 128;
+        constexpr int kRuns = kWin / SUB;
+        const float np16 = __shfl_xor_sync(0xffffffffu, n0, 16);
+        const float r16 = chan_level_r(n0, np16);
+        const bool up16 = (lane & 16) != 0;
+        for (int w0 = c_lo; w0 < c_hi; w0 += kWin) {     // uniform over the warp
+            float s[16], m[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) s[i] = m[i] = 0.f;
+#pragma unroll
+            for (int c = 0; c < kWin / 32; ++c) {
+                const int j0 = w0 + c * 32;
+                if (j0 >= c_hi) break;  // uniform
+                float v[32];
+                tmem_load32(tb + uint32_t(j0), v);
+#pragma unroll
+                for (int r = 0; r < kRunsPerChunk; ++r) {
+                    float bb[SUB];
+                    lds_vec(bias + j0 + r * SUB, bb);
+                    float sum = 0.f;
+#pragma unroll
+                    for (int i = 0; i < SUB; ++i) {
+                        v[r * SUB + i] += bb[i];
+                        sum += v[r * SUB + i];
+                    }
+                    const float mean = sum * (1.f / SUB);
+                    float m2 = 0.f;
+#pragma unroll
+                    for (int i = 0; i < SUB; ++i) {
+                        const float d = v[r * SUB + i] - mean;
+                        m2 = fmaf(d, d, m2);
+                    }
+                    const int slot = c * kRunsPerChunk + r;
+                    const float rs = row_ok ? sum : 0.f, rm = row_ok ? m2 : 0.f;
+                    if (slot < 16) {
+                        s[slot] = rs;
+                        m[slot] = rm;
+                    } else {
+                        chan_level(s[slot - 16], m[slot - 16], rs, rm, n0, np16, r16, up16, 16);
+                    }
                 }
             }
+            if constexpr (kRuns <= 16) {
+                // no slot >= 16 in a window: the first level merges with empty partials
 #pragma unroll
-            for (int r = 0; r < 32 / SUB; ++r) {
-                float sum = 0.f;
+                for (int i = 0; i < 16; ++i) chan_level(s[i], m[i], 0.f, 0.f, n0, np16, r16, up16, 16);
+            } else {
+                // a window cut short by c_hi: slots it never made are empty
+                const int made = ((min(c_hi - w0, kWin) + 31) / 32) * kRunsPerChunk;
+                if (made <= 16) {
 #pragma unroll
-                for (int i = 0; i < SUB; ++i) sum += v[r * SUB + i];
-                acc[c32 * (32 / SUB) + r] = row_ok ? sum : 0.f;
+                    for (int i = 0; i < 16; ++i) chan_level(s[i], m[i], 0.f, 0.f, n0, np16, r16, up16, 16);
+                } else if (made < 32) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (i + 16 >= made) chan_level(s[i], m[i], 0.f, 0.f, n0, np16, r16, up16, 16);
+                }
+            }
+            warp_chan_scatter<8>(s, m, n0 + np16, lane);
+            if (lane < kRuns && w0 + lane * SUB < c_hi) {  // runs of the other column range stay theirs
+                red_s[q * 256 + w0 / SUB + lane] = s[0];
+                red_m[q * 256 + w0 / SUB + lane] = m[0];
             }
         }
     }
-#pragma unroll
-    for (int b = 0; b < kBlocks; ++b)
-        red[q * 256 + b * 32 + lane] = warp_reduce_scatter32(*reinterpret_cast<float(*)[32]>(&acc[b * 32]), lane);
 }
 
-template <bool SQUARED>
-__device__ __forceinline__ void gn_run_sums_any(int sub, uint32_t tb, int ncols, bool row_ok, const float* shift,
-                                                float* red, int q, int lane) {
-    if (sub == 4) gn_run_sums<4, SQUARED>(tb, ncols, row_ok, shift, red, q, lane);
-    else if (sub == 8) gn_run_sums<8, SQUARED>(tb, ncols, row_ok, shift, red, q, lane);
-    else if (sub == 16) gn_run_sums<16, SQUARED>(tb, ncols, row_ok, shift, red, q, lane);
-    else gn_run_sums<1, SQUARED>(tb, ncols, row_ok, shift, red, q, lane);
+__device__ __forceinline__ void gn_run_stats_any(int sub, uint32_t tb, int c_lo, int c_hi, bool row_ok,
+                                                 const float* bias, float* red_s, float* red_m, int q, int lane) {
+    if (sub == 4) gn_run_stats<4>(tb, c_lo, c_hi, row_ok, bias, red_s, red_m, q, lane);
+    else if (sub == 8) gn_run_stats<8>(tb, c_lo, c_hi, row_ok, bias, red_s, red_m, q, lane);
+    else if (sub == 16) gn_run_stats<16>(tb, c_lo, c_hi, row_ok, bias, red_s, red_m, q, lane);
+    else gn_run_stats<1>(tb, c_lo, c_hi, row_ok, bias, red_s, red_m, q, lane);
 }
 
 // GroupNorm of the runs of CPG consecutive channels held by one thread (CPG divides 32): two passes
@@ -207,23 +283,15 @@ __device__ __forceinline__ void row_group_norm(float (&v)[32], const float* gamm
     }
 }
 
-__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// 64-bit accesses are single-copy atomic: a word read with its epoch holds the value written with it.
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
-// Orders this thread's later loads after the relaxed loads that observed the peers' release stores.
-__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-
-__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+__device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int c0, int c1, int c2) {
@@ -283,11 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // exchange per-row LayerNorm partial sums through distributed shared memory.
     constexpr bool kClusterX = EPI == kEpiLNX;
     static_assert(!(PAIR && (kFusedGN || kClusterX)), "the exchanging epilogues run one CTA per tile");
-    // Epilogue warps: 4 (one per TMEM lane quarter), or 8 for the bf16 LayerNorm epilogues (two per
-    // quarter, each taking a column range); the bf16 transposer leaves warps 6-9 free for them.
-    constexpr int kEpiW = (BF16 && (EPI == kEpiLN || EPI == kEpiLNX)) ? 8 : 4;
+    // Epilogue warps: 4 (one per TMEM lane quarter), or 8 (two per quarter, each taking a column
+    // range) for the bf16 LayerNorm epilogues and the fused GroupNorm. The bf16 transposer leaves
+    // warps 6-9 free for them; a fused-GroupNorm CTA has one tile, so with fp32 data warps 6-9 first
+    // transpose x and then, the mainloop's operands all staged, join the epilogue.
+    constexpr int kEpiW = ((BF16 && (EPI == kEpiLN || EPI == kEpiLNX)) || kFusedGN) ? 8 : 4;
     constexpr int kEpiT = 32 * kEpiW;
-    static_assert(kWarpEpi0 + kEpiW <= xp_first<BF16>(), "epilogue and transposer warps overlap");
+    constexpr bool kShareXp = kFusedGN && !BF16;
+    static_assert(kShareXp || kWarpEpi0 + kEpiW <= xp_first<BF16>(), "epilogue and transposer warps overlap");
     using InT = typename std::conditional<BF16, __nv_bfloat16, float>::type;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -393,8 +464,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     // Everything above (barriers, TMEM, tensor-map prefetch) may overlap the previous kernel of the
     // stream; no global memory it may write (x, weights, parameters, workspace) is touched before
-    // this point.
-    griddep_wait();
+    // this point. Two roles go on without waiting: the x transposer touches no global memory, and
+    // the x loader reads only x, which the weight pack launched just before this kernel does not
+    // write (the pack itself starts only after all earlier work of the stream has finished).
+    {
+        const bool xp_role = !LINEAR && warp >= xp_first<BF16>() && warp < xp_first<BF16>() + xp_warps<BF16>();
+        if (!(xp_role || (warp == kWarpXld && a.early_inputs))) griddep_wait();
+    }
 
     int first_unit, unit_step;
     if (kFusedGN) {
@@ -594,174 +670,575 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int s2 = 0; s2 < SS; ++s2)
                     if (s_cnt > s2) mbar_drain(bar(i_sfull + s2), s2 < si ? sph : (sph ^ 1), a.status);
         }
-    } else if (warp >= xp_first<BF16>() && warp < xp_first<BF16>() + xp_warps<BF16>()) {
-        // ---------------------------------------------------------------- x transposer (conv mode)
-        // Staged x (rows = channels, time-contiguous) -> A tile (rows = time steps, 128 bytes of
-        // channels per row, 128-byte swizzle).
-        if (!LINEAR) {
-            constexpr int kXp0 = xp_first<BF16>(), kXpW = xp_warps<BF16>();
-            const int xw = warp - kXp0;
-            const int R = a.R, RS = a.RS;
-            int ai = 0, si = 0;
-            uint32_t aph = 0, sph = 0;
-            for (int u = first_unit; u < a.n_units; u += unit_step) {
-                for (int c = 0; c < a.n_ci_chunks; ++c) {
-                    // One lane waits; the shuffle hands its answer to the warp and reconverges it.
-                    int ok = 0;
-                    if (lane == 0)
-                        ok = mbar_wait(bar(i_sfull + si), sph, abort_flag, a.status, kWaitSFull, prog) &&
-                             wait_bar(i_aempty + ai, aph ^ 1, kWaitAEmpty);
-                    if (!__shfl_sync(0xffffffffu, ok, 0)) goto xp_done;
-                    uint8_t* slot = base + size_t(ai) * a.a_slot_bytes;
-                    if constexpr (BF16) {
-                        // 8x8 blocks (8 channels x 8 staged steps) through ldmatrix.trans + stmatrix,
-                        // four blocks (channel groups 4*quad .. 4*quad+3) per instruction pair. Lane l
-                        // gives row l%8 of block l/8: the source row is channel 8*cg + l%8 at staged
-                        // steps 8*tg.., the destination row is A row 8*tg + l%8 - t_shift (rows
-                        // outside the tile go to a scratch row). The staging row pitch RS is an odd
-                        // multiple of 16 bytes, so the 8 rows of a block hit 8 different bank groups.
-                        const uint32_t stg = sS + uint32_t(si * a.s_slot_bytes);
-                        const uint32_t dslot = smem_u32(slot);
-                        const uint32_t dummy = smem_u32(misc + 512) + uint32_t(lane * 16);
-                        const int n_tg = (a.t_shift + R + 7) / 8;
-                        const int mi = lane >> 3, ii = lane & 7;
-                        for (int opi = xw; opi < 2 * n_tg; opi += kXpW) {
-                            const int tg = opi >> 1, cg = (opi & 1) * 4 + mi;
-                            uint32_t r[4];
-                            ldmatrix_x4_trans(stg + uint32_t(((8 * cg + ii) * RS + 8 * tg) * 2), r);
-                            const int rr = 8 * tg + ii - a.t_shift;
-                            const uint32_t dst = (rr >= 0 && rr < R)
-                                                     ? dslot + uint32_t(rr * 128 + ((cg ^ (rr & 7)) << 4))
-                                                     : dummy;
-                            stmatrix_x4(dst, r);
-                        }
-                    } else {
-                        // Warp w owns the 16-byte column chunk w of every A row; its lanes take
-                        // consecutive rows, so the staged reads are consecutive elements (one
-                        // wavefront) and each group of 8 lanes writes 8 distinct swizzled chunks.
-                        const int cg = xw;
-                        const InT* col = reinterpret_cast<const InT*>(base + s_off + size_t(si) * a.s_slot_bytes) +
-                                         (cg * 4) * RS + a.t_shift;
-                        if (a.x3) {
-                            // 3xTF32: the TF32 head (rounded) in the first tile, the tail x - head in
-                            // the second (R rows further)
-#pragma unroll 2
-                            for (int r = lane; r < R; r += 32) {
-                                const InT* src = col + r;
-                                float v[4] = {float(src[0]), float(src[RS]), float(src[2 * RS]), float(src[3 * RS])};
-                                float h[4];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) h[e] = round_tf32(v[e]);
-                                const int off = r * 128 + ((cg ^ (r & 7)) << 4);
-                                *reinterpret_cast<uint4*>(slot + off) = make_uint4(
-                                    __float_as_uint(h[0]), __float_as_uint(h[1]), __float_as_uint(h[2]), __float_as_uint(h[3]));
-                                *reinterpret_cast<uint4*>(slot + R * 128 + off) =
-                                    make_uint4(__float_as_uint(v[0] - h[0]), __float_as_uint(v[1] - h[1]),
-                                               __float_as_uint(v[2] - h[2]), __float_as_uint(v[3] - h[3]));
+    } else {
+        // x transposer and epilogue (with fp32 data the fused GroupNorm's warps 6-9 are both, in turn)
+        if (warp >= xp_first<BF16>() && warp < xp_first<BF16>() + xp_warps<BF16>()) {
+            // ---------------------------------------------------------------- x transposer (conv mode)
+            // Staged x (rows = channels, time-contiguous) -> A tile (rows = time steps, 128 bytes of
+            // channels per row, 128-byte swizzle).
+            if (!LINEAR) {
+                constexpr int kXp0 = xp_first<BF16>(), kXpW = xp_warps<BF16>();
+                const int xw = warp - kXp0;
+                const int R = a.R, RS = a.RS;
+                int ai = 0, si = 0;
+                uint32_t aph = 0, sph = 0;
+                for (int u = first_unit; u < a.n_units; u += unit_step) {
+                    for (int c = 0; c < a.n_ci_chunks; ++c) {
+                        // One lane waits; the shuffle hands its answer to the warp and reconverges it.
+                        int ok = 0;
+                        if (lane == 0)
+                            ok = mbar_wait(bar(i_sfull + si), sph, abort_flag, a.status, kWaitSFull, prog) &&
+                                 wait_bar(i_aempty + ai, aph ^ 1, kWaitAEmpty);
+                        if (!__shfl_sync(0xffffffffu, ok, 0)) goto xp_done;
+                        uint8_t* slot = base + size_t(ai) * a.a_slot_bytes;
+                        if constexpr (BF16) {
+                            // 8x8 blocks (8 channels x 8 staged steps) through ldmatrix.trans + stmatrix,
+                            // four blocks (channel groups 4*quad .. 4*quad+3) per instruction pair. Lane l
+                            // gives row l%8 of block l/8: the source row is channel 8*cg + l%8 at staged
+                            // steps 8*tg.., the destination row is A row 8*tg + l%8 - t_shift (rows
+                            // outside the tile go to a scratch row). The staging row pitch RS is an odd
+                            // multiple of 16 bytes, so the 8 rows of a block hit 8 different bank groups.
+                            const uint32_t stg = sS + uint32_t(si * a.s_slot_bytes);
+                            const uint32_t dslot = smem_u32(slot);
+                            const uint32_t dummy = smem_u32(misc + 512) + uint32_t(lane * 16);
+                            const int n_tg = (a.t_shift + R + 7) / 8;
+                            const int mi = lane >> 3, ii = lane & 7;
+                            for (int opi = xw; opi < 2 * n_tg; opi += kXpW) {
+                                const int tg = opi >> 1, cg = (opi & 1) * 4 + mi;
+                                uint32_t r[4];
+                                ldmatrix_x4_trans(stg + uint32_t(((8 * cg + ii) * RS + 8 * tg) * 2), r);
+                                const int rr = 8 * tg + ii - a.t_shift;
+                                const uint32_t dst = (rr >= 0 && rr < R)
+                                                         ? dslot + uint32_t(rr * 128 + ((cg ^ (rr & 7)) << 4))
+                                                         : dummy;
+                                stmatrix_x4(dst, r);
                             }
                         } else {
+                            // Warp w owns the 16-byte column chunk w of every A row; its lanes take
+                            // consecutive rows, so the staged reads are consecutive elements (one
+                            // wavefront) and each group of 8 lanes writes 8 distinct swizzled chunks.
+                            const int cg = xw;
+                            const InT* col = reinterpret_cast<const InT*>(base + s_off + size_t(si) * a.s_slot_bytes) +
+                                             (cg * 4) * RS + a.t_shift;
+                            if (a.x3) {
+                                // 3xTF32: the TF32 head (rounded) in the first tile, the tail x - head in
+                                // the second (R rows further)
 #pragma unroll 2
-                            for (int r = lane; r < R; r += 32) {
-                                const InT* src = col + r;
-                                const uint4 pk = make_uint4(__float_as_uint(src[0]), __float_as_uint(src[RS]),
-                                                            __float_as_uint(src[2 * RS]), __float_as_uint(src[3 * RS]));
-                                // 16-byte chunk cg of row r sits at chunk position cg ^ (r & 7)
-                                *reinterpret_cast<uint4*>(slot + r * 128 + ((cg ^ (r & 7)) << 4)) = pk;
+                                for (int r = lane; r < R; r += 32) {
+                                    const InT* src = col + r;
+                                    float v[4] = {float(src[0]), float(src[RS]), float(src[2 * RS]), float(src[3 * RS])};
+                                    float h[4];
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) h[e] = round_tf32(v[e]);
+                                    const int off = r * 128 + ((cg ^ (r & 7)) << 4);
+                                    *reinterpret_cast<uint4*>(slot + off) = make_uint4(
+                                        __float_as_uint(h[0]), __float_as_uint(h[1]), __float_as_uint(h[2]), __float_as_uint(h[3]));
+                                    *reinterpret_cast<uint4*>(slot + R * 128 + off) =
+                                        make_uint4(__float_as_uint(v[0] - h[0]), __float_as_uint(v[1] - h[1]),
+                                                   __float_as_uint(v[2] - h[2]), __float_as_uint(v[3] - h[3]));
+                                }
+                            } else {
+#pragma unroll 2
+                                for (int r = lane; r < R; r += 32) {
+                                    const InT* src = col + r;
+                                    const uint4 pk = make_uint4(__float_as_uint(src[0]), __float_as_uint(src[RS]),
+                                                                __float_as_uint(src[2 * RS]), __float_as_uint(src[3 * RS]));
+                                    // 16-byte chunk cg of row r sits at chunk position cg ^ (r & 7)
+                                    *reinterpret_cast<uint4*>(slot + r * 128 + ((cg ^ (r & 7)) << 4)) = pk;
+                                }
+                            }
+                        }
+                        // Make the generic-proxy stores visible to the tensor core, then signal.
+                        fence_async_shared();
+                        __syncwarp();
+                        if (lane == 0) {
+                            arrive_leader(i_afull + ai);
+                            mbar_arrive(bar(i_sempty + si));
+                        }
+                        if (threadIdx.x == kXp0 * 32) prog[3] = prog[3] + 1;
+                        if (++ai == SA) { ai = 0; aph ^= 1; }
+                        if (++si == SS) { si = 0; sph ^= 1; }
+                    }
+                }
+            xp_done:;
+            }
+        }
+        if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiW) {
+            // ---------------------------------------------------------------- epilogue warps 2..(2+kEpiW-1)
+            const int q = warp & 3;       // TMEM lane quarter this warp may access
+            const int m = q * 32 + lane;  // tile row: time step (conv) or sample row (Linear)
+            const int er = threadIdx.x - kWarpEpi0 * 32;  // index among the epilogue threads
+            const int eg = (warp - kWarpEpi0) >> 2;       // column range (two warps per quarter)
+            bool mid_sync_done = false;
+            // Per-channel parameters of the current channel block, staged once in shared memory so the
+            // element loops below read them with conflict-free broadcast loads instead of global loads.
+            float* s_bias = epi + 3072;  // [256]
+            int staged_co = -1;
+            int obuf = 0;  // LayerNorm output staging: which of this warp's two tiles is next
+            if (kFusedGN && first_unit < a.n_units) {
+                // One unit per CTA: stage bias, gamma and beta of its channel block while the
+                // mainloop runs (gamma and beta go where the column scale / shift end up).
+                const int co_base = decode(first_unit).cbu * a.BN;
+                const int ncols = min(a.BN, a.C_out - co_base);
+                for (int col = er; col < 256; col += kEpiT) {
+                    const bool ok = col < ncols;
+                    s_bias[col] = (ok && a.bias) ? __ldg(a.bias + co_base + col) : 0.f;
+                    epi[2304 + col] = ok ? (a.gamma ? __ldg(a.gamma + co_base + col) : 1.f) : 0.f;
+                    epi[2560 + col] = (ok && a.beta) ? __ldg(a.beta + co_base + col) : 0.f;
+                }
+                named_bar_sync(1, kEpiT);
+            }
+            int lt = 0;
+            for (int u = first_unit; u < a.n_units; u += unit_step, ++lt) {
+                const int ab = a.n_acc == 2 ? (lt & 1) : 0;
+                const uint32_t acc_par = a.n_acc == 2 ? uint32_t((lt >> 1) & 1) : uint32_t(lt & 1);
+                if (er == 0) prog[7] = kWaitAccFull;
+                // One lane per warp waits; the shuffle reconverges the warp (the TMEM loads below are
+                // warp-collective), and the barrier ORs what every epilogue thread saw, so all four
+                // warps leave (or stay) together.
+                int got = 0;
+                if (lane == 0) got = wait_bar(i_accfull + ab, acc_par, kWaitAccFull);
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (named_bar_any(1, kEpiT, !got || *abort_flag != 0)) break;
+                __syncwarp();
+                if (er == 0) prog[7] = 0;
+                tc_fence_after();
+                const Unit un = decode(u);
+                OutT* y = static_cast<OutT*>(a.y);
+                const int row = un.row0 + m;
+                const bool row_ok = LINEAR ? (row < a.N) : (row < a.T_out);
+
+                if (EPI == kEpiDirect) {
+                    for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
+                        const int co_base = (un.cbu * a.cb_per_unit + cbi) * a.BN;
+                        const int ncols = min(a.BN, a.C_out - co_base);
+                        if (co_base != staged_co) {  // uniform over the epilogue threads
+                            named_bar_sync(1, kEpiT);
+                            for (int col = er; col < a.BN; col += kEpiT)
+                                s_bias[col] = (a.bias && col < ncols) ? __ldg(a.bias + co_base + col) : 0.f;
+                            named_bar_sync(1, kEpiT);
+                            staged_co = co_base;
+                        }
+                        const uint32_t tb =
+                            tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * (ab * a.cb_per_unit + cbi));
+                        for (int j0 = 0; j0 < ncols; j0 += 16) {
+                            float v[16];
+                            tmem_load16(tb + uint32_t(j0), v);
+                            {
+                                float bb[16];
+                                lds_vec(s_bias + j0, bb);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) v[i] += bb[i];
+                            }
+                            if (a.gelu) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
+                            }
+                            if (!row_ok) continue;
+                            if (LINEAR) {
+                                OutT* dst = y + (long long)row * a.C_out + co_base + j0;
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    if (j0 + i < ncols) store_out(dst + i, v[i]);
+                            } else {
+                                OutT* dst = y + ((long long)un.n * a.C_out + co_base + j0) * a.T_out + row;
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    if (j0 + i < ncols) store_out(dst + (long long)i * a.T_out, v[i]);
                             }
                         }
                     }
-                    // Make the generic-proxy stores visible to the tensor core, then signal.
-                    fence_async_shared();
-                    __syncwarp();
-                    if (lane == 0) {
-                        arrive_leader(i_afull + ai);
-                        mbar_arrive(bar(i_sempty + si));
-                    }
-                    if (threadIdx.x == kXp0 * 32) prog[3] = prog[3] + 1;
-                    if (++ai == SA) { ai = 0; aph ^= 1; }
-                    if (++si == SS) { si = 0; sph ^= 1; }
-                }
-            }
-        xp_done:;
-        }
-    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiW) {
-        // ---------------------------------------------------------------- epilogue warps 2..(2+kEpiW-1)
-        const int q = warp & 3;       // TMEM lane quarter this warp may access
-        const int m = q * 32 + lane;  // tile row: time step (conv) or sample row (Linear)
-        const int er = threadIdx.x - kWarpEpi0 * 32;  // index among the epilogue threads
-        const int eg = (warp - kWarpEpi0) >> 2;       // column range (two warps per quarter)
-        bool mid_sync_done = false;
-        // Per-channel parameters of the current channel block, staged once in shared memory so the
-        // element loops below read them with conflict-free broadcast loads instead of global loads.
-        float* s_bias = epi + 3072;  // [256]
-        int staged_co = -1;
-        int obuf = 0;  // LayerNorm output staging: which of this warp's two tiles is next
-        if (kFusedGN && first_unit < a.n_units) {
-            // One unit per CTA: stage bias, gamma and beta of its channel block while the
-            // mainloop runs (gamma and beta go where the column scale / shift end up).
-            const int co_base = decode(first_unit).cbu * a.BN;
-            const int ncols = min(a.BN, a.C_out - co_base);
-            for (int col = er; col < 256; col += kEpiT) {
-                const bool ok = col < ncols;
-                s_bias[col] = (ok && a.bias) ? __ldg(a.bias + co_base + col) : 0.f;
-                epi[2304 + col] = ok ? (a.gamma ? __ldg(a.gamma + co_base + col) : 1.f) : 0.f;
-                epi[2560 + col] = (ok && a.beta) ? __ldg(a.beta + co_base + col) : 0.f;
-            }
-            named_bar_sync(1, kEpiT);
-        }
-        int lt = 0;
-        for (int u = first_unit; u < a.n_units; u += unit_step, ++lt) {
-            const int ab = a.n_acc == 2 ? (lt & 1) : 0;
-            const uint32_t acc_par = a.n_acc == 2 ? uint32_t((lt >> 1) & 1) : uint32_t(lt & 1);
-            if (er == 0) prog[7] = kWaitAccFull;
-            // One lane per warp waits; the shuffle reconverges the warp (the TMEM loads below are
-            // warp-collective), and the barrier ORs what every epilogue thread saw, so all four
-            // warps leave (or stay) together.
-            int got = 0;
-            if (lane == 0) got = wait_bar(i_accfull + ab, acc_par, kWaitAccFull);
-            got = __shfl_sync(0xffffffffu, got, 0);
-            if (named_bar_any(1, kEpiT, !got || *abort_flag != 0)) break;
-            __syncwarp();
-            if (er == 0) prog[7] = 0;
-            tc_fence_after();
-            const Unit un = decode(u);
-            OutT* y = static_cast<OutT*>(a.y);
-            const int row = un.row0 + m;
-            const bool row_ok = LINEAR ? (row < a.N) : (row < a.T_out);
-
-            if (EPI == kEpiDirect) {
-                for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
-                    const int co_base = (un.cbu * a.cb_per_unit + cbi) * a.BN;
+                } else if (EPI == kEpiRowGN) {
+                    // ------------------------------------------------ row epilogue (Linear mode)
+                    // One thread owns one row (sample) and the channel block's columns: bias, optional
+                    // GroupNorm over runs of row_cpg channels, affine, then either GELU + store or a
+                    // running minimum (lowest channel on ties) for the row-min post-op.
+                    const int co_base = un.cbu * a.BN;
                     const int ncols = min(a.BN, a.C_out - co_base);
+                    float* s_gamma = epi + 2304;
+                    float* s_beta = epi + 2560;
                     if (co_base != staged_co) {  // uniform over the epilogue threads
                         named_bar_sync(1, kEpiT);
-                        for (int col = er; col < a.BN; col += kEpiT)
-                            s_bias[col] = (a.bias && col < ncols) ? __ldg(a.bias + co_base + col) : 0.f;
+                        for (int col = er; col < 256; col += kEpiT) {
+                            const bool ok = col < ncols;
+                            s_bias[col] = (ok && a.bias) ? __ldg(a.bias + co_base + col) : 0.f;
+                            s_gamma[col] = ok ? (a.gamma ? __ldg(a.gamma + co_base + col) : 1.f) : 0.f;
+                            s_beta[col] = (ok && a.beta) ? __ldg(a.beta + co_base + col) : 0.f;
+                        }
                         named_bar_sync(1, kEpiT);
                         staged_co = co_base;
                     }
-                    const uint32_t tb =
-                        tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * (ab * a.cb_per_unit + cbi));
-                    for (int j0 = 0; j0 < ncols; j0 += 16) {
-                        float v[16];
-                        tmem_load16(tb + uint32_t(j0), v);
+                    const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
+                    float best = __int_as_float(0x7f800000);
+                    int best_i = 0x7fffffff;
+                    OutT* dst = y + (long long)(row_ok ? row : 0) * a.C_out + co_base;
+                    for (int j0 = 0; j0 < ncols; j0 += 32) {
+                        float v[32];
+                        tmem_load32(tb + uint32_t(j0), v);
                         {
-                            float bb[16];
+                            float bb[32];
                             lds_vec(s_bias + j0, bb);
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] += bb[i];
+                            for (int i = 0; i < 32; ++i) v[i] += bb[i];
                         }
-                        if (a.gelu) {
+                        if (a.row_cpg == 8) row_group_norm<8>(v, s_gamma + j0, s_beta + j0, a.eps);
+                        else if (a.row_cpg == 16) row_group_norm<16>(v, s_gamma + j0, s_beta + j0, a.eps);
+                        else if (a.row_cpg == 32) row_group_norm<32>(v, s_gamma + j0, s_beta + j0, a.eps);
+                        if (a.rowmin) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
-                        }
-                        if (!row_ok) continue;
-                        if (LINEAR) {
-                            OutT* dst = y + (long long)row * a.C_out + co_base + j0;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (j0 + i < ncols) store_out(dst + i, v[i]);
+                            for (int i = 0; i < 32; ++i)
+                                if (j0 + i < ncols && v[i] < best) { best = v[i]; best_i = co_base + j0 + i; }
                         } else {
+                            if (a.gelu) {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+                            }
+                            if (row_ok) {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    if (j0 + i < ncols) store_out(dst + j0 + i, v[i]);
+                            }
+                        }
+                    }
+                    if (a.rowmin && row_ok)
+                        a.rowpart[(size_t)row * a.n_cb + un.cbu] = make_float2(best, __int_as_float(best_i));
+                } else if (EPI == kEpiLN || EPI == kEpiLNX) {
+                    // ------------------------------------------------ channel LayerNorm (conv mode)
+                    // One thread owns one time step. kEpiLN: this CTA holds every channel of the tile.
+                    // kEpiLNX: it holds channels [crank*BN, crank*BN + BN) and its cluster peer the rest
+                    // of the same 128 steps. With bf16 data two epilogue warps share each TMEM lane
+                    // quarter and split the channels in two column ranges. Statistics: one pass of sums
+                    // shifted by the range's first value gives each range's mean and M2; the ranges of
+                    // a CTA are merged through shared memory, the CTA halves of kEpiLNX through
+                    // distributed shared memory (remote stores + a remote arrival), all with Chan's
+                    // formula in a fixed order, so every thread of both CTAs computes the same mean and
+                    // variance. Then normalize + affine (+ GELU), staged per warp as [32 channels][32
+                    // steps] tiles in shared memory and written by TMA bulk stores (or direct stores
+                    // when y's layout does not allow TMA).
+                    float* s_bias = epi;
+                    float* s_gamma = epi + 256;
+                    float* s_beta = epi + 512;
+                    float* xbuf = epi + 768 + 256 * (lt & 1);  // [2 tiles][2][128]: the peer's mean and M2
+                    float* hst = epi + 1280 + 512 * (lt & 1);  // [2 tiles][2 ranges][128][2]: range statistics
+                    const int co_base = un.cbu * a.BN;
+                    const int ncols = min(a.BN, a.C_out - co_base);
+                    if (staged_co < 0) {
+                        for (int c = er; c < 256; c += kEpiT) {
+                            const bool ok = c < ncols;
+                            s_bias[c] = (ok && a.bias) ? __ldg(a.bias + co_base + c) : 0.f;
+                            s_gamma[c] = ok ? (a.gamma ? __ldg(a.gamma + co_base + c) : 1.f) : 0.f;
+                            s_beta[c] = (ok && a.beta) ? __ldg(a.beta + co_base + c) : 0.f;
+                        }
+                        named_bar_sync(1, kEpiT);
+                        staged_co = co_base;
+                    }
+                    // this warp's column range [c_lo, c_hi) (whole 32-column chunks but the last)
+                    const int half = kEpiW == 8 ? ((ncols + 63) / 64) * 32 : ncols;
+                    const int c_lo = eg == 0 ? 0 : min(half, ncols);
+                    const int c_hi = eg == 0 ? min(half, ncols) : ncols;
+                    const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
+                    float shift = 0.f, s1 = 0.f, s2 = 0.f;
+                    for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
+                        float v[32];
+                        tmem_load32(tb + uint32_t(j0), v);
+                        float bb[32];
+                        lds_vec(s_bias + j0, bb);
+                        if (j0 == c_lo) shift = v[0] + bb[0];
+                        if (j0 + 32 <= c_hi) {  // whole chunk (uniform): no per-column test
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const float d = v[i] + bb[i] - shift;
+                                s1 += d;
+                                s2 = fmaf(d, d, s2);
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (j0 + i < c_hi) {
+                                    const float d = v[i] + bb[i] - shift;
+                                    s1 += d;
+                                    s2 = fmaf(d, d, s2);
+                                }
+                        }
+                    }
+                    const float n_own = float(c_hi - c_lo);
+                    float mean = n_own > 0.f ? shift + s1 / n_own : 0.f;
+                    float m2 = n_own > 0.f ? fmaxf(s2 - s1 * (s1 / n_own), 0.f) : 0.f;
+                    float n_cta = n_own;
+                    if constexpr (kEpiW == 8) {
+                        // the two column ranges of this CTA, merged in range order
+                        hst[(eg * 128 + m) * 2] = mean;
+                        hst[(eg * 128 + m) * 2 + 1] = m2;
+                        named_bar_sync(1, kEpiT);
+                        float n0 = float(min(half, ncols)), mu0 = hst[m * 2], m20 = hst[m * 2 + 1];
+                        chan_merge(n0, mu0, m20, float(ncols) - float(min(half, ncols)), hst[(128 + m) * 2],
+                                   hst[(128 + m) * 2 + 1]);
+                        mean = mu0;
+                        m2 = m20;
+                        n_cta = n0;
+                    }
+                    if constexpr (kClusterX) {
+                        const uint32_t peer = crank ^ 1u;
+                        if (eg == 0) {
+                            st_shared_cluster_f32(map_shared_rank(smem_u32(xbuf + m), peer), mean);
+                            st_shared_cluster_f32(map_shared_rank(smem_u32(xbuf + 128 + m), peer), m2);
+                            mbar_arrive_cluster(map_shared_rank(bar(i_ex), peer));
+                        }
+                        mbar_wait_cluster(bar(i_ex), uint32_t(lt & 1), abort_flag, a.status, kWaitExchange, prog);
+                        const float n_peer = float(a.C_out - ncols);
+                        const float p_mean = xbuf[m], p_m2 = xbuf[128 + m];
+                        // Chan's merge of (rank 0 half, rank 1 half)
+                        const float na = crank == 0 ? n_cta : n_peer, nb = crank == 0 ? n_peer : n_cta;
+                        const float ma = crank == 0 ? mean : p_mean, mb = crank == 0 ? p_mean : mean;
+                        const float Ma = crank == 0 ? m2 : p_m2, Mb = crank == 0 ? p_m2 : m2;
+                        const float nt = na + nb, dlt = mb - ma;
+                        mean = ma + dlt * (nb / nt);
+                        m2 = Ma + Mb + dlt * dlt * (na * (nb / nt));
+                    }
+                    const float rstd = rsqrtf(m2 / float(a.C_out) + a.eps);
+                    if (a.tma_store) {
+                        OutT* ostage = reinterpret_cast<OutT*>(base + a.o_off) + (warp - kWarpEpi0) * (2 * 32 * 32);
+                        for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
+                            float v[32];
+                            tmem_load32(tb + uint32_t(j0), v);
+#pragma unroll
+                            for (int h = 0; h < 32; h += 16) {
+                                float bb[16], gg[16], be[16];
+                                lds_vec(s_bias + j0 + h, bb);
+                                lds_vec(s_gamma + j0 + h, gg);
+                                lds_vec(s_beta + j0 + h, be);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    v[h + i] = fmaf((v[h + i] + (bb[i] - mean)) * rstd, gg[i], be[i]);
+                            }
+                            if (a.gelu) {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+                            }
+                            // the store issued from this buffer two chunks ago has read it
+                            if (lane == 0) tma_store_wait_read_le1();
+                            __syncwarp();
+                            OutT* ob = ostage + obuf * (32 * 32);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) store_out(ob + i * 32 + lane, v[i]);
+                            fence_async_shared();
+                            __syncwarp();
+                            if (lane == 0)
+                                tma_store_3d(&tm_y, smem_u32(ob), un.row0 + q * 32, co_base + j0, un.n);
+                            obuf ^= 1;
+                        }
+                    } else {
+                        OutT* dst = y + ((long long)un.n * a.C_out + co_base) * a.T_out + row;
+                        for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
+                            float v[32];
+                            tmem_load32(tb + uint32_t(j0), v);
+#pragma unroll
+                            for (int h = 0; h < 32; h += 16) {
+                                float bb[16], gg[16], be[16];
+                                lds_vec(s_bias + j0 + h, bb);
+                                lds_vec(s_gamma + j0 + h, gg);
+                                lds_vec(s_beta + j0 + h, be);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    v[h + i] = fmaf((v[h + i] + (bb[i] - mean)) * rstd, gg[i], be[i]);
+                            }
+                            if (a.gelu) {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+                            }
+                            if (row_ok) {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    if (j0 + i < c_hi) store_out(dst + (long long)(j0 + i) * a.T_out, v[i]);
+                            }
+                        }
+                    }
+                } else {
+                    // ------------------------------------------------ fused GroupNorm (conv mode)
+                    // The CTAs of one (sample, channel block) together cover all T_out steps. Each
+                    // reduces per-group partial statistics over its tile, the partials are exchanged
+                    // (distributed shared memory inside a cluster, or global memory across a
+                    // cooperative grid) and merged with Chan's formula, and each CTA normalizes its
+                    // tile from TMEM and stores it once.
+                    const int co_base = un.cbu * a.BN;
+                    const int ncols = min(a.BN, a.C_out - co_base);
+                    const int cpg = a.cpg;
+                    const int ngroups = (ncols + cpg - 1) / cpg;
+                    const int nvalid_t = min(128, a.T_out - un.row0);
+                    const int tt = un.row0 / 128;
+                    // this warp's column range [c_lo, c_hi): the two warps of a lane quarter take one
+                    // half each (whole 32-column chunks but the last)
+                    const int half = ((ncols + 63) / 64) * 32;
+                    const int c_lo = eg == 0 ? 0 : min(half, ncols);
+                    const int c_hi = eg == 0 ? min(half, ncols) : ncols;
+                    // grid exchange: per (sample, channel block, time tile, group) two 64-bit words,
+                    // (mean | epoch) and (M2 | epoch). All words of a (sample, channel block) carry the
+                    // same epoch, one step per launch (the weight pack zeroes them), so this launch's
+                    // epoch is one past the one in this CTA's own word, read now so the load overlaps
+                    // the statistics pass.
+                    const size_t slot0 = size_t(un.n * a.n_cb + un.cbu) * a.n_t_tiles;
+                    unsigned long long* gx_me = a.gx + (slot0 + tt) * size_t(a.gstride) * 2;
+                    unsigned target = 0;
+                    if (EPI == kEpiGridGN) target = unsigned(ld_relaxed_gpu_u64(gx_me) >> 32) + 1u;
+                    float* red_s = epi;            // [4][256] per-warp run sums
+                    float* red_m = epi + 1024;     // [4][256] per-warp run M2
+                    float* part_mu = epi + 2048;   // [256] this CTA's group means (cluster exchange)
+                    float* colscale = epi + 2304;  // [256]
+                    float* colshift = epi + 2560;  // [256]
+                    float* gmean = epi + 2816;     // [256] group mean over all CTAs
+                    float* grstd = epi + 3328;     // [256] group 1/sqrt(var + eps)
+                    float* part_m2 = epi + 3584;   // [256] this CTA's group M2 (cluster exchange)
+                    const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
+                    // one pass over TMEM: sum and M2 of y = acc + bias per run of `sub` channels of each
+                    // row, merged over the warp's rows with Chan's formula
+                    const int nvalid_w = min(32, max(0, nvalid_t - q * 32));
+                    gn_run_stats_any(a.sub, tb, c_lo, c_hi, lane < nvalid_w, s_bias, red_s, red_m, q, lane);
+                    named_bar_sync(1, kEpiT);
+                    const int run = a.sub > 0 ? a.sub : 1;
+                    for (int g = er; g < ngroups; g += kEpiT) {
+                        // this CTA's part of group g: merge its runs over the four warps
+                        const int c0 = g * cpg, c_end = min(ncols, c0 + cpg);
+                        float gn = 0.f, gs = 0.f, gm2 = 0.f;
+                        for (int q2 = 0; q2 < 4; ++q2) {
+                            const float nq = float(min(32, max(0, nvalid_t - q2 * 32)) * run);
+                            if (nq <= 0.f) continue;
+                            for (int j = c0 / run; j < (c_end + run - 1) / run; ++j)
+                                chan_merge_sum(gn, gs, gm2, nq, red_s[q2 * 256 + j], red_m[q2 * 256 + j]);
+                        }
+                        const float mu = gs / gn;
+                        if (EPI == kEpiGridGN) {
+                            const unsigned long long tag = (unsigned long long)target << 32;
+                            st_relaxed_gpu_u64(gx_me + 2 * g, tag | __float_as_uint(mu));
+                            st_relaxed_gpu_u64(gx_me + 2 * g + 1, tag | __float_as_uint(gm2));
+                        } else {
+                            part_mu[g] = mu;
+                            part_m2[g] = gm2;
+                        }
+                    }
+                    if (EPI == kEpiClusterGN) {
+                        // partials of every CTA in the cluster become visible
+                        cluster_sync_all();
+                        mid_sync_done = true;
+                        for (int g = er; g < ngroups; g += kEpiT) {
+                            const float cw = float(min(ncols, g * cpg + cpg) - g * cpg);
+                            float gn = 0.f, gmu = 0.f, gm2 = 0.f;
+                            const uint32_t pmu = smem_u32(part_mu + g), pm2 = smem_u32(part_m2 + g);
+                            for (int rk = 0; rk < a.n_t_tiles; ++rk) {
+                                const float cnt = cw * float(min(128, a.T_out - rk * 128));
+                                chan_merge(gn, gmu, gm2, cnt, ld_shared_cluster_f32(map_shared_rank(pmu, uint32_t(rk))),
+                                           ld_shared_cluster_f32(map_shared_rank(pm2, uint32_t(rk))));
+                            }
+                            gmean[g] = gmu;
+                            grstd[g] = rsqrtf((gn > 0.f ? gm2 / gn : 0.f) + a.eps);
+                        }
+                    } else {
+                        // Every thread waits (bounded) for its groups' words from all peers: each word
+                        // carries its value and the epoch in one 64-bit access, so a word that shows this
+                        // launch's epoch holds this launch's value, with no fence on either side.
+                        const unsigned long long* gq = a.gx + slot0 * size_t(a.gstride) * 2;
+                        const size_t tile_words = size_t(a.gstride) * 2;
+                        for (int g = er; g < ngroups; g += kEpiT) {
+                            const float cw = float(min(ncols, g * cpg + cpg) - g * cpg);
+                            float gn = 0.f, gmu = 0.f, gm2 = 0.f;
+                            const uint64_t t0 = global_timer_ns();
+                            constexpr int kPollBatch = 4;  // peers whose words are in flight together
+                            for (int base_rk = 0; base_rk < a.n_t_tiles; base_rk += kPollBatch) {
+                                const int nrk = min(kPollBatch, a.n_t_tiles - base_rk);
+                                unsigned long long wmu[kPollBatch], wm2[kPollBatch];
+                                for (;;) {
+                                    bool all = true;
+#pragma unroll
+                                    for (int r = 0; r < kPollBatch; ++r) {
+                                        if (r < nrk) {
+                                            const unsigned long long* w = gq + size_t(base_rk + r) * tile_words + 2 * g;
+                                            wmu[r] = ld_relaxed_gpu_u64(w);
+                                            wm2[r] = ld_relaxed_gpu_u64(w + 1);
+                                            all &= unsigned(wmu[r] >> 32) == target && unsigned(wm2[r] >> 32) == target;
+                                        }
+                                    }
+                                    if (all || *abort_flag) break;
+                                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                                        if (atomicCAS(a.status, 0, 6) == 0) {
+                                            atomicExch(a.status + 1, kWaitGridPeers);
+                                            atomicExch(a.status + 2, int(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)));
+                                        }
+                                        *abort_flag = 1;
+                                        break;
+                                    }
+                                }
+#pragma unroll
+                                for (int r = 0; r < kPollBatch; ++r) {
+                                    if (r < nrk) {
+                                        const float cnt = cw * float(min(128, a.T_out - (base_rk + r) * 128));
+                                        chan_merge(gn, gmu, gm2, cnt, __uint_as_float(unsigned(wmu[r])),
+                                                   __uint_as_float(unsigned(wm2[r])));
+                                    }
+                                }
+                            }
+                            gmean[g] = gmu;
+                            grstd[g] = rsqrtf((gn > 0.f ? gm2 / gn : 0.f) + a.eps);
+                        }
+                    }
+                    named_bar_sync(1, kEpiT);
+                    for (int col = er; col < 256; col += kEpiT) {
+                        // colscale / colshift hold gamma / beta (staged before the mainloop)
+                        float sc = 0.f, sh = 0.f;
+                        if (col < ncols) {
+                            const int g = col / cpg;
+                            sc = grstd[g] * colscale[col];
+                            sh = colshift[col] + (s_bias[col] - gmean[g]) * sc;
+                        }
+                        colscale[col] = sc;
+                        colshift[col] = sh;
+                    }
+                    named_bar_sync(1, kEpiT);
+                    // normalize from TMEM; store once
+                    if (a.tma_store) {
+                        // Each warp stages its 32 time steps of every 32-channel chunk of its column range
+                        // as a [32 ch][32 t] tile in the operand rings (idle now that the tile's MMAs are
+                        // done) and sends it with a bulk store as soon as it is staged (rows past T_out
+                        // and channels past C_out are clipped). Before the CTA leaves, the stores only
+                        // have to finish reading shared memory.
+                        const int nch = (a.BN + 31) / 32;
+                        OutT* so = reinterpret_cast<OutT*>(base + size_t(SA) * a.a_slot_bytes) + q * (nch * 32 * 32);
+                        for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
+                            float v[32];
+                            tmem_load32(tb + uint32_t(j0), v);
+                            OutT* ob = so + (j0 / 32) * (32 * 32);
+#pragma unroll
+                            for (int h = 0; h < 32; h += 8) {
+                                float sc[8], sh[8];
+                                lds_vec(colscale + j0 + h, sc);
+                                lds_vec(colshift + j0 + h, sh);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    float o = fmaf(v[h + i], sc[i], sh[i]);
+                                    if (a.gelu) o = gelu_erf(o);
+                                    store_out(ob + (h + i) * 32 + lane, o);
+                                }
+                            }
+                            fence_async_shared();
+                            __syncwarp();
+                            if (lane == 0) tma_store_3d(&tm_y, smem_u32(ob), un.row0 + q * 32, co_base + j0, un.n);
+                        }
+                        if (lane == 0) tma_store_wait_read();
+                        __syncwarp();
+                    } else {
+                        for (int j0 = c_lo; j0 < c_hi; j0 += 16) {
+                            float v[16];
+                            tmem_load16(tb + uint32_t(j0), v);
+                            {
+                                float sc[16], sh[16];
+                                lds_vec(colscale + j0, sc);
+                                lds_vec(colshift + j0, sh);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) v[i] = fmaf(v[i], sc[i], sh[i]);
+                            }
+                            if (a.gelu) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
+                            }
+                            if (!row_ok) continue;
                             OutT* dst = y + ((long long)un.n * a.C_out + co_base + j0) * a.T_out + row;
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
@@ -769,406 +1246,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-            } else if (EPI == kEpiRowGN) {
-                // ------------------------------------------------ row epilogue (Linear mode)
-                // One thread owns one row (sample) and the channel block's columns: bias, optional
-                // GroupNorm over runs of row_cpg channels, affine, then either GELU + store or a
-                // running minimum (lowest channel on ties) for the row-min post-op.
-                const int co_base = un.cbu * a.BN;
-                const int ncols = min(a.BN, a.C_out - co_base);
-                float* s_gamma = epi + 2304;
-                float* s_beta = epi + 2560;
-                if (co_base != staged_co) {  // uniform over the epilogue threads
-                    named_bar_sync(1, kEpiT);
-                    for (int col = er; col < 256; col += kEpiT) {
-                        const bool ok = col < ncols;
-                        s_bias[col] = (ok && a.bias) ? __ldg(a.bias + co_base + col) : 0.f;
-                        s_gamma[col] = ok ? (a.gamma ? __ldg(a.gamma + co_base + col) : 1.f) : 0.f;
-                        s_beta[col] = (ok && a.beta) ? __ldg(a.beta + co_base + col) : 0.f;
-                    }
-                    named_bar_sync(1, kEpiT);
-                    staged_co = co_base;
-                }
-                const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
-                float best = __int_as_float(0x7f800000);
-                int best_i = 0x7fffffff;
-                OutT* dst = y + (long long)(row_ok ? row : 0) * a.C_out + co_base;
-                for (int j0 = 0; j0 < ncols; j0 += 32) {
-                    float v[32];
-                    tmem_load32(tb + uint32_t(j0), v);
-                    {
-                        float bb[32];
-                        lds_vec(s_bias + j0, bb);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] += bb[i];
-                    }
-                    if (a.row_cpg == 8) row_group_norm<8>(v, s_gamma + j0, s_beta + j0, a.eps);
-                    else if (a.row_cpg == 16) row_group_norm<16>(v, s_gamma + j0, s_beta + j0, a.eps);
-                    else if (a.row_cpg == 32) row_group_norm<32>(v, s_gamma + j0, s_beta + j0, a.eps);
-                    if (a.rowmin) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (j0 + i < ncols && v[i] < best) { best = v[i]; best_i = co_base + j0 + i; }
-                    } else {
-                        if (a.gelu) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-                        }
-                        if (row_ok) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (j0 + i < ncols) store_out(dst + j0 + i, v[i]);
-                        }
-                    }
-                }
-                if (a.rowmin && row_ok)
-                    a.rowpart[(size_t)row * a.n_cb + un.cbu] = make_float2(best, __int_as_float(best_i));
-            } else if (EPI == kEpiLN || EPI == kEpiLNX) {
-                // ------------------------------------------------ channel LayerNorm (conv mode)
-                // One thread owns one time step. kEpiLN: this CTA holds every channel of the tile.
-                // kEpiLNX: it holds channels [crank*BN, crank*BN + BN) and its cluster peer the rest
-                // of the same 128 steps. With bf16 data two epilogue warps share each TMEM lane
-                // quarter and split the channels in two column ranges. Statistics: one pass of sums
-                // shifted by the range's first value gives each range's mean and M2; the ranges of
-                // a CTA are merged through shared memory, the CTA halves of kEpiLNX through
-                // distributed shared memory (remote stores + a remote arrival), all with Chan's
-                // formula in a fixed order, so every thread of both CTAs computes the same mean and
-                // variance. Then normalize + affine (+ GELU), staged per warp as [32 channels][32
-                // steps] tiles in shared memory and written by TMA bulk stores (or direct stores
-                // when y's layout does not allow TMA).
-                float* s_bias = epi;
-                float* s_gamma = epi + 256;
-                float* s_beta = epi + 512;
-                float* xbuf = epi + 768 + 256 * (lt & 1);  // [2 tiles][2][128]: the peer's mean and M2
-                float* hst = epi + 1280 + 512 * (lt & 1);  // [2 tiles][2 ranges][128][2]: range statistics
-                const int co_base = un.cbu * a.BN;
-                const int ncols = min(a.BN, a.C_out - co_base);
-                if (staged_co < 0) {
-                    for (int c = er; c < 256; c += kEpiT) {
-                        const bool ok = c < ncols;
-                        s_bias[c] = (ok && a.bias) ? __ldg(a.bias + co_base + c) : 0.f;
-                        s_gamma[c] = ok ? (a.gamma ? __ldg(a.gamma + co_base + c) : 1.f) : 0.f;
-                        s_beta[c] = (ok && a.beta) ? __ldg(a.beta + co_base + c) : 0.f;
-                    }
-                    named_bar_sync(1, kEpiT);
-                    staged_co = co_base;
-                }
-                // this warp's column range [c_lo, c_hi) (whole 32-column chunks but the last)
-                const int half = kEpiW == 8 ? ((ncols + 63) / 64) * 32 : ncols;
-                const int c_lo = eg == 0 ? 0 : min(half, ncols);
-                const int c_hi = eg == 0 ? min(half, ncols) : ncols;
-                const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
-                float shift = 0.f, s1 = 0.f, s2 = 0.f;
-                for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
-                    float v[32];
-                    tmem_load32(tb + uint32_t(j0), v);
-                    float bb[32];
-                    lds_vec(s_bias + j0, bb);
-                    if (j0 == c_lo) shift = v[0] + bb[0];
-                    if (j0 + 32 <= c_hi) {  // whole chunk (uniform): no per-column test
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float d = v[i] + bb[i] - shift;
-                            s1 += d;
-                            s2 = fmaf(d, d, s2);
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (j0 + i < c_hi) {
-                                const float d = v[i] + bb[i] - shift;
-                                s1 += d;
-                                s2 = fmaf(d, d, s2);
-                            }
-                    }
-                }
-                const float n_own = float(c_hi - c_lo);
-                float mean = n_own > 0.f ? shift + s1 / n_own : 0.f;
-                float m2 = n_own > 0.f ? fmaxf(s2 - s1 * (s1 / n_own), 0.f) : 0.f;
-                float n_cta = n_own;
-                if constexpr (kEpiW == 8) {
-                    // the two column ranges of this CTA, merged in range order
-                    hst[(eg * 128 + m) * 2] = mean;
-                    hst[(eg * 128 + m) * 2 + 1] = m2;
-                    named_bar_sync(1, kEpiT);
-                    float n0 = float(min(half, ncols)), mu0 = hst[m * 2], m20 = hst[m * 2 + 1];
-                    chan_merge(n0, mu0, m20, float(ncols) - float(min(half, ncols)), hst[(128 + m) * 2],
-                               hst[(128 + m) * 2 + 1]);
-                    mean = mu0;
-                    m2 = m20;
-                    n_cta = n0;
-                }
-                if constexpr (kClusterX) {
-                    const uint32_t peer = crank ^ 1u;
-                    if (eg == 0) {
-                        st_shared_cluster_f32(map_shared_rank(smem_u32(xbuf + m), peer), mean);
-                        st_shared_cluster_f32(map_shared_rank(smem_u32(xbuf + 128 + m), peer), m2);
-                        mbar_arrive_cluster(map_shared_rank(bar(i_ex), peer));
-                    }
-                    mbar_wait_cluster(bar(i_ex), uint32_t(lt & 1), abort_flag, a.status, kWaitExchange, prog);
-                    const float n_peer = float(a.C_out - ncols);
-                    const float p_mean = xbuf[m], p_m2 = xbuf[128 + m];
-                    // Chan's merge of (rank 0 half, rank 1 half)
-                    const float na = crank == 0 ? n_cta : n_peer, nb = crank == 0 ? n_peer : n_cta;
-                    const float ma = crank == 0 ? mean : p_mean, mb = crank == 0 ? p_mean : mean;
-                    const float Ma = crank == 0 ? m2 : p_m2, Mb = crank == 0 ? p_m2 : m2;
-                    const float nt = na + nb, dlt = mb - ma;
-                    mean = ma + dlt * (nb / nt);
-                    m2 = Ma + Mb + dlt * dlt * (na * (nb / nt));
-                }
-                const float rstd = rsqrtf(m2 / float(a.C_out) + a.eps);
-                if (a.tma_store) {
-                    OutT* ostage = reinterpret_cast<OutT*>(base + a.o_off) + (warp - kWarpEpi0) * (2 * 32 * 32);
-                    for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
-                        float v[32];
-                        tmem_load32(tb + uint32_t(j0), v);
-#pragma unroll
-                        for (int h = 0; h < 32; h += 16) {
-                            float bb[16], gg[16], be[16];
-                            lds_vec(s_bias + j0 + h, bb);
-                            lds_vec(s_gamma + j0 + h, gg);
-                            lds_vec(s_beta + j0 + h, be);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                v[h + i] = fmaf((v[h + i] + (bb[i] - mean)) * rstd, gg[i], be[i]);
-                        }
-                        if (a.gelu) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-                        }
-                        // the store issued from this buffer two chunks ago has read it
-                        if (lane == 0) tma_store_wait_read_le1();
-                        __syncwarp();
-                        OutT* ob = ostage + obuf * (32 * 32);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) store_out(ob + i * 32 + lane, v[i]);
-                        fence_async_shared();
-                        __syncwarp();
-                        if (lane == 0)
-                            tma_store_3d(&tm_y, smem_u32(ob), un.row0 + q * 32, co_base + j0, un.n);
-                        obuf ^= 1;
-                    }
-                } else {
-                    OutT* dst = y + ((long long)un.n * a.C_out + co_base) * a.T_out + row;
-                    for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
-                        float v[32];
-                        tmem_load32(tb + uint32_t(j0), v);
-#pragma unroll
-                        for (int h = 0; h < 32; h += 16) {
-                            float bb[16], gg[16], be[16];
-                            lds_vec(s_bias + j0 + h, bb);
-                            lds_vec(s_gamma + j0 + h, gg);
-                            lds_vec(s_beta + j0 + h, be);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                v[h + i] = fmaf((v[h + i] + (bb[i] - mean)) * rstd, gg[i], be[i]);
-                        }
-                        if (a.gelu) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-                        }
-                        if (row_ok) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (j0 + i < c_hi) store_out(dst + (long long)(j0 + i) * a.T_out, v[i]);
-                        }
-                    }
-                }
-            } else {
-                // ------------------------------------------------ fused GroupNorm (conv mode)
-                // The CTAs of one (sample, channel block) together cover all T_out steps. Each
-                // reduces per-group partial statistics over its tile, the partials are exchanged
-                // (distributed shared memory inside a cluster, or global memory across a
-                // cooperative grid) and merged with Chan's formula, and each CTA normalizes its
-                // tile from TMEM and stores it once.
-                const int co_base = un.cbu * a.BN;
-                const int ncols = min(a.BN, a.C_out - co_base);
-                const int cpg = a.cpg;
-                // the exchange epoch: this CTA's own flag, read now so the load overlaps the passes
-                unsigned gn_epoch = 0;
-                if (EPI == kEpiGridGN)
-                    gn_epoch = *reinterpret_cast<volatile unsigned*>(
-                        a.gsync + (size_t(un.n * a.n_cb + un.cbu) * a.n_t_tiles + un.row0 / 128) * 256);
-                const int ngroups = (ncols + cpg - 1) / cpg;
-                const int nvalid_t = min(128, a.T_out - un.row0);
-                const int tt = un.row0 / 128;
-                float* red = epi;              // [4][256] per-warp partial sums
-                float* colsum = epi + 1024;    // [256]
-                float* gmean = epi + 1280;     // [256] group mean (this CTA, then all CTAs)
-                float* part = epi + 1536;      // [3][256] count, mean, M2 per group of this CTA
-                float* colscale = epi + 2304;  // [256]
-                float* colshift = epi + 2560;  // [256]
-                float* s_shift = epi + 3328;   // [256] group mean - bias, per column
-                const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
-                // pass 0: sums of the raw accumulator; the bias enters at group level as
-                // nvalid_t * sum(bias) -> count and mean of this CTA's part of each group
-                gn_run_sums_any<false>(a.sub, tb, ncols, row_ok, s_shift, red, q, lane);
-                named_bar_sync(1, kEpiT);
-                const int run = a.sub > 0 ? a.sub : 1;
-                for (int g = er; g < ngroups; g += kEpiT) {
-                    const int c0 = g * cpg, c_end = min(ncols, c0 + cpg);
-                    float sum = 0.f, bsum = 0.f;
-                    for (int j = c0 / run; j < (c_end + run - 1) / run; ++j)
-                        sum += red[j] + red[256 + j] + red[512 + j] + red[768 + j];
-                    for (int col = c0; col < c_end; ++col) bsum += s_bias[col];
-                    const float cnt = float((c_end - c0) * nvalid_t);
-                    const float mean = (sum + float(nvalid_t) * bsum) / cnt;
-                    gmean[g] = mean;
-                    part[g] = cnt;
-                    part[256 + g] = mean;
-                }
-                named_bar_sync(1, kEpiT);
-                for (int col = er; col < 256; col += kEpiT)
-                    s_shift[col] = col < ncols ? gmean[col / cpg] - s_bias[col] : 0.f;
-                named_bar_sync(1, kEpiT);
-                // pass 1: squared deviations from this CTA's group mean -> M2
-                gn_run_sums_any<true>(a.sub, tb, ncols, row_ok, s_shift, red, q, lane);
-                named_bar_sync(1, kEpiT);
-                for (int g = er; g < ngroups; g += kEpiT) {
-                    const int c0 = g * cpg, c_end = min(ncols, c0 + cpg);
-                    float sum = 0.f;
-                    for (int j = c0 / run; j < (c_end + run - 1) / run; ++j)
-                        sum += red[j] + red[256 + j] + red[512 + j] + red[768 + j];
-                    part[512 + g] = sum;
-                }
-                named_bar_sync(1, kEpiT);
-                if (EPI == kEpiClusterGN) {
-                    // partials of every CTA in the cluster become visible
-                    cluster_sync_all();
-                    mid_sync_done = true;
-                    for (int g = er; g < ngroups; g += kEpiT) {
-                        float gn = 0.f, gmu = 0.f, gm2 = 0.f;
-                        const uint32_t p0 = smem_u32(part + g);
-                        for (int rk = 0; rk < a.n_t_tiles; ++rk) {
-                            const uint32_t pr = map_shared_rank(p0, uint32_t(rk));
-                            chan_merge(gn, gmu, gm2, ld_shared_cluster_f32(pr), ld_shared_cluster_f32(pr + 1024),
-                                       ld_shared_cluster_f32(pr + 2048));
-                        }
-                        gmean[g] = gmu;
-                        colsum[g] = rsqrtf((gn > 0.f ? gm2 / gn : 0.f) + a.eps);  // group rstd
-                    }
-                } else {
-                    // Publish this CTA's partials, each with a release flag per group; then every
-                    // thread waits (bounded) for its groups' flags from all peers and merges. All
-                    // flags of a (sample, channel block) advance together, one step per launch, so
-                    // this launch's value is one past the CTA's own flag as read before the
-                    // statistics passes (the workspace starts at zero and the weight pack re-zeroes it).
-                    const size_t slot0 = size_t(un.n * a.n_cb + un.cbu) * a.n_t_tiles;
-                    float4* gp = a.gpart + (slot0 + tt) * 256;
-                    const unsigned target = gn_epoch + 1u;
-                    for (int g = er; g < ngroups; g += kEpiT) {
-                        gp[g] = make_float4(part[g], part[256 + g], part[512 + g], 0.f);
-                        st_release_gpu(a.gsync + (slot0 + tt) * 256 + g, target);
-                    }
-                    const float4* gq = a.gpart + slot0 * 256;
-                    for (int g = er; g < ngroups; g += kEpiT) {
-                        float gn = 0.f, gmu = 0.f, gm2 = 0.f;
-                        // all peers' flags of group g, polled together with relaxed loads (up to 16
-                        // tiles per load round), then one acquire fence before their partials are read
-                        const uint64_t t0 = global_timer_ns();
-                        for (int base_rk = 0; base_rk < a.n_t_tiles; base_rk += 16) {
-                            const int nrk = min(16, a.n_t_tiles - base_rk);
-                            for (;;) {
-                                bool all = true;
-#pragma unroll
-                                for (int r = 0; r < 16; ++r)
-                                    if (r < nrk)
-                                        all &= int(ld_relaxed_gpu(a.gsync + (slot0 + base_rk + r) * 256 + g) - target) >= 0;
-                                if (all || *abort_flag) break;
-                                if (global_timer_ns() - t0 > kWaitLimitNs) {
-                                    if (atomicCAS(a.status, 0, 6) == 0) {
-                                        atomicExch(a.status + 1, kWaitGridPeers);
-                                        atomicExch(a.status + 2, int(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)));
-                                    }
-                                    *abort_flag = 1;
-                                    break;
-                                }
-                            }
-                        }
-                        fence_acquire_gpu();
-                        for (int rk = 0; rk < a.n_t_tiles; ++rk) {
-                            const float4 pv = __ldcg(gq + size_t(rk) * 256 + g);
-                            chan_merge(gn, gmu, gm2, pv.x, pv.y, pv.z);
-                        }
-                        gmean[g] = gmu;
-                        colsum[g] = rsqrtf((gn > 0.f ? gm2 / gn : 0.f) + a.eps);  // group rstd
-                    }
-                }
-                named_bar_sync(1, kEpiT);
-                for (int col = er; col < 256; col += kEpiT) {
-                    // colscale / colshift hold gamma / beta (staged before the mainloop)
-                    float sc = 0.f, sh = 0.f;
-                    if (col < ncols) {
-                        const int g = col / cpg;
-                        sc = colsum[g] * colscale[col];
-                        sh = colshift[col] + (s_bias[col] - gmean[g]) * sc;
-                    }
-                    colscale[col] = sc;
-                    colshift[col] = sh;
-                }
-                named_bar_sync(1, kEpiT);
-                // normalize from TMEM; store once
-                if (a.tma_store) {
-                    // Each warp stages its 32 time steps of every 32-channel chunk as a [32 ch][32 t]
-                    // tile in the operand rings (idle now that the tile's MMAs are done) and sends
-                    // it with a TMA bulk store at once, so the stores overlap the staging of the
-                    // next chunks; rows past T_out and channels past C_out are clipped.
-                    const int nch = (a.BN + 31) / 32;
-                    OutT* so = reinterpret_cast<OutT*>(base + size_t(SA) * a.a_slot_bytes) + q * (nch * 32 * 32);
-                    for (int j0 = 0; j0 < ncols; j0 += 32) {
-                        float v[32];
-                        tmem_load32(tb + uint32_t(j0), v);
-#pragma unroll
-                        for (int h = 0; h < 32; h += 16) {
-                            float sc[16], sh[16];
-                            lds_vec(colscale + j0 + h, sc);
-                            lds_vec(colshift + j0 + h, sh);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) v[h + i] = fmaf(v[h + i], sc[i], sh[i]);
-                        }
-                        if (a.gelu) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-                        }
-                        OutT* ob = so + (j0 / 32) * (32 * 32);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) store_out(ob + i * 32 + lane, v[i]);
-                        fence_async_shared();
-                        __syncwarp();
-                        if (lane == 0) tma_store_3d(&tm_y, smem_u32(ob), un.row0 + q * 32, co_base + j0, un.n);
-                    }
-                    if (lane == 0) tma_store_wait_all();  // the staging must outlive the copies
-                    __syncwarp();
-                } else {
-                    for (int j0 = 0; j0 < ncols; j0 += 16) {
-                        float v[16];
-                        tmem_load16(tb + uint32_t(j0), v);
-                        {
-                            float sc[16], sh[16];
-                            lds_vec(colscale + j0, sc);
-                            lds_vec(colshift + j0, sh);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] = fmaf(v[i], sc[i], sh[i]);
-                        }
-                        if (a.gelu) {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
-                        }
-                        if (!row_ok) continue;
-                        OutT* dst = y + ((long long)un.n * a.C_out + co_base + j0) * a.T_out + row;
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (j0 + i < ncols) store_out(dst + (long long)i * a.T_out, v[i]);
-                    }
-                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) arrive_leader(i_accempty + ab);
+                if (threadIdx.x == kWarpEpi0 * 32) prog[4] = lt + 1;
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) arrive_leader(i_accempty + ab);
-            if (threadIdx.x == kWarpEpi0 * 32) prog[4] = lt + 1;
+            if (EPI == kEpiClusterGN && !mid_sync_done) cluster_sync_all();
+            if ((EPI == kEpiLN || EPI == kEpiLNX) && a.tma_store && lane == 0) tma_store_wait_all();
         }
-        if (EPI == kEpiClusterGN && !mid_sync_done) cluster_sync_all();
-        if ((EPI == kEpiLN || EPI == kEpiLNX) && a.tma_store && lane == 0) tma_store_wait_all();
     }
 
     if (EPI == kEpiClusterGN) {
