@@ -58,9 +58,6 @@ enum WaitSite {
 };
 
 
-__device__ __forceinline__ float load_in(const float* p) { return __ldg(p); }
-__device__ __forceinline__ float load_in(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-
 __device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
@@ -100,95 +97,91 @@ __device__ __forceinline__ void chan_merge(float& n_a, float& mu_a, float& m2_a,
     n_a = n;
 }
 
-// Chan's merge in (count, sum, M2) form: (n_a, s_a, m2_a) absorbs (n_b, s_b, m2_b).
-__device__ __forceinline__ void chan_merge_sum(float& n_a, float& s_a, float& m2_a, float n_b, float s_b, float m2_b) {
-    const float n = n_a + n_b;
-    const float den = n_a * n_b * n;
-    const float t = n_b * s_a - n_a * s_b;  // n_a * n_b * (mean_a - mean_b)
-    m2_a += m2_b + (den > 0.f ? t * t / den : 0.f);
-    s_a += s_b;
-    n_a = n;
+// Packed pairs of fp32 (Blackwell's paired fp32 add / sub / fma): lo in the low word.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float f2_hsum(uint64_t p) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
+    return lo + hi;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
 }
 
-// One level (lane distance d) of a butterfly reduce-scatter of (sum, M2) partials merged with
-// Chan's formula, for the slot pair (lo, lo + d): the lower lane of each lane pair keeps slot lo,
-// the upper one slot lo + d, each merged with its partner's copy. n / np: values behind this lane's
-// / the partner's partials; r = 1 / (n * np * (n + np)) (0 when either count is 0).
-__device__ __forceinline__ void chan_level(float& s_lo, float& m_lo, float s_hi, float m_hi, float n, float np,
-                                           float r, bool upper, int d) {
-    const float s_keep = upper ? s_hi : s_lo, s_send = upper ? s_lo : s_hi;
-    const float m_keep = upper ? m_hi : m_lo, m_send = upper ? m_lo : m_hi;
-    const float s_recv = __shfl_xor_sync(0xffffffffu, s_send, d);
-    const float m_recv = __shfl_xor_sync(0xffffffffu, m_send, d);
-    const float t = np * s_keep - n * s_recv;  // n * np * (mean_keep - mean_recv)
-    s_lo = s_keep + s_recv;
-    m_lo = fmaf(t * t, r, m_keep + m_recv);
-}
-
-__device__ __forceinline__ float chan_level_r(float n, float np) {
-    const float den = n * np * (n + np);
-    return den > 0.f ? 1.f / den : 0.f;
-}
-
-// Levels D, D/2, ..., 1 of the reduce-scatter over slots [0, 2D): every slot of a lane describes
-// `n` values on entry (one count for all its slots); on exit lane l holds, in slot 0, slot
-// (l mod 2D) merged over the 2D lanes that agree with l above bit log2(D).
-template <int D>
-__device__ __forceinline__ void warp_chan_scatter(float* s, float* m, float n, int lane) {
+// Reduce-scatter over the warp of N <= 32 per-lane slots (N a power of two): lane l ends with the
+// total over all 32 lanes of slot (l mod N) in v[0]. Lane distances 16 .. N add whole slot sets
+// (both lanes keep the sum); the distances below N halve the slots each lane keeps.
+template <int N>
+__device__ __forceinline__ void warp_sum_scatter(float* v, int lane) {
 #pragma unroll
-    for (int d = D; d >= 1; d >>= 1) {
-        const float np = __shfl_xor_sync(0xffffffffu, n, d);
-        const float r = chan_level_r(n, np);
+    for (int d = 16; d >= N && d >= 1; d >>= 1) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], d);
+    }
+#pragma unroll
+    for (int d = N / 2; d >= 1; d >>= 1) {
         const bool upper = (lane & d) != 0;
 #pragma unroll
-        for (int i = 0; i < d; ++i) chan_level(s[i], m[i], s[i + d], m[i + d], n, np, r, upper, d);
-        n += np;
+        for (int i = 0; i < d; ++i) {
+            const float send = upper ? v[i] : v[i + d];
+            const float keep = upper ? v[i + d] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+        }
     }
 }
 
-// One pass over columns [c_lo, c_hi) of this warp's TMEM lane quarter (c_lo a multiple of 32):
-// for every run of SUB consecutive channels of the thread's row (SUB = 4, 8, 16 divides the group
-// size; SUB = 1 is one run per channel), the sum and the sum of squared deviations from the run
-// mean of y = acc + bias (two passes over registers), then a Chan reduce-scatter over the warp's
-// rows. Afterwards red_s[q*256 + j] / red_m[q*256 + j] hold run j over the warp's valid rows
-// (rows past T_out count zero).
-template <int SUB>
-__device__ __forceinline__ void gn_run_stats(uint32_t tb, int c_lo, int c_hi, bool row_ok, const float* bias,
-                                             float* red_s, float* red_m, int q, int lane) {
-    const float n0 = row_ok ? float(SUB) : 0.f;
+// One pass over columns [c_lo, c_hi) of this warp's TMEM lane quarter (c_lo a multiple of 32): per
+// run of SUB consecutive channels of the thread's row (SUB = 4, 8, 16 divides the group size; SUB =
+// 1 is one run per channel) the sum of acc (SQUARED = false) or of (acc - shift[col])^2 (SQUARED =
+// true), rows past T_out contributing zero, then summed over the warp's rows: red[q*256 + run].
+template <int SUB, bool SQUARED>
+__device__ __forceinline__ void gn_run_pass(uint32_t tb, int c_lo, int c_hi, bool row_ok, const float* shift,
+                                            float* red, int q, int lane) {
     if constexpr (SUB == 1) {
         for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
-            float v[32], m[32];
+            float v[32];
             tmem_load32(tb + uint32_t(j0), v);
+            if (SQUARED) {
 #pragma unroll
-            for (int h = 0; h < 32; h += 16) {
-                float bb[16];
-                lds_vec(bias + j0 + h, bb);
+                for (int h = 0; h < 32; h += 8) {
+                    float sh[8];
+                    lds_vec(shift + j0 + h, sh);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[h + i] = row_ok ? v[h + i] + bb[i] : 0.f;
+                    for (int i = 0; i < 8; ++i) {
+                        const float d = v[h + i] - sh[i];
+                        v[h + i] = d * d;
+                    }
+                }
             }
 #pragma unroll
-            for (int i = 0; i < 32; ++i) m[i] = 0.f;
-            warp_chan_scatter<16>(v, m, n0, lane);
-            if (j0 + lane < c_hi) {
-                red_s[q * 256 + j0 + lane] = v[0];
-                red_m[q * 256 + j0 + lane] = m[0];
-            }
+            for (int i = 0; i < 32; ++i) v[i] = row_ok ? v[i] : 0.f;
+            warp_sum_scatter<32>(v, lane);
+            if (j0 + lane < c_hi) red[q * 256 + j0 + lane] = v[0];
         }
     } else {
-        // A window of up to 128 columns holds up to 32 runs (slot = run within the window). The
-        // scatter's first level (lanes 16 apart, slots 16 apart) is taken as soon as a slot >= 16
-        // is made, so only 16 (sum, M2) pairs stay live.
-        constexpr int kRunsPerChunk = 32 / SUB;           // runs per 32-column TMEM load
+        constexpr int kRunsPerChunk = 32 / SUB;            // runs per 32-column TMEM load
         constexpr int kWin = 32 * SUB < 128 ? 32 * SUB : 128;
-        constexpr int kRuns = kWin / SUB;
-        const float np16 = __shfl_xor_sync(0xffffffffu, n0, 16);
-        const float r16 = chan_level_r(n0, np16);
-        const bool up16 = (lane & 16) != 0;
-        for (int w0 = c_lo; w0 < c_hi; w0 += kWin) {     // uniform over the warp
-            float s[16], m[16];
+        constexpr int kRuns = kWin / SUB;                  // runs per window (one scatter)
+        for (int w0 = c_lo; w0 < c_hi; w0 += kWin) {      // uniform over the warp
+            float acc[kRuns];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) s[i] = m[i] = 0.f;
+            for (int i = 0; i < kRuns; ++i) acc[i] = 0.f;
 #pragma unroll
             for (int c = 0; c < kWin / 32; ++c) {
                 const int j0 = w0 + c * 32;
@@ -197,62 +190,44 @@ __device__ __forceinline__ void gn_run_stats(uint32_t tb, int c_lo, int c_hi, bo
                 tmem_load32(tb + uint32_t(j0), v);
 #pragma unroll
                 for (int r = 0; r < kRunsPerChunk; ++r) {
-                    float bb[SUB];
-                    lds_vec(bias + j0 + r * SUB, bb);
-                    float sum = 0.f;
+                    uint64_t sum2;
+                    if (SQUARED) {
+                        float sh[SUB];
+                        lds_vec(shift + j0 + r * SUB, sh);
+                        sum2 = 0ull;
 #pragma unroll
-                    for (int i = 0; i < SUB; ++i) {
-                        v[r * SUB + i] += bb[i];
-                        sum += v[r * SUB + i];
-                    }
-                    const float mean = sum * (1.f / SUB);
-                    float m2 = 0.f;
-#pragma unroll
-                    for (int i = 0; i < SUB; ++i) {
-                        const float d = v[r * SUB + i] - mean;
-                        m2 = fmaf(d, d, m2);
-                    }
-                    const int slot = c * kRunsPerChunk + r;
-                    const float rs = row_ok ? sum : 0.f, rm = row_ok ? m2 : 0.f;
-                    if (slot < 16) {
-                        s[slot] = rs;
-                        m[slot] = rm;
+                        for (int i = 0; i < SUB; i += 2) {
+                            const uint64_t d = f2_sub(f2_pack(v[r * SUB + i], v[r * SUB + i + 1]),
+                                                      f2_pack(sh[i], sh[i + 1]));
+                            sum2 = f2_fma(d, d, sum2);
+                        }
                     } else {
-                        chan_level(s[slot - 16], m[slot - 16], rs, rm, n0, np16, r16, up16, 16);
+                        uint64_t p[SUB / 2];
+#pragma unroll
+                        for (int i = 0; i < SUB / 2; ++i) p[i] = f2_pack(v[r * SUB + 2 * i], v[r * SUB + 2 * i + 1]);
+#pragma unroll
+                        for (int w = SUB / 2; w > 1; w >>= 1) {
+#pragma unroll
+                            for (int i = 0; i < w / 2; ++i) p[i] = f2_add(p[i], p[i + w / 2]);
+                        }
+                        sum2 = p[0];
                     }
+                    acc[c * kRunsPerChunk + r] = row_ok ? f2_hsum(sum2) : 0.f;
                 }
             }
-            if constexpr (kRuns <= 16) {
-                // no slot >= 16 in a window: the first level merges with empty partials
-#pragma unroll
-                for (int i = 0; i < 16; ++i) chan_level(s[i], m[i], 0.f, 0.f, n0, np16, r16, up16, 16);
-            } else {
-                // a window cut short by c_hi: slots it never made are empty
-                const int made = ((min(c_hi - w0, kWin) + 31) / 32) * kRunsPerChunk;
-                if (made <= 16) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) chan_level(s[i], m[i], 0.f, 0.f, n0, np16, r16, up16, 16);
-                } else if (made < 32) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (i + 16 >= made) chan_level(s[i], m[i], 0.f, 0.f, n0, np16, r16, up16, 16);
-                }
-            }
-            warp_chan_scatter<8>(s, m, n0 + np16, lane);
-            if (lane < kRuns && w0 + lane * SUB < c_hi) {  // runs of the other column range stay theirs
-                red_s[q * 256 + w0 / SUB + lane] = s[0];
-                red_m[q * 256 + w0 / SUB + lane] = m[0];
-            }
+            warp_sum_scatter<kRuns>(acc, lane);
+            if (lane < kRuns && w0 + lane * SUB < c_hi) red[q * 256 + w0 / SUB + lane] = acc[0];
         }
     }
 }
 
-__device__ __forceinline__ void gn_run_stats_any(int sub, uint32_t tb, int c_lo, int c_hi, bool row_ok,
-                                                 const float* bias, float* red_s, float* red_m, int q, int lane) {
-    if (sub == 4) gn_run_stats<4>(tb, c_lo, c_hi, row_ok, bias, red_s, red_m, q, lane);
-    else if (sub == 8) gn_run_stats<8>(tb, c_lo, c_hi, row_ok, bias, red_s, red_m, q, lane);
-    else if (sub == 16) gn_run_stats<16>(tb, c_lo, c_hi, row_ok, bias, red_s, red_m, q, lane);
-    else gn_run_stats<1>(tb, c_lo, c_hi, row_ok, bias, red_s, red_m, q, lane);
+template <bool SQUARED>
+__device__ __forceinline__ void gn_run_pass_any(int sub, uint32_t tb, int c_lo, int c_hi, bool row_ok,
+                                                const float* shift, float* red, int q, int lane) {
+    if (sub == 4) gn_run_pass<4, SQUARED>(tb, c_lo, c_hi, row_ok, shift, red, q, lane);
+    else if (sub == 8) gn_run_pass<8, SQUARED>(tb, c_lo, c_hi, row_ok, shift, red, q, lane);
+    else if (sub == 16) gn_run_pass<16, SQUARED>(tb, c_lo, c_hi, row_ok, shift, red, q, lane);
+    else gn_run_pass<1, SQUARED>(tb, c_lo, c_hi, row_ok, shift, red, q, lane);
 }
 
 // GroupNorm of the runs of CPG consecutive channels held by one thread (CPG divides 32): two passes
@@ -422,31 +397,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         else mbar_arrive(bar(i));
     };
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < SA; ++i) {
-            // TMA arrive, or one per transposer warp (of both CTAs of a pair)
-            mbar_init(bar(i_afull + i), LINEAR ? 1 : (PAIR ? 2 : 1) * xp_warps<BF16>());
-            mbar_init(bar(i_aempty + i), 1);
+    if (!LINEAR && threadIdx.x == 0) {
+        // The x boxes of this CTA's first unit head for L2 now; the loads that stage them come
+        // later. (A prefetch only fills L2, which every write reaches too, so it may run ahead of
+        // the kernels this one depends on.)
+        const int u0 = kFusedGN ? (blockIdx.z * a.n_t_tiles + blockIdx.x) * (a.n_cb / a.cb_per_unit) + blockIdx.y
+                                : ((PAIR || kClusterX) ? int(blockIdx.x >> 1) : int(blockIdx.x));
+        if (u0 < a.n_units) {
+            const Unit un0 = decode(u0);
+            for (int c = 0; c < a.n_ci_chunks; ++c)
+                tma_prefetch_3d(&tm_a, un0.row0 - a.pad_left - a.t_shift, c * a.BK, un0.n);
         }
-        for (int i = 0; i < SB; ++i) {
-            mbar_init(bar(i_bfull + i), 1);
-            mbar_init(bar(i_bempty + i), 1);
+    }
+    if (warp == kWarpTma) {
+        // barriers initialised by the 32 lanes together; arrival counts: A full: the TMA (Linear) or
+        // one per transposer warp (of both CTAs of a pair); accumulator empty: one per epilogue warp
+        // (of the pair); x staging empty: one per transposer warp; exchange: one per step, from the
+        // peer's first 4 epilogue warps; all others: one.
+        for (int i = lane; i < n_bars; i += 32) {
+            uint32_t cnt = 1;
+            if (i < i_aempty) cnt = LINEAR ? 1u : (PAIR ? 2u : 1u) * uint32_t(xp_warps<BF16>());
+            else if (i >= i_accempty && i < i_drain) cnt = (PAIR ? 2u : 1u) * uint32_t(kEpiW);
+            else if (i >= i_sempty && i < i_ex) cnt = uint32_t(xp_warps<BF16>());
+            else if (i >= i_ex) cnt = 128;
+            mbar_init(bar(i), cnt);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(i_accfull + i), 1);
-            mbar_init(bar(i_accempty + i), (PAIR ? 2 : 1) * kEpiW);  // one arrival per epilogue warp (of the pair)
-        }
-        mbar_init(bar(i_drain), 1);
-        for (int i = 0; i < 2; ++i) mbar_init(bar(i_ex + i), 128);  // one per step, from the peer's first 4 epilogue warps
-        for (int i = 0; i < SS; ++i) {
-            mbar_init(bar(i_sfull + i), 1);
-            mbar_init(bar(i_sempty + i), xp_warps<BF16>());  // one arrival per transposer warp
-        }
-        *abort_flag = 0;
-        for (int i = 0; i < kProgSlots; ++i) prog[i] = 0;
+        if (lane == 0) *abort_flag = 0;
+        if (lane < kProgSlots) prog[lane] = 0;
         fence_mbar_init();
-        prefetch_tensormap(&tm_a);
-        prefetch_tensormap(&tm_b);
+        if (lane == 0) {
+            prefetch_tensormap(&tm_a);
+            prefetch_tensormap(&tm_b);
+        }
     }
     if (warp == kWarpMma) {
         if constexpr (PAIR) {
@@ -469,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // write (the pack itself starts only after all earlier work of the stream has finished).
     {
         const bool xp_role = !LINEAR && warp >= xp_first<BF16>() && warp < xp_first<BF16>() + xp_warps<BF16>();
-        if (!(xp_role || (warp == kWarpXld && a.early_inputs))) griddep_wait();
+        if (!(xp_role || warp == kWarpTma || (warp == kWarpXld && a.early_inputs))) griddep_wait();
     }
 
     int first_unit, unit_step;
@@ -504,6 +486,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tx_stage = tx_mult * uint32_t(a.b_slot_bytes + (LINEAR ? a.a_slot_bytes : 0));
         const int co_half = PAIR ? int(rank) * (a.BN / 2) : 0;
         const int nparts = (!LINEAR && !BF16 && a.x3) ? 2 : 1;
+        // When x may be read early, this warp (running already) stages the first x boxes of its
+        // first unit before it waits for the weight pack; the x loader goes on from the next box.
+        const int x_early = (!LINEAR && a.early_inputs && first_unit < a.n_units) ? min(SS, a.n_ci_chunks) : 0;
+        if (x_early > 0 && lane == 0) {
+            const Unit un0 = decode(first_unit);
+            const uint32_t box_bytes = uint32_t(a.RS * a.BK * (BF16 ? 2 : 4));
+            for (int c = 0; c < x_early; ++c) {
+                mbar_arrive_expect_tx(bar(i_sfull + c), box_bytes);
+                tma_load_3d(sS + c * a.s_slot_bytes, &tm_a, bar(i_sfull + c), un0.row0 - a.pad_left - a.t_shift,
+                            c * a.BK, un0.n);
+            }
+        }
+        __syncwarp();
+        griddep_wait();
         for (int u = first_unit; u < a.n_units && !aborting(); u += unit_step) {
             const Unit un = decode(u);
             for (int c = 0; c < a.n_ci_chunks; ++c) {
@@ -651,14 +647,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // convolution's zero padding.
         if (!LINEAR && lane == 0) {
             const uint32_t box_bytes = uint32_t(a.RS * a.BK * (BF16 ? 2 : 4));
-            int si = 0;
-            uint32_t sph = 0;
-            long long s_cnt = 0;
+            // the first x_early boxes of the first unit were staged by the TMA producer warp
+            const int x_early = (a.early_inputs && first_unit < a.n_units) ? min(SS, a.n_ci_chunks) : 0;
+            int si = x_early == SS ? 0 : x_early;
+            uint32_t sph = x_early == SS ? 1u : 0u;
+            long long s_cnt = x_early;
             for (int u = first_unit; u < a.n_units && !*abort_flag; u += unit_step) {
                 const Unit un = decode(u);
                 const int t0 = un.row0 - a.pad_left - a.t_shift;  // multiple of 16 bytes of elements
-                for (int c = 0; c < a.n_ci_chunks; ++c) {
-                    if (!mbar_wait(bar(i_sempty + si), sph ^ 1, abort_flag, a.status, kWaitSEmpty, prog)) goto xld_done;
+                for (int c = u == first_unit ? x_early : 0; c < a.n_ci_chunks; ++c) {
+                    if (!mbar_try_wait(bar(i_sempty + si), sph ^ 1) &&
+                        !mbar_wait(bar(i_sempty + si), sph ^ 1, abort_flag, a.status, kWaitSEmpty, prog))
+                        goto xld_done;
                     mbar_arrive_expect_tx(bar(i_sfull + si), box_bytes);
                     tma_load_3d(sS + si * a.s_slot_bytes, &tm_a, bar(i_sfull + si), t0, c * a.BK, un.n);
                     ++s_cnt;
@@ -1081,38 +1081,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                     unsigned target = 0;
                     if (EPI == kEpiGridGN) target = unsigned(ld_relaxed_gpu_u64(gx_me) >> 32) + 1u;
                     float* red_s = epi;            // [4][256] per-warp run sums
-                    float* red_m = epi + 1024;     // [4][256] per-warp run M2
+                    float* red_m = epi + 1024;     // [4][256] per-warp run sums of squared deviations
                     float* part_mu = epi + 2048;   // [256] this CTA's group means (cluster exchange)
                     float* colscale = epi + 2304;  // [256]
                     float* colshift = epi + 2560;  // [256]
                     float* gmean = epi + 2816;     // [256] group mean over all CTAs
                     float* grstd = epi + 3328;     // [256] group 1/sqrt(var + eps)
                     float* part_m2 = epi + 3584;   // [256] this CTA's group M2 (cluster exchange)
+                    float* s_shift = epi;          // [256] part_mu - bias per column (over red_s, read
+                                                   // before it is written)
                     const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
-                    // one pass over TMEM: sum and M2 of y = acc + bias per run of `sub` channels of each
-                    // row, merged over the warp's rows with Chan's formula
+                    // two passes over TMEM: per run of `sub` channels, the sums of acc (the bias enters at
+                    // group level as nvalid_t * sum(bias)) -> this CTA's group means; then the squared
+                    // deviations of y = acc + bias from them -> M2
                     const int nvalid_w = min(32, max(0, nvalid_t - q * 32));
-                    gn_run_stats_any(a.sub, tb, c_lo, c_hi, lane < nvalid_w, s_bias, red_s, red_m, q, lane);
+                    const bool row_in = lane < nvalid_w;
+                    gn_run_pass_any<false>(a.sub, tb, c_lo, c_hi, row_in, s_shift, red_s, q, lane);
                     named_bar_sync(1, kEpiT);
                     const int run = a.sub > 0 ? a.sub : 1;
                     for (int g = er; g < ngroups; g += kEpiT) {
-                        // this CTA's part of group g: merge its runs over the four warps
                         const int c0 = g * cpg, c_end = min(ncols, c0 + cpg);
-                        float gn = 0.f, gs = 0.f, gm2 = 0.f;
-                        for (int q2 = 0; q2 < 4; ++q2) {
-                            const float nq = float(min(32, max(0, nvalid_t - q2 * 32)) * run);
-                            if (nq <= 0.f) continue;
-                            for (int j = c0 / run; j < (c_end + run - 1) / run; ++j)
-                                chan_merge_sum(gn, gs, gm2, nq, red_s[q2 * 256 + j], red_m[q2 * 256 + j]);
-                        }
-                        const float mu = gs / gn;
+                        float sum = 0.f, bsum = 0.f;
+                        for (int j = c0 / run; j < (c_end + run - 1) / run; ++j)
+                            sum += red_s[j] + red_s[256 + j] + red_s[512 + j] + red_s[768 + j];
+                        for (int col = c0; col < c_end; ++col) bsum += s_bias[col];
+                        part_mu[g] = (sum + float(nvalid_t) * bsum) / float((c_end - c0) * nvalid_t);
+                    }
+                    named_bar_sync(1, kEpiT);
+                    for (int col = er; col < 256; col += kEpiT)
+                        s_shift[col] = col < ncols ? part_mu[col / cpg] - s_bias[col] : 0.f;
+                    named_bar_sync(1, kEpiT);
+                    gn_run_pass_any<true>(a.sub, tb, c_lo, c_hi, row_in, s_shift, red_m, q, lane);
+                    named_bar_sync(1, kEpiT);
+                    for (int g = er; g < ngroups; g += kEpiT) {
+                        const int c0 = g * cpg, c_end = min(ncols, c0 + cpg);
+                        float m2 = 0.f;
+                        for (int j = c0 / run; j < (c_end + run - 1) / run; ++j)
+                            m2 += red_m[j] + red_m[256 + j] + red_m[512 + j] + red_m[768 + j];
                         if (EPI == kEpiGridGN) {
                             const unsigned long long tag = (unsigned long long)target << 32;
-                            st_relaxed_gpu_u64(gx_me + 2 * g, tag | __float_as_uint(mu));
-                            st_relaxed_gpu_u64(gx_me + 2 * g + 1, tag | __float_as_uint(gm2));
+                            st_relaxed_gpu_u64(gx_me + 2 * g, tag | __float_as_uint(part_mu[g]));
+                            st_relaxed_gpu_u64(gx_me + 2 * g + 1, tag | __float_as_uint(m2));
                         } else {
-                            part_mu[g] = mu;
-                            part_m2[g] = gm2;
+                            part_m2[g] = m2;
                         }
                     }
                     if (EPI == kEpiClusterGN) {
