@@ -146,33 +146,39 @@ __device__ __forceinline__ void warp_sum_scatter(float* v, int lane) {
     }
 }
 
-// One pass over columns [c_lo, c_hi) of this warp's TMEM lane quarter (c_lo a multiple of 32): per
-// run of SUB consecutive channels of the thread's row (SUB = 4, 8, 16 divides the group size; SUB =
-// 1 is one run per channel) the sum of acc (SQUARED = false) or of (acc - shift[col])^2 (SQUARED =
-// true), rows past T_out contributing zero, then summed over the warp's rows: red[q*256 + run].
-template <int SUB, bool SQUARED>
-__device__ __forceinline__ void gn_run_pass(uint32_t tb, int c_lo, int c_hi, bool row_ok, const float* shift,
-                                            float* red, int q, int lane) {
+// Moments of this warp's rows over columns [c_lo, c_hi) of its TMEM lane quarter (c_lo a multiple
+// of 32), for every run of SUB consecutive channels (SUB = 4, 8, 16 divides the group size; SUB = 1
+// is one run per channel), window by window (up to 32 runs): first the sum of acc over the run
+// (red_s[q*256 + run]), then, with the run's mean m known to every lane, the sum over the run of
+// (acc + bc[col] - m)^2 (red_m[q*256 + run]), where bc is the bias minus its mean over the run, so
+// that this is the run's sum of squared deviations of y = acc + bias from its mean. Rows past T_out
+// (row_ok false) count zero; n_rows is the number of valid rows of the warp.
+template <int SUB>
+__device__ __forceinline__ void gn_run_moments(uint32_t tb, int c_lo, int c_hi, bool row_ok, int n_rows,
+                                               const float* bc, float* red_s, float* red_m, int q, int lane) {
+    const float inv_n = n_rows > 0 ? 1.f / float(n_rows * SUB) : 0.f;
     if constexpr (SUB == 1) {
         for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
             float v[32];
             tmem_load32(tb + uint32_t(j0), v);
-            if (SQUARED) {
-#pragma unroll
-                for (int h = 0; h < 32; h += 8) {
-                    float sh[8];
-                    lds_vec(shift + j0 + h, sh);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float d = v[h + i] - sh[i];
-                        v[h + i] = d * d;
-                    }
-                }
-            }
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = row_ok ? v[i] : 0.f;
             warp_sum_scatter<32>(v, lane);
-            if (j0 + lane < c_hi) red[q * 256 + j0 + lane] = v[0];
+            if (j0 + lane < c_hi) red_s[q * 256 + j0 + lane] = v[0];
+            const float m_lane = v[0] * inv_n;  // mean of column j0 + lane
+            tmem_load32(tb + uint32_t(j0), v);
+#pragma unroll
+            for (int h = 0; h < 32; h += 8) {
+                float b8[8];
+                lds_vec(bc + j0 + h, b8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float d = v[h + i] + b8[i] - __shfl_sync(0xffffffffu, m_lane, h + i);
+                    v[h + i] = row_ok ? d * d : 0.f;
+                }
+            }
+            warp_sum_scatter<32>(v, lane);
+            if (j0 + lane < c_hi) red_m[q * 256 + j0 + lane] = v[0];
         }
     } else {
         constexpr int kRunsPerChunk = 32 / SUB;            // runs per 32-column TMEM load
@@ -190,44 +196,57 @@ __device__ __forceinline__ void gn_run_pass(uint32_t tb, int c_lo, int c_hi, boo
                 tmem_load32(tb + uint32_t(j0), v);
 #pragma unroll
                 for (int r = 0; r < kRunsPerChunk; ++r) {
-                    uint64_t sum2;
-                    if (SQUARED) {
-                        float sh[SUB];
-                        lds_vec(shift + j0 + r * SUB, sh);
-                        sum2 = 0ull;
+                    uint64_t p[SUB / 2];
 #pragma unroll
-                        for (int i = 0; i < SUB; i += 2) {
-                            const uint64_t d = f2_sub(f2_pack(v[r * SUB + i], v[r * SUB + i + 1]),
-                                                      f2_pack(sh[i], sh[i + 1]));
-                            sum2 = f2_fma(d, d, sum2);
-                        }
-                    } else {
-                        uint64_t p[SUB / 2];
+                    for (int i = 0; i < SUB / 2; ++i) p[i] = f2_pack(v[r * SUB + 2 * i], v[r * SUB + 2 * i + 1]);
 #pragma unroll
-                        for (int i = 0; i < SUB / 2; ++i) p[i] = f2_pack(v[r * SUB + 2 * i], v[r * SUB + 2 * i + 1]);
+                    for (int w = SUB / 2; w > 1; w >>= 1) {
 #pragma unroll
-                        for (int w = SUB / 2; w > 1; w >>= 1) {
-#pragma unroll
-                            for (int i = 0; i < w / 2; ++i) p[i] = f2_add(p[i], p[i + w / 2]);
-                        }
-                        sum2 = p[0];
+                        for (int i = 0; i < w / 2; ++i) p[i] = f2_add(p[i], p[i + w / 2]);
                     }
-                    acc[c * kRunsPerChunk + r] = row_ok ? f2_hsum(sum2) : 0.f;
+                    acc[c * kRunsPerChunk + r] = row_ok ? f2_hsum(p[0]) : 0.f;
                 }
             }
             warp_sum_scatter<kRuns>(acc, lane);
-            if (lane < kRuns && w0 + lane * SUB < c_hi) red[q * 256 + w0 / SUB + lane] = acc[0];
+            const bool mine = lane < kRuns && w0 + lane * SUB < c_hi;  // lane's run lies in this range
+            if (mine) red_s[q * 256 + w0 / SUB + lane] = acc[0];
+            const float m_lane = acc[0] * inv_n;  // mean of acc over run (lane mod kRuns)
+#pragma unroll
+            for (int i = 0; i < kRuns; ++i) acc[i] = 0.f;
+#pragma unroll
+            for (int c = 0; c < kWin / 32; ++c) {
+                const int j0 = w0 + c * 32;
+                if (j0 >= c_hi) break;  // uniform
+                float v[32];
+                tmem_load32(tb + uint32_t(j0), v);
+#pragma unroll
+                for (int r = 0; r < kRunsPerChunk; ++r) {
+                    const int slot = c * kRunsPerChunk + r;
+                    const float m = __shfl_sync(0xffffffffu, m_lane, slot);
+                    const uint64_t mm = f2_pack(m, m);
+                    float b[SUB];
+                    lds_vec(bc + j0 + r * SUB, b);
+                    uint64_t sq = 0ull;
+#pragma unroll
+                    for (int i = 0; i < SUB; i += 2) {
+                        const uint64_t d = f2_sub(f2_add(f2_pack(v[r * SUB + i], v[r * SUB + i + 1]), f2_pack(b[i], b[i + 1])), mm);
+                        sq = f2_fma(d, d, sq);
+                    }
+                    acc[slot] = row_ok ? f2_hsum(sq) : 0.f;
+                }
+            }
+            warp_sum_scatter<kRuns>(acc, lane);
+            if (mine) red_m[q * 256 + w0 / SUB + lane] = acc[0];
         }
     }
 }
 
-template <bool SQUARED>
-__device__ __forceinline__ void gn_run_pass_any(int sub, uint32_t tb, int c_lo, int c_hi, bool row_ok,
-                                                const float* shift, float* red, int q, int lane) {
-    if (sub == 4) gn_run_pass<4, SQUARED>(tb, c_lo, c_hi, row_ok, shift, red, q, lane);
-    else if (sub == 8) gn_run_pass<8, SQUARED>(tb, c_lo, c_hi, row_ok, shift, red, q, lane);
-    else if (sub == 16) gn_run_pass<16, SQUARED>(tb, c_lo, c_hi, row_ok, shift, red, q, lane);
-    else gn_run_pass<1, SQUARED>(tb, c_lo, c_hi, row_ok, shift, red, q, lane);
+__device__ __forceinline__ void gn_run_moments_any(int sub, uint32_t tb, int c_lo, int c_hi, bool row_ok, int n_rows,
+                                                   const float* bc, float* red_s, float* red_m, int q, int lane) {
+    if (sub == 4) gn_run_moments<4>(tb, c_lo, c_hi, row_ok, n_rows, bc, red_s, red_m, q, lane);
+    else if (sub == 8) gn_run_moments<8>(tb, c_lo, c_hi, row_ok, n_rows, bc, red_s, red_m, q, lane);
+    else if (sub == 16) gn_run_moments<16>(tb, c_lo, c_hi, row_ok, n_rows, bc, red_s, red_m, q, lane);
+    else gn_run_moments<1>(tb, c_lo, c_hi, row_ok, n_rows, bc, red_s, red_m, q, lane);
 }
 
 // GroupNorm of the runs of CPG consecutive channels held by one thread (CPG divides 32): two passes
@@ -787,6 +806,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     epi[2560 + col] = (ok && a.beta) ? __ldg(a.beta + co_base + col) : 0.f;
                 }
                 named_bar_sync(1, kEpiT);
+                // the bias minus its mean over the column's run of `sub` channels (in epi[2816..3072),
+                // free until the statistics are merged)
+                const int run = a.sub > 0 ? a.sub : 1;
+                for (int col = er; col < 256; col += kEpiT) {
+                    const int r0 = col - col % run;
+                    float mb = 0.f;
+                    for (int i = 0; i < run; ++i) mb += s_bias[r0 + i];
+                    epi[2816 + col] = s_bias[col] - mb * (1.f / float(run));
+                }
+                // (the epilogue's first barrier, at the accumulator wait, orders these)
             }
             int lt = 0;
             for (int u = first_unit; u < a.n_units; u += unit_step, ++lt) {
@@ -1088,42 +1117,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float* gmean = epi + 2816;     // [256] group mean over all CTAs
                     float* grstd = epi + 3328;     // [256] group 1/sqrt(var + eps)
                     float* part_m2 = epi + 3584;   // [256] this CTA's group M2 (cluster exchange)
-                    float* s_shift = epi;          // [256] part_mu - bias per column (over red_s, read
-                                                   // before it is written)
+                    const float* s_bc = epi + 2816;  // [256] bias minus its run mean (gmean's area, later)
                     const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
-                    // two passes over TMEM: per run of `sub` channels, the sums of acc (the bias enters at
-                    // group level as nvalid_t * sum(bias)) -> this CTA's group means; then the squared
-                    // deviations of y = acc + bias from them -> M2
+                    // this warp's moments per run of `sub` channels (two sweeps of its TMEM columns), then
+                    // this CTA's (count, mean, M2) per group, merged over runs and warps
                     const int nvalid_w = min(32, max(0, nvalid_t - q * 32));
-                    const bool row_in = lane < nvalid_w;
-                    gn_run_pass_any<false>(a.sub, tb, c_lo, c_hi, row_in, s_shift, red_s, q, lane);
+                    gn_run_moments_any(a.sub, tb, c_lo, c_hi, lane < nvalid_w, nvalid_w, s_bc, red_s, red_m, q, lane);
                     named_bar_sync(1, kEpiT);
                     const int run = a.sub > 0 ? a.sub : 1;
                     for (int g = er; g < ngroups; g += kEpiT) {
                         const int c0 = g * cpg, c_end = min(ncols, c0 + cpg);
-                        float sum = 0.f, bsum = 0.f;
-                        for (int j = c0 / run; j < (c_end + run - 1) / run; ++j)
-                            sum += red_s[j] + red_s[256 + j] + red_s[512 + j] + red_s[768 + j];
-                        for (int col = c0; col < c_end; ++col) bsum += s_bias[col];
-                        part_mu[g] = (sum + float(nvalid_t) * bsum) / float((c_end - c0) * nvalid_t);
-                    }
-                    named_bar_sync(1, kEpiT);
-                    for (int col = er; col < 256; col += kEpiT)
-                        s_shift[col] = col < ncols ? part_mu[col / cpg] - s_bias[col] : 0.f;
-                    named_bar_sync(1, kEpiT);
-                    gn_run_pass_any<true>(a.sub, tb, c_lo, c_hi, row_in, s_shift, red_m, q, lane);
-                    named_bar_sync(1, kEpiT);
-                    for (int g = er; g < ngroups; g += kEpiT) {
-                        const int c0 = g * cpg, c_end = min(ncols, c0 + cpg);
-                        float m2 = 0.f;
-                        for (int j = c0 / run; j < (c_end + run - 1) / run; ++j)
-                            m2 += red_m[j] + red_m[256 + j] + red_m[512 + j] + red_m[768 + j];
+                        float gn = 0.f, gmu = 0.f, gm2 = 0.f;
+                        for (int j = c0 / run; j < (c_end + run - 1) / run; ++j) {
+                            float mb = 0.f;  // the bias mean of run j
+                            for (int i = 0; i < run; ++i) mb += s_bias[j * run + i];
+                            mb *= 1.f / float(run);
+                            for (int q2 = 0; q2 < 4; ++q2) {
+                                const int nr = min(32, max(0, nvalid_t - q2 * 32));
+                                if (nr == 0) continue;
+                                const float nq = float(nr * run);
+                                chan_merge(gn, gmu, gm2, nq, red_s[q2 * 256 + j] / nq + mb, red_m[q2 * 256 + j]);
+                            }
+                        }
                         if (EPI == kEpiGridGN) {
                             const unsigned long long tag = (unsigned long long)target << 32;
-                            st_relaxed_gpu_u64(gx_me + 2 * g, tag | __float_as_uint(part_mu[g]));
-                            st_relaxed_gpu_u64(gx_me + 2 * g + 1, tag | __float_as_uint(m2));
+                            st_relaxed_gpu_u64(gx_me + 2 * g, tag | __float_as_uint(gmu));
+                            st_relaxed_gpu_u64(gx_me + 2 * g + 1, tag | __float_as_uint(gm2));
                         } else {
-                            part_m2[g] = m2;
+                            part_mu[g] = gmu;
+                            part_m2[g] = gm2;
                         }
                     }
                     if (EPI == kEpiClusterGN) {
@@ -1152,7 +1174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float cw = float(min(ncols, g * cpg + cpg) - g * cpg);
                             float gn = 0.f, gmu = 0.f, gm2 = 0.f;
                             const uint64_t t0 = global_timer_ns();
-                            constexpr int kPollBatch = 4;  // peers whose words are in flight together
+                            constexpr int kPollBatch = 2;  // peers whose words are in flight together
                             for (int base_rk = 0; base_rk < a.n_t_tiles; base_rk += kPollBatch) {
                                 const int nrk = min(kPollBatch, a.n_t_tiles - base_rk);
                                 unsigned long long wmu[kPollBatch], wm2[kPollBatch];
