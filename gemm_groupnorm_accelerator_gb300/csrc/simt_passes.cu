@@ -310,12 +310,13 @@ __global__ void __launch_bounds__(256) normalize8_kernel(NormArgs a, const float
                 }
             } else {
                 const float sc = gs.y * ga, of = be - gs.x * gs.y * ga;
+                const uint64_t sp = f2_pack(sc, sc), op = f2_pack(of, of);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) r[j] = fmaf(r[j], sc, of);
+                for (int j = 0; j < 8; j += 2) f2_unpack(f2_fma(f2_pack(r[j], r[j + 1]), sp, op), r[j], r[j + 1]);
             }
             if (GELU) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) r[j] = gelu_erf(r[j]);
+                for (int j = 0; j < 8; j += 2) f2_unpack(gelu_erf2(f2_pack(r[j], r[j + 1])), r[j], r[j + 1]);
             }
             if constexpr (sizeof(OutT) == 4) {
                 float4* dst = reinterpret_cast<float4*>(y + row * a.T_out);
@@ -359,11 +360,13 @@ __global__ void __launch_bounds__(256) normalize8_ln_kernel(NormArgs a, const fl
         const float4* src = reinterpret_cast<const float4*>(raw + row * a.T_out);
         const float4 v0 = src[2 * i], v1 = src[2 * i + 1];
         float r[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        const uint64_t gp = f2_pack(ga, ga), bp = f2_pack(be, be);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) r[j] = fmaf((r[j] - mu[j]) * rs[j], ga, be);
-        if (GELU) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) r[j] = gelu_erf(r[j]);
+        for (int j = 0; j < 8; j += 2) {
+            uint64_t o = f2_fma(f2_mul(f2_sub(f2_pack(r[j], r[j + 1]), f2_pack(mu[j], mu[j + 1])),
+                                       f2_pack(rs[j], rs[j + 1])), gp, bp);
+            if (GELU) o = gelu_erf2(o);
+            f2_unpack(o, r[j], r[j + 1]);
         }
         if constexpr (sizeof(OutT) == 4) {
             float4* dst = reinterpret_cast<float4*>(y + row * a.T_out);

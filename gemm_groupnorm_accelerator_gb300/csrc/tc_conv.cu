@@ -97,33 +97,6 @@ __device__ __forceinline__ void chan_merge(float& n_a, float& mu_a, float& m2_a,
     n_a = n;
 }
 
-// Packed pairs of fp32 (Blackwell's paired fp32 add / sub / fma): lo in the low word.
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ float f2_hsum(uint64_t p) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
-    return lo + hi;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-
 // Reduce-scatter over the warp of N <= 32 per-lane slots (N a power of two): lane l ends with the
 // total over all 32 lanes of slot (l mod N) in v[0]. Lane distances 16 .. N add whole slot sets
 // (both lanes keep the sum); the distances below N halve the slots each lane keeps.
@@ -307,6 +280,31 @@ __device__ __forceinline__ void tma_store_wait_read_le1() {
 // Every bulk store issued by this thread has completed (its writes are done).
 __device__ __forceinline__ void tma_store_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// LayerNorm of one 32-column chunk of a row from its mean and 1/sqrt(var + eps): per column
+// ((v + bias) - mean) * rstd * gamma + beta, then GELU when asked, in paired fp32 arithmetic (each
+// pair rounded as the scalar form ((v + (bias - mean)) * rstd) * gamma + beta).
+__device__ __forceinline__ void ln_affine_gelu(float (&v)[32], const float* bias, const float* gamma, const float* beta,
+                                               float mean, float rstd, bool gelu) {
+    const uint64_t mp = f2_pack(mean, mean), rp = f2_pack(rstd, rstd);
+#pragma unroll
+    for (int h = 0; h < 32; h += 16) {
+        float bb[16], gg[16], be[16];
+        lds_vec(bias + h, bb);
+        lds_vec(gamma + h, gg);
+        lds_vec(beta + h, be);
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            const uint64_t t = f2_add(f2_pack(v[h + i], v[h + i + 1]), f2_sub(f2_pack(bb[i], bb[i + 1]), mp));
+            const uint64_t o = f2_fma(f2_mul(t, rp), f2_pack(gg[i], gg[i + 1]), f2_pack(be[i], be[i + 1]));
+            f2_unpack(o, v[h + i], v[h + i + 1]);
+        }
+    }
+    if (gelu) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) f2_unpack(gelu_erf2(f2_pack(v[i], v[i + 1])), v[i], v[i + 1]);
+    }
 }
 
 struct Unit {
@@ -973,13 +971,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float bb[32];
                         lds_vec(s_bias + j0, bb);
                         if (j0 == c_lo) shift = v[0] + bb[0];
-                        if (j0 + 32 <= c_hi) {  // whole chunk (uniform): no per-column test
+                        if (j0 + 32 <= c_hi) {  // whole chunk (uniform): no per-column test, paired sums
+                            const uint64_t sp = f2_pack(shift, shift);
+                            uint64_t p1 = 0ull, p2 = 0ull;
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                const float d = v[i] + bb[i] - shift;
-                                s1 += d;
-                                s2 = fmaf(d, d, s2);
+                            for (int i = 0; i < 32; i += 2) {
+                                const uint64_t d = f2_sub(f2_add(f2_pack(v[i], v[i + 1]), f2_pack(bb[i], bb[i + 1])), sp);
+                                p1 = f2_add(p1, d);
+                                p2 = f2_fma(d, d, p2);
                             }
+                            s1 += f2_hsum(p1);
+                            s2 += f2_hsum(p2);
                         } else {
 #pragma unroll
                             for (int i = 0; i < 32; ++i)
@@ -1030,20 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
                             float v[32];
                             tmem_load32(tb + uint32_t(j0), v);
-#pragma unroll
-                            for (int h = 0; h < 32; h += 16) {
-                                float bb[16], gg[16], be[16];
-                                lds_vec(s_bias + j0 + h, bb);
-                                lds_vec(s_gamma + j0 + h, gg);
-                                lds_vec(s_beta + j0 + h, be);
-#pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    v[h + i] = fmaf((v[h + i] + (bb[i] - mean)) * rstd, gg[i], be[i]);
-                            }
-                            if (a.gelu) {
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-                            }
+                            ln_affine_gelu(v, s_bias + j0, s_gamma + j0, s_beta + j0, mean, rstd, a.gelu != 0);
                             // the store issued from this buffer two chunks ago has read it
                             if (lane == 0) tma_store_wait_read_le1();
                             __syncwarp();
@@ -1061,20 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
                             float v[32];
                             tmem_load32(tb + uint32_t(j0), v);
-#pragma unroll
-                            for (int h = 0; h < 32; h += 16) {
-                                float bb[16], gg[16], be[16];
-                                lds_vec(s_bias + j0 + h, bb);
-                                lds_vec(s_gamma + j0 + h, gg);
-                                lds_vec(s_beta + j0 + h, be);
-#pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    v[h + i] = fmaf((v[h + i] + (bb[i] - mean)) * rstd, gg[i], be[i]);
-                            }
-                            if (a.gelu) {
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-                            }
+                            ln_affine_gelu(v, s_bias + j0, s_gamma + j0, s_beta + j0, mean, rstd, a.gelu != 0);
                             if (row_ok) {
 #pragma unroll
                                 for (int i = 0; i < 32; ++i)
