@@ -59,6 +59,8 @@ def _load():
             lib.oracle_rowmin_bias.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_long, f64p, f32p, f64p, i32p]
             lib.oracle_conv1d_norm.argtypes = [P(OracleParams), f32p, f32p, f32p, f32p, f32p, f32p, f64p, i32p,
                                                ctypes.c_int]
+            lib.oracle_ln_avgpool3d_gelu.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                                     ctypes.c_float, f32p, f32p, f32p, ctypes.c_int, f64p, ctypes.c_int]
             lib.oracle_conv1d_norm_samples.argtypes = [P(OracleParams), f32p, f32p, f32p, f32p, f32p, f32p, i32p,
                                                        ctypes.c_int, f64p, i32p, ctypes.c_int]
             _lib = lib
@@ -193,3 +195,21 @@ def conv1d_norm_samples(p: OracleParams, ns, x, w, b=None, gamma=None, beta=None
     if rc != 0:
         raise ValueError("oracle_conv1d_norm_samples rejected its arguments")
     return y, am
+
+
+def ln_avgpool3d_gelu(z: np.ndarray, eps: float, sum_weight: float, gamma=None, beta=None,
+                      nthreads: Optional[int] = None) -> np.ndarray:
+    """[p4]'s add + LayerNorm(last dim) + AvgPool3d(2) + GELU on z [..., D, H, W] (float32), every
+    leading index an independent slice; returns [..., D//2, H//2, W//2] in float64."""
+    z = np.ascontiguousarray(z, dtype=np.float32)
+    *lead, D, H, W = z.shape
+    count = int(np.prod(lead)) if lead else 1
+    lib = _load()
+    out = np.empty((count, D // 2, H // 2, W // 2), dtype=np.float64)
+    gp, bp = _f32(gamma), _f32(beta)
+    rc = lib.oracle_ln_avgpool3d_gelu(D, H, W, eps, sum_weight, z.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                      gp[1], bp[1], count, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                                      nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_ln_avgpool3d_gelu rejected its arguments")
+    return out.reshape(*lead, D // 2, H // 2, W // 2)

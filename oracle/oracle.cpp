@@ -13,7 +13,8 @@
 //   [p1] Kimi-K2.6 l2_p35 page: Conv1d(128->256, k=3, s=1, p=1) + GroupNorm(32).
 //   [p2] Kimi-K2.6 l2_p75 page: Linear(8192->8192) + GroupNorm(512) + min(dim=1) + bias.
 //   [p3] Kimi-K2.6 l1_p5 page: causal Conv1d, k=4, left pad (k-1)*dilation.
-//   [p4] Kimi-K2.6 l2_p3 page: LayerNorm with affine and exact-erf GELU.
+//   [p4] Kimi-K2.6 l2_p3 page: LayerNorm with affine and exact-erf GELU; its second operator
+//        (scalar add, LayerNorm over the last dimension, AvgPool3d 2x2x2, GELU).
 //
 // Parity pins: every function below is pinned by tests that do not re-run this
 // code's formulas (delta kernels, the worked causal example of [p3], GELU(1)
@@ -238,6 +239,60 @@ int oracle_conv1d_norm_samples(const OracleParams* p, const float* x, const floa
                                     argmin_n ? argmin_n + i * T_out : nullptr, nthreads);
         if (rc != 0) return rc;
     }
+    return 0;
+}
+
+// [p4]'s second operator, after its transposed convolution: add the scalar sum_weight, LayerNorm
+// over the last (contiguous) dimension W with per-position gamma[W] / beta[W] (population variance
+// in two passes, eps inside the square root), AvgPool3d with kernel 2 and stride 2 over (D, H, W)
+// (floor: a trailing odd plane, row or column takes part in no window), then exact GELU.
+// z [N][C][D][H][W]; out [N][C][D/2][H/2][W/2] (double). gamma / beta may be null (1 and 0).
+// Only the (n, c) slices listed in `ncs` (count of them; null means all N*C in order) are
+// evaluated, slice i of the output going to out + i * (D/2)*(H/2)*(W/2); z holds those slices
+// in the same order (z + i * D*H*W).
+int oracle_ln_avgpool3d_gelu(int D, int H, int W, float eps, float sum_weight, const float* z, const float* gamma,
+                             const float* beta, int count, double* out, int nthreads) {
+    if (D < 1 || H < 1 || W < 1 || count < 0 || !(eps > 0.0f)) return -1;
+    const long D2 = D / 2, H2 = H / 2, W2 = W / 2;
+    const double inv_sqrt2 = 1.0 / std::sqrt(2.0);
+    parallel_for(count, nthreads, [&](long i) {
+        const float* zs = z + i * (long)D * H * W;
+        std::vector<double> ln((size_t)D * H * W);
+        for (long d = 0; d < D; ++d) {
+            for (long h = 0; h < H; ++h) {
+                const float* row = zs + (d * H + h) * W;
+                double* lr = ln.data() + (d * H + h) * W;
+                double sum = 0.0;
+                for (long w = 0; w < W; ++w) sum += (double)row[w] + (double)sum_weight;
+                const double mean = sum / (double)W;
+                double ss = 0.0;
+                for (long w = 0; w < W; ++w) {
+                    const double dv = (double)row[w] + (double)sum_weight - mean;
+                    ss += dv * dv;
+                }
+                const double inv = 1.0 / std::sqrt(ss / (double)W + (double)eps);
+                for (long w = 0; w < W; ++w) {
+                    const double ga = gamma ? (double)gamma[w] : 1.0;
+                    const double be = beta ? (double)beta[w] : 0.0;
+                    lr[w] = ((double)row[w] + (double)sum_weight - mean) * inv * ga + be;
+                }
+            }
+        }
+        double* os = out + i * D2 * H2 * W2;
+        for (long d2 = 0; d2 < D2; ++d2) {
+            for (long h2 = 0; h2 < H2; ++h2) {
+                for (long w2 = 0; w2 < W2; ++w2) {
+                    double acc = 0.0;
+                    for (long a = 0; a < 2; ++a)
+                        for (long b = 0; b < 2; ++b)
+                            for (long c = 0; c < 2; ++c)
+                                acc += ln[((2 * d2 + a) * H + 2 * h2 + b) * W + 2 * w2 + c];
+                    const double v = acc / 8.0;
+                    os[(d2 * H2 + h2) * W2 + w2] = 0.5 * v * (1.0 + std::erf(v * inv_sqrt2));
+                }
+            }
+        }
+    });
     return 0;
 }
 

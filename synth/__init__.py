@@ -220,3 +220,61 @@ def make_inputs(wl: Workload, seed: int = 0, n_rows: Optional[int] = None, row_o
         out["x"] = round_bf16(out["x"])
         out["w"] = round_bf16(out["w"])
     return out
+
+
+# ----------------------------------------------------------------------------------------------
+# [p4]'s second operator: add a scalar, LayerNorm over the last dimension, AvgPool3d 2x2x2, GELU
+
+
+@dataclasses.dataclass(frozen=True)
+class LnPoolWorkload:
+    """Shape of the LayerNorm(W) + AvgPool3d + GELU pass: z [N][C][D][H][W] fp32 (in [p4] the
+    output of ConvTranspose3d(32 -> 64, k 3, stride 2, pad 1, output pad 1) on x [32, 32, 16, 32,
+    32]); gamma / beta [W]; a scalar added before the LayerNorm."""
+
+    name: str
+    N: int
+    C: int
+    D: int
+    H: int
+    W: int
+    eps: float = 1e-5
+    sum_weight: float = 1.0
+    has_affine: bool = True
+    description: str = ""
+
+    @property
+    def out_shape(self):
+        return (self.N, self.C, self.D // 2, self.H // 2, self.W // 2)
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """z read once, gamma / beta read once, the pooled output written once (fp32)."""
+        n_in = self.N * self.C * self.D * self.H * self.W
+        n_out = self.N * self.C * (self.D // 2) * (self.H // 2) * (self.W // 2)
+        return 4 * (n_in + n_out + (2 * self.W if self.has_affine else 0))
+
+    def replace(self, **kw) -> "LnPoolWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+LN_AVGPOOL3D_GELU = LnPoolWorkload(
+    "layernorm_w_avgpool3d_gelu_f32_n32_c64_d32_h64_w64", N=32, C=64, D=32, H=64, W=64,
+    description="+ scalar, LayerNorm over W=64, AvgPool3d 2x2x2, exact GELU, fp32, z [32,64,32,64,64]")
+
+
+def make_lnpool_inputs(wl: LnPoolWorkload, seed: int = 0, n_slices: Optional[int] = None,
+                       slice_offset: int = 0) -> Dict[str, np.ndarray]:
+    """z ~ N(0, 1) (standing in for the transposed convolution's output), gamma ~ N(1, 0.1),
+    beta ~ N(0, 0.1). ``n_slices`` / ``slice_offset`` draw only the (n, c) slices [slice_offset,
+    slice_offset + n_slices) in n-major order, returned as [n_slices][D][H][W]."""
+    per = wl.D * wl.H * wl.W
+    total = wl.N * wl.C
+    n = total if n_slices is None else n_slices
+    z = normal_slice(seed, STREAM_X, slice_offset * per, n * per)
+    z = z.reshape(wl.N, wl.C, wl.D, wl.H, wl.W) if n_slices is None else z.reshape(n, wl.D, wl.H, wl.W)
+    out = {"z": z, "gamma": None, "beta": None}
+    if wl.has_affine:
+        out["gamma"] = normal(seed, STREAM_GAMMA, wl.W, 1.0, 0.1)
+        out["beta"] = normal(seed, STREAM_BETA, wl.W, 0.0, 0.1)
+    return out

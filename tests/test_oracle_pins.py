@@ -314,3 +314,62 @@ def test_oracle_rejects_invalid_shapes():
     with pytest.raises(ValueError):
         oracle.conv1d_norm(oracle.params(1, 1, 6, 8, 3, norm=1, groups=4), np.zeros((1, 1, 8), np.float32),
                            np.zeros((6, 1, 3), np.float32))
+
+
+# ------------------------------------------------------------------ [p4]'s LayerNorm(W) + AvgPool3d + GELU
+def _torch_ln_pool_gelu(z, eps, sw, ga, be):
+    t = torch.from_numpy(z).double() + float(np.float32(sw))
+    W = z.shape[-1]
+    t = F.layer_norm(t, (W,), None if ga is None else torch.from_numpy(ga).double(),
+                     None if be is None else torch.from_numpy(be).double(), eps=float(np.float32(eps)))
+    t = F.avg_pool3d(t, kernel_size=2)
+    return F.gelu(t, approximate="none").numpy()
+
+
+@pytest.mark.parametrize("shape,affine", [((2, 3, 4, 6, 64), True), ((1, 2, 5, 7, 10), True),
+                                          ((2, 1, 2, 2, 128), False), ((1, 1, 3, 3, 3), True)])
+def test_ln_avgpool3d_gelu_matches_torch_float64(shape, affine):
+    # [p4]'s second operator against the library composition in float64: layer_norm over the last
+    # dimension, avg_pool3d(kernel 2) (odd extents floor), exact GELU
+    rng = np.random.default_rng(11)
+    z = rng.normal(0.5, 2.0, size=shape).astype(np.float32)
+    W = shape[-1]
+    ga = rng.normal(1.0, 0.1, size=W).astype(np.float32) if affine else None
+    be = rng.normal(0.0, 0.1, size=W).astype(np.float32) if affine else None
+    got = oracle.ln_avgpool3d_gelu(z, 1e-5, 1.0, ga, be)
+    ref = _torch_ln_pool_gelu(z, 1e-5, 1.0, ga, be)
+    assert got.shape == ref.shape
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_ln_avgpool3d_gelu_closed_forms():
+    # rows constant along W: LayerNorm gives beta exactly, so every output is GELU of the mean of
+    # beta over its two columns
+    D, H, W = 4, 2, 8
+    be = np.arange(W, dtype=np.float32) / 8.0
+    z = np.broadcast_to(np.arange(D * H, dtype=np.float32).reshape(D, H, 1) * 3.0, (D, H, W)).copy()
+    got = oracle.ln_avgpool3d_gelu(z[None], 1e-5, 0.0, None, be)[0]
+    pair = (be[0::2].astype(np.float64) + be[1::2]) / 2.0
+    expect = 0.5 * pair * (1.0 + np.array([math.erf(v / math.sqrt(2.0)) for v in pair]))
+    for d2 in range(D // 2):
+        for h2 in range(H // 2):
+            np.testing.assert_allclose(got[d2, h2], expect, rtol=0, atol=1e-15)
+    # a ramp along W: mean (W-1)/2, population variance (W^2-1)/12, so window w' averages to
+    # (2w' + 1/2 - (W-1)/2) / sqrt(var + eps) whatever D and H
+    W = 16
+    ramp = np.broadcast_to(np.arange(W, dtype=np.float32), (2, 2, W)).copy()
+    eps = np.float32(1e-5)
+    got = oracle.ln_avgpool3d_gelu(ramp[None], float(eps), 0.0)[0][0, 0]
+    var = (W * W - 1) / 12.0
+    v = (2.0 * np.arange(W // 2) + 0.5 - (W - 1) / 2.0) / math.sqrt(var + float(eps))
+    expect = 0.5 * v * (1.0 + np.array([math.erf(x / math.sqrt(2.0)) for x in v]))
+    np.testing.assert_allclose(got, expect, rtol=0, atol=1e-14)
+
+
+def test_ln_avgpool3d_gelu_sum_weight_cancels():
+    # LayerNorm subtracts the row mean, so the scalar added before it cannot change the result
+    rng = np.random.default_rng(5)
+    z = rng.normal(size=(2, 4, 4, 32)).astype(np.float32)
+    a = oracle.ln_avgpool3d_gelu(z, 1e-5, 0.0)
+    b = oracle.ln_avgpool3d_gelu(z, 1e-5, 3.5)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
