@@ -105,6 +105,8 @@ class ClockSampler:
 def workload_by_name(name):
     if name in synth.BY_NAME:
         return synth.BY_NAME[name]
+    if name in ("ln_avgpool3d_gelu", synth.LN_AVGPOOL3D_GELU.name):
+        return synth.LN_AVGPOOL3D_GELU
     short = {"conv_gn": synth.CONV_GN, "conv_gn_tiny": synth.CONV_GN_TINY, "causal_conv": synth.CAUSAL_CONV,
              "linear_gn_rowmin": synth.LINEAR_GN_ROWMIN, "conv_ln_gelu_bf16": synth.CONV_LN_GELU_BF16,
              "causal_conv_gn32": synth.CAUSAL_CONV_GN32}
@@ -522,6 +524,133 @@ def read_traffic(workload, path):
     return None
 
 
+# ----------------------------------------------------------------- [p4]'s LayerNorm(W) + AvgPool3d + GELU
+
+def lnpool_config(wl, extra):
+    cfg = {"workload": wl.name, "z": [wl.N, wl.C, wl.D, wl.H, wl.W], "out": list(wl.out_shape), "eps": wl.eps,
+           "sum_weight": wl.sum_weight, "affine": wl.has_affine}
+    cfg.update(extra)
+    return cfg
+
+
+def lnpool_oracle_sample(wl, seconds):
+    """Time the oracle on a bounded number of (n, c) slices; GB/s of the operator's bytes."""
+    import oracle
+    per_slice = wl.algorithmic_bytes / (wl.N * wl.C)
+    n = 8
+    inp = synth.make_lnpool_inputs(wl, n_slices=n)
+    threads = oracle.default_threads()
+    run = lambda: oracle.ln_avgpool3d_gelu(inp["z"], wl.eps, wl.sum_weight, inp["gamma"], inp["beta"],
+                                           nthreads=threads)
+    run()
+    runs, t0 = 0, time.perf_counter()
+    while True:
+        run()
+        runs += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or runs >= 200:
+            break
+    return {"value": per_slice * n * runs / el / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{runs} run(s) on {n} of {wl.N * wl.C} (n, c) slices, {el:.1f} s wall"}
+
+
+def lnpool_arm(args, wl):
+    """The memory-bound pass on its own: GB/s of z read + output written (+ gamma / beta)."""
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            cpu = lnpool_oracle_sample(wl, seconds=max(1.0, args.cpu_seconds))
+            line = {"impl": "reference", "metric": "LayerNorm(W)+AvgPool3d+GELU GB/s", "value": cpu["value"],
+                    "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                    "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                    "dtype": "f64", "data": "synthetic", "config": lnpool_config(wl, {}), "cpu_baseline": cpu,
+                    "e2e": {"value": cpu["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            print(json.dumps(line), flush=True)
+        return
+    import torch
+    import gemm_groupnorm_accelerator_gb300 as c1n
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    c1n.load()
+    peaks = load_peaks()
+    inp = synth.make_lnpool_inputs(wl, n_slices=wl.N * wl.C, slice_offset=rank * wl.N * wl.C)
+    z = torch.from_numpy(inp["z"]).to(dev).view(wl.N, wl.C, wl.D, wl.H, wl.W)
+    ga = torch.from_numpy(inp["gamma"]).to(dev) if inp["gamma"] is not None else None
+    be = torch.from_numpy(inp["beta"]).to(dev) if inp["beta"] is not None else None
+    out = torch.empty(wl.out_shape, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = lambda i: c1n.ln_avgpool3d_gelu(z, wl.sum_weight, ga, be, eps=wl.eps, out=out)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    graphs = capture_graphs(step, 1, dev) if not args.eager else None
+    run_step = (lambda i: graphs[0].replay()) if graphs else step
+    for i in range(3):
+        run_step(i)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        run_step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if pg is not None:
+        pg.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = t0.elapsed_time(t1) / args.steps
+    if pg is not None:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t[0])
+    nbytes = wl.algorithmic_bytes
+    value = nbytes * world / (ms / 1e3) / 1e9
+    ach = nbytes / (ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+            "traffic": None, "peak_source": peaks["source"], "kernel": "ln_avgpool3d_gelu_kernel",
+            "kernel_ms": ms, "algorithmic_bytes": nbytes}
+    # end to end: z from pinned host memory in and the pooled output back, every step
+    zh = torch.from_numpy(inp["z"]).pin_memory()
+    oh = torch.empty(wl.out_shape, dtype=torch.float32).pin_memory()
+    e_steps = max(1, min(args.steps, 5))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e_steps):
+        z.view(-1).copy_(zh.view(-1), non_blocking=True)
+        step(i)
+        oh.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1) / e_steps
+    e2e = {"value": nbytes * world / (e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": zh.numel() * 4,
+           "d2h_bytes_per_step": oh.numel() * 4}
+    if rank == 0:
+        cpu = None if (world > 1 or args.no_cpu_baseline) else lnpool_oracle_sample(wl, seconds=args.cpu_seconds)
+        line = {"metric": "LayerNorm(W)+AvgPool3d+GELU GB/s", "value": value, "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": lnpool_config(wl, {"parallelism": f"dp{world}" if world > 1 else "single",
+                                             "l2": "working set larger than L2",
+                                             "launch": "cuda graph replay" if graphs else "eager"}),
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -540,7 +669,9 @@ def main():
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     wl = workload_by_name(args.workload)
-    if args.impl == "reference":
+    if isinstance(wl, synth.LnPoolWorkload):
+        lnpool_arm(args, wl)
+    elif args.impl == "reference":
         reference_arm(args, wl)
     else:
         our_arm(args, wl)

@@ -31,10 +31,15 @@ EXPORTED_SYMBOLS = (
     "conv1d_norm_desc_create", "conv1d_norm_workspace_size", "conv1d_norm_set_workspace", "conv1d_norm_plan_info",
     "conv1d_norm_run", "conv1d_norm_run_ex", "conv1d_norm_pack_weights", "conv1d_norm_check", "conv1d_norm_destroy",
     "conv1d_norm_status_string", "conv1d_norm_last_error", "conv1d_norm_version", "conv1d_norm_run_static_scratch",
-    "conv1d_norm_set_profiling", "conv1d_norm_kernel_times",
+    "conv1d_norm_set_profiling", "conv1d_norm_kernel_times", "ln_avgpool3d_gelu_run",
 )
 
 STATIC_SCRATCH_BYTES = 4 << 20  # C1N_STATIC_SCRATCH_BYTES
+
+
+class LnPoolParams(ctypes.Structure):
+    """c1n_lnpool_params: z [N][C][D][H][W] fp32 and the LayerNorm eps."""
+    _fields_ = [(n, ctypes.c_int32) for n in ("N", "C", "D", "H", "W")] + [("eps", ctypes.c_float)]
 
 
 class Params(ctypes.Structure):
@@ -114,6 +119,8 @@ def load(build_if_missing: bool = True):
         lib.conv1d_norm_last_error.argtypes = []
         lib.conv1d_norm_last_error.restype = ctypes.c_char_p
         lib.conv1d_norm_version.restype = ctypes.c_int32
+        lib.ln_avgpool3d_gelu_run.argtypes = [P(LnPoolParams), vp, ctypes.c_float, vp, vp, vp, vp]
+        lib.ln_avgpool3d_gelu_run.restype = ctypes.c_int
         for name in ("conv1d_norm_desc_create", "conv1d_norm_workspace_size", "conv1d_norm_set_workspace",
                      "conv1d_norm_plan_info", "conv1d_norm_run", "conv1d_norm_run_ex", "conv1d_norm_pack_weights",
                      "conv1d_norm_check", "conv1d_norm_run_static_scratch", "conv1d_norm_set_profiling",
@@ -177,6 +184,27 @@ def conv1d_norm_pack_weights(desc: int, w: int, workspace: Optional[int], worksp
 def conv1d_norm_run_static_scratch(desc: int, args: Args, stream: int) -> None:
     """Run without any allocation, using the library's fixed device scratch (see the C header)."""
     _check(load().conv1d_norm_run_static_scratch(desc, ctypes.byref(args), stream))
+
+
+def ln_avgpool3d_gelu_run(params: LnPoolParams, z: int, sum_weight: float, gamma: Optional[int], beta: Optional[int],
+                          out: int, stream: int) -> None:
+    """[p4]'s scalar add + LayerNorm(last dim) + AvgPool3d(2) + GELU pass (see the C header)."""
+    _check(load().ln_avgpool3d_gelu_run(ctypes.byref(params), z, sum_weight, gamma, beta, out, stream))
+
+
+def ln_avgpool3d_gelu(z, sum_weight: float, gamma=None, beta=None, eps: float = 1e-5, out=None):
+    """Torch convenience wrapper: z [N, C, D, H, W] float32 CUDA tensor (contiguous) -> a new (or the
+    given) [N, C, D//2, H//2, W//2] float32 tensor, computed on the current stream."""
+    import torch
+    if z.dim() != 5 or z.dtype != torch.float32 or not z.is_cuda or not z.is_contiguous():
+        raise ValueError("z must be a contiguous 5-D float32 CUDA tensor")
+    N, C, D, H, W = z.shape
+    if out is None:
+        out = torch.empty((N, C, D // 2, H // 2, W // 2), dtype=torch.float32, device=z.device)
+    p = LnPoolParams(N, C, D, H, W, eps)
+    ln_avgpool3d_gelu_run(p, z.data_ptr(), float(sum_weight), _ptr(gamma), _ptr(beta), out.data_ptr(),
+                          torch.cuda.current_stream(z.device).cuda_stream)
+    return out
 
 
 def conv1d_norm_check(desc: int, workspace: Optional[int], stream: int) -> None:

@@ -833,6 +833,27 @@ const char* conv1d_norm_status_string(c1n_status s) {
 
 const char* conv1d_norm_last_error(void) { return g_last_error.c_str(); }
 
-int32_t conv1d_norm_version(void) { return 110; }
+c1n_status ln_avgpool3d_gelu_run(const c1n_lnpool_params* p, const float* z, float sum_weight, const float* gamma,
+                                 const float* beta, float* out, c1n_stream_t stream) {
+    g_last_error.clear();
+    if (!p || !z || !out) return fail(C1N_ERR_INVALID_ARG, "params, z and out must be non-NULL");
+    if (p->N < 1 || p->C < 1 || p->D < 1 || p->H < 1 || p->W < 1)
+        return fail(C1N_ERR_INVALID_ARG, "N, C, D, H, W must be >= 1 (got %d, %d, %d, %d, %d)", p->N, p->C, p->D,
+                    p->H, p->W);
+    if (!(p->eps > 0.0f)) return fail(C1N_ERR_INVALID_ARG, "eps must be > 0");
+    if (p->W != 64 && p->W != 128 && p->W != 256 && p->W != 512)
+        return fail(C1N_ERR_UNSUPPORTED, "W = %d: the pass takes W = 64, 128, 256 or 512", p->W);
+    if (!aligned16(z) || !aligned16(out)) return fail(C1N_ERR_ALIGNMENT, "z and out must be 16-byte aligned");
+    if (p->D < 2 || p->H < 2) return C1N_OK;  // no pooling window: empty output
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    e = launch_ln_avgpool3d_gelu(*p, z, sum_weight, gamma, beta, out, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "LayerNorm + AvgPool3d + GELU launch");
+    return C1N_OK;
+}
+
+int32_t conv1d_norm_version(void) { return 111; }
 
 }  // extern "C"

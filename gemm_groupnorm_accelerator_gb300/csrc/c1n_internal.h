@@ -110,6 +110,11 @@ cudaError_t launch_rowmin_finish(const c1n_params& p, const Plan& pl, const floa
 cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream,
                                 unsigned* zero = nullptr, int nzero = 0);
 
+// [p4]'s LayerNorm(last dim) + AvgPool3d + GELU pass; p already validated (W in 64, 128, 256, 512).
+cudaError_t launch_ln_avgpool3d_gelu(const c1n_lnpool_params& p, const float* z, float sum_weight,
+                                     const float* gamma, const float* beta, float* out, int num_sms,
+                                     cudaStream_t stream);
+
 // Tensor-core kernels. `tm_a`: x (conv mode, staged time-contiguous boxes) or X (Linear mode);
 // `tm_b`: packed weights (conv mode) or W (Linear mode).
 // kEpiLNX: channel LayerNorm over the two channel halves held by the two CTAs of a cluster.

@@ -9,7 +9,8 @@
  *        channels of every row and a broadcast add of a per-channel bias.
  *   [p3] Kimi-K2.6 l1_p5 page — causal Conv1d: left padding (k-1)*dilation, tap 0 is the oldest
  *        input; the convolution viewed as a GEMM with M = N*T_out, N = C_out, K = C_in*k.
- *   [p4] Kimi-K2.6 l2_p3 page — LayerNorm with affine and the exact-erf GELU.
+ *   [p4] Kimi-K2.6 l2_p3 page — LayerNorm with affine and the exact-erf GELU; its scalar add,
+ *        LayerNorm over the last dimension, AvgPool3d and GELU (ln_avgpool3d_gelu_run below).
  *
  *   c[n][co][t] = b[co] + sum_ci sum_kk w[co][ci][kk] * x[n][ci][t*stride + kk*dilation - pad_left]
  *                 (x = 0 outside [0, T));  T_out = (T + pad_left + pad_right - dilation*(k-1) - 1)/stride + 1
@@ -222,6 +223,30 @@ typedef struct {
 } c1n_kernel_time;
 c1n_status conv1d_norm_set_profiling(c1n_desc* desc, int32_t enable);
 c1n_status conv1d_norm_kernel_times(c1n_desc* desc, c1n_kernel_time* out, int32_t capacity, int32_t* count);
+
+/* [p4]'s second operator (Kimi-K2.6 l2_p3 page, the model's steps after its ConvTranspose3d: a
+ * scalar added, LayerNorm over the last dimension, AvgPool3d with kernel 2, GELU):
+ *
+ *   s[n][c][d][h][w] = z[n][c][d][h][w] + sum_weight
+ *   l = (s - mean_w s) / sqrt(var_w s + eps) * gamma[w] + beta[w]   (statistics over the W values of
+ *        one (n, c, d, h) row, population variance)
+ *   out[n][c][d'][h'][w'] = GELU(mean of l over d in {2d', 2d'+1}, h in {2h', 2h'+1}, w in {2w', 2w'+1})
+ *
+ *   - z [N][C][D][H][W] fp32, out [N][C][D/2][H/2][W/2] fp32 (floor: a trailing odd plane, row or
+ *     column belongs to no window), both dense and 16-byte aligned, caller-owned, not overlapping.
+ *   - gamma, beta [W] fp32 or NULL (1 and 0).
+ *   - W must be 64, 128, 256 or 512 (a row is spread over the lanes of one warp or half-warp);
+ *     N, C, D, H >= 1; eps > 0. Otherwise C1N_ERR_INVALID_ARG (bad values) or C1N_ERR_UNSUPPORTED
+ *     (another W), and nothing is launched. D < 2 or H < 2 leaves an empty output (C1N_OK).
+ *   - One kernel on `stream`, asynchronous; no workspace, no allocation, no synchronisation.
+ *   - GELU and the statistics as in the fused operator; memory-bound: z is read once and the pooled
+ *     output written once. */
+typedef struct {
+    int32_t N, C, D, H, W;
+    float eps;
+} c1n_lnpool_params;
+c1n_status ln_avgpool3d_gelu_run(const c1n_lnpool_params* p, const float* z, float sum_weight, const float* gamma,
+                                 const float* beta, float* out, c1n_stream_t stream);
 
 /* Library version: major*10000 + minor*100 + patch. */
 int32_t conv1d_norm_version(void);

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def _declared_functions():
     src = open(os.path.join(ROOT, "include", "conv1d_norm.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(conv1d_norm_\w+)\s*\(", src)))
+    return sorted(set(re.findall(r"^(?:c1n_status|void|const char\*|int32_t)\s+(\w+)\s*\(", src, flags=re.M)))
 
 
 def test_library_exports_every_declared_symbol():
@@ -197,3 +197,24 @@ def test_profiling_toggle_without_a_run():
 def test_status_strings():
     for s in range(8):
         assert c1n.conv1d_norm_status_string(s)
+
+
+def test_ln_avgpool3d_gelu_validation_without_device():
+    # argument errors are reported before anything touches a device
+    z = ctypes.c_void_p(4096)  # never dereferenced: every call below fails validation first
+    ok = c1n.LnPoolParams(2, 3, 4, 4, 64, 1e-5)
+    cases = [
+        (c1n.LnPoolParams(0, 3, 4, 4, 64, 1e-5), z.value, z.value, c1n.ERR_INVALID_ARG),
+        (c1n.LnPoolParams(2, 3, 4, 4, 64, 0.0), z.value, z.value, c1n.ERR_INVALID_ARG),
+        (c1n.LnPoolParams(2, 3, 4, 4, 48, 1e-5), z.value, z.value, c1n.ERR_UNSUPPORTED),
+        (c1n.LnPoolParams(2, 3, 4, 4, 96, 1e-5), z.value, z.value, c1n.ERR_UNSUPPORTED),
+        (ok, None, z.value, c1n.ERR_INVALID_ARG),
+        (ok, z.value + 4, z.value, c1n.ERR_ALIGNMENT),
+        (ok, z.value, z.value + 8, c1n.ERR_ALIGNMENT),
+    ]
+    for p, zp, op, status in cases:
+        with pytest.raises(c1n.C1NError) as e:
+            c1n.ln_avgpool3d_gelu_run(p, zp, 1.0, None, None, op, 0)
+        assert e.value.status == status, (p.W, p.eps, status)
+    # no pooling window (D or H below 2): nothing to do, nothing launched
+    c1n.ln_avgpool3d_gelu_run(c1n.LnPoolParams(2, 3, 1, 4, 64, 1e-5), z.value, 1.0, None, None, z.value, 0)

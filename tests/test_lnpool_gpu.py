@@ -1,0 +1,75 @@
+"""GPU parity of [p4]'s second operator (scalar add, LayerNorm over the last dimension W, AvgPool3d
+2x2x2, exact GELU) through the C ABI against the CPU oracle on the same seeded inputs. fp32 CUDA-core
+arithmetic: max abs error 1e-4, the SIMT fp32 tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+
+SMALL = {
+    "w64": synth.LN_AVGPOOL3D_GELU.replace(N=2, C=3, D=6, H=8, W=64),
+    "w64_odd_dh": synth.LN_AVGPOOL3D_GELU.replace(N=2, C=2, D=5, H=7, W=64),
+    "w64_no_affine": synth.LN_AVGPOOL3D_GELU.replace(N=1, C=4, D=4, H=4, W=64, has_affine=False),
+    "w64_sum_weight": synth.LN_AVGPOOL3D_GELU.replace(N=1, C=2, D=4, H=6, W=64, sum_weight=-2.5),
+    "w128": synth.LN_AVGPOOL3D_GELU.replace(N=2, C=2, D=4, H=3, W=128),
+    "w256": synth.LN_AVGPOOL3D_GELU.replace(N=1, C=3, D=2, H=4, W=256),
+    "w512": synth.LN_AVGPOOL3D_GELU.replace(N=1, C=2, D=3, H=2, W=512),
+    "many_groups": synth.LN_AVGPOOL3D_GELU.replace(N=3, C=5, D=16, H=34, W=64),
+}
+
+
+def _run(c1n, wl, z):
+    zt = torch.from_numpy(np.ascontiguousarray(z)).cuda()
+    inp = synth.make_lnpool_inputs(wl.replace(N=1, C=1, D=2, H=2))  # gamma / beta only
+    ga = None if inp["gamma"] is None else torch.from_numpy(inp["gamma"]).cuda()
+    be = None if inp["beta"] is None else torch.from_numpy(inp["beta"]).cuda()
+    out = torch.full(wl.out_shape, float("nan"), dtype=torch.float32, device="cuda")
+    c1n.ln_avgpool3d_gelu(zt, wl.sum_weight, ga, be, eps=wl.eps, out=out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), inp["gamma"], inp["beta"]
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_shapes(cuda_lib, name):
+    wl = SMALL[name]
+    z = synth.make_lnpool_inputs(wl)["z"]
+    got, ga, be = _run(cuda_lib, wl, z)
+    ref = oracle.ln_avgpool3d_gelu(z, wl.eps, wl.sum_weight, ga, be)
+    assert np.all(np.isfinite(got)), "unwritten outputs"
+    err = float(np.max(np.abs(got.astype(np.float64) - ref)))
+    assert err <= TOL, f"{name}: max abs err {err:.3e}"
+
+
+def test_nothing_written_past_the_output(cuda_lib):
+    # the output sits inside a larger buffer whose tail must stay untouched
+    wl = SMALL["w64_odd_dh"]
+    z = torch.from_numpy(synth.make_lnpool_inputs(wl)["z"]).cuda()
+    n_out = int(np.prod(wl.out_shape))
+    buf = torch.full((n_out + 1024,), 7.0, dtype=torch.float32, device="cuda")
+    cuda_lib.ln_avgpool3d_gelu(z, wl.sum_weight, eps=wl.eps, out=buf[:n_out].view(wl.out_shape))
+    torch.cuda.synchronize()
+    assert torch.all(buf[n_out:] == 7.0)
+
+
+def test_full_size_sampled_slices(cuda_lib):
+    # [p4]'s shape, z [32, 64, 32, 64, 64] (1.07 GB), in the launch configuration the benchmark times;
+    # the oracle evaluates a few (n, c) slices one by one
+    wl = synth.LN_AVGPOOL3D_GELU
+    inp = synth.make_lnpool_inputs(wl)
+    z = torch.from_numpy(inp["z"]).cuda()
+    ga, be = torch.from_numpy(inp["gamma"]).cuda(), torch.from_numpy(inp["beta"]).cuda()
+    out = cuda_lib.ln_avgpool3d_gelu(z, wl.sum_weight, ga, be, eps=wl.eps)
+    torch.cuda.synchronize()
+    got = out.view(wl.N * wl.C, *wl.out_shape[2:]).cpu().numpy()
+    del z, out
+    for s in (0, 1, 777, wl.N * wl.C - 1):
+        zs = inp["z"].reshape(wl.N * wl.C, wl.D, wl.H, wl.W)[s:s + 1]
+        ref = oracle.ln_avgpool3d_gelu(zs, wl.eps, wl.sum_weight, inp["gamma"], inp["beta"])[0]
+        err = float(np.max(np.abs(got[s].astype(np.float64) - ref)))
+        assert err <= TOL, f"slice {s}: max abs err {err:.3e}"
