@@ -59,6 +59,7 @@ def _load():
             lib.oracle_rowmin_bias.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_long, f64p, f32p, f64p, i32p]
             lib.oracle_conv1d_norm.argtypes = [P(OracleParams), f32p, f32p, f32p, f32p, f32p, f32p, f64p, i32p,
                                                ctypes.c_int]
+            lib.oracle_conv_transpose3d.argtypes = [ctypes.c_int] * 10 + [f32p, f32p, f32p, f64p, ctypes.c_int]
             lib.oracle_ln_avgpool3d_gelu.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                                      ctypes.c_float, f32p, f32p, f32p, ctypes.c_int, f64p, ctypes.c_int]
             lib.oracle_conv1d_norm_samples.argtypes = [P(OracleParams), f32p, f32p, f32p, f32p, f32p, f32p, i32p,
@@ -213,3 +214,28 @@ def ln_avgpool3d_gelu(z: np.ndarray, eps: float, sum_weight: float, gamma=None, 
     if rc != 0:
         raise ValueError("oracle_ln_avgpool3d_gelu rejected its arguments")
     return out.reshape(*lead, D // 2, H // 2, W // 2)
+
+
+def conv_transpose3d_shape(D, H, W, k, stride, pad, out_pad):
+    f = lambda n: (n - 1) * stride - 2 * pad + (k - 1) + out_pad + 1
+    return f(D), f(H), f(W)
+
+
+def conv_transpose3d(x: np.ndarray, w: np.ndarray, b=None, stride: int = 1, pad: int = 0, out_pad: int = 0,
+                     nthreads: Optional[int] = None) -> np.ndarray:
+    """[p4]'s ConvTranspose3d: x [N][C_in][D][H][W], w [C_in][C_out][k][k][k] float32 -> float64 output."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, C_in, D, H, W = x.shape
+    _, C_out, k, _, _ = w.shape
+    Do, Ho, Wo = conv_transpose3d_shape(D, H, W, k, stride, pad, out_pad)
+    lib = _load()
+    out = np.empty((N, C_out, Do, Ho, Wo), dtype=np.float64)
+    bp = _f32(b)
+    rc = lib.oracle_conv_transpose3d(N, C_in, C_out, D, H, W, k, stride, pad, out_pad,
+                                     x.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                     w.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), bp[1],
+                                     out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_conv_transpose3d rejected its arguments")
+    return out

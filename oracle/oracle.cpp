@@ -242,6 +242,57 @@ int oracle_conv1d_norm_samples(const OracleParams* p, const float* x, const floa
     return 0;
 }
 
+// [p4]'s transposed 3-D convolution (ConvTranspose3d, dilation 1), the plain gather form of its
+// definition: output position o along each axis receives input i through tap k when
+// o = i*stride - pad + k, so
+//   y[n][co][od][oh][ow] = b[co] + sum_{ci, kd, kh, kw} x[n][ci][id][ih][iw] * w[ci][co][kd][kh][kw]
+// over the taps for which id = (od + pad - kd) / stride (and likewise ih, iw) is a whole number
+// inside the input. Output extent per axis: (in - 1)*stride - 2*pad + (k - 1) + output_pad + 1.
+// Layouts: x [N][C_in][D][H][W], w [C_in][C_out][k][k][k] (cubic kernel), b [C_out] or null,
+// y [N][C_out][Do][Ho][Wo] (double).
+int oracle_conv_transpose3d(int N, int C_in, int C_out, int D, int H, int W, int k, int stride, int pad,
+                            int out_pad, const float* x, const float* w, const float* b, double* y, int nthreads) {
+    if (N < 1 || C_in < 1 || C_out < 1 || D < 1 || H < 1 || W < 1 || k < 1 || stride < 1 || pad < 0 ||
+        out_pad < 0 || out_pad >= stride)
+        return -1;
+    const long Do = (long)(D - 1) * stride - 2 * pad + (k - 1) + out_pad + 1;
+    const long Ho = (long)(H - 1) * stride - 2 * pad + (k - 1) + out_pad + 1;
+    const long Wo = (long)(W - 1) * stride - 2 * pad + (k - 1) + out_pad + 1;
+    if (Do < 1 || Ho < 1 || Wo < 1) return -1;
+    // the input index of output o through tap kk, or -1 when there is none
+    auto in_of = [&](long o, long kk, long extent) -> long {
+        const long t = o + pad - kk;
+        if (t < 0 || t % stride != 0) return -1;
+        const long i = t / stride;
+        return i < extent ? i : -1;
+    };
+    parallel_for((long)N * C_out, nthreads, [&](long job) {
+        const long n = job / C_out, co = job % C_out;
+        for (long od = 0; od < Do; ++od)
+            for (long oh = 0; oh < Ho; ++oh)
+                for (long ow = 0; ow < Wo; ++ow) {
+                    double acc = b ? (double)b[co] : 0.0;
+                    for (long ci = 0; ci < C_in; ++ci)
+                        for (long kd = 0; kd < k; ++kd) {
+                            const long id = in_of(od, kd, D);
+                            if (id < 0) continue;
+                            for (long kh = 0; kh < k; ++kh) {
+                                const long ih = in_of(oh, kh, H);
+                                if (ih < 0) continue;
+                                for (long kw = 0; kw < k; ++kw) {
+                                    const long iw = in_of(ow, kw, W);
+                                    if (iw < 0) continue;
+                                    acc += (double)x[(((n * C_in + ci) * D + id) * H + ih) * W + iw] *
+                                           (double)w[(((ci * C_out + co) * k + kd) * k + kh) * k + kw];
+                                }
+                            }
+                        }
+                    y[(((n * C_out + co) * Do + od) * Ho + oh) * Wo + ow] = acc;
+                }
+    });
+    return 0;
+}
+
 // [p4]'s second operator, after its transposed convolution: add the scalar sum_weight, LayerNorm
 // over the last (contiguous) dimension W with per-position gamma[W] / beta[W] (population variance
 // in two passes, eps inside the square root), AvgPool3d with kernel 2 and stride 2 over (D, H, W)

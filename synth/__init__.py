@@ -278,3 +278,67 @@ def make_lnpool_inputs(wl: LnPoolWorkload, seed: int = 0, n_slices: Optional[int
         out["gamma"] = normal(seed, STREAM_GAMMA, wl.W, 1.0, 0.1)
         out["beta"] = normal(seed, STREAM_BETA, wl.W, 0.0, 0.1)
     return out
+
+
+@dataclasses.dataclass(frozen=True)
+class ConvT3dWorkload:
+    """[p4]'s ConvTranspose3d (cubic kernel, dilation 1, with bias) whose output feeds the
+    LayerNorm(W) + AvgPool3d + GELU pass."""
+
+    name: str
+    N: int
+    C_in: int
+    C_out: int
+    D: int
+    H: int
+    W: int
+    k: int = 3
+    stride: int = 2
+    pad: int = 1
+    out_pad: int = 1
+    description: str = ""
+
+    @property
+    def out_dhw(self):
+        f = lambda n: (n - 1) * self.stride - 2 * self.pad + (self.k - 1) + self.out_pad + 1
+        return f(self.D), f(self.H), f(self.W)
+
+    @property
+    def macs(self) -> int:
+        """Multiply-adds that meet an input voxel (taps that fall outside the input do not count)."""
+        total = 0
+        Do, Ho, Wo = self.out_dhw
+        per_axis = []
+        for n_in, n_out in ((self.D, Do), (self.H, Ho), (self.W, Wo)):
+            cnt = 0
+            for o in range(n_out):
+                for kk in range(self.k):
+                    t = o + self.pad - kk
+                    if t >= 0 and t % self.stride == 0 and t // self.stride < n_in:
+                        cnt += 1
+            per_axis.append(cnt)
+        total = per_axis[0] * per_axis[1] * per_axis[2]
+        return self.N * self.C_out * self.C_in * total
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.macs
+
+    def replace(self, **kw) -> "ConvT3dWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+CONV_TRANSPOSE3D = ConvT3dWorkload(
+    "conv_transpose3d_f32_n32_c32x64_d16_h32_w32_k3_s2", N=32, C_in=32, C_out=64, D=16, H=32, W=32,
+    description="ConvTranspose3d 32->64, k 3, stride 2, pad 1, output pad 1, fp32: x [32,32,16,32,32] -> [32,64,32,64,64]")
+
+
+def make_convt3d_inputs(wl: ConvT3dWorkload, seed: int = 0, n_rows: Optional[int] = None,
+                        row_offset: int = 0) -> Dict[str, np.ndarray]:
+    """x ~ N(0, 1); w, b ~ U(+-1/sqrt(C_in*k^3)). ``n_rows`` / ``row_offset`` draw batch entries only."""
+    n = wl.N if n_rows is None else n_rows
+    per = wl.C_in * wl.D * wl.H * wl.W
+    a = 1.0 / math.sqrt(wl.C_in * wl.k ** 3)
+    x = normal_slice(seed, STREAM_X, row_offset * per, n * per).reshape(n, wl.C_in, wl.D, wl.H, wl.W)
+    w = uniform_pm(seed, STREAM_W, wl.C_in * wl.C_out * wl.k ** 3, a).reshape(wl.C_in, wl.C_out, wl.k, wl.k, wl.k)
+    return {"x": x, "w": w, "b": uniform_pm(seed, STREAM_B, wl.C_out, a)}

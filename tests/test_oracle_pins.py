@@ -373,3 +373,42 @@ def test_ln_avgpool3d_gelu_sum_weight_cancels():
     a = oracle.ln_avgpool3d_gelu(z, 1e-5, 0.0)
     b = oracle.ln_avgpool3d_gelu(z, 1e-5, 3.5)
     np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------ [p4]'s ConvTranspose3d
+@pytest.mark.parametrize("shape", [(2, 3, 4, 3, 5, 4, 3, 2, 1, 1), (1, 2, 3, 3, 3, 2, 3, 1, 1, 0),
+                                   (1, 4, 2, 2, 4, 3, 2, 2, 0, 1), (2, 2, 3, 2, 2, 5, 3, 3, 1, 2)])
+def test_conv_transpose3d_matches_torch_float64(shape):
+    # the gather form of the definition against the library's transposed convolution in float64
+    N, Ci, Co, D, H, W, k, s, p, op = shape
+    rng = np.random.default_rng(17)
+    x = rng.normal(size=(N, Ci, D, H, W)).astype(np.float32)
+    w = rng.uniform(-0.3, 0.3, size=(Ci, Co, k, k, k)).astype(np.float32)
+    b = rng.uniform(-0.3, 0.3, size=Co).astype(np.float32)
+    got = oracle.conv_transpose3d(x, w, b, stride=s, pad=p, out_pad=op)
+    ref = F.conv_transpose3d(torch.from_numpy(x).double(), torch.from_numpy(w).double(), torch.from_numpy(b).double(),
+                             stride=s, padding=p, output_padding=op).numpy()
+    assert got.shape == ref.shape
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_conv_transpose3d_scatter_form_and_page_shape():
+    # the scatter form (every input voxel adds w * x at o = i*stride - pad + k, cropped), written
+    # independently of the gather loops, on integers so both are exact; and the page's shape
+    # arithmetic: x [.., 16, 32, 32], k 3, stride 2, pad 1, output pad 1 -> [.., 32, 64, 64]
+    assert oracle.conv_transpose3d_shape(16, 32, 32, 3, 2, 1, 1) == (32, 64, 64)
+    rng = np.random.default_rng(3)
+    N, Ci, Co, D, H, W, k, s, p, op = 1, 2, 3, 3, 2, 4, 3, 2, 1, 1
+    x = rng.integers(-3, 4, size=(N, Ci, D, H, W)).astype(np.float32)
+    w = rng.integers(-2, 3, size=(Ci, Co, k, k, k)).astype(np.float32)
+    Do, Ho, Wo = oracle.conv_transpose3d_shape(D, H, W, k, s, p, op)
+    full = np.zeros((N, Co, (D - 1) * s + k + op, (H - 1) * s + k + op, (W - 1) * s + k + op))
+    for n in range(N):
+        for ci in range(Ci):
+            for i in range(D):
+                for j in range(H):
+                    for l in range(W):
+                        full[n, :, i * s:i * s + k, j * s:j * s + k, l * s:l * s + k] += x[n, ci, i, j, l] * w[ci]
+    ref = full[:, :, p:p + Do, p:p + Ho, p:p + Wo]
+    got = oracle.conv_transpose3d(x, w, None, stride=s, pad=p, out_pad=op)
+    np.testing.assert_array_equal(got, ref)
