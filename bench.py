@@ -107,6 +107,8 @@ def workload_by_name(name):
         return synth.BY_NAME[name]
     if name in ("ln_avgpool3d_gelu", synth.LN_AVGPOOL3D_GELU.name):
         return synth.LN_AVGPOOL3D_GELU
+    if name in ("p4", "conv_transpose3d", synth.CONV_TRANSPOSE3D.name):
+        return synth.CONV_TRANSPOSE3D
     short = {"conv_gn": synth.CONV_GN, "conv_gn_tiny": synth.CONV_GN_TINY, "causal_conv": synth.CAUSAL_CONV,
              "linear_gn_rowmin": synth.LINEAR_GN_ROWMIN, "conv_ln_gelu_bf16": synth.CONV_LN_GELU_BF16,
              "causal_conv_gn32": synth.CAUSAL_CONV_GN32}
@@ -651,6 +653,132 @@ def lnpool_arm(args, wl):
         pg.destroy_process_group()
 
 
+FP32_FMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # 152 SMs x 128 fp32 lanes x FMA at 2.07 GHz
+
+
+def p4_arm(args, wl):
+    """[p4]'s model after its weights on one GPU: ConvTranspose3d (CUDA cores) then + scalar,
+    LayerNorm(W), AvgPool3d, GELU; TFLOP/s of the transposed convolution's useful multiply-adds."""
+    world, rank, local = dist_env()
+    lp = synth.LN_AVGPOOL3D_GELU
+    if args.impl == "reference":
+        if rank == 0:
+            import oracle
+            inp = synth.make_convt3d_inputs(wl, n_rows=1)
+            gb = synth.make_lnpool_inputs(lp.replace(N=1, C=1, D=2, H=2))
+            threads = oracle.default_threads()
+            t0 = time.perf_counter()
+            runs = 0
+            while True:
+                y = oracle.conv_transpose3d(inp["x"], inp["w"], inp["b"], stride=wl.stride, pad=wl.pad,
+                                            out_pad=wl.out_pad, nthreads=threads)
+                oracle.ln_avgpool3d_gelu(y[0].astype(np.float32), lp.eps, lp.sum_weight, gb["gamma"], gb["beta"],
+                                         nthreads=threads)
+                runs += 1
+                el = time.perf_counter() - t0
+                if el >= max(1.0, args.cpu_seconds) or runs >= 20:
+                    break
+            value = wl.flops / wl.N * runs / el / 1e12
+            cpu = {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": f"{runs} run(s) of the model on 1 of {wl.N} samples, {el:.1f} s wall"}
+            print(json.dumps({"impl": "reference", "metric": "p4 ConvTranspose3d+LayerNorm+AvgPool3d+GELU TFLOP/s",
+                              "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                              "warmup": args.warmup, "ms_per_step": el / runs * 1e3, "higher_is_better": True,
+                              "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                              "config": {"workload": wl.name}, "cpu_baseline": cpu,
+                              "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                                      "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    import torch
+    import gemm_groupnorm_accelerator_gb300 as c1n
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    c1n.load()
+    peaks = load_peaks()
+    inp = synth.make_convt3d_inputs(wl, n_rows=wl.N, row_offset=rank * wl.N)
+    gb = synth.make_lnpool_inputs(lp.replace(N=1, C=1, D=2, H=2))
+    x, w, b = (torch.from_numpy(inp[k]).to(dev) for k in ("x", "w", "b"))
+    ga, be = torch.from_numpy(gb["gamma"]).to(dev), torch.from_numpy(gb["beta"]).to(dev)
+    Do, Ho, Wo = wl.out_dhw
+    y = torch.empty((wl.N, wl.C_out, Do, Ho, Wo), dtype=torch.float32, device=dev)
+    out = torch.empty((wl.N, wl.C_out, Do // 2, Ho // 2, Wo // 2), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    convt = lambda i: c1n.conv_transpose3d(x, w, b, stride=wl.stride, pad=wl.pad, out_pad=wl.out_pad, out=y)
+    lnp = lambda i: c1n.ln_avgpool3d_gelu(y, lp.sum_weight, ga, be, eps=lp.eps, out=out)
+
+    def step(i):
+        convt(i)
+        lnp(i)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if pg is not None:
+        pg.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = t0.elapsed_time(t1) / args.steps
+    if pg is not None:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t[0])
+    convt_ms = time_replays(convt, 1, dev, args.steps, eager=True)
+    lnp_ms = time_replays(lnp, 1, dev, args.steps, eager=True)
+    value = wl.flops * world / (ms / 1e3) / 1e12
+    ach = wl.flops / (convt_ms / 1e3) / 1e12
+    roof = {"bound": "alu", "achieved": ach, "peak": FP32_FMA_PEAK_TFLOPS, "unit": "TFLOP/s",
+            "frac": ach / FP32_FMA_PEAK_TFLOPS, "traffic": None,
+            "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
+            "kernel": "conv_transpose3d_k3s2_kernel", "kernel_ms": convt_ms, "algorithmic_flops": wl.flops,
+            "kernels_ms": {"conv_transpose3d": convt_ms, "ln_avgpool3d_gelu": lnp_ms},
+            "ln_avgpool3d_gelu_hbm_frac": lp.algorithmic_bytes / (lnp_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+    xh = torch.from_numpy(inp["x"]).pin_memory()
+    oh = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    e_steps = max(1, min(args.steps, 5))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e_steps):
+        x.copy_(xh, non_blocking=True)
+        step(i)
+        oh.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1) / e_steps
+    e2e = {"value": wl.flops * world / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": xh.numel() * 4,
+           "d2h_bytes_per_step": oh.numel() * 4}
+    if rank == 0:
+        line = {"metric": "p4 ConvTranspose3d+LayerNorm+AvgPool3d+GELU TFLOP/s", "value": value, "unit": "TFLOP/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": wl.name, "x": [wl.N, wl.C_in, wl.D, wl.H, wl.W], "C_out": wl.C_out,
+                           "k": wl.k, "stride": wl.stride, "pad": wl.pad, "out_pad": wl.out_pad,
+                           "then": lp.name, "parallelism": f"dp{world}" if world > 1 else "single",
+                           "l2": "working set larger than L2", "launch": "eager, two kernels per step"},
+                "roofline": roof, "cpu_baseline": None, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -671,6 +799,8 @@ def main():
     wl = workload_by_name(args.workload)
     if isinstance(wl, synth.LnPoolWorkload):
         lnpool_arm(args, wl)
+    elif isinstance(wl, synth.ConvT3dWorkload):
+        p4_arm(args, wl)
     elif args.impl == "reference":
         reference_arm(args, wl)
     else:

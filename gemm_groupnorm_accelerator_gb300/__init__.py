@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "conv1d_norm_run", "conv1d_norm_run_ex", "conv1d_norm_pack_weights", "conv1d_norm_check", "conv1d_norm_destroy",
     "conv1d_norm_status_string", "conv1d_norm_last_error", "conv1d_norm_version", "conv1d_norm_run_static_scratch",
     "conv1d_norm_set_profiling", "conv1d_norm_kernel_times", "ln_avgpool3d_gelu_run",
+    "conv_transpose3d_run",
 )
 
 STATIC_SCRATCH_BYTES = 4 << 20  # C1N_STATIC_SCRATCH_BYTES
@@ -40,6 +41,11 @@ STATIC_SCRATCH_BYTES = 4 << 20  # C1N_STATIC_SCRATCH_BYTES
 class LnPoolParams(ctypes.Structure):
     """c1n_lnpool_params: z [N][C][D][H][W] fp32 and the LayerNorm eps."""
     _fields_ = [(n, ctypes.c_int32) for n in ("N", "C", "D", "H", "W")] + [("eps", ctypes.c_float)]
+
+
+class ConvT3dParams(ctypes.Structure):
+    """c1n_convt3d_params: x [N][C_in][D][H][W], cubic kernel k, stride, pad, output pad."""
+    _fields_ = [(n, ctypes.c_int32) for n in ("N", "C_in", "C_out", "D", "H", "W", "k", "stride", "pad", "out_pad")]
 
 
 class Params(ctypes.Structure):
@@ -121,6 +127,8 @@ def load(build_if_missing: bool = True):
         lib.conv1d_norm_version.restype = ctypes.c_int32
         lib.ln_avgpool3d_gelu_run.argtypes = [P(LnPoolParams), vp, ctypes.c_float, vp, vp, vp, vp]
         lib.ln_avgpool3d_gelu_run.restype = ctypes.c_int
+        lib.conv_transpose3d_run.argtypes = [P(ConvT3dParams), vp, vp, vp, vp, vp]
+        lib.conv_transpose3d_run.restype = ctypes.c_int
         for name in ("conv1d_norm_desc_create", "conv1d_norm_workspace_size", "conv1d_norm_set_workspace",
                      "conv1d_norm_plan_info", "conv1d_norm_run", "conv1d_norm_run_ex", "conv1d_norm_pack_weights",
                      "conv1d_norm_check", "conv1d_norm_run_static_scratch", "conv1d_norm_set_profiling",
@@ -204,6 +212,29 @@ def ln_avgpool3d_gelu(z, sum_weight: float, gamma=None, beta=None, eps: float = 
     p = LnPoolParams(N, C, D, H, W, eps)
     ln_avgpool3d_gelu_run(p, z.data_ptr(), float(sum_weight), _ptr(gamma), _ptr(beta), out.data_ptr(),
                           torch.cuda.current_stream(z.device).cuda_stream)
+    return out
+
+
+def conv_transpose3d_run(params: ConvT3dParams, x: int, w: int, b: Optional[int], y: int, stream: int) -> None:
+    """[p4]'s ConvTranspose3d (see the C header)."""
+    _check(load().conv_transpose3d_run(ctypes.byref(params), x, w, b, y, stream))
+
+
+def conv_transpose3d(x, w, b=None, stride: int = 2, pad: int = 1, out_pad: int = 1, out=None):
+    """Torch convenience wrapper: x [N, C_in, D, H, W], w [C_in, C_out, k, k, k] float32 CUDA tensors
+    (contiguous) -> a new (or the given) [N, C_out, Do, Ho, Wo] float32 tensor on the current stream."""
+    import torch
+    for t in (x, w):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("x and w must be contiguous float32 CUDA tensors")
+    N, C_in, D, H, W = x.shape
+    C_out, k = w.shape[1], w.shape[2]
+    f = lambda n: (n - 1) * stride - 2 * pad + (k - 1) + out_pad + 1
+    if out is None:
+        out = torch.empty((N, C_out, f(D), f(H), f(W)), dtype=torch.float32, device=x.device)
+    p = ConvT3dParams(N, C_in, C_out, D, H, W, k, stride, pad, out_pad)
+    conv_transpose3d_run(p, x.data_ptr(), w.data_ptr(), _ptr(b), out.data_ptr(),
+                         torch.cuda.current_stream(x.device).cuda_stream)
     return out
 
 

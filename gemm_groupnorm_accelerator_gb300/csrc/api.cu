@@ -854,6 +854,23 @@ c1n_status ln_avgpool3d_gelu_run(const c1n_lnpool_params* p, const float* z, flo
     return C1N_OK;
 }
 
-int32_t conv1d_norm_version(void) { return 111; }
+c1n_status conv_transpose3d_run(const c1n_convt3d_params* p, const float* x, const float* w, const float* b, float* y,
+                                c1n_stream_t stream) {
+    g_last_error.clear();
+    if (!p || !x || !w || !y) return fail(C1N_ERR_INVALID_ARG, "params, x, w and y must be non-NULL");
+    if (p->N < 1 || p->C_in < 1 || p->C_out < 1 || p->D < 1 || p->H < 1 || p->W < 1)
+        return fail(C1N_ERR_INVALID_ARG, "N, C_in, C_out, D, H, W must be >= 1");
+    if (p->k != 3 || p->stride != 2 || p->pad != 1 || (p->out_pad != 0 && p->out_pad != 1))
+        return fail(C1N_ERR_UNSUPPORTED, "ConvTranspose3d takes k = 3, stride 2, pad 1, output pad 0 or 1 "
+                                         "(got k %d, stride %d, pad %d, output pad %d)", p->k, p->stride, p->pad, p->out_pad);
+    if (p->C_out % 32 != 0) return fail(C1N_ERR_UNSUPPORTED, "C_out = %d: a multiple of 32 is taken", p->C_out);
+    if ((long long)p->D * 4 * (p->C_out / 32) > 65535 || p->N > 65535)
+        return fail(C1N_ERR_UNSUPPORTED, "grid too large (D * 4 * C_out / 32 and N must stay <= 65535)");
+    cudaError_t e = launch_conv_transpose3d(*p, x, w, b, y, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ConvTranspose3d launch");
+    return C1N_OK;
+}
+
+int32_t conv1d_norm_version(void) { return 112; }
 
 }  // extern "C"

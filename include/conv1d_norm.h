@@ -248,6 +248,24 @@ typedef struct {
 c1n_status ln_avgpool3d_gelu_run(const c1n_lnpool_params* p, const float* z, float sum_weight, const float* gamma,
                                  const float* beta, float* out, c1n_stream_t stream);
 
+/* [p4]'s transposed 3-D convolution (Kimi-K2.6 l2_p3 page, ConvTranspose3d with bias, dilation 1),
+ * whose output the pass above takes as z:
+ *
+ *   y[n][co][od][oh][ow] = b[co] + sum_{ci, kd, kh, kw} x[n][ci][id][ih][iw] * w[ci][co][kd][kh][kw]
+ *   over the taps with od = id*stride - pad + kd (likewise h, w) and the input index inside the input;
+ *   output extent per axis (in - 1)*stride - 2*pad + (k - 1) + out_pad + 1.
+ *
+ *   - x [N][C_in][D][H][W], w [C_in][C_out][k][k][k] (the library's transposed-convolution weight
+ *     layout), b [C_out] or NULL, y [N][C_out][Do][Ho][Wo]; fp32, dense, caller-owned.
+ *   - Taken: k = 3, stride = 2, pad = 1, out_pad 0 or 1, C_out a multiple of 32, all extents >= 1;
+ *     other values: C1N_ERR_UNSUPPORTED (or C1N_ERR_INVALID_ARG for non-positive extents).
+ *   - One kernel on `stream` (CUDA cores, fp32 FMA), asynchronous; no workspace, no allocation. */
+typedef struct {
+    int32_t N, C_in, C_out, D, H, W, k, stride, pad, out_pad;
+} c1n_convt3d_params;
+c1n_status conv_transpose3d_run(const c1n_convt3d_params* p, const float* x, const float* w, const float* b, float* y,
+                                c1n_stream_t stream);
+
 /* Library version: major*10000 + minor*100 + patch. */
 int32_t conv1d_norm_version(void);
 

@@ -218,3 +218,19 @@ def test_ln_avgpool3d_gelu_validation_without_device():
         assert e.value.status == status, (p.W, p.eps, status)
     # no pooling window (D or H below 2): nothing to do, nothing launched
     c1n.ln_avgpool3d_gelu_run(c1n.LnPoolParams(2, 3, 1, 4, 64, 1e-5), z.value, 1.0, None, None, z.value, 0)
+
+
+def test_conv_transpose3d_validation_without_device():
+    p = lambda **kw: c1n.ConvT3dParams(*[kw.get(k, v) for k, v in (("N", 2), ("C_in", 4), ("C_out", 64), ("D", 3),
+                                                                   ("H", 3), ("W", 3), ("k", 3), ("stride", 2),
+                                                                   ("pad", 1), ("out_pad", 1))])
+    x = ctypes.c_void_p(4096).value
+    for params, status in ((p(N=0), c1n.ERR_INVALID_ARG), (p(k=5), c1n.ERR_UNSUPPORTED), (p(stride=1), c1n.ERR_UNSUPPORTED),
+                           (p(pad=0), c1n.ERR_UNSUPPORTED), (p(out_pad=2), c1n.ERR_UNSUPPORTED),
+                           (p(C_out=48), c1n.ERR_UNSUPPORTED)):
+        with pytest.raises(c1n.C1NError) as e:
+            c1n.conv_transpose3d_run(params, x, x, None, x, 0)
+        assert e.value.status == status
+    with pytest.raises(c1n.C1NError) as e:
+        c1n.conv_transpose3d_run(p(), None, x, None, x, 0)
+    assert e.value.status == c1n.ERR_INVALID_ARG

@@ -73,3 +73,56 @@ def test_full_size_sampled_slices(cuda_lib):
         ref = oracle.ln_avgpool3d_gelu(zs, wl.eps, wl.sum_weight, inp["gamma"], inp["beta"])[0]
         err = float(np.max(np.abs(got[s].astype(np.float64) - ref)))
         assert err <= TOL, f"slice {s}: max abs err {err:.3e}"
+
+
+# ------------------------------------------------------------------ [p4]'s ConvTranspose3d
+CT_SMALL = {
+    "page_like": synth.CONV_TRANSPOSE3D.replace(N=2, C_in=8, D=3, H=5, W=6),
+    "out_pad0": synth.CONV_TRANSPOSE3D.replace(N=1, C_in=5, D=4, H=3, W=7, out_pad=0),
+    "wide": synth.CONV_TRANSPOSE3D.replace(N=1, C_in=4, C_out=96, D=2, H=9, W=40),
+    "one": synth.CONV_TRANSPOSE3D.replace(N=1, C_in=3, D=1, H=1, W=1),
+}
+
+
+def _convt_gpu(c1n, wl, inp):
+    x = torch.from_numpy(inp["x"]).cuda()
+    w = torch.from_numpy(inp["w"]).cuda()
+    b = torch.from_numpy(inp["b"]).cuda()
+    Do, Ho, Wo = wl.out_dhw
+    y = torch.full((x.shape[0], wl.C_out, Do, Ho, Wo), float("nan"), dtype=torch.float32, device="cuda")
+    c1n.conv_transpose3d(x, w, b, stride=wl.stride, pad=wl.pad, out_pad=wl.out_pad, out=y)
+    torch.cuda.synchronize()
+    return y
+
+
+@pytest.mark.parametrize("name", list(CT_SMALL))
+def test_conv_transpose3d_small(cuda_lib, name):
+    wl = CT_SMALL[name]
+    inp = synth.make_convt3d_inputs(wl)
+    got = _convt_gpu(cuda_lib, wl, inp).cpu().numpy()
+    ref = oracle.conv_transpose3d(inp["x"], inp["w"], inp["b"], stride=wl.stride, pad=wl.pad, out_pad=wl.out_pad)
+    assert np.all(np.isfinite(got)), "unwritten outputs"
+    err = float(np.max(np.abs(got.astype(np.float64) - ref)))
+    assert err <= TOL, f"{name}: max abs err {err:.3e}"
+
+
+def test_p4_pipeline_full_size_sampled(cuda_lib):
+    # the page's model after its weights: ConvTranspose3d on x [32, 32, 16, 32, 32], then + sum_weight,
+    # LayerNorm over W = 64, AvgPool3d 2x2x2, GELU -- at full size on the GPU, checked against the
+    # oracle composition on two samples
+    wl = synth.CONV_TRANSPOSE3D
+    inp = synth.make_convt3d_inputs(wl)
+    y = _convt_gpu(cuda_lib, wl, inp)
+    lp = synth.LN_AVGPOOL3D_GELU
+    gb = synth.make_lnpool_inputs(lp.replace(N=1, C=1, D=2, H=2))
+    ga, be = torch.from_numpy(gb["gamma"]).cuda(), torch.from_numpy(gb["beta"]).cuda()
+    out = cuda_lib.ln_avgpool3d_gelu(y, lp.sum_weight, ga, be, eps=lp.eps)
+    torch.cuda.synchronize()
+    for n in (0, wl.N - 1):
+        yn = oracle.conv_transpose3d(inp["x"][n:n + 1], inp["w"], inp["b"], stride=wl.stride, pad=wl.pad,
+                                     out_pad=wl.out_pad)
+        err_y = float(np.max(np.abs(y[n].cpu().numpy().astype(np.float64) - yn[0])))
+        assert err_y <= TOL, f"ConvTranspose3d sample {n}: max abs err {err_y:.3e}"
+        ref = oracle.ln_avgpool3d_gelu(yn[0].astype(np.float32), lp.eps, lp.sum_weight, gb["gamma"], gb["beta"])
+        err = float(np.max(np.abs(out[n].cpu().numpy().astype(np.float64) - ref)))
+        assert err <= TOL, f"pipeline sample {n}: max abs err {err:.3e}"
