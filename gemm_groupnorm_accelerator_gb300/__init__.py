@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = (
     "conv1d_norm_run", "conv1d_norm_run_ex", "conv1d_norm_pack_weights", "conv1d_norm_check", "conv1d_norm_destroy",
     "conv1d_norm_status_string", "conv1d_norm_last_error", "conv1d_norm_version", "conv1d_norm_run_static_scratch",
     "conv1d_norm_set_profiling", "conv1d_norm_kernel_times", "ln_avgpool3d_gelu_run",
-    "conv_transpose3d_run",
+    "conv_transpose3d_run", "conv_transpose3d_workspace_size",
 )
 
 STATIC_SCRATCH_BYTES = 4 << 20  # C1N_STATIC_SCRATCH_BYTES
@@ -45,7 +45,8 @@ class LnPoolParams(ctypes.Structure):
 
 class ConvT3dParams(ctypes.Structure):
     """c1n_convt3d_params: x [N][C_in][D][H][W], cubic kernel k, stride, pad, output pad."""
-    _fields_ = [(n, ctypes.c_int32) for n in ("N", "C_in", "C_out", "D", "H", "W", "k", "stride", "pad", "out_pad")]
+    _fields_ = [(n, ctypes.c_int32) for n in ("N", "C_in", "C_out", "D", "H", "W", "k", "stride", "pad", "out_pad",
+                                              "math")]
 
 
 class Params(ctypes.Structure):
@@ -127,8 +128,10 @@ def load(build_if_missing: bool = True):
         lib.conv1d_norm_version.restype = ctypes.c_int32
         lib.ln_avgpool3d_gelu_run.argtypes = [P(LnPoolParams), vp, ctypes.c_float, vp, vp, vp, vp]
         lib.ln_avgpool3d_gelu_run.restype = ctypes.c_int
-        lib.conv_transpose3d_run.argtypes = [P(ConvT3dParams), vp, vp, vp, vp, vp]
+        lib.conv_transpose3d_run.argtypes = [P(ConvT3dParams), vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         lib.conv_transpose3d_run.restype = ctypes.c_int
+        lib.conv_transpose3d_workspace_size.argtypes = [P(ConvT3dParams), P(ctypes.c_size_t)]
+        lib.conv_transpose3d_workspace_size.restype = ctypes.c_int
         for name in ("conv1d_norm_desc_create", "conv1d_norm_workspace_size", "conv1d_norm_set_workspace",
                      "conv1d_norm_plan_info", "conv1d_norm_run", "conv1d_norm_run_ex", "conv1d_norm_pack_weights",
                      "conv1d_norm_check", "conv1d_norm_run_static_scratch", "conv1d_norm_set_profiling",
@@ -215,14 +218,25 @@ def ln_avgpool3d_gelu(z, sum_weight: float, gamma=None, beta=None, eps: float = 
     return out
 
 
-def conv_transpose3d_run(params: ConvT3dParams, x: int, w: int, b: Optional[int], y: int, stream: int) -> None:
+def conv_transpose3d_workspace_size(params: ConvT3dParams) -> int:
+    """Workspace bytes of the chosen plan (0 for the CUDA-core plan)."""
+    n = ctypes.c_size_t(0)
+    _check(load().conv_transpose3d_workspace_size(ctypes.byref(params), ctypes.byref(n)))
+    return n.value
+
+
+def conv_transpose3d_run(params: ConvT3dParams, x: int, w: int, b: Optional[int], y: int, workspace: Optional[int],
+                         workspace_bytes: int, stream: int) -> None:
     """[p4]'s ConvTranspose3d (see the C header)."""
-    _check(load().conv_transpose3d_run(ctypes.byref(params), x, w, b, y, stream))
+    _check(load().conv_transpose3d_run(ctypes.byref(params), x, w, b, y, workspace, workspace_bytes, stream))
 
 
-def conv_transpose3d(x, w, b=None, stride: int = 2, pad: int = 1, out_pad: int = 1, out=None):
+def conv_transpose3d(x, w, b=None, stride: int = 2, pad: int = 1, out_pad: int = 1, out=None, math: int = 0,
+                     workspace=None):
     """Torch convenience wrapper: x [N, C_in, D, H, W], w [C_in, C_out, k, k, k] float32 CUDA tensors
-    (contiguous) -> a new (or the given) [N, C_out, Do, Ho, Wo] float32 tensor on the current stream."""
+    (contiguous) -> a new (or the given) [N, C_out, Do, Ho, Wo] float32 tensor on the current stream.
+    math: 0 auto, 1 CUDA cores, 2 tensor cores. The workspace (a uint8 CUDA tensor) is allocated here
+    when the plan needs one and none is given."""
     import torch
     for t in (x, w):
         if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
@@ -232,9 +246,12 @@ def conv_transpose3d(x, w, b=None, stride: int = 2, pad: int = 1, out_pad: int =
     f = lambda n: (n - 1) * stride - 2 * pad + (k - 1) + out_pad + 1
     if out is None:
         out = torch.empty((N, C_out, f(D), f(H), f(W)), dtype=torch.float32, device=x.device)
-    p = ConvT3dParams(N, C_in, C_out, D, H, W, k, stride, pad, out_pad)
+    p = ConvT3dParams(N, C_in, C_out, D, H, W, k, stride, pad, out_pad, math)
+    need = conv_transpose3d_workspace_size(p)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     conv_transpose3d_run(p, x.data_ptr(), w.data_ptr(), _ptr(b), out.data_ptr(),
-                         torch.cuda.current_stream(x.device).cuda_stream)
+                         workspace.data_ptr() if need else None, need, torch.cuda.current_stream(x.device).cuda_stream)
     return out
 
 

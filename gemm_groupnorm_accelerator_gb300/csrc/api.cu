@@ -660,6 +660,28 @@ namespace c1n {
 void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
 }  // namespace c1n
 
+namespace {
+// Validates p; *tc tells whether the tensor-core plan runs (math 0 picks it when it takes the shape).
+c1n_status convt3d_plan(const c1n_convt3d_params* p, bool* tc) {
+    if (!p) return fail(C1N_ERR_INVALID_ARG, "params must be non-NULL");
+    if (p->N < 1 || p->C_in < 1 || p->C_out < 1 || p->D < 1 || p->H < 1 || p->W < 1)
+        return fail(C1N_ERR_INVALID_ARG, "N, C_in, C_out, D, H, W must be >= 1");
+    if (p->math < 0 || p->math > 2) return fail(C1N_ERR_INVALID_ARG, "math must be 0, 1 or 2");
+    if (p->k != 3 || p->stride != 2 || p->pad != 1 || (p->out_pad != 0 && p->out_pad != 1))
+        return fail(C1N_ERR_UNSUPPORTED, "ConvTranspose3d takes k = 3, stride 2, pad 1, output pad 0 or 1 "
+                                         "(got k %d, stride %d, pad %d, output pad %d)", p->k, p->stride, p->pad, p->out_pad);
+    if (p->C_out % 32 != 0) return fail(C1N_ERR_UNSUPPORTED, "C_out = %d: a multiple of 32 is taken", p->C_out);
+    if ((long long)p->D * 4 * (p->C_out / 32) > 65535 || p->N > 65535)
+        return fail(C1N_ERR_UNSUPPORTED, "grid too large (D * 4 * C_out / 32 and N must stay <= 65535)");
+    const int Wo = 2 * p->W - 1 + p->out_pad;
+    const bool tc_ok = p->C_in == 32 && p->C_out == 64 && Wo % 4 == 0;
+    if (p->math == 2 && !tc_ok)
+        return fail(C1N_ERR_UNSUPPORTED, "the tensor-core plan takes C_in = 32, C_out = 64 and Wo a multiple of 4");
+    *tc = p->math == 2 || (p->math == 0 && tc_ok);
+    return C1N_OK;
+}
+}  // namespace
+
 extern "C" {
 
 c1n_status conv1d_norm_desc_create(const c1n_params* params, c1n_desc** out) {
@@ -854,23 +876,50 @@ c1n_status ln_avgpool3d_gelu_run(const c1n_lnpool_params* p, const float* z, flo
     return C1N_OK;
 }
 
-c1n_status conv_transpose3d_run(const c1n_convt3d_params* p, const float* x, const float* w, const float* b, float* y,
-                                c1n_stream_t stream) {
+
+c1n_status conv_transpose3d_workspace_size(const c1n_convt3d_params* p, size_t* bytes) {
     g_last_error.clear();
-    if (!p || !x || !w || !y) return fail(C1N_ERR_INVALID_ARG, "params, x, w and y must be non-NULL");
-    if (p->N < 1 || p->C_in < 1 || p->C_out < 1 || p->D < 1 || p->H < 1 || p->W < 1)
-        return fail(C1N_ERR_INVALID_ARG, "N, C_in, C_out, D, H, W must be >= 1");
-    if (p->k != 3 || p->stride != 2 || p->pad != 1 || (p->out_pad != 0 && p->out_pad != 1))
-        return fail(C1N_ERR_UNSUPPORTED, "ConvTranspose3d takes k = 3, stride 2, pad 1, output pad 0 or 1 "
-                                         "(got k %d, stride %d, pad %d, output pad %d)", p->k, p->stride, p->pad, p->out_pad);
-    if (p->C_out % 32 != 0) return fail(C1N_ERR_UNSUPPORTED, "C_out = %d: a multiple of 32 is taken", p->C_out);
-    if ((long long)p->D * 4 * (p->C_out / 32) > 65535 || p->N > 65535)
-        return fail(C1N_ERR_UNSUPPORTED, "grid too large (D * 4 * C_out / 32 and N must stay <= 65535)");
-    cudaError_t e = launch_conv_transpose3d(*p, x, w, b, y, reinterpret_cast<cudaStream_t>(stream));
+    if (!bytes) return fail(C1N_ERR_INVALID_ARG, "bytes must be non-NULL");
+    bool tc = false;
+    c1n_status st = convt3d_plan(p, &tc);
+    if (st != C1N_OK) return st;
+    *bytes = tc ? convt3d_tc_workspace_bytes(*p) : 0;
+    return C1N_OK;
+}
+
+c1n_status conv_transpose3d_run(const c1n_convt3d_params* p, const float* x, const float* w, const float* b, float* y,
+                                void* workspace, size_t workspace_bytes, c1n_stream_t stream) {
+    g_last_error.clear();
+    bool tc = false;
+    c1n_status st = convt3d_plan(p, &tc);
+    if (st != C1N_OK) return st;
+    if (!x || !w || !y) return fail(C1N_ERR_INVALID_ARG, "x, w and y must be non-NULL");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (tc) {
+        const size_t need = convt3d_tc_workspace_bytes(*p);
+        if (!workspace || workspace_bytes < need)
+            return fail(C1N_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? workspace_bytes : 0);
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return fail(C1N_ERR_ALIGNMENT, "workspace not 256-byte aligned");
+        if (!aligned16(x) || !aligned16(y)) return fail(C1N_ERR_ALIGNMENT, "x and y must be 16-byte aligned");
+        int dev = 0, sms = 0, major = 0, minor = 0;
+        e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "device query");
+        if (!(major == 10 && minor == 3))
+            return fail(C1N_ERR_UNSUPPORTED, "the tensor-core plan is built for sm_103a; device is sm_%d%d", major, minor);
+        e = launch_conv_transpose3d_tc(*p, x, w, b, y, workspace, sms, s);
+        if (e != cudaSuccess) return cuda_fail(e, "ConvTranspose3d (tensor cores) launch");
+        return C1N_OK;
+    }
+    e = launch_conv_transpose3d(*p, x, w, b, y, s);
     if (e != cudaSuccess) return cuda_fail(e, "ConvTranspose3d launch");
     return C1N_OK;
 }
 
-int32_t conv1d_norm_version(void) { return 112; }
+int32_t conv1d_norm_version(void) { return 113; }
 
 }  // extern "C"

@@ -115,9 +115,13 @@ cudaError_t launch_ln_avgpool3d_gelu(const c1n_lnpool_params& p, const float* z,
                                      const float* gamma, const float* beta, float* out, int num_sms,
                                      cudaStream_t stream);
 
-// [p4]'s ConvTranspose3d (k 3, stride 2, pad 1; p already validated).
+// [p4]'s ConvTranspose3d (k 3, stride 2, pad 1; p already validated): CUDA-core kernel, and the
+// tensor-core plan (C_in 32, C_out 64) with its workspace (status word, channels-last x, packed weights).
 cudaError_t launch_conv_transpose3d(const c1n_convt3d_params& p, const float* x, const float* w, const float* b,
                                     float* y, cudaStream_t stream);
+size_t convt3d_tc_workspace_bytes(const c1n_convt3d_params& p);
+cudaError_t launch_conv_transpose3d_tc(const c1n_convt3d_params& p, const float* x, const float* w, const float* b,
+                                       float* y, void* workspace, int num_sms, cudaStream_t stream);
 
 // Tensor-core kernels. `tm_a`: x (conv mode, staged time-contiguous boxes) or X (Linear mode);
 // `tm_b`: packed weights (conv mode) or W (Linear mode).

@@ -259,12 +259,19 @@ c1n_status ln_avgpool3d_gelu_run(const c1n_lnpool_params* p, const float* z, flo
  *     layout), b [C_out] or NULL, y [N][C_out][Do][Ho][Wo]; fp32, dense, caller-owned.
  *   - Taken: k = 3, stride = 2, pad = 1, out_pad 0 or 1, C_out a multiple of 32, all extents >= 1;
  *     other values: C1N_ERR_UNSUPPORTED (or C1N_ERR_INVALID_ARG for non-positive extents).
- *   - One kernel on `stream` (CUDA cores, fp32 FMA), asynchronous; no workspace, no allocation. */
+ *   - math: 0 auto, 1 CUDA cores (fp32 FMA), 2 tensor cores (TF32 operands, fp32 accumulation; takes
+ *     C_in = 32, C_out = 64, Wo a multiple of 4, x and y 16-byte aligned, an sm_103a device —
+ *     C1N_ERR_UNSUPPORTED otherwise). Auto picks the tensor cores when they take the shape.
+ *   - The tensor-core plan needs a workspace (channels-last x, packed weights, a status word) of
+ *     conv_transpose3d_workspace_size() bytes, 256-byte aligned, caller-owned; the CUDA-core plan
+ *     needs none (0 bytes; workspace may be NULL). Asynchronous on `stream`; no allocation. */
 typedef struct {
     int32_t N, C_in, C_out, D, H, W, k, stride, pad, out_pad;
+    int32_t math;
 } c1n_convt3d_params;
+c1n_status conv_transpose3d_workspace_size(const c1n_convt3d_params* p, size_t* bytes);
 c1n_status conv_transpose3d_run(const c1n_convt3d_params* p, const float* x, const float* w, const float* b, float* y,
-                                c1n_stream_t stream);
+                                void* workspace, size_t workspace_bytes, c1n_stream_t stream);
 
 /* Library version: major*10000 + minor*100 + patch. */
 int32_t conv1d_norm_version(void);

@@ -223,14 +223,24 @@ def test_ln_avgpool3d_gelu_validation_without_device():
 def test_conv_transpose3d_validation_without_device():
     p = lambda **kw: c1n.ConvT3dParams(*[kw.get(k, v) for k, v in (("N", 2), ("C_in", 4), ("C_out", 64), ("D", 3),
                                                                    ("H", 3), ("W", 3), ("k", 3), ("stride", 2),
-                                                                   ("pad", 1), ("out_pad", 1))])
+                                                                   ("pad", 1), ("out_pad", 1), ("math", 0))])
     x = ctypes.c_void_p(4096).value
     for params, status in ((p(N=0), c1n.ERR_INVALID_ARG), (p(k=5), c1n.ERR_UNSUPPORTED), (p(stride=1), c1n.ERR_UNSUPPORTED),
                            (p(pad=0), c1n.ERR_UNSUPPORTED), (p(out_pad=2), c1n.ERR_UNSUPPORTED),
                            (p(C_out=48), c1n.ERR_UNSUPPORTED)):
         with pytest.raises(c1n.C1NError) as e:
-            c1n.conv_transpose3d_run(params, x, x, None, x, 0)
+            c1n.conv_transpose3d_run(params, x, x, None, x, None, 0, 0)
         assert e.value.status == status
     with pytest.raises(c1n.C1NError) as e:
-        c1n.conv_transpose3d_run(p(), None, x, None, x, 0)
+        c1n.conv_transpose3d_run(p(), None, x, None, x, None, 0, 0)
     assert e.value.status == c1n.ERR_INVALID_ARG
+    # plan choice: the tensor cores take C_in 32 / C_out 64 (and need a workspace), else CUDA cores
+    assert c1n.conv_transpose3d_workspace_size(p(C_in=32, W=32)) > 0
+    assert c1n.conv_transpose3d_workspace_size(p(C_in=16)) == 0
+    assert c1n.conv_transpose3d_workspace_size(p(C_in=32, W=32, math=1)) == 0
+    with pytest.raises(c1n.C1NError) as e:
+        c1n.conv_transpose3d_workspace_size(p(C_in=16, math=2))
+    assert e.value.status == c1n.ERR_UNSUPPORTED
+    with pytest.raises(c1n.C1NError) as e:  # the tensor-core plan without its workspace
+        c1n.conv_transpose3d_run(p(C_in=32, W=32), x, x, None, x, None, 0, 0)
+    assert e.value.status == c1n.ERR_WORKSPACE
