@@ -426,7 +426,8 @@ def kernel_times(op, step, i0, dev, n=5, graphs=True):
 def normalize_pass_roofline(wl, kern, peaks):
     """GB/s of the memory-bound passes of a two-pass plan: statistics (read the fp32 raw tile) and
     normalize (read raw + write y), against the measured HBM copy bandwidth; None when the plan
-    fuses normalization into the conv kernel."""
+    fuses normalization into the conv kernel. When the conv epilogue writes partial statistics, the
+    statistics pass is a small merge of those partials (its time only)."""
     y_elems = wl.N * wl.C_out * wl.T_out
     out = {}
     for name, nbytes in (("gn_stats", 4 * y_elems), ("ln_stats", 4 * y_elems),
@@ -434,6 +435,9 @@ def normalize_pass_roofline(wl, kern, peaks):
         if name in kern and kern[name] > 0:
             gbs = nbytes / (kern[name] / 1e3) / 1e9
             out[name] = {"ms": kern[name], "bytes": nbytes, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"]}
+    for name in ("gn_merge", "ln_merge"):
+        if name in kern and kern[name] > 0:
+            out[name] = {"ms": kern[name]}
     return out or None
 
 
@@ -513,13 +517,14 @@ def aggregate(ms_per_rank, flops_per_rank, world):
 
 def read_traffic(workload, path):
     """DRAM bytes per launch of the main kernel from a committed ncu summary, if it was taken on the
-    current kernel sources; None otherwise."""
+    current sources of that kernel (its .cu file and the shared headers); None otherwise."""
     try:
         from gemm_groupnorm_accelerator_gb300 import _build_lib
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
         rec = d.get(workload)
-        if rec and rec.get("source_fingerprint") == _build_lib._fingerprint() and rec.get("path") == path:
+        if rec and rec.get("path") == path and \
+                rec.get("source_fingerprint") == _build_lib.kernel_fingerprint(rec.get("source_file", "")):
             return rec["dram_bytes_per_launch"]
     except Exception:
         pass
@@ -657,8 +662,9 @@ FP32_FMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # 152 SMs x 128 fp32 lanes
 
 
 def p4_arm(args, wl):
-    """[p4]'s model after its weights on one GPU: ConvTranspose3d (CUDA cores) then + scalar,
-    LayerNorm(W), AvgPool3d, GELU; TFLOP/s of the transposed convolution's useful multiply-adds."""
+    """[p4]'s model after its weights on one GPU: ConvTranspose3d (tensor cores unless --math 1
+    asks for the CUDA cores) then + scalar, LayerNorm(W), AvgPool3d, GELU; TFLOP/s of the transposed
+    convolution's useful multiply-adds."""
     world, rank, local = dist_env()
     lp = synth.LN_AVGPOOL3D_GELU
     if args.impl == "reference":
@@ -710,7 +716,13 @@ def p4_arm(args, wl):
     y = torch.empty((wl.N, wl.C_out, Do, Ho, Wo), dtype=torch.float32, device=dev)
     out = torch.empty((wl.N, wl.C_out, Do // 2, Ho // 2, Wo // 2), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    convt = lambda i: c1n.conv_transpose3d(x, w, b, stride=wl.stride, pad=wl.pad, out_pad=wl.out_pad, out=y)
+    math = args.math if args.math in (1, 2) else 0
+    cp = c1n.ConvT3dParams(wl.N, wl.C_in, wl.C_out, wl.D, wl.H, wl.W, wl.k, wl.stride, wl.pad, wl.out_pad, math)
+    ws_bytes = c1n.conv_transpose3d_workspace_size(cp)
+    tensor_plan = ws_bytes > 0  # only the tensor-core plan takes a workspace
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    convt = lambda i: c1n.conv_transpose3d(x, w, b, stride=wl.stride, pad=wl.pad, out_pad=wl.out_pad, out=y,
+                                           math=math, workspace=ws)
     lnp = lambda i: c1n.ln_avgpool3d_gelu(y, lp.sum_weight, ga, be, eps=lp.eps, out=out)
 
     def step(i):
@@ -744,12 +756,25 @@ def p4_arm(args, wl):
     lnp_ms = time_replays(lnp, 1, dev, args.steps, eager=True)
     value = wl.flops * world / (ms / 1e3) / 1e12
     ach = wl.flops / (convt_ms / 1e3) / 1e12
-    roof = {"bound": "alu", "achieved": ach, "peak": FP32_FMA_PEAK_TFLOPS, "unit": "TFLOP/s",
-            "frac": ach / FP32_FMA_PEAK_TFLOPS, "traffic": None,
-            "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
-            "kernel": "conv_transpose3d_k3s2_kernel", "kernel_ms": convt_ms, "algorithmic_flops": wl.flops,
-            "kernels_ms": {"conv_transpose3d": convt_ms, "ln_avgpool3d_gelu": lnp_ms},
-            "ln_avgpool3d_gelu_hbm_frac": lp.algorithmic_bytes / (lnp_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+    common = {"kernels_ms": {"conv_transpose3d": convt_ms, "ln_avgpool3d_gelu": lnp_ms},
+              "ln_avgpool3d_gelu_hbm_frac": lp.algorithmic_bytes / (lnp_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+    if tensor_plan:
+        # Writing y (8x the input voxels, 64 channels) outweighs the contraction on this shape: the
+        # operator is bound by HBM. Bytes = x + w + b read once, y written once; the time is the
+        # whole operator (channels-last copy of x, weight pack, convt3d_tc_kernel).
+        gbs = wl.algorithmic_bytes / (convt_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"], "traffic": read_traffic(wl.name, "convt3d_tc"),
+                "peak_source": peaks.get("source", "MEASURED_PEAKS.json"),
+                "kernel": "convt3d_tc_kernel (timed with its channels-last copy and weight pack)",
+                "kernel_ms": convt_ms, "algorithmic_bytes": wl.algorithmic_bytes, "useful_tflops": ach,
+                "useful_tflops_frac_of_tf32": ach / (peaks["bf16_tflops"] * TF32_PER_BF16), **common}
+    else:
+        roof = {"bound": "alu", "achieved": ach, "peak": FP32_FMA_PEAK_TFLOPS, "unit": "TFLOP/s",
+                "frac": ach / FP32_FMA_PEAK_TFLOPS, "traffic": None,
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
+                "kernel": "conv_transpose3d_k3s2_kernel", "kernel_ms": convt_ms, "algorithmic_flops": wl.flops,
+                **common}
     xh = torch.from_numpy(inp["x"]).pin_memory()
     oh = torch.empty(out.shape, dtype=torch.float32).pin_memory()
     e_steps = max(1, min(args.steps, 5))
@@ -772,8 +797,11 @@ def p4_arm(args, wl):
                 "config": {"workload": wl.name, "x": [wl.N, wl.C_in, wl.D, wl.H, wl.W], "C_out": wl.C_out,
                            "k": wl.k, "stride": wl.stride, "pad": wl.pad, "out_pad": wl.out_pad,
                            "then": lp.name, "parallelism": f"dp{world}" if world > 1 else "single",
-                           "l2": "working set larger than L2", "launch": "eager, two kernels per step"},
-                "roofline": roof, "cpu_baseline": None, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks}
+                           "math": "tensor (tf32)" if tensor_plan else "cuda cores (fp32 fma)",
+                           "l2": "working set larger than L2",
+                           "launch": f"eager, {4 if tensor_plan else 2} kernels per step"},
+                "roofline": roof, "cpu_baseline": None, "e2e": e2e,
+                "gpu_launches": (4 if tensor_plan else 2) * args.steps, "clocks": clocks}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()

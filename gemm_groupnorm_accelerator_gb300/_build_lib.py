@@ -36,10 +36,20 @@ def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _fingerprint() -> str:
+def _headers():
+    return sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))) + \
+        [os.path.join(INCLUDE, "conv1d_norm.h")]
+
+
+def kernel_fingerprint(source: str) -> str:
+    """Hash of one translation unit (a csrc/*.cu file name), every header and the flags: a profile
+    of a kernel defined in that file stays valid while this does not change."""
+    return _fingerprint([os.path.join(CSRC, source)])
+
+
+def _fingerprint(sources=None) -> str:
     h = hashlib.sha256()
-    for f in _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))) + \
-            [os.path.join(INCLUDE, "conv1d_norm.h")]:
+    for f in (_sources() if sources is None else sources) + _headers():
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode())
             h.update(fh.read())

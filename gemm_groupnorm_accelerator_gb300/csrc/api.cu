@@ -350,6 +350,22 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
                     const bool need_stats = p.norm != C1N_NORM_NONE;
                     const bool need_raw = out_needs_second_pass && pl.bf16;
                     plan_workspace(p, pl, true, need_raw, need_stats);
+                    // The conv epilogue writes partial statistics with the raw tiles (GroupNorm:
+                    // when no group straddles a channel block), so no pass re-reads the raw output
+                    // for them; a small kernel merges the partials.
+                    size_t n_part = 0;
+                    if (p.norm == C1N_NORM_GROUP && (pl.n_cb == 1 || pl.BN % (p.C_out / p.groups) == 0)) {
+                        pl.part_kind = 1;
+                        pl.part_tiles = (int)ceil_div(pl.T_out, 128);
+                        n_part = (size_t)p.N * p.groups * pl.part_tiles;
+                    } else if (p.norm == C1N_NORM_CHANNEL_LAYER) {
+                        pl.part_kind = 2;
+                        n_part = (size_t)p.N * pl.n_cb * pl.T_out;
+                    }
+                    if (n_part) {
+                        pl.ws_part = pl.ws_total;
+                        pl.ws_total = round_up(pl.ws_part + n_part * sizeof(float2), 256);
+                    }
                     pl.kernels = 2 + (need_stats ? 1 : 0) + (p.post == C1N_POST_ROWMIN_BIAS ? 2 : 1);
                     return C1N_OK;
                 }
@@ -595,6 +611,9 @@ c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         t.row_cpg = (pl.row_epilogue && p.norm == C1N_NORM_GROUP) ? p.C_out / p.groups : 0;
         t.rowmin = (pl.row_epilogue && p.post == C1N_POST_ROWMIN_BIAS) ? 1 : 0;
         t.rowpart = reinterpret_cast<float2*>(wsb + pl.ws_rowpart);
+        t.part_kind = pl.part_kind;
+        t.part_tiles = pl.part_tiles;
+        t.part = reinterpret_cast<float2*>(wsb + pl.ws_part);
         t.eps = p.eps;
         const bool fused_ln = pl.path == C1N_PATH_TC_FUSED_LN;
         // GELU in the kernel whenever no later pass sees the values (the normalize pass applies it
@@ -614,6 +633,7 @@ c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         int epi = kEpiDirect;
         if (fused_ln) epi = pl.cluster == 2 ? kEpiLNX : kEpiLN;
         if (pl.row_epilogue) epi = kEpiRowGN;
+        if (pl.part_kind) epi = kEpiDirectStats;
         if (fused_gn) {
             // Cooperative grid when every CTA fits on the device at once (one per SM), else a cluster.
             const bool grid_fits = pl.path == C1N_PATH_TC_FUSED_GN && pl.n_units <= d->num_sms;
@@ -633,7 +653,12 @@ c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         if (fused_out) return C1N_OK;
     }
     if (!second) return C1N_OK;
-    if (need_stats) {
+    if (need_stats && pl.part_kind) {
+        const float2* part = reinterpret_cast<const float2*>(wsb + pl.ws_part);
+        mark(d, s, pl.part_kind == 1 ? "gn_merge" : "ln_merge");
+        e = pl.part_kind == 1 ? launch_gn_merge(p, pl, part, stats, s) : launch_ln_merge(p, pl, part, stats, s);
+        if (e != cudaSuccess) return cuda_fail(e, "statistics merge launch");
+    } else if (need_stats) {
         mark(d, s, p.norm == C1N_NORM_GROUP ? "gn_stats" : "ln_stats");
         e = p.norm == C1N_NORM_GROUP ? launch_gn_stats(p, pl, raw, stats, s) : launch_ln_stats(p, pl, raw, stats, s);
         if (e != cudaSuccess) return cuda_fail(e, "statistics launch");

@@ -48,6 +48,9 @@ struct Plan {
     size_t ws_gx = 0;                   // fused GroupNorm across a cooperative grid: exchange words
     size_t ws_rowpart = 0;              // fused row-min partials
     int row_epilogue = 0;               // Linear plan with the fused row epilogue
+    size_t ws_part = 0;                 // two-pass plan: partial statistics from the conv epilogue
+    int part_kind = 0;                  // 0: statistics pass over the raw output; 1 / 2: see TcArgs
+    int part_tiles = 0;                 // 128-row tiles along T_out
     int gx_words = 0;   // 32-bit words of the exchange area (zeroed by the weight pack)
     int gstride = 0;    // groups per channel block (exchange words per tile / 2)
 };
@@ -84,6 +87,13 @@ struct TcArgs {
     int row_cpg;       // row epilogue: GroupNorm over runs of row_cpg channels (8, 16, 32; 0 = none)
     int rowmin;        // row epilogue: keep (min, argmin) per row instead of storing y
     float2* rowpart;   // row epilogue: per (row, channel block) minimum and its channel (int bits)
+    // Two-pass plans (kEpiDirectStats): the epilogue stores the raw tile and its partial statistics
+    // (mean, M2) about the partial's own mean. GroupNorm (part_kind 1): per (sample, group, 128-row
+    // tile), at part[(n * groups + g) * part_tiles + row0 / 128]; channel LayerNorm (part_kind 2):
+    // per (sample, channel block, time step), at part[(n * n_cb + cb) * T_out + t].
+    int part_kind;
+    int part_tiles;
+    float2* part;
 };
 
 // Sets the calling thread's message returned by conv1d_norm_last_error().
@@ -93,6 +103,12 @@ void set_last_error(const char* msg);
 cudaError_t launch_simt_conv(const c1n_params& p, const Plan& pl, const void* x, const void* w, const float* b,
                              void* out, bool out_is_raw_f32, cudaStream_t stream);
 cudaError_t launch_gn_stats(const c1n_params& p, const Plan& pl, const float* raw, float2* stats, cudaStream_t stream);
+// Statistics from the tensor-core epilogue's partials (TcArgs::part): Chan's merge over the
+// 128-row tiles of each (sample, group), or over the channel blocks of each (sample, time step).
+cudaError_t launch_gn_merge(const c1n_params& p, const Plan& pl, const float2* part, float2* stats,
+                            cudaStream_t stream);
+cudaError_t launch_ln_merge(const c1n_params& p, const Plan& pl, const float2* part, float2* stats,
+                            cudaStream_t stream);
 cudaError_t launch_ln_stats(const c1n_params& p, const Plan& pl, const float* raw, float2* stats, cudaStream_t stream);
 cudaError_t launch_normalize(const c1n_params& p, const Plan& pl, const float* raw, const float2* stats,
                              const float* gamma, const float* beta, void* y, cudaStream_t stream);
@@ -126,7 +142,10 @@ cudaError_t launch_conv_transpose3d_tc(const c1n_convt3d_params& p, const float*
 // Tensor-core kernels. `tm_a`: x (conv mode, staged time-contiguous boxes) or X (Linear mode);
 // `tm_b`: packed weights (conv mode) or W (Linear mode).
 // kEpiLNX: channel LayerNorm over the two channel halves held by the two CTAs of a cluster.
-enum TcEpilogue { kEpiDirect = 0, kEpiClusterGN = 1, kEpiGridGN = 2, kEpiRowGN = 3, kEpiLN = 4, kEpiLNX = 5 };
+// kEpiDirectStats: the direct epilogue plus the partial statistics of a two-pass plan.
+enum TcEpilogue {
+    kEpiDirect = 0, kEpiClusterGN = 1, kEpiGridGN = 2, kEpiRowGN = 3, kEpiLN = 4, kEpiLNX = 5, kEpiDirectStats = 6
+};
 cudaError_t launch_tc(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                       const CUtensorMap& tm_y, bool linear, int epilogue, bool out_bf16, int num_sms,
                       cudaStream_t stream);

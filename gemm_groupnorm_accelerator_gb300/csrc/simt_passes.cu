@@ -2,6 +2,8 @@
 //   * simt_conv       — direct convolution from shared-memory tiles (fp32 FMA);
 //   * gn_stats        — GroupNorm mean / rstd per (n, group), two passes over the group;
 //   * ln_stats        — channel-LayerNorm mean / rstd per (n, t), two passes over channels;
+//   * gn_merge, ln_merge — the same statistics from the partial (mean, M2) sets that the
+//                       tensor-core epilogue of a two-pass plan writes (Chan's merge);
 //   * normalize       — (raw - mean) * rstd * gamma + beta, then GELU, float4 when rows allow it;
 //   * rowmin          — min (and lowest argmin) over channels of the normalized values per (n, t);
 //   * broadcast       — y[n][c][t] = rowmin[n][t] + bias2[c];
@@ -150,6 +152,57 @@ __global__ void __launch_bounds__(512) gn_stats_kernel(const float* __restrict__
     const float m1 = s1 * inv;
     const float var = fmaxf(s2 * inv - m1 * m1, 0.f);
     if (threadIdx.x == 0) stats[(long long)n * G + g] = make_float2(shift + m1, rsqrtf(var + eps));
+}
+
+// Chan's pairwise update of the moments (count n, mean mu, M2) with another set.
+__device__ __forceinline__ void merge_moments(float& n, float& mu, float& m2, float nb, float mub, float m2b) {
+    if (nb <= 0.f) return;
+    const float nn = n + nb;
+    const float d = mub - mu;
+    const float f = nb / nn;
+    mu += d * f;
+    m2 += m2b + d * d * n * f;
+    n = nn;
+}
+
+// GroupNorm statistics from the tensor-core epilogue's partials: one warp per (n, g); lane l
+// merges the 128-step tiles l, l + 32, ... in order, then the 32 lane results are merged in a
+// butterfly. Tile tt holds cpg * min(128, T_out - 128 tt) values.
+__global__ void __launch_bounds__(256) gn_merge_kernel(const float2* __restrict__ part, float2* __restrict__ stats,
+                                                       int NG, int n_tiles, int cpg, long long T_out, float eps) {
+    const int lane = threadIdx.x & 31;
+    const long long i = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (i >= NG) return;
+    float n = 0.f, mu = 0.f, m2 = 0.f;
+    for (int tt = lane; tt < n_tiles; tt += 32) {
+        const float2 v = __ldg(part + i * n_tiles + tt);
+        const long long rows = T_out - 128LL * tt;
+        merge_moments(n, mu, m2, float(cpg) * float(rows < 128 ? rows : 128), v.x, v.y);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float nb = __shfl_xor_sync(0xffffffffu, n, o);
+        const float mub = __shfl_xor_sync(0xffffffffu, mu, o);
+        const float m2b = __shfl_xor_sync(0xffffffffu, m2, o);
+        merge_moments(n, mu, m2, nb, mub, m2b);
+    }
+    if (lane == 0) stats[i] = make_float2(mu, rsqrtf((n > 0.f ? m2 / n : 0.f) + eps));
+}
+
+// Channel-LayerNorm statistics from the epilogue's partials: one thread per (n, t) merges the
+// n_cb channel blocks (block cb holds min(BN, C - cb BN) channels); coalesced over t.
+__global__ void __launch_bounds__(256) ln_merge_kernel(const float2* __restrict__ part, float2* __restrict__ stats,
+                                                       int N, int C, int BN, int n_cb, long long T_out, float eps) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)N * T_out) return;
+    const long long n = i / T_out, t = i - n * T_out;
+    float cnt = 0.f, mu = 0.f, m2 = 0.f;
+    for (int cb = 0; cb < n_cb; ++cb) {
+        const float2 v = __ldg(part + (n * n_cb + cb) * T_out + t);
+        const int c = C - cb * BN;
+        merge_moments(cnt, mu, m2, float(c < BN ? c : BN), v.x, v.y);
+    }
+    stats[i] = make_float2(mu, rsqrtf(m2 / cnt + eps));
 }
 
 // Channel-LayerNorm statistics per (n, t), read once. A CTA covers 32 * VEC consecutive t of one
@@ -579,6 +632,22 @@ cudaError_t launch_gn_stats(const c1n_params& p, const Plan& pl, const float* ra
                             cudaStream_t stream) {
     dim3 grid((unsigned)p.groups, (unsigned)p.N);
     gn_stats_kernel<<<grid, 512, 0, stream>>>(raw, stats, p.C_out, pl.T_out, p.groups, p.eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gn_merge(const c1n_params& p, const Plan& pl, const float2* part, float2* stats,
+                            cudaStream_t stream) {
+    const int NG = p.N * p.groups;
+    gn_merge_kernel<<<(NG + 7) / 8, 256, 0, stream>>>(part, stats, NG, pl.part_tiles, p.C_out / p.groups, pl.T_out,
+                                                     p.eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ln_merge(const c1n_params& p, const Plan& pl, const float2* part, float2* stats,
+                            cudaStream_t stream) {
+    const long long rows = (long long)p.N * pl.T_out;
+    ln_merge_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, stream>>>(part, stats, p.N, p.C_out, pl.BN, pl.n_cb,
+                                                                       pl.T_out, p.eps);
     return cudaGetLastError();
 }
 

@@ -835,19 +835,89 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int row = un.row0 + m;
                 const bool row_ok = LINEAR ? (row < a.N) : (row < a.T_out);
 
-                if (EPI == kEpiDirect) {
+                if (EPI == kEpiDirect || EPI == kEpiDirectStats) {
                     for (int cbi = 0; cbi < a.cb_per_unit; ++cbi) {
-                        const int co_base = (un.cbu * a.cb_per_unit + cbi) * a.BN;
+                        const int cb = un.cbu * a.cb_per_unit + cbi;
+                        const int co_base = cb * a.BN;
                         const int ncols = min(a.BN, a.C_out - co_base);
                         if (co_base != staged_co) {  // uniform over the epilogue threads
                             named_bar_sync(1, kEpiT);
                             for (int col = er; col < a.BN; col += kEpiT)
                                 s_bias[col] = (a.bias && col < ncols) ? __ldg(a.bias + co_base + col) : 0.f;
                             named_bar_sync(1, kEpiT);
+                            if (EPI == kEpiDirectStats && a.part_kind == 1) {
+                                // the bias minus its mean over the column's run of `sub` channels
+                                const int run = a.sub > 0 ? a.sub : 1;
+                                for (int col = er; col < 256; col += kEpiT) {
+                                    const int r0 = col - col % run;
+                                    float mb = 0.f;
+                                    for (int i = 0; i < run; ++i) mb += s_bias[r0 + i];
+                                    epi[2816 + col] = s_bias[col] - mb * (1.f / float(run));
+                                }
+                                named_bar_sync(1, kEpiT);
+                            }
                             staged_co = co_base;
                         }
                         const uint32_t tb =
                             tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * (ab * a.cb_per_unit + cbi));
+                        if (EPI == kEpiDirectStats && a.part_kind == 1) {
+                            // GroupNorm partials of this 128-row tile: per-warp moments per run of
+                            // `sub` channels, merged over the runs of each group and the four warps
+                            // (Chan's formula) into the tile's (mean, M2) per group. Groups lie inside
+                            // the channel block.
+                            float* red_s = epi;         // [4][256] per-warp run sums
+                            float* red_m = epi + 1024;  // [4][256] per-warp run sums of squared deviations
+                            const int nvalid_t = min(128, a.T_out - un.row0);
+                            const int nvalid_w = min(32, max(0, nvalid_t - q * 32));
+                            gn_run_moments_any(a.sub, tb, 0, ncols, lane < nvalid_w, nvalid_w, epi + 2816, red_s, red_m,
+                                               q, lane);
+                            named_bar_sync(1, kEpiT);
+                            const int run = a.sub > 0 ? a.sub : 1;
+                            const int cpg = a.cpg;
+                            const int ngroups = ncols / cpg;
+                            for (int g = er; g < ngroups && nvalid_t > 0; g += kEpiT) {
+                                float gn = 0.f, gmu = 0.f, gm2 = 0.f;
+                                for (int j = g * cpg / run; j < (g + 1) * cpg / run; ++j) {
+                                    float mb = 0.f;  // the bias mean of run j
+                                    for (int i = 0; i < run; ++i) mb += s_bias[j * run + i];
+                                    mb *= 1.f / float(run);
+                                    for (int q2 = 0; q2 < 4; ++q2) {
+                                        const int nr = min(32, max(0, nvalid_t - q2 * 32));
+                                        if (nr == 0) continue;
+                                        const float nq = float(nr * run);
+                                        chan_merge(gn, gmu, gm2, nq, red_s[q2 * 256 + j] / nq + mb, red_m[q2 * 256 + j]);
+                                    }
+                                }
+                                const size_t gi = size_t(un.n) * a.groups + co_base / cpg + g;
+                                a.part[gi * a.part_tiles + un.row0 / 128] = make_float2(gmu, gm2);
+                            }
+                            // red_s / red_m are read above before the next tile's moments overwrite them
+                            named_bar_sync(1, kEpiT);
+                        } else if (EPI == kEpiDirectStats && a.part_kind == 2) {
+                            // channel LayerNorm partials of this step over the block's channels: the
+                            // mean, then the sum of squared deviations from it (two sweeps of TMEM)
+                            float s1 = 0.f;
+                            for (int j0 = 0; j0 < ncols; j0 += 16) {
+                                float v[16], bb[16];
+                                tmem_load16(tb + uint32_t(j0), v);
+                                lds_vec(s_bias + j0, bb);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) s1 += (j0 + i < ncols) ? v[i] + bb[i] : 0.f;
+                            }
+                            const float mu = s1 / float(ncols);
+                            float m2 = 0.f;
+                            for (int j0 = 0; j0 < ncols; j0 += 16) {
+                                float v[16], bb[16];
+                                tmem_load16(tb + uint32_t(j0), v);
+                                lds_vec(s_bias + j0, bb);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    const float d = v[i] + bb[i] - mu;
+                                    m2 = (j0 + i < ncols) ? fmaf(d, d, m2) : m2;
+                                }
+                            }
+                            if (row_ok) a.part[(size_t(un.n) * a.n_cb + cb) * a.T_out + row] = make_float2(mu, m2);
+                        }
                         for (int j0 = 0; j0 < ncols; j0 += 16) {
                             float v[16];
                             tmem_load16(tb + uint32_t(j0), v);
@@ -1396,6 +1466,11 @@ cudaError_t launch_tc(const Plan& pl, const TcArgs& a, const CUtensorMap& tm_a, 
     if (epilogue == kEpiGridGN) {
         if (pl.bf16) return C1N_LAUNCH(false, true, __nv_bfloat16, kEpiGridGN, false);
         return C1N_LAUNCH(false, false, float, kEpiGridGN, false);
+    }
+    if (epilogue == kEpiDirectStats) {
+        // raw fp32 tiles plus partial statistics (two-pass plans)
+        if (pl.bf16) return C1N_LAUNCH2(false, true, float, kEpiDirectStats);
+        return C1N_LAUNCH2(false, false, float, kEpiDirectStats);
     }
     if (pl.bf16) {
         if (out_bf16) return C1N_LAUNCH2(false, true, __nv_bfloat16, kEpiDirect);

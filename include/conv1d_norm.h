@@ -84,7 +84,10 @@ typedef enum {
                                      cooperative grid when the whole grid fits on the GPU at once,
                                      else through distributed shared memory inside a thread-block
                                      cluster), then normalize their tiles in place and store once */
-    C1N_PATH_TC_TWO_PASS = 3,     /* tcgen05 conv writes raw tiles, then statistics + normalize pass */
+    C1N_PATH_TC_TWO_PASS = 3,     /* tcgen05 conv writes raw tiles and their partial statistics
+                                     (mean, M2 per tile), a small kernel merges the partials, then one
+                                     normalize pass; GroupNorm whose groups straddle a channel block
+                                     reads the raw output in a statistics pass instead */
     C1N_PATH_TC_LINEAR = 4,       /* T = 1, k = 1: tcgen05 GEMM (rows x out); GroupNorm over groups of
                                      8/16/32 channels, affine, GELU or row-min fused in the epilogue
                                      (row-min then needs one finisher kernel); other shapes use the

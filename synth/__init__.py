@@ -324,6 +324,15 @@ class ConvT3dWorkload:
     def flops(self) -> float:
         return 2.0 * self.macs
 
+    @property
+    def algorithmic_bytes(self) -> int:
+        """fp32 x, w and b read once and y written once."""
+        Do, Ho, Wo = self.out_dhw
+        x = self.N * self.C_in * self.D * self.H * self.W
+        w = self.C_in * self.C_out * self.k ** 3
+        y = self.N * self.C_out * Do * Ho * Wo
+        return 4 * (x + w + self.C_out + y)
+
     def replace(self, **kw) -> "ConvT3dWorkload":
         return dataclasses.replace(self, **kw)
 

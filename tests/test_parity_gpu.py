@@ -126,6 +126,14 @@ SMALL = {
     "ln_c512_bf16": synth.CONV_LN_GELU_BF16.replace(N=2, C_in=64, C_out=512, T=320),
     "gn_bf16": synth.CONV_GN.replace(N=2, C_in=64, C_out=128, T=512, groups=16, dtype=synth.DTYPE_BF16),
     "conv_bf16": synth.CAUSAL_CONV.replace(N=2, C_in=72, C_out=136, T=400, dtype=synth.DTYPE_BF16),
+    # two channel blocks of 192: 64-channel groups stay inside a block; 128-channel groups straddle
+    "gn_cb2": synth.CONV_GN.replace(N=2, C_in=32, C_out=384, T=640, groups=6),
+    "gn_cb2_straddle": synth.CONV_GN.replace(N=2, C_in=32, C_out=384, T=640, groups=3),
+    # 16 tiles of 128 steps, the last one 80 steps long
+    "gn_long_ragged": synth.CONV_GN.replace(N=2, C_in=32, C_out=64, T=2000, groups=8),
+    # three channel blocks (224, 224, 192): channel LayerNorm takes the two-pass plan
+    "ln_c640_f32": synth.CONV_LN_GELU_BF16.replace(N=2, C_in=40, C_out=640, T=200, dtype=synth.DTYPE_F32,
+                                                   post=synth.POST_NONE),
     "stride2_simt": synth.CONV_GN.replace(N=2, C_in=16, C_out=32, T=101, stride=2, groups=8),
     "odd_T_simt": synth.CAUSAL_CONV.replace(N=2, C_in=8, C_out=24, T=77),
 }
@@ -170,6 +178,47 @@ GN_NAMES = ["gn_tiny", "gn_c2_structure", "gn_cpg1", "gn_cpg4", "gn_cpg16", "gn_
             "gn_bf16", "gn_ragged_out"]
 
 
+def _kernel_names(c1n, wl, inp, force_path, mainloop):
+    params = c1n.make_params(wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right, wl.dilation,
+                             wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, 0, force_path, mainloop)
+    op = c1n.Conv1dNorm(params)
+    op.set_profiling(True)
+    bf = wl.dtype == synth.DTYPE_BF16
+    x, w = _to_dev(inp["x"], bf), _to_dev(inp["w"], bf)
+    b, ga, be = (_to_dev(inp[k], False) for k in ("b", "gamma", "beta"))
+    op(x, w, b, ga, be)
+    torch.cuda.synchronize()
+    op.check()
+    return [n for n, _ in op.kernel_times()]
+
+
+@pytest.mark.parametrize("name", GN_NAMES + ["gn_cb2", "gn_cb2_straddle", "gn_long_ragged", "gn_g1_twopass",
+                                             "ln_c640_f32", "ln_c384_f32", "ln_gelu_bf16"])
+@pytest.mark.parametrize("mode", ["single", "pair"])
+def test_two_pass_epilogue_partials(cuda_lib, name, mode):
+    # Two-pass plans: the conv epilogue writes the raw tile and its partial statistics, a small
+    # kernel merges them (no pass re-reads the raw output for statistics) -- except GroupNorm whose
+    # groups straddle a channel block, which keeps the statistics pass.
+    wl = SMALL[name]
+    inp = _inputs(wl)
+    mainloop = cuda_lib.MAINLOOP_SINGLE if mode == "single" else cuda_lib.MAINLOOP_PAIR
+    try:
+        cuda_lib.conv1d_norm_destroy(cuda_lib.conv1d_norm_desc_create(cuda_lib.make_params(
+            wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right, wl.dilation, wl.norm,
+            wl.groups, wl.eps, wl.post, wl.dtype, 0, cuda_lib.PATH_TC_TWO_PASS, mainloop)))
+    except cuda_lib.C1NError:
+        pytest.skip("plan cannot run on CTA pairs")
+    ref, _ = oracle_full(wl, inp)
+    y, am, path = run_gpu(cuda_lib, wl, inp, force_path=cuda_lib.PATH_TC_TWO_PASS, mainloop=mainloop)
+    assert path == "tc_two_pass"
+    compare(wl, y, am, ref, None, path, f"{name}/{mode}")
+    names = _kernel_names(cuda_lib, wl, inp, cuda_lib.PATH_TC_TWO_PASS, mainloop)
+    if wl.norm == synth.NORM_GROUP:
+        assert names[-2] == ("gn_stats" if name == "gn_cb2_straddle" else "gn_merge"), names
+    else:
+        assert names[-2] == "ln_merge", names
+
+
 @pytest.mark.parametrize("name", GN_NAMES)
 def test_group_norm_cluster_exchange_forced(cuda_lib, name):
     # the same fused kernel with the partial statistics exchanged through a cluster's DSMEM
@@ -203,7 +252,7 @@ def test_layer_norm_fused_forced(cuda_lib, name):
 
 
 @pytest.mark.parametrize("name,kernels", [("gn_tiny", ["pack_weights", "tc_conv"]),
-                                          ("ln_c384_f32", ["pack_weights", "tc_conv", "ln_stats", "normalize"]),
+                                          ("ln_c384_f32", ["pack_weights", "tc_conv", "ln_merge", "normalize"]),
                                           ("linear_rowmin", ["tc_conv", "rowmin_finish"]),
                                           ("stride2_simt", ["simt_conv", "gn_stats", "normalize"])])
 def test_kernel_times_list_every_launch(cuda_lib, name, kernels):
