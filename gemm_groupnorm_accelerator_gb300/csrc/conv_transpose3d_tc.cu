@@ -4,22 +4,27 @@
 // As a contraction: for every input voxel v = (n, i, j, l) and output parity p = (pd, ph, pw),
 //   y[n][co][2i+pd][2j+ph][2l+pw] = b[co] + sum_{delta <= p} sum_ci x[n][ci][v + delta] * w[ci][co][k(p, delta)]
 // with delta in {0, 1}^3 (componentwise at most p) and, per axis, k(0, 0) = 1, k(1, 0) = 2,
-// k(1, 1) = 0 (inputs past the end count zero). For one (pd, ph) "class" the rows (pw, co) form
-// M = 128, the voxels of a tile N = 128 (4 input rows j x 32 input columns l), and each shift delta
-// one K = 32 step: D[(pw, co)][v] += A_delta[(pw, co)][ci] * X[v + delta][ci], where A_delta holds the
-// weights of that tap (zero rows for pw = 0 when delta_w = 1). A class has 2, 4, 4 or 8 shifts.
+// k(1, 1) = 0 (inputs past the end count zero). For one (pd, ph) "class" the voxels of a tile
+// (4 input rows j x 32 input columns l) form M = 128, the (pw, co) pairs N = 128, and each shift
+// delta one K = 32 step: D[v][(pw, co)] += X[v + delta][ci] * B_delta[(pw, co)][ci], where B_delta
+// holds the weights of that tap (zero rows for pw = 0 when delta_w = 1). A class has 2, 4, 4 or 8
+// shifts.
 //
 // Operands: x is first rewritten channels-last (x_cl[n][d][h][w][ci]) so that a 32-voxel x 32-channel
 // box of it is a K-major, 128-byte-swizzled MMA operand; the shift is just a TMA coordinate on the
-// w / h / d dimensions (past the end -> zero fill). The class's A blocks (TF32-rounded, packed by a
-// small kernel) stay in shared memory for the CTA's whole life. CTAs are split over the four
-// classes in proportion to their shift counts; each walks its class's tiles.
+// w / h / d dimensions (past the end -> zero fill). The class's weight blocks (TF32-rounded, packed
+// by a small kernel) stay in shared memory for the CTA's whole life. Every tile writes the same
+// output bytes whatever its class, and the operator is bound by that write, so CTAs are split
+// over the four classes nearly evenly (a little more to the classes with more shifts); each walks
+// its class's tiles.
 //
-// Roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5 epilogue
-// (TMEM lane quarter q = rows 32q..32q+31: pw = q / 2, channels 32 (q % 2) ..). Two accumulators of
-// 128 columns, so the epilogue of one tile overlaps the next tile's MMAs. The epilogue interleaves
-// the two width parities through 128-byte-swizzled shared tiles [32 channels][32 ow] and sends them
-// with TMA bulk stores. Every wait is bounded.
+// Roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5 epilogue.
+// Epilogue warp q reads TMEM lanes 32q..32q+31, i.e. input row j = 4 jt + q and column l = lane;
+// its columns 0..63 hold width parity 0 and 64..127 parity 1 of channel co. A thread thus holds
+// both outputs 2l and 2l+1 of a channel and writes them as one 8-byte store: a warp writes 256
+// contiguous bytes of an output row per instruction, with no staging in shared memory. Two
+// accumulators of 128 columns, so the epilogue of one tile overlaps the next tile's MMAs. Every
+// wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -35,9 +40,8 @@ namespace c1n {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kSB = 3;                    // B ring stages
+constexpr int kSB = 5;                    // x (B ring) stages
 constexpr int kTileBytes = 128 * 128;     // one 128-row x 128-byte operand tile (16 KB)
-constexpr int kStageOut = 4 * 32 * 32 * 4;  // four 32 x 32 fp32 output tiles (16 KB), two buffers
 
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1, int c2,
                                             int c3, int c4) {
@@ -46,17 +50,6 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* m, 
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
         : "memory");
 }
-
-__device__ __forceinline__ void tma_store_5d(const CUtensorMap* m, uint32_t src, int c0, int c1, int c2, int c3,
-                                             int c4) {
-    asm volatile("cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];"
-                 ::"l"(reinterpret_cast<uint64_t>(m)), "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-                 : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-__device__ __forceinline__ void store_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-__device__ __forceinline__ void store_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // Time-bounded wait that ignores the abort flag: copies and MMAs in flight land before the CTA
 // (and its shared memory / TMEM) goes away.
@@ -71,6 +64,7 @@ struct ConvTArgs {
     int JT, LT;           // tiles along input rows (4 each) and input columns (32 each)
     int cta0[5];          // first CTA of each class (cta0[4] = grid)
     const float* bias;    // [64] or null
+    float* y;             // [N][64][Do][Ho][Wo], Do = 2D, Ho = 2H, Wo = 2W (output pad 1)
     int* status;          // [0] = 1 when a wait gave up (the output is then incomplete)
 };
 
@@ -83,7 +77,8 @@ __host__ __device__ constexpr int class_base(int c) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     convt3d_tc_kernel(const __grid_constant__ ConvTArgs a, const __grid_constant__ CUtensorMap tm_x,
-                      const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_y) {
+                      const __grid_constant__ CUtensorMap tm_w) {
+    __shared__ float s_bias[64];
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -94,11 +89,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ns = n_shifts(cls);
     const int cta_in = int(blockIdx.x) - a.cta0[cls], n_cta = a.cta0[cls + 1] - a.cta0[cls];
     const int tiles = a.N * a.D * a.JT * a.LT;
-    // shared memory: A blocks (8 max) | B ring | output staging (2 buffers) | barriers
+    // shared memory: weight blocks (8 max) | x ring | barriers
     const uint32_t sA = smem_u32(base);
     const uint32_t sB = sA + 8u * kTileBytes;
-    uint8_t* so = base + 8 * kTileBytes + kSB * kTileBytes;  // 1024-byte aligned
-    uint64_t* bars = reinterpret_cast<uint64_t*>(so + 2 * kStageOut);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + 8 * kTileBytes + kSB * kTileBytes);
     const uint32_t bar0 = smem_u32(bars);
     auto bar = [&](int i) { return bar0 + 8u * uint32_t(i); };
     const int i_afull = 0, i_bfull = 1, i_bempty = 1 + kSB, i_accfull = 1 + 2 * kSB, i_accempty = i_accfull + 2,
@@ -112,7 +106,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tensormap(&tm_x);
             prefetch_tensormap(&tm_w);
-            prefetch_tensormap(&tm_y);
         }
     }
     if (warp == 1) {
@@ -176,10 +169,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < ns; ++s) {
                 if (!wait_warp(i_bfull + bi, bph)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t al = desc_lo_sw128(sA + s * kTileBytes), bl = desc_lo_sw128(sB + bi * kTileBytes);
+                // A = the x tile (128 voxels x 32 channels), B = the shift's weight block
+                // (128 (pw, co) rows x 32 channels); both K-major, 128-byte swizzled
+                const uint32_t wl = desc_lo_sw128(sA + s * kTileBytes), xl = desc_lo_sw128(sB + bi * kTileBytes);
                 if (elect_one()) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) mma_issue<false, false>(d, al + 2u * k, bl + 2u * k, idesc, (s | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k) mma_issue<false, false>(d, xl + 2u * k, wl + 2u * k, idesc, (s | k) != 0 ? 1u : 0u);
                     mma_commit(bar(i_bempty + bi));
                 }
                 __syncwarp();
@@ -196,11 +191,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue (warps 2..5)
-        const int q = warp & 3;            // TMEM lane quarter: rows 32q .. 32q+31
-        const int pw = q >> 1, cb = q & 1;  // width parity, channel block (32 channels)
-        const int co = cb * 32 + lane;
-        const float bv = a.bias ? __ldg(a.bias + co) : 0.f;
-        int lt_ = 0, ob = 0;
+        const int q = warp & 3;  // TMEM lane quarter: input row jt * 4 + q, input column lt * 32 + lane
+        const int er = threadIdx.x - 64;
+        if (er < 64) s_bias[er] = a.bias ? __ldg(a.bias + er) : 0.f;
+        named_bar_sync(1, 128);
+        const size_t cstride = size_t(a.Do) * a.Ho * a.Wo;  // one output channel
+        int lt_ = 0;
         for (int t = cta_in; t < tiles; t += n_cta, ++lt_) {
             const int ab = lt_ & 1;
             const uint32_t acc_par = uint32_t((lt_ >> 1) & 1);
@@ -210,39 +206,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (named_bar_any(1, 128, !got || *abort_flag != 0)) break;
             tc_fence_after();
             const int lt = t % a.LT, jt = (t / a.LT) % a.JT, i = (t / (a.LT * a.JT)) % a.D, n = t / (a.LT * a.JT * a.D);
+            const int hin = jt * 4 + q, win = lt * 32 + lane;
+            const bool ok = hin < a.H && win < a.W;
+            // channel 0 of this thread's two outputs (2 win, 2 win + 1) in row (2i + pd, 2 hin + ph)
+            float* dst = a.y + ((size_t(n) * 64 * a.Do + size_t(2 * i + pd)) * a.Ho + size_t(ok ? 2 * hin + ph : 0)) * a.Wo +
+                         size_t(ok ? 2 * win : 0);
             const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(128 * ab);
-            for (int jj = 0; jj < 4; ++jj) {
-                float v[32];
-                tmem_load32(tb + uint32_t(jj * 32), v);  // input columns l = 0..31 of row jj
-                // buffer `ob` held the stores issued two rows ago: they must have read it
-                if (lane == 0) store_wait_read_le1();
-                named_bar_sync(1, 128);
-                // tiles of buffer ob: [cb][half], each [32 channels][32 ow], 128-byte swizzle
-                uint8_t* buf = so + ob * kStageOut;
+#pragma unroll 1
+            for (int cb = 0; cb < 2; ++cb) {
+                float v0[32], v1[32];
+                tmem_load32(tb + uint32_t(cb * 32), v0);       // parity 0, channels 32 cb ..
+                tmem_load32(tb + uint32_t(64 + cb * 32), v1);  // parity 1, the same channels
+                if (cb == 1) {
+                    // every column of this accumulator is in registers: the MMA may reuse it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(i_accempty + ab));
+                }
+                if (ok) {
 #pragma unroll
-                for (int l = 0; l < 32; ++l) {
-                    const int h = l >> 4, c = 2 * (l & 15) + pw;  // ow = 2l + pw -> half h, column c
-                    uint8_t* tile = buf + (cb * 2 + h) * 4096;
-                    *reinterpret_cast<float*>(tile + lane * 128 + (((c >> 2) ^ (lane & 7)) << 4) + (c & 3) * 4) =
-                        v[l] + bv;
+                    for (int c = 0; c < 32; ++c) {
+                        const float bv = s_bias[cb * 32 + c];
+                        *reinterpret_cast<float2*>(dst + size_t(cb * 32 + c) * cstride) = make_float2(v0[c] + bv, v1[c] + bv);
+                    }
                 }
-                fence_async_shared();
-                named_bar_sync(1, 128);
-                if (lane == 0) {
-                    // warp q sends tile (channel block q & 1, half q >> 1)
-                    const int tcb = q & 1, th = q >> 1;
-                    tma_store_5d(&tm_y, smem_u32(buf + (tcb * 2 + th) * 4096), 64 * lt + 32 * th,
-                                 2 * (jt * 4 + jj) + ph, 2 * i + pd, 32 * tcb, n);
-                }
-                __syncwarp();
-                ob ^= 1;
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(i_accempty + ab));
         }
-        if (lane == 0) store_wait_read_all();
-        __syncwarp();
     }
     __syncthreads();
     if (warp == 1) {
@@ -251,23 +240,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// x [N][C][S] -> x_cl [N][S][C] (S = D*H*W), 32 x 32 tiles through shared memory.
-__global__ void __launch_bounds__(256) to_channels_last_kernel(const float* __restrict__ x, float* __restrict__ xcl,
-                                                               int C, long long S) {
-    __shared__ float t[32][33];
-    const int n = blockIdx.z;
-    const long long s0 = (long long)blockIdx.x * 32;
-    const int c0 = blockIdx.y * 32;
-    for (int r = threadIdx.y; r < 32; r += 8) {
-        const int c = c0 + r;
-        const long long s = s0 + threadIdx.x;
-        t[r][threadIdx.x] = (c < C && s < S) ? __ldg(x + ((long long)n * C + c) * S + s) : 0.f;
+// x [N][32][S] -> x_cl [N][S][32] (S = D*H*W): a CTA moves 128 voxels x 32 channels through shared
+// memory, with 16-byte loads along S (when S is a multiple of 4) and 16-byte stores of 4 channels.
+// The row stride 129 keeps both shared-memory phases free of bank conflicts.
+__global__ void __launch_bounds__(256) to_channels_last32_kernel(const float* __restrict__ x, float* __restrict__ xcl,
+                                                                 long long S) {
+    __shared__ float t[32][129];
+    const int tid = threadIdx.x, n = blockIdx.y;
+    const long long s0 = (long long)blockIdx.x * 128;
+    const float* src = x + (long long)n * 32 * S;
+    const bool vec = (S & 3) == 0;
+    {
+        const int c = tid >> 3;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int v = ((tid & 7) + 8 * j) * 4;
+            const long long s = s0 + v;
+            float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (vec && s + 3 < S) {
+                q = __ldg(reinterpret_cast<const float4*>(src + c * S + s));
+            } else {
+                if (s < S) q.x = __ldg(src + c * S + s);
+                if (s + 1 < S) q.y = __ldg(src + c * S + s + 1);
+                if (s + 2 < S) q.z = __ldg(src + c * S + s + 2);
+                if (s + 3 < S) q.w = __ldg(src + c * S + s + 3);
+            }
+            t[c][v] = q.x;
+            t[c][v + 1] = q.y;
+            t[c][v + 2] = q.z;
+            t[c][v + 3] = q.w;
+        }
     }
     __syncthreads();
-    for (int r = threadIdx.y; r < 32; r += 8) {
-        const long long s = s0 + r;
-        const int c = c0 + threadIdx.x;
-        if (s < S && c < C) xcl[((long long)n * S + s) * C + c] = t[threadIdx.x][r];
+    const int k = tid & 7;  // channels 4k .. 4k+3
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int v = (tid >> 3) + 32 * j;
+        const long long s = s0 + v;
+        if (s < S)
+            *reinterpret_cast<float4*>(xcl + ((long long)n * S + s) * 32 + 4 * k) =
+                make_float4(t[4 * k][v], t[4 * k + 1][v], t[4 * k + 2][v], t[4 * k + 3][v]);
     }
 }
 
@@ -335,12 +347,11 @@ cudaError_t launch_conv_transpose3d_tc(const c1n_convt3d_params& p, const float*
     cudaError_t e = cudaMemsetAsync(status, 0, 256, stream);
     if (e != cudaSuccess) return e;
     const long long S = (long long)p.D * p.H * p.W;
-    to_channels_last_kernel<<<dim3((unsigned)((S + 31) / 32), (unsigned)((p.C_in + 31) / 32), (unsigned)p.N),
-                              dim3(32, 8), 0, stream>>>(x, xcl, p.C_in, S);
+    to_channels_last32_kernel<<<dim3((unsigned)((S + 127) / 128), (unsigned)p.N), 256, 0, stream>>>(x, xcl, S);
     pack_convt_weights_kernel<<<18, 256, 0, stream>>>(w, wp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    CUtensorMap tm_x, tm_w, tm_y;
+    CUtensorMap tm_x, tm_w;
     {
         const cuuint64_t dims[5] = {32, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)p.D, (cuuint64_t)p.N};
         const cuuint64_t str[4] = {32 * 4, (cuuint64_t)p.W * 32 * 4, (cuuint64_t)p.H * p.W * 32 * 4,
@@ -354,13 +365,6 @@ cudaError_t launch_conv_transpose3d_tc(const c1n_convt3d_params& p, const float*
         const cuuint32_t box[2] = {32, 128};
         if (!encode_f32(&tm_w, wp, 2, dims, str, box)) return cudaErrorInvalidValue;
     }
-    {
-        const cuuint64_t dims[5] = {(cuuint64_t)Wo, (cuuint64_t)Ho, (cuuint64_t)Do, 64, (cuuint64_t)p.N};
-        const cuuint64_t str[4] = {(cuuint64_t)Wo * 4, (cuuint64_t)Ho * Wo * 4, (cuuint64_t)Do * Ho * Wo * 4,
-                                   (cuuint64_t)64 * Do * Ho * Wo * 4};
-        const cuuint32_t box[5] = {32, 1, 1, 32, 1};
-        if (!encode_f32(&tm_y, y, 5, dims, str, box)) return cudaErrorInvalidValue;
-    }
     ConvTArgs a;
     a.N = p.N;
     a.D = p.D;
@@ -372,15 +376,18 @@ cudaError_t launch_conv_transpose3d_tc(const c1n_convt3d_params& p, const float*
     a.JT = (p.H + 3) / 4;
     a.LT = (p.W + 31) / 32;
     a.bias = b;
+    a.y = y;
     a.status = status;
-    // CTAs per class in proportion to its shifts (2, 4, 4, 8 of 18), at least one each, no more than
-    // the class has tiles
+    // CTAs per class: every tile writes the same 64 KB, and a tile's MMAs (0.2 - 1.3 us at 2, 4, 4,
+    // 8 shifts) take about as long as its share of the HBM write at the most, so the classes get
+    // nearly even shares, weighted by shifts + 16 (18 : 20 : 20 : 24); at least one CTA each and
+    // no more than the class has tiles.
     const long long tiles = (long long)p.N * p.D * a.JT * a.LT;
     int grid = num_sms > 4 ? num_sms : 4;
     a.cta0[0] = 0;
     int left = grid;
     for (int c = 0; c < 4; ++c) {
-        int k = c == 3 ? left : (grid * n_shifts(c) + 9) / 18;
+        int k = c == 3 ? left : (grid * (n_shifts(c) + 16) + 41) / 82;
         if (k < 1) k = 1;
         if (k > left - (3 - c)) k = left - (3 - c);
         if (k > tiles) k = (int)tiles;
@@ -388,10 +395,10 @@ cudaError_t launch_conv_transpose3d_tc(const c1n_convt3d_params& p, const float*
         left -= k;
     }
     grid = a.cta0[4];
-    const int smem = 1024 + 8 * kTileBytes + kSB * kTileBytes + 2 * kStageOut + 256;
+    const int smem = 1024 + 8 * kTileBytes + kSB * kTileBytes + 256;
     e = cudaFuncSetAttribute(convt3d_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    convt3d_tc_kernel<<<grid, kThreads, smem, stream>>>(a, tm_x, tm_w, tm_y);
+    convt3d_tc_kernel<<<grid, kThreads, smem, stream>>>(a, tm_x, tm_w);
     return cudaGetLastError();
 }
 
