@@ -662,9 +662,10 @@ FP32_FMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # 152 SMs x 128 fp32 lanes
 
 
 def p4_arm(args, wl):
-    """[p4]'s model after its weights on one GPU: ConvTranspose3d (tensor cores unless --math 1
-    asks for the CUDA cores) then + scalar, LayerNorm(W), AvgPool3d, GELU; TFLOP/s of the transposed
-    convolution's useful multiply-adds."""
+    """[p4]'s model after its weights on one GPU: ConvTranspose3d, + scalar, LayerNorm(W), AvgPool3d,
+    GELU -- by default in one tensor-core kernel; --p4-two-kernel runs the ConvTranspose3d operator
+    (tensor cores unless --math 1 asks for the CUDA cores) and then the pass. TFLOP/s of the
+    transposed convolution's useful multiply-adds."""
     world, rank, local = dist_env()
     lp = synth.LN_AVGPOOL3D_GELU
     if args.impl == "reference":
@@ -713,21 +714,33 @@ def p4_arm(args, wl):
     x, w, b = (torch.from_numpy(inp[k]).to(dev) for k in ("x", "w", "b"))
     ga, be = torch.from_numpy(gb["gamma"]).to(dev), torch.from_numpy(gb["beta"]).to(dev)
     Do, Ho, Wo = wl.out_dhw
-    y = torch.empty((wl.N, wl.C_out, Do, Ho, Wo), dtype=torch.float32, device=dev)
     out = torch.empty((wl.N, wl.C_out, Do // 2, Ho // 2, Wo // 2), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     math = args.math if args.math in (1, 2) else 0
     cp = c1n.ConvT3dParams(wl.N, wl.C_in, wl.C_out, wl.D, wl.H, wl.W, wl.k, wl.stride, wl.pad, wl.out_pad, math)
-    ws_bytes = c1n.conv_transpose3d_workspace_size(cp)
-    tensor_plan = ws_bytes > 0  # only the tensor-core plan takes a workspace
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-    convt = lambda i: c1n.conv_transpose3d(x, w, b, stride=wl.stride, pad=wl.pad, out_pad=wl.out_pad, out=y,
-                                           math=math, workspace=ws)
-    lnp = lambda i: c1n.ln_avgpool3d_gelu(y, lp.sum_weight, ga, be, eps=lp.eps, out=out)
+    # Default: the whole model in one tensor-core kernel (the convolution's output stays on chip);
+    # --p4-two-kernel or --math 1: the ConvTranspose3d operator, then the LayerNorm/pool/GELU pass.
+    fused = not args.p4_two_kernel and math != 1
+    if fused:
+        fws = torch.empty(c1n.conv_transpose3d_ln_avgpool3d_gelu_workspace_size(cp), dtype=torch.uint8, device=dev)
+        model = lambda i: c1n.conv_transpose3d_ln_avgpool3d_gelu(x, w, b, lp.sum_weight, ga, be, eps=lp.eps, out=out,
+                                                                 workspace=fws)
+        step = model
+        tensor_plan = True
+        n_kernels = 3
+    else:
+        y = torch.empty((wl.N, wl.C_out, Do, Ho, Wo), dtype=torch.float32, device=dev)
+        ws_bytes = c1n.conv_transpose3d_workspace_size(cp)
+        tensor_plan = ws_bytes > 0  # only the tensor-core plan takes a workspace
+        ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+        convt = lambda i: c1n.conv_transpose3d(x, w, b, stride=wl.stride, pad=wl.pad, out_pad=wl.out_pad, out=y,
+                                               math=math, workspace=ws)
+        lnp = lambda i: c1n.ln_avgpool3d_gelu(y, lp.sum_weight, ga, be, eps=lp.eps, out=out)
+        n_kernels = 4 if tensor_plan else 2
 
-    def step(i):
-        convt(i)
-        lnp(i)
+        def step(i):
+            convt(i)
+            lnp(i)
 
     for i in range(args.warmup):
         step(i)
@@ -752,29 +765,46 @@ def p4_arm(args, wl):
         t = torch.tensor([ms], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms = float(t[0])
-    convt_ms = time_replays(convt, 1, dev, args.steps, eager=True)
-    lnp_ms = time_replays(lnp, 1, dev, args.steps, eager=True)
     value = wl.flops * world / (ms / 1e3) / 1e12
-    ach = wl.flops / (convt_ms / 1e3) / 1e12
-    common = {"kernels_ms": {"conv_transpose3d": convt_ms, "ln_avgpool3d_gelu": lnp_ms},
-              "ln_avgpool3d_gelu_hbm_frac": lp.algorithmic_bytes / (lnp_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
-    if tensor_plan:
-        # Writing y (8x the input voxels, 64 channels) outweighs the contraction on this shape: the
-        # operator is bound by HBM. Bytes = x + w + b read once, y written once; the time is the
-        # whole operator (channels-last copy of x, weight pack, convt3d_tc_kernel).
-        gbs = wl.algorithmic_bytes / (convt_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": gbs / peaks["hbm_gbs"], "traffic": read_traffic(wl.name, "convt3d_tc"),
-                "peak_source": peaks.get("source", "MEASURED_PEAKS.json"),
-                "kernel": "convt3d_tc_kernel (timed with its channels-last copy and weight pack)",
-                "kernel_ms": convt_ms, "algorithmic_bytes": wl.algorithmic_bytes, "useful_tflops": ach,
-                "useful_tflops_frac_of_tf32": ach / (peaks["bf16_tflops"] * TF32_PER_BF16), **common}
+    tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
+    if fused:
+        # The contraction bounds the one-pass model: x (67 MB) in and the pooled output (134 MB) out
+        # take ~30 us of HBM, the multiply-adds ~60 us of TF32 tensor time. The time is the whole
+        # operator (channels-last copy of x, weight pack, convt3d_lnpool_fused_kernel).
+        model_ms = time_replays(model, 1, dev, args.steps, eager=True)
+        ach = wl.flops / (model_ms / 1e3) / 1e12
+        fbytes = 4 * (inp["x"].size + inp["w"].size + inp["b"].size + 2 * wl.W * 2 + out.numel())
+        issued = 2.0 * 864 * 128 * 32 * 2 * wl.N * wl.D * ((wl.H + 3) // 4)
+        roof = {"bound": "tensor", "achieved": ach, "peak": tf32_peak, "unit": "TFLOP/s", "frac": ach / tf32_peak,
+                "traffic": read_traffic(wl.name, "convt3d_lnpool_fused"),
+                "peak_source": peaks.get("source", "MEASURED_PEAKS.json") + " (bf16 x 1.1/2.25 for tf32)",
+                "kernel": "convt3d_lnpool_fused_kernel (timed with its channels-last copy and weight pack)",
+                "kernel_ms": model_ms, "algorithmic_flops": wl.flops, "issued_mma_flops": issued,
+                "algorithmic_bytes": fbytes, "hbm_frac": fbytes / (model_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                "kernels_ms": {"conv_transpose3d_ln_avgpool3d_gelu": model_ms}}
     else:
-        roof = {"bound": "alu", "achieved": ach, "peak": FP32_FMA_PEAK_TFLOPS, "unit": "TFLOP/s",
-                "frac": ach / FP32_FMA_PEAK_TFLOPS, "traffic": None,
-                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
-                "kernel": "conv_transpose3d_k3s2_kernel", "kernel_ms": convt_ms, "algorithmic_flops": wl.flops,
-                **common}
+        convt_ms = time_replays(convt, 1, dev, args.steps, eager=True)
+        lnp_ms = time_replays(lnp, 1, dev, args.steps, eager=True)
+        ach = wl.flops / (convt_ms / 1e3) / 1e12
+        common = {"kernels_ms": {"conv_transpose3d": convt_ms, "ln_avgpool3d_gelu": lnp_ms},
+                  "ln_avgpool3d_gelu_hbm_frac": lp.algorithmic_bytes / (lnp_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+        if tensor_plan:
+            # Writing y (8x the input voxels, 64 channels) outweighs the contraction on this shape:
+            # the operator is bound by HBM. Bytes = x + w + b read once, y written once; the time is
+            # the whole operator (channels-last copy of x, weight pack, convt3d_tc_kernel).
+            gbs = wl.algorithmic_bytes / (convt_ms / 1e3) / 1e9
+            roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / peaks["hbm_gbs"], "traffic": read_traffic(wl.name, "convt3d_tc"),
+                    "peak_source": peaks.get("source", "MEASURED_PEAKS.json"),
+                    "kernel": "convt3d_tc_kernel (timed with its channels-last copy and weight pack)",
+                    "kernel_ms": convt_ms, "algorithmic_bytes": wl.algorithmic_bytes, "useful_tflops": ach,
+                    "useful_tflops_frac_of_tf32": ach / tf32_peak, **common}
+        else:
+            roof = {"bound": "alu", "achieved": ach, "peak": FP32_FMA_PEAK_TFLOPS, "unit": "TFLOP/s",
+                    "frac": ach / FP32_FMA_PEAK_TFLOPS, "traffic": None,
+                    "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
+                    "kernel": "conv_transpose3d_k3s2_kernel", "kernel_ms": convt_ms, "algorithmic_flops": wl.flops,
+                    **common}
     xh = torch.from_numpy(inp["x"]).pin_memory()
     oh = torch.empty(out.shape, dtype=torch.float32).pin_memory()
     e_steps = max(1, min(args.steps, 5))
@@ -798,10 +828,11 @@ def p4_arm(args, wl):
                            "k": wl.k, "stride": wl.stride, "pad": wl.pad, "out_pad": wl.out_pad,
                            "then": lp.name, "parallelism": f"dp{world}" if world > 1 else "single",
                            "math": "tensor (tf32)" if tensor_plan else "cuda cores (fp32 fma)",
+                           "plan": "one-pass model kernel" if fused else "ConvTranspose3d, then the pass",
                            "l2": "working set larger than L2",
-                           "launch": f"eager, {4 if tensor_plan else 2} kernels per step"},
+                           "launch": f"eager, {n_kernels} kernels per step"},
                 "roofline": roof, "cpu_baseline": None, "e2e": e2e,
-                "gpu_launches": (4 if tensor_plan else 2) * args.steps, "clocks": clocks}
+                "gpu_launches": n_kernels * args.steps, "clocks": clocks}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
@@ -818,6 +849,8 @@ def main():
     ap.add_argument("--path", type=int, default=-1, help="force an execution path (c1n_path)")
     ap.add_argument("--mainloop", type=int, default=0, help="0 auto, 1 one CTA per tile, 2 CTA pairs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--p4-two-kernel", action="store_true",
+                    help="p4 workload: ConvTranspose3d then the LayerNorm/pool/GELU pass instead of the one-pass kernel")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--oracle-rows", type=int, default=2, help="batch entries per reference-arm step")
     ap.add_argument("--metric", default="fused conv1d+GroupNorm TFLOP/s")

@@ -33,6 +33,7 @@ EXPORTED_SYMBOLS = (
     "conv1d_norm_status_string", "conv1d_norm_last_error", "conv1d_norm_version", "conv1d_norm_run_static_scratch",
     "conv1d_norm_set_profiling", "conv1d_norm_kernel_times", "ln_avgpool3d_gelu_run",
     "conv_transpose3d_run", "conv_transpose3d_workspace_size",
+    "conv_transpose3d_ln_avgpool3d_gelu_run", "conv_transpose3d_ln_avgpool3d_gelu_workspace_size",
 )
 
 STATIC_SCRATCH_BYTES = 4 << 20  # C1N_STATIC_SCRATCH_BYTES
@@ -132,6 +133,11 @@ def load(build_if_missing: bool = True):
         lib.conv_transpose3d_run.restype = ctypes.c_int
         lib.conv_transpose3d_workspace_size.argtypes = [P(ConvT3dParams), P(ctypes.c_size_t)]
         lib.conv_transpose3d_workspace_size.restype = ctypes.c_int
+        lib.conv_transpose3d_ln_avgpool3d_gelu_run.argtypes = [P(ConvT3dParams), ctypes.c_float, ctypes.c_float, vp, vp,
+                                                               vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.conv_transpose3d_ln_avgpool3d_gelu_run.restype = ctypes.c_int
+        lib.conv_transpose3d_ln_avgpool3d_gelu_workspace_size.argtypes = [P(ConvT3dParams), P(ctypes.c_size_t)]
+        lib.conv_transpose3d_ln_avgpool3d_gelu_workspace_size.restype = ctypes.c_int
         for name in ("conv1d_norm_desc_create", "conv1d_norm_workspace_size", "conv1d_norm_set_workspace",
                      "conv1d_norm_plan_info", "conv1d_norm_run", "conv1d_norm_run_ex", "conv1d_norm_pack_weights",
                      "conv1d_norm_check", "conv1d_norm_run_static_scratch", "conv1d_norm_set_profiling",
@@ -252,6 +258,45 @@ def conv_transpose3d(x, w, b=None, stride: int = 2, pad: int = 1, out_pad: int =
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     conv_transpose3d_run(p, x.data_ptr(), w.data_ptr(), _ptr(b), out.data_ptr(),
                          workspace.data_ptr() if need else None, need, torch.cuda.current_stream(x.device).cuda_stream)
+    return out
+
+
+def conv_transpose3d_ln_avgpool3d_gelu_workspace_size(params: ConvT3dParams) -> int:
+    """Workspace bytes of the fused model kernel."""
+    n = ctypes.c_size_t(0)
+    _check(load().conv_transpose3d_ln_avgpool3d_gelu_workspace_size(ctypes.byref(params), ctypes.byref(n)))
+    return n.value
+
+
+def conv_transpose3d_ln_avgpool3d_gelu_run(params: ConvT3dParams, eps: float, sum_weight: float, x: int, w: int,
+                                           b: Optional[int], gamma: Optional[int], beta: Optional[int], out: int,
+                                           workspace: int, workspace_bytes: int, stream: int) -> None:
+    """[p4]'s whole model in one pass (see the C header)."""
+    _check(load().conv_transpose3d_ln_avgpool3d_gelu_run(ctypes.byref(params), eps, sum_weight, x, w, b, gamma, beta,
+                                                         out, workspace, workspace_bytes, stream))
+
+
+def conv_transpose3d_ln_avgpool3d_gelu(x, w, b, sum_weight: float, gamma=None, beta=None, eps: float = 1e-5,
+                                       stride: int = 2, pad: int = 1, out_pad: int = 1, out=None, workspace=None):
+    """Torch convenience wrapper: x [N, 32, D, H, 32], w [32, 64, 3, 3, 3] float32 CUDA tensors
+    (contiguous) -> a new (or the given) [N, 64, D, H, 32] float32 tensor on the current stream:
+    GELU(AvgPool3d(2)(LayerNorm_W(ConvTranspose3d(x) + sum_weight))). The workspace (a uint8 CUDA
+    tensor) is allocated here when none is given."""
+    import torch
+    for t in (x, w):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("x and w must be contiguous float32 CUDA tensors")
+    N, C_in, D, H, W = x.shape
+    C_out, k = w.shape[1], w.shape[2]
+    if out is None:
+        out = torch.empty((N, C_out, D, H, W), dtype=torch.float32, device=x.device)
+    p = ConvT3dParams(N, C_in, C_out, D, H, W, k, stride, pad, out_pad, 2)
+    need = conv_transpose3d_ln_avgpool3d_gelu_workspace_size(p)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    conv_transpose3d_ln_avgpool3d_gelu_run(p, eps, sum_weight, x.data_ptr(), w.data_ptr(), _ptr(b), _ptr(gamma),
+                                           _ptr(beta), out.data_ptr(), workspace.data_ptr(), need,
+                                           torch.cuda.current_stream(x.device).cuda_stream)
     return out
 
 

@@ -705,6 +705,18 @@ c1n_status convt3d_plan(const c1n_convt3d_params* p, bool* tc) {
     *tc = p->math == 2 || (p->math == 0 && tc_ok);
     return C1N_OK;
 }
+// The fused model kernel takes the page's shape only.
+c1n_status convt3d_fused_check(const c1n_convt3d_params* p) {
+    if (!p) return fail(C1N_ERR_INVALID_ARG, "params must be non-NULL");
+    if (p->N < 1 || p->C_in < 1 || p->C_out < 1 || p->D < 1 || p->H < 1 || p->W < 1)
+        return fail(C1N_ERR_INVALID_ARG, "N, C_in, C_out, D, H, W must be >= 1");
+    if (p->C_in != 32 || p->C_out != 64 || p->W != 32 || p->k != 3 || p->stride != 2 || p->pad != 1 || p->out_pad != 1)
+        return fail(C1N_ERR_UNSUPPORTED, "the fused model takes C_in 32, C_out 64, W 32, k 3, stride 2, pad 1, "
+                                         "output pad 1 (got C_in %d, C_out %d, W %d, k %d, stride %d, pad %d, output pad %d)",
+                    p->C_in, p->C_out, p->W, p->k, p->stride, p->pad, p->out_pad);
+    if ((long long)p->N * p->D * ((p->H + 3) / 4) > 0x7fffffffLL) return fail(C1N_ERR_UNSUPPORTED, "too many tiles");
+    return C1N_OK;
+}
 }  // namespace
 
 extern "C" {
@@ -945,6 +957,43 @@ c1n_status conv_transpose3d_run(const c1n_convt3d_params* p, const float* x, con
     return C1N_OK;
 }
 
-int32_t conv1d_norm_version(void) { return 113; }
+c1n_status conv_transpose3d_ln_avgpool3d_gelu_workspace_size(const c1n_convt3d_params* p, size_t* bytes) {
+    g_last_error.clear();
+    if (!bytes) return fail(C1N_ERR_INVALID_ARG, "bytes is NULL");
+    c1n_status st = convt3d_fused_check(p);
+    if (st != C1N_OK) return st;
+    *bytes = convt3d_lnpool_fused_workspace_bytes(*p);
+    return C1N_OK;
+}
+
+c1n_status conv_transpose3d_ln_avgpool3d_gelu_run(const c1n_convt3d_params* p, float eps, float sum_weight,
+                                                  const float* x, const float* w, const float* b,
+                                                  const float* gamma, const float* beta, float* out,
+                                                  void* workspace, size_t workspace_bytes, c1n_stream_t stream) {
+    g_last_error.clear();
+    c1n_status st = convt3d_fused_check(p);
+    if (st != C1N_OK) return st;
+    if (!(eps > 0.f)) return fail(C1N_ERR_INVALID_ARG, "eps must be > 0");
+    if (!x || !w || !out) return fail(C1N_ERR_INVALID_ARG, "x, w and out must be non-NULL");
+    const size_t need = convt3d_lnpool_fused_workspace_bytes(*p);
+    if (!workspace || workspace_bytes < need)
+        return fail(C1N_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? workspace_bytes : 0);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(C1N_ERR_ALIGNMENT, "workspace not 256-byte aligned");
+    if (!aligned16(x) || !aligned16(out)) return fail(C1N_ERR_ALIGNMENT, "x and out must be 16-byte aligned");
+    int dev = 0, sms = 0, major = 0, minor = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    if (!(major == 10 && minor == 3))
+        return fail(C1N_ERR_UNSUPPORTED, "the fused model kernel is built for sm_103a; device is sm_%d%d", major, minor);
+    e = launch_convt3d_lnpool_fused(*p, eps, sum_weight, x, w, b, gamma, beta, out, workspace, sms,
+                                    reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fused ConvTranspose3d + LayerNorm / AvgPool3d / GELU launch");
+    return C1N_OK;
+}
+
+int32_t conv1d_norm_version(void) { return 114; }
 
 }  // extern "C"

@@ -136,6 +136,13 @@ cudaError_t launch_ln_avgpool3d_gelu(const c1n_lnpool_params& p, const float* z,
 cudaError_t launch_conv_transpose3d(const c1n_convt3d_params& p, const float* x, const float* w, const float* b,
                                     float* y, cudaStream_t stream);
 size_t convt3d_tc_workspace_bytes(const c1n_convt3d_params& p);
+// [p4]'s model in one tensor-core kernel (C_in 32, C_out 64, W 32, output pad 1; p validated):
+// ConvTranspose3d with + sum_weight, LayerNorm over W_out = 64, AvgPool3d(2) and GELU in the
+// epilogue; workspace: status word, channels-last x, the two channel halves' packed weights.
+size_t convt3d_lnpool_fused_workspace_bytes(const c1n_convt3d_params& p);
+cudaError_t launch_convt3d_lnpool_fused(const c1n_convt3d_params& p, float eps, float sum_weight, const float* x,
+                                        const float* w, const float* b, const float* gamma, const float* beta,
+                                        float* out, void* workspace, int num_sms, cudaStream_t stream);
 cudaError_t launch_conv_transpose3d_tc(const c1n_convt3d_params& p, const float* x, const float* w, const float* b,
                                        float* y, void* workspace, int num_sms, cudaStream_t stream);
 

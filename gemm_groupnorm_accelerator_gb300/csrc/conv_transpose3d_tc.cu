@@ -34,6 +34,7 @@
 #include <mutex>
 
 #include "c1n_internal.h"
+#include "c1n_math.cuh"
 #include "sm100_ptx.cuh"
 
 namespace c1n {
@@ -305,6 +306,334 @@ __global__ void __launch_bounds__(256) pack_convt_weights_kernel(const float* __
     }
 }
 
+// ------------------------------------------------------------------------------------------------
+// [p4]'s whole model after its weights in one kernel: the transposed convolution above, with the
+// scalar add, LayerNorm over the output's last dimension, AvgPool3d(2) and GELU in its epilogue.
+//
+// With output pad 1 and W = 32 (so W_out = 64, the LayerNorm width), the outputs of a tile of
+// 4 input rows x the 32 input columns of one input depth i, over all four (pd, ph) classes and both
+// width parities, are everything two things need: each LayerNorm row (co, od = 2i + pd, oh = 2j + ph),
+// 64 values along ow = 2l + pw, lies in one warp (lane l holds ow = 2l and 2l + 1), and the 2 x 2 x 2
+// pooling window of output (co, i, j, l) is exactly the eight (pd, ph, pw) outputs of input voxel
+// (j, l), i.e. one thread. The convolution's output never leaves the SM.
+//
+// A CTA owns one half of the 64 channels (32) and accumulates all four classes of a tile at once,
+// at accumulator column pw * 128 + pos * 32 + co, pos(pd, ph): (0,0) -> 0, (0,1) -> 1, (1,1) -> 2,
+// (1,0) -> 3. The classes an input shift delta = (dd, dh, dw) feeds (pd >= dd, ph >= dh) are then a
+// contiguous pos range: all four, {1, 2}, {2, 3} or {2}; and dw = 1 feeds width parity 1 only. So
+// per tile each of the eight shifted x boxes is loaded once, and its MMAs (K = 32) cover one or two
+// contiguous column ranges (N = 256, 128, 64 or 32) -- 864 of the 1152 columns x shifts of the
+// per-class form, i.e. no MMA on a tap that does not exist. The half's weight rows for every
+// (shift, column) in that order (864 rows x 32 channels, TF32) stay in shared memory.
+//
+// Roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-9 epilogue.
+// Epilogue warp w reads TMEM lane quarter q = w & 3 (input row 4 jt + q, column l = lane) and the
+// two classes pos = 2e, 2e + 1 (e = (w - 2) >> 2): per class and channel, the 64-value row's mean
+// and then variance by reduce-scatters over the warp (lane c ends with channel c's sum), affine,
+// and the class's two width parities added into the pool sum; the two warps of a quarter add
+// their sums through shared memory, and one writes GELU(sum / 8) for its 32 voxels, 128 contiguous
+// bytes per channel. Two accumulators of 256 columns: the epilogue of one tile overlaps the next
+// tile's MMAs. Every wait is bounded.
+constexpr int kFThreads = 320;
+constexpr int kFStages = 6;            // x ring stages
+constexpr int kFRows = 864;            // weight rows of one channel half
+constexpr int kFWBytes = kFRows * 128;
+
+// Columns of the pos range that shift (dd, dh) feeds: first pos and count.
+__host__ __device__ constexpr int fz_pos0(int dd, int dh) { return dd == 0 ? (dh == 0 ? 0 : 1) : 2; }
+__host__ __device__ constexpr int fz_npos(int dd, int dh) { return dd == 0 ? (dh == 0 ? 4 : 2) : (dh == 0 ? 2 : 1); }
+// Weight rows of shift s = 4 dd + 2 dh + dw (two width parities when dw = 0) and where they start.
+__host__ __device__ constexpr int fz_rows(int s) { return ((s & 1) ? 1 : 2) * 32 * fz_npos(s >> 2, (s >> 1) & 1); }
+__host__ __device__ constexpr int fz_row0(int s) {
+    int r = 0;
+    for (int i = 0; i < s; ++i) r += fz_rows(i);
+    return r;
+}
+static_assert(fz_row0(8) == kFRows, "weight row count");
+// (pd, ph) of column position pos
+__host__ __device__ constexpr int fz_pd(int pos) { return pos >= 2 ? 1 : 0; }
+__host__ __device__ constexpr int fz_ph(int pos) { return (pos == 1 || pos == 2) ? 1 : 0; }
+
+__device__ __forceinline__ void lds_vec8(const float* p, float (&o)[8]) {
+    const float4 u = *reinterpret_cast<const float4*>(p), v = *reinterpret_cast<const float4*>(p + 4);
+    o[0] = u.x; o[1] = u.y; o[2] = u.z; o[3] = u.w;
+    o[4] = v.x; o[5] = v.y; o[6] = v.z; o[7] = v.w;
+}
+
+// Reduce-scatter over the warp of 32 per-lane values: lane c ends with the sum over all lanes of
+// value c in v[0] (five exchange rounds, each halving the values a lane keeps).
+__device__ __forceinline__ void reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+        const bool upper = (lane & d) != 0;
+#pragma unroll
+        for (int i = 0; i < d; ++i) {
+            const float send = upper ? v[i] : v[i + d];
+            const float keep = upper ? v[i + d] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+        }
+    }
+}
+
+struct FusedArgs {
+    int N, D, H, JT;
+    float eps, sum_weight;
+    const float* bias;   // [64] or null
+    const float* gamma;  // [64] (LayerNorm over W_out) or null
+    const float* beta;   // [64] or null
+    float* out;          // [N][64][D][H][32]
+    int* status;
+};
+
+__global__ void __launch_bounds__(kFThreads, 1)
+    convt3d_lnpool_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__ CUtensorMap tm_x,
+                                const __grid_constant__ CUtensorMap tm_w) {
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ float s_bias[32];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = int(blockIdx.x & 1u);
+    const int cta_in = int(blockIdx.x >> 1), n_cta = int(gridDim.x >> 1);
+    const int tiles = a.N * a.D * a.JT;
+    // shared memory: weights | x ring | pool exchange [4][32][32] | statistics [8][2][32] | barriers
+    const uint32_t sW = smem_u32(base);
+    const uint32_t sX = sW + uint32_t(kFWBytes);
+    float* xch = reinterpret_cast<float*>(base + kFWBytes + kFStages * kTileBytes);
+    float* stat = xch + 4 * 32 * 32;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stat + 8 * 2 * 32);
+    const uint32_t bar0 = smem_u32(bars);
+    auto bar = [&](int i) { return bar0 + 8u * uint32_t(i); };
+    const int i_wfull = 0, i_xfull = 1, i_xempty = 1 + kFStages, i_accfull = 1 + 2 * kFStages,
+              i_accempty = i_accfull + 2, i_drain = i_accempty + 2, n_bars = i_drain + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + n_bars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    if (warp == 0) {
+        if (lane < n_bars) mbar_init(bar(lane), (lane >= i_accempty && lane < i_drain) ? 8u : 1u);
+        if (lane == 0) *abort_flag = 0;
+        fence_mbar_init();
+        if (lane == 0) {
+            prefetch_tensormap(&tm_x);
+            prefetch_tensormap(&tm_w);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512u);
+        tmem_relinquish();
+    }
+    if (threadIdx.x >= 64 && threadIdx.x < 96) {
+        const int co = half * 32 + (threadIdx.x - 64);
+        s_bias[threadIdx.x - 64] = a.bias ? __ldg(a.bias + co) : 0.f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    auto wait = [&](int i, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar(i), parity)) return true;
+        return mbar_wait(bar(i), parity, abort_flag, a.status, 0, nullptr);
+    };
+    auto wait_warp = [&](int i, uint32_t parity) -> bool { return __all_sync(0xffffffffu, wait(i, parity)); };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        long long x_cnt = 0;
+        int xi = 0;
+        uint32_t xph = 0;
+        if (elect_one()) {
+            mbar_arrive_expect_tx(bar(i_wfull), uint32_t(kFWBytes));
+            for (int m = 0; m < kFRows / 96; ++m)
+                tma_load_2d(sW + uint32_t(m * 96 * 128), &tm_w, bar(i_wfull), 0, half * kFRows + m * 96);
+        }
+        __syncwarp();
+        for (int t = cta_in; t < tiles && !__any_sync(0xffffffffu, *abort_flag != 0); t += n_cta) {
+            const int jt = t % a.JT, i = (t / a.JT) % a.D, n = t / (a.JT * a.D);
+            for (int s = 0; s < 8; ++s) {
+                if (!wait_warp(i_xempty + xi, xph ^ 1)) goto prod_done;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(bar(i_xfull + xi), kTileBytes);
+                    tma_load_5d(sX + uint32_t(xi * kTileBytes), &tm_x, bar(i_xfull + xi), 0, s & 1, jt * 4 + ((s >> 1) & 1),
+                                i + (s >> 2), n);
+                }
+                __syncwarp();
+                ++x_cnt;
+                if (++xi == kFStages) { xi = 0; xph ^= 1; }
+            }
+        }
+    prod_done:
+        if (*abort_flag && lane == 0) {
+            drain_wait(bar(i_wfull), 0);
+            for (int s2 = 0; s2 < kFStages; ++s2)
+                if (x_cnt > s2) drain_wait(bar(i_xfull + s2), s2 < xi ? xph : (xph ^ 1));
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        const uint32_t idesc32 = make_idesc(2u, 2u, 0u, 0u, 128u, 32u), idesc64 = make_idesc(2u, 2u, 0u, 0u, 128u, 64u),
+                       idesc128 = make_idesc(2u, 2u, 0u, 0u, 128u, 128u), idesc256 = make_idesc(2u, 2u, 0u, 0u, 128u, 256u);
+        auto idesc_of = [&](int n) { return n == 256 ? idesc256 : n == 128 ? idesc128 : n == 64 ? idesc64 : idesc32; };
+        const uint32_t wl0 = desc_lo_sw128(sW);
+        int xi = 0, lt_ = 0;
+        uint32_t xph = 0;
+        bool ok = wait_warp(i_wfull, 0);
+        tc_fence_after();
+        for (int t = cta_in; ok && t < tiles; t += n_cta, ++lt_) {
+            const int ab = lt_ & 1;
+            const uint32_t acc_par = uint32_t((lt_ >> 1) & 1);
+            if (!wait_warp(i_accempty + ab, acc_par ^ 1)) break;
+            tc_fence_after();
+            const uint32_t d = tmem_base + uint32_t(256 * ab);
+            for (int s = 0; s < 8; ++s) {
+                if (!wait_warp(i_xfull + xi, xph)) { ok = false; break; }
+                tc_fence_after();
+                const int dd = s >> 2, dh = (s >> 1) & 1, dw = s & 1;
+                const int ncol = 32 * fz_npos(dd, dh), col0 = 32 * fz_pos0(dd, dh), row0 = fz_row0(s);
+                const uint32_t xl = desc_lo_sw128(sX + uint32_t(xi * kTileBytes));
+                if (elect_one()) {
+                    if (dw == 0 && ncol == 128) {
+                        // both width parities over all four classes: columns 0 .. 255 in one MMA
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_issue<false, false>(d, xl + 2u * k, wl0 + uint32_t(row0 * 8) + 2u * k, idesc256, (s | k) != 0 ? 1u : 0u);
+                    } else {
+                        for (int pw = dw; pw < 2; ++pw) {
+                            const uint32_t wl = wl0 + uint32_t((row0 + (dw ? 0 : pw * ncol)) * 8);
+                            const uint32_t dc = d + uint32_t(pw * 128 + col0);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) mma_issue<false, false>(dc, xl + 2u * k, wl + 2u * k, idesc_of(ncol), 1u);
+                        }
+                    }
+                    mma_commit(bar(i_xempty + xi));
+                }
+                __syncwarp();
+                if (++xi == kFStages) { xi = 0; xph ^= 1; }
+            }
+            if (!ok) break;
+            if (elect_one()) mma_commit(bar(i_accfull + ab));
+            __syncwarp();
+        }
+        if (elect_one()) mma_commit(bar(i_drain));
+        __syncwarp();
+        if (lane == 0) drain_wait(bar(i_drain), 0);
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 2..9)
+        const int q = warp & 3, e = (warp - 2) >> 2;
+        const int ew = warp - 2;
+        float* st_mean = stat + ew * 64;
+        float* st_rstd = st_mean + 32;
+        float* xq = xch + q * 1024;  // [32 channels][32 lanes]
+        // LayerNorm affine of this lane's two output columns ow = 2 lane, 2 lane + 1
+        const float g0 = a.gamma ? __ldg(a.gamma + 2 * lane) : 1.f, g1 = a.gamma ? __ldg(a.gamma + 2 * lane + 1) : 1.f;
+        const float bsum = (a.beta ? __ldg(a.beta + 2 * lane) + __ldg(a.beta + 2 * lane + 1) : 0.f);
+        const float sw = a.sum_weight;
+        int lt_ = 0;
+        for (int t = cta_in; t < tiles; t += n_cta, ++lt_) {
+            const int ab = lt_ & 1;
+            const uint32_t acc_par = uint32_t((lt_ >> 1) & 1);
+            int got = 0;
+            if (lane == 0) got = wait(i_accfull + ab, acc_par);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (named_bar_any(1, 256, !got || *abort_flag != 0)) break;
+            tc_fence_after();
+            const int jt = t % a.JT, i = (t / a.JT) % a.D, n = t / (a.JT * a.D);
+            const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
+            float pool[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) pool[c] = 0.f;
+#pragma unroll 1
+            for (int pp = 0; pp < 2; ++pp) {
+                const int pos = 2 * e + pp;
+                float v0[32], v1[32], tv[32];
+                tmem_load32(tb + uint32_t(pos * 32), v0);        // width parity 0, channels 0..31
+                tmem_load32(tb + uint32_t(128 + pos * 32), v1);  // width parity 1
+                if (pp == 1) {
+                    // every column this warp needs from the accumulator is in registers
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(i_accempty + ab));
+                }
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float bb = s_bias[c] + sw;
+                    v0[c] += bb;
+                    v1[c] += bb;
+                    tv[c] = v0[c] + v1[c];
+                }
+                reduce_scatter32(tv, lane);  // lane c: the row sum of channel c
+                st_mean[lane] = tv[0] * (1.f / 64.f);
+                __syncwarp();
+#pragma unroll
+                for (int h = 0; h < 32; h += 8) {
+                    float m8[8];
+                    lds_vec8(st_mean + h, m8);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        v0[h + c] -= m8[c];
+                        v1[h + c] -= m8[c];
+                        tv[h + c] = fmaf(v0[h + c], v0[h + c], v1[h + c] * v1[h + c]);
+                    }
+                }
+                reduce_scatter32(tv, lane);  // lane c: the row sum of squared deviations of channel c
+                st_rstd[lane] = rsqrtf(tv[0] * (1.f / 64.f) + a.eps);
+                __syncwarp();
+#pragma unroll
+                for (int h = 0; h < 32; h += 8) {
+                    float r8[8];
+                    lds_vec8(st_rstd + h, r8);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) pool[h + c] += fmaf(r8[c], fmaf(g0, v0[h + c], g1 * v1[h + c]), bsum);
+                }
+                __syncwarp();  // the statistics slots are read before the next class overwrites them
+            }
+            // the quarter's two warps add their classes; warp e = 0 writes the pooled output
+            if (e == 1) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) xq[c * 32 + lane] = pool[c];
+            }
+            named_bar_sync(2 + q, 64);
+            if (e == 0) {
+                const int hin = jt * 4 + q;
+                if (hin < a.H) {
+                    float* dst = a.out + ((size_t(n) * 64 + size_t(half * 32)) * a.D + size_t(i)) * size_t(a.H) * 32 +
+                                 size_t(hin) * 32 + size_t(lane);
+                    const size_t cstride = size_t(a.D) * a.H * 32;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) dst[size_t(c) * cstride] = gelu_erf((pool[c] + xq[c * 32 + lane]) * 0.125f);
+                }
+            }
+            named_bar_sync(2 + q, 64);  // the exchange slots are read before the next tile refills them
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512u);
+    }
+}
+
+// The weights of the fused kernel: per channel half, row fz_row0(s) + r of shift s = (dd, dh, dw)
+// holds, for accumulator column pw * 128 + pos * 32 + co (in the kernel's column order), the 32
+// input channels of tap (k(pd, dd), k(ph, dh), k(pw, dw)), TF32-rounded; k(0, 0) = 1, k(1, 0) = 2,
+// k(1, 1) = 0.
+__global__ void __launch_bounds__(256) pack_fused_weights_kernel(const float* __restrict__ w, float* __restrict__ wp) {
+    const int half = blockIdx.y;
+    const int r = blockIdx.x * 8 + (threadIdx.x >> 5), ci = threadIdx.x & 31;
+    if (r >= kFRows) return;
+    int s = 0;
+    while (s < 7 && r >= fz_row0(s + 1)) ++s;
+    const int dd = s >> 2, dh = (s >> 1) & 1, dw = s & 1;
+    const int ncol = 32 * fz_npos(dd, dh);
+    int lr = r - fz_row0(s);
+    int pw = 1;
+    if (dw == 0) {
+        pw = lr / ncol;
+        lr -= pw * ncol;
+    }
+    const int pos = fz_pos0(dd, dh) + lr / 32, co = half * 32 + lr % 32;
+    auto tap = [](int p, int dl) { return p == 0 ? 1 : (dl == 0 ? 2 : 0); };
+    const int kd = tap(fz_pd(pos), dd), kh = tap(fz_ph(pos), dh), kw = tap(pw, dw);
+    wp[((size_t)half * kFRows + r) * 32 + ci] = round_tf32(__ldg(w + (((ci * 64 + co) * 3 + kd) * 3 + kh) * 3 + kw));
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -399,6 +728,64 @@ cudaError_t launch_conv_transpose3d_tc(const c1n_convt3d_params& p, const float*
     e = cudaFuncSetAttribute(convt3d_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     convt3d_tc_kernel<<<grid, kThreads, smem, stream>>>(a, tm_x, tm_w);
+    return cudaGetLastError();
+}
+
+size_t convt3d_lnpool_fused_workspace_bytes(const c1n_convt3d_params& p) {
+    const size_t xcl = (size_t)p.N * p.C_in * p.D * p.H * p.W * 4;
+    return 256 + ((xcl + 1023) / 1024) * 1024 + 2 * (size_t)kFWBytes;
+}
+
+cudaError_t launch_convt3d_lnpool_fused(const c1n_convt3d_params& p, float eps, float sum_weight, const float* x,
+                                        const float* w, const float* b, const float* gamma, const float* beta,
+                                        float* out, void* workspace, int num_sms, cudaStream_t stream) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* status = reinterpret_cast<int*>(ws);
+    const size_t xcl_bytes = ((size_t)p.N * p.C_in * p.D * p.H * p.W * 4 + 1023) / 1024 * 1024;
+    float* xcl = reinterpret_cast<float*>(ws + 256);
+    float* wp = reinterpret_cast<float*>(ws + 256 + xcl_bytes);
+    cudaError_t e = cudaMemsetAsync(status, 0, 256, stream);
+    if (e != cudaSuccess) return e;
+    const long long S = (long long)p.D * p.H * p.W;
+    to_channels_last32_kernel<<<dim3((unsigned)((S + 127) / 128), (unsigned)p.N), 256, 0, stream>>>(x, xcl, S);
+    pack_fused_weights_kernel<<<dim3(kFRows / 8, 2), 256, 0, stream>>>(w, wp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tm_x, tm_w;
+    {
+        const cuuint64_t dims[5] = {32, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)p.D, (cuuint64_t)p.N};
+        const cuuint64_t str[4] = {32 * 4, (cuuint64_t)p.W * 32 * 4, (cuuint64_t)p.H * p.W * 32 * 4,
+                                   (cuuint64_t)p.D * p.H * p.W * 32 * 4};
+        const cuuint32_t box[5] = {32, 32, 4, 1, 1};
+        if (!encode_f32(&tm_x, xcl, 5, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {32, 2 * kFRows};
+        const cuuint64_t str[1] = {32 * 4};
+        const cuuint32_t box[2] = {32, 96};
+        if (!encode_f32(&tm_w, wp, 2, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    FusedArgs a;
+    a.N = p.N;
+    a.D = p.D;
+    a.H = p.H;
+    a.JT = (p.H + 3) / 4;
+    a.eps = eps;
+    a.sum_weight = sum_weight;
+    a.bias = b;
+    a.gamma = gamma;
+    a.beta = beta;
+    a.out = out;
+    a.status = status;
+    // persistent: pairs of CTAs (one per channel half) walk the tiles
+    const long long tiles = (long long)p.N * p.D * a.JT;
+    long long pairs = num_sms / 2;
+    if (pairs > tiles) pairs = tiles;
+    if (pairs < 1) pairs = 1;
+    const int smem = 1024 + kFWBytes + kFStages * kTileBytes + 4 * 32 * 32 * 4 + 8 * 2 * 32 * 4 + 256;
+    e = cudaFuncSetAttribute(convt3d_lnpool_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    convt3d_lnpool_fused_kernel<<<(unsigned)(2 * pairs), kFThreads, smem, stream>>>(a, tm_x, tm_w);
     return cudaGetLastError();
 }
 

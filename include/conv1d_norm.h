@@ -276,6 +276,32 @@ c1n_status conv_transpose3d_workspace_size(const c1n_convt3d_params* p, size_t* 
 c1n_status conv_transpose3d_run(const c1n_convt3d_params* p, const float* x, const float* w, const float* b, float* y,
                                 void* workspace, size_t workspace_bytes, c1n_stream_t stream);
 
+/* [p4]'s whole model after its weights in one pass (Kimi-K2.6 l2_p3 page: ConvTranspose3d, then
+ * + sum_weight, LayerNorm over the last dimension, AvgPool3d(kernel 2, stride 2), exact GELU):
+ *
+ *   y   = ConvTranspose3d(x; w, b)                     as conv_transpose3d_run defines it
+ *   out[n][c][i][j][l] = GELU( mean over a, b2, e in {0,1} of
+ *                              LN(y + sum_weight)[n][c][2i+a][2j+b2][2l+e] )
+ *   LN over the last dimension (W_out = 64 values): (v - mean) / sqrt(var + eps) * gamma[w] + beta[w],
+ *   population variance; gamma, beta [64] (NULL: 1 and 0).
+ *
+ *   - x [N][32][D][H][32], w [32][64][3][3][3], b [64] or NULL; out [N][64][D][H][32] (the pooled
+ *     output has the input's spatial extent); fp32, dense, caller-owned; x and out 16-byte aligned.
+ *   - Taken: C_in 32, C_out 64, W 32, k 3, stride 2, pad 1, output pad 1 (the page's model), D, H,
+ *     N >= 1, eps > 0; other shapes C1N_ERR_UNSUPPORTED (run conv_transpose3d_run, then
+ *     ln_avgpool3d_gelu_run). `math` is ignored (tensor cores: TF32 operands, fp32 accumulation and
+ *     statistics). Needs an sm_103a device.
+ *   - The convolution's output stays on chip: x is read once (after a channels-last copy into the
+ *     workspace) and out written once.
+ *   - workspace: conv_transpose3d_ln_avgpool3d_gelu_workspace_size() bytes, 256-byte aligned,
+ *     caller-owned (status word, channels-last x, packed weights). Asynchronous on `stream`; no
+ *     allocation; three kernels. */
+c1n_status conv_transpose3d_ln_avgpool3d_gelu_workspace_size(const c1n_convt3d_params* p, size_t* bytes);
+c1n_status conv_transpose3d_ln_avgpool3d_gelu_run(const c1n_convt3d_params* p, float eps, float sum_weight,
+                                                  const float* x, const float* w, const float* b,
+                                                  const float* gamma, const float* beta, float* out,
+                                                  void* workspace, size_t workspace_bytes, c1n_stream_t stream);
+
 /* Library version: major*10000 + minor*100 + patch. */
 int32_t conv1d_norm_version(void);
 

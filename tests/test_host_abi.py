@@ -244,3 +244,31 @@ def test_conv_transpose3d_validation_without_device():
     with pytest.raises(c1n.C1NError) as e:  # the tensor-core plan without its workspace
         c1n.conv_transpose3d_run(p(C_in=32, W=32), x, x, None, x, None, 0, 0)
     assert e.value.status == c1n.ERR_WORKSPACE
+
+
+def test_fused_p4_model_validation_without_device():
+    # the one-pass model takes the page's shape only (C_in 32, C_out 64, W 32, k 3, stride 2, pad 1,
+    # output pad 1); everything is checked before any device call
+    p = lambda **kw: c1n.ConvT3dParams(*[kw.get(k, v) for k, v in (("N", 2), ("C_in", 32), ("C_out", 64), ("D", 3),
+                                                                   ("H", 5), ("W", 32), ("k", 3), ("stride", 2),
+                                                                   ("pad", 1), ("out_pad", 1), ("math", 0))])
+    x = ctypes.c_void_p(4096).value
+    need = c1n.conv_transpose3d_ln_avgpool3d_gelu_workspace_size(p())
+    # status word + channels-last x + two channel halves of 864 packed weight rows
+    assert need == 256 + (2 * 32 * 3 * 5 * 32 * 4 + 1023) // 1024 * 1024 + 2 * 864 * 128
+    for params, status in ((p(N=0), c1n.ERR_INVALID_ARG), (p(W=16), c1n.ERR_UNSUPPORTED),
+                           (p(C_in=16), c1n.ERR_UNSUPPORTED), (p(C_out=32), c1n.ERR_UNSUPPORTED),
+                           (p(out_pad=0), c1n.ERR_UNSUPPORTED), (p(k=5), c1n.ERR_UNSUPPORTED)):
+        with pytest.raises(c1n.C1NError) as e:
+            c1n.conv_transpose3d_ln_avgpool3d_gelu_run(params, 1e-5, 1.0, x, x, None, None, None, x, x, need, 0)
+        assert e.value.status == status
+    bad = ((dict(eps=0.0), c1n.ERR_INVALID_ARG), (dict(x=None), c1n.ERR_INVALID_ARG),
+           (dict(ws_bytes=need - 1), c1n.ERR_WORKSPACE), (dict(ws=x + 16), c1n.ERR_ALIGNMENT),
+           (dict(out=x + 4), c1n.ERR_ALIGNMENT))
+    for kw, status in bad:
+        a = dict(eps=1e-5, x=x, out=x, ws=x, ws_bytes=need)
+        a.update(kw)
+        with pytest.raises(c1n.C1NError) as e:
+            c1n.conv_transpose3d_ln_avgpool3d_gelu_run(p(), a["eps"], 1.0, a["x"], x, None, None, None, a["out"], a["ws"],
+                                                       a["ws_bytes"], 0)
+        assert e.value.status == status

@@ -153,3 +153,72 @@ def test_p4_pipeline_full_size_sampled(cuda_lib, math):
         err = float(np.max(np.abs(out[n].cpu().numpy().astype(np.float64) - ref)))
         assert err <= tol_out, f"pipeline sample {n}: max abs err {err:.3e}"
         print(f"math {math} sample {n}: conv err {err_y:.2e}, pipeline err {err:.2e}")
+
+
+# ------------------------------------------------------------------ the whole model in one kernel
+
+FUSED = {
+    "fused_one_row": synth.CONV_TRANSPOSE3D.replace(N=1, D=1, H=1),
+    "fused_ragged_h": synth.CONV_TRANSPOSE3D.replace(N=2, D=3, H=5),
+    "fused_h8": synth.CONV_TRANSPOSE3D.replace(N=1, D=2, H=8),
+}
+
+
+def _fused_gpu(c1n, wl, inp, gb, lp, affine=True, bias=True):
+    x = torch.from_numpy(inp["x"]).cuda()
+    w = torch.from_numpy(inp["w"]).cuda()
+    b = torch.from_numpy(inp["b"]).cuda() if bias else None
+    ga = torch.from_numpy(gb["gamma"]).cuda() if affine else None
+    be = torch.from_numpy(gb["beta"]).cuda() if affine else None
+    out = torch.full((x.shape[0], wl.C_out, wl.D, wl.H, wl.W), float("nan"), dtype=torch.float32, device="cuda")
+    c1n.conv_transpose3d_ln_avgpool3d_gelu(x, w, b, lp.sum_weight, ga, be, eps=lp.eps, out=out)
+    torch.cuda.synchronize()
+    return out
+
+
+def _model_oracle(wl, inp, gb, lp, n, affine=True, bias=True):
+    y = oracle.conv_transpose3d(inp["x"][n:n + 1], inp["w"], inp["b"] if bias else None, stride=wl.stride, pad=wl.pad,
+                                out_pad=wl.out_pad)
+    return oracle.ln_avgpool3d_gelu(y[0].astype(np.float32), lp.eps, lp.sum_weight, gb["gamma"] if affine else None,
+                                    gb["beta"] if affine else None)
+
+
+TOL_FUSED = 2e-2  # TF32 operands into a LayerNorm (the same bound as the two-kernel pipeline on the tensor cores)
+
+
+@pytest.mark.parametrize("name", list(FUSED))
+@pytest.mark.parametrize("affine,bias", [(True, True), (False, False)])
+def test_fused_model_small(cuda_lib, name, affine, bias):
+    wl = FUSED[name]
+    lp = synth.LN_AVGPOOL3D_GELU
+    inp = synth.make_convt3d_inputs(wl)
+    gb = synth.make_lnpool_inputs(lp.replace(N=1, C=1, D=2, H=2))
+    got = _fused_gpu(cuda_lib, wl, inp, gb, lp, affine, bias).cpu().numpy()
+    assert np.all(np.isfinite(got)), "unwritten outputs"
+    for n in range(wl.N):
+        ref = _model_oracle(wl, inp, gb, lp, n, affine, bias)
+        err = float(np.max(np.abs(got[n].astype(np.float64) - ref)))
+        assert err <= TOL_FUSED, f"{name} sample {n}: max abs err {err:.3e}"
+
+
+def test_fused_model_full_size(cuda_lib):
+    # the page's model at full size: the one-pass kernel against the oracle on two samples, and
+    # against the two-kernel path (tensor-core ConvTranspose3d, then the LayerNorm/pool/GELU pass)
+    # everywhere -- both use the same TF32 products, so they agree far inside the oracle tolerance
+    wl = synth.CONV_TRANSPOSE3D
+    lp = synth.LN_AVGPOOL3D_GELU
+    inp = synth.make_convt3d_inputs(wl)
+    gb = synth.make_lnpool_inputs(lp.replace(N=1, C=1, D=2, H=2))
+    fused = _fused_gpu(cuda_lib, wl, inp, gb, lp)
+    y = _convt_gpu(cuda_lib, wl, inp, math=2)
+    ga, be = torch.from_numpy(gb["gamma"]).cuda(), torch.from_numpy(gb["beta"]).cuda()
+    two = cuda_lib.ln_avgpool3d_gelu(y, lp.sum_weight, ga, be, eps=lp.eps)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(fused).all())
+    diff = float((fused - two).abs().max())
+    assert diff <= 1e-3, f"fused vs two-kernel path: max abs diff {diff:.3e}"
+    for n in (0, wl.N - 1):
+        ref = _model_oracle(wl, inp, gb, lp, n)
+        err = float(np.max(np.abs(fused[n].cpu().numpy().astype(np.float64) - ref)))
+        assert err <= TOL_FUSED, f"sample {n}: max abs err {err:.3e}"
+        print(f"fused sample {n}: err {err:.2e}; vs two-kernel path {diff:.2e}")
