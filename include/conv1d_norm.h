@@ -292,7 +292,9 @@ c1n_status conv_transpose3d_run(const c1n_convt3d_params* p, const float* x, con
  *     ln_avgpool3d_gelu_run). `math` is ignored (tensor cores: TF32 operands, fp32 accumulation and
  *     statistics). Needs an sm_103a device.
  *   - The convolution's output stays on chip: x is read once (after a channels-last copy into the
- *     workspace) and out written once.
+ *     workspace) and out written once. b and sum_weight are constant along every LayerNorm row and
+ *     cancel in it (LN(v + const) = LN(v)); they are accepted for the model's definition and do not
+ *     change the result.
  *   - workspace: conv_transpose3d_ln_avgpool3d_gelu_workspace_size() bytes, 256-byte aligned,
  *     caller-owned (status word, channels-last x, packed weights). Asynchronous on `stream`; no
  *     allocation; three kernels. */
