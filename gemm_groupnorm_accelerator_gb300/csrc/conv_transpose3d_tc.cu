@@ -330,18 +330,19 @@ __global__ void __launch_bounds__(256) pack_convt_weights_kernel(const float* __
 // ow), so they cancel in LayerNorm's centring: LN(y + b[co] + s) = LN(y) exactly. The kernel
 // normalizes the bare accumulators and reads neither.
 //
-// Roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-9 epilogue.
-// Epilogue warp w reads TMEM lane quarter q = w & 3 (input row 4 jt + q, column l = lane) and the
-// two classes pos = 2e, 2e + 1 (e = (w - 2) >> 2): per class and channel, the 64-value row's sum
-// and sum of squares (each lane's partial values transposed through the warp's shared-memory
-// scratch, so that lane c adds up channel c), mean and rstd, affine, and the class's two width
-// parities added into the pool sum; the two warps of a
-// quarter exchange half their sums through shared memory and each writes GELU(sum / 8) for 16
-// channels of its 32 voxels, 128 contiguous bytes per channel. Two accumulators of 256 columns:
-// the epilogue of one tile overlaps the next tile's MMAs. Every wait is bounded.
-constexpr int kFThreads = 320;
+// Roles (576 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-17 epilogue.
+// Epilogue warp w reads TMEM lane quarter q = w & 3 (input row 4 jt + q, column l = lane) and owns
+// channels 8g .. 8g + 7 (g = (w - 2) >> 2) of all four classes: per class and channel, the
+// 64-value row's sum and sum of squares (each lane's values transposed through the warp's shared
+// scratch and added up by column), mean and rstd, affine, and the class's two width parities added
+// into the pool sum; then GELU(sum / 8) for its 8 channels of the 32 voxels, 128 contiguous bytes
+// per channel. Sixteen epilogue warps at under 100 registers each keep four or five warps on every
+// scheduler to hide the latencies. Two accumulators of 256 columns: the epilogue of one tile
+// overlaps the next tile's MMAs. Every wait is bounded.
+constexpr int kFThreads = 576;          // warp 0 TMA, warp 1 MMA, warps 2-17 epilogue
+constexpr int kFEpiWarps = 16;
 constexpr int kFStages = 4;            // x ring stages
-constexpr int kFScr = 32 * 36;         // floats of one epilogue warp's transpose scratch [32 lanes][36]
+constexpr int kFScr = 32 * 20;         // floats of one epilogue warp's transpose scratch [32 lanes][20]
 constexpr int kFRows = 864;            // weight rows of one channel half
 constexpr int kFWBytes = kFRows * 128;
 
@@ -359,6 +360,19 @@ static_assert(fz_row0(8) == kFRows, "weight row count");
 // (pd, ph) of column position pos
 __host__ __device__ constexpr int fz_pd(int pos) { return pos >= 2 ? 1 : 0; }
 __host__ __device__ constexpr int fz_ph(int pos) { return (pos == 1 || pos == 2) ? 1 : 0; }
+
+// Load 8 consecutive 32-bit TMEM columns of this warp's 32 lanes (one lane per thread) and wait.
+__device__ __forceinline__ void tmem_load8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
 
 struct FusedArgs {
     int N, D, H, JT;
@@ -378,13 +392,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const int half = int(blockIdx.x & 1u);
     const int cta_in = int(blockIdx.x >> 1), n_cta = int(gridDim.x >> 1);
     const int tiles = a.N * a.D * a.JT;
-    // shared memory: weights | x ring | per epilogue warp a transpose scratch [32][36] | statistics
-    // [8][2][32] | barriers
+    // shared memory: weights | x ring | per epilogue warp a transpose scratch [32][20] and statistics
+    // [16] | barriers
     const uint32_t sW = smem_u32(base);
     const uint32_t sX = sW + uint32_t(kFWBytes);
     float* scratch = reinterpret_cast<float*>(base + kFWBytes + kFStages * kTileBytes);
-    float* stat = scratch + 8 * kFScr;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(stat + 8 * 2 * 32);
+    float* stat = scratch + kFEpiWarps * kFScr;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stat + kFEpiWarps * 16);
     const uint32_t bar0 = smem_u32(bars);
     auto bar = [&](int i) { return bar0 + 8u * uint32_t(i); };
     const int i_wfull = 0, i_xfull = 1, i_xempty = 1 + kFStages, i_accfull = 1 + 2 * kFStages,
@@ -392,7 +406,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + n_bars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     if (warp == 0) {
-        if (lane < n_bars) mbar_init(bar(lane), (lane >= i_accempty && lane < i_drain) ? 8u : 1u);
+        if (lane < n_bars) mbar_init(bar(lane), (lane >= i_accempty && lane < i_drain) ? uint32_t(kFEpiWarps) : 1u);
         if (lane == 0) *abort_flag = 0;
         fence_mbar_init();
         if (lane == 0) {
@@ -506,24 +520,23 @@ __global__ void __launch_bounds__(kFThreads, 1)
         if (lane == 0) drain_wait(bar(i_drain), 0);
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ epilogue (warps 2..9)
-        // The bias and the scalar add are constant along a LayerNorm row (one channel, all ow), so
-        // they cancel in v - mean(v): the rows are normalized straight from the accumulators. The
-        // row moments come from one sweep (sums of v and v^2 over 64 values of accumulators with no
-        // constant offset), in paired fp32 arithmetic.
-        const int q = warp & 3, e = (warp - 2) >> 2;
-        const int ew = warp - 2;
-        float* st_mean = stat + ew * 64;
-        float* st_rstd = st_mean + 32;
-        // this warp's scratch: the transposes of the row reductions, then the pool sums handed to
-        // the quarter's other warp ([16 channels][32 lanes]); the partner's scratch is read back
-        float* scr = scratch + ew * kFScr;
-        const float* pscr = scratch + (ew ^ 4) * kFScr;
+        // ------------------------------------------------------------ epilogue (warps 2..17)
+        // Warp w reads TMEM lane quarter q = w & 3 (input row 4 jt + q, column l = lane) and owns
+        // channels 8g .. 8g + 7 (g = (w - 2) >> 2) of all four classes, so it holds every value its
+        // pooled outputs need. The bias and the scalar add are constant along a LayerNorm row (one
+        // channel, all ow), so they cancel in v - mean(v): rows are normalized straight from the
+        // accumulators. Row moments (sum of v and of v^2 over the 64 values) in one sweep.
+        const int q = warp & 3, g = (warp - 2) >> 2, ew = warp - 2;
+        float* scr = scratch + ew * kFScr;  // [32 lanes][20]: 8 sums, 8 sums of squares, padding
+        float* st = stat + ew * 16;         // [8 means][8 rstd]
         // LayerNorm affine of this lane's two output columns ow = 2 lane, 2 lane + 1
         const float g0 = a.gamma ? __ldg(a.gamma + 2 * lane) : 1.f, g1 = a.gamma ? __ldg(a.gamma + 2 * lane + 1) : 1.f;
+        const float gs = g0 + g1;
         // the four classes' affine shifts, averaged with the pool's 1/8
         const float shift8 = 0.5f * (a.beta ? __ldg(a.beta + 2 * lane) + __ldg(a.beta + 2 * lane + 1) : 0.f);
-        const uint64_t gg0 = f2_pack(g0, g0), gg1 = f2_pack(g1, g1), ngs = f2_pack(-(g0 + g1), -(g0 + g1));
+        // column reads of the transpose: lane (col = lane & 15, rows 16 (lane >> 4) + ...), the upper
+        // half rotated by 4 rows so the two halves fall on different banks
+        const int rcol = lane & 15, rhi = lane >> 4;
         int lt_ = 0;
         for (int t = cta_in; t < tiles; t += n_cta, ++lt_) {
             const int ab = lt_ & 1;
@@ -531,128 +544,74 @@ __global__ void __launch_bounds__(kFThreads, 1)
             int got = 0;
             if (lane == 0) got = wait(i_accfull + ab, acc_par);
             got = __shfl_sync(0xffffffffu, got, 0);
-            if (named_bar_any(1, 256, !got || *abort_flag != 0)) break;
+            if (named_bar_any(1, 32 * kFEpiWarps, !got || *abort_flag != 0)) break;
             tc_fence_after();
             const int jt = t % a.JT, i = (t / a.JT) % a.D, n = t / (a.JT * a.D);
-            const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
-            uint64_t pool[16];  // channel pairs (2c, 2c + 1)
+            const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab + 8 * g);
+            float pool[8];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) pool[c] = 0ull;
-#pragma unroll 1
-            for (int pp = 0; pp < 2; ++pp) {
-                const int pos = 2 * e + pp;
-                // Row moments: per lane and channel, v0 + v1 and v0^2 + v1^2; the 32 lanes' values of
-                // a channel are added up by a transpose through shared memory (lane l writes row l,
-                // lane c sums column c; row stride 36 keeps both directions free of bank conflicts).
-                float s2[32];
+            for (int c = 0; c < 8; ++c) pool[c] = 0.f;
 #pragma unroll
-                for (int h = 0; h < 32; h += 16) {
-                    float v0[16], v1[16], s1[16];
-                    tmem_load16(tb + uint32_t(pos * 32 + h), v0);        // width parity 0
-                    tmem_load16(tb + uint32_t(128 + pos * 32 + h), v1);  // width parity 1
-#pragma unroll
-                    for (int c = 0; c < 16; c += 2) {
-                        const uint64_t a0 = f2_pack(v0[c], v0[c + 1]), a1 = f2_pack(v1[c], v1[c + 1]);
-                        f2_unpack(f2_add(a0, a1), s1[c], s1[c + 1]);
-                        f2_unpack(f2_fma(a0, a0, f2_mul(a1, a1)), s2[h + c], s2[h + c + 1]);
-                    }
-#pragma unroll
-                    for (int c = 0; c < 16; c += 4)
-                        *reinterpret_cast<float4*>(scr + lane * 36 + h + c) = make_float4(s1[c], s1[c + 1], s1[c + 2], s1[c + 3]);
-                }
-                __syncwarp();
-                float sum1;
-                {
-                    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll
-                    for (int r = 0; r < 32; r += 4) {
-                        p0 += scr[r * 36 + lane];
-                        p1 += scr[(r + 1) * 36 + lane];
-                        p2 += scr[(r + 2) * 36 + lane];
-                        p3 += scr[(r + 3) * 36 + lane];
-                    }
-                    sum1 = (p0 + p1) + (p2 + p3);
-                }
-                __syncwarp();  // every column is read before the squares overwrite the rows
-#pragma unroll
-                for (int c = 0; c < 32; c += 4)
-                    *reinterpret_cast<float4*>(scr + lane * 36 + c) = make_float4(s2[c], s2[c + 1], s2[c + 2], s2[c + 3]);
-                __syncwarp();
-                float sum2;
-                {
-                    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll
-                    for (int r = 0; r < 32; r += 4) {
-                        p0 += scr[r * 36 + lane];
-                        p1 += scr[(r + 1) * 36 + lane];
-                        p2 += scr[(r + 2) * 36 + lane];
-                        p3 += scr[(r + 3) * 36 + lane];
-                    }
-                    sum2 = (p0 + p1) + (p2 + p3);
-                }
-                {
-                    const float mean = sum1 * (1.f / 64.f);
-                    st_mean[lane] = mean;
-                    st_rstd[lane] = rsqrtf(fmaxf(fmaf(sum2, 1.f / 64.f, -mean * mean), 0.f) + a.eps);
-                }
-                __syncwarp();
-                // normalize, affine, and add the class's two width parities into the pool sums (the
-                // accumulator columns read again)
-                float v0[32], v1[32];
-                tmem_load32(tb + uint32_t(pos * 32), v0);
-                tmem_load32(tb + uint32_t(128 + pos * 32), v1);
-                if (pp == 1) {
+            for (int pos = 0; pos < 4; ++pos) {
+                float v0[8], v1[8];
+                tmem_load8(tb + uint32_t(pos * 32), v0);        // width parity 0, channels 8g ..
+                tmem_load8(tb + uint32_t(128 + pos * 32), v1);  // width parity 1
+                if (pos == 3) {
                     // every column this warp needs from the accumulator is in registers
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(i_accempty + ab));
                 }
+                float s1[8], s2[8];
 #pragma unroll
-                for (int h = 0; h < 32; h += 4) {
-                    const float4 m4 = *reinterpret_cast<const float4*>(st_mean + h);
-                    const float4 r4 = *reinterpret_cast<const float4*>(st_rstd + h);
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int c = h + 2 * u;
-                        const uint64_t mm = u ? f2_pack(m4.z, m4.w) : f2_pack(m4.x, m4.y);
-                        const uint64_t rr = u ? f2_pack(r4.z, r4.w) : f2_pack(r4.x, r4.y);
-                        // g0 (v0 - m) + g1 (v1 - m), then scaled by rstd into the pool sum
-                        uint64_t tt = f2_fma(gg0, f2_pack(v0[c], v0[c + 1]), f2_mul(gg1, f2_pack(v1[c], v1[c + 1])));
-                        tt = f2_fma(ngs, mm, tt);
-                        pool[c / 2] = f2_fma(rr, tt, pool[c / 2]);
-                    }
+                for (int c = 0; c < 8; ++c) {
+                    s1[c] = v0[c] + v1[c];
+                    s2[c] = fmaf(v0[c], v0[c], v1[c] * v1[c]);
                 }
-                __syncwarp();  // the statistics slots are read before the next class overwrites them
-            }
-            // The quarter's two warps add their classes: warp e finishes channels [16e, 16e + 16)
-            // and hands the other half of its sums over.
-            uint64_t mine[8];  // (register indices stay compile-time constants)
+                *reinterpret_cast<float4*>(scr + lane * 20) = make_float4(s1[0], s1[1], s1[2], s1[3]);
+                *reinterpret_cast<float4*>(scr + lane * 20 + 4) = make_float4(s1[4], s1[5], s1[6], s1[7]);
+                *reinterpret_cast<float4*>(scr + lane * 20 + 8) = make_float4(s2[0], s2[1], s2[2], s2[3]);
+                *reinterpret_cast<float4*>(scr + lane * 20 + 12) = make_float4(s2[4], s2[5], s2[6], s2[7]);
+                __syncwarp();
+                // lane: column rcol (sum of channel rcol, or squares of channel rcol - 8) over 16 rows
+                float p0 = 0.f, p1 = 0.f;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint64_t other = e ? pool[c] : pool[8 + c];
-                mine[c] = e ? pool[8 + c] : pool[c];
-                float lo, hi;
-                f2_unpack(other, lo, hi);
-                scr[(2 * c) * 32 + lane] = lo;  // the partner's channel 16 (1 - e) + 2c
-                scr[(2 * c + 1) * 32 + lane] = hi;
+                for (int r = 0; r < 16; r += 2) {
+                    p0 += scr[(16 * rhi + ((r + 4 * rhi) & 15)) * 20 + rcol];
+                    p1 += scr[(16 * rhi + ((r + 1 + 4 * rhi) & 15)) * 20 + rcol];
+                }
+                float tot = p0 + p1;
+                tot += __shfl_xor_sync(0xffffffffu, tot, 16);
+                const float sq = __shfl_down_sync(0xffffffffu, tot, 8);  // lanes 0-7: channel's squares
+                if (lane < 8) {
+                    const float mean = tot * (1.f / 64.f);
+                    st[lane] = mean;
+                    st[8 + lane] = rsqrtf(fmaxf(fmaf(sq, 1.f / 64.f, -mean * mean), 0.f) + a.eps);
+                }
+                __syncwarp();
+                const float4 m0 = *reinterpret_cast<const float4*>(st), m1 = *reinterpret_cast<const float4*>(st + 4);
+                const float4 r0 = *reinterpret_cast<const float4*>(st + 8), r1 = *reinterpret_cast<const float4*>(st + 12);
+                const float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+                const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    pool[c] = fmaf(rr[c], fmaf(g0, v0[c], fmaf(g1, v1[c], -gs * mm[c])), pool[c]);
+                __syncwarp();  // the scratch and statistics are read before the next class overwrites them
             }
-            named_bar_sync(2 + q, 64);
             const int hin = jt * 4 + q;
             if (hin < a.H) {
                 const size_t cstride = size_t(a.D) * a.H * 32;
-                float* dst = a.out + ((size_t(n) * 64 + size_t(half * 32 + 16 * e)) * a.D + size_t(i)) * size_t(a.H) * 32 +
+                float* dst = a.out + ((size_t(n) * 64 + size_t(half * 32 + 8 * g)) * a.D + size_t(i)) * size_t(a.H) * 32 +
                              size_t(hin) * 32 + size_t(lane);
                 const uint64_t sh = f2_pack(shift8, shift8), k8 = f2_pack(0.125f, 0.125f);
 #pragma unroll
-                for (int c = 0; c < 16; c += 2) {
-                    const uint64_t tot = f2_add(mine[c / 2], f2_pack(pscr[c * 32 + lane], pscr[(c + 1) * 32 + lane]));
+                for (int c = 0; c < 8; c += 2) {
                     float o0, o1;
-                    f2_unpack(gelu_erf2(f2_fma(tot, k8, sh)), o0, o1);
+                    f2_unpack(gelu_erf2(f2_fma(f2_pack(pool[c], pool[c + 1]), k8, sh)), o0, o1);
                     dst[size_t(c) * cstride] = o0;
                     dst[size_t(c + 1) * cstride] = o1;
                 }
             }
-            named_bar_sync(2 + q, 64);  // the partner has read this scratch before the next tile reuses it
         }
     }
     __syncthreads();
@@ -835,7 +794,7 @@ cudaError_t launch_convt3d_lnpool_fused(const c1n_convt3d_params& p, float eps, 
     long long pairs = num_sms / 2;
     if (pairs > tiles) pairs = tiles;
     if (pairs < 1) pairs = 1;
-    const int smem = 1024 + kFWBytes + kFStages * kTileBytes + 8 * kFScr * 4 + 8 * 2 * 32 * 4 + 256;
+    const int smem = 1024 + kFWBytes + kFStages * kTileBytes + kFEpiWarps * kFScr * 4 + kFEpiWarps * 16 * 4 + 256;
     e = cudaFuncSetAttribute(convt3d_lnpool_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     convt3d_lnpool_fused_kernel<<<(unsigned)(2 * pairs), kFThreads, smem, stream>>>(a, tm_x, tm_w);
