@@ -522,7 +522,7 @@ def read_traffic(workload, path):
         from gemm_groupnorm_accelerator_gb300 import _build_lib
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
-        rec = d.get(workload)
+        rec = d.get(f"{workload}:{path}", d.get(workload))  # a workload with several plans: one key each
         if rec and rec.get("path") == path and \
                 rec.get("source_fingerprint") == _build_lib.kernel_fingerprint(rec.get("source_file", "")):
             return rec["dram_bytes_per_launch"]
