@@ -412,3 +412,22 @@ def test_conv_transpose3d_scatter_form_and_page_shape():
     ref = full[:, :, p:p + Do, p:p + Ho, p:p + Wo]
     got = oracle.conv_transpose3d(x, w, None, stride=s, pad=p, out_pad=op)
     np.testing.assert_array_equal(got, ref)
+
+
+def test_p4_model_conv_bias_cancels_in_layernorm():
+    # The conv bias is one constant per channel, i.e. per LayerNorm row along W, so the page's model
+    # (ConvTranspose3d, + scalar, LayerNorm over W, AvgPool3d, GELU) does not depend on it: the
+    # one-pass kernel relies on this and normalizes the bare accumulators. (Tolerance: the float32
+    # rounding of y + b, which the LayerNorm input goes through.)
+    rng = np.random.default_rng(11)
+    x = rng.normal(size=(1, 3, 2, 2, 4)).astype(np.float32)
+    w = rng.uniform(-0.3, 0.3, size=(3, 4, 3, 3, 3)).astype(np.float32)
+    b = rng.uniform(-2.0, 2.0, size=4).astype(np.float32)
+    ga = rng.normal(1.0, 0.1, size=8).astype(np.float32)
+    be = rng.normal(0.0, 0.1, size=8).astype(np.float32)
+    with_b = oracle.conv_transpose3d(x, w, b, stride=2, pad=1, out_pad=1)[0].astype(np.float32)
+    without = oracle.conv_transpose3d(x, w, None, stride=2, pad=1, out_pad=1)[0].astype(np.float32)
+    assert not np.allclose(with_b, without)
+    a1 = oracle.ln_avgpool3d_gelu(with_b, 1e-5, 1.0, ga, be)
+    a0 = oracle.ln_avgpool3d_gelu(without, 1e-5, 0.0, ga, be)
+    np.testing.assert_allclose(a1, a0, rtol=0, atol=2e-5)
