@@ -10,6 +10,8 @@
 //   * pack_weights    — w[co][ci][kk] -> wp[kk][co][ci_pad] (tf32-rounded for fp32 data).
 // Operator definitions: Kimi-K2.6 l2_p35 page (Conv1d + GroupNorm), l2_p75 page (row-min + bias),
 // l1_p5 page (causal padding), l2_p3 page (LayerNorm with affine, exact GELU).
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -542,37 +544,37 @@ __global__ void __launch_bounds__(256) rowmin_finish_kernel(int C, int n_cb, con
     }
 }
 
-// One CTA per output channel co: read the row w[co][*][*] (C_in*k contiguous values) with
-// coalesced loads into shared memory, then write each tap's row wp[kk][co][0..ci_pad) contiguously.
-// tf32_mode: 0 none (bf16), 1 round to TF32, 2 TF32 head at taps 0..k-1 and TF32 tail at taps k..2k-1.
+// Weight pack: one thread per (output channel co, input channel slot ci < ci_pad) reads the k taps
+// w[co][ci][0..k-1] and writes wp[kk][co][ci] for each tap, coalesced along ci (slots past C_in
+// are zero). At most 128 CTAs of 128 threads, no shared memory, at most 32 registers: the conv
+// kernel that follows (launched early through programmatic dependence; 480 threads x 128
+// registers, ~224 KB of shared memory) fits on an SM beside one of them and stages x while the
+// pack runs. fp32 weights are rounded to TF32; with tf32_mode 2 the TF32 tail
+// w - tf32(w) goes to taps k..2k-1. Also zeroes `nzero` words at `zero`.
 template <typename InT, typename PackT>
-__global__ void __launch_bounds__(256) pack_weights_kernel(int C_out, int C_in, int k, int ci_pad, int tf32_mode,
+__global__ void __launch_bounds__(128, 16) pack_weights_kernel(int C_out, int C_in, int k, int ci_pad, int tf32_mode,
                                                            const InT* __restrict__ w, PackT* __restrict__ wp,
                                                            unsigned* __restrict__ zero, int nzero) {
-    extern __shared__ float row[];  // [C_in * k]
     // the conv kernel that follows may start its setup now (it waits for this kernel before it
     // reads the packed weights)
     griddep_launch_dependents();
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nzero; i += gridDim.x * blockDim.x) zero[i] = 0u;
-    const long long rk = (long long)C_in * k;
-    for (int co = blockIdx.x; co < C_out; co += gridDim.x) {
-        const InT* src = w + co * rk;
-        for (long long i = threadIdx.x; i < rk; i += blockDim.x) row[i] = to_f32(src[i]);
-        __syncthreads();
+    const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x, step = (long long)gridDim.x * blockDim.x;
+    for (long long i = i0; i < nzero; i += step) zero[i] = 0u;
+    const long long total = (long long)C_out * ci_pad;
+    for (long long e = i0; e < total; e += step) {
+        const int co = int(e / ci_pad), ci = int(e - (long long)co * ci_pad);
+        const InT* src = w + ((long long)co * C_in + ci) * k;
         for (int kk = 0; kk < k; ++kk) {
-            PackT* dst = wp + ((long long)kk * C_out + co) * ci_pad;
-            for (int ci = threadIdx.x; ci < ci_pad; ci += blockDim.x) {
-                float v = ci < C_in ? row[(long long)ci * k + kk] : 0.f;
-                if constexpr (sizeof(PackT) == 4) {
-                    const float hi = tf32_mode ? round_tf32(v) : v;
-                    dst[ci] = hi;
-                    if (tf32_mode == 2) dst[(long long)k * C_out * ci_pad + ci] = round_tf32(v - hi);
-                } else {
-                    dst[ci] = __float2bfloat16_rn(v);  // exact: v came from a bf16
-                }
+            const float v = ci < C_in ? to_f32(src[kk]) : 0.f;
+            PackT* dst = wp + ((long long)kk * C_out + co) * ci_pad + ci;
+            if constexpr (sizeof(PackT) == 4) {
+                const float hi = tf32_mode ? round_tf32(v) : v;
+                *dst = hi;
+                if (tf32_mode == 2) dst[(long long)k * C_out * ci_pad] = round_tf32(v - hi);
+            } else {
+                *dst = __float2bfloat16_rn(v);  // exact: v came from a bf16
             }
         }
-        __syncthreads();
     }
 }
 
@@ -768,18 +770,17 @@ cudaError_t launch_rowmin_finish(const c1n_params& p, const Plan& pl, const floa
 
 cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream,
                                 unsigned* zero, int nzero) {
-    const size_t smem = sizeof(float) * (size_t)p.C_in * p.k;
-    const int grid = p.C_out < 4096 ? p.C_out : 4096;
+    const long long total = (long long)p.C_out * pl.ci_pad;
+    const long long work = total > nzero ? total : nzero;
+    const int grid = (int)std::min<long long>((work + 127) / 128, 128);
     if (pl.bf16) {
-        auto k = pack_weights_kernel<__nv_bfloat16, __nv_bfloat16>;
-        if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k<<<grid, 256, smem, stream>>>(p.C_out, p.C_in, p.k, pl.ci_pad, 0, static_cast<const __nv_bfloat16*>(w),
-                                       static_cast<__nv_bfloat16*>(wp), zero, nzero);
+        pack_weights_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 128, 0, stream>>>(
+            p.C_out, p.C_in, p.k, pl.ci_pad, 0, static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(wp),
+            zero, nzero);
     } else {
-        auto k = pack_weights_kernel<float, float>;
-        if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k<<<grid, 256, smem, stream>>>(p.C_out, p.C_in, p.k, pl.ci_pad, pl.x3 ? 2 : 1, static_cast<const float*>(w),
-                                       static_cast<float*>(wp), zero, nzero);
+        pack_weights_kernel<float, float><<<grid, 128, 0, stream>>>(p.C_out, p.C_in, p.k, pl.ci_pad, pl.x3 ? 2 : 1,
+                                                                    static_cast<const float*>(w),
+                                                                    static_cast<float*>(wp), zero, nzero);
     }
     return cudaGetLastError();
 }
