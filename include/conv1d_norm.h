@@ -9,8 +9,10 @@
  *        channels of every row and a broadcast add of a per-channel bias.
  *   [p3] Kimi-K2.6 l1_p5 page — causal Conv1d: left padding (k-1)*dilation, tap 0 is the oldest
  *        input; the convolution viewed as a GEMM with M = N*T_out, N = C_out, K = C_in*k.
- *   [p4] Kimi-K2.6 l2_p3 page — LayerNorm with affine and the exact-erf GELU; its scalar add,
- *        LayerNorm over the last dimension, AvgPool3d and GELU (ln_avgpool3d_gelu_run below).
+ *   [p4] Kimi-K2.6 l2_p3 page — LayerNorm with affine and the exact-erf GELU; its model's
+ *        ConvTranspose3d, scalar add, LayerNorm over the last dimension, AvgPool3d and GELU
+ *        (conv_transpose3d_run, ln_avgpool3d_gelu_run and the one-pass
+ *        conv_transpose3d_ln_avgpool3d_gelu_run below).
  *
  *   c[n][co][t] = b[co] + sum_ci sum_kk w[co][ci][kk] * x[n][ci][t*stride + kk*dilation - pad_left]
  *                 (x = 0 outside [0, T));  T_out = (T + pad_left + pad_right - dilation*(k-1) - 1)/stride + 1
