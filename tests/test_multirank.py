@@ -67,3 +67,13 @@ def test_shards_are_disjoint_rows_of_one_batch():
 def test_aggregate_uses_the_slowest_rank():
     value, slowest = bench.aggregate([2.0, 4.0], 1e12, 2)
     assert slowest == 4.0 and abs(value - 2 * 1e12 / 4e-3 / 1e12) < 1e-9
+
+
+def test_p4_shards_are_disjoint_batch_entries_of_one_batch():
+    # the p4 workload shards its batch the same way: rank r draws entries [r N, (r + 1) N) of one
+    # global batch, so the ranks together run one bigger model batch (weak scaling)
+    wl = synth.CONV_TRANSPOSE3D.replace(N=2, D=2, H=4, W=4)
+    full = synth.make_convt3d_inputs(wl.replace(N=4))
+    parts = [synth.make_convt3d_inputs(wl, n_rows=wl.N, row_offset=r * wl.N) for r in range(2)]
+    assert np.array_equal(np.concatenate([p["x"] for p in parts]), full["x"])
+    assert all(np.array_equal(p["w"], full["w"]) and np.array_equal(p["b"], full["b"]) for p in parts)
