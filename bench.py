@@ -782,6 +782,7 @@ def p4_arm(args, wl):
         model_ms = time_replays(model, 1, dev, args.steps, eager=True)
         ach = wl.flops / (model_ms / 1e3) / 1e12
         fbytes = 4 * (inp["x"].size + inp["w"].size + inp["b"].size + 2 * wl.W * 2 + out.numel())
+        # issued MMA work: per tile (128 voxels) and channel half, 864 weight rows x K = 32, two halves
         issued = 2.0 * 864 * 128 * 32 * 2 * wl.N * wl.D * ((wl.H + 3) // 4)
         roof = {"bound": "tensor", "achieved": ach, "peak": tf32_peak, "unit": "TFLOP/s", "frac": ach / tf32_peak,
                 "traffic": read_traffic(wl.name, "convt3d_lnpool_fused"),
