@@ -70,7 +70,7 @@ class ClockSampler:
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -190,6 +190,235 @@ def reference_arm(args, wl):
 
 # ------------------------------------------------------------------------------------------ our arm
 
+EXTRA_WORKLOADS = ("conv_gn_tiny", "causal_conv", "linear_gn_rowmin", "conv_ln_gelu_bf16")
+# forced two-pass plans on the largest outputs: where the memory-bound normalize pass is measured
+NORMALIZE_PASS_WORKLOADS = ("causal_conv_gn32", "conv_ln_gelu_bf16")
+
+
+class ConvRun:
+    """One operator configuration through the C ABI on device-resident inputs: the descriptor, its
+    rank's inputs, rotating x / y buffer sets (more than 2x L2 of them unless one set already
+    exceeds L2) and one CUDA graph per set holding one whole step (weight pack + every kernel of
+    the operator, as the library enqueues them)."""
+
+    def __init__(self, c1n, wl, args, dev, rank, math_mode=None, path=None, mainloop=None):
+        import torch
+        self.torch, self.wl, self.dev = torch, wl, dev
+        math_mode = args.math if math_mode is None else math_mode
+        path = args.path if path is None else path
+        mainloop = args.mainloop if mainloop is None else mainloop
+        params = c1n.make_params(wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right,
+                                 wl.dilation, wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, math_mode, path, mainloop)
+        self.op = op = c1n.Conv1dNorm(params, device=dev)
+        self.path, self.math = op.path, math_mode
+        # Weak scaling: rank r runs the per-GPU workload on batch rows [r*N, (r+1)*N) of one global
+        # batch of world*N entries (GroupNorm / LayerNorm / row-min statistics are per sample or per
+        # row, so no data crosses ranks).
+        self.inp = inp = shard_inputs(wl, rank)
+        self.bf = bf = wl.dtype == synth.DTYPE_BF16
+        self.tdt = tdt = torch.bfloat16 if bf else torch.float32
+
+        def dev_t(a, cast=True):
+            if a is None:
+                return None
+            t = torch.from_numpy(a).to(dev)
+            return t.to(tdt) if (cast and bf) else t
+
+        self.w = dev_t(inp["w"])
+        self.b, self.ga, self.be, self.b2 = (dev_t(inp[k], cast=False) for k in ("b", "gamma", "beta", "bias2"))
+        x0 = dev_t(inp["x"])
+        self.y_shape = (wl.N, wl.C_out, op.T_out)
+        self.per_set = x0.numel() * x0.element_size() + int(np.prod(self.y_shape)) * (2 if bf else 4)
+        self.n_sets = 1 if self.per_set >= L2_BYTES else min(16, math.ceil(2 * L2_BYTES / self.per_set))
+        self.xs = [x0] + [x0.clone() for _ in range(self.n_sets - 1)]
+        self.ys = [torch.empty(self.y_shape, dtype=op.out_dtype(), device=dev) for _ in range(self.n_sets)]
+        self.am = (torch.empty((wl.N, op.T_out), dtype=torch.int32, device=dev)
+                   if wl.post == synth.POST_ROWMIN_BIAS else None)
+        self.stream = torch.cuda.current_stream(dev)
+        self.graphs = None
+        # kernels of one step, and of one call with the weights already packed
+        self.kernels = op.info.kernels
+        self.kernels_packed = self.kernels - (1 if self.path not in ("simt", "tc_linear") else 0)
+
+    def step(self, i):
+        j = i % self.n_sets
+        self.op(self.xs[j], self.w, self.b, self.ga, self.be, bias2=self.b2, out=self.ys[j], argmin=self.am)
+
+    def packed_call(self, i):
+        j = i % self.n_sets
+        self.op(self.xs[j], self.w, self.b, self.ga, self.be, bias2=self.b2, out=self.ys[j], argmin=self.am,
+                weights_packed=True)
+
+    def prepare(self, warmup, eager=False):
+        for i in range(warmup):
+            self.step(i)
+        self.torch.cuda.synchronize()
+        self.op.check()
+        self.graphs = None if eager else capture_graphs(self.step, self.n_sets, self.dev)
+        for i in range(max(3, warmup)):
+            self.run_step(i)
+        self.torch.cuda.synchronize()
+
+    def run_step(self, i):
+        if self.graphs:
+            self.graphs[i % self.n_sets].replay()
+        else:
+            self.step(i)
+
+    @property
+    def launch_mode(self):
+        return "cuda graph replay, one graph per step" if self.graphs else "eager"
+
+    def timed_blocks(self, steps, min_seconds, barrier, pg=None, i0=0):
+        """Time back-to-back blocks of exactly `steps` steps, each bracketed by a barrier and a device
+        synchronize on both sides and timed with CUDA events on the launching stream, until the blocks
+        cover at least `min_seconds` (3 blocks at least). Returns (ms per step of each block, max over
+        ranks)."""
+        torch = self.torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def block(i):
+            barrier()
+            torch.cuda.synchronize()
+            e0.record(self.stream)
+            for k in range(steps):
+                self.run_step(i + k)
+            e1.record(self.stream)
+            torch.cuda.synchronize()
+            barrier()
+            return e0.elapsed_time(e1) / steps
+
+        first = block(i0)
+        n_blocks = max(3, math.ceil(min_seconds * 1e3 / max(first * steps, 1e-3)))
+        if pg is not None:  # every rank runs the same number of blocks
+            t = torch.tensor([n_blocks], device=self.dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            n_blocks = int(t[0])
+        ms = [block(i0 + (r + 1) * steps) for r in range(n_blocks)]
+        if pg is not None:
+            t = torch.tensor(ms, device=self.dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            ms = [float(v) for v in t]
+        self.op.check()
+        return ms
+
+    def back_to_back_ms(self, launches=20, reps=10):
+        """Mean device time of one operator call with the weights already packed, from one CUDA
+        graph of `launches` calls back to back (inputs rotating over the buffer sets), timed with
+        CUDA events around `reps` replays. With one kernel per call this is that kernel's average
+        launch duration. None when the graph cannot be captured."""
+        torch = self.torch
+        self.op.pack_weights(self.w)
+        g = capture_graphs(lambda j: [self.packed_call(i) for i in range(launches)], 1, self.dev)
+        if not g:
+            return None
+        for _ in range(2):
+            g[0].replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for _ in range(reps):
+            g[0].replay()
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        self.op.check()
+        return e0.elapsed_time(e1) / (reps * launches)
+
+    def kernel_marks(self, i0):
+        """Per-kernel device times of one step from the library's event marks (an event pair around
+        each kernel inside a replayed graph: each time includes the pair's own overhead)."""
+        return kernel_times(self.op, self.step, i0, self.dev, n=5, graphs=bool(self.graphs))
+
+    def close(self):
+        self.op.close()
+        self.graphs = None
+        self.xs = self.ys = None
+        self.torch.cuda.synchronize()
+        self.torch.cuda.empty_cache()
+
+
+def conv_roofline(wl, run, peaks, kern, b2b_ms):
+    """Roofline entry of the dominant kernel (the conv kernel with its fused epilogue). Algorithmic
+    bytes: x and w read once, the per-channel parameters, and the conv kernel's output written once
+    (y, or the fp32 raw tile on the two-pass plans); FLOPs = 2 M N K."""
+    path = run.path
+    flops = wl.flops
+    nbytes = wl.algorithmic_bytes
+    y_elems = wl.N * wl.C_out * wl.T_out
+    if kern.get("normalize") is not None or kern.get("rowmin") is not None:
+        nbytes += y_elems * (4 - wl.elem_bytes)  # raw fp32 tile instead of y
+    conv_name = "simt_conv" if path == "simt" else "tc_conv"
+    if b2b_ms is not None and run.kernels_packed == 1:
+        conv_ms = b2b_ms
+        timing = "back to back: one CUDA graph of 20 launches of the kernel (weights packed once), events around the replays"
+    elif b2b_ms is not None and conv_name == "tc_conv" and path == "tc_linear":
+        conv_ms = b2b_ms  # conservative: includes the small finisher kernel that follows it
+        timing = ("back to back: graph of 20 operator calls (this kernel + the row-min finisher), events around the "
+                  "replays; the finisher's time is counted against this kernel")
+    else:
+        conv_ms = kern.get(conv_name, b2b_ms)
+        timing = "event pair around the kernel inside a replayed graph (includes the pair's own overhead: an upper bound)"
+    tc_peak = peaks["bf16_tflops"] * (1.0 if run.bf else TF32_PER_BF16)
+    t_flop = flops / (tc_peak * 1e12)
+    t_byte = nbytes / (peaks["hbm_gbs"] * 1e9)
+    if path == "simt":
+        ach = flops / (conv_ms / 1e3) / 1e12
+        roof = {"bound": "alu", "achieved": ach, "peak": FP32_FMA_PEAK_TFLOPS, "unit": "TFLOP/s",
+                "frac": ach / FP32_FMA_PEAK_TFLOPS}
+    elif t_byte >= t_flop:
+        ach = nbytes / (conv_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"]}
+    else:
+        ach = flops / (conv_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s", "frac": ach / tc_peak}
+    roof.update({"traffic": read_traffic(wl.name, path),
+                 "peak_source": peaks["source"] + ("" if run.bf else " (bf16 x 1.1/2.25 for tf32)"),
+                 "kernel": f"tc_conv_kernel ({path})" if path != "simt" else "simt_conv_kernel",
+                 "kernel_ms": conv_ms, "kernel_timing": timing, "kernels_ms_event_pairs": kern,
+                 "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                 "tensor_frac": (flops / (conv_ms / 1e3) / 1e12) / tc_peak,
+                 "hbm_frac": (nbytes / (conv_ms / 1e3) / 1e9) / peaks["hbm_gbs"]})
+    return roof
+
+
+def rowmin_finisher(wl, kern, peaks):
+    """GB/s of the row-min finisher (per-(row, channel block) partials read, y and argmin written)
+    from its event-pair time (an upper bound on the kernel time, so a lower bound on GB/s)."""
+    ms = kern.get("rowmin_finish")
+    if not ms:
+        return None
+    n_cb = -(-wl.C_out // 256)
+    nbytes = wl.N * wl.T_out * (n_cb * 8 + 4) + wl.N * wl.C_out * wl.T_out * wl.elem_bytes + 4 * wl.C_out
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"kernel": "rowmin_finish_kernel", "ms_event_pair": ms, "bytes": nbytes, "GB/s": gbs,
+            "frac": gbs / peaks["hbm_gbs"]}
+
+
+def measure_workload(c1n, wl, args, dev, rank, peaks, steps, min_seconds, barrier, pg=None, path=None):
+    """One workload measured the way the headline is (without e2e and oracle legs): returns a dict
+    for the line's `workloads` object."""
+    run = ConvRun(c1n, wl, args, dev, rank, path=path)
+    try:
+        run.prepare(args.warmup, eager=args.eager)
+        ms_blocks = run.timed_blocks(steps, min_seconds, barrier, pg)
+        ms = statistics.median(ms_blocks)
+        kern = run.kernel_marks(args.warmup + steps)
+        b2b = run.back_to_back_ms()
+        roof = conv_roofline(wl, run, peaks, kern, b2b)
+        out = {"workload": wl.name, "gemm_mnk": list(wl.gemm_mnk), "plan": run.path,
+               "cta_pair": int(run.op.info.cta_pair), "dtype": dtype_name(wl, run.path, run.math),
+               "ms_per_step": ms, "tflops": wl.flops / (ms / 1e3) / 1e12, "blocks": len(ms_blocks),
+               "steps_per_block": steps, "kernels_per_step": run.kernels, "roofline": roof,
+               "normalize_pass": normalize_pass_roofline(wl, kern, peaks)}
+        fin = rowmin_finisher(wl, kern, peaks) if wl.post == synth.POST_ROWMIN_BIAS else None
+        if fin:
+            out["finisher"] = fin
+        return out
+    finally:
+        run.close()
+
+
 def our_arm(args, wl):
     import torch
     import gemm_groupnorm_accelerator_gb300 as c1n
@@ -207,127 +436,63 @@ def our_arm(args, wl):
     c1n.load()
     peaks = load_peaks()
 
-    params = c1n.make_params(wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right, wl.dilation,
-                             wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, args.math, args.path, args.mainloop)
-    op = c1n.Conv1dNorm(params, device=dev)
-    path = op.path
-    # Weak scaling: rank r runs the per-GPU workload on batch rows [r*N, (r+1)*N) of one global
-    # batch of world*N entries (GroupNorm / LayerNorm / row-min statistics are per sample or per
-    # row, so no data crosses ranks).
-    inp = shard_inputs(wl, rank)
-    bf = wl.dtype == synth.DTYPE_BF16
-    tdt = torch.bfloat16 if bf else torch.float32
-
-    def dev_t(a, cast=True):
-        if a is None:
-            return None
-        t = torch.from_numpy(a).to(dev)
-        return t.to(tdt) if (cast and bf) else t
-
-    w = dev_t(inp["w"])
-    b, ga, be, b2 = (dev_t(inp[k], cast=False) for k in ("b", "gamma", "beta", "bias2"))
-    x0 = dev_t(inp["x"])
-    out_dt = op.out_dtype()
-    y_shape = (wl.N, wl.C_out, op.T_out)
-    per_set = x0.numel() * x0.element_size() + int(np.prod(y_shape)) * (2 if bf else 4)
-    n_sets = 1 if per_set >= L2_BYTES else min(16, math.ceil(2 * L2_BYTES / per_set))
-    xs = [x0] + [x0.clone() for _ in range(n_sets - 1)]
-    ys = [torch.empty(y_shape, dtype=out_dt, device=dev) for _ in range(n_sets)]
-    am = torch.empty((wl.N, op.T_out), dtype=torch.int32, device=dev) if wl.post == synth.POST_ROWMIN_BIAS else None
-    stream = torch.cuda.current_stream(dev)
-
-    def step(i):
-        j = i % n_sets
-        op.pack_weights(w)
-        op(xs[j], w, b, ga, be, bias2=b2, out=ys[j], argmin=am, weights_packed=True)
-
     def barrier():
         if pg is not None:
             pg.barrier()
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    op.check()
-
-    # One CUDA graph per input buffer set holds one step (pack + operator) as the device runs it, so
-    # the timed region measures the GPU rather than the host's per-launch overhead (at ~20 us per
-    # step on the small workloads the eager Python loop cannot keep the GPU busy).
-    graphs = capture_graphs(step, n_sets, dev) if not args.eager else None
-    launch_mode = "cuda graph replay, one graph per step" if graphs else "eager"
-
-    def run_step(i):
-        if graphs:
-            graphs[i % n_sets].replay()
-        else:
-            step(i)
-
-    for i in range(max(3, args.warmup)):
-        run_step(i)
-    torch.cuda.synchronize()
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    run = ConvRun(c1n, wl, args, dev, rank)
+    run.prepare(args.warmup, eager=args.eager)
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
-    barrier()
-    torch.cuda.synchronize()
-    t_start.record(stream)
-    for i in range(args.steps):
-        run_step(args.warmup + i)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    clocks = sampler.stop() if sampler else None
-    op.check()
-    total_ms = t_start.elapsed_time(t_end)
-    ms = total_ms / args.steps
-    # device time of the weight pack alone and of the operator alone, the same way
-    pack_ms = time_replays(lambda i: op.pack_weights(w), n_sets, dev, args.steps, eager=not graphs)
-    main_ms = time_replays(lambda i: op(xs[i % n_sets], w, b, ga, be, bias2=b2, out=ys[i % n_sets], argmin=am,
-                                        weights_packed=True), n_sets, dev, args.steps, eager=not graphs)
-    if pg is not None:
-        t = torch.tensor([ms, main_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms, main_ms = float(t[0]), float(t[1])
+    # Timed region: R back-to-back blocks of exactly --steps steps inside a window of at least
+    # --min-seconds, so the clock sampler sees the GPU under load; the median block is reported.
+    ms_blocks = run.timed_blocks(args.steps, args.min_seconds, barrier, pg)
+    ms = statistics.median(ms_blocks)
     value, ms = aggregate([ms], wl.flops, world)
-
-    # per-kernel device times from the library's event marks (a few extra steps after the timed
-    # region, same inputs and launch configuration, replayed from a graph when the step is)
-    kern = kernel_times(op, step, args.warmup + args.steps, dev, n=5, graphs=bool(graphs))
-    conv_name = "simt_conv" if path == "simt" else "tc_conv"
-    conv_ms = kern.get(conv_name, main_ms)
-
-    # roofline of the dominant kernel (the conv kernel with its fused epilogue). Its algorithmic
-    # bytes: x and w read once, the per-channel parameters, and its output written once (y, or
-    # the fp32 raw tile on the two-pass plans).
-    flops = wl.flops
-    nbytes = wl.algorithmic_bytes
-    y_elems = wl.N * wl.C_out * wl.T_out
-    if kern.get("normalize") is not None or kern.get("rowmin") is not None:
-        nbytes += y_elems * (4 - wl.elem_bytes)  # raw fp32 tile instead of y
-    tc_peak = peaks["bf16_tflops"] * (1.0 if bf else TF32_PER_BF16)
-    t_flop = flops / (tc_peak * 1e12)
-    t_byte = nbytes / (peaks["hbm_gbs"] * 1e9)
-    if t_byte >= t_flop:
-        ach = nbytes / (conv_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / peaks["hbm_gbs"]}
-    else:
-        ach = flops / (conv_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s", "frac": ach / tc_peak}
-    roof.update({"traffic": read_traffic(wl.name, path), "peak_source": peaks["source"],
-                 "kernel": f"tc_conv_kernel ({path})", "kernel_ms": conv_ms, "op_ms": main_ms, "pack_ms": pack_ms,
-                 "kernels_ms": kern, "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
-                 "tensor_frac": (flops / (conv_ms / 1e3) / 1e12) / tc_peak,
-                 "hbm_frac": (nbytes / (conv_ms / 1e3) / 1e9) / peaks["hbm_gbs"]})
+    kern = run.kernel_marks(args.warmup + args.steps)
+    b2b = run.back_to_back_ms()
+    roof = conv_roofline(wl, run, peaks, kern, b2b)
+    pack_ms = time_replays(lambda i: run.op.pack_weights(run.w), run.n_sets, dev, args.steps, eager=not run.graphs)
+    roof["pack_ms_graph_per_call"] = pack_ms
     norm_pass = normalize_pass_roofline(wl, kern, peaks)
 
-    e2e = measure_e2e(args, wl, op, inp, dev, tdt, bf, w, b, ga, be, b2, am)
+    e2e = measure_e2e(args, wl, run.op, run.inp, dev, run.tdt, run.bf, run.w, run.b, run.ga, run.be, run.b2, run.am)
     if pg is not None:
         t = torch.tensor([e2e["ms_per_step"]], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         e2e["ms_per_step"] = float(t[0])
         e2e["value"] = wl.flops * world / (e2e["ms_per_step"] / 1e3) / 1e12
+    config = config_of(wl, {"path": run.path, "cta_pair": int(run.op.info.cta_pair),
+                            "parallelism": f"dp{world}" if world > 1 else "single",
+                            "l2": f"inputs rotate over {run.n_sets} x/y buffer sets "
+                                  f"({run.n_sets * run.per_set / 2**20:.0f} MiB > 129 MiB L2)"
+                            if run.n_sets > 1 else "working set larger than L2",
+                            "step": "one operator call through the C ABI: weight pack + fused kernel",
+                            "launch": run.launch_mode,
+                            "timed_region": f"{len(ms_blocks)} blocks of {args.steps} steps (median block reported; "
+                                            f"every block bracketed by barrier + synchronize)"})
+    launches = args.steps * run.kernels
+    run.close()
+
+    # The other workloads and the normalize-pass measurements, in the same process and under the
+    # same clock record (one GPU per process: rank 0 of a single-GPU run only).
+    workloads, norm_runs = {}, {}
+    default_run = args.workload == synth.CONV_GN.name and world == 1 and not args.no_extra
+    if default_run:
+        for name in EXTRA_WORKLOADS:
+            w2 = workload_by_name(name)
+            workloads[name] = measure_workload(c1n, w2, args, dev, rank, peaks, args.steps, args.extra_seconds,
+                                               barrier)
+        for name in NORMALIZE_PASS_WORKLOADS:
+            w2 = workload_by_name(name)
+            r = measure_workload(c1n, w2, args, dev, rank, peaks, args.steps, args.extra_seconds, barrier,
+                                 path=c1n.PATH_TC_TWO_PASS)
+            norm_runs[name] = {"workload": w2.name, "plan": r["plan"], "ms_per_step": r["ms_per_step"],
+                               "passes": r["normalize_pass"], "conv_roofline": r["roofline"]}
+    clocks = sampler.stop() if sampler else None
+    if norm_pass is None and norm_runs:
+        norm_pass = {"forced two-pass plans (the normalize pass on the largest outputs)": norm_runs}
 
     if rank == 0:
         cpu = None
@@ -335,16 +500,11 @@ def our_arm(args, wl):
             cpu = time_oracle(wl, seconds=args.cpu_seconds)
         line = {"metric": args.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": dtype_name(wl, path, args.math), "data": "synthetic",
-                "config": config_of(wl, {"path": path, "cta_pair": int(op.info.cta_pair), "parallelism": f"dp{world}" if world > 1 else "single",
-                                         "l2": f"inputs rotate over {n_sets} x/y buffer sets "
-                                               f"({n_sets * per_set / 2**20:.0f} MiB > 129 MiB L2)"
-                                         if n_sets > 1 else "working set larger than L2",
-                                         "step": "weight pack + fused kernel through the C ABI",
-                                         "launch": launch_mode}),
-                "roofline": roof, "normalize_pass": norm_pass, "cpu_baseline": cpu,
+                "vs_baseline": None, "dtype": dtype_name(wl, run.path, args.math), "data": "synthetic",
+                "config": config, "roofline": roof, "normalize_pass": norm_pass, "workloads": workloads or None,
+                "cpu_baseline": cpu,
                 "e2e": {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step", "pipeline")},
-                "gpu_launches": args.steps * op.info.kernels, "clocks": clocks}
+                "gpu_launches": launches, "clocks": clocks}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
@@ -434,7 +594,8 @@ def normalize_pass_roofline(wl, kern, peaks):
                          ("normalize", (4 + wl.elem_bytes) * y_elems)):
         if name in kern and kern[name] > 0:
             gbs = nbytes / (kern[name] / 1e3) / 1e9
-            out[name] = {"ms": kern[name], "bytes": nbytes, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"]}
+            out[name] = {"ms": kern[name], "bytes": nbytes, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"],
+                         "timing": "event pair around the kernel in a replayed graph (an upper bound on its time)"}
     for name in ("gn_merge", "ln_merge"):
         if name in kern and kern[name] > 0:
             out[name] = {"ms": kern[name]}
@@ -782,8 +943,14 @@ def p4_arm(args, wl):
         model_ms = time_replays(model, 1, dev, args.steps, eager=True)
         ach = wl.flops / (model_ms / 1e3) / 1e12
         fbytes = 4 * (inp["x"].size + inp["w"].size + inp["b"].size + 2 * wl.W * 2 + out.numel())
-        # issued MMA work: per tile (128 voxels) and channel half, 864 weight rows x K = 32, two halves
-        issued = 2.0 * 864 * 128 * 32 * 2 * wl.N * wl.D * ((wl.H + 3) // 4)
+        # Issued MMA work of the one-pass kernel: a tile is 4 x 32 input voxels (MMA M = 128) of one
+        # (n, d) plane; per tile and channel half the MMAs have N = the 864 resident weight rows (the
+        # taps that meet an input, 27 per output parity class x C_out/2 = 32 channels of the half)
+        # and K = C_in = 32; two channel halves per tile.
+        assert (wl.C_in, wl.C_out, wl.k, wl.W) == (32, 64, 3, 32), "tile constants below assume the page's shape"
+        tile_m, rows_per_half, halves = 4 * wl.W, 27 * (wl.C_out // 2), 2
+        tiles = wl.N * wl.D * ((wl.H + 3) // 4)
+        issued = 2.0 * tile_m * rows_per_half * wl.C_in * halves * tiles
         roof = {"bound": "tensor", "achieved": ach, "peak": tf32_peak, "unit": "TFLOP/s", "frac": ach / tf32_peak,
                 "traffic": read_traffic(wl.name, "convt3d_lnpool_fused"),
                 "peak_source": peaks.get("source", "MEASURED_PEAKS.json") + " (bf16 x 1.1/2.25 for tf32)",
@@ -834,7 +1001,8 @@ def p4_arm(args, wl):
         cpu = None if (world > 1 or args.no_cpu_baseline) else p4_oracle_sample(wl, lp, args.cpu_seconds)
         line = {"metric": "p4 ConvTranspose3d+LayerNorm+AvgPool3d+GELU TFLOP/s", "value": value, "unit": "TFLOP/s",
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "tf32" if tensor_plan else "f32", "data": "synthetic",
                 "config": {"workload": wl.name, "x": [wl.N, wl.C_in, wl.D, wl.H, wl.W], "C_out": wl.C_out,
                            "k": wl.k, "stride": wl.stride, "pad": wl.pad, "out_pad": wl.out_pad,
                            "then": lp.name, "parallelism": f"dp{world}" if world > 1 else "single",
@@ -866,6 +1034,12 @@ def main():
     ap.add_argument("--oracle-rows", type=int, default=2, help="batch entries per reference-arm step")
     ap.add_argument("--metric", default="fused conv1d+GroupNorm TFLOP/s")
     ap.add_argument("--eager", action="store_true", help="time the eager launch loop instead of CUDA graph replays")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="the timed blocks of --steps steps repeat until they cover this long (clock sampling window)")
+    ap.add_argument("--extra-seconds", type=float, default=0.3,
+                    help="the same for each of the other workloads of the default run")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="default run: skip the other workloads and the forced two-pass normalize measurements")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     wl = workload_by_name(args.workload)

@@ -213,15 +213,47 @@ def ln_avgpool3d_gelu(z, sum_weight: float, gamma=None, beta=None, eps: float = 
     """Torch convenience wrapper: z [N, C, D, H, W] float32 CUDA tensor (contiguous) -> a new (or the
     given) [N, C, D//2, H//2, W//2] float32 tensor, computed on the current stream."""
     import torch
-    if z.dim() != 5 or z.dtype != torch.float32 or not z.is_cuda or not z.is_contiguous():
-        raise ValueError("z must be a contiguous 5-D float32 CUDA tensor")
+    if z.dim() != 5:
+        raise ValueError(f"z must be 5-D [N, C, D, H, W], got shape {tuple(z.shape)}")
     N, C, D, H, W = z.shape
+    _check_tensor("z", z, (N, C, D, H, W), torch.float32)
+    if not z.is_cuda:
+        raise ValueError("z must be a CUDA tensor")
+    for name, t in (("gamma", gamma), ("beta", beta)):
+        _check_tensor(name, t, (W,), torch.float32, z.device, optional=True)
+    _check_tensor("out", out, (N, C, D // 2, H // 2, W // 2), torch.float32, z.device, optional=True)
     if out is None:
         out = torch.empty((N, C, D // 2, H // 2, W // 2), dtype=torch.float32, device=z.device)
     p = LnPoolParams(N, C, D, H, W, eps)
     ln_avgpool3d_gelu_run(p, z.data_ptr(), float(sum_weight), _ptr(gamma), _ptr(beta), out.data_ptr(),
                           torch.cuda.current_stream(z.device).cuda_stream)
     return out
+
+
+def _convt3d_shapes(x, w):
+    """(N, C_in, D, H, W, C_out, k) of x [N, C_in, D, H, W] and w [C_in, C_out, k, k, k], both dense
+    float32 CUDA tensors on one device; ValueError otherwise."""
+    import torch
+    if x.dim() != 5 or w.dim() != 5:
+        raise ValueError(f"x and w must be 5-D, got shapes {tuple(x.shape)} and {tuple(w.shape)}")
+    N, C_in, D, H, W = x.shape
+    C_out, k = w.shape[1], w.shape[2]
+    _check_tensor("x", x, (N, C_in, D, H, W), torch.float32)
+    _check_tensor("w", w, (C_in, C_out, k, k, k), torch.float32)
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    _check_tensor("w", w, (C_in, C_out, k, k, k), torch.float32, x.device)
+    return N, C_in, D, H, W, C_out, k
+
+
+def _check_workspace(ws, need: int, device) -> None:
+    import torch
+    if ws.dtype != torch.uint8 or ws.dim() != 1 or not ws.is_contiguous():
+        raise ValueError("workspace must be a dense 1-D uint8 tensor")
+    if ws.numel() < need:
+        raise ValueError(f"workspace holds {ws.numel()} bytes, {need} needed")
+    if not ws.is_cuda or ws.device != device:
+        raise ValueError(f"workspace is on {ws.device}, expected {device}")
 
 
 def conv_transpose3d_workspace_size(params: ConvT3dParams) -> int:
@@ -244,17 +276,17 @@ def conv_transpose3d(x, w, b=None, stride: int = 2, pad: int = 1, out_pad: int =
     math: 0 auto, 1 CUDA cores, 2 tensor cores. The workspace (a uint8 CUDA tensor) is allocated here
     when the plan needs one and none is given."""
     import torch
-    for t in (x, w):
-        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError("x and w must be contiguous float32 CUDA tensors")
-    N, C_in, D, H, W = x.shape
-    C_out, k = w.shape[1], w.shape[2]
+    N, C_in, D, H, W, C_out, k = _convt3d_shapes(x, w)
     f = lambda n: (n - 1) * stride - 2 * pad + (k - 1) + out_pad + 1
+    _check_tensor("b", b, (C_out,), torch.float32, x.device, optional=True)
+    _check_tensor("out", out, (N, C_out, f(D), f(H), f(W)), torch.float32, x.device, optional=True)
     if out is None:
         out = torch.empty((N, C_out, f(D), f(H), f(W)), dtype=torch.float32, device=x.device)
     p = ConvT3dParams(N, C_in, C_out, D, H, W, k, stride, pad, out_pad, math)
     need = conv_transpose3d_workspace_size(p)
-    if need and (workspace is None or workspace.numel() < need):
+    if need and workspace is not None:
+        _check_workspace(workspace, need, x.device)
+    if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     conv_transpose3d_run(p, x.data_ptr(), w.data_ptr(), _ptr(b), out.data_ptr(),
                          workspace.data_ptr() if need else None, need, torch.cuda.current_stream(x.device).cuda_stream)
@@ -283,16 +315,19 @@ def conv_transpose3d_ln_avgpool3d_gelu(x, w, b, sum_weight: float, gamma=None, b
     GELU(AvgPool3d(2)(LayerNorm_W(ConvTranspose3d(x) + sum_weight))). The workspace (a uint8 CUDA
     tensor) is allocated here when none is given."""
     import torch
-    for t in (x, w):
-        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError("x and w must be contiguous float32 CUDA tensors")
-    N, C_in, D, H, W = x.shape
-    C_out, k = w.shape[1], w.shape[2]
+    N, C_in, D, H, W, C_out, k = _convt3d_shapes(x, w)
+    w_out = (W - 1) * stride - 2 * pad + (k - 1) + out_pad + 1  # the LayerNorm width
+    _check_tensor("b", b, (C_out,), torch.float32, x.device, optional=True)
+    for name, t in (("gamma", gamma), ("beta", beta)):
+        _check_tensor(name, t, (w_out,), torch.float32, x.device, optional=True)
+    _check_tensor("out", out, (N, C_out, D, H, W), torch.float32, x.device, optional=True)
     if out is None:
         out = torch.empty((N, C_out, D, H, W), dtype=torch.float32, device=x.device)
     p = ConvT3dParams(N, C_in, C_out, D, H, W, k, stride, pad, out_pad, 2)
     need = conv_transpose3d_ln_avgpool3d_gelu_workspace_size(p)
-    if workspace is None or workspace.numel() < need:
+    if workspace is not None:
+        _check_workspace(workspace, need, x.device)
+    else:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     conv_transpose3d_ln_avgpool3d_gelu_run(p, eps, sum_weight, x.data_ptr(), w.data_ptr(), _ptr(b), _ptr(gamma),
                                            _ptr(beta), out.data_ptr(), workspace.data_ptr(), need,
@@ -334,6 +369,25 @@ def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+def _check_tensor(name: str, t, shape, dtype, device=None, optional: bool = False) -> None:
+    """Raise ValueError unless `t` is a tensor of exactly `shape` and `dtype`, dense (contiguous) and,
+    when `device` is given, a CUDA tensor on that device. Shape and dtype are checked first, so the
+    checks also run on tensors of a machine without a GPU. The C library sees only raw pointers: a
+    tensor of the wrong size would become out-of-bounds device accesses, not an error status."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and (not t.is_cuda or t.device != device):
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
 class Conv1dNorm:
     """One descriptor plus its workspace; calls go through ``conv1d_norm_run_ex`` on the current stream."""
 
@@ -356,8 +410,31 @@ class Conv1dNorm:
         import torch
         return torch.bfloat16 if self.params.dtype == BF16 else torch.float32
 
+    def _device(self):
+        import torch
+        return self.workspace.device if self.workspace.is_cuda else None
+
+    def validate(self, x, w, b=None, gamma=None, beta=None, bias2=None, out=None, argmin=None) -> None:
+        """Raise ValueError unless every tensor matches the descriptor: x [N, C_in, T] and w
+        [C_out, C_in, k] in the descriptor's dtype; b, gamma, beta, bias2 [C_out] float32; out
+        [N, C_out, T_out] in the output dtype; argmin [N, T_out] int32; all dense, on the workspace's
+        device. bias2 is required with the row-min post-op."""
+        import torch
+        p = self.params
+        dt = self.out_dtype()
+        dev = self._device()
+        _check_tensor("x", x, (p.N, p.C_in, p.T), dt, dev)
+        _check_tensor("w", w, (p.C_out, p.C_in, p.k), dt, dev)
+        for name, t in (("b", b), ("gamma", gamma), ("beta", beta)):
+            _check_tensor(name, t, (p.C_out,), torch.float32, dev, optional=True)
+        _check_tensor("bias2", bias2, (p.C_out,), torch.float32, dev, optional=p.post != POST_ROWMIN_BIAS)
+        _check_tensor("out", out, (p.N, p.C_out, self.T_out), dt, dev, optional=True)
+        _check_tensor("argmin", argmin, (p.N, self.T_out), torch.int32, dev, optional=True)
+
     def pack_weights(self, w, stream=None):
         import torch
+        p = self.params
+        _check_tensor("w", w, (p.C_out, p.C_in, p.k), self.out_dtype(), self._device())
         s = torch.cuda.current_stream(w.device).cuda_stream if stream is None else stream
         conv1d_norm_pack_weights(self.desc, w.data_ptr(), None, 0, s)
 
@@ -365,6 +442,7 @@ class Conv1dNorm:
                  weights_packed=False):
         import torch
         p = self.params
+        self.validate(x, w, b, gamma, beta, bias2, out, argmin)
         if out is None:
             out = torch.empty((p.N, p.C_out, self.T_out), dtype=self.out_dtype(), device=x.device)
         args = Args(_ptr(x), _ptr(w), _ptr(b), _ptr(gamma), _ptr(beta), _ptr(bias2), _ptr(out), _ptr(argmin), None, 0,

@@ -10,6 +10,7 @@ import concurrent.futures as cf
 import glob
 import hashlib
 import os
+import re
 import shutil
 import subprocess
 
@@ -41,10 +42,25 @@ def _headers():
         [os.path.join(INCLUDE, "conv1d_norm.h")]
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and with runs of whitespace collapsed: what the compiler turns
+    into code (string literals in these sources hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_fingerprint(source: str) -> str:
-    """Hash of one translation unit (a csrc/*.cu file name), every header and the flags: a profile
-    of a kernel defined in that file stays valid while this does not change."""
-    return _fingerprint([os.path.join(CSRC, source)])
+    """Hash of the code of one translation unit (a csrc/*.cu file name), of every header and of the
+    flags, comments and layout left out: a profile of a kernel defined in that file stays valid
+    while this does not change (a comment-only edit keeps it)."""
+    h = hashlib.sha256()
+    for f in [os.path.join(CSRC, source)] + _headers():
+        with open(f, encoding="utf-8") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(_code_only(fh.read()).encode())
+    h.update(" ".join(ARCH + [f for f in NVCC_FLAGS if f not in (INCLUDE, CSRC)]).encode())
+    return h.hexdigest()
 
 
 def _fingerprint(sources=None) -> str:

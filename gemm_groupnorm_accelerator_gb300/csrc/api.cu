@@ -373,9 +373,12 @@ c1n_status make_plan(const c1n_params& p, Plan& pl) {
             }
         }
     }
-    if (p.math == C1N_MATH_TENSOR || p.math == C1N_MATH_TENSOR_X3 || want != C1N_PATH_AUTO)
+    // No silent fallback: a shape the tensor-core path cannot take is refused; the SIMT fp32 CUDA
+    // path runs only when the caller asks for it (math = SIMT).
+    if (want != C1N_PATH_AUTO)
         return fail(C1N_ERR_UNSUPPORTED, "tensor-core path unavailable: %s", *why ? why : "forced path not applicable");
-    return choose_simt();
+    return fail(C1N_ERR_UNSUPPORTED, "tensor-core path unavailable: %s (math = SIMT runs the fp32 CUDA-core path)",
+                *why ? why : "no tensor-core plan takes this operator");
 }
 
 c1n_status validate(const c1n_params* p) {
@@ -567,17 +570,13 @@ c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         }
         const bool fused_gn = pl.path == C1N_PATH_TC_FUSED_GN || pl.path == C1N_PATH_TC_FUSED_GN_DSMEM;
         const bool fused_ln_path = pl.path == C1N_PATH_TC_FUSED_LN;
-        // The fused GroupNorm tile is stored by one TMA bulk store when y's rows are 16-byte
-        // multiples and the staging tile fits in the operand rings. The fused LayerNorm stores
-        // 32 x 32 tiles staged per warp; their 32-channel boxes must not reach into the other
-        // CTA's channel half (BN a multiple of 32 when the channels are split).
+        // The fused LayerNorm stores 32 x 32 tiles staged per warp by TMA bulk stores when y's rows
+        // are 16-byte multiples; their 32-channel boxes must not reach into the other CTA's channel
+        // half (BN a multiple of 32 when the channels are split). (The fused GroupNorm epilogue
+        // stores straight from registers.)
         const bool y_tma_ok = aligned16(a->y) && (pl.T_out * pl.esize) % 16 == 0;
         const bool box_ok = pl.n_cb == 1 || pl.BN % 32 == 0;  // 32-channel boxes stay in this CTA's block
-        const bool tma_store =
-            y_tma_ok && box_ok &&
-            ((fused_gn && (size_t)round_up(pl.BN, 32) * 128 * pl.esize <=
-                              (size_t)pl.stages_b * pl.b_slot_bytes + (size_t)pl.stages_s * pl.s_slot_bytes) ||
-             (fused_ln_path && pl.o_bytes > 0));
+        const bool tma_store = y_tma_ok && box_ok && fused_ln_path && pl.o_bytes > 0;
         if (tma_store && d->tm_y_ptr != a->y) {
             const cuuint64_t es = (cuuint64_t)pl.esize;
             cuuint64_t dy[3] = {(cuuint64_t)pl.T_out, (cuuint64_t)p.C_out, (cuuint64_t)p.N};

@@ -770,9 +770,12 @@ cudaError_t launch_rowmin_finish(const c1n_params& p, const Plan& pl, const floa
 
 cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream,
                                 unsigned* zero, int nzero) {
+    // One (co, ci) slot per thread where the grid allows, so all weight loads are in flight at once;
+    // at most 8 CTAs of 128 threads per SM (of 152), so the conv kernel launched behind this one (1
+    // CTA of 480 threads per SM) fits beside them.
     const long long total = (long long)p.C_out * pl.ci_pad;
     const long long work = total > nzero ? total : nzero;
-    const int grid = (int)std::min<long long>((work + 127) / 128, 128);
+    const int grid = (int)std::min<long long>((work + 127) / 128, 152 * 8);
     if (pl.bf16) {
         pack_weights_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 128, 0, stream>>>(
             p.C_out, p.C_in, p.k, pl.ci_pad, 0, static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(wp),

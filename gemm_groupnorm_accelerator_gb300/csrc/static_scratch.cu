@@ -54,6 +54,14 @@ extern "C" c1n_status conv1d_norm_run_static_scratch(c1n_desc* desc, const c1n_a
         c1n::set_last_error("args->workspace must be NULL: the fixed scratch is the workspace");
         return C1N_ERR_INVALID_ARG;
     }
+    // Every descriptor packs its weights into the same array, so weights packed by an earlier call
+    // may belong to another operator; the pack also resets the fused GroupNorm exchange words.
+    // Every call therefore packs.
+    if (args->flags & C1N_FLAG_WEIGHTS_PACKED) {
+        c1n::set_last_error("C1N_FLAG_WEIGHTS_PACKED is not accepted here: the fixed scratch is shared by every "
+                            "descriptor, so each call packs its own weights");
+        return C1N_ERR_INVALID_ARG;
+    }
     size_t need = 0;
     c1n_status st = conv1d_norm_workspace_size(desc, &need);
     if (st != C1N_OK) return st;

@@ -214,6 +214,107 @@ __device__ __forceinline__ void gn_run_moments(uint32_t tb, int c_lo, int c_hi, 
     }
 }
 
+// Statistics of y = acc + bias over every run of SUB consecutive channels of this warp's columns
+// [c_lo, c_hi) (c_lo a multiple of 32) and its valid rows, from ONE sweep of TMEM (one wait per
+// window of 32 or 64 columns): each run's values are summed as d = y - K with K a value of that run
+// (row 0 of the warp, the run's first channel, the same for every lane), so the run's
+// M2 = sum d^2 - (sum d)^2 / n does not cancel however far the data sit from zero. The sums go
+// across the warp by reduce-scatters; lane l < runs-per-window then writes its run's mean and M2 to
+// red_mean / red_m2[q * 256 + run]. Rows past T_out (row_ok false) count zero; n_rows is the number
+// of valid rows of the warp (0: nothing is counted).
+template <int SUB>
+__device__ __forceinline__ void gn_run_stats(uint32_t tb, int c_lo, int c_hi, bool row_ok, int n_rows,
+                                             const float* bias, float* red_mean, float* red_m2, int q, int lane) {
+    constexpr int kWin = SUB == 1 ? 32 : (8 * SUB < 128 ? 8 * SUB : 128);
+    constexpr int kRuns = kWin / SUB;         // runs per window: a power of two <= 32
+    constexpr int kRunsPerChunk = 32 / SUB;   // runs per 32-column TMEM load
+    const float inv_n = n_rows > 0 ? 1.f / float(n_rows * SUB) : 0.f;
+#pragma unroll 1
+    for (int w0 = c_lo; w0 < c_hi; w0 += kWin) {  // uniform over the warp
+        float s1[kRuns], s2[kRuns];
+        float k_mine = 0.f;  // K of run (lane mod kRuns) of this window
+#pragma unroll
+        for (int c = 0; c < kWin / 32; ++c) {
+            const int j0 = w0 + c * 32;
+            if (j0 >= c_hi) {  // uniform: runs past the range stay empty
+#pragma unroll
+                for (int r = 0; r < kRunsPerChunk; ++r) s1[c * kRunsPerChunk + r] = s2[c * kRunsPerChunk + r] = 0.f;
+                continue;
+            }
+            float v[32];
+            tmem_load32(tb + uint32_t(j0), v);
+#pragma unroll
+            for (int r = 0; r < kRunsPerChunk; ++r) {
+                const int slot = c * kRunsPerChunk + r;
+                if constexpr (SUB == 1) {
+                    const float y = v[r] + bias[j0 + r];
+                    const float K = __shfl_sync(0xffffffffu, y, 0);
+                    if (lane == slot) k_mine = K;
+                    const float d = row_ok ? y - K : 0.f;
+                    s1[slot] = d;
+                    s2[slot] = d * d;
+                } else {
+                    float b[SUB];
+                    lds_vec(bias + j0 + r * SUB, b);
+                    const float K = __shfl_sync(0xffffffffu, v[r * SUB] + b[0], 0);
+                    if ((lane & (kRuns - 1)) == slot) k_mine = K;
+                    const uint64_t kk = f2_pack(K, K);
+                    uint64_t p1 = 0ull, p2 = 0ull;
+#pragma unroll
+                    for (int i = 0; i < SUB; i += 2) {
+                        const uint64_t d = f2_sub(f2_add(f2_pack(v[r * SUB + i], v[r * SUB + i + 1]), f2_pack(b[i], b[i + 1])), kk);
+                        p1 = f2_add(p1, d);
+                        p2 = f2_fma(d, d, p2);
+                    }
+                    s1[slot] = row_ok ? f2_hsum(p1) : 0.f;
+                    s2[slot] = row_ok ? f2_hsum(p2) : 0.f;
+                }
+            }
+        }
+        warp_sum_scatter<kRuns>(s1, lane);
+        warp_sum_scatter<kRuns>(s2, lane);
+        if (lane < kRuns && w0 + lane * SUB < c_hi) {
+            const float m = s1[0] * inv_n;
+            red_mean[q * 256 + w0 / SUB + lane] = k_mine + m;
+            red_m2[q * 256 + w0 / SUB + lane] = fmaxf(s2[0] - s1[0] * m, 0.f);
+        }
+    }
+}
+
+// Chan's pairwise merge of two (count, mean, M2) summaries, a first then b: the order is part of the
+// result (floating point), so callers that must agree bit for bit merge in one fixed order.
+__device__ __forceinline__ void stats_merge(float& n, float& mu, float& m2, float nb, float mub, float m2b) {
+    const float nt = n + nb;
+    if (nt <= 0.f) return;
+    const float f = nb / nt;
+    const float d = mub - mu;
+    mu = fmaf(d, f, mu);
+    m2 = m2 + m2b + d * d * (n * f);
+    n = nt;
+}
+
+// Merge with the summary held by lane (lane ^ d) of the warp, the lower lane's summary first, so
+// both lanes of the pair end with the same bits.
+__device__ __forceinline__ void stats_merge_xor(float& n, float& mu, float& m2, int d, int lane) {
+    const float n_o = __shfl_xor_sync(0xffffffffu, n, d);
+    const float mu_o = __shfl_xor_sync(0xffffffffu, mu, d);
+    const float m2_o = __shfl_xor_sync(0xffffffffu, m2, d);
+    const bool upper = (lane & d) != 0;  // the partner is the lower lane: its summary goes first
+    float na = upper ? n_o : n, ma = upper ? mu_o : mu, Ma = upper ? m2_o : m2;
+    stats_merge(na, ma, Ma, upper ? n : n_o, upper ? mu : mu_o, upper ? m2 : m2_o);
+    n = na;
+    mu = ma;
+    m2 = Ma;
+}
+
+__device__ __forceinline__ void gn_run_stats_any(int sub, uint32_t tb, int c_lo, int c_hi, bool row_ok, int n_rows,
+                                                 const float* bias, float* red_mean, float* red_m2, int q, int lane) {
+    if (sub == 4) gn_run_stats<4>(tb, c_lo, c_hi, row_ok, n_rows, bias, red_mean, red_m2, q, lane);
+    else if (sub == 8) gn_run_stats<8>(tb, c_lo, c_hi, row_ok, n_rows, bias, red_mean, red_m2, q, lane);
+    else if (sub == 16) gn_run_stats<16>(tb, c_lo, c_hi, row_ok, n_rows, bias, red_mean, red_m2, q, lane);
+    else gn_run_stats<1>(tb, c_lo, c_hi, row_ok, n_rows, bias, red_mean, red_m2, q, lane);
+}
+
 __device__ __forceinline__ void gn_run_moments_any(int sub, uint32_t tb, int c_lo, int c_hi, bool row_ok, int n_rows,
                                                    const float* bc, float* red_s, float* red_m, int q, int lane) {
     if (sub == 4) gn_run_moments<4>(tb, c_lo, c_hi, row_ok, n_rows, bc, red_s, red_m, q, lane);
@@ -304,6 +405,36 @@ __device__ __forceinline__ void ln_affine_gelu(float (&v)[32], const float* bias
     if (gelu) {
 #pragma unroll
         for (int i = 0; i < 32; i += 2) f2_unpack(gelu_erf2(f2_pack(v[i], v[i + 1])), v[i], v[i + 1]);
+    }
+}
+
+// Fused GroupNorm output: out = acc * colscale + colshift (then GELU when asked) for this warp's
+// columns [c_lo, c_hi), stored straight from registers. The 32 lanes of a warp hold 32 consecutive
+// time steps of one channel, so each store writes 128 contiguous bytes (64 for bf16). The code runs
+// once per launch: the chunk loop stays rolled so its instructions are fetched once and reused.
+template <bool GELU, typename OutT>
+__device__ __forceinline__ void gn_normalize_store(uint32_t tb, int c_lo, int c_hi, const float* colscale,
+                                                   const float* colshift, OutT* ybase, int T_out, bool row_ok) {
+    OutT* dst = ybase + (long long)c_lo * T_out;
+    const long long step = T_out;
+#pragma unroll 1
+    for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
+        float v[32];
+        tmem_load32(tb + uint32_t(j0), v);
+        const int nv = row_ok ? min(32, c_hi - j0) : 0;  // columns of this chunk to store
+#pragma unroll
+        for (int h = 0; h < 32; h += 8) {
+            float sc[8], sh[8];
+            lds_vec(colscale + j0 + h, sc);
+            lds_vec(colshift + j0 + h, sh);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float o = fmaf(v[h + i], sc[i], sh[i]);
+                if constexpr (GELU) o = gelu_erf(o);
+                if (h + i < nv) store_out(dst, o);
+                dst += step;
+            }
+        }
     }
 }
 
@@ -794,7 +925,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int obuf = 0;  // LayerNorm output staging: which of this warp's two tiles is next
             if (kFusedGN && first_unit < a.n_units) {
                 // One unit per CTA: stage bias, gamma and beta of its channel block while the
-                // mainloop runs (gamma and beta go where the column scale / shift end up).
+                // mainloop runs (gamma and beta go where the column scale / shift end up). (Warps that
+                // were x transposers have not waited for the preceding kernel yet.)
+                griddep_wait();
                 const int co_base = decode(first_unit).cbu * a.BN;
                 const int ncols = min(a.BN, a.C_out - co_base);
                 for (int col = er; col < 256; col += kEpiT) {
@@ -802,16 +935,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     s_bias[col] = (ok && a.bias) ? __ldg(a.bias + co_base + col) : 0.f;
                     epi[2304 + col] = ok ? (a.gamma ? __ldg(a.gamma + co_base + col) : 1.f) : 0.f;
                     epi[2560 + col] = (ok && a.beta) ? __ldg(a.beta + co_base + col) : 0.f;
-                }
-                named_bar_sync(1, kEpiT);
-                // the bias minus its mean over the column's run of `sub` channels (in epi[2816..3072),
-                // free until the statistics are merged)
-                const int run = a.sub > 0 ? a.sub : 1;
-                for (int col = er; col < 256; col += kEpiT) {
-                    const int r0 = col - col % run;
-                    float mb = 0.f;
-                    for (int i = 0; i < run; ++i) mb += s_bias[r0 + i];
-                    epi[2816 + col] = s_bias[col] - mb * (1.f / float(run));
                 }
                 // (the epilogue's first barrier, at the accumulator wait, orders these)
             }
@@ -1131,16 +1254,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     // ------------------------------------------------ fused GroupNorm (conv mode)
                     // The CTAs of one (sample, channel block) together cover all T_out steps. Each
-                    // reduces per-group partial statistics over its tile, the partials are exchanged
-                    // (distributed shared memory inside a cluster, or global memory across a
-                    // cooperative grid) and merged with Chan's formula, and each CTA normalizes its
-                    // tile from TMEM and stores it once.
+                    // takes the (mean, M2) of every group over its tile from one sweep of TMEM, the
+                    // statistics are exchanged (global memory across a cooperative grid, or distributed
+                    // shared memory inside a cluster) and merged, and each CTA normalizes its tile from
+                    // TMEM and stores it once, straight from registers.
                     const int co_base = un.cbu * a.BN;
                     const int ncols = min(a.BN, a.C_out - co_base);
                     const int cpg = a.cpg;
                     const int ngroups = (ncols + cpg - 1) / cpg;
                     const int nvalid_t = min(128, a.T_out - un.row0);
                     const int tt = un.row0 / 128;
+                    const int P = a.n_t_tiles;  // tiles (CTAs) whose statistics make up one group
                     // this warp's column range [c_lo, c_hi): the two warps of a lane quarter take one
                     // half each (whole 32-column chunks but the last)
                     const int half = ((ncols + 63) / 64) * 32;
@@ -1150,39 +1274,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // (mean | epoch) and (M2 | epoch). All words of a (sample, channel block) carry the
                     // same epoch, one step per launch (the weight pack zeroes them), so this launch's
                     // epoch is one past the one in this CTA's own word, read now so the load overlaps
-                    // the statistics pass.
+                    // the statistics sweep.
                     const size_t slot0 = size_t(un.n * a.n_cb + un.cbu) * a.n_t_tiles;
                     unsigned long long* gx_me = a.gx + (slot0 + tt) * size_t(a.gstride) * 2;
                     unsigned target = 0;
                     if (EPI == kEpiGridGN) target = unsigned(ld_relaxed_gpu_u64(gx_me) >> 32) + 1u;
-                    float* red_s = epi;            // [4][256] per-warp run sums
-                    float* red_m = epi + 1024;     // [4][256] per-warp run sums of squared deviations
-                    float* part_mu = epi + 2048;   // [256] this CTA's group means (cluster exchange)
+                    float* red_mean = epi;         // [4][256] per lane quarter and run: mean of y over the run
+                    float* red_m2 = epi + 1024;    // [4][256] ... and its M2
+                    float* part_mu = epi + 2048;   // [256] this CTA's group means (cluster); peers' means (grid)
                     float* colscale = epi + 2304;  // [256]
                     float* colshift = epi + 2560;  // [256]
                     float* gmean = epi + 2816;     // [256] group mean over all CTAs
                     float* grstd = epi + 3328;     // [256] group 1/sqrt(var + eps)
-                    float* part_m2 = epi + 3584;   // [256] this CTA's group M2 (cluster exchange)
-                    const float* s_bc = epi + 2816;  // [256] bias minus its run mean (gmean's area, later)
+                    float* part_m2 = epi + 3584;   // [256] this CTA's group M2 (cluster); peers' M2 (grid)
                     const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
-                    // this warp's moments per run of `sub` channels (two sweeps of its TMEM columns), then
-                    // this CTA's (count, mean, M2) per group, merged over runs and warps
                     const int nvalid_w = min(32, max(0, nvalid_t - q * 32));
-                    gn_run_moments_any(a.sub, tb, c_lo, c_hi, lane < nvalid_w, nvalid_w, s_bc, red_s, red_m, q, lane);
+                    gn_run_stats_any(a.sub, tb, c_lo, c_hi, lane < nvalid_w, nvalid_w, s_bias, red_mean, red_m2, q,
+                                     lane);
                     named_bar_sync(1, kEpiT);
+                    // This CTA's (mean, M2) per group from its (run, lane quarter) entries by the
+                    // parallel-axis formula: the count-weighted mean, then the entries' M2 plus each
+                    // entry's count times the squared distance of its mean from the group mean.
                     const int run = a.sub > 0 ? a.sub : 1;
+                    float qn[4];  // count of one run's entry in lane quarter q2
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) qn[q2] = float(min(32, max(0, nvalid_t - q2 * 32)) * run);
                     for (int g = er; g < ngroups; g += kEpiT) {
-                        const int c0 = g * cpg, c_end = min(ncols, c0 + cpg);
-                        float gn = 0.f, gmu = 0.f, gm2 = 0.f;
-                        for (int j = c0 / run; j < (c_end + run - 1) / run; ++j) {
-                            float mb = 0.f;  // the bias mean of run j
-                            for (int i = 0; i < run; ++i) mb += s_bias[j * run + i];
-                            mb *= 1.f / float(run);
+                        const int j_lo = g * cpg / run, j_hi = (min(ncols, g * cpg + cpg) + run - 1) / run;
+                        float n_tot = 0.f, s = 0.f;
+                        for (int j = j_lo; j < j_hi; ++j) {
+#pragma unroll
                             for (int q2 = 0; q2 < 4; ++q2) {
-                                const int nr = min(32, max(0, nvalid_t - q2 * 32));
-                                if (nr == 0) continue;
-                                const float nq = float(nr * run);
-                                chan_merge(gn, gmu, gm2, nq, red_s[q2 * 256 + j] / nq + mb, red_m[q2 * 256 + j]);
+                                n_tot += qn[q2];
+                                s = fmaf(qn[q2], red_mean[q2 * 256 + j], s);  // (qn = 0: the entry is finite)
+                            }
+                        }
+                        const float gmu = n_tot > 0.f ? s / n_tot : 0.f;
+                        float gm2 = 0.f;
+                        for (int j = j_lo; j < j_hi; ++j) {
+#pragma unroll
+                            for (int q2 = 0; q2 < 4; ++q2) {
+                                const float d = red_mean[q2 * 256 + j] - gmu;
+                                gm2 += fmaf(qn[q2] * d, d, red_m2[q2 * 256 + j]);
                             }
                         }
                         if (EPI == kEpiGridGN) {
@@ -1202,7 +1335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float cw = float(min(ncols, g * cpg + cpg) - g * cpg);
                             float gn = 0.f, gmu = 0.f, gm2 = 0.f;
                             const uint32_t pmu = smem_u32(part_mu + g), pm2 = smem_u32(part_m2 + g);
-                            for (int rk = 0; rk < a.n_t_tiles; ++rk) {
+                            for (int rk = 0; rk < P; ++rk) {
                                 const float cnt = cw * float(min(128, a.T_out - rk * 128));
                                 chan_merge(gn, gmu, gm2, cnt, ld_shared_cluster_f32(map_shared_rank(pmu, uint32_t(rk))),
                                            ld_shared_cluster_f32(map_shared_rank(pm2, uint32_t(rk))));
@@ -1211,32 +1344,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                             grstd[g] = rsqrtf((gn > 0.f ? gm2 / gn : 0.f) + a.eps);
                         }
                     } else {
-                        // Every thread waits (bounded) for its groups' words from all peers: each word
-                        // carries its value and the epoch in one 64-bit access, so a word that shows this
-                        // launch's epoch holds this launch's value, with no fence on either side.
+                        // Each (group, peer tile) pair has a thread that waits (bounded) for that peer's
+                        // two words: a word carries its value and the epoch in one 64-bit access, so a
+                        // word showing this launch's epoch holds this launch's value, with no fence on
+                        // either side, and all peers' words are in flight at once. The P threads of a
+                        // group then merge by shuffles (P a power of two, all pairs in one pass), or one
+                        // thread per group merges them in peer order. Either way every CTA of the sample
+                        // merges the same values in the same order and normalizes with identical bits.
                         const unsigned long long* gq = a.gx + slot0 * size_t(a.gstride) * 2;
                         const size_t tile_words = size_t(a.gstride) * 2;
-                        for (int g = er; g < ngroups; g += kEpiT) {
-                            const float cw = float(min(ncols, g * cpg + cpg) - g * cpg);
-                            float gn = 0.f, gmu = 0.f, gm2 = 0.f;
-                            const uint64_t t0 = global_timer_ns();
-                            constexpr int kPollBatch = 2;  // peers whose words are in flight together
-                            for (int base_rk = 0; base_rk < a.n_t_tiles; base_rk += kPollBatch) {
-                                const int nrk = min(kPollBatch, a.n_t_tiles - base_rk);
-                                unsigned long long wmu[kPollBatch], wm2[kPollBatch];
-                                for (;;) {
-                                    bool all = true;
-#pragma unroll
-                                    for (int r = 0; r < kPollBatch; ++r) {
-                                        if (r < nrk) {
-                                            const unsigned long long* w = gq + size_t(base_rk + r) * tile_words + 2 * g;
-                                            wmu[r] = ld_relaxed_gpu_u64(w);
-                                            wm2[r] = ld_relaxed_gpu_u64(w + 1);
-                                            all &= unsigned(wmu[r] >> 32) == target && unsigned(wm2[r] >> 32) == target;
-                                        }
-                                    }
-                                    if (all || *abort_flag) break;
-                                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                        const bool tree = (P & (P - 1)) == 0 && P <= 32 && ngroups * P <= kEpiT;
+                        const bool in_smem = ngroups * P <= 256;  // peers' words kept for the serial merge
+                        const uint64_t t0 = global_timer_ns();
+                        for (int base = 0; base < ngroups * P; base += kEpiT) {  // uniform over the warp
+                            const int idx = base + er;
+                            const int g = idx / P, p = idx - g * P;
+                            unsigned long long wmu = 0ull, wm2 = 0ull;
+                            if (g < ngroups) {
+                                const unsigned long long* w = gq + size_t(p) * tile_words + 2 * g;
+                                for (uint32_t it = 0;; ++it) {
+                                    wmu = ld_relaxed_gpu_u64(w);
+                                    wm2 = ld_relaxed_gpu_u64(w + 1);
+                                    if ((unsigned(wmu >> 32) == target && unsigned(wm2 >> 32) == target) || *abort_flag)
+                                        break;
+                                    if ((it & 15u) == 15u && global_timer_ns() - t0 > kWaitLimitNs) {
                                         if (atomicCAS(a.status, 0, 6) == 0) {
                                             atomicExch(a.status + 1, kWaitGridPeers);
                                             atomicExch(a.status + 2, int(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)));
@@ -1245,17 +1376,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         break;
                                     }
                                 }
-#pragma unroll
-                                for (int r = 0; r < kPollBatch; ++r) {
-                                    if (r < nrk) {
-                                        const float cnt = cw * float(min(128, a.T_out - (base_rk + r) * 128));
-                                        chan_merge(gn, gmu, gm2, cnt, __uint_as_float(unsigned(wmu[r])),
-                                                   __uint_as_float(unsigned(wm2[r])));
-                                    }
-                                }
                             }
-                            gmean[g] = gmu;
-                            grstd[g] = rsqrtf((gn > 0.f ? gm2 / gn : 0.f) + a.eps);
+                            if (tree) {
+                                float n = 0.f, mu = 0.f, m2 = 0.f;
+                                if (g < ngroups) {
+                                    n = float(min(ncols, g * cpg + cpg) - g * cpg) * float(min(128, a.T_out - p * 128));
+                                    mu = __uint_as_float(unsigned(wmu));
+                                    m2 = __uint_as_float(unsigned(wm2));
+                                }
+                                for (int d = 1; d < P; d <<= 1) stats_merge_xor(n, mu, m2, d, lane);
+                                if (g < ngroups && p == 0) {
+                                    gmean[g] = mu;
+                                    grstd[g] = rsqrtf(m2 / n + a.eps);
+                                }
+                            } else if (in_smem && g < ngroups) {
+                                part_mu[idx] = __uint_as_float(unsigned(wmu));
+                                part_m2[idx] = __uint_as_float(unsigned(wm2));
+                            }
+                        }
+                        if (!tree) {
+                            named_bar_sync(1, kEpiT);
+                            for (int g = er; g < ngroups; g += kEpiT) {
+                                const float cw = float(min(ncols, g * cpg + cpg) - g * cpg);
+                                float n = 0.f, mu = 0.f, m2 = 0.f;
+                                for (int p = 0; p < P; ++p) {
+                                    float pm, pv;
+                                    if (in_smem) {
+                                        pm = part_mu[g * P + p];
+                                        pv = part_m2[g * P + p];
+                                    } else {  // more pairs than fit: read the words again (they hold this
+                                              // launch's values by now)
+                                        const unsigned long long* w = gq + size_t(p) * tile_words + 2 * g;
+                                        pm = __uint_as_float(unsigned(ld_relaxed_gpu_u64(w)));
+                                        pv = __uint_as_float(unsigned(ld_relaxed_gpu_u64(w + 1)));
+                                    }
+                                    stats_merge(n, mu, m2, cw * float(min(128, a.T_out - p * 128)), pm, pv);
+                                }
+                                gmean[g] = mu;
+                                grstd[g] = rsqrtf(m2 / n + a.eps);
+                            }
                         }
                     }
                     named_bar_sync(1, kEpiT);
@@ -1271,59 +1430,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         colshift[col] = sh;
                     }
                     named_bar_sync(1, kEpiT);
-                    // normalize from TMEM; store once
-                    if (a.tma_store) {
-                        // Each warp stages its 32 time steps of every 32-channel chunk of its column range
-                        // as a [32 ch][32 t] tile in the operand rings (idle now that the tile's MMAs are
-                        // done) and sends it with a bulk store as soon as it is staged (rows past T_out
-                        // and channels past C_out are clipped). Before the CTA leaves, the stores only
-                        // have to finish reading shared memory.
-                        const int nch = (a.BN + 31) / 32;
-                        OutT* so = reinterpret_cast<OutT*>(base + size_t(SA) * a.a_slot_bytes) + q * (nch * 32 * 32);
-                        for (int j0 = c_lo; j0 < c_hi; j0 += 32) {
-                            float v[32];
-                            tmem_load32(tb + uint32_t(j0), v);
-                            OutT* ob = so + (j0 / 32) * (32 * 32);
-#pragma unroll
-                            for (int h = 0; h < 32; h += 8) {
-                                float sc[8], sh[8];
-                                lds_vec(colscale + j0 + h, sc);
-                                lds_vec(colshift + j0 + h, sh);
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    float o = fmaf(v[h + i], sc[i], sh[i]);
-                                    if (a.gelu) o = gelu_erf(o);
-                                    store_out(ob + (h + i) * 32 + lane, o);
-                                }
-                            }
-                            fence_async_shared();
-                            __syncwarp();
-                            if (lane == 0) tma_store_3d(&tm_y, smem_u32(ob), un.row0 + q * 32, co_base + j0, un.n);
-                        }
-                        if (lane == 0) tma_store_wait_read();
-                        __syncwarp();
-                    } else {
-                        for (int j0 = c_lo; j0 < c_hi; j0 += 16) {
-                            float v[16];
-                            tmem_load16(tb + uint32_t(j0), v);
-                            {
-                                float sc[16], sh[16];
-                                lds_vec(colscale + j0, sc);
-                                lds_vec(colshift + j0, sh);
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) v[i] = fmaf(v[i], sc[i], sh[i]);
-                            }
-                            if (a.gelu) {
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
-                            }
-                            if (!row_ok) continue;
-                            OutT* dst = y + ((long long)un.n * a.C_out + co_base + j0) * a.T_out + row;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (j0 + i < ncols) store_out(dst + (long long)i * a.T_out, v[i]);
-                        }
-                    }
+                    // Normalize from TMEM and store straight from registers: the 32 lanes of a warp hold
+                    // 32 consecutive time steps of a channel, so every store writes 128 contiguous bytes
+                    // (64 for bf16). Two 32-column TMEM loads share one wait.
+                    // (GELU or not is decided once, outside the unrolled loops, so the loop without it
+                    // is compact straight-line code)
+                    OutT* ybase = y + ((long long)un.n * a.C_out + co_base) * a.T_out + row;
+                    if (a.gelu) gn_normalize_store<true>(tb, c_lo, c_hi, colscale, colshift, ybase, a.T_out, row_ok);
+                    else gn_normalize_store<false>(tb, c_lo, c_hi, colscale, colshift, ybase, a.T_out, row_ok);
                 }
                 tc_fence_before();
                 __syncwarp();

@@ -66,9 +66,11 @@ typedef enum { C1N_NORM_NONE = 0, C1N_NORM_GROUP = 1, C1N_NORM_CHANNEL_LAYER = 2
 typedef enum { C1N_POST_NONE = 0, C1N_POST_GELU_ERF = 1, C1N_POST_ROWMIN_BIAS = 2 } c1n_post;
 typedef enum { C1N_F32 = 0, C1N_BF16 = 1 } c1n_dtype;
 
-/* Arithmetic used for the contraction. AUTO picks the tensor-core path when the shape allows it
- * (TF32 tensor cores for fp32 data, BF16 for bf16 data) and the SIMT fp32 CUDA path otherwise;
- * TENSOR fails with C1N_ERR_UNSUPPORTED instead of falling back; SIMT always uses fp32 FMA.
+/* Arithmetic used for the contraction. AUTO and TENSOR take the tensor-core path (TF32 tensor
+ * cores for fp32 data, BF16 for bf16 data); a shape that path cannot take (stride > 1, T not a
+ * multiple of 16 bytes of elements, more than 16 taps, ...) makes desc_create return
+ * C1N_ERR_UNSUPPORTED: there is no silent fallback to another kind of arithmetic. SIMT (the fp32
+ * FMA CUDA-core path, which takes every valid shape) runs only when the caller asks for it.
  * TENSOR_X3 (fp32 data, convolution plans): fp32-accurate tensor cores. Each operand is split into
  * a TF32 head and a TF32 tail (x = hi + lo, hi = x rounded to TF32, lo = x - hi) and the products
  * are accumulated in fp32 as hi*hi + hi*lo + lo*hi (three MMAs per step; lo*lo, ~2^-22 of the
@@ -196,6 +198,8 @@ c1n_status conv1d_norm_check(const c1n_desc* desc, void* workspace, c1n_stream_t
  *
  *   - args->x, w, b, gamma, beta, bias2, y, argmin as for conv1d_norm_run_ex; args->workspace must
  *     be NULL (the array is the workspace).
+ *   - args->flags must not hold C1N_FLAG_WEIGHTS_PACKED (C1N_ERR_INVALID_ARG): the array is shared
+ *     by every descriptor, so the packed weights in it may be another operator's; every call packs.
  *   - Returns C1N_ERR_WORKSPACE if conv1d_norm_workspace_size(desc) exceeds C1N_STATIC_SCRATCH_BYTES.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *     that device current; make that first call before any stream capture.

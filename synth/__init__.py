@@ -22,8 +22,10 @@ bf16 inputs are float32 values rounded to the nearest bf16 (ties to even) by
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
 import math
+import os
 from typing import Dict, Optional
 
 import numpy as np
@@ -63,20 +65,46 @@ def uniform01(seed: int, stream: int, count: int, start: int = 0) -> np.ndarray:
     return (raw_u64(seed, stream, start, count) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
 
 
+_CHUNK = 1 << 22
+_pool = None
+
+
+def _map_chunks(fn, count: int) -> None:
+    """fn(s, n) for the chunks [s, s + n) of range(count), on a thread pool when there are several
+    (numpy releases the interpreter lock in these array operations). Each chunk is a pure function
+    of its counters, so the result does not depend on the thread count or order."""
+    global _pool
+    chunks = [(s, min(_CHUNK, count - s)) for s in range(0, count, _CHUNK)]
+    if len(chunks) <= 1:
+        for s, n in chunks:
+            fn(s, n)
+        return
+    if _pool is None:
+        _pool = concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(32, os.cpu_count() or 1)))
+    list(_pool.map(lambda c: fn(*c), chunks))
+
+
 def uniform_pm(seed: int, stream: int, count: int, a: float) -> np.ndarray:
     """float32 samples of U(-a, a)."""
-    return (a * (2.0 * uniform01(seed, stream, count) - 1.0)).astype(np.float32)
+    out = np.empty(count, dtype=np.float32)
+
+    def fill(s, n):
+        out[s:s + n] = (a * (2.0 * uniform01(seed, stream, n, start=s) - 1.0)).astype(np.float32)
+
+    _map_chunks(fill, count)
+    return out
 
 
 def normal_slice(seed: int, stream: int, start: int, count: int, mu: float = 0.0, sigma: float = 1.0) -> np.ndarray:
     """Elements start .. start+count-1 of the stream's N(mu, sigma) sequence (float32)."""
     out = np.empty(count, dtype=np.float32)
-    chunk = 1 << 22
-    for s in range(0, count, chunk):
-        n = min(chunk, count - s)
+
+    def fill(s, n):
         u = uniform01(seed, stream, 2 * n, start=2 * (start + s))
         r = np.sqrt(-2.0 * np.log1p(-u[0::2]))
         out[s:s + n] = (mu + sigma * r * np.cos(2.0 * math.pi * u[1::2])).astype(np.float32)
+
+    _map_chunks(fill, count)
     return out
 
 

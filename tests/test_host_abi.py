@@ -135,13 +135,18 @@ def test_simt_forced_and_tensor_forced():
     d = c1n.conv1d_norm_desc_create(_params(wl, math=c1n.MATH_SIMT))
     assert c1n.conv1d_norm_plan_info(d).path == c1n.PATH_SIMT
     c1n.conv1d_norm_destroy(d)
-    # stride 2 has no tensor-core plan: AUTO takes the SIMT kernels, TENSOR refuses.
-    d = c1n.conv1d_norm_desc_create(_params(wl, stride=2))
-    assert c1n.conv1d_norm_plan_info(d).path == c1n.PATH_SIMT
-    c1n.conv1d_norm_destroy(d)
-    with pytest.raises(c1n.C1NError) as e:
-        c1n.conv1d_norm_desc_create(_params(wl, stride=2, math=c1n.MATH_TENSOR))
-    assert e.value.status == c1n.ERR_UNSUPPORTED
+    # No silent fallback: shapes without a tensor-core plan (stride 2; T not a multiple of 16 bytes
+    # of elements) are refused under AUTO as under TENSOR, and run on the SIMT path only when the
+    # caller asks for it.
+    for bad in (dict(stride=2), dict(T=77), dict(T=126)):
+        for math in (c1n.MATH_AUTO, c1n.MATH_TENSOR):
+            with pytest.raises(c1n.C1NError) as e:
+                c1n.conv1d_norm_desc_create(_params(wl, math=math, **bad))
+            assert e.value.status == c1n.ERR_UNSUPPORTED
+            assert "SIMT" in str(e.value) or math == c1n.MATH_TENSOR
+        d = c1n.conv1d_norm_desc_create(_params(wl, math=c1n.MATH_SIMT, **bad))
+        assert c1n.conv1d_norm_plan_info(d).path == c1n.PATH_SIMT
+        c1n.conv1d_norm_destroy(d)
     d = c1n.conv1d_norm_desc_create(_params(wl, force_path=c1n.PATH_TC_TWO_PASS))
     assert c1n.conv1d_norm_plan_info(d).path == c1n.PATH_TC_TWO_PASS
     c1n.conv1d_norm_destroy(d)
@@ -272,3 +277,16 @@ def test_fused_p4_model_validation_without_device():
             c1n.conv_transpose3d_ln_avgpool3d_gelu_run(p(), a["eps"], 1.0, a["x"], x, None, None, None, a["out"], a["ws"],
                                                        a["ws_bytes"], 0)
         assert e.value.status == status
+
+
+def test_static_scratch_refuses_prepacked_weights_without_device():
+    # The entry point without allocation shares one array among all descriptors, so weights packed
+    # by an earlier call may be another operator's: it refuses the flag before touching the device.
+    d = c1n.conv1d_norm_desc_create(_params(synth.CONV_GN_TINY))
+    lib = c1n.load()
+    args = c1n.Args(16, 16, None, None, None, None, 16, None, None, 0, c1n.FLAG_WEIGHTS_PACKED)
+    assert lib.conv1d_norm_run_static_scratch(d, ctypes.byref(args), None) == c1n.ERR_INVALID_ARG
+    assert b"WEIGHTS_PACKED" in lib.conv1d_norm_last_error()
+    args = c1n.Args(16, 16, None, None, None, None, 16, None, 4096, 1 << 20, 0)  # a workspace is refused too
+    assert lib.conv1d_norm_run_static_scratch(d, ctypes.byref(args), None) == c1n.ERR_INVALID_ARG
+    c1n.conv1d_norm_destroy(d)

@@ -137,6 +137,8 @@ SMALL = {
     "stride2_simt": synth.CONV_GN.replace(N=2, C_in=16, C_out=32, T=101, stride=2, groups=8),
     "odd_T_simt": synth.CAUSAL_CONV.replace(N=2, C_in=8, C_out=24, T=77),
 }
+# shapes no tensor-core plan takes: refused unless the caller asks for the SIMT path
+TC_REFUSED = {"stride2_simt", "odd_T_simt"}
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
@@ -145,10 +147,17 @@ def test_small_shapes(cuda_lib, name, mode):
     # auto: the planner's choice; single: one CTA per 128-row tile; pair: CTA-pair (cta_group::2)
     # mainloop where the plan allows it; simt: the fp32 CUDA-core check path
     wl = SMALL[name]
-    inp = _inputs(wl)
-    ref, ref_am = oracle_full(wl, inp)
     math = 1 if mode == "simt" else 0
     mainloop = {"single": cuda_lib.MAINLOOP_SINGLE, "pair": cuda_lib.MAINLOOP_PAIR}.get(mode, cuda_lib.MAINLOOP_AUTO)
+    if name in TC_REFUSED and math == 0:
+        with pytest.raises(cuda_lib.C1NError) as e:
+            cuda_lib.conv1d_norm_desc_create(cuda_lib.make_params(
+                wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right, wl.dilation, wl.norm,
+                wl.groups, wl.eps, wl.post, wl.dtype, 0, -1, mainloop))
+        assert e.value.status == cuda_lib.ERR_UNSUPPORTED
+        return
+    inp = _inputs(wl)
+    ref, ref_am = oracle_full(wl, inp)
     if mode == "pair":
         try:
             cuda_lib.conv1d_norm_destroy(cuda_lib.conv1d_norm_desc_create(cuda_lib.make_params(
@@ -260,7 +269,8 @@ def test_kernel_times_list_every_launch(cuda_lib, name, kernels):
     wl = SMALL[name]
     inp = _inputs(wl)
     params = cuda_lib.make_params(wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right,
-                                  wl.dilation, wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, 0,
+                                  wl.dilation, wl.norm, wl.groups, wl.eps, wl.post, wl.dtype,
+                                  cuda_lib.MATH_SIMT if name in TC_REFUSED else 0,
                                   cuda_lib.PATH_TC_TWO_PASS if name == "ln_c384_f32" else -1)
     op = cuda_lib.Conv1dNorm(params)
     op.set_profiling(True)
