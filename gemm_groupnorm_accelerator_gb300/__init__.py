@@ -75,6 +75,7 @@ class Args(ctypes.Structure):
 
 
 FLAG_WEIGHTS_PACKED = 1
+FLAG_TEST_STALL_EXCHANGE = 2  # testing aid: see C1N_FLAG_TEST_STALL_EXCHANGE in the C header
 
 
 class C1NError(RuntimeError):

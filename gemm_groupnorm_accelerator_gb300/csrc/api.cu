@@ -641,6 +641,12 @@ c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
             else return fail(C1N_ERR_UNSUPPORTED, "fused GroupNorm grid of %d CTAs exceeds the %d SMs of this device",
                              pl.n_units, d->num_sms);
         }
+        if (a->flags & C1N_FLAG_TEST_STALL_EXCHANGE) {
+            if (epi != kEpiGridGN)
+                return fail(C1N_ERR_INVALID_ARG, "C1N_FLAG_TEST_STALL_EXCHANGE needs the fused GroupNorm plan that "
+                                                 "exchanges statistics through global memory");
+            t.test_stall = 1;
+        }
         mark(d, s, "tc_conv");
         e = launch_tc(pl, t, d->tm_a, d->tm_b, tma_store ? d->tm_y : d->tm_b, linear, epi, out_bf16, d->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
@@ -822,6 +828,11 @@ c1n_status conv1d_norm_check(const c1n_desc* desc, void* workspace, c1n_stream_t
     if (e != cudaSuccess) return cuda_fail(e, "status read");
     if (word[0] != 0) {
         e = cudaMemsetAsync(ws, 0, sizeof(word), s);
+        // A run that gave up may have left the fused GroupNorm exchange words with mixed epochs:
+        // zero them (the state the weight pack leaves) so the next run agrees on its epoch.
+        const Plan& pl = desc->plan;
+        if (e == cudaSuccess && pl.gx_words > 0)
+            e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + pl.ws_gx, 0, (size_t)pl.gx_words * 4, s);
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
         if (e != cudaSuccess) return cuda_fail(e, "status reset");
         if (word[0] == C1N_ERR_TIMEOUT)

@@ -94,6 +94,7 @@ struct TcArgs {
     int part_kind;
     int part_tiles;
     float2* part;
+    int test_stall;  // C1N_FLAG_TEST_STALL_EXCHANGE: the first CTA withholds its exchange words
 };
 
 // Sets the calling thread's message returned by conv1d_norm_last_error().

@@ -1319,9 +1319,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                         if (EPI == kEpiGridGN) {
+                            // (testing aid: the first CTA withholds its words, so its sample's waits run out)
+                            const bool withhold = a.test_stall && (blockIdx.x | blockIdx.y | blockIdx.z) == 0;
                             const unsigned long long tag = (unsigned long long)target << 32;
-                            st_relaxed_gpu_u64(gx_me + 2 * g, tag | __float_as_uint(gmu));
-                            st_relaxed_gpu_u64(gx_me + 2 * g + 1, tag | __float_as_uint(gm2));
+                            if (!withhold) {
+                                st_relaxed_gpu_u64(gx_me + 2 * g, tag | __float_as_uint(gmu));
+                                st_relaxed_gpu_u64(gx_me + 2 * g + 1, tag | __float_as_uint(gm2));
+                            }
                         } else {
                             part_mu[g] = gmu;
                             part_m2[g] = gm2;

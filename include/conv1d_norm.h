@@ -174,6 +174,13 @@ typedef struct {
 /* The weights were already packed into this workspace by conv1d_norm_pack_weights (same w, same
  * workspace); run_ex then skips its own packing step. */
 #define C1N_FLAG_WEIGHTS_PACKED 1u
+/* Testing aid for the device failure path (no counterpart on the pages): on the fused GroupNorm
+ * plan whose CTAs exchange statistics through global memory, the first CTA withholds its partial
+ * statistics, so the bounded waits of the CTAs of its sample run out (after about one second). The
+ * kernel then records C1N_ERR_TIMEOUT (site 10, the grid exchange) in the workspace status word and
+ * returns; y is unspecified. Nothing faults or hangs. Other plans refuse the flag with
+ * C1N_ERR_INVALID_ARG. conv1d_norm_check reports the timeout and resets the exchange state. */
+#define C1N_FLAG_TEST_STALL_EXCHANGE 2u
 
 c1n_status conv1d_norm_run_ex(c1n_desc* desc, const c1n_args* args, c1n_stream_t stream);
 
@@ -185,7 +192,10 @@ c1n_status conv1d_norm_pack_weights(c1n_desc* desc, const void* w, void* workspa
                                     c1n_stream_t stream);
 
 /* Synchronise `stream`, read and clear the device status word of the given workspace (NULL: the
- * attached one) and return C1N_OK, C1N_ERR_TIMEOUT or C1N_ERR_DEVICE. */
+ * attached one) and return C1N_OK, C1N_ERR_TIMEOUT or C1N_ERR_DEVICE (the message from
+ * conv1d_norm_last_error names the wait site, the CTA and the pipeline's progress counters). After
+ * a device failure it also resets the fused GroupNorm exchange words of that workspace, so the next
+ * run (weights packed or not) starts from a consistent state. */
 c1n_status conv1d_norm_check(const c1n_desc* desc, void* workspace, c1n_stream_t stream);
 
 /* Operator run for callers that cannot allocate device memory (no counterpart on the pages; this is

@@ -134,17 +134,17 @@ def test_conv_transpose3d_tensor_core_shapes(cuda_lib, name, math):
 def test_p4_pipeline_full_size_sampled(cuda_lib, math):
     # the page's model after its weights: ConvTranspose3d on x [32, 32, 16, 32, 32], then + sum_weight,
     # LayerNorm over W = 64, AvgPool3d 2x2x2, GELU -- at full size on the GPU, checked against the
-    # oracle composition on two samples
+    # oracle composition on samples spread over the batch
     wl = synth.CONV_TRANSPOSE3D
     inp = synth.make_convt3d_inputs(wl)
     y = _convt_gpu(cuda_lib, wl, inp, math=math)
-    tol_y, tol_out = (TOL, TOL) if math == 1 else (TOL_TF32, 2e-2)
+    tol_y, tol_out = (TOL, TOL) if math == 1 else (TOL_TF32, TOL_TF32)
     lp = synth.LN_AVGPOOL3D_GELU
     gb = synth.make_lnpool_inputs(lp.replace(N=1, C=1, D=2, H=2))
     ga, be = torch.from_numpy(gb["gamma"]).cuda(), torch.from_numpy(gb["beta"]).cuda()
     out = cuda_lib.ln_avgpool3d_gelu(y, lp.sum_weight, ga, be, eps=lp.eps)
     torch.cuda.synchronize()
-    for n in (0, wl.N - 1):
+    for n in (0, 9, 22, wl.N - 1):
         yn = oracle.conv_transpose3d(inp["x"][n:n + 1], inp["w"], inp["b"], stride=wl.stride, pad=wl.pad,
                                      out_pad=wl.out_pad)
         err_y = float(np.max(np.abs(y[n].cpu().numpy().astype(np.float64) - yn[0])))
@@ -183,7 +183,11 @@ def _model_oracle(wl, inp, gb, lp, n, affine=True, bias=True):
                                     gb["beta"] if affine else None)
 
 
-TOL_FUSED = 2e-2  # TF32 operands into a LayerNorm (the same bound as the two-kernel pipeline on the tensor cores)
+# TF32 operands (x and w rounded to TF32, fp32 accumulation) into a LayerNorm: the tensor-path bound of
+# 5e-3 on unit-scale outputs. The relative TF32 error of y (~6e-4 rms) becomes an absolute error of
+# the same order after the LayerNorm and shrinks by the 8-value average of the pool; measured at full
+# size: 5.7e-4 at most over 8 batch entries.
+TOL_FUSED = TOL_TF32
 
 
 @pytest.mark.parametrize("name", list(FUSED))
@@ -202,7 +206,7 @@ def test_fused_model_small(cuda_lib, name, affine, bias):
 
 
 def test_fused_model_full_size(cuda_lib):
-    # the page's model at full size: the one-pass kernel against the oracle on two samples, and
+    # the page's model at full size: the one-pass kernel against the oracle on 8 spread samples, and
     # against the two-kernel path (tensor-core ConvTranspose3d, then the LayerNorm/pool/GELU pass)
     # everywhere -- both use the same TF32 products, so they agree far inside the oracle tolerance
     wl = synth.CONV_TRANSPOSE3D
@@ -217,7 +221,7 @@ def test_fused_model_full_size(cuda_lib):
     assert bool(torch.isfinite(fused).all())
     diff = float((fused - two).abs().max())
     assert diff <= 1e-3, f"fused vs two-kernel path: max abs diff {diff:.3e}"
-    for n in (0, wl.N - 1):
+    for n in (0, 4, 9, 13, 18, 22, 27, wl.N - 1):
         ref = _model_oracle(wl, inp, gb, lp, n)
         err = float(np.max(np.abs(fused[n].cpu().numpy().astype(np.float64) - ref)))
         assert err <= TOL_FUSED, f"sample {n}: max abs err {err:.3e}"

@@ -368,7 +368,9 @@ def test_causal_conv_full_sampled(cuda_lib):
     y, _, path = run_gpu(cuda_lib, wl, inp)
     assert path == "tc_direct"
     y1, _, _ = run_gpu(cuda_lib, wl, inp, mainloop=cuda_lib.MAINLOOP_PAIR)
-    ns = [0, wl.N - 1]
+    # 8 samples spread over the batch: the persistent CTAs (one per SM) walk 2048 tiles, so these
+    # samples' tiles fall in the first, middle and last work units of the schedule
+    ns = [0, 4, 9, 13, 18, 22, 27, wl.N - 1]
     ref, _ = oracle.conv1d_norm_samples(oracle.params_of(wl), ns, inp["x"], inp["w"], inp["b"])
     compare(wl, y[ns], None, ref, None, path, wl.name)
     compare(wl, y1[ns], None, ref, None, path, wl.name + " (CTA-pair mainloop)")
@@ -380,7 +382,8 @@ def test_linear_gn_rowmin_full_sampled(cuda_lib):
     inp = _inputs(wl)
     y, am, path = run_gpu(cuda_lib, wl, inp)
     assert path == "tc_linear"
-    ns = [0, 1, 500, wl.N - 1]
+    # one row from each of the eight 128-row M tiles (the CTA pairs take 256-row tiles)
+    ns = [5, 130, 300, 420, 555, 700, 833, wl.N - 1]
     p = oracle.params_of(wl)
     ref, ref_am = oracle.conv1d_norm_samples(p, ns, inp["x"], inp["w"], inp["b"], inp["gamma"], inp["beta"],
                                              inp["bias2"])
@@ -399,7 +402,7 @@ def test_conv_ln_gelu_bf16_full_sampled(cuda_lib):
     assert path == "tc_fused_ln"
     y2, _, path2 = run_gpu(cuda_lib, wl, inp, force_path=cuda_lib.PATH_TC_TWO_PASS)
     assert path2 == "tc_two_pass"
-    ns = [0, wl.N - 1]
+    ns = [0, 9, 18, 27, 36, 45, 54, wl.N - 1]  # spread over the persistent clusters' schedule
     ref, _ = oracle.conv1d_norm_samples(oracle.params_of(wl), ns, inp["x"], inp["w"], inp["b"], inp["gamma"],
                                         inp["beta"])
     compare(wl, y[ns], None, ref, None, path, wl.name)
