@@ -181,6 +181,10 @@ bool plan_tc_geometry(const c1n_params& p, Plan& pl, bool cluster, bool pair = f
         pl.tmem_cols = 512;
     }
     if (pl.pair) plan_stages(pl, 2, 8, 3);  // half-size B slots: a deeper weight ring
+    else if (cluster) plan_stages(pl, std::max(2, std::min(pl.n_ci_chunks, 4)), 4, 2);  // one tile per CTA: A
+                                                                                        // slots for up to 4
+                                                                                        // chunks, so x staging
+                                                                                        // runs ahead of the MMA
     else plan_stages(pl, 2, 4, 4);
     return pl.smem_bytes <= 227 * 1024;
 }

@@ -228,7 +228,7 @@ __device__ __forceinline__ void gn_run_stats(uint32_t tb, int c_lo, int c_hi, bo
     constexpr int kWin = SUB == 1 ? 32 : (8 * SUB < 128 ? 8 * SUB : 128);
     constexpr int kRuns = kWin / SUB;         // runs per window: a power of two <= 32
     constexpr int kRunsPerChunk = 32 / SUB;   // runs per 32-column TMEM load
-    const float inv_n = n_rows > 0 ? 1.f / float(n_rows * SUB) : 0.f;
+    const float inv_n = n_rows > 0 ? __fdividef(1.f, float(n_rows * SUB)) : 0.f;
 #pragma unroll 1
     for (int w0 = c_lo; w0 < c_hi; w0 += kWin) {  // uniform over the warp
         float s1[kRuns], s2[kRuns];
@@ -243,40 +243,70 @@ __device__ __forceinline__ void gn_run_stats(uint32_t tb, int c_lo, int c_hi, bo
             }
             float v[32];
             tmem_load32(tb + uint32_t(j0), v);
+            // y = v + bias for the whole chunk first, then every run's shift K (independent loads
+            // and shuffles), then the runs' sums in two interleaved chains each, so the runs overlap
+            // instead of waiting on one another
+            float bb[32];
+            lds_vec(bias + j0, bb);
 #pragma unroll
-            for (int r = 0; r < kRunsPerChunk; ++r) {
-                const int slot = c * kRunsPerChunk + r;
-                if constexpr (SUB == 1) {
-                    const float y = v[r] + bias[j0 + r];
-                    const float K = __shfl_sync(0xffffffffu, y, 0);
+            for (int i = 0; i < 32; i += 2) f2_unpack(f2_add(f2_pack(v[i], v[i + 1]), f2_pack(bb[i], bb[i + 1])), v[i], v[i + 1]);
+            if constexpr (SUB == 1) {
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    const int slot = c * kRunsPerChunk + r;
+                    const float K = __shfl_sync(0xffffffffu, v[r], 0);
                     if (lane == slot) k_mine = K;
-                    const float d = row_ok ? y - K : 0.f;
+                    const float d = row_ok ? v[r] - K : 0.f;
                     s1[slot] = d;
                     s2[slot] = d * d;
-                } else {
-                    float b[SUB];
-                    lds_vec(bias + j0 + r * SUB, b);
-                    const float K = __shfl_sync(0xffffffffu, v[r * SUB] + b[0], 0);
-                    if ((lane & (kRuns - 1)) == slot) k_mine = K;
-                    const uint64_t kk = f2_pack(K, K);
-                    uint64_t p1 = 0ull, p2 = 0ull;
+                }
+            } else {
+                float K[kRunsPerChunk];
 #pragma unroll
-                    for (int i = 0; i < SUB; i += 2) {
-                        const uint64_t d = f2_sub(f2_add(f2_pack(v[r * SUB + i], v[r * SUB + i + 1]), f2_pack(b[i], b[i + 1])), kk);
-                        p1 = f2_add(p1, d);
-                        p2 = f2_fma(d, d, p2);
+                for (int r = 0; r < kRunsPerChunk; ++r) K[r] = __shfl_sync(0xffffffffu, v[r * SUB], 0);
+#pragma unroll
+                for (int r = 0; r < kRunsPerChunk; ++r) {
+                    const int slot = c * kRunsPerChunk + r;
+                    if ((lane & (kRuns - 1)) == slot) k_mine = K[r];
+                    const uint64_t kk = f2_pack(K[r], K[r]);
+                    uint64_t p1a = 0ull, p1b = 0ull, p2a = 0ull, p2b = 0ull;
+#pragma unroll
+                    for (int i = 0; i < SUB; i += 4) {
+                        const uint64_t da = f2_sub(f2_pack(v[r * SUB + i], v[r * SUB + i + 1]), kk);
+                        const uint64_t db = f2_sub(f2_pack(v[r * SUB + i + 2], v[r * SUB + i + 3]), kk);
+                        p1a = f2_add(p1a, da);
+                        p1b = f2_add(p1b, db);
+                        p2a = f2_fma(da, da, p2a);
+                        p2b = f2_fma(db, db, p2b);
                     }
-                    s1[slot] = row_ok ? f2_hsum(p1) : 0.f;
-                    s2[slot] = row_ok ? f2_hsum(p2) : 0.f;
+                    s1[slot] = row_ok ? f2_hsum(f2_add(p1a, p1b)) : 0.f;
+                    s2[slot] = row_ok ? f2_hsum(f2_add(p2a, p2b)) : 0.f;
                 }
             }
         }
-        warp_sum_scatter<kRuns>(s1, lane);
-        warp_sum_scatter<kRuns>(s2, lane);
+        float t1, t2;
+        if constexpr (kRuns <= 16) {
+            // one reduce-scatter over both sums: lane l ends with slot l mod 2kRuns, the sum of d for
+            // lanes below kRuns, of d^2 for the next kRuns lanes
+            float sv[2 * kRuns];
+#pragma unroll
+            for (int i = 0; i < kRuns; ++i) {
+                sv[i] = s1[i];
+                sv[kRuns + i] = s2[i];
+            }
+            warp_sum_scatter<2 * kRuns>(sv, lane);
+            t1 = sv[0];
+            t2 = __shfl_sync(0xffffffffu, sv[0], (lane + kRuns) & 31);
+        } else {
+            warp_sum_scatter<kRuns>(s1, lane);
+            warp_sum_scatter<kRuns>(s2, lane);
+            t1 = s1[0];
+            t2 = s2[0];
+        }
         if (lane < kRuns && w0 + lane * SUB < c_hi) {
-            const float m = s1[0] * inv_n;
+            const float m = t1 * inv_n;
             red_mean[q * 256 + w0 / SUB + lane] = k_mine + m;
-            red_m2[q * 256 + w0 / SUB + lane] = fmaxf(s2[0] - s1[0] * m, 0.f);
+            red_m2[q * 256 + w0 / SUB + lane] = fmaxf(t2 - t1 * m, 0.f);
         }
     }
 }
@@ -286,7 +316,7 @@ __device__ __forceinline__ void gn_run_stats(uint32_t tb, int c_lo, int c_hi, bo
 __device__ __forceinline__ void stats_merge(float& n, float& mu, float& m2, float nb, float mub, float m2b) {
     const float nt = n + nb;
     if (nt <= 0.f) return;
-    const float f = nb / nt;
+    const float f = __fdividef(nb, nt);  // (counts are exact integers; 2-ulp quotient is plenty)
     const float d = mub - mu;
     mu = fmaf(d, f, mu);
     m2 = m2 + m2b + d * d * (n * f);
@@ -474,13 +504,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // exchange per-row LayerNorm partial sums through distributed shared memory.
     constexpr bool kClusterX = EPI == kEpiLNX;
     static_assert(!(PAIR && (kFusedGN || kClusterX)), "the exchanging epilogues run one CTA per tile");
-    // Epilogue warps: 4 (one per TMEM lane quarter), or 8 (two per quarter, each taking a column
-    // range) for the bf16 LayerNorm epilogues and the fused GroupNorm. The bf16 transposer leaves
-    // warps 6-9 free for them; a fused-GroupNorm CTA has one tile, so with fp32 data warps 6-9 first
-    // transpose x and then, the mainloop's operands all staged, join the epilogue.
-    constexpr int kEpiW = ((BF16 && (EPI == kEpiLN || EPI == kEpiLNX)) || kFusedGN) ? 8 : 4;
+    // Epilogue warps: 4 (one per TMEM lane quarter), 8 (two per quarter, each taking a column range)
+    // for the bf16 LayerNorm epilogues, whose transposer leaves warps 6-9 free, or 12 (warps 2-13,
+    // three per quarter) for the fused GroupNorm: a fused-GroupNorm CTA has one tile, so its x
+    // transposer warps first stage x and then, the mainloop's operands all staged, join the epilogue.
+    constexpr int kEpiW = kFusedGN ? 12 : ((BF16 && (EPI == kEpiLN || EPI == kEpiLNX)) ? 8 : 4);
     constexpr int kEpiT = 32 * kEpiW;
-    constexpr bool kShareXp = kFusedGN && !BF16;
+    constexpr bool kShareXp = kFusedGN;
     static_assert(kShareXp || kWarpEpi0 + kEpiW <= xp_first<BF16>(), "epilogue and transposer warps overlap");
     using InT = typename std::conditional<BF16, __nv_bfloat16, float>::type;
     extern __shared__ uint8_t dyn_smem[];
@@ -545,17 +575,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         else mbar_arrive(bar(i));
     };
 
-    if (!LINEAR && threadIdx.x == 0) {
-        // The x boxes of this CTA's first unit head for L2 now; the loads that stage them come
-        // later. (A prefetch only fills L2, which every write reaches too, so it may run ahead of
-        // the kernels this one depends on.)
-        const int u0 = kFusedGN ? (blockIdx.z * a.n_t_tiles + blockIdx.x) * (a.n_cb / a.cb_per_unit) + blockIdx.y
-                                : ((PAIR || kClusterX) ? int(blockIdx.x >> 1) : int(blockIdx.x));
-        if (u0 < a.n_units) {
-            const Unit un0 = decode(u0);
-            for (int c = 0; c < a.n_ci_chunks; ++c)
-                tma_prefetch_3d(&tm_a, un0.row0 - a.pad_left - a.t_shift, c * a.BK, un0.n);
+    // This CTA's first unit, and how many of its x boxes are staged at entry: when the preceding
+    // launch is this library's weight pack (which does not write x), thread 0 arms the first x
+    // staging barriers itself and issues those boxes before the CTA's setup; the other boxes of
+    // the unit head for L2. (A prefetch only fills L2, which every write reaches too, so it may run
+    // ahead of the kernels this one depends on.)
+    const int u0 = kFusedGN ? (blockIdx.z * a.n_t_tiles + blockIdx.x) * (a.n_cb / a.cb_per_unit) + blockIdx.y
+                            : ((PAIR || kClusterX) ? int(blockIdx.x >> 1) : int(blockIdx.x));
+    const int x_early = (!LINEAR && a.early_inputs && u0 < a.n_units) ? min(SS, a.n_ci_chunks) : 0;
+    if (!LINEAR && threadIdx.x == 0 && u0 < a.n_units) {
+        const Unit un0 = decode(u0);
+        const int t0 = un0.row0 - a.pad_left - a.t_shift;
+        const uint32_t box_bytes = uint32_t(a.RS * a.BK * (BF16 ? 2 : 4));
+        for (int c = 0; c < x_early; ++c) mbar_init(bar(i_sfull + c), 1);
+        if (x_early > 0) fence_mbar_init();
+        for (int c = 0; c < x_early; ++c) {
+            mbar_arrive_expect_tx(bar(i_sfull + c), box_bytes);
+            tma_load_3d(sS + c * a.s_slot_bytes, &tm_a, bar(i_sfull + c), t0, c * a.BK, un0.n);
         }
+        for (int c = x_early; c < a.n_ci_chunks; ++c) tma_prefetch_3d(&tm_a, t0, c * a.BK, un0.n);
     }
     if (warp == kWarpTma) {
         // barriers initialised by the 32 lanes together; arrival counts: A full: the TMA (Linear) or
@@ -563,6 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (of the pair); x staging empty: one per transposer warp; exchange: one per step, from the
         // peer's first 4 epilogue warps; all others: one.
         for (int i = lane; i < n_bars; i += 32) {
+            if (i >= i_sfull && i < i_sfull + x_early) continue;  // armed by thread 0 at entry
             uint32_t cnt = 1;
             if (i < i_aempty) cnt = LINEAR ? 1u : (PAIR ? 2u : 1u) * uint32_t(xp_warps<BF16>());
             else if (i >= i_accempty && i < i_drain) cnt = (PAIR ? 2u : 1u) * uint32_t(kEpiW);
@@ -634,18 +673,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tx_stage = tx_mult * uint32_t(a.b_slot_bytes + (LINEAR ? a.a_slot_bytes : 0));
         const int co_half = PAIR ? int(rank) * (a.BN / 2) : 0;
         const int nparts = (!LINEAR && !BF16 && a.x3) ? 2 : 1;
-        // When x may be read early, this warp (running already) stages the first x boxes of its
-        // first unit before it waits for the weight pack; the x loader goes on from the next box.
-        const int x_early = (!LINEAR && a.early_inputs && first_unit < a.n_units) ? min(SS, a.n_ci_chunks) : 0;
-        if (x_early > 0 && lane == 0) {
-            const Unit un0 = decode(first_unit);
-            const uint32_t box_bytes = uint32_t(a.RS * a.BK * (BF16 ? 2 : 4));
-            for (int c = 0; c < x_early; ++c) {
-                mbar_arrive_expect_tx(bar(i_sfull + c), box_bytes);
-                tma_load_3d(sS + c * a.s_slot_bytes, &tm_a, bar(i_sfull + c), un0.row0 - a.pad_left - a.t_shift,
-                            c * a.BK, un0.n);
-            }
-        }
         __syncwarp();
         griddep_wait();
         for (int u = first_unit; u < a.n_units && !aborting(); u += unit_step) {
@@ -795,8 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // convolution's zero padding.
         if (!LINEAR && lane == 0) {
             const uint32_t box_bytes = uint32_t(a.RS * a.BK * (BF16 ? 2 : 4));
-            // the first x_early boxes of the first unit were staged by the TMA producer warp
-            const int x_early = (a.early_inputs && first_unit < a.n_units) ? min(SS, a.n_ci_chunks) : 0;
+            // the first x_early boxes of the first unit were issued by thread 0 at entry
             int si = x_early == SS ? 0 : x_early;
             uint32_t sph = x_early == SS ? 1u : 0u;
             long long s_cnt = x_early;
@@ -916,18 +942,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int q = warp & 3;       // TMEM lane quarter this warp may access
             const int m = q * 32 + lane;  // tile row: time step (conv) or sample row (Linear)
             const int er = threadIdx.x - kWarpEpi0 * 32;  // index among the epilogue threads
-            const int eg = (warp - kWarpEpi0) >> 2;       // column range (two warps per quarter)
+            const int eg = (warp - kWarpEpi0) >> 2;       // column range (kEpiW / 4 warps per quarter)
             bool mid_sync_done = false;
             // Per-channel parameters of the current channel block, staged once in shared memory so the
             // element loops below read them with conflict-free broadcast loads instead of global loads.
             float* s_bias = epi + 3072;  // [256]
             int staged_co = -1;
             int obuf = 0;  // LayerNorm output staging: which of this warp's two tiles is next
+            // Grid exchange of the fused GroupNorm: this launch's epoch is one past the one in this
+            // CTA's own first word (all words of a (sample, channel block) carry the same epoch after
+            // every launch), read here, while the mainloop runs, rather than on the epilogue's path.
+            unsigned gx_target = 0;
             if (kFusedGN && first_unit < a.n_units) {
                 // One unit per CTA: stage bias, gamma and beta of its channel block while the
                 // mainloop runs (gamma and beta go where the column scale / shift end up). (Warps that
                 // were x transposers have not waited for the preceding kernel yet.)
                 griddep_wait();
+                if (EPI == kEpiGridGN) {
+                    const Unit un0 = decode(first_unit);
+                    const size_t w0i = (size_t(un0.n * a.n_cb + un0.cbu) * a.n_t_tiles + un0.row0 / 128) * size_t(a.gstride) * 2;
+                    gx_target = unsigned(ld_relaxed_gpu_u64(a.gx + w0i) >> 32) + 1u;
+                }
                 const int co_base = decode(first_unit).cbu * a.BN;
                 const int ncols = min(a.BN, a.C_out - co_base);
                 for (int col = er; col < 256; col += kEpiT) {
@@ -1265,20 +1300,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int nvalid_t = min(128, a.T_out - un.row0);
                     const int tt = un.row0 / 128;
                     const int P = a.n_t_tiles;  // tiles (CTAs) whose statistics make up one group
-                    // this warp's column range [c_lo, c_hi): the two warps of a lane quarter take one
-                    // half each (whole 32-column chunks but the last)
-                    const int half = ((ncols + 63) / 64) * 32;
-                    const int c_lo = eg == 0 ? 0 : min(half, ncols);
-                    const int c_hi = eg == 0 ? min(half, ncols) : ncols;
+                    // this warp's column range [c_lo, c_hi): the kEpiW / 4 warps of a lane quarter take
+                    // one part each (whole 32-column chunks but the last)
+                    constexpr int kParts = kEpiW / 4;
+                    const int part = ((ncols + kParts - 1) / kParts + 31) / 32 * 32;
+                    const int c_lo = min(eg * part, ncols);
+                    const int c_hi = min(c_lo + part, ncols);
                     // grid exchange: per (sample, channel block, time tile, group) two 64-bit words,
-                    // (mean | epoch) and (M2 | epoch). All words of a (sample, channel block) carry the
-                    // same epoch, one step per launch (the weight pack zeroes them), so this launch's
-                    // epoch is one past the one in this CTA's own word, read now so the load overlaps
-                    // the statistics sweep.
+                    // (mean | epoch) and (M2 | epoch), one epoch step per launch (the weight pack
+                    // zeroes them); this launch's epoch was read before the accumulator wait
                     const size_t slot0 = size_t(un.n * a.n_cb + un.cbu) * a.n_t_tiles;
                     unsigned long long* gx_me = a.gx + (slot0 + tt) * size_t(a.gstride) * 2;
-                    unsigned target = 0;
-                    if (EPI == kEpiGridGN) target = unsigned(ld_relaxed_gpu_u64(gx_me) >> 32) + 1u;
+                    const unsigned target = gx_target;
                     float* red_mean = epi;         // [4][256] per lane quarter and run: mean of y over the run
                     float* red_m2 = epi + 1024;    // [4][256] ... and its M2
                     float* part_mu = epi + 2048;   // [256] this CTA's group means (cluster); peers' means (grid)
@@ -1309,7 +1342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 s = fmaf(qn[q2], red_mean[q2 * 256 + j], s);  // (qn = 0: the entry is finite)
                             }
                         }
-                        const float gmu = n_tot > 0.f ? s / n_tot : 0.f;
+                        const float gmu = n_tot > 0.f ? __fdividef(s, n_tot) : 0.f;
                         float gm2 = 0.f;
                         for (int j = j_lo; j < j_hi; ++j) {
 #pragma unroll
@@ -1391,7 +1424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 for (int d = 1; d < P; d <<= 1) stats_merge_xor(n, mu, m2, d, lane);
                                 if (g < ngroups && p == 0) {
                                     gmean[g] = mu;
-                                    grstd[g] = rsqrtf(m2 / n + a.eps);
+                                    grstd[g] = rsqrtf(__fdividef(m2, n) + a.eps);
                                 }
                             } else if (in_smem && g < ngroups) {
                                 part_mu[idx] = __uint_as_float(unsigned(wmu));
