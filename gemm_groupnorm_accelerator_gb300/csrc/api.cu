@@ -114,8 +114,11 @@ void plan_channel_blocks(const c1n_params& p, Plan& pl) {
     pl.b_slot_bytes = pl.BN * 128;
 }
 
-// Ring depths from the shared-memory budget (one CTA per SM), after the output staging area.
-// The weight and x-staging rings give way first, down to three slots, then to two.
+// Ring depths from the shared-memory budget (one CTA per SM), after the output staging area. The
+// x-staging ring gives way first (down to two slots: its boxes are small and prefetched to L2),
+// then the weight ring (whose 16-32 KB stages come from L2 with ~1 us of latency and feed every
+// MMA), then the A ring. (bf16 LayerNorm, 5 taps: 3 weight stages instead of 2 took a short burst
+// of calls from 266 to 250 us each; under seconds of load the power cap holds both near 267 us.)
 void plan_stages(Plan& pl, int max_a, int max_b, int max_s) {
     const int budget = 227 * 1024 - 1024 - kTcMiscBytes;
     pl.stages_a = max_a;
@@ -125,21 +128,22 @@ void plan_stages(Plan& pl, int max_a, int max_b, int max_s) {
         return pl.stages_a * pl.a_slot_bytes + pl.stages_b * pl.b_slot_bytes + pl.stages_s * pl.s_slot_bytes +
                pl.o_bytes;
     };
-    while (total() > budget && pl.stages_b > 3) --pl.stages_b;
-    while (total() > budget && pl.stages_s > 3) --pl.stages_s;
-    while (total() > budget && pl.stages_b > 2) --pl.stages_b;
     while (total() > budget && pl.stages_s > 2) --pl.stages_s;
+    while (total() > budget && pl.stages_b > 2) --pl.stages_b;
     while (total() > budget && pl.stages_a > 2) --pl.stages_a;
     pl.smem_bytes = 1024 + total() + kTcMiscBytes;
 }
 
-// CTA pairs (cta_group::2) need an MMA N that splits into two halves of whole 16-row groups. AUTO
-// uses them for the Linear GEMM (measured 0.88 vs 0.70 of tensor peak on 1024x8192x8192) but not
-// for the convolution, whose A tiles are rebuilt by each CTA's transposer warps and where one CTA
-// per tile measured faster (causal 32x256x8192 k4: 0.185 vs 0.204 ms).
+// CTA pairs (cta_group::2) need an MMA N that splits into two halves of whole 16-row groups. Each
+// CTA of a pair streams half of the weight tile through its shared memory. AUTO uses them for the
+// Linear GEMM (0.88 vs 0.70 of tensor peak on 1024x8192x8192) and for convolutions with at least
+// two 256-row units per pair of SMs (causal 32x256x8192 k4: 200 vs 209 us with four A slots per
+// CTA); smaller convolutions keep one CTA per 128-row tile (more tiles to spread over the SMs).
 bool pair_ok(const c1n_params& p, const Plan& pl, bool linear) {
     if (pl.BN % 32 != 0 || p.mainloop == C1N_MAINLOOP_SINGLE || pl.x3) return false;
-    return linear || p.mainloop == C1N_MAINLOOP_PAIR;
+    if (linear || p.mainloop == C1N_MAINLOOP_PAIR) return true;
+    const long long pair_units = (long long)p.N * ceil_div(pl.T_out, 256) * pl.n_cb;
+    return pair_units >= kMinSmCount;
 }
 
 // Geometry of the tensor-core conv tiles: 128 output time steps x BN channels per tile (256 steps
@@ -180,7 +184,7 @@ bool plan_tc_geometry(const c1n_params& p, Plan& pl, bool cluster, bool pair = f
         pl.n_acc = 2;
         pl.tmem_cols = 512;
     }
-    if (pl.pair) plan_stages(pl, 2, 8, 3);  // half-size B slots: a deeper weight ring
+    if (pl.pair) plan_stages(pl, 4, 8, 2);  // half-size B slots: a deeper weight ring; A slots for 4 chunks
     else if (cluster) plan_stages(pl, std::max(2, std::min(pl.n_ci_chunks, 4)), 4, 2);  // one tile per CTA: A
                                                                                         // slots for up to 4
                                                                                         // chunks, so x staging

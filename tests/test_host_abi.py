@@ -70,11 +70,22 @@ def test_conv_gn_cluster_geometry():
 @pytest.mark.parametrize("wl", [synth.CAUSAL_CONV, synth.LINEAR_GN_ROWMIN, synth.CONV_LN_GELU_BF16],
                          ids=lambda w: w.name)
 def test_cta_pair_mainloop(wl):
-    # CTA pairs: 256-row tiles, each CTA stages half of the B tile; AUTO pairs the Linear GEMM only
-    linear = wl is synth.LINEAR_GN_ROWMIN
+    # CTA pairs: 256-row tiles, each CTA stages half of the B tile. AUTO pairs the Linear GEMM and
+    # convolutions with at least 152 units of 256 rows; the 512-channel LayerNorm plan exchanges
+    # statistics between single CTAs and does not pair.
+    paired = wl is not synth.CONV_LN_GELU_BF16
     d = c1n.conv1d_norm_desc_create(_params(wl))
     info = c1n.conv1d_norm_plan_info(d)
-    assert (info.cta_pair, info.tile_t) == ((1, 256) if linear else (0, 128))
+    assert (info.cta_pair, info.tile_t) == ((1, 256) if paired else (0, 128))
+    c1n.conv1d_norm_destroy(d)
+    # a small convolution keeps one CTA per 128-row tile under AUTO; SINGLE and PAIR force either
+    small = synth.CAUSAL_CONV.replace(N=2, T=1024)
+    for mainloop, want in ((c1n.MAINLOOP_AUTO, 0), (c1n.MAINLOOP_SINGLE, 0), (c1n.MAINLOOP_PAIR, 1)):
+        d = c1n.conv1d_norm_desc_create(_params(small, mainloop=mainloop))
+        assert c1n.conv1d_norm_plan_info(d).cta_pair == want
+        c1n.conv1d_norm_destroy(d)
+    d = c1n.conv1d_norm_desc_create(_params(synth.CAUSAL_CONV, mainloop=c1n.MAINLOOP_SINGLE))
+    assert c1n.conv1d_norm_plan_info(d).cta_pair == 0
     c1n.conv1d_norm_destroy(d)
     # (the 512-channel LayerNorm cluster plan exchanges statistics between single CTAs: pairs need
     # the two-pass plan there)

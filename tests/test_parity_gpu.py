@@ -365,15 +365,15 @@ def test_conv_gn_full(cuda_lib):
 def test_causal_conv_full_sampled(cuda_lib):
     wl = synth.CAUSAL_CONV
     inp = _inputs(wl)
-    y, _, path = run_gpu(cuda_lib, wl, inp)
+    y, _, path = run_gpu(cuda_lib, wl, inp)  # AUTO: CTA pairs at this size
     assert path == "tc_direct"
-    y1, _, _ = run_gpu(cuda_lib, wl, inp, mainloop=cuda_lib.MAINLOOP_PAIR)
+    y1, _, _ = run_gpu(cuda_lib, wl, inp, mainloop=cuda_lib.MAINLOOP_SINGLE)
     # 8 samples spread over the batch: the persistent CTAs (one per SM) walk 2048 tiles, so these
     # samples' tiles fall in the first, middle and last work units of the schedule
     ns = [0, 4, 9, 13, 18, 22, 27, wl.N - 1]
     ref, _ = oracle.conv1d_norm_samples(oracle.params_of(wl), ns, inp["x"], inp["w"], inp["b"])
     compare(wl, y[ns], None, ref, None, path, wl.name)
-    compare(wl, y1[ns], None, ref, None, path, wl.name + " (CTA-pair mainloop)")
+    compare(wl, y1[ns], None, ref, None, path, wl.name + " (one CTA per tile)")
     assert np.all(np.isfinite(y)) and np.all(np.isfinite(y1))
 
 
