@@ -198,8 +198,8 @@ NORMALIZE_PASS_WORKLOADS = ("causal_conv_gn32", "conv_ln_gelu_bf16")
 class ConvRun:
     """One operator configuration through the C ABI on device-resident inputs: the descriptor, its
     rank's inputs, rotating x / y buffer sets (more than 2x L2 of them unless one set already
-    exceeds L2) and one CUDA graph per set holding one whole step (weight pack + every kernel of
-    the operator, as the library enqueues them)."""
+    exceeds L2) and CUDA graphs of whole steps (every kernel of the operator, as the library
+    enqueues them): one per set, and for the timed blocks one graph of a block's K steps."""
 
     def __init__(self, c1n, wl, args, dev, rank, math_mode=None, path=None, mainloop=None):
         import torch
@@ -236,6 +236,7 @@ class ConvRun:
                    if wl.post == synth.POST_ROWMIN_BIAS else None)
         self.stream = torch.cuda.current_stream(dev)
         self.graphs = None
+        self.block_graphs = {}
         # kernels of one step, and of one call with the weights already packed
         self.kernels = op.info.kernels
         self.kernels_packed = self.kernels - (1 if self.path not in ("simt", "tc_linear") else 0)
@@ -267,34 +268,62 @@ class ConvRun:
 
     @property
     def launch_mode(self):
-        return "cuda graph replay, one graph per step" if self.graphs else "eager"
+        return ("one CUDA graph per timed block, holding its K steps (each step one operator call, x / y "
+                "rotating over the buffer sets)" if self.graphs else "eager")
+
+    def run_block(self, steps, i0):
+        """Steps i0 .. i0 + steps - 1: one replay of a graph of those K steps (captured once per K
+        and starting buffer set), or the eager loop."""
+        if not self.graphs:
+            for k in range(steps):
+                self.step(i0 + k)
+            return
+        key = (steps, i0 % self.n_sets)
+        if key not in self.block_graphs:
+            g = capture_graphs(lambda j: [self.step(i0 + k) for k in range(steps)], 1, self.dev)
+            self.block_graphs[key] = g[0] if g else None
+        g = self.block_graphs[key]
+        if g is None:
+            for k in range(steps):
+                self.run_step(i0 + k)
+        else:
+            g.replay()
 
     def timed_blocks(self, steps, min_seconds, barrier, pg=None, i0=0):
         """Time back-to-back blocks of exactly `steps` steps, each bracketed by a barrier and a device
         synchronize on both sides and timed with CUDA events on the launching stream, until the blocks
-        cover at least `min_seconds` (3 blocks at least). Returns (ms per step of each block, max over
-        ranks)."""
+        cover at least `min_seconds` (3 blocks at least). Every block runs steps i0 .. i0 + K - 1 (one
+        replay of the same block graph; consecutive steps use different buffer sets, and so do the
+        last step of a block and the first of the next when there are several sets). Returns (ms
+        per step of each block, max over ranks)."""
         torch = self.torch
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if self.n_sets > 1 and (steps - 1) % self.n_sets == 0:
+            i0_next = 1  # (K - 1) a multiple of the set count: shift alternate blocks by one set
+        else:
+            i0_next = 0
+        starts = [i0, i0 + i0_next]
+        for i in starts:  # capture and warm the block graphs before timing
+            self.run_block(steps, i)
+        torch.cuda.synchronize()
 
         def block(i):
             barrier()
             torch.cuda.synchronize()
             e0.record(self.stream)
-            for k in range(steps):
-                self.run_step(i + k)
+            self.run_block(steps, i)
             e1.record(self.stream)
             torch.cuda.synchronize()
             barrier()
             return e0.elapsed_time(e1) / steps
 
-        first = block(i0)
+        first = block(starts[0])
         n_blocks = max(3, math.ceil(min_seconds * 1e3 / max(first * steps, 1e-3)))
         if pg is not None:  # every rank runs the same number of blocks
             t = torch.tensor([n_blocks], device=self.dev)
             pg.all_reduce(t, op=pg.ReduceOp.MAX)
             n_blocks = int(t[0])
-        ms = [block(i0 + (r + 1) * steps) for r in range(n_blocks)]
+        ms = [block(starts[(r + 1) % 2]) for r in range(n_blocks)]
         if pg is not None:
             t = torch.tensor(ms, device=self.dev)
             pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -306,10 +335,13 @@ class ConvRun:
         """Mean device time of one operator call with the weights already packed, from one CUDA
         graph of `launches` calls back to back (inputs rotating over the buffer sets), timed with
         CUDA events around `reps` replays. With one kernel per call this is that kernel's average
-        launch duration. None when the graph cannot be captured."""
+        launch duration. None when the graph cannot be captured. (A plan without a separate weight
+        pack is timed as it runs in a step.)"""
         torch = self.torch
-        self.op.pack_weights(self.w)
-        g = capture_graphs(lambda j: [self.packed_call(i) for i in range(launches)], 1, self.dev)
+        call = self.step if self.kernels_packed == self.kernels else self.packed_call
+        if call is self.packed_call:
+            self.op.pack_weights(self.w)
+        g = capture_graphs(lambda j: [call(i) for i in range(launches)], 1, self.dev)
         if not g:
             return None
         for _ in range(2):
@@ -350,7 +382,9 @@ def conv_roofline(wl, run, peaks, kern, b2b_ms):
     conv_name = "simt_conv" if path == "simt" else "tc_conv"
     if b2b_ms is not None and run.kernels_packed == 1:
         conv_ms = b2b_ms
-        timing = "back to back: one CUDA graph of 20 launches of the kernel (weights packed once), events around the replays"
+        timing = ("back to back: one CUDA graph of 20 launches of the kernel"
+                  + ("" if run.kernels_packed == run.kernels else " (weights packed once)")
+                  + ", events around the replays")
     elif b2b_ms is not None and conv_name == "tc_conv" and path == "tc_linear":
         conv_ms = b2b_ms  # conservative: includes the small finisher kernel that follows it
         timing = ("back to back: graph of 20 operator calls (this kernel + the row-min finisher), events around the "
@@ -358,7 +392,12 @@ def conv_roofline(wl, run, peaks, kern, b2b_ms):
     else:
         conv_ms = kern.get(conv_name, b2b_ms)
         timing = "event pair around the kernel inside a replayed graph (includes the pair's own overhead: an upper bound)"
-    tc_peak = peaks["bf16_tflops"] * (1.0 if run.bf else TF32_PER_BF16)
+    # The kernel is timed after seconds of back-to-back calls (the timed blocks come first), where
+    # the power cap sets the clock: the tensor peak is the sustained cuBLAS figure, the burst one
+    # is reported beside it.
+    ratio = 1.0 if run.bf else TF32_PER_BF16
+    tc_peak = peaks["bf16_tflops_sustained"] * ratio
+    tc_burst = peaks["bf16_tflops"] * ratio
     t_flop = flops / (tc_peak * 1e12)
     t_byte = nbytes / (peaks["hbm_gbs"] * 1e9)
     if path == "simt":
@@ -371,9 +410,13 @@ def conv_roofline(wl, run, peaks, kern, b2b_ms):
                 "frac": ach / peaks["hbm_gbs"]}
     else:
         ach = flops / (conv_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s", "frac": ach / tc_peak}
+        roof = {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s", "frac": ach / tc_peak,
+                "frac_of_burst_peak": ach / tc_burst}
     roof.update({"traffic": read_traffic(wl.name, path),
                  "peak_source": peaks["source"] + ("" if run.bf else " (bf16 x 1.1/2.25 for tf32)"),
+                 "peak_kind": ("copy bandwidth" if roof["bound"] == "hbm" else
+                               "sustained (the kernel is timed after seconds of back-to-back calls)"
+                               if roof["bound"] == "tensor" else "derived"),
                  "kernel": f"tc_conv_kernel ({path})" if path != "simt" else "simt_conv_kernel",
                  "kernel_ms": conv_ms, "kernel_timing": timing, "kernels_ms_event_pairs": kern,
                  "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
@@ -399,23 +442,31 @@ def measure_workload(c1n, wl, args, dev, rank, peaks, steps, min_seconds, barrie
     """One workload measured the way the headline is (without e2e and oracle legs): returns a dict
     for the line's `workloads` object."""
     run = ConvRun(c1n, wl, args, dev, rank, path=path)
+    sampler = None
     try:
         run.prepare(args.warmup, eager=args.eager)
+        sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+        if sampler:
+            sampler.start()
         ms_blocks = run.timed_blocks(steps, min_seconds, barrier, pg)
         ms = statistics.median(ms_blocks)
         kern = run.kernel_marks(args.warmup + steps)
         b2b = run.back_to_back_ms()
+        clocks = sampler.stop() if sampler else None
+        sampler = None
         roof = conv_roofline(wl, run, peaks, kern, b2b)
         out = {"workload": wl.name, "gemm_mnk": list(wl.gemm_mnk), "plan": run.path,
                "cta_pair": int(run.op.info.cta_pair), "dtype": dtype_name(wl, run.path, run.math),
                "ms_per_step": ms, "tflops": wl.flops / (ms / 1e3) / 1e12, "blocks": len(ms_blocks),
                "steps_per_block": steps, "kernels_per_step": run.kernels, "roofline": roof,
-               "normalize_pass": normalize_pass_roofline(wl, kern, peaks)}
+               "normalize_pass": normalize_pass_roofline(wl, kern, peaks), "clocks": clocks}
         fin = rowmin_finisher(wl, kern, peaks) if wl.post == synth.POST_ROWMIN_BIAS else None
         if fin:
             out["finisher"] = fin
         return out
     finally:
+        if sampler:
+            sampler.stop()
         run.close()
 
 
@@ -453,8 +504,9 @@ def our_arm(args, wl):
     kern = run.kernel_marks(args.warmup + args.steps)
     b2b = run.back_to_back_ms()
     roof = conv_roofline(wl, run, peaks, kern, b2b)
-    pack_ms = time_replays(lambda i: run.op.pack_weights(run.w), run.n_sets, dev, args.steps, eager=not run.graphs)
-    roof["pack_ms_graph_per_call"] = pack_ms
+    if run.kernels_packed < run.kernels:  # the weight pack is a kernel of its own
+        roof["pack_ms_graph_per_call"] = time_replays(lambda i: run.op.pack_weights(run.w), run.n_sets, dev,
+                                                      args.steps, eager=not run.graphs)
     norm_pass = normalize_pass_roofline(wl, kern, peaks)
 
     e2e = measure_e2e(args, wl, run.op, run.inp, dev, run.tdt, run.bf, run.w, run.b, run.ga, run.be, run.b2, run.am)
@@ -935,7 +987,9 @@ def p4_arm(args, wl):
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms = float(t[0])
     value = wl.flops * world / (ms / 1e3) / 1e12
-    tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
+    # timed after the seconds-long timed region: the sustained tensor peak (burst beside it)
+    tf32_peak = peaks["bf16_tflops_sustained"] * TF32_PER_BF16
+    tf32_burst = peaks["bf16_tflops"] * TF32_PER_BF16
     if fused:
         # The contraction bounds the one-pass model: x (67 MB) in and the pooled output (134 MB) out
         # take ~30 us of HBM, the multiply-adds ~60 us of TF32 tensor time. The time is the whole
@@ -952,8 +1006,9 @@ def p4_arm(args, wl):
         tiles = wl.N * wl.D * ((wl.H + 3) // 4)
         issued = 2.0 * tile_m * rows_per_half * wl.C_in * halves * tiles
         roof = {"bound": "tensor", "achieved": ach, "peak": tf32_peak, "unit": "TFLOP/s", "frac": ach / tf32_peak,
-                "traffic": read_traffic(wl.name, "convt3d_lnpool_fused"),
+                "frac_of_burst_peak": ach / tf32_burst, "traffic": read_traffic(wl.name, "convt3d_lnpool_fused"),
                 "peak_source": peaks.get("source", "MEASURED_PEAKS.json") + " (bf16 x 1.1/2.25 for tf32)",
+                "peak_kind": "sustained (timed after the seconds-long timed region)",
                 "kernel": "convt3d_lnpool_fused_kernel (timed with its channels-last copy and weight pack)",
                 "kernel_ms": model_ms, "algorithmic_flops": wl.flops, "issued_mma_flops": issued,
                 "algorithmic_bytes": fbytes, "hbm_frac": fbytes / (model_ms / 1e3) / 1e9 / peaks["hbm_gbs"],

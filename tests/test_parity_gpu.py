@@ -183,6 +183,52 @@ def test_group_norm_two_pass_forced(cuda_lib, name):
     compare(wl, y, am, ref, None, path, name)
 
 
+@pytest.mark.parametrize("name,math", [("gn_c2_structure", 0), ("gn_bf16", 0), ("gn_cpg16", 3)])
+def test_fused_gn_weights_change_between_calls(cuda_lib, name, math):
+    # Every call packs its weights: a call with new weights must see them, and calls on weights
+    # packed beforehand (C1N_FLAG_WEIGHTS_PACKED) must interleave with packing calls (the grid
+    # exchange's epochs stay in step).
+    wl = SMALL[name]
+    inp = _inputs(wl)
+    inp2 = dict(inp, w=(-0.5 * inp["w"][::-1]).copy())  # other weights, same shapes and scale
+    ref1, _ = oracle_full(wl, inp)
+    ref2, _ = oracle_full(wl, inp2)
+    params = cuda_lib.make_params(wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right,
+                                  wl.dilation, wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, math)
+    op = cuda_lib.Conv1dNorm(params)
+    assert op.path == "tc_fused_gn" and op.info.kernels == 2
+    bf = wl.dtype == synth.DTYPE_BF16
+    x, w1, w2 = _to_dev(inp["x"], bf), _to_dev(inp["w"], bf), _to_dev(inp2["w"], bf)
+    b, ga, be = (_to_dev(inp[k], False) for k in ("b", "gamma", "beta"))
+    tol = 1e-4 if math == 3 else None
+    outs = []
+    for w, packed in ((w1, False), (w2, False), (w1, False), (w2, True), (w2, False)):
+        if packed:
+            op.pack_weights(w1)  # the flag says: use what is packed (w1), not the w passed
+        outs.append(op(x, w, b, ga, be, weights_packed=packed).float().cpu().numpy())
+        op.check()
+    compare(wl, outs[0], None, ref1, None, op.path, name + " (w1)", tol)
+    compare(wl, outs[1], None, ref2, None, op.path, name + " (w2)", tol)
+    np.testing.assert_array_equal(outs[2], outs[0])  # same inputs, same bits
+    np.testing.assert_array_equal(outs[3], outs[0])  # pre-packed w1
+    np.testing.assert_array_equal(outs[4], outs[1])
+    # The same call captured once in a CUDA graph and replayed: new contents of the weight buffer
+    # between replays must be packed and used.
+    wbuf = w1.clone()
+    y = torch.empty_like(op(x, wbuf, b, ga, be))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        op(x, wbuf, b, ga, be, out=y)
+    for w, want in ((w2, outs[1]), (w1, outs[0]), (w2, outs[1])):
+        wbuf.copy_(w)
+        g.replay()
+        torch.cuda.synchronize()
+        op.check()
+        np.testing.assert_array_equal(y.float().cpu().numpy(), want)
+    op.close()
+
+
 GN_NAMES = ["gn_tiny", "gn_c2_structure", "gn_cpg1", "gn_cpg4", "gn_cpg16", "gn_cpg25", "gn_cpg128", "gn_gelu",
             "gn_bf16", "gn_ragged_out"]
 
@@ -260,18 +306,18 @@ def test_layer_norm_fused_forced(cuda_lib, name):
     compare(wl, y, am, ref, None, path, name)
 
 
-@pytest.mark.parametrize("name,kernels", [("gn_tiny", ["pack_weights", "tc_conv"]),
-                                          ("ln_c384_f32", ["pack_weights", "tc_conv", "ln_merge", "normalize"]),
-                                          ("linear_rowmin", ["tc_conv", "rowmin_finish"]),
-                                          ("stride2_simt", ["simt_conv", "gn_stats", "normalize"])])
-def test_kernel_times_list_every_launch(cuda_lib, name, kernels):
+@pytest.mark.parametrize("name,path,kernels", [("gn_tiny", -1, ["pack_weights", "tc_conv"]),  # grid exchange
+                                               ("gn_tiny", 5, ["pack_weights", "tc_conv"]),  # cluster exchange
+                                               ("ln_c384_f32", 3, ["pack_weights", "tc_conv", "ln_merge", "normalize"]),
+                                               ("linear_rowmin", -1, ["tc_conv", "rowmin_finish"]),
+                                               ("stride2_simt", -1, ["simt_conv", "gn_stats", "normalize"])])
+def test_kernel_times_list_every_launch(cuda_lib, name, path, kernels):
     # the profiling hook reports each kernel one run launches, in order, with its device time
     wl = SMALL[name]
     inp = _inputs(wl)
     params = cuda_lib.make_params(wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right,
                                   wl.dilation, wl.norm, wl.groups, wl.eps, wl.post, wl.dtype,
-                                  cuda_lib.MATH_SIMT if name in TC_REFUSED else 0,
-                                  cuda_lib.PATH_TC_TWO_PASS if name == "ln_c384_f32" else -1)
+                                  cuda_lib.MATH_SIMT if name in TC_REFUSED else 0, path)
     op = cuda_lib.Conv1dNorm(params)
     op.set_profiling(True)
     x, w = _to_dev(inp["x"], False), _to_dev(inp["w"], False)
