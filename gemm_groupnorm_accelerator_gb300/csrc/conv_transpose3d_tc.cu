@@ -339,10 +339,15 @@ __global__ void __launch_bounds__(256) pack_convt_weights_kernel(const float* __
 // per channel. Sixteen epilogue warps at under 100 registers each keep four or five warps on every
 // scheduler to hide the latencies. Two accumulators of 256 columns: the epilogue of one tile
 // overlaps the next tile's MMAs. Every wait is bounded.
+//
+// A warp's 32 LayerNorm rows of a tile (4 classes x 8 channels) are handled together: one sweep of
+// its 64 accumulator values per lane gives every row's two sums, a 64-slot reduce-scatter over the
+// warp leaves lane r with row r's totals (no shared-memory transpose, no per-class round trips), the
+// rows' (mean, rstd) go through shared memory to every lane, and a second sweep applies them.
 constexpr int kFThreads = 576;          // warp 0 TMA, warp 1 MMA, warps 2-17 epilogue
 constexpr int kFEpiWarps = 16;
 constexpr int kFStages = 4;            // x ring stages
-constexpr int kFScr = 32 * 20;         // floats of one epilogue warp's transpose scratch [32 lanes][20]
+constexpr int kFStat = 64;             // floats of one epilogue warp's row statistics [32 rows][mean, rstd]
 constexpr int kFRows = 864;            // weight rows of one channel half
 constexpr int kFWBytes = kFRows * 128;
 
@@ -361,17 +366,43 @@ static_assert(fz_row0(8) == kFRows, "weight row count");
 __host__ __device__ constexpr int fz_pd(int pos) { return pos >= 2 ? 1 : 0; }
 __host__ __device__ constexpr int fz_ph(int pos) { return (pos == 1 || pos == 2) ? 1 : 0; }
 
-// Load 8 consecutive 32-bit TMEM columns of this warp's 32 lanes (one lane per thread) and wait.
-__device__ __forceinline__ void tmem_load8(uint32_t taddr, float (&v)[8]) {
-    uint32_t r[8];
+// This warp's eight 8-column segments of one accumulator (for class position pos, width parity 0 at
+// columns tb + pos * 32 and width parity 1 at tb + 128 + pos * 32): eight loads, one wait. v[pos * 8 + c]
+// is parity 0 and v[32 + pos * 8 + c] parity 1 of channel c.
+__device__ __forceinline__ void tmem_load_classes(uint32_t tb, float (&v)[64]) {
+    uint32_t r[64];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%65];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16, %17, %18, %19, %20, %21, %22, %23}, [%66];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24, %25, %26, %27, %28, %29, %30, %31}, [%67];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%32, %33, %34, %35, %36, %37, %38, %39}, [%68];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%40, %41, %42, %43, %44, %45, %46, %47}, [%69];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%48, %49, %50, %51, %52, %53, %54, %55}, [%70];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%56, %57, %58, %59, %60, %61, %62, %63}, [%71];\n\t"
         "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-        : "r"(taddr)
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(tb), "r"(tb + 32u), "r"(tb + 64u), "r"(tb + 96u), "r"(tb + 128u), "r"(tb + 160u), "r"(tb + 192u),
+          "r"(tb + 224u)
         : "memory");
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Reduce-scatter of 64 per-lane slots over the warp by recursive halving: at distance d the lane
+// with bit d set keeps the upper half of its remaining slots and adds its partner's upper half, so
+// lane l ends with the warp totals of slots 2l (in v[0]) and 2l + 1 (in v[1]).
+__device__ __forceinline__ void warp_sum_scatter64(float (&v)[64], int lane) {
+#pragma unroll
+    for (int d = 16, h = 32; d >= 1; d >>= 1, h >>= 1) {
+        const bool upper = (lane & d) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = upper ? v[i] : v[i + h];
+            const float keep = upper ? v[i + h] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+        }
+    }
 }
 
 struct FusedArgs {
@@ -392,13 +423,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const int half = int(blockIdx.x & 1u);
     const int cta_in = int(blockIdx.x >> 1), n_cta = int(gridDim.x >> 1);
     const int tiles = a.N * a.D * a.JT;
-    // shared memory: weights | x ring | per epilogue warp a transpose scratch [32][20] and statistics
-    // [16] | barriers
+    // shared memory: weights | x ring | per epilogue warp its rows' statistics [32][2] | barriers
     const uint32_t sW = smem_u32(base);
     const uint32_t sX = sW + uint32_t(kFWBytes);
-    float* scratch = reinterpret_cast<float*>(base + kFWBytes + kFStages * kTileBytes);
-    float* stat = scratch + kFEpiWarps * kFScr;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(stat + kFEpiWarps * 16);
+    float* stat = reinterpret_cast<float*>(base + kFWBytes + kFStages * kTileBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stat + kFEpiWarps * kFStat);
     const uint32_t bar0 = smem_u32(bars);
     auto bar = [&](int i) { return bar0 + 8u * uint32_t(i); };
     const int i_wfull = 0, i_xfull = 1, i_xempty = 1 + kFStages, i_accfull = 1 + 2 * kFStages,
@@ -525,18 +554,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
         // channels 8g .. 8g + 7 (g = (w - 2) >> 2) of all four classes, so it holds every value its
         // pooled outputs need. The bias and the scalar add are constant along a LayerNorm row (one
         // channel, all ow), so they cancel in v - mean(v): rows are normalized straight from the
-        // accumulators. Row moments (sum of v and of v^2 over the 64 values) in one sweep.
+        // accumulators. Row r = pos * 8 + c of the warp is (class pos, channel 8g + c).
         const int q = warp & 3, g = (warp - 2) >> 2, ew = warp - 2;
-        float* scr = scratch + ew * kFScr;  // [32 lanes][20]: 8 sums, 8 sums of squares, padding
-        float* st = stat + ew * 16;         // [8 means][8 rstd]
+        float* st = stat + ew * kFStat;  // [row][mean, rstd]
         // LayerNorm affine of this lane's two output columns ow = 2 lane, 2 lane + 1
         const float g0 = a.gamma ? __ldg(a.gamma + 2 * lane) : 1.f, g1 = a.gamma ? __ldg(a.gamma + 2 * lane + 1) : 1.f;
         const float gs = g0 + g1;
         // the four classes' affine shifts, averaged with the pool's 1/8
         const float shift8 = 0.5f * (a.beta ? __ldg(a.beta + 2 * lane) + __ldg(a.beta + 2 * lane + 1) : 0.f);
-        // column reads of the transpose: lane (col = lane & 15, rows 16 (lane >> 4) + ...), the upper
-        // half rotated by 4 rows so the two halves fall on different banks
-        const int rcol = lane & 15, rhi = lane >> 4;
         int lt_ = 0;
         for (int t = cta_in; t < tiles; t += n_cta, ++lt_) {
             const int ab = lt_ & 1;
@@ -548,56 +573,41 @@ __global__ void __launch_bounds__(kFThreads, 1)
             tc_fence_after();
             const int jt = t % a.JT, i = (t / a.JT) % a.D, n = t / (a.JT * a.D);
             const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab + 8 * g);
+            {
+                // each row's sum of v and of v^2 over its 64 values (two per lane), slots 2r and 2r + 1
+                float sv[64];
+                {
+                    float v[64];
+                    tmem_load_classes(tb, v);
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) {
+                        sv[2 * r] = v[r] + v[32 + r];
+                        sv[2 * r + 1] = fmaf(v[r], v[r], v[32 + r] * v[32 + r]);
+                    }
+                }
+                warp_sum_scatter64(sv, lane);
+                const float mean = sv[0] * (1.f / 64.f);
+                const float rstd = rsqrtf(fmaxf(fmaf(sv[1], 1.f / 64.f, -mean * mean), 0.f) + a.eps);
+                *reinterpret_cast<float2*>(st + 2 * lane) = make_float2(mean, rstd);
+            }
+            __syncwarp();
+            float v[64];
+            tmem_load_classes(tb, v);
+            // every column this warp needs from the accumulator is in registers
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(i_accempty + ab));
             float pool[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) pool[c] = 0.f;
 #pragma unroll
-            for (int pos = 0; pos < 4; ++pos) {
-                float v0[8], v1[8];
-                tmem_load8(tb + uint32_t(pos * 32), v0);        // width parity 0, channels 8g ..
-                tmem_load8(tb + uint32_t(128 + pos * 32), v1);  // width parity 1
-                if (pos == 3) {
-                    // every column this warp needs from the accumulator is in registers
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(i_accempty + ab));
-                }
-                float s1[8], s2[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    s1[c] = v0[c] + v1[c];
-                    s2[c] = fmaf(v0[c], v0[c], v1[c] * v1[c]);
-                }
-                *reinterpret_cast<float4*>(scr + lane * 20) = make_float4(s1[0], s1[1], s1[2], s1[3]);
-                *reinterpret_cast<float4*>(scr + lane * 20 + 4) = make_float4(s1[4], s1[5], s1[6], s1[7]);
-                *reinterpret_cast<float4*>(scr + lane * 20 + 8) = make_float4(s2[0], s2[1], s2[2], s2[3]);
-                *reinterpret_cast<float4*>(scr + lane * 20 + 12) = make_float4(s2[4], s2[5], s2[6], s2[7]);
-                __syncwarp();
-                // lane: column rcol (sum of channel rcol, or squares of channel rcol - 8) over 16 rows
-                float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-                for (int r = 0; r < 16; r += 2) {
-                    p0 += scr[(16 * rhi + ((r + 4 * rhi) & 15)) * 20 + rcol];
-                    p1 += scr[(16 * rhi + ((r + 1 + 4 * rhi) & 15)) * 20 + rcol];
-                }
-                float tot = p0 + p1;
-                tot += __shfl_xor_sync(0xffffffffu, tot, 16);
-                const float sq = __shfl_down_sync(0xffffffffu, tot, 8);  // lanes 0-7: channel's squares
-                if (lane < 8) {
-                    const float mean = tot * (1.f / 64.f);
-                    st[lane] = mean;
-                    st[8 + lane] = rsqrtf(fmaxf(fmaf(sq, 1.f / 64.f, -mean * mean), 0.f) + a.eps);
-                }
-                __syncwarp();
-                const float4 m0 = *reinterpret_cast<const float4*>(st), m1 = *reinterpret_cast<const float4*>(st + 4);
-                const float4 r0 = *reinterpret_cast<const float4*>(st + 8), r1 = *reinterpret_cast<const float4*>(st + 12);
-                const float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-                const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    pool[c] = fmaf(rr[c], fmaf(g0, v0[c], fmaf(g1, v1[c], -gs * mm[c])), pool[c]);
-                __syncwarp();  // the scratch and statistics are read before the next class overwrites them
+            for (int r = 0; r < 32; r += 2) {
+                const float4 mr = *reinterpret_cast<const float4*>(st + 2 * r);  // rows r, r + 1
+                const int c = r & 7;
+                pool[c] = fmaf(mr.y, fmaf(g0, v[r], fmaf(g1, v[32 + r], -gs * mr.x)), pool[c]);
+                pool[c + 1] = fmaf(mr.w, fmaf(g0, v[r + 1], fmaf(g1, v[33 + r], -gs * mr.z)), pool[c + 1]);
             }
+            __syncwarp();  // the statistics are read before the next tile overwrites them
             const int hin = jt * 4 + q;
             if (hin < a.H) {
                 const size_t cstride = size_t(a.D) * a.H * 32;
@@ -794,7 +804,7 @@ cudaError_t launch_convt3d_lnpool_fused(const c1n_convt3d_params& p, float eps, 
     long long pairs = num_sms / 2;
     if (pairs > tiles) pairs = tiles;
     if (pairs < 1) pairs = 1;
-    const int smem = 1024 + kFWBytes + kFStages * kTileBytes + kFEpiWarps * kFScr * 4 + kFEpiWarps * 16 * 4 + 256;
+    const int smem = 1024 + kFWBytes + kFStages * kTileBytes + kFEpiWarps * kFStat * 4 + 256;
     e = cudaFuncSetAttribute(convt3d_lnpool_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     convt3d_lnpool_fused_kernel<<<(unsigned)(2 * pairs), kFThreads, smem, stream>>>(a, tm_x, tm_w);
