@@ -135,8 +135,9 @@ def dtype_name(wl, path, math=0):
 
 # ------------------------------------------------------------------------------------------ oracle arm
 
-def time_oracle(wl, seconds=10.0, max_runs=50, n_rows=None):
-    """Time the CPU oracle on `n_rows` batch entries of the workload (whole workload by default)."""
+def time_oracle(wl, seconds=10.0, max_runs=50, n_rows=None, single_seconds=0.0):
+    """Time the CPU oracle on `n_rows` batch entries of the workload (whole workload by default), on
+    all host cores; with single_seconds > 0 also on one thread (one batch entry per run)."""
     import oracle
     rows = wl.N if n_rows is None else n_rows
     sub = wl.replace(N=rows)
@@ -153,9 +154,25 @@ def time_oracle(wl, seconds=10.0, max_runs=50, n_rows=None):
         if el >= seconds or runs >= max_runs:
             break
     flops = sub.flops * runs
-    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{runs} run(s) of the full operator on {rows} of {wl.N} batch entries "
-                      f"({sub.flops / 1e9:.3f} GFLOP each), {el:.1f} s wall"}
+    out = {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+           "sample": f"{runs} run(s) of the full operator on {rows} of {wl.N} batch entries "
+                     f"({sub.flops / 1e9:.3f} GFLOP each), {el:.1f} s wall"}
+    if single_seconds > 0:
+        one = wl.replace(N=1)
+        inp1 = synth.make_inputs(wl, seed=0, n_rows=1)
+        p1 = oracle.params_of(one)
+        runs1, t1 = 0, time.perf_counter()
+        while True:
+            oracle.conv1d_norm(p1, inp1["x"], inp1["w"], inp1["b"], inp1["gamma"], inp1["beta"], inp1["bias2"],
+                               nthreads=1)
+            runs1 += 1
+            el1 = time.perf_counter() - t1
+            if el1 >= single_seconds or runs1 >= max_runs:
+                break
+        out["single_thread"] = {"value": one.flops * runs1 / el1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                                "sample": f"{runs1} run(s) on 1 batch entry ({one.flops / 1e9:.3f} GFLOP "
+                                          f"each), {el1:.1f} s wall"}
+    return out
 
 
 def reference_arm(args, wl):
@@ -549,7 +566,7 @@ def our_arm(args, wl):
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
-            cpu = time_oracle(wl, seconds=args.cpu_seconds)
+            cpu = time_oracle(wl, seconds=args.cpu_seconds, single_seconds=2.0)
         line = {"metric": args.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": dtype_name(wl, run.path, args.math), "data": "synthetic",
