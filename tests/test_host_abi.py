@@ -163,6 +163,25 @@ def test_simt_forced_and_tensor_forced():
     c1n.conv1d_norm_destroy(d)
 
 
+def test_halo_past_one_staged_box_is_refused():
+    # (k - 1) d = 120 rows is the longest halo a staged x box (256 time steps) holds with the tile's
+    # 128 rows; one more dilation step is refused by the tensor-core plans (SIMT still takes it)
+    wl = synth.CAUSAL_CONV.replace(N=2, C_in=32, C_out=64, T=512, k=16, dilation=8, pad_left=120, pad_right=0)
+    d = c1n.conv1d_norm_desc_create(_params(wl))
+    assert c1n.PATH_NAMES[c1n.conv1d_norm_plan_info(d).path] == "tc_direct"
+    c1n.conv1d_norm_destroy(d)
+    far = wl.replace(dilation=9, pad_left=135)
+    with pytest.raises(c1n.C1NError) as e:
+        c1n.conv1d_norm_desc_create(_params(far))
+    assert e.value.status == c1n.ERR_UNSUPPORTED
+    d = c1n.conv1d_norm_desc_create(_params(far, math=c1n.MATH_SIMT))
+    assert c1n.conv1d_norm_plan_info(d).path == c1n.PATH_SIMT
+    c1n.conv1d_norm_destroy(d)
+    with pytest.raises(c1n.C1NError) as e:  # more than 16 taps
+        c1n.conv1d_norm_desc_create(_params(wl.replace(k=17, dilation=1, pad_left=16)))
+    assert e.value.status == c1n.ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("bad", [dict(N=0), dict(C_in=0), dict(k=0), dict(stride=0), dict(dilation=0),
                                  dict(pad_left=-1), dict(groups=3), dict(eps=0.0), dict(eps=float("nan")),
                                  dict(norm=7), dict(post=5), dict(dtype=3), dict(math=9), dict(math=4), dict(T=2, k=5),

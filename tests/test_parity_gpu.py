@@ -134,6 +134,13 @@ SMALL = {
     # three channel blocks (224, 224, 192): channel LayerNorm takes the two-pass plan
     "ln_c640_f32": synth.CONV_LN_GELU_BF16.replace(N=2, C_in=40, C_out=640, T=200, dtype=synth.DTYPE_F32,
                                                    post=synth.POST_NONE),
+    # the most taps (16) and the longest halo one staged x box holds ((k - 1) d = 120 rows)
+    "conv_k16_maxhalo": synth.CAUSAL_CONV.replace(N=2, C_in=32, C_out=64, T=512, k=16, dilation=8, pad_left=120,
+                                                  pad_right=0),
+    "gn_k16_d2": synth.CONV_GN.replace(N=2, C_in=32, C_out=64, T=256, k=16, dilation=2, pad_left=15, pad_right=15,
+                                       groups=8),
+    "ln_bf16_k16_maxhalo": synth.CONV_LN_GELU_BF16.replace(N=2, C_in=64, C_out=128, T=256, k=16, dilation=8,
+                                                           pad_left=56, pad_right=64),
     "stride2_simt": synth.CONV_GN.replace(N=2, C_in=16, C_out=32, T=101, stride=2, groups=8),
     "odd_T_simt": synth.CAUSAL_CONV.replace(N=2, C_in=8, C_out=24, T=77),
 }
