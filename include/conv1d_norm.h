@@ -104,9 +104,10 @@ typedef enum {
 /* Tensor-core mainloop. PAIR: two CTAs on neighbouring SMs (a thread-block cluster of two)
  * compute one 256-row x BN tile with tcgen05.mma.cta_group::2; each CTA stages its own 128 rows of
  * A and half of the BN columns of B, so every SM streams a third less operand data per MMA.
- * SINGLE: one CTA per 128-row tile. AUTO takes PAIR for the Linear plan and SINGLE for the
- * convolution plans (the faster of the two on each). PAIR fails with C1N_ERR_UNSUPPORTED where the
- * plan cannot use pairs (fused GroupNorm, SIMT, MMA N not a multiple of 32). */
+ * SINGLE: one CTA per 128-row tile. AUTO takes PAIR for the Linear plan and for convolution plans
+ * with at least 148 units of 256 rows (about two per pair of SMs), SINGLE for
+ * smaller convolutions (more tiles to spread over the SMs). PAIR fails with C1N_ERR_UNSUPPORTED
+ * where the plan cannot use pairs (fused GroupNorm, SIMT, MMA N not a multiple of 32). */
 typedef enum { C1N_MAINLOOP_AUTO = 0, C1N_MAINLOOP_SINGLE = 1, C1N_MAINLOOP_PAIR = 2 } c1n_mainloop;
 
 typedef struct {
