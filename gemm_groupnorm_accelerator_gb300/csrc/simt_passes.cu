@@ -408,12 +408,14 @@ __global__ void __launch_bounds__(256) normalize8_ln_kernel(NormArgs a, const fl
         rs[2 * k + 1] = q.w;
     }
     const int c_end = min(a.C, (int)(blockIdx.y + 1) * 64);
-#pragma unroll 2
+    // (four rows' loads in flight per thread; the raw tile is read once and y written once, so both
+    // stream past L1 and are marked first to evict from L2)
+#pragma unroll 4
     for (int c = blockIdx.y * 64; c < c_end; ++c) {
         const long long row = (long long)n * a.C + c;
         const float ga = gamma ? __ldg(gamma + c) : 1.f, be = beta ? __ldg(beta + c) : 0.f;
         const float4* src = reinterpret_cast<const float4*>(raw + row * a.T_out);
-        const float4 v0 = src[2 * i], v1 = src[2 * i + 1];
+        const float4 v0 = __ldcs(src + 2 * i), v1 = __ldcs(src + 2 * i + 1);
         float r[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
         const uint64_t gp = f2_pack(ga, ga), bp = f2_pack(be, be);
 #pragma unroll
@@ -425,12 +427,12 @@ __global__ void __launch_bounds__(256) normalize8_ln_kernel(NormArgs a, const fl
         }
         if constexpr (sizeof(OutT) == 4) {
             float4* dst = reinterpret_cast<float4*>(y + row * a.T_out);
-            dst[2 * i] = make_float4(r[0], r[1], r[2], r[3]);
-            dst[2 * i + 1] = make_float4(r[4], r[5], r[6], r[7]);
+            __stcs(dst + 2 * i, make_float4(r[0], r[1], r[2], r[3]));
+            __stcs(dst + 2 * i + 1, make_float4(r[4], r[5], r[6], r[7]));
         } else {
             uint4* dst = reinterpret_cast<uint4*>(y + row * a.T_out);
-            dst[i] = make_uint4(pack_bf16x2(r[0], r[1]), pack_bf16x2(r[2], r[3]), pack_bf16x2(r[4], r[5]),
-                                pack_bf16x2(r[6], r[7]));
+            __stcs(dst + i, make_uint4(pack_bf16x2(r[0], r[1]), pack_bf16x2(r[2], r[3]), pack_bf16x2(r[4], r[5]),
+                                       pack_bf16x2(r[6], r[7])));
         }
     }
 }
