@@ -577,8 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // This CTA's first unit, and how many of its x boxes are staged at entry: when the preceding
     // launch is this library's weight pack (which does not write x), thread 0 arms the first x
-    // staging barriers itself and issues those boxes before the CTA's setup; the other boxes of
-    // the unit head for L2. (A prefetch only fills L2, which every write reaches too, so it may run
+    // staging barriers itself and issues those boxes before the CTA's setup; otherwise the unit's
+    // boxes head for L2. (A prefetch only fills L2, which every write reaches too, so it may run
     // ahead of the kernels this one depends on.)
     const int u0 = kFusedGN ? (blockIdx.z * a.n_t_tiles + blockIdx.x) * (a.n_cb / a.cb_per_unit) + blockIdx.y
                             : ((PAIR || kClusterX) ? int(blockIdx.x >> 1) : int(blockIdx.x));
@@ -593,7 +593,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(bar(i_sfull + c), box_bytes);
             tma_load_3d(sS + c * a.s_slot_bytes, &tm_a, bar(i_sfull + c), t0, c * a.BK, un0.n);
         }
-        for (int c = x_early; c < a.n_ci_chunks; ++c) tma_prefetch_3d(&tm_a, t0, c * a.BK, un0.n);
+        // With the first boxes in flight, prefetching the others would only delay them (every CTA's
+        // loads share HBM at entry; the loader fetches the rest as slots free up). Without them,
+        // the prefetch warms L2 for the loader.
+        if (x_early == 0)
+            for (int c = 0; c < a.n_ci_chunks; ++c) tma_prefetch_3d(&tm_a, t0, c * a.BK, un0.n);
     }
     if (warp == kWarpTma) {
         // barriers initialised by the 32 lanes together; arrival counts: A full: the TMA (Linear) or
