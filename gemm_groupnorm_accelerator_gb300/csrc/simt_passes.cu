@@ -11,6 +11,7 @@
 // Operator definitions: Kimi-K2.6 l2_p35 page (Conv1d + GroupNorm), l2_p75 page (row-min + bias),
 // l1_p5 page (causal padding), l2_p3 page (LayerNorm with affine, exact GELU).
 #include <algorithm>
+#include <atomic>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -557,8 +558,12 @@ template <typename InT, typename PackT>
 __global__ void __launch_bounds__(128, 16) pack_weights_kernel(int C_out, int C_in, int k, int ci_pad, int tf32_mode,
                                                            const InT* __restrict__ w, PackT* __restrict__ wp,
                                                            unsigned* __restrict__ zero, int nzero) {
-    // the conv kernel that follows may start its setup now (it waits for this kernel before it
-    // reads the packed weights)
+    // Launched with programmatic dependence, so its launch may overlap the end of the preceding
+    // kernel: wait for that kernel first (it may write w, or still read the packed weights), and
+    // only then let the conv kernel that follows start its setup (it waits for this kernel before
+    // it reads the packed weights; its early x loads need all earlier work done, which this wait
+    // gives).
+    griddep_wait();
     griddep_launch_dependents();
     const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x, step = (long long)gridDim.x * blockDim.x;
     for (long long i = i0; i < nzero; i += step) zero[i] = 0u;
@@ -770,6 +775,9 @@ cudaError_t launch_rowmin_finish(const c1n_params& p, const Plan& pl, const floa
     return cudaGetLastError();
 }
 
+// Set once the driver has refused programmatic dependence for the pack (then launched plainly).
+static std::atomic<int> pdl_pack_refused{0};
+
 cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream,
                                 unsigned* zero, int nzero) {
     // One (co, ci) slot per thread where the grid allows, so all weight loads are in flight at once;
@@ -778,16 +786,30 @@ cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void*
     const long long total = (long long)p.C_out * pl.ci_pad;
     const long long work = total > nzero ? total : nzero;
     const int grid = (int)std::min<long long>((work + 127) / 128, 152 * 8);
-    if (pl.bf16) {
-        pack_weights_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 128, 0, stream>>>(
-            p.C_out, p.C_in, p.k, pl.ci_pad, 0, static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(wp),
-            zero, nzero);
-    } else {
-        pack_weights_kernel<float, float><<<grid, 128, 0, stream>>>(p.C_out, p.C_in, p.k, pl.ci_pad, pl.x3 ? 2 : 1,
-                                                                    static_cast<const float*>(w),
-                                                                    static_cast<float*>(wp), zero, nzero);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_pack_refused.load() ? 0 : 1;
+    for (;;) {
+        cudaError_t e;
+        if (pl.bf16)
+            e = cudaLaunchKernelEx(&cfg, pack_weights_kernel<__nv_bfloat16, __nv_bfloat16>, p.C_out, p.C_in, p.k,
+                                   pl.ci_pad, 0, static_cast<const __nv_bfloat16*>(w),
+                                   static_cast<__nv_bfloat16*>(wp), zero, nzero);
+        else
+            e = cudaLaunchKernelEx(&cfg, pack_weights_kernel<float, float>, p.C_out, p.C_in, p.k, pl.ci_pad,
+                                   pl.x3 ? 2 : 1, static_cast<const float*>(w), static_cast<float*>(wp), zero,
+                                   nzero);
+        if (e == cudaSuccess || cfg.numAttrs == 0) return e;
+        cudaGetLastError();  // the attribute refused: launch plainly from now on
+        pdl_pack_refused.store(1);
+        cfg.numAttrs = 0;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace c1n

@@ -817,6 +817,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_drain(bar(i_drain), 0, a.status);
+            // The MMAs are done: let the stream's next kernel launch now, so its launch overlaps this
+            // kernel's epilogue (it waits for this kernel's completion before it reads or writes
+            // anything this kernel touches: the library's weight pack does so first thing).
+            griddep_launch_dependents();
         }
     } else if (warp == kWarpXld) {
         // ---------------------------------------------------------------- x staging loader (conv mode)
