@@ -246,6 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The row stride 129 keeps both shared-memory phases free of bank conflicts.
 __global__ void __launch_bounds__(256) to_channels_last32_kernel(const float* __restrict__ x, float* __restrict__ xcl,
                                                                  long long S) {
+    // the one-pass model's weight pack, which does not read x_cl, may start alongside
+    griddep_launch_dependents();
     __shared__ float t[32][129];
     const int tid = threadIdx.x, n = blockIdx.y;
     const long long s0 = (long long)blockIdx.x * 128;
@@ -451,6 +453,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above may overlap the weight pack launched just before (programmatic dependence);
+    // nothing below runs before the pack, and the channels-last copy it waits for, have finished.
+    griddep_wait();
     auto wait = [&](int i, uint32_t parity) -> bool {
         if (mbar_try_wait(bar(i), parity)) return true;
         return mbar_wait(bar(i), parity, abort_flag, a.status, 0, nullptr);
@@ -635,7 +640,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
 // holds, for accumulator column pw * 128 + pos * 32 + co (in the kernel's column order), the 32
 // input channels of tap (k(pd, dd), k(ph, dh), k(pw, dw)), TF32-rounded; k(0, 0) = 1, k(1, 0) = 2,
 // k(1, 1) = 0.
-__global__ void __launch_bounds__(256) pack_fused_weights_kernel(const float* __restrict__ w, float* __restrict__ wp) {
+__device__ __forceinline__ void pack_fused_row(const float* __restrict__ w, float* __restrict__ wp) {
     const int half = blockIdx.y;
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5), ci = threadIdx.x & 31;
     if (r >= kFRows) return;
@@ -653,6 +658,38 @@ __global__ void __launch_bounds__(256) pack_fused_weights_kernel(const float* __
     auto tap = [](int p, int dl) { return p == 0 ? 1 : (dl == 0 ? 2 : 0); };
     const int kd = tap(fz_pd(pos), dd), kh = tap(fz_ph(pos), dh), kw = tap(pw, dw);
     wp[((size_t)half * kFRows + r) * 32 + ci] = round_tf32(__ldg(w + (((ci * 64 + co) * 3 + kd) * 3 + kh) * 3 + kw));
+}
+
+__global__ void __launch_bounds__(256) pack_fused_weights_kernel(const float* __restrict__ w, float* __restrict__ wp) {
+    // Launched with programmatic dependence behind the channels-last copy, which starts after all
+    // earlier work (so w is ready and no earlier model kernel still reads wp): the fused kernel may
+    // set up now; it waits for this kernel, and this kernel ends only after the copy.
+    griddep_launch_dependents();
+    pack_fused_row(w, wp);
+    griddep_wait();
+}
+
+// Launch with programmatic dependence on the stream's preceding kernel (the kernel waits for it in
+// code); plainly once the driver has refused the attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+    static std::atomic<int> refused{0};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = refused.load() ? 0 : 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (e == cudaSuccess || cfg.numAttrs == 0) return e;
+    cudaGetLastError();
+    refused.store(1);
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -769,8 +806,7 @@ cudaError_t launch_convt3d_lnpool_fused(const c1n_convt3d_params& p, float eps, 
     if (e != cudaSuccess) return e;
     const long long S = (long long)p.D * p.H * p.W;
     to_channels_last32_kernel<<<dim3((unsigned)((S + 127) / 128), (unsigned)p.N), 256, 0, stream>>>(x, xcl, S);
-    pack_fused_weights_kernel<<<dim3(kFRows / 8, 2), 256, 0, stream>>>(w, wp);
-    e = cudaGetLastError();
+    e = launch_pdl(pack_fused_weights_kernel, dim3(kFRows / 8, 2), dim3(256), 0, stream, w, wp);
     if (e != cudaSuccess) return e;
     CUtensorMap tm_x, tm_w;
     {
@@ -807,8 +843,8 @@ cudaError_t launch_convt3d_lnpool_fused(const c1n_convt3d_params& p, float eps, 
     const int smem = 1024 + kFWBytes + kFStages * kTileBytes + kFEpiWarps * kFStat * 4 + 256;
     e = cudaFuncSetAttribute(convt3d_lnpool_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    convt3d_lnpool_fused_kernel<<<(unsigned)(2 * pairs), kFThreads, smem, stream>>>(a, tm_x, tm_w);
-    return cudaGetLastError();
+    return launch_pdl(convt3d_lnpool_fused_kernel, dim3((unsigned)(2 * pairs)), dim3(kFThreads), size_t(smem), stream,
+                      a, tm_x, tm_w);
 }
 
 }  // namespace c1n
