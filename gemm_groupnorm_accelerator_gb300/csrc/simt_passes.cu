@@ -547,13 +547,13 @@ __global__ void __launch_bounds__(256) rowmin_finish_kernel(int C, int n_cb, con
     }
 }
 
-// Weight pack: one thread per (output channel co, input channel slot ci < ci_pad) reads the k taps
-// w[co][ci][0..k-1] and writes wp[kk][co][ci] for each tap, coalesced along ci (slots past C_in
-// are zero). At most 128 CTAs of 128 threads, no shared memory, at most 32 registers: the conv
-// kernel that follows (launched early through programmatic dependence; 480 threads x 128
-// registers, ~224 KB of shared memory) fits on an SM beside one of them and stages x while the
-// pack runs. fp32 weights are rounded to TF32; with tf32_mode 2 the TF32 tail
-// w - tf32(w) goes to taps k..2k-1. Also zeroes `nzero` words at `zero`.
+// Weight pack: each thread walks (output channel co, input channel slot ci < ci_pad) slots, reads
+// the k taps w[co][ci][0..k-1] and writes wp[kk][co][ci] for each tap, coalesced along ci (slots
+// past C_in are zero). At most 2 CTAs of 128 threads per SM, no shared memory, at most 32
+// registers: the conv kernel that follows (launched early through programmatic dependence; 480
+// threads x 128 registers, ~224 KB of shared memory) fits on an SM beside them and stages x while
+// the pack runs. fp32 weights are rounded to TF32; with tf32_mode 2 the TF32 tail w - tf32(w)
+// goes to taps k..2k-1. Also zeroes `nzero` words at `zero`.
 template <typename InT, typename PackT>
 __global__ void __launch_bounds__(128, 16) pack_weights_kernel(int C_out, int C_in, int k, int ci_pad, int tf32_mode,
                                                            const InT* __restrict__ w, PackT* __restrict__ wp,
@@ -780,12 +780,13 @@ static std::atomic<int> pdl_pack_refused{0};
 
 cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream,
                                 unsigned* zero, int nzero) {
-    // One (co, ci) slot per thread where the grid allows, so all weight loads are in flight at once;
-    // at most 8 CTAs of 128 threads per SM (of 152), so the conv kernel launched behind this one (1
-    // CTA of 480 threads per SM) fits beside them.
+    // One (co, ci) slot per thread where the grid allows, so the weight loads are in flight at once,
+    // but at most 2 CTAs of 128 threads per SM (of 152): launched early, the CTAs wait beside the
+    // preceding kernel's warps (8 per SM slowed the bf16 LayerNorm kernel's epilogue, 287 vs 269 us
+    // per step), and the conv kernel launched behind them (1 CTA of 480 threads per SM) fits beside.
     const long long total = (long long)p.C_out * pl.ci_pad;
     const long long work = total > nzero ? total : nzero;
-    const int grid = (int)std::min<long long>((work + 127) / 128, 152 * 8);
+    const int grid = (int)std::min<long long>((work + 127) / 128, 152 * 2);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(128);
