@@ -154,7 +154,11 @@ c1n_status conv1d_norm_plan_info(const c1n_desc* desc, c1n_plan_info* info);
 
 /* Enqueue the operator on `stream`, using the attached workspace. x, w, y are device pointers in
  * the descriptor's dtype; b, gamma, beta are device fp32 pointers or NULL (no bias; gamma = 1,
- * beta = 0). Needs post != ROWMIN_BIAS (use run_ex for bias2/argmin). Asynchronous. */
+ * beta = 0). Needs post != ROWMIN_BIAS (use run_ex for bias2/argmin). Asynchronous. The tensor-core
+ * kernels release programmatic dependents once their MMAs are done: a kernel the caller launches
+ * next on `stream` with programmatic stream serialization must, as that launch mode requires, wait
+ * (griddepcontrol.wait / cudaGridDependencySynchronize) before it reads y. Ordinary launches, copies
+ * and events are ordered as usual. */
 c1n_status conv1d_norm_run(c1n_desc* desc, const void* x, const void* w, const float* b,
                            const float* gamma, const float* beta, void* y, c1n_stream_t stream);
 
