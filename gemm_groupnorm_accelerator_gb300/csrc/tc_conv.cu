@@ -985,17 +985,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = first_unit; u < a.n_units; u += unit_step, ++lt) {
                 const int ab = a.n_acc == 2 ? (lt & 1) : 0;
                 const uint32_t acc_par = a.n_acc == 2 ? uint32_t((lt >> 1) & 1) : uint32_t(lt & 1);
-                if (er == 0) prog[7] = kWaitAccFull;
                 // One lane per warp waits; the shuffle reconverges the warp (the TMEM loads below are
-                // warp-collective), and the barrier ORs what every epilogue thread saw, so all four
-                // warps leave (or stay) together.
-                int got = 0;
-                if (lane == 0) got = wait_bar(i_accfull + ab, acc_par, kWaitAccFull);
-                got = __shfl_sync(0xffffffffu, got, 0);
-                if (named_bar_any(1, kEpiT, !got || *abort_flag != 0)) break;
-                __syncwarp();
-                if (er == 0) prog[7] = 0;
-                tc_fence_after();
+                // warp-collective), and the barrier ORs what every epilogue thread saw, so all the
+                // epilogue warps leave (or stay) together. False: give up.
+                auto acc_wait = [&]() -> bool {
+                    if (er == 0) prog[7] = kWaitAccFull;
+                    int got = 0;
+                    if (lane == 0) got = wait_bar(i_accfull + ab, acc_par, kWaitAccFull);
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    if (named_bar_any(1, kEpiT, !got || *abort_flag != 0)) return false;
+                    __syncwarp();
+                    if (er == 0) prog[7] = 0;
+                    tc_fence_after();
+                    return true;
+                };
+                // (the fused GroupNorm waits further down, once the index arithmetic of its tile,
+                // which does not need the accumulator, is done)
+                if constexpr (!kFusedGN) {
+                    if (!acc_wait()) break;
+                }
                 const Unit un = decode(u);
                 OutT* y = static_cast<OutT*>(a.y);
                 const int row = un.row0 + m;
@@ -1330,18 +1338,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float* part_m2 = epi + 3584;   // [256] this CTA's group M2 (cluster); peers' M2 (grid)
                     const uint32_t tb = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(256 * ab);
                     const int nvalid_w = min(32, max(0, nvalid_t - q * 32));
+                    // Every loop over groups or columns below has one iteration at most per thread
+                    // (ngroups <= 256 <= kEpiT), so its divisions are taken here, before the wait.
+                    static_assert(!kFusedGN || kEpiT >= 256, "one group and one column per epilogue thread");
+                    const int run = a.sub > 0 ? a.sub : 1;
+                    float qn[4];  // count of one run's entry in lane quarter q2
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) qn[q2] = float(min(32, max(0, nvalid_t - q2 * 32)) * run);
+                    const int g_me = er;  // this thread's group in the merge
+                    const int j_lo = g_me * cpg / run, j_hi = (min(ncols, g_me * cpg + cpg) + run - 1) / run;
+                    const int g_col = er < ncols ? er / cpg : 0;  // group of this thread's column
+                    int x_g = er / P, x_p = er - (er / P) * P;     // (group, peer) of the exchange pair
+                    if (!acc_wait()) break;
                     gn_run_stats_any(a.sub, tb, c_lo, c_hi, lane < nvalid_w, nvalid_w, s_bias, red_mean, red_m2, q,
                                      lane);
                     named_bar_sync(1, kEpiT);
                     // This CTA's (mean, M2) per group from its (run, lane quarter) entries by the
                     // parallel-axis formula: the count-weighted mean, then the entries' M2 plus each
                     // entry's count times the squared distance of its mean from the group mean.
-                    const int run = a.sub > 0 ? a.sub : 1;
-                    float qn[4];  // count of one run's entry in lane quarter q2
-#pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) qn[q2] = float(min(32, max(0, nvalid_t - q2 * 32)) * run);
-                    for (int g = er; g < ngroups; g += kEpiT) {
-                        const int j_lo = g * cpg / run, j_hi = (min(ncols, g * cpg + cpg) + run - 1) / run;
+                    if (g_me < ngroups) {
+                        const int g = g_me;
                         float n_tot = 0.f, s = 0.f;
                         for (int j = j_lo; j < j_hi; ++j) {
 #pragma unroll
@@ -1403,7 +1419,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t t0 = global_timer_ns();
                         for (int base = 0; base < ngroups * P; base += kEpiT) {  // uniform over the warp
                             const int idx = base + er;
-                            const int g = idx / P, p = idx - g * P;
+                            if (base > 0) {
+                                x_g = idx / P;
+                                x_p = idx - x_g * P;
+                            }
+                            const int g = x_g, p = x_p;
                             unsigned long long wmu = 0ull, wm2 = 0ull;
                             if (g < ngroups) {
                                 const unsigned long long* w = gq + size_t(p) * tile_words + 2 * g;
@@ -1463,11 +1483,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     named_bar_sync(1, kEpiT);
-                    for (int col = er; col < 256; col += kEpiT) {
+                    if (er < 256) {
+                        const int col = er;
                         // colscale / colshift hold gamma / beta (staged before the mainloop)
                         float sc = 0.f, sh = 0.f;
                         if (col < ncols) {
-                            const int g = col / cpg;
+                            const int g = g_col;
                             sc = grstd[g] * colscale[col];
                             sh = colshift[col] + (s_bias[col] - gmean[g]) * sc;
                         }
