@@ -54,7 +54,7 @@ template <bool BF16> __host__ __device__ constexpr int xp_warps() { return BF16 
 // Where a bounded wait gave up (status word detail).
 enum WaitSite {
     kWaitAEmpty = 1, kWaitBEmpty, kWaitAFull, kWaitBFull, kWaitAccEmpty, kWaitAccFull, kWaitDrain, kWaitSEmpty,
-    kWaitSFull, kWaitGridPeers, kWaitExchange
+    kWaitSFull, kWaitGridPeers, kWaitExchange, kWaitAccInit
 };
 
 
@@ -214,8 +214,8 @@ __device__ __forceinline__ void gn_run_moments(uint32_t tb, int c_lo, int c_hi, 
     }
 }
 
-// Statistics of y = acc + bias over every run of SUB consecutive channels of this warp's columns
-// [c_lo, c_hi) (c_lo a multiple of 32) and its valid rows, from ONE sweep of TMEM (one wait per
+// Statistics of y over every run of SUB consecutive channels of this warp's columns [c_lo, c_hi)
+// (c_lo a multiple of 32) and its valid rows (the accumulator holds y, bias included), from ONE sweep of TMEM (one wait per
 // window of 32 or 64 columns): each run's values are summed as d = y - K with K a value of that run
 // (row 0 of the warp, the run's first channel, the same for every lane), so the run's
 // M2 = sum d^2 - (sum d)^2 / n does not cancel however far the data sit from zero. The sums go
@@ -224,7 +224,7 @@ __device__ __forceinline__ void gn_run_moments(uint32_t tb, int c_lo, int c_hi, 
 // of valid rows of the warp (0: nothing is counted).
 template <int SUB>
 __device__ __forceinline__ void gn_run_stats(uint32_t tb, int c_lo, int c_hi, bool row_ok, int n_rows,
-                                             const float* bias, float* red_mean, float* red_m2, int q, int lane) {
+                                             float* red_mean, float* red_m2, int q, int lane) {
     constexpr int kWin = SUB == 1 ? 32 : (8 * SUB < 128 ? 8 * SUB : 128);
     constexpr int kRuns = kWin / SUB;         // runs per window: a power of two <= 32
     constexpr int kRunsPerChunk = 32 / SUB;   // runs per 32-column TMEM load
@@ -243,13 +243,8 @@ __device__ __forceinline__ void gn_run_stats(uint32_t tb, int c_lo, int c_hi, bo
             }
             float v[32];
             tmem_load32(tb + uint32_t(j0), v);
-            // y = v + bias for the whole chunk first, then every run's shift K (independent loads
-            // and shuffles), then the runs' sums in two interleaved chains each, so the runs overlap
-            // instead of waiting on one another
-            float bb[32];
-            lds_vec(bias + j0, bb);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) f2_unpack(f2_add(f2_pack(v[i], v[i + 1]), f2_pack(bb[i], bb[i + 1])), v[i], v[i + 1]);
+            // every run's shift K first (independent shuffles), then the runs' sums in two
+            // interleaved chains each, so the runs overlap instead of waiting on one another
             if constexpr (SUB == 1) {
 #pragma unroll
                 for (int r = 0; r < 32; ++r) {
@@ -338,11 +333,11 @@ __device__ __forceinline__ void stats_merge_xor(float& n, float& mu, float& m2, 
 }
 
 __device__ __forceinline__ void gn_run_stats_any(int sub, uint32_t tb, int c_lo, int c_hi, bool row_ok, int n_rows,
-                                                 const float* bias, float* red_mean, float* red_m2, int q, int lane) {
-    if (sub == 4) gn_run_stats<4>(tb, c_lo, c_hi, row_ok, n_rows, bias, red_mean, red_m2, q, lane);
-    else if (sub == 8) gn_run_stats<8>(tb, c_lo, c_hi, row_ok, n_rows, bias, red_mean, red_m2, q, lane);
-    else if (sub == 16) gn_run_stats<16>(tb, c_lo, c_hi, row_ok, n_rows, bias, red_mean, red_m2, q, lane);
-    else gn_run_stats<1>(tb, c_lo, c_hi, row_ok, n_rows, bias, red_mean, red_m2, q, lane);
+                                                 float* red_mean, float* red_m2, int q, int lane) {
+    if (sub == 4) gn_run_stats<4>(tb, c_lo, c_hi, row_ok, n_rows, red_mean, red_m2, q, lane);
+    else if (sub == 8) gn_run_stats<8>(tb, c_lo, c_hi, row_ok, n_rows, red_mean, red_m2, q, lane);
+    else if (sub == 16) gn_run_stats<16>(tb, c_lo, c_hi, row_ok, n_rows, red_mean, red_m2, q, lane);
+    else gn_run_stats<1>(tb, c_lo, c_hi, row_ok, n_rows, red_mean, red_m2, q, lane);
 }
 
 __device__ __forceinline__ void gn_run_moments_any(int sub, uint32_t tb, int c_lo, int c_hi, bool row_ok, int n_rows,
@@ -524,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
     const int i_afull = 0, i_aempty = SA, i_bfull = 2 * SA, i_bempty = 2 * SA + SB, i_accfull = 2 * SA + 2 * SB,
               i_accempty = i_accfull + 2, i_drain = i_accempty + 2, i_sfull = i_drain + 1, i_sempty = i_sfull + SS,
-              i_ex = i_sempty + SS, n_bars = i_ex + 2;
+              i_ex = i_sempty + SS, i_accinit = i_ex + 2, n_bars = i_ex + 3;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + n_bars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // progress counters: [0] B loads issued, [1] A chunks consumed by the MMA, [2] units issued by
@@ -603,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // barriers initialised by the 32 lanes together; arrival counts: A full: the TMA (Linear) or
         // one per transposer warp (of both CTAs of a pair); accumulator empty: one per epilogue warp
         // (of the pair); x staging empty: one per transposer warp; exchange: one per step, from the
-        // peer's first 4 epilogue warps; all others: one.
+        // peer's first 4 epilogue warps; accumulator initialised: one per warp 2-5; all others: one.
         for (int i = lane; i < n_bars; i += 32) {
             if (i >= i_sfull && i < i_sfull + x_early) continue;  // armed by thread 0 at entry
             uint32_t cnt = 1;
@@ -611,6 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             else if (i >= i_accempty && i < i_drain) cnt = (PAIR ? 2u : 1u) * uint32_t(kEpiW);
             else if (i >= i_sempty && i < i_ex) cnt = uint32_t(xp_warps<BF16>());
             else if (i >= i_ex) cnt = 128;
+            if (i == i_accinit) cnt = 4;
             mbar_init(bar(i), cnt);
         }
         if (lane == 0) *abort_flag = 0;
@@ -757,6 +753,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     prog[11] = ai | (int(aph) << 8) | (bi << 16) | (int(bph) << 24);
                 }
                 if (!wait_warp(i_accempty + ab, acc_par ^ 1, kWaitAccEmpty)) break;
+                // fused GroupNorm: the accumulator starts as the bias, written by warps 2-5
+                if (kFusedGN && lt == 0 && !wait_warp(i_accinit, 0, kWaitAccInit)) break;
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + uint32_t(256 * ab * a.cb_per_unit);
                 for (int c = 0; c < a.n_ci_chunks && ok; ++c) {
@@ -776,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t al = LINEAR ? a_lo0 + uint32_t(bi) * a_step : a_lo + uint32_t(kk) * tap_step;
                             const uint32_t bl = b_lo0 + uint32_t(bi) * b_step;
                             const uint32_t bl2 = b_lo0 + uint32_t(bi2) * b_step;
-                            const uint32_t acc0 = (c | kk) != 0 ? 1u : 0u;
+                            const uint32_t acc0 = (kFusedGN || (c | kk) != 0) ? 1u : 0u;
                             if (elect_one()) {
                                 mma_issue<BF16, PAIR>(d, al, bl, idesc, acc0);
                                 mma_issue<BF16, PAIR>(d, al + 2u, bl + 2u, idesc, 1u);
@@ -966,20 +964,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // mainloop runs (gamma and beta go where the column scale / shift end up). (Warps that
                 // were x transposers have not waited for the preceding kernel yet.)
                 griddep_wait();
+                if (er < 128) {  // warps 2-5, which have no role in the mainloop
+                    const int co_base = decode(first_unit).cbu * a.BN;
+                    const int ncols = min(a.BN, a.C_out - co_base);
+                    for (int col = er; col < 256; col += 128) {
+                        const bool ok = col < ncols;
+                        s_bias[col] = (ok && a.bias) ? __ldg(a.bias + co_base + col) : 0.f;
+                        epi[2304 + col] = ok ? (a.gamma ? __ldg(a.gamma + co_base + col) : 1.f) : 0.f;
+                        epi[2560 + col] = (ok && a.beta) ? __ldg(a.beta + co_base + col) : 0.f;
+                    }
+                    // (the epilogue's first barrier, at the accumulator wait, orders these for the
+                    // other epilogue warps)
+                    // The accumulator starts as the bias (every row of column j holds bias[j]) and the
+                    // MMAs add the convolution to it, so the epilogue reads y itself from TMEM. Each of
+                    // the four warps writes its lane quarter, then signals the MMA warp.
+                    named_bar_sync(2, 128);
+                    const uint32_t tq = tmem_base + (uint32_t(q * 32) << 16);
+#pragma unroll 1
+                    for (int j0 = 0; j0 < ncols; j0 += 32) {
+                        float bv[32];
+                        lds_vec(s_bias + j0, bv);
+                        tmem_store32(tq + uint32_t(j0), bv);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(i_accinit));
+                }
+                // (after the accumulator's first operand, which the MMAs wait for)
                 if (EPI == kEpiGridGN) {
                     const Unit un0 = decode(first_unit);
                     const size_t w0i = (size_t(un0.n * a.n_cb + un0.cbu) * a.n_t_tiles + un0.row0 / 128) * size_t(a.gstride) * 2;
                     gx_target = unsigned(ld_relaxed_gpu_u64(a.gx + w0i) >> 32) + 1u;
                 }
-                const int co_base = decode(first_unit).cbu * a.BN;
-                const int ncols = min(a.BN, a.C_out - co_base);
-                for (int col = er; col < 256; col += kEpiT) {
-                    const bool ok = col < ncols;
-                    s_bias[col] = (ok && a.bias) ? __ldg(a.bias + co_base + col) : 0.f;
-                    epi[2304 + col] = ok ? (a.gamma ? __ldg(a.gamma + co_base + col) : 1.f) : 0.f;
-                    epi[2560 + col] = (ok && a.beta) ? __ldg(a.beta + co_base + col) : 0.f;
-                }
-                // (the epilogue's first barrier, at the accumulator wait, orders these)
             }
             int lt = 0;
             for (int u = first_unit; u < a.n_units; u += unit_step, ++lt) {
@@ -1350,8 +1367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int g_col = er < ncols ? er / cpg : 0;  // group of this thread's column
                     int x_g = er / P, x_p = er - (er / P) * P;     // (group, peer) of the exchange pair
                     if (!acc_wait()) break;
-                    gn_run_stats_any(a.sub, tb, c_lo, c_hi, lane < nvalid_w, nvalid_w, s_bias, red_mean, red_m2, q,
-                                     lane);
+                    gn_run_stats_any(a.sub, tb, c_lo, c_hi, lane < nvalid_w, nvalid_w, red_mean, red_m2, q, lane);
                     named_bar_sync(1, kEpiT);
                     // This CTA's (mean, M2) per group from its (run, lane quarter) entries by the
                     // parallel-axis formula: the count-weighted mean, then the entries' M2 plus each
@@ -1490,7 +1506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (col < ncols) {
                             const int g = g_col;
                             sc = grstd[g] * colscale[col];
-                            sh = colshift[col] + (s_bias[col] - gmean[g]) * sc;
+                            sh = colshift[col] - gmean[g] * sc;  // (gmean: the mean of y = acc)
                         }
                         colscale[col] = sc;
                         colshift[col] = sh;
