@@ -26,11 +26,13 @@
 // Linear mode (T = 1, k = 1; Kimi-K2.6 l2_p75 page): x is X[rows][in] and already K-major, so TMA
 // loads the A operand as well; D[row][co].
 //
-// Epilogues: direct (bias, optional exact GELU, store) and cluster GroupNorm (Kimi-K2.6 l2_p35
-// page): the CTAs of a thread-block cluster together cover all T_out steps of one sample; each
-// reduces per-(group) partial statistics over its tile (column sums across the 128 lanes by a
-// butterfly reduce-scatter), the partials are merged through distributed shared memory with
-// Chan's pairwise formula, and every CTA normalizes its tile straight from TMEM and stores it once.
+// Epilogues: direct (bias, optional exact GELU, store), fused GroupNorm (Kimi-K2.6 l2_p35 page) and
+// fused channel LayerNorm. Fused GroupNorm: the CTAs of one sample (a cooperative grid, or a
+// thread-block cluster) together cover all its T_out steps, one tile each; the accumulator starts
+// as the bias, so TMEM holds y; each CTA reduces per-group partial statistics over its tile (column
+// sums across the 128 lanes by butterfly reduce-scatters), the partials are exchanged through
+// global memory (epoch-tagged words) or distributed shared memory and merged with Chan's pairwise
+// formula, and every CTA normalizes its tile straight from TMEM and stores it once.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
