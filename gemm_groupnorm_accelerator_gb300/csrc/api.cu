@@ -134,6 +134,13 @@ void plan_stages(Plan& pl, int max_a, int max_b, int max_s) {
     pl.smem_bytes = 1024 + total() + kTcMiscBytes;
 }
 
+// The weight pack releases the fused-GroupNorm conv kernel that follows before it waits for the
+// preceding kernel when the grid is large: the conv CTAs then take the SMs as the preceding
+// kernel's leave, instead of launching once the pack has waited (conv_gn, 128 CTAs: 17.75 vs
+// 18.06 us per step). The conv kernel then waits for the pack before it loads x; with few CTAs the
+// early x loads matter more (2 CTAs: 8.0 vs 8.2 us), and the pack releases after its wait.
+bool pack_releases_first(const Plan& pl) { return pl.path == C1N_PATH_TC_FUSED_GN && pl.n_units >= 32; }
+
 // CTA pairs (cta_group::2) need an MMA N that splits into two halves of whole 16-row groups. Each
 // CTA of a pair streams half of the weight tile through its shared memory. AUTO uses them for the
 // Linear GEMM (0.88 vs 0.70 of tensor peak on 1024x8192x8192) and for convolutions with at least
@@ -536,7 +543,7 @@ c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
             if (!(a->flags & C1N_FLAG_WEIGHTS_PACKED)) {
                 unsigned* zero = pl.gx_words ? reinterpret_cast<unsigned*>(wsb + pl.ws_gx) : nullptr;
                 mark(d, s, "pack_weights");
-                e = launch_pack_weights(p, pl, a->w, wp, s, zero, pl.gx_words);
+                e = launch_pack_weights(p, pl, a->w, wp, s, zero, pl.gx_words, pack_releases_first(pl));
                 if (e != cudaSuccess) return cuda_fail(e, "weight pack launch");
             }
             wsrc = wp;
@@ -613,8 +620,9 @@ c1n_status run_body(c1n_desc* d, const c1n_args* a, cudaStream_t s) {
         t.gx = reinterpret_cast<unsigned long long*>(wsb + pl.ws_gx);
         t.gstride = pl.gstride;
         // x may be read before the kernel waits on its predecessor only when that predecessor is
-        // the weight pack launched just above (which itself starts after all earlier work)
-        t.early_inputs = (!linear && !(a->flags & C1N_FLAG_WEIGHTS_PACKED)) ? 1 : 0;
+        // the weight pack launched just above and it releases this kernel only after its own wait
+        // for all earlier work
+        t.early_inputs = (!linear && !(a->flags & C1N_FLAG_WEIGHTS_PACKED) && !pack_releases_first(pl)) ? 1 : 0;
         t.row_cpg = (pl.row_epilogue && p.norm == C1N_NORM_GROUP) ? p.C_out / p.groups : 0;
         t.rowmin = (pl.row_epilogue && p.post == C1N_POST_ROWMIN_BIAS) ? 1 : 0;
         t.rowpart = reinterpret_cast<float2*>(wsb + pl.ws_rowpart);

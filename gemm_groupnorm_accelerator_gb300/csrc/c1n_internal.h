@@ -125,7 +125,7 @@ cudaError_t launch_rowmin_finish(const c1n_params& p, const Plan& pl, const floa
 // Also zeroes `nzero` words at `zero` (the fused-GroupNorm arrival counters) when given.
 // fp32 weights are rounded to TF32; with pl.x3 the TF32 tail w - tf32(w) follows as taps k..2k-1.
 cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream,
-                                unsigned* zero = nullptr, int nzero = 0);
+                                unsigned* zero = nullptr, int nzero = 0, bool release_first = false);
 
 // [p4]'s LayerNorm(last dim) + AvgPool3d + GELU pass; p already validated (W in 64, 128, 256, 512).
 cudaError_t launch_ln_avgpool3d_gelu(const c1n_lnpool_params& p, const float* z, float sum_weight,

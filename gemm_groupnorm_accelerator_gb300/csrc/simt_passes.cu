@@ -557,14 +557,16 @@ __global__ void __launch_bounds__(256) rowmin_finish_kernel(int C, int n_cb, con
 template <typename InT, typename PackT>
 __global__ void __launch_bounds__(128, 16) pack_weights_kernel(int C_out, int C_in, int k, int ci_pad, int tf32_mode,
                                                            const InT* __restrict__ w, PackT* __restrict__ wp,
-                                                           unsigned* __restrict__ zero, int nzero) {
+                                                           unsigned* __restrict__ zero, int nzero, int release_first) {
     // Launched with programmatic dependence, so its launch may overlap the end of the preceding
-    // kernel: wait for that kernel first (it may write w, or still read the packed weights), and
-    // only then let the conv kernel that follows start its setup (it waits for this kernel before
-    // it reads the packed weights; its early x loads need all earlier work done, which this wait
-    // gives).
+    // kernel: it waits for that kernel before it touches anything (that kernel may write w, or
+    // still read the packed weights). The conv kernel that follows is released either after that
+    // wait (it may then load x before waiting for this kernel: all earlier work is done) or, with
+    // release_first, at once: its CTAs then take the SMs as the preceding kernel's leave, and it
+    // waits for this kernel before it reads any global input.
+    if (release_first) griddep_launch_dependents();
     griddep_wait();
-    griddep_launch_dependents();
+    if (!release_first) griddep_launch_dependents();
     const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x, step = (long long)gridDim.x * blockDim.x;
     for (long long i = i0; i < nzero; i += step) zero[i] = 0u;
     const long long total = (long long)C_out * ci_pad;
@@ -779,7 +781,7 @@ cudaError_t launch_rowmin_finish(const c1n_params& p, const Plan& pl, const floa
 static std::atomic<int> pdl_pack_refused{0};
 
 cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void* w, void* wp, cudaStream_t stream,
-                                unsigned* zero, int nzero) {
+                                unsigned* zero, int nzero, bool release_first) {
     // One (co, ci) slot per thread where the grid allows, so the weight loads are in flight at once,
     // but at most 2 CTAs of 128 threads per SM (of 152): launched early, the CTAs wait beside the
     // preceding kernel's warps (8 per SM slowed the bf16 LayerNorm kernel's epilogue, 287 vs 269 us
@@ -801,11 +803,11 @@ cudaError_t launch_pack_weights(const c1n_params& p, const Plan& pl, const void*
         if (pl.bf16)
             e = cudaLaunchKernelEx(&cfg, pack_weights_kernel<__nv_bfloat16, __nv_bfloat16>, p.C_out, p.C_in, p.k,
                                    pl.ci_pad, 0, static_cast<const __nv_bfloat16*>(w),
-                                   static_cast<__nv_bfloat16*>(wp), zero, nzero);
+                                   static_cast<__nv_bfloat16*>(wp), zero, nzero, release_first ? 1 : 0);
         else
             e = cudaLaunchKernelEx(&cfg, pack_weights_kernel<float, float>, p.C_out, p.C_in, p.k, pl.ci_pad,
                                    pl.x3 ? 2 : 1, static_cast<const float*>(w), static_cast<float*>(wp), zero,
-                                   nzero);
+                                   nzero, release_first ? 1 : 0);
         if (e == cudaSuccess || cfg.numAttrs == 0) return e;
         cudaGetLastError();  // the attribute refused: launch plainly from now on
         pdl_pack_refused.store(1);
