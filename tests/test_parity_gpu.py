@@ -415,6 +415,61 @@ def test_conv_gn_full(cuda_lib):
     assert np.max(np.abs(g.var(axis=2) - 1.0)) < 1e-2
 
 
+def test_chained_calls_read_the_producers_output(cuda_lib):
+    # Two fused-GroupNorm calls on one stream, the first one's y being the second one's x, as in
+    # stacked layers. Each conv kernel lets the next kernel launch once its MMAs are done, before
+    # its epilogue has stored y, and at this size the weight pack lets the second conv launch before
+    # the pack itself waits: the second conv must still read the finished y. Its output must equal,
+    # bit for bit, the same call made after a full synchronisation, eagerly and in a CUDA graph.
+    wl_b = synth.CONV_GN
+    wl_a = synth.Workload("chain_producer_n16_c64x128_t1024", N=wl_b.N, C_in=64, C_out=wl_b.C_in, T=wl_b.T, k=3,
+                          pad_left=1, pad_right=1, norm=synth.NORM_GROUP, groups=16)
+    ops, dev = [], []
+    for wl in (wl_a, wl_b):
+        params = cuda_lib.make_params(wl.N, wl.C_in, wl.C_out, wl.T, wl.k, wl.stride, wl.pad_left, wl.pad_right,
+                                      wl.dilation, wl.norm, wl.groups, wl.eps, wl.post, wl.dtype, 0)
+        op = cuda_lib.Conv1dNorm(params)
+        assert op.path == "tc_fused_gn"
+        inp = _inputs(wl)
+        ops.append(op)
+        dev.append({k: _to_dev(inp[k], False) for k in ("x", "w", "b", "gamma", "beta")})
+    op_a, op_b = ops
+    a, b = dev
+    y_a = torch.empty((wl_a.N, wl_a.C_out, op_a.T_out), device="cuda")
+    y_b = torch.empty((wl_b.N, wl_b.C_out, op_b.T_out), device="cuda")
+
+    def chain():
+        op_a(a["x"], a["w"], a["b"], a["gamma"], a["beta"], out=y_a)
+        op_b(y_a, b["w"], b["b"], b["gamma"], b["beta"], out=y_b)
+
+    chain()
+    torch.cuda.synchronize()
+    op_a.check()
+    op_b.check()
+    x_b = y_a.clone()
+    torch.cuda.synchronize()
+    want = op_b(x_b, b["w"], b["b"], b["gamma"], b["beta"])
+    torch.cuda.synchronize()
+    assert torch.equal(y_b, want)
+    for _ in range(3):  # again, behind other work, eagerly
+        y_a.fill_(float("nan"))
+        y_b.fill_(float("nan"))
+        chain()
+    torch.cuda.synchronize()
+    assert torch.equal(y_a, x_b) and torch.equal(y_b, want)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    for _ in range(3):
+        y_a.fill_(float("nan"))
+        y_b.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        op_a.check()
+        op_b.check()
+        assert torch.equal(y_a, x_b) and torch.equal(y_b, want)
+
+
 def test_causal_conv_full_sampled(cuda_lib):
     wl = synth.CAUSAL_CONV
     inp = _inputs(wl)
