@@ -82,8 +82,9 @@ struct TcArgs {
     // per (sample, channel block, time tile, group) two 64-bit words: (mean | epoch), (M2 | epoch)
     unsigned long long* gx;
     int gstride;       // groups per (sample, channel block, time tile) in gx
-    int early_inputs;  // the preceding launch is this library's weight pack (launched without
-                       // programmatic dependence): x may be read before griddepcontrol.wait
+    int early_inputs;  // the preceding launch is this library's weight pack, which released this
+                       // kernel after its own wait for all earlier work: x may be read before
+                       // griddepcontrol.wait
     int row_cpg;       // row epilogue: GroupNorm over runs of row_cpg channels (8, 16, 32; 0 = none)
     int rowmin;        // row epilogue: keep (min, argmin) per row instead of storing y
     float2* rowpart;   // row epilogue: per (row, channel block) minimum and its channel (int bits)

@@ -573,9 +573,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     // This CTA's first unit, and how many of its x boxes are staged at entry: when the preceding
-    // launch is this library's weight pack (which does not write x), thread 0 arms the first x
-    // staging barriers itself and issues those boxes before the CTA's setup; otherwise the unit's
-    // boxes head for L2. (A prefetch only fills L2, which every write reaches too, so it may run
+    // launch is this library's weight pack (which does not write x) and it released this kernel
+    // only after its own wait for all earlier work, thread 0 arms the first x staging barriers
+    // itself and issues those boxes before the CTA's setup; otherwise the unit's boxes head for L2. (A prefetch only fills L2, which every write reaches too, so it may run
     // ahead of the kernels this one depends on.)
     const int u0 = kFusedGN ? (blockIdx.z * a.n_t_tiles + blockIdx.x) * (a.n_cb / a.cb_per_unit) + blockIdx.y
                             : ((PAIR || kClusterX) ? int(blockIdx.x >> 1) : int(blockIdx.x));
